@@ -1,0 +1,44 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case compiles a copy of oracle.c with one planted mistake (on the CPU)
+and runs the pin suite against it in a subprocess; the suite must fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "wrong_fp4_max": ("div_f32(amax, 6.0f)", "div_f32(amax, 4.0f)"),
+    "dropped_b_scale": ("double sb = orc_e4m3_decode(j->sfb[n * G + g]);", "double sb = 1.0;"),
+    "wrong_group_index": ("double sa = orc_e4m3_decode(j->sfa[m * G + g]);",
+                          "double sa = orc_e4m3_decode(j->sfa[m * G]);"),
+    "swapped_nibbles": ("e2m1_at(j->b, j->K / 2, n, k)", "e2m1_at(j->b, j->K / 2, n, k ^ 1)"),
+    "ties_to_odd": ("(c & 1) == 0 && (best & 1) == 1", "(c & 1) == 1 && (best & 1) == 0"),
+    "fp8_block_index": ("j->sb8[(n / 128) * KB + kb]", "j->sb8[(n % 2) * KB + kb]"),
+    "fp8_no_scale_rounding": ("float s = div_f32(amax, 448.0f);", "float s = (float)(amax / 447.0);"),
+    "dispatch_unaligned": ("int32_t padded = (counts[e] + block - 1) / block * block;",
+                           "int32_t padded = counts[e];"),
+    "lowrank_sign": ("y += prod;\n                    s += fabs(prod);", "y -= prod;\n                    s += fabs(prod);"),
+    "swiglu_sign": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(g[i])) * u[i];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "oracle.c")).read()
+    assert src.count(old) == 1, name
+    mutant = tmp_path / "oracle_mutant.c"
+    mutant.write_text(src.replace(old, new))
+    so = tmp_path / "liboracle_mutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(so),
+                           str(mutant), "-lm"])
+    env = dict(os.environ, ORACLE_SO=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

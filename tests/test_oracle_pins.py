@@ -1,0 +1,384 @@
+"""Pins of the FP64 oracle against facts fixed by the pages and by mathematics.
+
+Each test checks the oracle against something other than itself: golden
+values derived by hand from the pages (tests/golden/*, each cited), closed
+forms, invariants, library routines (ml_dtypes / torch dtype casts, numpy
+matmul) on cases where the method reduces to them, and brute force.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.conftest import read_golden
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+
+def test_e2m1_value_set():
+    for code, val in read_golden("e2m1_values.txt"):
+        got = oracle.e2m1_decode(int(code))
+        assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val))
+    assert max(oracle.e2m1_table()) == 6.0 and len(set(oracle.e2m1_table())) == 15  # +-0 equal
+
+
+def test_e2m1_round_nearest_even_and_saturation():
+    for x, code, val in read_golden("e2m1_rne.txt"):
+        c = oracle.e2m1_encode(float(x))
+        assert c == int(code), (x, c, code)
+        assert oracle.e2m1_decode(c) == float(val)
+
+
+def test_e2m1_matches_ml_dtypes_sweep():
+    ml = pytest.importorskip("ml_dtypes")
+    g = np.random.default_rng(1)
+    xs = np.concatenate([np.linspace(-7, 7, 5601, dtype=np.float32),
+                         g.standard_normal(3000).astype(np.float32) * 3,
+                         np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -5.0],
+                                  dtype=np.float32)])
+    ref = xs.astype(ml.float4_e2m1fn).view(np.uint8) & 0xF
+    got = np.array([oracle.e2m1_encode(float(v)) for v in xs], dtype=np.uint8)
+    assert np.array_equal(ref, got)
+
+
+def test_e4m3_facts():
+    for code, val in read_golden("e4m3_facts.txt"):
+        got = oracle.e4m3_decode(int(code))
+        assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val))
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+    fin = oracle.e4m3_table()[:127]
+    assert np.all(np.diff(fin) > 0) and fin[-1] == 448.0
+
+
+def test_e4m3_matches_torch_cast():
+    g = np.random.default_rng(2)
+    mags = np.exp(g.uniform(np.log(2.0 ** -12), np.log(448.0), 20000)).astype(np.float32)
+    xs = np.concatenate([mags, -mags, oracle.e4m3_table()[:127].astype(np.float32),
+                         ((oracle.e4m3_table()[1:127] + oracle.e4m3_table()[:126]) / 2).astype(np.float32)])
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v)) for v in xs], dtype=np.uint8)
+    assert np.array_equal(ref, got)
+
+
+def test_e4m3_saturates():
+    for v in (448.0, 449.0, 463.9, 464.0, 500.0, 1e6):
+        assert oracle.e4m3_encode(v) == 0x7E
+        assert oracle.e4m3_encode(-v) == 0xFE
+
+
+# ---------------------------------------------------------------------------
+# quantizers
+# ---------------------------------------------------------------------------
+
+def _lib_q4(x):
+    """FP4 group-16 quantization with library casts (ml_dtypes E2M1, torch e4m3)."""
+    ml = pytest.importorskip("ml_dtypes")
+    x = np.asarray(x, dtype=np.float32)
+    M, K = x.shape
+    grp = np.abs(x.reshape(M, K // 16, 16)).max(axis=2)
+    # torch's e4m3 cast does not saturate (>= 464 gives NaN); the scale saturates at 448
+    s_code = torch.from_numpy(np.minimum(grp / np.float32(6), np.float32(448)).astype(np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    s = torch.from_numpy(s_code).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    s_full = np.repeat(s, 16, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = (x / s_full).astype(np.float32)
+    codes = q.astype(ml.float4_e2m1fn).view(np.uint8) & 0xF
+    codes[s_full == 0] = 0
+    return codes, s_code
+
+
+def _quant_inputs(seed=3, M=24, K=128):
+    g = np.random.default_rng(seed)
+    x = g.standard_normal((M, K)).astype(np.float32)
+    x[0, :16] = 0.0                                   # zero group -> s = 0 -> codes 0
+    x[1, 16:32] *= np.float32(1e-4)                   # subnormal / zero e4m3 scale
+    x[2, :] *= np.float32(2000.0)                     # amax/6 > 448 -> saturated scale
+    x[3, 32:48] = np.float32(6.0) * np.float32(0.171875)  # exact grid points
+    x[4, :] = -np.abs(x[4, :]) * np.float32(1e-3)
+    if M > 5:
+        x[5, :16] = np.linspace(-3, 3, 16, dtype=np.float32)
+    return x
+
+
+def test_q4_quantize_matches_library_casts():
+    x = _quant_inputs()
+    ref_codes, ref_sf = _lib_q4(x)
+    codes, sf = oracle.q4_quantize(x)
+    assert np.array_equal(sf, ref_sf)
+    assert np.array_equal(oracle.unpack_e2m1(codes, x.shape[1]), ref_codes)
+
+
+def test_q4_quantize_bf16_input_and_packing():
+    xb = torch.from_numpy(_quant_inputs(seed=4, M=8, K=64)).to(torch.bfloat16)
+    codes, sf = oracle.q4_quantize(xb)
+    ref_codes, ref_sf = _lib_q4(xb.float().numpy())
+    assert np.array_equal(sf, ref_sf)
+    # packing: element 2i in the low nibble, 2i+1 in the high nibble
+    assert np.array_equal(codes, (ref_codes[:, 0::2] | (ref_codes[:, 1::2] << 4)).astype(np.uint8))
+
+
+def test_q4_brute_force_nearest_and_error_bound():
+    """Each code is a nearest grid point of x/s (brute force over all 16 codes)."""
+    x = _quant_inputs(seed=5, M=6, K=64)
+    codes, sf = oracle.q4_quantize(x)
+    c = oracle.unpack_e2m1(codes, 64)
+    for m in range(6):
+        for k in range(64):
+            s = oracle.e4m3_decode(sf[m, k // 16])
+            if s == 0:
+                assert c[m, k] == 0
+                continue
+            q = np.float32(x[m, k]) / np.float32(s)
+            dists = [abs(oracle.e2m1_decode(cc) - float(q)) for cc in range(16)]
+            if abs(q) <= 6:
+                assert abs(oracle.e2m1_decode(c[m, k]) - float(q)) == min(dists)
+                # dequantization error at most half the local grid spacing times s
+                assert abs(oracle.e2m1_decode(c[m, k]) * s - x[m, k]) <= 1.0 * s + 1e-30
+            else:
+                assert abs(oracle.e2m1_decode(c[m, k])) == 6.0
+
+
+def test_q4_scale_is_nearest_e4m3_of_amax_over_6():
+    x = _quant_inputs(seed=6, M=6, K=64)
+    _, sf = oracle.q4_quantize(x)
+    fin = oracle.e4m3_table()[:127]
+    for m in range(6):
+        for g in range(4):
+            t = float(np.float32(np.abs(x[m, g * 16:(g + 1) * 16]).max()) / np.float32(6))
+            d = np.abs(fin - t)
+            assert d[sf[m, g]] == d.min()
+
+
+def test_q8_quantize_matches_library_casts():
+    g = np.random.default_rng(7)
+    x = g.standard_normal((5, 256)).astype(np.float32)
+    x[:, 7] *= 50
+    x[2, 128:] = 0
+    codes, scales = oracle.q8_quantize(x, rows_per_block=1)
+    amax = np.abs(x.reshape(5, 2, 128)).max(axis=2)
+    s = (amax / np.float32(448)).astype(np.float32)
+    assert np.array_equal(scales, s)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = (x / np.repeat(s, 128, axis=1)).astype(np.float32)
+    q[np.repeat(s, 128, axis=1) == 0] = 0
+    ref = torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+
+
+def test_q8_block_128x128_scales():
+    g = np.random.default_rng(8)
+    w = (g.standard_normal((256, 256)) * 0.02).astype(np.float32)
+    w[130, 5] = 3.0
+    codes, scales = oracle.q8_quantize(w, rows_per_block=128)
+    assert scales.shape == (2, 2)
+    assert scales[1, 0] == np.float32(3.0) / np.float32(448)
+    for rb in range(2):
+        for kb in range(2):
+            blk = w[rb * 128:(rb + 1) * 128, kb * 128:(kb + 1) * 128]
+            assert scales[rb, kb] == np.float32(np.abs(blk).max()) / np.float32(448)
+
+
+# ---------------------------------------------------------------------------
+# GEMMs
+# ---------------------------------------------------------------------------
+
+def _dequant_fp4_lib(codes, sf, K):
+    ml = pytest.importorskip("ml_dtypes")
+    c = oracle.unpack_e2m1(codes, K)
+    vals = c.view(ml.float4_e2m1fn).astype(np.float64)
+    s = torch.from_numpy(np.ascontiguousarray(sf)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return vals * np.repeat(s, 16, axis=1)
+
+
+@pytest.mark.parametrize("K,expect,sfc", [tuple(r) for r in read_golden("fp4_gemm_allones.txt")])
+def test_gemm_fp4_all_ones_closed_form(K, expect, sfc):
+    K = int(K)
+    a, sa = oracle.q4_quantize(np.ones((3, K), np.float32))
+    b, sb = oracle.q4_quantize(np.ones((5, K), np.float32))
+    assert np.all(sa == int(sfc)) and np.all(sb == int(sfc))
+    y, s = oracle.gemm_fp4(a, sa, b, sb, K)
+    assert np.all(y == float(expect)) and np.all(s == float(expect))
+
+
+def test_gemm_fp4_identity_weights_return_dequantized_x():
+    K = 64
+    g = np.random.default_rng(9)
+    x = g.standard_normal((4, K)).astype(np.float32)
+    a, sa = oracle.q4_quantize(x)
+    b, sb = oracle.q4_quantize(np.eye(K, dtype=np.float32))
+    y, _ = oracle.gemm_fp4(a, sa, b, sb, K)
+    xhat = _dequant_fp4_lib(a, sa, K)
+    assert np.array_equal(y, xhat * 1.03125)   # identity rows dequantize to 1.03125
+
+
+def test_gemm_fp4_matches_matmul_of_dequantized():
+    g = np.random.default_rng(10)
+    for (M, N, K) in [(1, 1, 16), (3, 4, 32), (4, 3, 48), (2, 5, 64)]:
+        x = g.standard_normal((M, K)).astype(np.float32)
+        w = g.standard_normal((N, K)).astype(np.float32)
+        a, sa = oracle.q4_quantize(x)
+        b, sb = oracle.q4_quantize(w)
+        y, s = oracle.gemm_fp4(a, sa, b, sb, K)
+        xa, wb = _dequant_fp4_lib(a, sa, K), _dequant_fp4_lib(b, sb, K)
+        ref = xa @ wb.T
+        assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+        assert np.allclose(s, np.abs(xa) @ np.abs(wb).T, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_fp4_scale_linearity():
+    g = np.random.default_rng(11)
+    x = g.standard_normal((3, 64)).astype(np.float32)
+    w = g.standard_normal((4, 64)).astype(np.float32)
+    b, sb = oracle.q4_quantize(w)
+    a0, sa0 = oracle.q4_quantize(x)
+    y0, _ = oracle.gemm_fp4(a0, sa0, b, sb, 64)
+    for j in (1, 3, -2):
+        a1, sa1 = oracle.q4_quantize(x * np.float32(2.0 ** j))
+        assert np.array_equal(a1, a0)
+        assert np.array_equal(sa1.astype(int), sa0.astype(int) + 8 * j)  # exponent field + j
+        y1, _ = oracle.gemm_fp4(a1, sa1, b, sb, 64)
+        assert np.array_equal(y1, y0 * 2.0 ** j)
+
+
+def test_gemm_fp4_lowrank_bias_alpha_colscale():
+    g = np.random.default_rng(12)
+    M, N, K, r = 3, 5, 32, 4
+    x = g.standard_normal((M, K)).astype(np.float32)
+    w = g.standard_normal((N, K)).astype(np.float32)
+    A = (g.standard_normal((K, r)) * 0.02).astype(np.float32)
+    B = (g.standard_normal((r, N)) * 0.02).astype(np.float32)
+    bias = (g.standard_normal(N) * 0.1).astype(np.float32)
+    cs = g.uniform(0.5, 2, N).astype(np.float32)
+    a, sa = oracle.q4_quantize(x)
+    b, sb = oracle.q4_quantize(w)
+    t = oracle.lowrank_t(x, A)
+    assert np.allclose(t, x.astype(np.float64) @ A.astype(np.float64), rtol=1e-13, atol=1e-15)
+    y, s = oracle.gemm_fp4(a, sa, b, sb, K, alpha=0.75, col_scale=cs, t=t, lora_b=B, bias=bias)
+    main = _dequant_fp4_lib(a, sa, K) @ _dequant_fp4_lib(b, sb, K).T
+    ref = 0.75 * cs[None, :].astype(np.float64) * main + t @ B.astype(np.float64) + bias[None, :]
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_fp8_matches_matmul_of_dequantized():
+    g = np.random.default_rng(13)
+    M, N, K = 3, 256, 256
+    x = g.standard_normal((M, K)).astype(np.float32)
+    x[:, 3] *= 50
+    w = (g.standard_normal((N, K)) * 0.02).astype(np.float32)
+    a, sa = oracle.q8_quantize(x, 1)
+    b, sb = oracle.q8_quantize(w, 128)
+    y, s = oracle.gemm_fp8(a, sa, b, sb)
+    dq = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    xa = dq(a) * np.repeat(sa.astype(np.float64), 128, axis=1)
+    wb = dq(b) * np.repeat(np.repeat(sb.astype(np.float64), 128, axis=1), 128, axis=0)[:N]
+    assert np.allclose(y, xa @ wb.T, rtol=1e-12, atol=1e-12)
+    # the quantized product approximates the fp32 product (fp8: 3 mantissa bits)
+    assert np.abs(y - x.astype(np.float64) @ w.T.astype(np.float64)).max() < 0.05 * s.max()
+
+
+# ---------------------------------------------------------------------------
+# MoE
+# ---------------------------------------------------------------------------
+
+def test_moe_dispatch_hand_case():
+    gold = {r[0]: [int(v) for v in r[1:]] for r in read_golden("moe_dispatch_2x8.txt")}
+    ids = np.array([[t % 2, 1 - t % 2] for t in range(8)], dtype=np.int32)
+    counts, offsets, por = oracle.moe_dispatch(ids, E=2, block=128)
+    assert counts.tolist() == gold["counts"]
+    assert offsets.tolist() == gold["offsets"]
+    assert por[0:8].tolist() == gold["expert0_pairs"]
+    assert por[128:136].tolist() == gold["expert1_pairs"]
+    assert np.all(por[8:128] == -1) and np.all(por[136:] == -1)
+
+
+def test_moe_dispatch_properties():
+    g = np.random.default_rng(14)
+    T, k, E = 300, 4, 9
+    # k distinct experts per token, expert 4 never chosen (an empty expert)
+    ids = np.stack([g.choice([e for e in range(E) if e != 4], k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts, offsets, por = oracle.moe_dispatch(ids, E=E, block=128)
+    assert counts[4] == 0 and offsets[5] == offsets[4]
+    assert np.array_equal(counts, np.bincount(ids.ravel(), minlength=E))
+    assert np.all(offsets % 128 == 0)
+    real = por[por >= 0]
+    assert sorted(real.tolist()) == list(range(T * k))
+    for e in range(E):
+        seg = por[offsets[e]:offsets[e] + counts[e]]
+        assert np.all(ids.ravel()[seg] == e) and np.all(np.diff(seg) > 0)
+        assert np.all(por[offsets[e] + counts[e]:offsets[e + 1]] == -1)
+
+
+def test_swiglu_closed_forms():
+    g = np.array([0.0, 50.0, -50.0, 1.0, -1.0])
+    u = np.array([3.0, 2.0, 2.0, 1.0, 1.0])
+    h = oracle.swiglu(g, u)
+    assert h[0] == 0.0 and abs(h[1] - 100.0) < 1e-12 and abs(h[2]) < 1e-18
+    assert abs(h[3] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert abs(h[3] - h[4] - 1.0) < 1e-15   # silu(x) - silu(-x) = x
+
+
+def _quantized_experts(weights):
+    gu = [oracle.q4_quantize(wgu) for wgu, _ in weights]
+    dn = [oracle.q4_quantize(wd) for _, wd in weights]
+    return [c for c, _ in gu], [s for _, s in gu], [c for c, _ in dn], [s for _, s in dn]
+
+
+def test_moe_layer_all_ones_hand_case():
+    gold = {r[0]: float(r[1]) for r in read_golden("moe_layer_allones.txt")}
+    H = F = 32
+    weights = [(np.full((2 * F, H), v, np.float32), np.full((H, F), v, np.float32)) for v in (1.0, 2.0)]
+    x = np.ones((3, H), np.float32)
+    ids = np.array([[0, 1]] * 3, dtype=np.int32)
+    w = np.full((3, 2), 0.5, np.float32)
+    res = oracle.moe_layer(x, ids, w, *_quantized_experts(weights), F=F)
+    assert np.all(res["out"] == gold["out"])
+    assert np.all(res["inter"][0]["h"] == gold["h_expert0"])
+    assert np.all(res["inter"][1]["h"] == gold["h_expert1"])
+    assert np.all(res["inter"][0]["y"] == gold["y_expert0"])
+    assert np.all(res["inter"][1]["y"] == gold["y_expert1"])
+
+
+def test_moe_layer_expert_relabel_invariance():
+    g = np.random.default_rng(15)
+    T, H, F, E, k = 4, 32, 16, 3, 2
+    x = g.standard_normal((T, H)).astype(np.float32)
+    weights = [((g.standard_normal((2 * F, H)) * 0.3).astype(np.float32),
+                (g.standard_normal((H, F)) * 0.3).astype(np.float32)) for _ in range(E)]
+    ids = np.array([[0, 1], [2, 0], [1, 2], [0, 2]], dtype=np.int32)
+    w = g.uniform(0.1, 1, (T, k)).astype(np.float32)
+    base = oracle.moe_layer(x, ids, w, *_quantized_experts(weights), F=F)["out"]
+    perm = np.array([2, 0, 1])             # new label of old expert e is perm[e]
+    inv = np.argsort(perm)
+    relab = oracle.moe_layer(x, perm[ids], w, *_quantized_experts([weights[i] for i in inv]), F=F)["out"]
+    assert np.array_equal(base, relab)
+    # swapping the two slots of each token (with their weights) also changes nothing
+    swapped = oracle.moe_layer(x, ids[:, ::-1], w[:, ::-1], *_quantized_experts(weights), F=F)["out"]
+    assert np.allclose(base, swapped, rtol=2 ** -8, atol=0)
+
+
+def test_moe_layer_top1_single_expert_is_dense_ffn():
+    g = np.random.default_rng(16)
+    T, H, F = 3, 32, 16
+    x = g.standard_normal((T, H)).astype(np.float32)
+    wgu = (g.standard_normal((2 * F, H)) * 0.3).astype(np.float32)
+    wd = (g.standard_normal((H, F)) * 0.3).astype(np.float32)
+    res = oracle.moe_layer(x, np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32),
+                           *_quantized_experts([(wgu, wd)]), F=F)
+    # dense path written with library pieces: dequantize + numpy matmul + silu
+    a, sa = oracle.q4_quantize(x)
+    gw, gs = oracle.q4_quantize(wgu)
+    gu = _dequant_fp4_lib(a, sa, H) @ _dequant_fp4_lib(gw, gs, H).T
+    gg, uu = gu[:, :F], gu[:, F:]
+    h = torch.from_numpy(gg / (1 + np.exp(-gg)) * uu).to(torch.bfloat16).float().numpy()
+    hq, hs = oracle.q4_quantize(h)
+    dw, ds = oracle.q4_quantize(wd)
+    y = _dequant_fp4_lib(hq, hs, F) @ _dequant_fp4_lib(dw, ds, F).T
+    ref = torch.from_numpy(y).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(res["out"], ref)
