@@ -1,0 +1,258 @@
+"""Block-scaled FP4 / FP8 GEMM for GB300 (sm_103a): Python binding.
+
+Thin ctypes binding of the C ABI in ``include/bsgemm.h``: it marshals torch
+tensors (device memory, the current stream) into the library's entry points
+and allocates outputs with torch.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback.  If ``libbsgemm.so`` has not
+been built, ``load()`` raises.
+
+    Y = (Q(X) Q(W)^T) (.) scale + L(X) + b
+    ("Warp-specialised W4A4 kernel on the newest GPU architecture", section 1)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from ._build import LIB as _LIB_PATH
+
+__all__ = [
+    "load", "sf_bytes", "sf_offset", "q4_quantize", "q8_quantize", "gemm_fp4", "gemm_fp8",
+    "grouped_gemm_fp4", "moe_dispatch", "moe_finalize", "moe_rows_bound", "device_status",
+    "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE",
+]
+
+BS_OK, BS_ERR_INVALID, BS_ERR_ALIGN, BS_ERR_UNSUPPORTED, BS_ERR_CUDA, BS_ERR_TIMEOUT, BS_ERR_OFFSETS = range(7)
+DTYPE_F32, DTYPE_BF16 = 0, 1
+FMT_FP4, FMT_FP8 = 0, 1
+EPI_STORE, EPI_SWIGLU, EPI_COMBINE = 0, 1, 2
+Q8_TOKEN, Q8_BLOCK = 1, 128
+
+
+class BSError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"bsgemm status {status}: {msg}")
+        self.status = status
+
+
+class GemmArgs(ctypes.Structure):
+    _fields_ = [
+        ("fmt", ctypes.c_int), ("a", ctypes.c_void_p), ("sfa", ctypes.c_void_p), ("b", ctypes.c_void_p),
+        ("sfb", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+        ("alpha", ctypes.c_float), ("col_scale", ctypes.c_void_p), ("lora_t", ctypes.c_void_p),
+        ("lora_b_t", ctypes.c_void_p), ("r", ctypes.c_int), ("bias", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("out_dtype", ctypes.c_int), ("ldo", ctypes.c_int64), ("num_sms", ctypes.c_int),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str | None = None):
+    """Load libbsgemm.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or os.environ.get("BSGEMM_LIB") or _LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library not built: {p} is missing (run __graft_entry__.build())")
+        lib = ctypes.CDLL(p)
+        P, I64, I, F, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.bs_sf_bytes.restype = SZ
+        lib.bs_sf_bytes.argtypes = [I64, I64]
+        lib.bs_sf_offset.restype = I64
+        lib.bs_sf_offset.argtypes = [I64, I64, I64]
+        lib.q4_quantize.restype = I
+        lib.q4_quantize.argtypes = [P, I, I64, I64, I64, P, P, P, P, I, P, P]
+        lib.q8_quantize.restype = I
+        lib.q8_quantize.argtypes = [P, I, I64, I64, I64, I, P, P, P]
+        lib.bs_gemm.restype = I
+        lib.bs_gemm.argtypes = [ctypes.POINTER(GemmArgs), P]
+        lib.bs_grouped_gemm.restype = I
+        lib.bs_grouped_gemm.argtypes = [ctypes.POINTER(GemmArgs), I, P, P, I, P, P, P, I64, P]
+        lib.bs_moe_rows_bound.restype = I64
+        lib.bs_moe_rows_bound.argtypes = [I64, I, I]
+        lib.bs_moe_dispatch_workspace_bytes.restype = SZ
+        lib.bs_moe_dispatch_workspace_bytes.argtypes = [I64, I, I]
+        lib.bs_moe_dispatch.restype = I
+        lib.bs_moe_dispatch.argtypes = [P, P, I64, I, I, P, P, P, P, P, P, SZ, P]
+        lib.bs_moe_finalize.restype = I
+        lib.bs_moe_finalize.argtypes = [P, P, I64, P]
+        lib.bs_get_device_status.restype = I
+        lib.bs_get_device_status.argtypes = [ctypes.POINTER(I)]
+        lib.bs_clear_device_status.restype = I
+        lib.bs_clear_device_status.argtypes = []
+        lib.bs_status_string.restype = ctypes.c_char_p
+        lib.bs_status_string.argtypes = [I]
+        lib.bs_last_error.restype = ctypes.c_char_p
+        lib.bs_last_error.argtypes = []
+        _ = F
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != BS_OK:
+        lib = load()
+        raise BSError(status, lib.bs_last_error().decode(errors="replace") or
+                      lib.bs_status_string(status).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def sf_bytes(rows: int, K: int) -> int:
+    """Bytes of the MMA-layout scale tensor of an [rows, K] FP4 operand."""
+    return int(load().bs_sf_bytes(rows, K))
+
+
+def sf_offset(row: int, group: int, K: int) -> int:
+    return int(load().bs_sf_offset(row, group, K))
+
+
+def q4_quantize(x: torch.Tensor, gather: torch.Tensor | None = None, rows: int | None = None,
+                lora_a_t: torch.Tensor | None = None, out=None, stream=None):
+    """FP4 E2M1 group-16 quantization.  Returns (codes [M, K/2] u8, sf u8 [sf_bytes],
+    lora_t bf16 [M, 64] or None).  With ``gather``, output row i is x[gather[i]]
+    (negative: zero row) and M = len(gather) (or ``rows``)."""
+    assert x.is_cuda and x.dim() == 2 and x.stride(1) == 1
+    M = int(rows if rows is not None else (gather.numel() if gather is not None else x.shape[0]))
+    K = x.shape[1]
+    if out is None:
+        codes = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+        sf = torch.empty(sf_bytes(M, K), dtype=torch.uint8, device=x.device)
+        lt = torch.empty((M, 64), dtype=torch.bfloat16, device=x.device) if lora_a_t is not None else None
+    else:
+        codes, sf, lt = out
+    _check(load().q4_quantize(_ptr(x), _dt(x), M, K, x.stride(0), _ptr(gather), _ptr(codes), _ptr(sf),
+                              _ptr(lora_a_t), 32 if lora_a_t is not None else 0, _ptr(lt), _stream(stream)))
+    return codes, sf, lt
+
+
+def q8_quantize(x: torch.Tensor, mode: int = Q8_TOKEN, out=None, stream=None):
+    """FP8 e4m3 quantization.  TOKEN mode: scales fp32 [K/128, M]; BLOCK mode:
+    scales fp32 [ceil(M/128), K/128]."""
+    assert x.is_cuda and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if out is None:
+        codes = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+        shape = (K // 128, M) if mode == Q8_TOKEN else ((M + 127) // 128, K // 128)
+        scales = torch.empty(shape, dtype=torch.float32, device=x.device)
+    else:
+        codes, scales = out
+    _check(load().q8_quantize(_ptr(x), _dt(x), M, K, x.stride(0), mode, _ptr(codes), _ptr(scales),
+                              _stream(stream)))
+    return codes, scales
+
+
+def _args(fmt, a, sfa, b, sfb, M, N, K, out, alpha=1.0, col_scale=None, lora_t=None, lora_b_t=None,
+          bias=None, num_sms=0):
+    g = GemmArgs()
+    g.fmt = fmt
+    g.a, g.sfa, g.b, g.sfb = a.data_ptr(), sfa.data_ptr(), b.data_ptr(), sfb.data_ptr()
+    g.M, g.N, g.K = M, N, K
+    g.alpha = alpha
+    g.col_scale = None if col_scale is None else col_scale.data_ptr()
+    g.lora_t = None if lora_t is None else lora_t.data_ptr()
+    g.lora_b_t = None if lora_b_t is None else lora_b_t.data_ptr()
+    g.r = 32 if lora_t is not None else 0
+    g.bias = None if bias is None else bias.data_ptr()
+    if out is not None:
+        g.out = out.data_ptr()
+        g.out_dtype = _dt(out)
+        g.ldo = out.stride(0)
+    g.num_sms = num_sms
+    return g
+
+
+def gemm_fp4(a, sfa, b, sfb, K: int, out_dtype=torch.bfloat16, alpha: float = 1.0, col_scale=None,
+             lora_t=None, lora_b_t=None, bias=None, out=None, num_sms: int = 0, stream=None):
+    """Dense block-scaled FP4 GEMM: Y[M, N] from A codes [M, K/2] and B codes [N, K/2]."""
+    M, N = a.shape[0], b.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    g = _args(FMT_FP4, a, sfa, b, sfb, M, N, K, out, alpha, col_scale, lora_t, lora_b_t, bias, num_sms)
+    _check(load().bs_gemm(ctypes.byref(g), _stream(stream)))
+    return out
+
+
+def gemm_fp8(a, sa, b, sb, out_dtype=torch.bfloat16, out=None, num_sms: int = 0, stream=None):
+    """Dense FP8 GEMM with 1x128 A scales [K/128, M] and 128x128 B scales."""
+    M, K = a.shape
+    N = b.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    g = _args(FMT_FP8, a, sa, b, sb, M, N, K, out, num_sms=num_sms)
+    _check(load().bs_gemm(ctypes.byref(g), _stream(stream)))
+    return out
+
+
+def grouped_gemm_fp4(a, sfa, b, sfb, K: int, N: int, E: int, offsets, counts, epilogue: int, out=None,
+                     token_of=None, weight_of=None, out32=None, num_sms: int = 0, stream=None):
+    """FP4 GEMM grouped over experts (rows of ``a`` grouped by ``offsets``/``counts``)."""
+    M = a.shape[0]
+    g = _args(FMT_FP4, a, sfa, b, sfb, M, N, K, out, num_sms=num_sms)
+    ld32 = 0 if out32 is None else out32.stride(0)
+    _check(load().bs_grouped_gemm(ctypes.byref(g), E, _ptr(offsets), _ptr(counts), epilogue, _ptr(token_of),
+                                  _ptr(weight_of), _ptr(out32), ld32, _stream(stream)))
+    return out
+
+
+def moe_rows_bound(T: int, k: int, E: int) -> int:
+    return int(load().bs_moe_rows_bound(T, k, E))
+
+
+def moe_dispatch(topk_ids, topk_w, E: int, out=None, workspace=None, stream=None):
+    """Group (token, slot) pairs by expert.  Returns dict(counts, offsets,
+    pair_of_row, token_of, weight_of) of device tensors (rows = moe_rows_bound)."""
+    lib = load()
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    rows = moe_rows_bound(T, k, E)
+    if out is None:
+        out = dict(counts=torch.empty(E, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   pair_of_row=torch.empty(rows, dtype=torch.int32, device=dev),
+                   token_of=torch.empty(rows, dtype=torch.int32, device=dev),
+                   weight_of=torch.empty(rows, dtype=torch.float32, device=dev))
+    wsb = int(lib.bs_moe_dispatch_workspace_bytes(T, k, E))
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    _check(lib.bs_moe_dispatch(_ptr(topk_ids), _ptr(topk_w), T, k, E, _ptr(out["counts"]), _ptr(out["offsets"]),
+                               _ptr(out["pair_of_row"]), _ptr(out["token_of"]), _ptr(out["weight_of"]),
+                               _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def moe_finalize(out32, out_bf16, stream=None):
+    _check(load().bs_moe_finalize(_ptr(out32), _ptr(out_bf16), out32.numel(), _stream(stream)))
+    return out_bf16
+
+
+def device_status() -> tuple[int, int]:
+    d = ctypes.c_int(0)
+    s = load().bs_get_device_status(ctypes.byref(d))
+    return int(s), int(d.value)
+
+
+def clear_device_status():
+    _check(load().bs_clear_device_status())

@@ -1,0 +1,372 @@
+// api.cu -- the C ABI declared in include/bsgemm.h: host-side validation,
+// TMA tensor-map encoding, the sticky device status word, and launches.
+// Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "bsgemm.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+bs_status fail(bs_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+bs_status fail(bs_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+bs_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(BS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device status word: one per device, address looked up once per device.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+bool device_info(int** status, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return false;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    g_status_ptr[dev] = static_cast<int*>(p);
+    g_sm_count[dev] = n;
+  }
+  if (status) *status = g_status_ptr[dev];
+  if (sms) *sms = g_sm_count[dev];
+  return true;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D tiled map over a row-major [rows, inner] matrix.
+bs_status make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+                   uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(BS_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if (rows == 0) rows = 1;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  (void)esize;
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(BS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return BS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t bs_sf_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return (size_t)((rows + 127) / 128 * 128) * (size_t)(K / 16);
+}
+
+int64_t bs_sf_offset(int64_t row, int64_t group, int64_t K) {
+  const int64_t kchunks = K / 64;
+  return ((row / 128) * kchunks + group / 4) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + group % 4;
+}
+
+const char* bs_status_string(bs_status s) {
+  switch (s) {
+    case BS_OK: return "ok";
+    case BS_ERR_INVALID: return "invalid argument";
+    case BS_ERR_ALIGN: return "misaligned pointer, leading dimension or size";
+    case BS_ERR_UNSUPPORTED: return "unsupported combination";
+    case BS_ERR_CUDA: return "CUDA error";
+    case BS_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case BS_ERR_OFFSETS: return "inconsistent expert offsets or ids";
+  }
+  return "unknown status";
+}
+
+const char* bs_last_error(void) { return g_err; }
+
+bs_status bs_get_device_status(int* detail) {
+  int* p = nullptr;
+  if (!device_info(&p, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  int v = 0;
+  cudaError_t e = cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading device status");
+  if (detail) *detail = v;
+  return static_cast<bs_status>(v & 0xFF);
+}
+
+bs_status bs_clear_device_status(void) {
+  int* p = nullptr;
+  if (!device_info(&p, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  int zero = 0;
+  cudaError_t e = cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing device status");
+  return BS_OK;
+}
+
+bs_status q4_quantize(const void* x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx, const int32_t* gather,
+                      uint8_t* codes, uint8_t* sf, const void* lora_a_t, int r, void* lora_t,
+                      bs_stream_t stream) {
+  if (M < 0 || K <= 0) return fail(BS_ERR_INVALID, "q4_quantize: M=%lld K=%lld", (long long)M, (long long)K);
+  if (dt != BS_DTYPE_F32 && dt != BS_DTYPE_BF16) return fail(BS_ERR_INVALID, "q4_quantize: dtype %d", (int)dt);
+  if (K % 64) return fail(BS_ERR_ALIGN, "q4_quantize: K=%lld not a multiple of 64", (long long)K);
+  if (M == 0) return BS_OK;
+  if (!x || !codes || !sf) return fail(BS_ERR_INVALID, "q4_quantize: null pointer");
+  if (ldx < K || ldx % 8 || !aligned16(x) || !aligned16(codes) || !aligned16(sf))
+    return fail(BS_ERR_ALIGN, "q4_quantize: x/codes/sf must be 16-byte aligned and ldx %% 8 == 0, ldx >= K");
+  const bool want_lora = lora_a_t || lora_t || r;
+  if (want_lora) {
+    if (!lora_a_t || !lora_t || r != 32) return fail(BS_ERR_INVALID, "q4_quantize: low-rank needs A^T, T and r == 32");
+    if (dt != BS_DTYPE_BF16) return fail(BS_ERR_UNSUPPORTED, "q4_quantize: low-rank branch needs bf16 input");
+    if (!aligned16(lora_a_t) || !aligned16(lora_t)) return fail(BS_ERR_ALIGN, "q4_quantize: low-rank buffers misaligned");
+  }
+  if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = bsk::launch_q4_quantize(x, dt == BS_DTYPE_BF16, M, K, ldx, gather, codes, sf, s);
+  if (e != cudaSuccess) return cuda_fail(e, "q4_quantize launch");
+  if (want_lora) {
+    e = bsk::launch_lowrank_t(x, M, K, ldx, gather, lora_a_t, lora_t, s);
+    if (e != cudaSuccess) return cuda_fail(e, "low-rank launch");
+  }
+  return BS_OK;
+}
+
+bs_status q8_quantize(const void* x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx, int mode, uint8_t* codes,
+                      float* scales, bs_stream_t stream) {
+  if (M < 0 || K <= 0) return fail(BS_ERR_INVALID, "q8_quantize: M=%lld K=%lld", (long long)M, (long long)K);
+  if (dt != BS_DTYPE_F32 && dt != BS_DTYPE_BF16) return fail(BS_ERR_INVALID, "q8_quantize: dtype %d", (int)dt);
+  if (mode != BS_Q8_TOKEN_1x128 && mode != BS_Q8_BLOCK_128x128) return fail(BS_ERR_INVALID, "q8_quantize: mode %d", mode);
+  if (K % 128) return fail(BS_ERR_ALIGN, "q8_quantize: K=%lld not a multiple of 128", (long long)K);
+  if (M == 0) return BS_OK;
+  if (!x || !codes || !scales) return fail(BS_ERR_INVALID, "q8_quantize: null pointer");
+  if (ldx < K || ldx % 8 || !aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3))
+    return fail(BS_ERR_ALIGN, "q8_quantize: misaligned input/output or ldx");
+  if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_q8_quantize(x, dt == BS_DTYPE_BF16, M, K, ldx, mode, codes, scales,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "q8_quantize launch");
+  return BS_OK;
+}
+
+static bs_status check_common(const bs_gemm_args* a, bool grouped) {
+  if (!a) return fail(BS_ERR_INVALID, "null args");
+  if (a->M < 0 || a->N <= 0 || a->K <= 0) return fail(BS_ERR_INVALID, "bad sizes M=%lld N=%lld K=%lld",
+                                                    (long long)a->M, (long long)a->N, (long long)a->K);
+  if (a->M > (1LL << 30) || a->N > (1LL << 30) || a->K > (1LL << 30)) return fail(BS_ERR_INVALID, "sizes too large");
+  if (a->N % 128) return fail(BS_ERR_ALIGN, "N=%lld not a multiple of 128", (long long)a->N);
+  if (!a->a || !a->b || !a->sfa || !a->sfb) return fail(BS_ERR_INVALID, "null operand");
+  if (!aligned16(a->a) || !aligned16(a->b) || !aligned16(a->sfa) || !aligned16(a->sfb))
+    return fail(BS_ERR_ALIGN, "operands must be 16-byte aligned");
+  if (!grouped || a->out) {
+    if (!a->out) return fail(BS_ERR_INVALID, "null out");
+    if (a->out_dtype != BS_DTYPE_F32 && a->out_dtype != BS_DTYPE_BF16) return fail(BS_ERR_INVALID, "out dtype");
+    if (!aligned16(a->out) || a->ldo % 8 || a->ldo < a->N) return fail(BS_ERR_ALIGN, "out must be 16-byte aligned, ldo %% 8 == 0, ldo >= N");
+  }
+  if (a->num_sms < 0) return fail(BS_ERR_INVALID, "num_sms < 0");
+  return BS_OK;
+}
+
+static bs_status fp4_maps(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows) {
+  const uint64_t kb = (uint64_t)a->K / 2;
+  bs_status st = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, kb, (uint64_t)a->M, kb, 128, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != BS_OK) return st;
+  st = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->b, kb, (uint64_t)b_rows, kb, 128, 128,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != BS_OK) return st;
+  if (a->lora_t) {
+    st = make_map(&L.tmT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a->lora_t, 64, (uint64_t)a->M, 128, 32, 128,
+                  CU_TENSOR_MAP_SWIZZLE_64B);
+    if (st != BS_OK) return st;
+    st = make_map(&L.tmL, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a->lora_b_t, 32, (uint64_t)a->N, 64, 32, 128,
+                  CU_TENSOR_MAP_SWIZZLE_64B);
+    if (st != BS_OK) return st;
+  } else {
+    memset(&L.tmT, 0, sizeof L.tmT);
+    memset(&L.tmL, 0, sizeof L.tmL);
+  }
+  return BS_OK;
+}
+
+bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
+  bs_status st = check_common(a, false);
+  if (st != BS_OK) return st;
+  int* status = nullptr;
+  int sms = 0;
+  if (!device_info(&status, &sms)) return fail(BS_ERR_CUDA, "no current device");
+  if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (a->fmt == BS_FMT_FP4) {
+    if (a->K % 64) return fail(BS_ERR_ALIGN, "FP4: K=%lld not a multiple of 64", (long long)a->K);
+    const bool lora = a->lora_t != nullptr;
+    if (lora) {
+      if (!a->lora_b_t || a->r != 32) return fail(BS_ERR_INVALID, "low-rank branch needs lora_b_t and r == 32");
+      if (a->alpha != 1.0f || a->col_scale)
+        return fail(BS_ERR_UNSUPPORTED, "low-rank branch with alpha != 1 or col_scale");
+      if (!aligned16(a->lora_t) || !aligned16(a->lora_b_t)) return fail(BS_ERR_ALIGN, "low-rank buffers misaligned");
+    }
+    if (a->M == 0) return BS_OK;
+    bsk::Fp4Launch L;
+    memset(&L, 0, sizeof L);
+    st = fp4_maps(L, a, a->N);
+    if (st != BS_OK) return st;
+    L.p.sfa = static_cast<const uint8_t*>(a->sfa);
+    L.p.sfb = static_cast<const uint8_t*>(a->sfb);
+    L.p.M = (int)a->M;
+    L.p.N = (int)a->N;
+    L.p.K = (int)a->K;
+    L.p.alpha = a->alpha;
+    L.p.col_scale = a->col_scale;
+    L.p.bias = a->bias;
+    L.p.out = a->out;
+    L.p.out_bf16 = a->out_dtype == BS_DTYPE_BF16;
+    L.p.ldo = a->ldo;
+    L.p.E = 0;
+    L.p.status = status;
+    L.lora = lora;
+    L.epilogue = bsk::kEpiStore;
+    const long long tiles = ((a->M + 127) / 128) * ((a->N + 255) / 256);
+    L.grid = (int)(tiles < sms ? tiles : sms);
+    cudaError_t e = bsk::launch_fp4_gemm(L, s);
+    if (e != cudaSuccess) return cuda_fail(e, "FP4 GEMM launch");
+    return BS_OK;
+  }
+  if (a->fmt == BS_FMT_FP8) {
+    return fail(BS_ERR_UNSUPPORTED, "FP8 GEMM not built yet");
+  }
+  return fail(BS_ERR_INVALID, "fmt %d", a->fmt);
+}
+
+bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, const int32_t* counts,
+                          int epilogue, const int32_t* token_of, const float* weight_of, float* out32,
+                          int64_t ld_out32, bs_stream_t stream) {
+  if (!a) return fail(BS_ERR_INVALID, "null args");
+  if (epilogue != BS_EPI_STORE && epilogue != BS_EPI_SWIGLU && epilogue != BS_EPI_COMBINE)
+    return fail(BS_ERR_INVALID, "epilogue %d", epilogue);
+  bs_status st = check_common(a, epilogue == BS_EPI_COMBINE);
+  if (st != BS_OK) return st;
+  if (a->fmt != BS_FMT_FP4) return fail(BS_ERR_UNSUPPORTED, "grouped GEMM is FP4 only");
+  if (a->K % 64) return fail(BS_ERR_ALIGN, "FP4: K=%lld not a multiple of 64", (long long)a->K);
+  if (E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "E=%d outside [1, 1024]", E);
+  if (!offsets || !counts) return fail(BS_ERR_INVALID, "null offsets/counts");
+  if (a->lora_t || a->col_scale || a->bias || a->alpha != 1.0f)
+    return fail(BS_ERR_UNSUPPORTED, "grouped GEMM takes no alpha/col_scale/bias/low-rank");
+  if (epilogue == BS_EPI_SWIGLU && a->out_dtype != BS_DTYPE_BF16) return fail(BS_ERR_INVALID, "SWIGLU output is bf16");
+  if (epilogue == BS_EPI_COMBINE) {
+    if (!token_of || !weight_of || !out32) return fail(BS_ERR_INVALID, "COMBINE needs token_of, weight_of, out32");
+    if (!aligned16(out32) || ld_out32 % 4 || ld_out32 < a->N) return fail(BS_ERR_ALIGN, "out32 misaligned or ld_out32 < N");
+  }
+  const int64_t wrows = (epilogue == BS_EPI_SWIGLU ? 2 : 1) * a->N * (int64_t)E;
+  if (wrows > (1LL << 30)) return fail(BS_ERR_INVALID, "stacked weights too large");
+  int* status = nullptr;
+  int sms = 0;
+  if (!device_info(&status, &sms)) return fail(BS_ERR_CUDA, "no current device");
+  if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
+  if (a->M == 0) return BS_OK;
+  bsk::Fp4Launch L;
+  memset(&L, 0, sizeof L);
+  st = fp4_maps(L, a, wrows);
+  if (st != BS_OK) return st;
+  L.p.sfa = static_cast<const uint8_t*>(a->sfa);
+  L.p.sfb = static_cast<const uint8_t*>(a->sfb);
+  L.p.M = (int)a->M;
+  L.p.N = (int)a->N;
+  L.p.K = (int)a->K;
+  L.p.alpha = 1.0f;
+  L.p.out = a->out;
+  L.p.out_bf16 = a->out_dtype == BS_DTYPE_BF16;
+  L.p.ldo = a->ldo;
+  L.p.E = E;
+  L.p.offsets = offsets;
+  L.p.counts = counts;
+  L.p.token_of = token_of;
+  L.p.weight_of = weight_of;
+  L.p.out32 = out32;
+  L.p.ld_out32 = ld_out32;
+  L.p.status = status;
+  L.lora = false;
+  L.epilogue = epilogue;
+  L.grid = sms;
+  cudaError_t e = bsk::launch_fp4_gemm(L, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "grouped FP4 GEMM launch");
+  return BS_OK;
+}
+
+int64_t bs_moe_rows_bound(int64_t T, int k, int E) {
+  if (T < 0 || k <= 0 || E <= 0) return 0;
+  return T * k + (int64_t)E * 127;
+}
+
+size_t bs_moe_dispatch_workspace_bytes(int64_t T, int k, int E) {
+  if (T < 0 || k <= 0 || E <= 0) return 0;
+  const int64_t P = T * k;
+  const int64_t chunks = P > 0 ? (P + 1023) / 1024 : 1;
+  return (size_t)chunks * (size_t)E * sizeof(int32_t);
+}
+
+bs_status bs_moe_dispatch(const int32_t* topk_ids, const float* topk_w, int64_t T, int k, int E, int32_t* counts,
+                          int32_t* offsets, int32_t* pair_of_row, int32_t* token_of, float* weight_of,
+                          void* workspace, size_t workspace_bytes, bs_stream_t stream) {
+  if (T < 0 || k <= 0 || E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "dispatch: T=%lld k=%d E=%d", (long long)T, k, E);
+  if (T * k > (1LL << 30)) return fail(BS_ERR_INVALID, "dispatch: too many pairs");
+  if (!counts || !offsets || !pair_of_row || !token_of || !weight_of || !workspace || (T > 0 && (!topk_ids || !topk_w)))
+    return fail(BS_ERR_INVALID, "dispatch: null pointer");
+  if (workspace_bytes < bs_moe_dispatch_workspace_bytes(T, k, E))
+    return fail(BS_ERR_INVALID, "dispatch: workspace too small (%zu < %zu)", workspace_bytes,
+                bs_moe_dispatch_workspace_bytes(T, k, E));
+  int* status = nullptr;
+  if (!device_info(&status, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_moe_dispatch(topk_ids, topk_w, T, k, E, counts, offsets, pair_of_row, token_of,
+                                           weight_of, static_cast<int*>(workspace), bs_moe_rows_bound(T, k, E),
+                                           status, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
+  return BS_OK;
+}
+
+bs_status bs_moe_finalize(float* out32, void* out_bf16, int64_t n, bs_stream_t stream) {
+  if (n < 0) return fail(BS_ERR_INVALID, "finalize: n < 0");
+  if (n == 0) return BS_OK;
+  if (!out32 || !out_bf16) return fail(BS_ERR_INVALID, "finalize: null pointer");
+  if (!aligned16(out32) || !aligned16(out_bf16)) return fail(BS_ERR_ALIGN, "finalize: buffers must be 16-byte aligned");
+  if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_moe_finalize(out32, out_bf16, n, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  return BS_OK;
+}
+
+}  // extern "C"

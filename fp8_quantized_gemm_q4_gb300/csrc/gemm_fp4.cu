@@ -1,0 +1,509 @@
+// gemm_fp4.cu -- persistent warp-specialised block-scaled FP4 GEMM for sm_103a.
+//
+//   Y = (Q(X) Q(W)^T) (.) scale + L(X) + b
+//   ("Warp-specialised W4A4 kernel on the newest GPU architecture", section 1)
+//
+// One CTA per SM loops over output tiles of 128 x 256 (persistent tile
+// scheduling, same page, section 5.3).  Warp roles (section 5.2):
+//   warp 0      TMA producer of the main operands: A/B E2M1 codes through
+//               128B-swizzled tensor maps, their e4m3 block scales through
+//               contiguous bulk copies (the scales are stored in the order the
+//               tensor core reads them)
+//   warp 1      allocates tensor memory; one lane issues tcgen05.cp (scales
+//               shared -> tensor memory) and tcgen05.mma kind::mxf4nvf4 with
+//               block16 ue4m3 scales into the fp32 accumulator in tensor
+//               memory, then the low-rank MMAs
+//   warp 2      TMA producer of the low-rank operands (T hi|lo, Bl^T): its own
+//               single-slot pipeline, independent of the main ring
+//               (section 4: three independent pipelines)
+//   warp 3      builds the grouped tile table, then idles
+//   warps 4-11  epilogue: tcgen05.ld of the accumulator (two warps per
+//               32-lane quarter, each half of the columns), free the
+//               accumulator, then scale / bias / SwiGLU / routed combine and
+//               store
+// Each role keeps its own PipeState (section 5.1); every wait is bounded.
+//
+// Grouped mode walks per-expert row segments ("DeepGEMM teardown", 5.3;
+// "DeepGEMM for Hopper MoE", 2.2/3): tiles are enumerated expert by expert,
+// n-block by n-block, m-block by m-block, from an in-kernel prefix sum of
+// ceil(count_e / 128) * n_blocks.
+#include "budget.hpp"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bsk {
+namespace fp4 {
+
+constexpr int BM = 128, BN = 256, BK = 256;
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kMaxExperts = 1024;
+constexpr int kMisc = 2048 + (kMaxExperts + 1) * 4 + 1024;  // barriers + tile table + slack
+
+constexpr Fp4TileShape kShapeLora{BM, BN, BK, 1, true, 32, kMisc};
+constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 1, false, 32, kMisc};
+constexpr int kStagesLora = fp4_main_stages(kShapeLora);
+constexpr int kStagesNoLora = fp4_main_stages(kShapeNoLora);
+static_assert(kStagesLora >= 2 && kStagesNoLora >= 2, "pipeline needs at least double buffering");
+static_assert(fp4_smem_total(kShapeLora, kStagesLora) + kAlign <= kSmemPerCta + kAlign, "smem budget");
+static_assert(fp4_stage_bytes(kShapeNoLora) == 16384 + 32768 + 2048 + 4096, "stage layout");
+constexpr int kSfBuffers = 2;
+constexpr int kTmemAcc = 0;
+constexpr int kTmemSf = BN;                        // scale staging after the accumulator
+constexpr int kSfColsPerMma = 4 + BN / 32;         // 4 for A, 8 for B
+constexpr int kSfColsPerStage = (BK / 64) * kSfColsPerMma;
+static_assert(fp4_tmem_cols(kShapeLora, 1, kSfBuffers) <= kTmemCols, "tmem budget");
+constexpr int kTmemAlloc = pow2_cols(fp4_tmem_cols(kShapeLora, 1, kSfBuffers));
+
+// Per-stage layout (bytes from the stage base; every piece 1024-aligned or 16-aligned).
+constexpr int kOffA = 0;
+constexpr int kOffB = BM * BK / 2;                  // 16384
+constexpr int kOffSfa = kOffB + BN * BK / 2;        // 49152
+constexpr int kOffSfb = kOffSfa + BM * BK / 16;     // 51200
+constexpr int kStageBytes = kOffSfb + BN * BK / 16; // 55296
+static_assert(kStageBytes % kAlign == 0, "stage alignment");
+// Low-rank slot: T hi [128 x 32 bf16], T lo, Bl^T [256 x 32 bf16], 64B swizzle.
+constexpr int kLoraThi = 0, kLoraTlo = 8192, kLoraBl = 16384, kLoraBytes = 32768;
+static_assert(kLoraBytes == fp4_lora_bytes(kShapeLora), "lora slot layout");
+
+constexpr uint32_t kIdescMain = idesc_mxf4nvf4(BM, BN);
+constexpr uint32_t kIdescLora = idesc_bf16(BM, BN);
+
+struct Tile {
+  int row0;       // first A row (128-aligned)
+  int rows;       // valid rows in this tile (<= 128)
+  int brow0;      // first B row of accumulator columns [0, 128)
+  int brow1;      // first B row of accumulator columns [128, 256)
+  int sfb_blk1;   // scale block of brow1 (a valid block even when brow1 is past the weights)
+  int col0;       // first output column
+  int expert;
+};
+
+struct Smem {
+  uint8_t* stages;
+  uint8_t* lora;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint64_t* lora_full;
+  uint64_t* lora_empty;
+  uint64_t* drain;
+  uint32_t* tmem_base;
+  int* abort_flag;
+  int* total_tiles;
+  int* prefix;  // [E + 1]
+};
+
+template <int kStages, bool kLora>
+__device__ __forceinline__ Smem carve(uint8_t* base) {
+  Smem s;
+  s.stages = base;
+  s.lora = base + kStages * kStageBytes;
+  uint8_t* misc = s.lora + (kLora ? kLoraBytes : 0);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+  s.full = bars;
+  s.empty = bars + kStages;
+  s.acc_full = bars + 2 * kStages;
+  s.acc_empty = s.acc_full + 1;
+  s.lora_full = s.acc_full + 2;
+  s.lora_empty = s.acc_full + 3;
+  s.drain = s.acc_full + 4;
+  s.tmem_base = reinterpret_cast<uint32_t*>(s.acc_full + 5);
+  s.abort_flag = reinterpret_cast<int*>(s.tmem_base + 1);
+  s.total_tiles = s.abort_flag + 1;
+  s.prefix = s.total_tiles + 2;
+  return s;
+}
+
+__device__ __forceinline__ int dense_tiles(const Fp4Params& p) {
+  return ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+}
+
+template <int kEpi>
+__device__ __forceinline__ int n_blocks(const Fp4Params& p) {
+  return kEpi == kEpiSwiglu ? p.N / 128 : (p.N + BN - 1) / BN;
+}
+
+template <int kEpi>
+__device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, int t) {
+  Tile tl;
+  if (p.E == 0) {
+    const int num_m = (p.M + BM - 1) / BM;
+    const int mb = t % num_m, nb = t / num_m;
+    tl.expert = 0;
+    tl.row0 = mb * BM;
+    tl.rows = min(BM, p.M - tl.row0);
+    tl.col0 = nb * BN;
+    tl.brow0 = nb * BN;
+    tl.brow1 = tl.brow0 + 128;
+    tl.sfb_blk1 = (tl.brow1 < p.N) ? tl.brow1 / 128 : tl.brow0 / 128;
+    return tl;
+  }
+  // binary search: largest e with prefix[e] <= t
+  int lo = 0, hi = p.E - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int cnt = p.counts[e];
+  const int mblk = (cnt + BM - 1) / BM;
+  const int local = t - prefix[e];
+  const int nb = local / mblk, mb = local % mblk;
+  tl.expert = e;
+  tl.row0 = p.offsets[e] + mb * BM;
+  tl.rows = min(BM, cnt - mb * BM);
+  const int64_t wrows = (kEpi == kEpiSwiglu) ? 2LL * p.N : (int64_t)p.N;  // weight rows per expert
+  if (kEpi == kEpiSwiglu) {
+    tl.col0 = nb * 128;
+    tl.brow0 = (int)(e * wrows + nb * 128);           // gate rows
+    tl.brow1 = (int)(e * wrows + p.N + nb * 128);     // up rows
+    tl.sfb_blk1 = tl.brow1 / 128;
+  } else {
+    tl.col0 = nb * BN;
+    tl.brow0 = (int)(e * wrows + nb * BN);
+    tl.brow1 = tl.brow0 + 128;
+    tl.sfb_blk1 = (nb * BN + 128 < p.N) ? tl.brow1 / 128 : tl.brow0 / 128;
+  }
+  return tl;
+}
+
+template <int kStages, bool kLora, int kEpi>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmL,
+                    const Fp4Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kAlign - 1) &
+                                             ~static_cast<uintptr_t>(kAlign - 1));
+  Smem sm = carve<kStages, kLora>(base);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  volatile int* abort_flag = sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    mbar_init(sm.acc_full, 1);
+    mbar_init(sm.acc_empty, 8);  // one arrive per epilogue warp
+    mbar_init(sm.lora_full, 1);
+    mbar_init(sm.lora_empty, 1);
+    mbar_init(sm.drain, 1);
+    *sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (kLora) {
+      prefetch_tmap(&tmT);
+      prefetch_tmap(&tmL);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(sm.tmem_base, kTmemAlloc);
+    tmem_relinquish();
+  }
+  if (warp == 3) {
+    // Tile table.  Dense: closed form.  Grouped: validate the offset table and
+    // prefix-sum the tiles of each expert.
+    if (p.E == 0) {
+      if (lane == 0) *sm.total_tiles = dense_tiles(p);
+    } else {
+      const int nb = n_blocks<kEpi>(p);
+      int running = 0;
+      bool bad = false;
+      for (int e0 = 0; e0 < p.E; e0 += 32) {
+        const int e = e0 + lane;
+        int tiles = 0;
+        if (e < p.E) {
+          const int off = p.offsets[e], cnt = p.counts[e], nxt = p.offsets[e + 1];
+          if (cnt < 0 || (off % BM) != 0 || off + cnt > nxt || nxt > p.M) bad = true;
+          tiles = ((max(cnt, 0) + BM - 1) / BM) * nb;
+        }
+        int incl = tiles;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          int v = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += v;
+        }
+        if (e < p.E) sm.prefix[e] = running + incl - tiles;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      bad = __any_sync(0xffffffffu, bad) || p.offsets[0] != 0;
+      if (lane == 0) {
+        sm.prefix[p.E] = running;
+        *sm.total_tiles = bad ? 0 : running;
+        if (bad && blockIdx.x == 0) record_status(p.status, kStatusOffsets, 1);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_base;
+  const int total = *sm.total_tiles;
+  const int kchunks = p.K / 64;
+  const int kstages = (kchunks + 3) / 4;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    PipeState<kStages> ps;
+    uint32_t issued_mask = 0, last_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = tile_of<kEpi>(p, sm.prefix, t);
+      const uint8_t* sfa_src = p.sfa + (size_t)(tl.row0 / 128) * kchunks * 512;
+      const uint8_t* sfb0_src = p.sfb + (size_t)(tl.brow0 / 128) * kchunks * 512;
+      const uint8_t* sfb1_src = p.sfb + (size_t)tl.sfb_blk1 * kchunks * 512;
+      for (int ks = 0; ks < kstages; ++ks) {
+        if (!mbar_wait(&sm.empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 10)) { ok = false; break; }
+        const int nmma = min(4, kchunks - 4 * ks);
+        uint8_t* st = sm.stages + ps.index * kStageBytes;
+        uint64_t* bar = &sm.full[ps.index];
+        mbar_arrive_expect_tx(bar, (uint32_t)(BM * 128 + BN * 128 + nmma * 512 * 3));
+        tma_load_2d(st + kOffA, &tmA, bar, ks * 128, tl.row0);
+        tma_load_2d(st + kOffB, &tmB, bar, ks * 128, tl.brow0);
+        tma_load_2d(st + kOffB + 128 * 128, &tmB, bar, ks * 128, tl.brow1);
+        bulk_load(st + kOffSfa, sfa_src + ks * 2048, nmma * 512, bar);
+        bulk_load(st + kOffSfb, sfb0_src + ks * 2048, nmma * 512, bar);
+        bulk_load(st + kOffSfb + 2048, sfb1_src + ks * 2048, nmma * 512, bar);
+        issued_mask |= 1u << ps.index;
+        last_phase = (last_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
+        ps.advance();
+      }
+    }
+    if (*abort_flag) {
+      // Let copies already in flight land before the CTA can exit.
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(&sm.full[s], (last_phase >> s) & 1u) && globaltimer() - t0 < 100000000ull) {
+          }
+        }
+    }
+  } else if (warp == 2 && lane == 0) {
+    // ------------------------------------------------------------------ low-rank producer
+    if (kLora) {
+      uint32_t phase = 0;
+      bool issued = false;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const Tile tl = tile_of<kEpi>(p, sm.prefix, t);
+        if (!mbar_wait(sm.lora_empty, phase ^ 1u, abort_flag, p.status, 20)) break;
+        mbar_arrive_expect_tx(sm.lora_full, (uint32_t)kLoraBytes);
+        tma_load_2d(sm.lora + kLoraThi, &tmT, sm.lora_full, 0, tl.row0);
+        tma_load_2d(sm.lora + kLoraTlo, &tmT, sm.lora_full, 32, tl.row0);
+        tma_load_2d(sm.lora + kLoraBl, &tmL, sm.lora_full, 0, tl.brow0);
+        tma_load_2d(sm.lora + kLoraBl + 8192, &tmL, sm.lora_full, 0, tl.brow1);
+        issued = true;
+        phase ^= 1u;
+      }
+      if (*abort_flag && issued) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(sm.lora_full, phase ^ 1u) && globaltimer() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    PipeState<kStages> ps;
+    uint32_t acc_phase = 0, lora_phase = 0, sf_buf = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      if (!mbar_wait(sm.acc_empty, acc_phase ^ 1u, abort_flag, p.status, 30)) break;
+      tc_fence_after();
+      for (int ks = 0; ks < kstages; ++ks) {
+        if (!mbar_wait(&sm.full[ps.index], ps.phase, abort_flag, p.status, 31)) { ok = false; break; }
+        tc_fence_after();
+        const int nmma = min(4, kchunks - 4 * ks);
+        uint8_t* st = sm.stages + ps.index * kStageBytes;
+        const uint32_t sa = smem_u32(st + kOffA), sb = smem_u32(st + kOffB);
+        const uint32_t ssfa = smem_u32(st + kOffSfa), ssfb = smem_u32(st + kOffSfb);
+        const uint32_t sf_col = kTmemSf + sf_buf * kSfColsPerStage;
+        for (int j = 0; j < nmma; ++j) {
+          const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
+          tc_cp_32x128b_warpx4(col, smem_desc(ssfa + 512 * j, 0, 128, kLayoutNone));
+          tc_cp_32x128b_warpx4(col + 4, smem_desc(ssfb + 512 * j, 0, 128, kLayoutNone));
+          tc_cp_32x128b_warpx4(col + 8, smem_desc(ssfb + 2048 + 512 * j, 0, 128, kLayoutNone));
+        }
+        for (int j = 0; j < nmma; ++j) {
+          const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
+          mma_mxf4nvf4(tmem + kTmemAcc, smem_desc(sa + 32 * j, 16, 1024, kLayoutSw128),
+                       smem_desc(sb + 32 * j, 16, 1024, kLayoutSw128), kIdescMain, col, col + 4,
+                       (ks > 0 || j > 0) ? 1u : 0u);
+        }
+        tc_commit(&sm.empty[ps.index]);
+        sf_buf ^= 1u;
+        ps.advance();
+      }
+      if (!ok) break;
+      if (kLora) {
+        if (!mbar_wait(sm.lora_full, lora_phase, abort_flag, p.status, 32)) break;
+        tc_fence_after();
+        const uint32_t thi = smem_u32(sm.lora + kLoraThi), tlo = smem_u32(sm.lora + kLoraTlo);
+        const uint32_t bl = smem_u32(sm.lora + kLoraBl);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t ta = part == 0 ? thi : tlo;
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            mma_bf16(tmem + kTmemAcc, smem_desc(ta + 32 * kk, 16, 512, kLayoutSw64),
+                     smem_desc(bl + 32 * kk, 16, 512, kLayoutSw64), kIdescLora, 1u);
+        }
+        tc_commit(sm.lora_empty);
+        lora_phase ^= 1u;
+      }
+      tc_commit(sm.acc_full);
+      acc_phase ^= 1u;
+    }
+    // Drain: every tcgen05 op issued above has finished before TMEM is freed.
+    tc_commit(sm.drain);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(sm.drain, 0) && globaltimer() - t0 < 1000000000ull) {
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp % 4;               // tensor-memory lane quarter
+    const int half = (warp - kEpiWarp0) / 4;
+    const int r_in_tile = q * 32 + lane;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = tile_of<kEpi>(p, sm.prefix, t);
+      // one lane polls, the warp follows (keeps the .sync.aligned loads convergent)
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(sm.acc_full, acc_phase, abort_flag, p.status, 40) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[4][32];
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      if (kEpi == kEpiSwiglu) {
+        tmem_ld32(lane_base + kTmemAcc + 64 * half, v[0]);
+        tmem_ld32(lane_base + kTmemAcc + 64 * half + 32, v[1]);
+        tmem_ld32(lane_base + kTmemAcc + 128 + 64 * half, v[2]);
+        tmem_ld32(lane_base + kTmemAcc + 128 + 64 * half + 32, v[3]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + kTmemAcc + 128 * half + 32 * c, v[c]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.acc_empty);
+      acc_phase ^= 1u;
+
+      const bool row_ok = r_in_tile < tl.rows;
+      const int64_t row = (int64_t)tl.row0 + r_in_tile;
+      if (kEpi == kEpiSwiglu) {
+        // h = bf16(silu(g) * u); padding rows of the segment are written as zeros.
+        const int col = tl.col0 + 64 * half;
+        uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * p.ldo + col;
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float hv[2];
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int cc = c + 2 * i + k2;
+              const float g = __uint_as_float(v[cc / 32][cc % 32]);
+              const float u = __uint_as_float(v[2 + cc / 32][cc % 32]);
+              hv[k2] = row_ok ? (g / (1.0f + __expf(-g))) * u : 0.0f;
+            }
+            w[i] = pack_bf16x2(hv[0], hv[1]);
+          }
+          *reinterpret_cast<uint4*>(out + c) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else if (kEpi == kEpiCombine) {
+        const int col = tl.col0 + 128 * half;
+        if (row_ok && col < p.N) {
+          const int tok = p.token_of[row];
+          const float wt = p.weight_of[row];
+          if (tok >= 0) {
+            float* dst = p.out32 + (int64_t)tok * p.ld_out32 + col;
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+              const float a0 = wt * __uint_as_float(v[c / 32][c % 32]);
+              const float a1 = wt * __uint_as_float(v[c / 32][c % 32 + 1]);
+              const float a2 = wt * __uint_as_float(v[c / 32][c % 32 + 2]);
+              const float a3 = wt * __uint_as_float(v[c / 32][c % 32 + 3]);
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c), "f"(a0), "f"(a1),
+                           "f"(a2), "f"(a3)
+                           : "memory");
+            }
+          }
+        }
+      } else {
+        const int col = tl.col0 + 128 * half;
+        if (row_ok && col < p.N) {
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int n = col + c + i;
+              float a = __uint_as_float(v[(c + i) / 32][(c + i) % 32]);
+              float sc = p.alpha;
+              if (p.col_scale) sc *= p.col_scale[n];
+              a *= sc;
+              if (p.bias) a += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.bias)[n]);
+              y[i] = a;
+            }
+            if (p.out_bf16) {
+              uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * p.ldo + col + c;
+              *reinterpret_cast<uint4*>(out) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                          pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+            } else {
+              float* out = reinterpret_cast<float*>(p.out) + row * p.ldo + col + c;
+              *reinterpret_cast<float4*>(out) = make_float4(y[0], y[1], y[2], y[3]);
+              *reinterpret_cast<float4*>(out + 4) = make_float4(y[4], y[5], y[6], y[7]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemAlloc);
+  }
+}
+
+template <int kStages, bool kLora, int kEpi>
+static cudaError_t launch_one(const Fp4Launch& L, cudaStream_t stream) {
+  auto kern = fp4_gemm_kernel<kStages, kLora, kEpi>;
+  const int smem = fp4_smem_total(kLora ? kShapeLora : kShapeNoLora, kStages) + kAlign;
+  static_assert(fp4_smem_total(kShapeLora, kStagesLora) + kAlign <= kSmemPerCta, "lora smem");
+  static_assert(fp4_smem_total(kShapeNoLora, kStagesNoLora) + kAlign <= kSmemPerCta, "smem");
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<L.grid, kThreads, smem, stream>>>(L.tmA, L.tmB, L.tmT, L.tmL, L.p);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4
+
+cudaError_t launch_fp4_gemm(const Fp4Launch& L, cudaStream_t stream) {
+  using namespace fp4;
+  if (L.lora) {
+    if (L.epilogue != kEpiStore) return cudaErrorInvalidValue;
+    return launch_one<kStagesLora, true, kEpiStore>(L, stream);
+  }
+  switch (L.epilogue) {
+    case kEpiStore: return launch_one<kStagesNoLora, false, kEpiStore>(L, stream);
+    case kEpiSwiglu: return launch_one<kStagesNoLora, false, kEpiSwiglu>(L, stream);
+    case kEpiCombine: return launch_one<kStagesNoLora, false, kEpiCombine>(L, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int fp4_stages(bool lora) { return lora ? fp4::kStagesLora : fp4::kStagesNoLora; }
+
+}  // namespace bsk

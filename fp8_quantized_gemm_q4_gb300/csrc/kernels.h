@@ -1,0 +1,81 @@
+// kernels.h -- internal interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not installed; the public ABI is bsgemm.h.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bsk {
+
+enum { kEpiStore = 0, kEpiSwiglu = 1, kEpiCombine = 2 };
+
+struct Fp4Params {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int M, N, K;            // N: output columns
+  float alpha;
+  const float* col_scale; // [N] or null
+  const void* bias;       // bf16 [N] or null
+  void* out;
+  int out_bf16;
+  long long ldo;
+  // grouped (E > 0)
+  int E;
+  const int* offsets;     // [E+1]
+  const int* counts;      // [E]
+  const int* token_of;
+  const float* weight_of;
+  float* out32;
+  long long ld_out32;
+  int* status;
+};
+
+struct Fp4Launch {
+  CUtensorMap tmA, tmB, tmT, tmL;
+  Fp4Params p;
+  bool lora;
+  int epilogue;
+  int grid;
+};
+
+cudaError_t launch_fp4_gemm(const Fp4Launch& L, cudaStream_t stream);
+int fp4_stages(bool lora);
+
+struct Fp8Params {
+  const float* sfa;       // [K/128, M]
+  const float* sfb;       // [ceil(N/128), K/128]
+  int M, N, K;
+  void* out;
+  int out_bf16;
+  long long ldo;
+  float* work;            // split-K partials (decode), may be null
+  int* counters;          // split-K tile counters (decode), may be null
+  int splits;
+  int* status;
+};
+
+struct Fp8Launch {
+  CUtensorMap tmA, tmB;
+  Fp8Params p;
+  bool swap_ab;           // decode: weight rows fill the MMA M dimension
+  int tile_n;             // MMA N of the swap-AB kernel (16..256)
+  int grid;
+};
+
+cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream);
+
+// quantizers
+cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx,
+                               const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream);
+cudaError_t launch_lowrank_t(const void* x, long long M, long long K, long long ldx, const int* gather,
+                             const void* lora_a_t, void* lora_t, cudaStream_t stream);
+cudaError_t launch_q8_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx, int mode,
+                               uint8_t* codes, float* scales, cudaStream_t stream);
+
+// MoE
+cudaError_t launch_moe_dispatch(const int* topk_ids, const float* topk_w, long long T, int k, int E,
+                                int* counts, int* offsets, int* pair_of_row, int* token_of, float* weight_of,
+                                int* work, long long rows_bound, int* status, cudaStream_t stream);
+cudaError_t launch_moe_finalize(float* out32, void* out_bf16, long long n, cudaStream_t stream);
+
+}  // namespace bsk

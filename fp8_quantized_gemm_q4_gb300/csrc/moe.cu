@@ -1,0 +1,180 @@
+// moe.cu -- grouping of routed (token, slot) pairs by expert and the final
+// fp32 -> bf16 cast of the combined MoE output.
+//
+// Grouping ("DeepGEMM teardown (FP8 GEMM)", section 5.3: pass group offsets,
+// keep each expert's rows contiguous and movable in blocks) is a stable
+// counting sort over the flattened pair index p = t*k + slot:
+//   1. count:  one warp per chunk of 1024 pairs -> histogram [chunk][E]
+//   2. scan:   one CTA: per-expert running sums over chunks (stable bases),
+//              counts, and 128-aligned segment offsets
+//   3. place:  one warp per chunk, pairs in order; ranks among equal experts
+//              inside each 32-pair round come from __match_any_sync, so the
+//              result is identical to a sequential stable sort; padding rows
+//              get pair/token -1 and weight 0
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bsk {
+
+constexpr int kChunk = 1024;
+constexpr int kSegAlign = 128;
+
+__global__ void __launch_bounds__(32) moe_count_kernel(const int* __restrict__ ids, long long P, int E,
+                                                       int* __restrict__ hist, int* status) {
+  extern __shared__ int cnt[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const long long p0 = (long long)blockIdx.x * kChunk;
+  for (int i = lane; i < kChunk; i += 32) {
+    const long long p = p0 + i;
+    if (p >= P) break;
+    const int e = ids[p];
+    if (e < 0 || e >= E) {
+      record_status(status, kStatusOffsets, 2);
+      continue;
+    }
+    atomicAdd(&cnt[e], 1);
+  }
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) hist[(long long)blockIdx.x * E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(1024) moe_scan_kernel(int* __restrict__ hist, int nchunks, int E,
+                                                        int* __restrict__ counts, int* __restrict__ offsets) {
+  __shared__ int padded[1024];
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int h = hist[(long long)c * E + e];
+      hist[(long long)c * E + e] = total;  // exclusive base of chunk c inside expert e
+      total += h;
+    }
+    counts[e] = total;
+  }
+  const int pad = (e < E) ? (total + kSegAlign - 1) / kSegAlign * kSegAlign : 0;
+  // block-wide exclusive scan of the padded sizes
+  const int lane = e & 31, warp = e >> 5;
+  int incl = pad;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int wi = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += v;
+    }
+    warp_sums[lane] = wi - w;
+  }
+  __syncthreads();
+  const int excl = warp_sums[warp] + incl - pad;
+  padded[e] = excl;
+  if (e < E) offsets[e] = excl;
+  if (e == E - 1) offsets[E] = excl + pad;
+  __syncthreads();
+  if (e < E)
+    for (int c = 0; c < nchunks; ++c) hist[(long long)c * E + e] += padded[e];
+}
+
+__global__ void __launch_bounds__(32) moe_place_kernel(const int* __restrict__ ids, const float* __restrict__ w,
+                                                       long long P, int k, int E, const int* __restrict__ base,
+                                                       const int* __restrict__ counts,
+                                                       const int* __restrict__ offsets, int* __restrict__ pair_of_row,
+                                                       int* __restrict__ token_of, float* __restrict__ weight_of,
+                                                       long long rows_bound) {
+  extern __shared__ int pos[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) pos[e] = base[(long long)blockIdx.x * E + e];
+  __syncwarp();
+  const long long p0 = (long long)blockIdx.x * kChunk;
+  for (int i = 0; i < kChunk; i += 32) {
+    const long long p = p0 + i + lane;
+    const bool live = p < P;
+    int e = live ? ids[p] : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int leader = __ffs(peers) - 1;
+    int slot = 0;
+    if (e >= 0) slot = pos[e] + rank;
+    __syncwarp();
+    if (e >= 0 && lane == leader) pos[e] += __popc(peers);
+    __syncwarp();
+    if (e >= 0) {
+      pair_of_row[slot] = (int)p;
+      token_of[slot] = (int)(p / k);
+      weight_of[slot] = w[p];
+    }
+  }
+  // padding rows: a share of [0, rows_bound) per warp
+  const long long per = (rows_bound + gridDim.x - 1) / gridDim.x;
+  const long long r0 = (long long)blockIdx.x * per;
+  const long long r1 = min(rows_bound, r0 + per);
+  for (long long r = r0 + lane; r < r1; r += 32) {
+    bool pad_row = r >= offsets[E];
+    if (!pad_row) {
+      int lo = 0, hi = E - 1;  // largest e with offsets[e] <= r
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      pad_row = r >= (long long)offsets[lo] + counts[lo];
+    }
+    if (pad_row) {
+      pair_of_row[r] = -1;
+      token_of[r] = -1;
+      weight_of[r] = 0.0f;
+    }
+  }
+}
+
+__global__ void moe_finalize_kernel(float* __restrict__ out32, __nv_bfloat16* __restrict__ out, long long n) {
+  const long long n4 = n / 4;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    float4 v = reinterpret_cast<float4*>(out32)[i];
+    reinterpret_cast<float4*>(out32)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    reinterpret_cast<uint2*>(out)[i] = o;
+  }
+  for (long long i = n4 * 4 + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    out[i] = __float2bfloat16_rn(out32[i]);
+    out32[i] = 0.0f;
+  }
+}
+
+long long moe_chunks(long long P) { return (P + kChunk - 1) / kChunk; }
+
+cudaError_t launch_moe_dispatch(const int* topk_ids, const float* topk_w, long long T, int k, int E, int* counts,
+                                int* offsets, int* pair_of_row, int* token_of, float* weight_of, int* work,
+                                long long rows_bound, int* status, cudaStream_t stream) {
+  const long long P = T * k;
+  const long long nch = moe_chunks(P) > 0 ? moe_chunks(P) : 1;
+  const size_t smem = (size_t)E * sizeof(int);
+  moe_count_kernel<<<(unsigned)nch, 32, smem, stream>>>(topk_ids, P, E, work, status);
+  moe_scan_kernel<<<1, 1024, 0, stream>>>(work, (int)nch, E, counts, offsets);
+  moe_place_kernel<<<(unsigned)nch, 32, smem, stream>>>(topk_ids, topk_w, P, k, E, work, counts, offsets,
+                                                         pair_of_row, token_of, weight_of, rows_bound);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_finalize(float* out32, void* out_bf16, long long n, cudaStream_t stream) {
+  long long blocks = (n / 4 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  moe_finalize_kernel<<<(unsigned)blocks, 256, 0, stream>>>(out32, reinterpret_cast<__nv_bfloat16*>(out_bf16), n);
+  return cudaGetLastError();
+}
+
+}  // namespace bsk

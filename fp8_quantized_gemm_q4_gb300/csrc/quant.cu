@@ -1,0 +1,274 @@
+// quant.cu -- activation / weight quantizers for sm_103a.
+//
+// FP4: per group of 16 K elements s = e4m3(fl32(amax / 6)), code =
+// e2m1(fl32(x / s)) ("Tencent AI Infra interview notes": E2M1 format table,
+// per-group quantization, online activation quantization).  Each thread owns 8
+// consecutive elements (one 128-bit bf16 load), a group is a lane pair (one
+// shuffle for its amax), and the four scales of a 64-element chunk are
+// gathered by shuffles into the 32-bit word the tensor core reads, written at
+// its place in the MMA scale layout.  Codes use the hardware cvt with round to
+// nearest even and saturation; the divisions are IEEE.
+//
+// FP8: s = fl32(amax / 448), code = e4m3(fl32(x / s)) per 1x128 token block or
+// 128x128 weight block ("DeepGEMM teardown (FP8 GEMM)", sections 2.2 and 5.2).
+//
+// Low-rank left factor T = X A of L(X) = X A B ("Warp-specialised W4A4
+// kernel", section 1) on the unquantized bf16 rows, fp32 accumulation on the
+// warp-level tensor-core path, written as bf16 hi|lo pairs.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bsk {
+
+__device__ __forceinline__ void load8(const void* x, int x_bf16, long long off, float (&v)[8]) {
+  if (x_bf16) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(x) + off));
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + off));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + off + 4));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
+// One warp per (row, 256-element segment), grid-stride.  Rows in [M, Mpad)
+// (the 128-row padding of the scale tensor) get zero scales, no codes.
+__global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict__ x, int x_bf16, long long M,
+                                                          long long Mpad, long long K, long long ldx,
+                                                          const int* __restrict__ gather,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int lane = threadIdx.x & 31;
+  const long long nseg = (K + 255) / 256;
+  const long long total = Mpad * nseg;
+  const long long kchunks = K / 64;
+  for (long long w = (long long)blockIdx.x * 8 + threadIdx.x / 32; w < total; w += (long long)gridDim.x * 8) {
+    const long long row = w / nseg, seg = w % nseg;
+    const long long k0 = seg * 256 + lane * 8;
+    const bool active = k0 < K;
+    long long src = row < M ? row : -1;
+    if (src >= 0 && gather) src = gather[row];
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    if (active && src >= 0) load8(x, x_bf16, src * ldx + k0, v);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const uint32_t s_code = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
+    const float s = e4m3_to_f32(s_code);
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = (s == 0.0f) ? 0.0f : __fdiv_rn(v[i], s);
+    const uint32_t word = f32x8_to_e2m1x8(q);
+    if (active && row < M) *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + k0 / 2) = word;
+    const uint32_t b1 = __shfl_down_sync(0xffffffffu, s_code, 2);
+    const uint32_t b2 = __shfl_down_sync(0xffffffffu, s_code, 4);
+    const uint32_t b3 = __shfl_down_sync(0xffffffffu, s_code, 6);
+    if (active && (lane & 7) == 0) {
+      const long long chunk = k0 / 64;
+      const long long off = ((row / 128) * kchunks + chunk) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4;
+      *reinterpret_cast<uint32_t*>(sf + off) = s_code | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+  }
+}
+
+// T[m, j] = sum_k x[src(m), k] * At[j, k] for j < 32, on mma.sync m16n8k16
+// (bf16 x bf16 -> fp32).  A CTA owns 16 rows; its 8 warps interleave the K
+// steps and reduce through shared memory.  Output bf16 [M, 64]: hi | lo.
+__global__ void __launch_bounds__(256) lowrank_t_kernel(const __nv_bfloat16* __restrict__ x, long long M,
+                                                        long long K, long long ldx,
+                                                        const int* __restrict__ gather,
+                                                        const __nv_bfloat16* __restrict__ at,
+                                                        __nv_bfloat16* __restrict__ t_out) {
+  __shared__ float red[8][16][33];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane / 4, tq = lane % 4;
+  const long long r0 = (long long)blockIdx.x * 16;
+  long long src_lo = r0 + g < M ? r0 + g : -1, src_hi = r0 + g + 8 < M ? r0 + g + 8 : -1;
+  if (gather) {
+    if (src_lo >= 0) src_lo = gather[src_lo];
+    if (src_hi >= 0) src_hi = gather[src_hi];
+  }
+  const uint32_t* xlo = src_lo >= 0 ? reinterpret_cast<const uint32_t*>(x + src_lo * ldx) : nullptr;
+  const uint32_t* xhi = src_hi >= 0 ? reinterpret_cast<const uint32_t*>(x + src_hi * ldx) : nullptr;
+  float d[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[i][j] = 0.0f;
+  for (long long k = (long long)warp * 16; k < K; k += 8 * 16) {
+    const long long c0 = (k + 2 * tq) / 2, c1 = (k + 2 * tq + 8) / 2;  // uint32 (bf16 pair) index
+    const uint32_t a0 = xlo ? __ldg(xlo + c0) : 0u, a1 = xhi ? __ldg(xhi + c0) : 0u;
+    const uint32_t a2 = xlo ? __ldg(xlo + c1) : 0u, a3 = xhi ? __ldg(xhi + c1) : 0u;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const uint32_t* brow = reinterpret_cast<const uint32_t*>(at + (long long)(nt * 8 + g) * K);
+      const uint32_t b0 = __ldg(brow + c0), b1 = __ldg(brow + c1);
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+          "{%0, %1, %2, %3};"
+          : "+f"(d[nt][0]), "+f"(d[nt][1]), "+f"(d[nt][2]), "+f"(d[nt][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    red[warp][g][nt * 8 + 2 * tq] = d[nt][0];
+    red[warp][g][nt * 8 + 2 * tq + 1] = d[nt][1];
+    red[warp][g + 8][nt * 8 + 2 * tq] = d[nt][2];
+    red[warp][g + 8][nt * 8 + 2 * tq + 1] = d[nt][3];
+  }
+  __syncthreads();
+  for (int o = threadIdx.x; o < 16 * 32; o += 256) {
+    const int rr = o / 32, j = o % 32;
+    const long long row = r0 + rr;
+    if (row >= M) continue;
+    float s = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += red[w][rr][j];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(s);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(s - __bfloat162float(hi));
+    t_out[row * 64 + j] = hi;
+    t_out[row * 64 + 32 + j] = lo;
+  }
+}
+
+// FP8 1x128: one warp per (row, 128-block), 4 elements per lane.
+__global__ void __launch_bounds__(256) q8_token_kernel(const void* __restrict__ x, int x_bf16, long long M,
+                                                       long long K, long long ldx, uint8_t* __restrict__ codes,
+                                                       float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const long long nkb = K / 128;
+  const long long total = M * nkb;
+  for (long long w = (long long)blockIdx.x * 8 + threadIdx.x / 32; w < total; w += (long long)gridDim.x * 8) {
+    const long long row = w / nkb, kb = w % nkb;
+    const long long off = row * ldx + kb * 128 + lane * 4;
+    float v[4];
+    if (x_bf16) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(x) + off));
+      v[0] = __uint_as_float(raw.x << 16);
+      v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+      v[2] = __uint_as_float(raw.y << 16);
+      v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+    } else {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + off));
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    }
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float s = __fdiv_rn(amax, 448.0f);
+    float q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = (s == 0.0f) ? 0.0f : __fdiv_rn(v[i], s);
+    const uint32_t c = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
+    *reinterpret_cast<uint32_t*>(codes + row * K + kb * 128 + lane * 4) = c;
+    if (lane == 0) scales[kb * M + row] = s;
+  }
+}
+
+// FP8 128x128 blocks: one CTA (256 threads) per block.
+__global__ void __launch_bounds__(256) q8_block_kernel(const void* __restrict__ x, int x_bf16, long long M,
+                                                       long long K, long long ldx, uint8_t* __restrict__ codes,
+                                                       float* __restrict__ scales) {
+  __shared__ float wmax[8];
+  const long long rb = blockIdx.y, kb = blockIdx.x;
+  const int tid = threadIdx.x;
+  // thread -> (row r = tid / 2 .. in 2 passes of 64 rows? keep it simple: 64 elements each)
+  const int r_local = tid / 2, c_local = (tid % 2) * 64;
+  const long long row = rb * 128 + r_local;
+  float v[64];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 64; i += 8) {
+    float t8[8];
+    if (row < M) {
+      load8(x, x_bf16, row * ldx + kb * 128 + c_local + i, t8);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) t8[j] = 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[i + j] = t8[j];
+      amax = fmaxf(amax, fabsf(t8[j]));
+    }
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  if ((tid & 31) == 0) wmax[tid / 32] = amax;
+  __syncthreads();
+  amax = wmax[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, wmax[i]);
+  const float s = __fdiv_rn(amax, 448.0f);
+  if (tid == 0) scales[rb * (K / 128) + kb] = s;
+  if (row < M) {
+#pragma unroll
+    for (int i = 0; i < 64; i += 16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float q0 = (s == 0.0f) ? 0.0f : __fdiv_rn(v[i + 4 * j], s);
+        const float q1 = (s == 0.0f) ? 0.0f : __fdiv_rn(v[i + 4 * j + 1], s);
+        const float q2 = (s == 0.0f) ? 0.0f : __fdiv_rn(v[i + 4 * j + 2], s);
+        const float q3 = (s == 0.0f) ? 0.0f : __fdiv_rn(v[i + 4 * j + 3], s);
+        w[j] = f32x2_to_e4m3x2(q0, q1) | (f32x2_to_e4m3x2(q2, q3) << 16);
+      }
+      *reinterpret_cast<uint4*>(codes + row * K + kb * 128 + c_local + i) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx,
+                               const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream) {
+  const long long Mpad = (M + 127) / 128 * 128;
+  const long long warps = Mpad * ((K + 255) / 256);
+  long long blocks = (warps + 7) / 8;
+  const long long cap = (long long)sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  q4_quantize_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, x_bf16, M, Mpad, K, ldx, gather, codes, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lowrank_t(const void* x, long long M, long long K, long long ldx, const int* gather,
+                             const void* lora_a_t, void* lora_t, cudaStream_t stream) {
+  const long long blocks = (M + 15) / 16;
+  lowrank_t_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(x), M, K, ldx,
+                                                          gather, reinterpret_cast<const __nv_bfloat16*>(lora_a_t),
+                                                          reinterpret_cast<__nv_bfloat16*>(lora_t));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q8_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx, int mode,
+                               uint8_t* codes, float* scales, cudaStream_t stream) {
+  if (mode == 1) {
+    const long long warps = M * (K / 128);
+    long long blocks = (warps + 7) / 8;
+    const long long cap = (long long)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    q8_token_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, x_bf16, M, K, ldx, codes, scales);
+  } else {
+    dim3 grid((unsigned)(K / 128), (unsigned)((M + 127) / 128));
+    q8_block_kernel<<<grid, 256, 0, stream>>>(x, x_bf16, M, K, ldx, codes, scales);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace bsk

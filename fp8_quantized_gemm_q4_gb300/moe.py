@@ -1,0 +1,94 @@
+"""Grouped FP4 MoE layer composed from the library's entry points.
+
+Order of the layer ("DeepGEMM for Hopper MoE", sections 1 and 3; "DeepGEMM
+teardown (FP8 GEMM)", section 5.3):
+
+  1. bs_moe_dispatch     group the (token, slot) pairs by expert into
+                         128-aligned contiguous segments
+  2. q4_quantize         gather each routed token's row and quantize it online
+  3. bs_grouped_gemm     gate/up GEMM per expert with the SwiGLU epilogue
+                         h = bf16(silu(x W_gate^T) * (x W_up^T))
+  4. q4_quantize         re-quantize h online
+  5. bs_grouped_gemm     down GEMM per expert with the routed combine epilogue
+                         out32[token] += w * (h W_down^T)   (fp32 reductions)
+  6. bs_moe_finalize     out = bf16(out32), out32 reset to zero
+
+Every step is one or more of the library's kernels; this module only holds
+the buffers and calls them in order.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import (EPI_COMBINE, EPI_SWIGLU, grouped_gemm_fp4, moe_dispatch, moe_finalize, moe_rows_bound,
+               q4_quantize, sf_bytes)
+
+
+@dataclass
+class MoEWeights:
+    """Stacked FP4 expert weights: gate/up [E*2F, H] (gate rows first per
+    expert) and down [E*H, F], codes plus MMA-layout scales."""
+    E: int
+    H: int
+    F: int
+    wgu_codes: torch.Tensor
+    wgu_sf: torch.Tensor
+    wd_codes: torch.Tensor
+    wd_sf: torch.Tensor
+
+
+def quantize_expert_weights(wgu_list, wd_list, device="cuda") -> MoEWeights:
+    """Quantize per-expert bf16 weights (offline, outside the layer's timed path)."""
+    E = len(wgu_list)
+    F2, H = wgu_list[0].shape
+    F = F2 // 2
+    wgu_codes = torch.empty((E * F2, H // 2), dtype=torch.uint8, device=device)
+    wgu_sf = torch.empty(sf_bytes(E * F2, H), dtype=torch.uint8, device=device)
+    wd_codes = torch.empty((E * H, F // 2), dtype=torch.uint8, device=device)
+    wd_sf = torch.empty(sf_bytes(E * H, F), dtype=torch.uint8, device=device)
+    per_gu, per_d = sf_bytes(F2, H), sf_bytes(H, F)
+    for e in range(E):
+        wgu = wgu_list[e].to(device)
+        wd = wd_list[e].to(device)
+        q4_quantize(wgu, out=(wgu_codes[e * F2:(e + 1) * F2], wgu_sf[e * per_gu:(e + 1) * per_gu], None))
+        q4_quantize(wd, out=(wd_codes[e * H:(e + 1) * H], wd_sf[e * per_d:(e + 1) * per_d], None))
+    return MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf)
+
+
+class MoELayer:
+    """Holds the per-call buffers of one layer shape so repeated calls (and a
+    CUDA-graph capture) allocate nothing."""
+
+    def __init__(self, weights: MoEWeights, T: int, k: int, device="cuda"):
+        self.w = weights
+        self.T, self.k = T, k
+        E, H, F = weights.E, weights.H, weights.F
+        self.rows = moe_rows_bound(T, k, E)
+        self.xq = torch.empty((self.rows, H // 2), dtype=torch.uint8, device=device)
+        self.xs = torch.empty(sf_bytes(self.rows, H), dtype=torch.uint8, device=device)
+        self.h = torch.zeros((self.rows, F), dtype=torch.bfloat16, device=device)
+        self.hq = torch.empty((self.rows, F // 2), dtype=torch.uint8, device=device)
+        self.hs = torch.empty(sf_bytes(self.rows, F), dtype=torch.uint8, device=device)
+        self.out32 = torch.zeros((T, H), dtype=torch.float32, device=device)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        self.disp = None
+        self.workspace = None
+
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor) -> torch.Tensor:
+        w = self.w
+        self.disp = moe_dispatch(topk_ids, topk_w, w.E, out=self.disp, workspace=self.workspace)
+        if self.workspace is None:
+            # keep the workspace moe_dispatch allocated for later calls
+            pass
+        d = self.disp
+        q4_quantize(x, gather=d["token_of"], rows=self.rows, out=(self.xq, self.xs, None))
+        grouped_gemm_fp4(self.xq, self.xs, w.wgu_codes, w.wgu_sf, K=w.H, N=w.F, E=w.E, offsets=d["offsets"],
+                         counts=d["counts"], epilogue=EPI_SWIGLU, out=self.h)
+        q4_quantize(self.h, out=(self.hq, self.hs, None))
+        grouped_gemm_fp4(self.hq, self.hs, w.wd_codes, w.wd_sf, K=w.F, N=w.H, E=w.E, offsets=d["offsets"],
+                         counts=d["counts"], epilogue=EPI_COMBINE, token_of=d["token_of"],
+                         weight_of=d["weight_of"], out32=self.out32)
+        moe_finalize(self.out32, self.out)
+        return self.out

@@ -1,0 +1,251 @@
+/*
+ * bsgemm.h -- C ABI of the block-scaled FP4 / FP8 GEMM library for GB300
+ * (sm_103a).
+ *
+ * The library computes the block-scaled low-precision matrix multiply
+ *
+ *     Y = (Q(X) Q(W)^T) (.) scale + L(X) + b
+ *
+ * ("Warp-specialised W4A4 kernel on the newest GPU architecture", section 1),
+ * with Q = FP4 E2M1 codes and one e4m3 scale per 16 consecutive K elements
+ * ("Tencent AI Infra interview notes", FP4 format table and per-group
+ * quantization), or Q = FP8 e4m3 codes with fp32 scales per 1x128 activation
+ * block and per 128x128 weight block ("DeepGEMM teardown (FP8 GEMM)",
+ * sections 2.2-2.3), always accumulating in FP32; densely and grouped over
+ * MoE experts ("DeepGEMM teardown", section 5.3; "DeepGEMM for Hopper MoE",
+ * sections 1 and 3).
+ *
+ * Conventions shared by every entry point:
+ *  - All pointers are DEVICE pointers unless stated otherwise.  The caller
+ *    allocates and owns every buffer; the library never allocates, frees or
+ *    synchronises.  Calls are asynchronous on `stream` (NULL = legacy stream).
+ *  - Matrices are row-major with the K dimension contiguous ("K-major").
+ *    Leading dimensions are in elements.
+ *  - Host-side validation happens before any launch: a call that returns
+ *    anything but BS_OK has launched nothing.
+ *  - Device-side failures (a bounded pipeline wait that timed out, an
+ *    inconsistent expert-offset table) set a sticky device status word that
+ *    bs_get_device_status() reads back; kernels never trap.
+ *  - Values are assumed finite.
+ */
+#ifndef BSGEMM_H
+#define BSGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *bs_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    BS_OK = 0,
+    BS_ERR_INVALID = 1,     /* null pointer, bad size or enum value */
+    BS_ERR_ALIGN = 2,       /* pointer / leading dimension not 16-byte aligned, K or N not a multiple of the block */
+    BS_ERR_UNSUPPORTED = 3, /* valid request this build does not implement */
+    BS_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute, tensor-map encode) */
+    BS_ERR_TIMEOUT = 5,     /* device status: a bounded pipeline wait gave up */
+    BS_ERR_OFFSETS = 6      /* device status: expert offsets / counts inconsistent */
+} bs_status;
+
+typedef enum { BS_DTYPE_F32 = 0, BS_DTYPE_BF16 = 1 } bs_dtype;
+
+typedef enum { BS_FMT_FP4 = 0, BS_FMT_FP8 = 1 } bs_format;
+
+typedef enum {
+    BS_EPI_STORE = 0,  /* Y rows written to `out` */
+    BS_EPI_SWIGLU = 1, /* grouped only: out[r, n] = bf16(silu(g[r,n]) * u[r,n]) */
+    BS_EPI_COMBINE = 2 /* grouped only: out32[token_of[r], n] += weight_of[r] * y[r, n] */
+} bs_epilogue;
+
+typedef enum { BS_Q8_TOKEN_1x128 = 1, BS_Q8_BLOCK_128x128 = 128 } bs_q8_mode;
+
+/* ---------------------------------------------------------------------------
+ * FP4 scale-factor layout ("MMA layout").
+ *
+ * The e4m3 group scales of an [rows, K] FP4 operand are stored in the order
+ * the tensor core reads them: 512-byte tiles, one per (128-row block rb,
+ * 64-element K chunk kc), tiles ordered rb-major (tile index rb*(K/64)+kc);
+ * inside a tile the scale of row r (0..127) and group j (0..3, 16 elements
+ * each) is at byte (r % 32) * 16 + (r / 32) * 4 + j.  Rows are padded to a
+ * multiple of 128; padding rows hold zero scales after q4_quantize.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of the scale tensor of an [rows, K] FP4 operand (K % 64 == 0). */
+size_t bs_sf_bytes(int64_t rows, int64_t K);
+
+/* Byte offset of the scale of (row, group) where group = k / 16. */
+int64_t bs_sf_offset(int64_t row, int64_t group, int64_t K);
+
+/* ---------------------------------------------------------------------------
+ * q4_quantize -- FP4 E2M1 group-16 quantization of activations or weights
+ * ("Tencent AI Infra interview notes", FP4 format table and per-group
+ * quantization; online activation quantization in Q "How does hardware
+ * quantize").  For output row i (source row g = gather ? gather[i] : i; a
+ * negative g gives an all-zero row) and every group of 16 K elements:
+ *     s    = e4m3_rn_satfinite(fl32(amax / 6))
+ *     code = e2m1_rn_satfinite(fl32(x / s))     (0 when s == 0)
+ * IEEE fp32 division, round to nearest even, saturation at 448 / 6, the sign
+ * of a value that rounds to zero is kept (code 0b1000).
+ *
+ *   x       [*, ldx] fp32 or bf16 (dt); 16-byte aligned, ldx % 8 == 0
+ *   M, K    output rows, K % 64 == 0
+ *   gather  [M] int32 source-row map, or NULL
+ *   codes   [M, K/2] bytes: element k in the low nibble of byte k/2 if k is
+ *           even, in the high nibble if odd
+ *   sf      bs_sf_bytes(M, K) bytes in the MMA layout above
+ *   lora_a_t, r, lora_t (optional, all NULL/0 or all set; bf16 input only):
+ *           the left factor of the low-rank branch L(X) = X A B,
+ *           T = X A on the UNQUANTIZED rows, with lora_a_t = A^T bf16 [r, K]
+ *           (K contiguous) and r == 32.  lora_t receives bf16 [M, 2r]:
+ *           columns [0, r) = hi = bf16(T), [r, 2r) = lo = bf16(T - hi), so
+ *           hi + lo carries T to about 2^-17 relative.
+ * ------------------------------------------------------------------------- */
+bs_status q4_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx,
+                      const int32_t *gather, uint8_t *codes, uint8_t *sf,
+                      const void *lora_a_t, int r, void *lora_t, bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * q8_quantize -- FP8 e4m3 quantization with fp32 block scales ("DeepGEMM
+ * teardown", section 2.2 per-token / per-block scaling, section 5.2 scale =
+ * max_val / 448).  For every block (1 x 128 in BS_Q8_TOKEN_1x128 mode,
+ * 128 x 128 in BS_Q8_BLOCK_128x128 mode):
+ *     s    = fl32(amax / 448)
+ *     code = e4m3_rn_satfinite(fl32(x / s))     (0 when s == 0)
+ *
+ *   x       [M, ldx] fp32 or bf16; 16-byte aligned, ldx % 8 == 0; K % 128 == 0
+ *   codes   [M, K] bytes
+ *   scales  TOKEN mode: fp32 [K/128, M] (K-block major: the scales of one K
+ *           block are contiguous over rows);
+ *           BLOCK mode: fp32 [ceil(M/128), K/128]
+ * ------------------------------------------------------------------------- */
+bs_status q8_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx,
+                      int mode, uint8_t *codes, float *scales, bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * bs_gemm -- dense block-scaled GEMM, Y[M, N] = A[M, K] B[N, K]^T.
+ *
+ * FP4 (fmt = BS_FMT_FP4; "Warp-specialised W4A4 kernel", section 1):
+ *     Y[m,n] = alpha * col_scale[n] * sum_g sfa[m,g] sfb[n,g] sum_{k in g} a b
+ *              + sum_r T[m,r] Bl[r,n] + bias[n]
+ *   a, b       codes [M, K/2] / [N, K/2] as written by q4_quantize
+ *   sfa, sfb   bs_sf_bytes(M, K) / bs_sf_bytes(N, K) scale bytes (MMA layout)
+ *   alpha      scalar (1 = none); col_scale fp32 [N] or NULL
+ *   lora_t     bf16 [M, 2r] hi|lo from q4_quantize, or NULL; lora_b_t =
+ *              Bl^T bf16 [N, r]; r == 32.  With lora_t set, alpha must be 1
+ *              and col_scale NULL (BS_ERR_UNSUPPORTED otherwise).
+ * FP8 (fmt = BS_FMT_FP8; "DeepGEMM for Hopper MoE", section 2.1;
+ *      "DeepGEMM teardown", sections 2.2-2.3):
+ *     Y[m,n] = sum_kb sa[kb,m] * sb[n/128,kb] * sum_{k in kb} a b  (kb: 128 wide)
+ *   a, b       e4m3 codes [M, K] / [N, K]
+ *   sfa        fp32 [K/128, M] (q8_quantize TOKEN mode)
+ *   sfb        fp32 [ceil(N/128), K/128] (q8_quantize BLOCK mode)
+ *   alpha / col_scale / lora / bias must be 1 / NULL / NULL / NULL.
+ * Common:
+ *   bias       bf16 [N] or NULL (FP4 only)
+ *   out        [M, ldo] fp32 or bf16 (out_dtype), 16-byte aligned, ldo % 8 == 0
+ *   M >= 0, N % 128 == 0, K % 64 == 0 (FP4) or K % 128 == 0 (FP8)
+ *   num_sms    persistent grid size limit (0 = all SMs)
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int fmt;                 /* bs_format */
+    const uint8_t *a;
+    const void *sfa;
+    const uint8_t *b;
+    const void *sfb;
+    int64_t M, N, K;
+    float alpha;
+    const float *col_scale;
+    const void *lora_t;
+    const void *lora_b_t;
+    int r;
+    const void *bias;
+    void *out;
+    int out_dtype;           /* bs_dtype */
+    int64_t ldo;
+    int num_sms;
+} bs_gemm_args;
+
+bs_status bs_gemm(const bs_gemm_args *args, bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * bs_grouped_gemm -- FP4 GEMM grouped over E experts in one persistent
+ * launch ("DeepGEMM teardown", section 1.2 grouped/segmented GEMM and 5.3
+ * group offsets; "DeepGEMM for Hopper MoE", section 3 fused expert compute).
+ *
+ * Rows of A are grouped by expert: expert e owns rows
+ * [offsets[e], offsets[e] + counts[e]); every offsets[e] is a multiple of 128
+ * and offsets[e+1] >= offsets[e] + counts[e] (bs_moe_dispatch writes such
+ * tables).  Expert weights are stacked: B rows [e*Nw, (e+1)*Nw) belong to
+ * expert e, with their scales in one bs_sf_bytes(E*Nw, K) tensor; Nw % 128 == 0.
+ *
+ *   args->a/sfa     A codes / scales for all rows (rows = args->M, the size
+ *                   of the grouped buffers, >= offsets[E])
+ *   args->b/sfb     stacked expert weights, Nw = 2N (SWIGLU) or N (others)
+ *   args->N         output columns per row
+ *   offsets, counts device int32 [E+1] / [E]
+ *   epilogue        BS_EPI_STORE:   out[r, n] = y (rows r < offsets[e]+counts[e])
+ *                   BS_EPI_SWIGLU:  weights rows [0, N) of an expert are the
+ *                                   gate, rows [N, 2N) the up projection;
+ *                                   out bf16 [M, N] = bf16(silu(g) * u), padding
+ *                                   rows of each segment are written as 0
+ *                   BS_EPI_COMBINE: out32[token_of[r], n] += weight_of[r] * y[r, n]
+ *                                   (fp32 reductions; out32 [*, ld_out32] must
+ *                                   be zeroed by the caller or bs_moe_finalize)
+ *   token_of, weight_of  int32 / fp32 [M] (COMBINE only)
+ * Only alpha = 1, no col_scale, no lora and no bias are accepted here.
+ * Offsets that break the contract set BS_ERR_OFFSETS in the device status and
+ * the kernel writes nothing.
+ * ------------------------------------------------------------------------- */
+bs_status bs_grouped_gemm(const bs_gemm_args *args, int E, const int32_t *offsets,
+                          const int32_t *counts, int epilogue, const int32_t *token_of,
+                          const float *weight_of, float *out32, int64_t ld_out32,
+                          bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * bs_moe_dispatch -- group the T*k (token, slot) pairs of a top-k routing by
+ * expert ("DeepGEMM teardown", section 5.3: each expert's rows contiguous and
+ * movable in whole blocks).  Rows of expert e, in increasing pair index
+ * p = t*k + slot, occupy [offsets[e], offsets[e] + counts[e]); offsets[e] is
+ * the running sum of counts rounded up to 128.  Unused rows up to
+ * bs_moe_rows_bound() get pair -1, token -1 and weight 0.
+ *
+ *   topk_ids   int32 [T, k], values in [0, E); topk_w fp32 [T, k]
+ *   counts     int32 [E];  offsets int32 [E+1]
+ *   pair_of_row, token_of int32 [rows_bound]; weight_of fp32 [rows_bound]
+ *   workspace  bs_moe_dispatch_workspace_bytes(T, k, E) bytes of device scratch
+ * Out-of-range expert ids set BS_ERR_OFFSETS in the device status.
+ * ------------------------------------------------------------------------- */
+int64_t bs_moe_rows_bound(int64_t T, int k, int E);
+size_t bs_moe_dispatch_workspace_bytes(int64_t T, int k, int E);
+bs_status bs_moe_dispatch(const int32_t *topk_ids, const float *topk_w, int64_t T, int k,
+                          int E, int32_t *counts, int32_t *offsets, int32_t *pair_of_row,
+                          int32_t *token_of, float *weight_of, void *workspace,
+                          size_t workspace_bytes, bs_stream_t stream);
+
+/* bs_moe_finalize -- out[i] = bf16(out32[i]) for n elements, then out32[i] = 0
+ * so the accumulator is ready for the next layer call ("DeepGEMM for Hopper
+ * MoE", section 3: FP16-class output of the weighted sum). */
+bs_status bs_moe_finalize(float *out32, void *out_bf16, int64_t n, bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Status.
+ * ------------------------------------------------------------------------- */
+/* Reads (synchronously) and returns the sticky device status word of the
+ * current device: BS_OK, BS_ERR_TIMEOUT or BS_ERR_OFFSETS.  *detail (if not
+ * NULL) receives the raw word (error code in the low byte, site id above). */
+bs_status bs_get_device_status(int *detail);
+/* Resets the device status word of the current device to BS_OK (synchronous). */
+bs_status bs_clear_device_status(void);
+/* Static description of a status code. */
+const char *bs_status_string(bs_status s);
+/* Last host-side error message of this thread (after a non-OK return). */
+const char *bs_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSGEMM_H */

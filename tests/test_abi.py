@@ -1,0 +1,116 @@
+"""The C-ABI library loads, exports every symbol include/bsgemm.h declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bsgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import fp8_quantized_gemm_q4_gb300 as bs
+    return bs.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return")))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("q4_quantize", "q8_quantize", "bs_gemm", "bs_grouped_gemm", "bs_moe_dispatch",
+              "bs_moe_finalize", "bs_sf_bytes", "bs_sf_offset", "bs_get_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_sf_layout_helpers(lib):
+    import fp8_quantized_gemm_q4_gb300 as bs
+    assert bs.sf_bytes(128, 64) == 512
+    assert bs.sf_bytes(1, 64) == 512          # rows pad to 128
+    assert bs.sf_bytes(129, 128) == 2 * 128 * 8
+    # tile (rb, kc) = rb * (K/64) + kc; inside: (r % 32) * 16 + (r / 32) * 4 + j
+    K = 256
+    assert bs.sf_offset(0, 0, K) == 0
+    assert bs.sf_offset(0, 3, K) == 3
+    assert bs.sf_offset(0, 4, K) == 512
+    assert bs.sf_offset(1, 0, K) == 16
+    assert bs.sf_offset(32, 0, K) == 4
+    assert bs.sf_offset(127, 15, K) == 3 * 512 + 31 * 16 + 3 * 4 + 3
+    assert bs.sf_offset(128, 0, K) == 4 * 512
+    # the map is a bijection onto [0, sf_bytes)
+    rows = 256
+    offs = {bs.sf_offset(r, g, K) for r in range(rows) for g in range(K // 16)}
+    assert offs == set(range(bs.sf_bytes(rows, K)))
+
+
+def test_host_validation_rejects_before_launch(lib):
+    import fp8_quantized_gemm_q4_gb300 as bs
+    P = ctypes.c_void_p
+    fake = P(1 << 20)        # never dereferenced: validation fails first
+    # K not a multiple of 64
+    assert lib.q4_quantize(fake, 1, 4, 100, 100, None, fake, fake, None, 0, None, None) == bs.BS_ERR_ALIGN
+    # null output
+    assert lib.q4_quantize(fake, 1, 4, 64, 64, None, None, fake, None, 0, None, None) == bs.BS_ERR_INVALID
+    # bad dtype
+    assert lib.q4_quantize(fake, 7, 4, 64, 64, None, fake, fake, None, 0, None, None) == bs.BS_ERR_INVALID
+    # misaligned input pointer
+    assert lib.q4_quantize(P((1 << 20) + 2), 1, 4, 64, 64, None, fake, fake, None, 0, None, None) == bs.BS_ERR_ALIGN
+    # low-rank with the wrong rank
+    assert lib.q4_quantize(fake, 1, 4, 64, 64, None, fake, fake, fake, 16, fake, None) == bs.BS_ERR_INVALID
+    # M == 0 is a no-op
+    assert lib.q4_quantize(None, 1, 0, 64, 64, None, None, None, None, 0, None, None) == bs.BS_OK
+    # q8: K % 128
+    assert lib.q8_quantize(fake, 1, 4, 64, 64, 1, fake, fake, None) == bs.BS_ERR_ALIGN
+    assert lib.q8_quantize(fake, 1, 4, 128, 128, 3, fake, fake, None) == bs.BS_ERR_INVALID
+    g = bs.GemmArgs()
+    g.fmt, g.a, g.sfa, g.b, g.sfb, g.out = 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20
+    g.M, g.N, g.K, g.alpha, g.ldo, g.out_dtype = 64, 100, 128, 1.0, 128, 1
+    assert lib.bs_gemm(ctypes.byref(g), None) == bs.BS_ERR_ALIGN      # N % 128
+    g.N = 128
+    g.out = None
+    assert lib.bs_gemm(ctypes.byref(g), None) == bs.BS_ERR_INVALID    # null out
+    g.out = 1 << 20
+    g.ldo = 100
+    assert lib.bs_gemm(ctypes.byref(g), None) == bs.BS_ERR_ALIGN      # ldo
+    g.ldo = 128
+    g.fmt = 9
+    assert lib.bs_gemm(ctypes.byref(g), None) in (bs.BS_ERR_INVALID, bs.BS_ERR_CUDA)
+    g.fmt = 0
+    # grouped: E out of range, bad epilogue
+    assert lib.bs_grouped_gemm(ctypes.byref(g), 0, fake, fake, 0, None, None, None, 0, None) == bs.BS_ERR_INVALID
+    assert lib.bs_grouped_gemm(ctypes.byref(g), 4, fake, fake, 7, None, None, None, 0, None) == bs.BS_ERR_INVALID
+    # COMBINE without routing tables
+    assert lib.bs_grouped_gemm(ctypes.byref(g), 4, fake, fake, 2, None, None, None, 0, None) == bs.BS_ERR_INVALID
+    # dispatch: workspace too small / bad E
+    assert lib.bs_moe_dispatch(fake, fake, 8, 2, 2, fake, fake, fake, fake, fake, fake, 1, None) == bs.BS_ERR_INVALID
+    assert lib.bs_moe_dispatch(fake, fake, 8, 2, 0, fake, fake, fake, fake, fake, fake, 1 << 20, None) == bs.BS_ERR_INVALID
+    assert lib.bs_moe_rows_bound(8, 2, 2) == 16 + 2 * 127
+    assert lib.bs_moe_finalize(P((1 << 20) + 4), fake, 8, None) == bs.BS_ERR_ALIGN
+    assert lib.bs_status_string(5) == b"device pipeline wait timed out"
+    assert b"K=100" in lib.bs_last_error() or lib.bs_last_error() != b""
+
+
+def test_product_path_has_no_oracle_or_cpu_fallback():
+    pkg = os.path.join(ROOT, "fp8_quantized_gemm_q4_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".hpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "liboracle" not in src, f

@@ -1,0 +1,141 @@
+"""Grouped FP4 MoE path on the GPU vs the FP64 oracle.
+
+Dispatch is integer work: bit-exact.  The grouped GEMMs are checked in
+stages, because re-quantizing a slightly different h may legitimately flip a
+code: (1) h against the oracle's SwiGLU of the oracle GEMMs on the GPU's own
+activation codes; (2) the GPU's re-quantized h bit-exact against the oracle
+re-quantizing the GPU's h; (3) the combined output against the oracle fed
+with the GPU's quantized h.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.conftest import read_golden
+from tests.helpers import gemm_errors, sf_rowmajor
+
+pytestmark = pytest.mark.gpu
+
+
+def test_dispatch_hand_case(cuda_lib):
+    bs = cuda_lib
+    gold = {r[0]: [int(v) for v in r[1:]] for r in read_golden("moe_dispatch_2x8.txt")}
+    ids = torch.tensor([[t % 2, 1 - t % 2] for t in range(8)], dtype=torch.int32)
+    w = torch.full((8, 2), 0.5)
+    d = bs.moe_dispatch(ids.cuda(), w.cuda(), E=2)
+    torch.cuda.synchronize()
+    assert d["counts"].tolist() == gold["counts"]
+    assert d["offsets"].tolist() == gold["offsets"]
+    por = d["pair_of_row"].cpu()
+    assert por[0:8].tolist() == gold["expert0_pairs"] and por[128:136].tolist() == gold["expert1_pairs"]
+    assert (por[8:128] == -1).all() and (por[136:] == -1).all()
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 4, 2), (300, 9, 4), (4096, 64, 8), (16384, 256, 8)])
+def test_dispatch_bit_exact(cuda_lib, T, E, k):
+    bs = cuda_lib
+    r = workloads.moe_routing(T, E, k)
+    ids, w = torch.from_numpy(r["topk_ids"]), torch.from_numpy(r["topk_w"])
+    d = bs.moe_dispatch(ids.cuda(), w.cuda(), E=E)
+    torch.cuda.synchronize()
+    counts, offsets, por = oracle.moe_dispatch(r["topk_ids"], E)
+    assert np.array_equal(d["counts"].cpu().numpy(), counts)
+    assert np.array_equal(d["offsets"].cpu().numpy(), offsets)
+    gp = d["pair_of_row"].cpu().numpy()
+    assert np.array_equal(gp[:offsets[E]], por)
+    assert np.all(gp[offsets[E]:] == -1)
+    tok = d["token_of"].cpu().numpy()
+    wt = d["weight_of"].cpu().numpy()
+    real = gp >= 0
+    assert np.array_equal(tok[real], gp[real] // k) and np.all(tok[~real] == -1)
+    assert np.array_equal(wt[real], r["topk_w"].reshape(-1)[gp[real]]) and np.all(wt[~real] == 0)
+    assert bs.device_status()[0] == 0
+
+
+def _small_moe(T=200, H=256, F=128, E=5, k=2, seed=3):
+    r = workloads.moe_routing(T, E, k, index=seed)
+    x = workloads.moe_activations(T, H, index=seed)
+    ws = [workloads.moe_expert_weights(e, F, H, index=seed) for e in range(E)]
+    return r, x, ws
+
+
+@pytest.mark.parametrize("T,H,F,E,k", [(200, 256, 128, 5, 2), (1000, 512, 256, 8, 4), (64, 256, 128, 16, 8)])
+def test_grouped_layer_staged(cuda_lib, T, H, F, E, k):
+    bs = cuda_lib
+    from fp8_quantized_gemm_q4_gb300.moe import MoELayer, quantize_expert_weights
+    r, x, ws = _small_moe(T, H, F, E, k)
+    W = quantize_expert_weights([a for a, _ in ws], [b for _, b in ws])
+    layer = MoELayer(W, T, k)
+    out = layer.forward(x.cuda(), torch.from_numpy(r["topk_ids"]).cuda(), torch.from_numpy(r["topk_w"]).cuda())
+    torch.cuda.synchronize()
+    assert bs.device_status()[0] == 0
+    counts, offsets, por = oracle.moe_dispatch(r["topk_ids"], E)
+    rows = offsets[E]
+    # activation codes of the routed rows
+    xq = layer.xq.cpu().numpy()[:rows]
+    real = por >= 0
+    oa, osa = oracle.q4_quantize(x[por[real] // k])
+    assert np.array_equal(xq[real], oa)
+    assert np.array_equal(sf_rowmajor(layer.xs.cpu().numpy(), rows, H)[real], osa)
+    # stage 1: h from the oracle GEMMs on the GPU codes
+    h = layer.h.float().cpu().numpy()[:rows]
+    assert np.all(h[~real] == 0)
+    wgu = [oracle.q4_quantize(a) for a, _ in ws]
+    wd = [oracle.q4_quantize(b) for _, b in ws]
+    for e in range(E):
+        seg = np.arange(offsets[e], offsets[e] + counts[e])
+        if len(seg) == 0:
+            continue
+        gu, s_gu = oracle.gemm_fp4(xq[seg], sf_rowmajor(layer.xs.cpu().numpy(), rows, H)[seg], wgu[e][0], wgu[e][1], H)
+        g, u = gu[:, :F], gu[:, F:]
+        h_ref = oracle.swiglu(g, u)
+        # error of silu(g) u from |g - g_ref| <= 1e-3 S_g and |u - u_ref| <= 1e-3 S_u, plus bf16 rounding
+        sig = 1.0 / (1.0 + np.exp(-g))
+        dsilu = np.abs(sig * (1 + g * (1 - sig)))
+        bound = 1e-3 * (dsilu * np.abs(u) * s_gu[:, :F] + np.abs(g * sig) * s_gu[:, F:]) + 2.0 ** -8 * np.abs(h_ref)
+        assert np.all(np.abs(h[seg] - h_ref) <= bound + 1e-30), e
+    # stage 2: re-quantized h bit-exact against the oracle on the GPU's h
+    hq = layer.hq.cpu().numpy()[:rows]
+    ohq, ohs = oracle.q4_quantize(layer.h[:rows].cpu())
+    assert np.array_equal(hq, ohq)
+    assert np.array_equal(sf_rowmajor(layer.hs.cpu().numpy(), rows, F), ohs)
+    # stage 3: combine against the oracle down GEMM on the GPU's quantized h
+    ref = np.zeros((T, H))
+    S = np.zeros((T, H))
+    wflat = r["topk_w"].reshape(-1).astype(np.float64)
+    for e in range(E):
+        seg = np.arange(offsets[e], offsets[e] + counts[e])
+        if len(seg) == 0:
+            continue
+        y, sy = oracle.gemm_fp4(hq[seg], ohs[seg], wd[e][0], wd[e][1], F)
+        pairs = por[seg]
+        np.add.at(ref, pairs // k, wflat[pairs][:, None] * y)
+        np.add.at(S, pairs // k, np.abs(wflat[pairs][:, None]) * sy)
+    ok, ratio, rel = gemm_errors(out.float().cpu().numpy(), ref, S, True)
+    assert ok, (ratio, rel)
+    # out32 was reset by the finalize step
+    assert float(layer.out32.abs().max()) == 0.0
+
+
+def test_layer_end_to_end_report(cuda_lib):
+    """End to end against the oracle's own layer (its own h and re-quantization):
+    looser, reported, with a bound that allows re-quantization flips."""
+    bs = cuda_lib
+    from fp8_quantized_gemm_q4_gb300.moe import MoELayer, quantize_expert_weights
+    T, H, F, E, k = 64, 256, 128, 4, 2
+    r, x, ws = _small_moe(T, H, F, E, k)
+    W = quantize_expert_weights([a for a, _ in ws], [b for _, b in ws])
+    out = MoELayer(W, T, k).forward(x.cuda(), torch.from_numpy(r["topk_ids"]).cuda(),
+                                    torch.from_numpy(r["topk_w"]).cuda())
+    torch.cuda.synchronize()
+    wgu = [oracle.q4_quantize(a) for a, _ in ws]
+    wd = [oracle.q4_quantize(b) for _, b in ws]
+    ref = oracle.moe_layer(x, r["topk_ids"], r["topk_w"], [c for c, _ in wgu], [s for _, s in wgu],
+                           [c for c, _ in wd], [s for _, s in wd], F=F)["out"]
+    o = out.float().cpu().numpy()
+    rel = np.abs(o - ref).max() / np.abs(ref).max()
+    print(f"end-to-end MoE max |err| / max |ref| = {rel:.3g}")
+    assert rel < 0.05
+    assert bs.device_status()[0] == 0

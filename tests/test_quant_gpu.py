@@ -1,0 +1,117 @@
+"""GPU quantizers vs the FP64 oracle: codes and scales bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.helpers import sf_rowmajor
+
+pytestmark = pytest.mark.gpu
+
+
+def special_rows(x):
+    """Plant edge cases: zero group, tiny (subnormal / zero scale), huge (saturated
+    scale), exact grid points, negative values rounding to -0, ties."""
+    x = x.clone()
+    M, K = x.shape
+    if M > 0:
+        x[0, :16] = 0
+    if M > 1:
+        x[1, :] *= 1e-4
+    if M > 2:
+        x[2, :] *= 3000.0
+    if M > 3:
+        x[3, :16] = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0] * 2) * 0.171875 * (6.0 / 6.0)
+    if M > 4:
+        x[4, :] = -x[4, :].abs() * 1e-3
+    if M > 5:
+        x[5, 16:32] = 1e-12
+    return x
+
+
+@pytest.mark.parametrize("M,K,dtype", [(1, 64, torch.float32), (3, 128, torch.float32),
+                                       (128, 512, torch.float32), (300, 320, torch.float32),
+                                       (257, 1024, torch.bfloat16), (64, 8192, torch.bfloat16)])
+def test_q4_quantize_bit_exact(cuda_lib, M, K, dtype):
+    bs = cuda_lib
+    g = torch.Generator().manual_seed(M * 7 + K)
+    x = special_rows(torch.randn(M, K, generator=g)).to(dtype)
+    codes, sf, _ = bs.q4_quantize(x.cuda())
+    torch.cuda.synchronize()
+    oc, os_ = oracle.q4_quantize(x)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    sfn = sf.cpu().numpy()
+    assert np.array_equal(sf_rowmajor(sfn, M, K), os_)
+    # padding rows of the last 128-row block carry zero scales
+    Mpad = (M + 127) // 128 * 128
+    if Mpad > M:
+        pad = sf_rowmajor(sfn, Mpad, K)[M:]
+        assert np.all(pad == 0)
+
+
+def test_q4_quantize_gather(cuda_lib):
+    bs = cuda_lib
+    x = torch.randn(50, 256).to(torch.bfloat16)
+    gather = torch.tensor([3, -1, 49, 0, 3, 17, -1, 8], dtype=torch.int32)
+    codes, sf, _ = bs.q4_quantize(x.cuda(), gather=gather.cuda())
+    rows = torch.stack([x[i] if i >= 0 else torch.zeros(256, dtype=x.dtype) for i in gather.tolist()])
+    oc, os_ = oracle.q4_quantize(rows)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), 8, 256), os_)
+
+
+def test_q4_quantize_full_size_activation(cuda_lib):
+    """The 8192 x 8192 bf16 activation of the dense low-rank workload, every row."""
+    bs = cuda_lib
+    x = workloads.dense_lowrank(lowrank=False, bias=False)["x"]
+    codes, sf, _ = bs.q4_quantize(x.cuda())
+    torch.cuda.synchronize()
+    rows = np.r_[0:64, 4000:4064, 8128:8192]
+    oc, os_ = oracle.q4_quantize(x[rows])
+    assert np.array_equal(codes.cpu().numpy()[rows], oc)
+    assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), 8192, 8192)[rows], os_)
+
+
+def test_q4_lowrank_left_factor(cuda_lib):
+    bs = cuda_lib
+    d = workloads.dense_lowrank(M=200, N=256, K=1024)
+    x, a = d["x"], d["lora_a"]
+    _, _, lt = bs.q4_quantize(x.cuda(), lora_a_t=a.t().contiguous().cuda())
+    torch.cuda.synchronize()
+    t = lt.float().cpu().numpy().astype(np.float64)
+    t_gpu = t[:, :32] + t[:, 32:]
+    t_ref = oracle.lowrank_t(x, a)
+    mag = np.abs(x.float().numpy().astype(np.float64)) @ np.abs(a.float().numpy().astype(np.float64))
+    assert np.all(np.abs(t_gpu - t_ref) <= 1e-5 * mag + 2.0 ** -16 * np.abs(t_ref))
+    assert np.all(t[:, 32:] == (t_gpu - t[:, :32]))  # lo is the bf16 remainder
+
+
+@pytest.mark.parametrize("M,K,dtype", [(1, 4096, torch.bfloat16), (16, 4096, torch.bfloat16),
+                                       (130, 256, torch.float32), (4096, 4096, torch.bfloat16)])
+def test_q8_token_bit_exact(cuda_lib, M, K, dtype):
+    bs = cuda_lib
+    if K == 4096:
+        x = workloads.fp8_sweep(M)["x"]
+    else:
+        x = special_rows(torch.randn(M, K)).to(dtype)
+    codes, scales = bs.q8_quantize(x.cuda(), mode=bs.Q8_TOKEN)
+    torch.cuda.synchronize()
+    rows = np.arange(M) if M <= 256 else np.r_[0:128, M - 128:M]
+    oc, os_ = oracle.q8_quantize(x[rows], rows_per_block=1)
+    assert np.array_equal(codes.cpu().numpy()[rows], oc)
+    assert np.array_equal(scales.cpu().numpy().T[rows], os_)   # [K/128, M] layout
+
+
+@pytest.mark.parametrize("N,K", [(200, 384), (7168, 4096)])
+def test_q8_block_bit_exact(cuda_lib, N, K):
+    bs = cuda_lib
+    if N == 7168:
+        w = workloads.fp8_sweep(1)["w"]
+    else:
+        w = (torch.randn(N, K) * 0.02).to(torch.bfloat16)
+    codes, scales = bs.q8_quantize(w.cuda(), mode=bs.Q8_BLOCK)
+    torch.cuda.synchronize()
+    oc, os_ = oracle.q8_quantize(w, rows_per_block=128)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(scales.cpu().numpy(), os_)
