@@ -1,0 +1,391 @@
+"""Benchmark of the block-scaled GEMM hot path on GB300.
+
+Default workload: dense W4A4 with low-rank branch, M = N = K = 8192, bf16 X and
+W ~ N(0,1), A[K,32] and B[32,N] ~ N(0,0.02), bias ~ N(0,0.1), bf16 output.
+One step = q4_quantize(X) (codes, scales and the low-rank left factor T = XA)
+followed by the block-scaled FP4 GEMM with the low-rank branch and bias; the
+weights are quantized once, before timing (they are offline in the method).
+Metric: TFLOPS = 2*M*N*K / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dense_lowrank|dense_tiny|fp8_m1|fp8_m16|fp8_m64|fp8_m128|fp8_m4096|moe_small|moe_large]
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+step (the path has no exchange step): value = total work / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # dense tensor peaks, profiling recipe table
+NOMINAL_FP8_OVER_BF16 = 4.5 / 2.25
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+class DenseLowRank:
+    """Dense W4A4 + low-rank + bias (default), or the tiny fp32 dense case."""
+
+    def __init__(self, tiny=False):
+        self.tiny = tiny
+        if tiny:
+            self.M, self.N, self.K = 128, 256, 512
+            self.name = "dense_w4a4_tiny_128x256x512"
+        else:
+            self.M = self.N = self.K = 8192
+            self.name = "dense_w4a4_lowrank_8192x8192x8192_r32_bias_bf16out"
+        self.flops = 2.0 * self.M * self.N * self.K
+        self.metric = "block-scaled FP4 GEMM TFLOPS (dense W4A4, low-rank branch, bias)"
+        self.unit = "TFLOPS"
+        self.higher_is_better = True
+        self.dtype = "e2m1 x e2m1 (e4m3 group-16 scales), fp32 accumulate, bf16 out"
+
+    def host_inputs(self):
+        import workloads
+        if self.tiny:
+            return workloads.dense_tiny()
+        return workloads.dense_lowrank()
+
+    # --- GPU arm
+    def setup(self, dev):
+        import torch
+        import fp8_quantized_gemm_q4_gb300 as bs
+        d = self.host_inputs()
+        self.h = d
+        self.x = d["x"].to(dev)
+        w = d["w"].to(dev)
+        self.wq, self.ws, _ = bs.q4_quantize(w)
+        del w
+        M, N, K = self.M, self.N, self.K
+        self.xq = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+        self.xs = torch.empty(bs.sf_bytes(M, K), dtype=torch.uint8, device=dev)
+        if not self.tiny:
+            self.at = d["lora_a"].t().contiguous().to(dev)
+            self.bt = d["lora_b"].t().contiguous().to(dev)
+            self.bias = d["bias"].to(dev)
+            self.lt = torch.empty((M, 64), dtype=torch.bfloat16, device=dev)
+            self.out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        else:
+            self.at = self.bt = self.bias = self.lt = None
+            self.out = torch.empty((M, N), dtype=torch.float32, device=dev)
+        self.launches_per_step = 2 + (0 if self.tiny else 1)
+        self.bytes_in = self.x.numel() * self.x.element_size()
+        self.bytes_out = self.out.numel() * self.out.element_size()
+
+    def step(self, x=None, gemm_events=None):
+        import fp8_quantized_gemm_q4_gb300 as bs
+        x = self.x if x is None else x
+        bs.q4_quantize(x, lora_a_t=self.at, out=(self.xq, self.xs, self.lt))
+        if gemm_events:
+            gemm_events[0].record()
+        bs.gemm_fp4(self.xq, self.xs, self.wq, self.ws, self.K, lora_t=self.lt, lora_b_t=self.bt, bias=self.bias,
+                    out=self.out)
+        if gemm_events:
+            gemm_events[1].record()
+        return self.out
+
+    def roofline(self, gemm_ms, peaks, source):
+        tflops = self.flops / (gemm_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+        return {"bound": "tensor", "kernel": "fp4_gemm_kernel", "achieved": round(tflops, 1),
+                "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                "peak_source": f"{source} bf16 burst x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/bf16)",
+                "algorithmic_flops_per_launch": self.flops, "kernel_ms": round(gemm_ms, 5)}
+
+    # --- CPU oracle arm
+    def oracle_sample(self, rows, cols, nthreads):
+        """Quantize `rows` rows of X (+ low-rank factor) and compute their GEMM
+        against the first `cols` weight rows with the FP64 oracle."""
+        import oracle
+        h = self.h
+        if not hasattr(self, "_ow"):
+            self._ow = {}
+        key = cols
+        if key not in self._ow:
+            self._ow[key] = oracle.q4_quantize(h["w"][:cols])
+        ob, osb = self._ow[key]
+        x = h["x"][:rows]
+        t0 = time.perf_counter()
+        oa, osa = oracle.q4_quantize(x)
+        t = None if self.tiny else oracle.lowrank_t(x, h["lora_a"])
+        oracle.gemm_fp4(oa, osa, ob, osb, self.K, t=t, lora_b=None if self.tiny else h["lora_b"][:, :cols],
+                        bias=None if self.tiny else h["bias"][:cols], nthreads=nthreads)
+        return time.perf_counter() - t0, 2.0 * rows * cols * self.K
+
+
+WORKLOADS = {
+    "dense_lowrank": lambda: DenseLowRank(tiny=False),
+    "dense_tiny": lambda: DenseLowRank(tiny=True),
+}
+
+
+def traffic_for(kernel_src: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    src = os.path.join(ROOT, kernel_src)
+    h = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    ent = d.get(kernel_src)
+    if ent and ent.get("source_sha1") == h:
+        return ent.get("dram_bytes_per_launch")
+    return None
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, wl, rank, world, dev, peaks, source):
+    import torch
+    import torch.distributed as dist
+    wl.setup(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        wl.step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[torch.cuda.current_device()]))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(float(i))          # L2 flush, outside the per-step events
+        ev[i][0].record(stream)
+        wl.step(gemm_events=gev[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    gemm_ms = sum(a.elapsed_time(b) for a, b in gev) / K
+    if world > 1:
+        t = torch.tensor([step_ms, gemm_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, gemm_ms = float(t[0]), float(t[1])
+
+    # end to end through the public API with pinned host buffers
+    xh = wl.x.cpu().pin_memory()
+    yh = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+    xd = torch.empty_like(wl.x)
+    Ke = args.e2e_steps if args.e2e_steps > 0 else max(1, min(K, 100))
+    for _ in range(3):
+        xd.copy_(xh, non_blocking=True)
+        yh.copy_(wl.step(xd), non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        xd.copy_(xh, non_blocking=True)
+        yh.copy_(wl.step(xd), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    import fp8_quantized_gemm_q4_gb300 as bs
+    st, detail = bs.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
+    value = world * wl.flops / (step_ms * 1e-3) / 1e12
+    roof = wl.roofline(gemm_ms, peaks, source)
+    roof["traffic"] = traffic_for("fp8_quantized_gemm_q4_gb300/csrc/gemm_fp4.cu")
+    line = {
+        "metric": wl.metric, "value": round(value, 2), "unit": wl.unit, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": wl.higher_is_better,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, pages' shapes)",
+        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(world * wl.flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": wl.unit,
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": wl.bytes_in,
+                "d2h_bytes_per_step": wl.bytes_out},
+        "gpu_launches": K * wl.launches_per_step,
+        "roofline": roof,
+        "clocks": clk,
+        "timed_wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    return line
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    """The FP64 oracle timed on the host cores on a bounded sample of rows
+    (threads split rows, so the sample is a multiple of the thread count)."""
+    import oracle
+    oracle.build()
+    nthreads = oracle.default_threads()
+    cols = wl.N
+    dt1, _ = wl.oracle_sample(1, cols, 1)                  # calibration: one row, one thread
+    rows = min(wl.M, max(1, int(budget_s / max(dt1, 1e-6))) * nthreads)
+    dt, fl = wl.oracle_sample(rows, cols, nthreads)
+    return {"value": round(fl / dt / 1e12, 8), "unit": wl.unit, "cores": min(nthreads, rows), "kind": "oracle",
+            "sample": f"{rows} rows x {cols} cols x K={wl.K} (quantize + low-rank + GEMM), {dt:.1f} s",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args, wl):
+    """The oracle as the reference arm: each step one bounded sample of the
+    workload (one row per host thread against a slice of the columns)."""
+    import oracle
+    oracle.build()
+    wl.h = wl.host_inputs()
+    nthreads = oracle.default_threads()
+    rows = min(wl.M, nthreads)
+    dt1, _ = wl.oracle_sample(1, wl.N, 1)                  # one row, one thread, all columns
+    total_steps = args.steps + args.warmup
+    per_step = max(0.01, 90.0 / max(total_steps, 1))
+    cols = max(128, min(wl.N, int(wl.N * per_step / max(dt1, 1e-6)) // 128 * 128))
+    for _ in range(args.warmup):
+        wl.oracle_sample(rows, cols, nthreads)
+    tot_t = tot_f = 0.0
+    for _ in range(args.steps):
+        t, f = wl.oracle_sample(rows, cols, nthreads)
+        tot_t += t
+        tot_f += f
+    value = tot_f / tot_t / 1e12
+    sample = f"{rows} rows x {cols} cols x K={wl.K} per step (quantize + low-rank + GEMM)"
+    return {
+        "impl": "reference", "metric": wl.metric, "value": round(value, 8), "unit": wl.unit, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+        "higher_is_better": wl.higher_is_better, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (oracle)", "data": "synthetic (seeded, pages' shapes)",
+        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 8), "unit": wl.unit, "cores": rows, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 8), "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dense_lowrank", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (default min(steps, 100))")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    wl = WORKLOADS[args.workload]()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, wl)), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    peaks, source = load_peaks()
+    line = run_ours(args, wl, rank, world, dev, peaks, source)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -189,6 +189,7 @@ static bs_status check_common(const bs_gemm_args* a, bool grouped) {
                                                     (long long)a->M, (long long)a->N, (long long)a->K);
   if (a->M > (1LL << 30) || a->N > (1LL << 30) || a->K > (1LL << 30)) return fail(BS_ERR_INVALID, "sizes too large");
   if (a->N % 128) return fail(BS_ERR_ALIGN, "N=%lld not a multiple of 128", (long long)a->N);
+  if (a->M == 0) return BS_OK;  // nothing to compute; operands may be empty (null)
   if (!a->a || !a->b || !a->sfa || !a->sfb) return fail(BS_ERR_INVALID, "null operand");
   if (!aligned16(a->a) || !aligned16(a->b) || !aligned16(a->sfa) || !aligned16(a->sfb))
     return fail(BS_ERR_ALIGN, "operands must be 16-byte aligned");
