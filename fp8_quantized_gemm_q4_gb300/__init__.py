@@ -81,6 +81,8 @@ def load(path: str | None = None):
         lib.bs_moe_dispatch_workspace_bytes.argtypes = [I64, I, I]
         lib.bs_moe_dispatch.restype = I
         lib.bs_moe_dispatch.argtypes = [P, P, I64, I, I, P, P, P, P, P, P, SZ, P]
+        lib.bs_moe_dispatch_noalloc.restype = I
+        lib.bs_moe_dispatch_noalloc.argtypes = [P, P, I64, I, I, P, P, P, P, P, P]
         lib.bs_moe_finalize.restype = I
         lib.bs_moe_finalize.argtypes = [P, P, I64, P]
         lib.bs_get_device_status.restype = I

@@ -12,6 +12,9 @@
 #include "bsgemm.h"
 #include "kernels.h"
 
+static_assert(BS_MOE_DISPATCH_NOALLOC_MAX_BYTES == bsk::kNoAllocDispatchScratchBytes,
+              "header limit and static scratch size must agree");
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -356,6 +359,28 @@ bs_status bs_moe_dispatch(const int32_t* topk_ids, const float* topk_w, int64_t 
                                            weight_of, static_cast<int*>(workspace), bs_moe_rows_bound(T, k, E),
                                            status, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
+  return BS_OK;
+}
+
+bs_status bs_moe_dispatch_noalloc(const int32_t* topk_ids, const float* topk_w, int64_t T, int k, int E,
+                                  int32_t* counts, int32_t* offsets, int32_t* pair_of_row, int32_t* token_of,
+                                  float* weight_of, bs_stream_t stream) {
+  if (T < 0 || k <= 0 || E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "dispatch: T=%lld k=%d E=%d", (long long)T, k, E);
+  if (T * k > (1LL << 30)) return fail(BS_ERR_INVALID, "dispatch: too many pairs");
+  const size_t need = bs_moe_dispatch_workspace_bytes(T, k, E);
+  if (need > BS_MOE_DISPATCH_NOALLOC_MAX_BYTES)
+    return fail(BS_ERR_INVALID,
+                "dispatch_noalloc: T*k=%lld pairs with E=%d need %zu bytes of scratch, above the %u-byte static "
+                "array; use bs_moe_dispatch with a caller workspace",
+                (long long)(T * k), E, need, (unsigned)BS_MOE_DISPATCH_NOALLOC_MAX_BYTES);
+  if (!counts || !offsets || !pair_of_row || !token_of || !weight_of || (T > 0 && (!topk_ids || !topk_w)))
+    return fail(BS_ERR_INVALID, "dispatch: null pointer");
+  int* status = nullptr;
+  if (!device_info(&status, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_moe_dispatch_noalloc(topk_ids, topk_w, T, k, E, counts, offsets, pair_of_row, token_of,
+                                                   weight_of, bs_moe_rows_bound(T, k, E), status,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch_noalloc");
   return BS_OK;
 }
 

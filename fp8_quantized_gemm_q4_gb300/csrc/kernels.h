@@ -78,4 +78,10 @@ cudaError_t launch_moe_dispatch(const int* topk_ids, const float* topk_w, long l
                                 int* work, long long rows_bound, int* status, cudaStream_t stream);
 cudaError_t launch_moe_finalize(float* out32, void* out_bf16, long long n, cudaStream_t stream);
 
+// Grouping whose histogram scratch is the library's static device array.
+constexpr size_t kNoAllocDispatchScratchBytes = size_t(1) << 20;
+cudaError_t launch_moe_dispatch_noalloc(const int* topk_ids, const float* topk_w, long long T, int k, int E,
+                                        int* counts, int* offsets, int* pair_of_row, int* token_of,
+                                        float* weight_of, long long rows_bound, int* status, cudaStream_t stream);
+
 }  // namespace bsk

@@ -11,6 +11,8 @@
 //              inside each 32-pair round come from __match_any_sync, so the
 //              result is identical to a sequential stable sort; padding rows
 //              get pair/token -1 and weight 0
+#include <mutex>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -175,6 +177,57 @@ cudaError_t launch_moe_finalize(float* out32, void* out_bf16, long long n, cudaS
   if (blocks < 1) blocks = 1;
   moe_finalize_kernel<<<(unsigned)blocks, 256, 0, stream>>>(out32, reinterpret_cast<__nv_bfloat16*>(out_bf16), n);
   return cudaGetLastError();
+}
+
+}  // namespace bsk
+
+namespace bsk {
+
+// ---------------------------------------------------------------------------
+// Grouping with library-owned scratch, for callers that cannot allocate.
+//
+// The histogram / stable-base table of the grouping lives in this fixed
+// device array instead of a caller-provided workspace.  Every GPU that loads
+// the library keeps the array until the process exits.  All calls share it
+// and it keeps whatever the last call left there; the count step overwrites
+// every entry the later steps read, so nothing has to be cleared first.
+// Calls whose kernels overlap on the GPU (two streams, or two threads) race
+// on the array and must be serialised by the caller.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) int g_dispatch_scratch[kNoAllocDispatchScratchBytes / sizeof(int)];
+
+namespace {
+std::mutex g_scratch_mu;
+int* g_scratch_ptr[64] = {};
+}  // namespace
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+cudaError_t dispatch_scratch_ptr(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    int* p = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_dispatch_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_moe_dispatch_noalloc(const int* topk_ids, const float* topk_w, long long T, int k, int E,
+                                        int* counts, int* offsets, int* pair_of_row, int* token_of,
+                                        float* weight_of, long long rows_bound, int* status, cudaStream_t stream) {
+  int* scratch = nullptr;
+  cudaError_t e = dispatch_scratch_ptr(&scratch);
+  if (e != cudaSuccess) return e;
+  return launch_moe_dispatch(topk_ids, topk_w, T, k, E, counts, offsets, pair_of_row, token_of, weight_of, scratch,
+                             rows_bound, status, stream);
 }
 
 }  // namespace bsk

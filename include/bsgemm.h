@@ -225,6 +225,37 @@ bs_status bs_moe_dispatch(const int32_t *topk_ids, const float *topk_w, int64_t 
                           int32_t *token_of, float *weight_of, void *workspace,
                           size_t workspace_bytes, bs_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * bs_moe_dispatch_noalloc -- the same grouping as bs_moe_dispatch, for callers
+ * that cannot allocate device memory: a serving runtime that hands out only a
+ * fixed memory arena created at start-up, a plugin whose enqueue path must not
+ * allocate, or a latency-critical loop where an allocation could synchronise
+ * the device.  Such a caller has no place to put bs_moe_dispatch's workspace,
+ * so this entry point uses a scratch array that the library itself holds in
+ * static device memory; the caller still passes every input and output buffer.
+ * The pages have no counterpart of this call.
+ *
+ *   Arguments, layout and results: as bs_moe_dispatch, minus the workspace.
+ *   Limit: bs_moe_dispatch_workspace_bytes(T, k, E) must not exceed
+ *          BS_MOE_DISPATCH_NOALLOC_MAX_BYTES (1 MiB; e.g. E = 256 allows up to
+ *          1024 chunks of 1024 pairs, T*k <= 1,048,576); larger requests
+ *          return BS_ERR_INVALID with a message and launch nothing.
+ *   Memory: every GPU that loads the library holds the 1 MiB array until the
+ *          process exits.  It calls no cudaMalloc / cudaFree or other
+ *          allocating routine.
+ *   Set-up: the first call on a device looks up the array's device address
+ *          (once per device, with that device current); make that first call
+ *          before any stream capture.
+ *   Sharing: all calls share the array and it keeps the last call's
+ *          contents (each call overwrites everything it reads).  Calls whose
+ *          kernels can overlap on the GPU -- different streams or host threads
+ *          -- race on it; serialise them.
+ * ------------------------------------------------------------------------- */
+#define BS_MOE_DISPATCH_NOALLOC_MAX_BYTES (1u << 20)
+bs_status bs_moe_dispatch_noalloc(const int32_t *topk_ids, const float *topk_w, int64_t T, int k, int E,
+                                  int32_t *counts, int32_t *offsets, int32_t *pair_of_row,
+                                  int32_t *token_of, float *weight_of, bs_stream_t stream);
+
 /* bs_moe_finalize -- out[i] = bf16(out32[i]) for n elements, then out32[i] = 0
  * so the accumulator is ready for the next layer call ("DeepGEMM for Hopper
  * MoE", section 3: FP16-class output of the weighted sum). */
