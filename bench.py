@@ -190,15 +190,199 @@ class DenseLowRank:
         return time.perf_counter() - t0, 2.0 * rows * cols * self.K
 
 
+class Fp8Sweep:
+    """FP8 e4m3 GEMM, N = 7168, K = 4096, one M of {1, 16, 64, 128, 4096}.
+    Step = q8_quantize(X, 1x128) + FP8 GEMM (weights quantized 128x128 once)."""
+
+    def __init__(self, M):
+        self.M, self.N, self.K = M, 7168, 4096
+        self.name = f"fp8_e4m3_M{M}_N7168_K4096_outliers"
+        self.flops = 2.0 * self.M * self.N * self.K
+        self.metric = f"FP8 block-scaled GEMM TFLOPS (M={M}, N=7168, K=4096)"
+        self.unit = "TFLOPS"
+        self.higher_is_better = True
+        self.dtype = "e4m3 x e4m3 (fp32 1x128 / 128x128 scales), fp32 accumulate, bf16 out"
+        self.kernel_src = "fp8_quantized_gemm_q4_gb300/csrc/gemm_fp8.cu"
+        # algorithmic bytes of the GEMM kernel: weights + weight scales + activation codes/scales + output
+        self.gemm_bytes = (self.N * self.K + (self.N // 128) * (self.K // 128) * 4 + self.M * self.K
+                           + (self.K // 128) * self.M * 4 + self.M * self.N * 2)
+
+    def host_inputs(self):
+        import workloads
+        return workloads.fp8_sweep(self.M)
+
+    def setup(self, dev):
+        import torch
+        import fp8_quantized_gemm_q4_gb300 as bs
+        d = self.host_inputs()
+        self.h = d
+        self.x = d["x"].to(dev)
+        self.wq, self.ws = bs.q8_quantize(d["w"].to(dev), mode=bs.Q8_BLOCK)
+        self.xq = torch.empty((self.M, self.K), dtype=torch.uint8, device=dev)
+        self.xs = torch.empty((self.K // 128, self.M), dtype=torch.float32, device=dev)
+        self.out = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 2
+        self.bytes_in = self.x.numel() * 2
+        self.bytes_out = self.out.numel() * 2
+
+    def step(self, x=None, gemm_events=None):
+        import fp8_quantized_gemm_q4_gb300 as bs
+        x = self.x if x is None else x
+        bs.q8_quantize(x, out=(self.xq, self.xs))
+        if gemm_events:
+            gemm_events[0].record()
+        bs.gemm_fp8(self.xq, self.xs, self.wq, self.ws, out=self.out)
+        if gemm_events:
+            gemm_events[1].record()
+        return self.out
+
+    def roofline(self, gemm_ms, peaks, source):
+        if self.M <= 128:
+            gbs = self.gemm_bytes / (gemm_ms * 1e-3) / 1e9
+            peak = peaks["hbm_gbs"]
+            return {"bound": "hbm", "kernel": "fp8_gemm_kernel", "achieved": round(gbs, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": f"{source} HBM copy",
+                    "algorithmic_bytes_per_launch": self.gemm_bytes, "kernel_ms": round(gemm_ms, 5)}
+        tflops = self.flops / (gemm_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
+        return {"bound": "tensor", "kernel": "fp8_gemm_kernel", "achieved": round(tflops, 1), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                "peak_source": f"{source} bf16 burst x {NOMINAL_FP8_OVER_BF16:g} (nominal FP8/bf16)",
+                "algorithmic_flops_per_launch": self.flops, "kernel_ms": round(gemm_ms, 5)}
+
+    def oracle_sample(self, rows, cols, nthreads):
+        import oracle
+        h = self.h
+        if not hasattr(self, "_ow"):
+            self._ow = {}
+        if cols not in self._ow:
+            self._ow[cols] = oracle.q8_quantize(h["w"][:cols], rows_per_block=128)
+        ob, osb = self._ow[cols]
+        t0 = time.perf_counter()
+        oa, osa = oracle.q8_quantize(h["x"][:rows], rows_per_block=1)
+        oracle.gemm_fp8(oa, osa, ob, osb, nthreads=nthreads)
+        return time.perf_counter() - t0, 2.0 * rows * cols * self.K
+
+
+class MoEWorkload:
+    """Grouped FP4 MoE layer: dispatch, gather + quantize, gate/up GEMM + SwiGLU,
+    re-quantize, down GEMM + routed combine, bf16 cast (one step = one layer)."""
+
+    def __init__(self, large):
+        import workloads
+        cfg = workloads.MOE_LARGE if large else workloads.MOE_SMALL
+        self.index = 4 if large else 3
+        self.T, self.H, self.E, self.k, self.F = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["F"]
+        self.M, self.N, self.K = self.T, self.H, self.H
+        self.name = f"moe_fp4_T{self.T}_H{self.H}_E{self.E}_k{self.k}_F{self.F}"
+        self.metric = f"MoE grouped FP4 layer TFLOPS (T={self.T}, H={self.H}, E={self.E}, k={self.k}, F={self.F})"
+        self.unit = "TFLOPS"
+        self.higher_is_better = True
+        self.dtype = "e2m1 x e2m1 (e4m3 group-16 scales), fp32 accumulate, bf16 out"
+        # real rows only: gate/up 2*rows*H*2F, down 2*rows*F*H
+        rows = self.T * self.k
+        self.flops = 2.0 * rows * self.H * 2 * self.F + 2.0 * rows * self.F * self.H
+
+    def host_inputs(self):
+        import workloads
+        r = workloads.moe_routing(self.T, self.E, self.k, index=self.index)
+        return dict(x=workloads.moe_activations(self.T, self.H, index=self.index), routing=r)
+
+    def setup(self, dev):
+        import torch
+        import workloads
+        from fp8_quantized_gemm_q4_gb300.moe import MoELayer, quantize_expert_weights
+        d = self.host_inputs()
+        self.h = d
+        self.x = d["x"].to(dev)
+        self.ids = torch.from_numpy(d["routing"]["topk_ids"]).to(dev)
+        self.w = torch.from_numpy(d["routing"]["topk_w"]).to(dev)
+        gu, dn = [], []
+        W = None
+        # quantize expert by expert so the bf16 weights never all sit on the device
+        import fp8_quantized_gemm_q4_gb300 as bs
+        F2, H, F, E = 2 * self.F, self.H, self.F, self.E
+        wgu_codes = torch.empty((E * F2, H // 2), dtype=torch.uint8, device=dev)
+        wgu_sf = torch.empty(bs.sf_bytes(E * F2, H), dtype=torch.uint8, device=dev)
+        wd_codes = torch.empty((E * H, F // 2), dtype=torch.uint8, device=dev)
+        wd_sf = torch.empty(bs.sf_bytes(E * H, F), dtype=torch.uint8, device=dev)
+        pg, pd = bs.sf_bytes(F2, H), bs.sf_bytes(H, F)
+        for e in range(E):
+            wgu, wd = workloads.moe_expert_weights(e, F, H, index=self.index, device=dev)
+            bs.q4_quantize(wgu, out=(wgu_codes[e * F2:(e + 1) * F2], wgu_sf[e * pg:(e + 1) * pg], None))
+            bs.q4_quantize(wd, out=(wd_codes[e * H:(e + 1) * H], wd_sf[e * pd:(e + 1) * pd], None))
+        from fp8_quantized_gemm_q4_gb300.moe import MoEWeights
+        W = MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf)
+        self.layer = MoELayer(W, self.T, self.k, device=dev)
+        self.out = self.layer.out
+        # dispatch 3 + quantize 1 + gather 1 + gemm 1 + quantize 1 + gemm 1 + finalize 1
+        self.launches_per_step = 9
+        self.bytes_in = self.x.numel() * 2 + self.ids.numel() * 4 + self.w.numel() * 4
+        self.bytes_out = self.out.numel() * 2
+        counts = torch.bincount(self.ids.flatten().long(), minlength=E).cpu()
+        self.load_hist = {"max": int(counts.max()), "min": int(counts.min()), "empty": int((counts == 0).sum())}
+
+    def step(self, x=None, gemm_events=None):
+        x = self.x if x is None else x
+        if gemm_events:
+            gemm_events[0].record()
+        out = self.layer.forward(x, self.ids, self.w)
+        if gemm_events:
+            gemm_events[1].record()
+        return out
+
+    def roofline(self, layer_ms, peaks, source):
+        tflops = self.flops / (layer_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+        return {"bound": "tensor", "kernel": "whole layer (grouped fp4_gemm_kernel x2 + quantize + dispatch)",
+                "achieved": round(tflops, 1), "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                "peak_source": f"{source} bf16 burst x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/bf16)",
+                "algorithmic_flops_per_launch": self.flops, "kernel_ms": round(layer_ms, 5),
+                "expert_load": getattr(self, "load_hist", None)}
+
+    def oracle_sample(self, rows, cols, nthreads):
+        """`rows` tokens through the oracle's layer (cols ignored)."""
+        import oracle
+        import workloads
+        h = self.h
+        r = h["routing"]
+        toks = list(range(rows))
+        experts = sorted(set(int(e) for t in toks for e in r["topk_ids"][t]))
+        if not hasattr(self, "_ow"):
+            self._ow = {}
+        for e in experts:
+            if e not in self._ow:
+                wgu, wd = workloads.moe_expert_weights(e, self.F, self.H, index=self.index, device="cuda")
+                self._ow[e] = (oracle.q4_quantize(wgu.cpu()), oracle.q4_quantize(wd.cpu()))
+        E = self.E
+        gc = [self._ow[e][0][0] if e in self._ow else None for e in range(E)]
+        gs = [self._ow[e][0][1] if e in self._ow else None for e in range(E)]
+        dc = [self._ow[e][1][0] if e in self._ow else None for e in range(E)]
+        ds = [self._ow[e][1][1] if e in self._ow else None for e in range(E)]
+        t0 = time.perf_counter()
+        oracle.moe_layer(h["x"][:rows], r["topk_ids"][:rows], r["topk_w"][:rows], gc, gs, dc, ds, F=self.F,
+                         nthreads=nthreads)
+        fl = 2.0 * rows * self.k * (self.H * 2 * self.F + self.F * self.H)
+        return time.perf_counter() - t0, fl
+
+
 WORKLOADS = {
     "dense_lowrank": lambda: DenseLowRank(tiny=False),
     "dense_tiny": lambda: DenseLowRank(tiny=True),
+    "fp8_m1": lambda: Fp8Sweep(1),
+    "fp8_m16": lambda: Fp8Sweep(16),
+    "fp8_m64": lambda: Fp8Sweep(64),
+    "fp8_m128": lambda: Fp8Sweep(128),
+    "fp8_m4096": lambda: Fp8Sweep(4096),
+    "moe_small": lambda: MoEWorkload(large=False),
+    "moe_large": lambda: MoEWorkload(large=True),
 }
 
 
-def traffic_for(kernel_src: str):
+def traffic_for(kernel_src: str, workload: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source (else None)."""
+    summary, if it was taken on the current kernel source and this workload
+    (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -206,13 +390,30 @@ def traffic_for(kernel_src: str):
         d = json.load(f)
     src = os.path.join(ROOT, kernel_src)
     h = hashlib.sha1(open(src, "rb").read()).hexdigest()
-    ent = d.get(kernel_src)
-    if ent and ent.get("source_sha1") == h:
-        return ent.get("dram_bytes_per_launch")
+    for ent in d.get("entries", []):
+        if ent.get("kernel_src") == kernel_src and ent.get("source_sha1") == h and ent.get("workload") == workload:
+            return ent.get("dram_bytes_per_launch")
     return None
 
 
 # ---------------------------------------------------------------------------
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings (the slowest replica sets the job's
+    time).  Works with NCCL on GPUs and gloo on CPU."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(work_per_rank, world, step_ms):
+    """Whole-job rate: all ranks' work over the (max-over-ranks) step time."""
+    return world * work_per_rank / (step_ms * 1e-3)
+
+
 def run_ours(args, wl, rank, world, dev, peaks, source):
     import torch
     import torch.distributed as dist
@@ -246,10 +447,7 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
     clk = clocks.stop()
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     gemm_ms = sum(a.elapsed_time(b) for a, b in gev) / K
-    if world > 1:
-        t = torch.tensor([step_ms, gemm_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, gemm_ms = float(t[0]), float(t[1])
+    step_ms, gemm_ms = max_over_ranks([step_ms, gemm_ms], dev)
 
     # end to end through the public API with pinned host buffers
     xh = wl.x.cpu().pin_memory()
@@ -268,18 +466,16 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks([e2e_ms], dev)
 
     import fp8_quantized_gemm_q4_gb300 as bs
     st, detail = bs.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
-    value = world * wl.flops / (step_ms * 1e-3) / 1e12
+    value = job_throughput(wl.flops, world, step_ms) / 1e12
     roof = wl.roofline(gemm_ms, peaks, source)
-    roof["traffic"] = traffic_for("fp8_quantized_gemm_q4_gb300/csrc/gemm_fp4.cu")
+    roof["traffic"] = traffic_for(getattr(wl, "kernel_src", "fp8_quantized_gemm_q4_gb300/csrc/gemm_fp4.cu"),
+                                  wl.name)
     line = {
         "metric": wl.metric, "value": round(value, 2), "unit": wl.unit, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": wl.higher_is_better,
@@ -287,7 +483,7 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
                    "parallelism": f"replicas x{world}"},
-        "e2e": {"value": round(world * wl.flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": wl.unit,
+        "e2e": {"value": round(job_throughput(wl.flops, world, e2e_ms) / 1e12, 2), "unit": wl.unit,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": wl.bytes_in,
                 "d2h_bytes_per_step": wl.bytes_out},
         "gpu_launches": K * wl.launches_per_step,

@@ -20,7 +20,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 
 __all__ = [
-    "load", "sf_bytes", "sf_offset", "q4_quantize", "q8_quantize", "gemm_fp4", "gemm_fp8",
+    "load", "sf_bytes", "sf_offset", "q4_quantize", "fp4_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
     "grouped_gemm_fp4", "moe_dispatch", "moe_finalize", "moe_rows_bound", "device_status",
     "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE",
 ]
@@ -69,6 +69,8 @@ def load(path: str | None = None):
         lib.bs_sf_offset.argtypes = [I64, I64, I64]
         lib.q4_quantize.restype = I
         lib.q4_quantize.argtypes = [P, I, I64, I64, I64, P, P, P, P, I, P, P]
+        lib.bs_fp4_gather_rows.restype = I
+        lib.bs_fp4_gather_rows.argtypes = [P, P, I64, I64, P, I64, P, P, P]
         lib.q8_quantize.restype = I
         lib.q8_quantize.argtypes = [P, I, I64, I64, I64, I, P, P, P]
         lib.bs_gemm.restype = I
@@ -148,6 +150,17 @@ def q4_quantize(x: torch.Tensor, gather: torch.Tensor | None = None, rows: int |
     _check(load().q4_quantize(_ptr(x), _dt(x), M, K, x.stride(0), _ptr(gather), _ptr(codes), _ptr(sf),
                               _ptr(lora_a_t), 32 if lora_a_t is not None else 0, _ptr(lt), _stream(stream)))
     return codes, sf, lt
+
+
+def fp4_gather_rows(codes, sf, K: int, gather, out=None, stream=None):
+    """Rows gather[i] of an FP4 matrix (codes + MMA-layout scales); -1 -> zero row."""
+    rows_out = gather.numel()
+    if out is None:
+        out = (torch.empty((rows_out, K // 2), dtype=torch.uint8, device=codes.device),
+               torch.empty(sf_bytes(rows_out, K), dtype=torch.uint8, device=codes.device))
+    _check(load().bs_fp4_gather_rows(_ptr(codes), _ptr(sf), codes.shape[0], K, _ptr(gather), rows_out,
+                                     _ptr(out[0]), _ptr(out[1]), _stream(stream)))
+    return out
 
 
 def q8_quantize(x: torch.Tensor, mode: int = Q8_TOKEN, out=None, stream=None):

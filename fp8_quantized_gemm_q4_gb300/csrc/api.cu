@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -160,12 +161,35 @@ bs_status q4_quantize(const void* x, bs_dtype dt, int64_t M, int64_t K, int64_t 
   }
   if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (want_lora && K % 256 == 0) {
+    // one pass over X for codes, scales and T
+    cudaError_t e = bsk::launch_q4_lowrank_fused(x, M, K, ldx, gather, lora_a_t, codes, sf, lora_t, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fused quantize + low-rank launch");
+    return BS_OK;
+  }
   cudaError_t e = bsk::launch_q4_quantize(x, dt == BS_DTYPE_BF16, M, K, ldx, gather, codes, sf, s);
   if (e != cudaSuccess) return cuda_fail(e, "q4_quantize launch");
   if (want_lora) {
     e = bsk::launch_lowrank_t(x, M, K, ldx, gather, lora_a_t, lora_t, s);
     if (e != cudaSuccess) return cuda_fail(e, "low-rank launch");
   }
+  return BS_OK;
+}
+
+bs_status bs_fp4_gather_rows(const uint8_t* codes_in, const uint8_t* sf_in, int64_t rows_in, int64_t K,
+                             const int32_t* gather, int64_t rows_out, uint8_t* codes_out, uint8_t* sf_out,
+                             bs_stream_t stream) {
+  if (rows_in < 0 || rows_out < 0 || K <= 0) return fail(BS_ERR_INVALID, "gather_rows: bad sizes");
+  if (K % 64) return fail(BS_ERR_ALIGN, "gather_rows: K=%lld not a multiple of 64", (long long)K);
+  if (rows_out == 0) return BS_OK;
+  if (!gather || !codes_out || !sf_out || (rows_in > 0 && (!codes_in || !sf_in)))
+    return fail(BS_ERR_INVALID, "gather_rows: null pointer");
+  if (!aligned16(codes_out) || !aligned16(sf_out) || (codes_in && !aligned16(codes_in)) || (sf_in && !aligned16(sf_in)))
+    return fail(BS_ERR_ALIGN, "gather_rows: buffers must be 16-byte aligned");
+  if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_fp4_gather_rows(codes_in, sf_in, rows_in, K, gather, rows_out, codes_out, sf_out,
+                                              reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gather_rows launch");
   return BS_OK;
 }
 
@@ -205,13 +229,25 @@ static bs_status check_common(const bs_gemm_args* a, bool grouped) {
   return BS_OK;
 }
 
+// FP4 stage depth: 256 K elements (128-byte rows, 128B swizzle) measured
+// faster than 128 (64-byte rows) on GB300 even though the finer ring holds
+// more stages; BSGEMM_FP4_BK=128 selects the finer ring (for measurements).
+static int fp4_bk() {
+  static int bk = [] {
+    const char* e = getenv("BSGEMM_FP4_BK");
+    return (e && atoi(e) == 128) ? 128 : 256;
+  }();
+  return bk;
+}
+
 static bs_status fp4_maps(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows) {
   const uint64_t kb = (uint64_t)a->K / 2;
-  bs_status st = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, kb, (uint64_t)a->M, kb, 128, 128,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
+  L.bk = fp4_bk();
+  const uint32_t box = (uint32_t)L.bk / 2;
+  const CUtensorMapSwizzle sw = L.bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  bs_status st = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, kb, (uint64_t)a->M, kb, box, 128, sw);
   if (st != BS_OK) return st;
-  st = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->b, kb, (uint64_t)b_rows, kb, 128, 128,
-                CU_TENSOR_MAP_SWIZZLE_128B);
+  st = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->b, kb, (uint64_t)b_rows, kb, box, 128, sw);
   if (st != BS_OK) return st;
   if (a->lora_t) {
     st = make_map(&L.tmT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a->lora_t, 64, (uint64_t)a->M, 128, 32, 128,
@@ -271,7 +307,37 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     return BS_OK;
   }
   if (a->fmt == BS_FMT_FP8) {
-    return fail(BS_ERR_UNSUPPORTED, "FP8 GEMM not built yet");
+    if (a->K % 128) return fail(BS_ERR_ALIGN, "FP8: K=%lld not a multiple of 128", (long long)a->K);
+    if (a->alpha != 1.0f || a->col_scale || a->lora_t || a->bias)
+      return fail(BS_ERR_UNSUPPORTED, "FP8 GEMM takes no alpha/col_scale/low-rank/bias");
+    if (reinterpret_cast<uintptr_t>(a->sfa) & 3 || reinterpret_cast<uintptr_t>(a->sfb) & 3)
+      return fail(BS_ERR_ALIGN, "FP8 scales must be 4-byte aligned");
+    if (a->M == 0) return BS_OK;
+    bsk::Fp8Launch L;
+    memset(&L, 0, sizeof L);
+    L.tile_n = bsk::fp8_tile_n(a->M);
+    // swap-AB: the weights [N, K] are the MMA's A operand, the tokens [M, K] its B
+    st = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->b, (uint64_t)a->K, (uint64_t)a->N, (uint64_t)a->K,
+                  128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BS_OK) return st;
+    st = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, (uint64_t)a->K, (uint64_t)a->M, (uint64_t)a->K,
+                  128, (uint32_t)L.tile_n, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BS_OK) return st;
+    L.p.sfa = static_cast<const float*>(a->sfa);
+    L.p.sfb = static_cast<const float*>(a->sfb);
+    L.p.M = (int)a->M;
+    L.p.N = (int)a->N;
+    L.p.K = (int)a->K;
+    L.p.out = a->out;
+    L.p.out_bf16 = a->out_dtype == BS_DTYPE_BF16;
+    L.p.ldo = a->ldo;
+    L.p.status = status;
+    L.swap_ab = true;
+    const long long tiles = ((a->N + 127) / 128) * ((a->M + L.tile_n - 1) / L.tile_n);
+    L.grid = (int)(tiles < sms ? tiles : sms);
+    cudaError_t e = bsk::launch_fp8_gemm(L, s);
+    if (e != cudaSuccess) return cuda_fail(e, "FP8 GEMM launch");
+    return BS_OK;
   }
   return fail(BS_ERR_INVALID, "fmt %d", a->fmt);
 }

@@ -34,40 +34,48 @@
 namespace bsk {
 namespace fp4 {
 
-constexpr int BM = 128, BN = 256, BK = 256;
+constexpr int BM = 128, BN = 256;
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
 constexpr int kMaxExperts = 1024;
 constexpr int kMisc = 2048 + (kMaxExperts + 1) * 4 + 1024;  // barriers + tile table + slack
-
-constexpr Fp4TileShape kShapeLora{BM, BN, BK, 1, true, 32, kMisc};
-constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 1, false, 32, kMisc};
-constexpr int kStagesLora = fp4_main_stages(kShapeLora);
-constexpr int kStagesNoLora = fp4_main_stages(kShapeNoLora);
-static_assert(kStagesLora >= 2 && kStagesNoLora >= 2, "pipeline needs at least double buffering");
-static_assert(fp4_smem_total(kShapeLora, kStagesLora) + kAlign <= kSmemPerCta + kAlign, "smem budget");
-static_assert(fp4_stage_bytes(kShapeNoLora) == 16384 + 32768 + 2048 + 4096, "stage layout");
 constexpr int kSfBuffers = 2;
 constexpr int kTmemAcc = 0;
 constexpr int kTmemSf = BN;                        // scale staging after the accumulator
 constexpr int kSfColsPerMma = 4 + BN / 32;         // 4 for A, 8 for B
-constexpr int kSfColsPerStage = (BK / 64) * kSfColsPerMma;
-static_assert(fp4_tmem_cols(kShapeLora, 1, kSfBuffers) <= kTmemCols, "tmem budget");
-constexpr int kTmemAlloc = pow2_cols(fp4_tmem_cols(kShapeLora, 1, kSfBuffers));
-
-// Per-stage layout (bytes from the stage base; every piece 1024-aligned or 16-aligned).
-constexpr int kOffA = 0;
-constexpr int kOffB = BM * BK / 2;                  // 16384
-constexpr int kOffSfa = kOffB + BN * BK / 2;        // 49152
-constexpr int kOffSfb = kOffSfa + BM * BK / 16;     // 51200
-constexpr int kStageBytes = kOffSfb + BN * BK / 16; // 55296
-static_assert(kStageBytes % kAlign == 0, "stage alignment");
 // Low-rank slot: T hi [128 x 32 bf16], T lo, Bl^T [256 x 32 bf16], 64B swizzle.
 constexpr int kLoraThi = 0, kLoraTlo = 8192, kLoraBl = 16384, kLoraBytes = 32768;
-static_assert(kLoraBytes == fp4_lora_bytes(kShapeLora), "lora slot layout");
-
 constexpr uint32_t kIdescMain = idesc_mxf4nvf4(BM, BN);
 constexpr uint32_t kIdescLora = idesc_bf16(BM, BN);
+
+// Stage geometry for a K depth of BK FP4 elements per stage: rows of BK/2
+// bytes in the matching TMA / MMA swizzle (128 B for BK = 256, 64 B for 128).
+template <int BK>
+struct Geo {
+  static_assert(BK == 128 || BK == 256, "stage depth");
+  static constexpr int kRowBytes = BK / 2;
+  static constexpr uint32_t kLayout = BK == 256 ? kLayoutSw128 : kLayoutSw64;
+  static constexpr int kSbo = 8 * kRowBytes;              // 8-row swizzle atom
+  static constexpr int kMmas = BK / 64;                   // K = 64 per MMA
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = BM * kRowBytes;
+  static constexpr int kOffSfa = kOffB + BN * kRowBytes;
+  static constexpr int kOffSfb = kOffSfa + kMmas * 512;
+  static constexpr int kStageBytes = kOffSfb + 2 * kMmas * 512;
+  static_assert(kStageBytes % kAlign == 0, "stage alignment");
+  static constexpr int kSfColsPerStage = kMmas * kSfColsPerMma;
+  static constexpr Fp4TileShape kShapeLora{BM, BN, BK, 1, true, 32, kMisc};
+  static constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 1, false, 32, kMisc};
+  static_assert(kStageBytes == fp4_stage_bytes(kShapeNoLora), "stage layout matches the budget");
+  static_assert(kLoraBytes == fp4_lora_bytes(kShapeLora), "lora slot layout matches the budget");
+  static constexpr int kStagesLora = fp4_main_stages(kShapeLora) < 16 ? fp4_main_stages(kShapeLora) : 16;
+  static constexpr int kStagesNoLora = fp4_main_stages(kShapeNoLora) < 16 ? fp4_main_stages(kShapeNoLora) : 16;
+  static_assert(kStagesLora >= 2 && kStagesNoLora >= 2, "pipeline needs at least double buffering");
+  static_assert(fp4_smem_total(kShapeLora, kStagesLora) + kAlign <= kSmemPerCta, "lora smem");
+  static_assert(fp4_smem_total(kShapeNoLora, kStagesNoLora) + kAlign <= kSmemPerCta, "smem");
+  static_assert(fp4_tmem_cols(kShapeLora, 1, kSfBuffers) <= kTmemCols, "tmem budget");
+  static constexpr int kTmemAlloc = pow2_cols(fp4_tmem_cols(kShapeLora, 1, kSfBuffers));
+};
 
 struct Tile {
   int row0;       // first A row (128-aligned)
@@ -95,7 +103,7 @@ struct Smem {
   int* prefix;  // [E + 1]
 };
 
-template <int kStages, bool kLora>
+template <int kStages, bool kLora, int kStageBytes>
 __device__ __forceinline__ Smem carve(uint8_t* base) {
   Smem s;
   s.stages = base;
@@ -169,7 +177,7 @@ __device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, i
   return tl;
 }
 
-template <int kStages, bool kLora, int kEpi>
+template <int BK, int kStages, bool kLora, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmL,
@@ -177,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kAlign - 1) &
                                              ~static_cast<uintptr_t>(kAlign - 1));
-  Smem sm = carve<kStages, kLora>(base);
+  using G = Geo<BK>;
+  Smem sm = carve<kStages, kLora, G::kStageBytes>(base);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   volatile int* abort_flag = sm.abort_flag;
 
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(sm.tmem_base, kTmemAlloc);
+    tmem_alloc(sm.tmem_base, G::kTmemAlloc);
     tmem_relinquish();
   }
   if (warp == 3) {
@@ -246,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *sm.tmem_base;
   const int total = *sm.total_tiles;
   const int kchunks = p.K / 64;
-  const int kstages = (kchunks + 3) / 4;
+  const int kstages = (kchunks + G::kMmas - 1) / G::kMmas;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -260,16 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* sfb1_src = p.sfb + (size_t)tl.sfb_blk1 * kchunks * 512;
       for (int ks = 0; ks < kstages; ++ks) {
         if (!mbar_wait(&sm.empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 10)) { ok = false; break; }
-        const int nmma = min(4, kchunks - 4 * ks);
-        uint8_t* st = sm.stages + ps.index * kStageBytes;
+        const int nmma = min(G::kMmas, kchunks - G::kMmas * ks);
+        uint8_t* st = sm.stages + ps.index * G::kStageBytes;
         uint64_t* bar = &sm.full[ps.index];
-        mbar_arrive_expect_tx(bar, (uint32_t)(BM * 128 + BN * 128 + nmma * 512 * 3));
-        tma_load_2d(st + kOffA, &tmA, bar, ks * 128, tl.row0);
-        tma_load_2d(st + kOffB, &tmB, bar, ks * 128, tl.brow0);
-        tma_load_2d(st + kOffB + 128 * 128, &tmB, bar, ks * 128, tl.brow1);
-        bulk_load(st + kOffSfa, sfa_src + ks * 2048, nmma * 512, bar);
-        bulk_load(st + kOffSfb, sfb0_src + ks * 2048, nmma * 512, bar);
-        bulk_load(st + kOffSfb + 2048, sfb1_src + ks * 2048, nmma * 512, bar);
+        mbar_arrive_expect_tx(bar, (uint32_t)((BM + BN) * G::kRowBytes + nmma * 512 * 3));
+        tma_load_2d(st + G::kOffA, &tmA, bar, ks * G::kRowBytes, tl.row0);
+        tma_load_2d(st + G::kOffB, &tmB, bar, ks * G::kRowBytes, tl.brow0);
+        tma_load_2d(st + G::kOffB + 128 * G::kRowBytes, &tmB, bar, ks * G::kRowBytes, tl.brow1);
+        bulk_load(st + G::kOffSfa, sfa_src + ks * G::kMmas * 512, nmma * 512, bar);
+        bulk_load(st + G::kOffSfb, sfb0_src + ks * G::kMmas * 512, nmma * 512, bar);
+        bulk_load(st + G::kOffSfb + G::kMmas * 512, sfb1_src + ks * G::kMmas * 512, nmma * 512, bar);
         issued_mask |= 1u << ps.index;
         last_phase = (last_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
         ps.advance();
@@ -317,21 +326,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ks < kstages; ++ks) {
         if (!mbar_wait(&sm.full[ps.index], ps.phase, abort_flag, p.status, 31)) { ok = false; break; }
         tc_fence_after();
-        const int nmma = min(4, kchunks - 4 * ks);
-        uint8_t* st = sm.stages + ps.index * kStageBytes;
-        const uint32_t sa = smem_u32(st + kOffA), sb = smem_u32(st + kOffB);
-        const uint32_t ssfa = smem_u32(st + kOffSfa), ssfb = smem_u32(st + kOffSfb);
-        const uint32_t sf_col = kTmemSf + sf_buf * kSfColsPerStage;
+        const int nmma = min(G::kMmas, kchunks - G::kMmas * ks);
+        uint8_t* st = sm.stages + ps.index * G::kStageBytes;
+        const uint32_t sa = smem_u32(st + G::kOffA), sb = smem_u32(st + G::kOffB);
+        const uint32_t ssfa = smem_u32(st + G::kOffSfa), ssfb = smem_u32(st + G::kOffSfb);
+        const uint32_t sf_col = kTmemSf + sf_buf * G::kSfColsPerStage;
         for (int j = 0; j < nmma; ++j) {
           const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
           tc_cp_32x128b_warpx4(col, smem_desc(ssfa + 512 * j, 0, 128, kLayoutNone));
           tc_cp_32x128b_warpx4(col + 4, smem_desc(ssfb + 512 * j, 0, 128, kLayoutNone));
-          tc_cp_32x128b_warpx4(col + 8, smem_desc(ssfb + 2048 + 512 * j, 0, 128, kLayoutNone));
+          tc_cp_32x128b_warpx4(col + 8, smem_desc(ssfb + G::kMmas * 512 + 512 * j, 0, 128, kLayoutNone));
         }
         for (int j = 0; j < nmma; ++j) {
           const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
-          mma_mxf4nvf4(tmem + kTmemAcc, smem_desc(sa + 32 * j, 16, 1024, kLayoutSw128),
-                       smem_desc(sb + 32 * j, 16, 1024, kLayoutSw128), kIdescMain, col, col + 4,
+          mma_mxf4nvf4(tmem + kTmemAcc, smem_desc(sa + 32 * j, 16, G::kSbo, G::kLayout),
+                       smem_desc(sb + 32 * j, 16, G::kSbo, G::kLayout), kIdescMain, col, col + 4,
                        (ks > 0 || j > 0) ? 1u : 0u);
         }
         tc_commit(&sm.empty[ps.index]);
@@ -472,38 +481,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemAlloc);
+    tmem_dealloc(tmem, G::kTmemAlloc);
   }
 }
 
-template <int kStages, bool kLora, int kEpi>
+template <int BK, bool kLora, int kEpi>
 static cudaError_t launch_one(const Fp4Launch& L, cudaStream_t stream) {
-  auto kern = fp4_gemm_kernel<kStages, kLora, kEpi>;
-  const int smem = fp4_smem_total(kLora ? kShapeLora : kShapeNoLora, kStages) + kAlign;
-  static_assert(fp4_smem_total(kShapeLora, kStagesLora) + kAlign <= kSmemPerCta, "lora smem");
-  static_assert(fp4_smem_total(kShapeNoLora, kStagesNoLora) + kAlign <= kSmemPerCta, "smem");
+  using G = Geo<BK>;
+  constexpr int kStages = kLora ? G::kStagesLora : G::kStagesNoLora;
+  auto kern = fp4_gemm_kernel<BK, kStages, kLora, kEpi>;
+  const int smem = fp4_smem_total(kLora ? G::kShapeLora : G::kShapeNoLora, kStages) + kAlign;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, kThreads, smem, stream>>>(L.tmA, L.tmB, L.tmT, L.tmL, L.p);
   return cudaGetLastError();
 }
 
-}  // namespace fp4
-
-cudaError_t launch_fp4_gemm(const Fp4Launch& L, cudaStream_t stream) {
-  using namespace fp4;
+template <int BK>
+static cudaError_t launch_bk(const Fp4Launch& L, cudaStream_t stream) {
   if (L.lora) {
     if (L.epilogue != kEpiStore) return cudaErrorInvalidValue;
-    return launch_one<kStagesLora, true, kEpiStore>(L, stream);
+    return launch_one<BK, true, kEpiStore>(L, stream);
   }
   switch (L.epilogue) {
-    case kEpiStore: return launch_one<kStagesNoLora, false, kEpiStore>(L, stream);
-    case kEpiSwiglu: return launch_one<kStagesNoLora, false, kEpiSwiglu>(L, stream);
-    case kEpiCombine: return launch_one<kStagesNoLora, false, kEpiCombine>(L, stream);
+    case kEpiStore: return launch_one<BK, false, kEpiStore>(L, stream);
+    case kEpiSwiglu: return launch_one<BK, false, kEpiSwiglu>(L, stream);
+    case kEpiCombine: return launch_one<BK, false, kEpiCombine>(L, stream);
   }
   return cudaErrorInvalidValue;
 }
 
-int fp4_stages(bool lora) { return lora ? fp4::kStagesLora : fp4::kStagesNoLora; }
+}  // namespace fp4
+
+cudaError_t launch_fp4_gemm(const Fp4Launch& L, cudaStream_t stream) {
+  if (L.bk == 256) return fp4::launch_bk<256>(L, stream);
+  if (L.bk == 128) return fp4::launch_bk<128>(L, stream);
+  return cudaErrorInvalidValue;
+}
+
+int fp4_stages(bool lora, int bk) {
+  if (bk == 256) return lora ? fp4::Geo<256>::kStagesLora : fp4::Geo<256>::kStagesNoLora;
+  return lora ? fp4::Geo<128>::kStagesLora : fp4::Geo<128>::kStagesNoLora;
+}
 
 }  // namespace bsk

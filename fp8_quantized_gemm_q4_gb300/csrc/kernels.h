@@ -36,10 +36,11 @@ struct Fp4Launch {
   bool lora;
   int epilogue;
   int grid;
+  int bk;                 // K elements per pipeline stage: 128 or 256 (tensor maps must match)
 };
 
 cudaError_t launch_fp4_gemm(const Fp4Launch& L, cudaStream_t stream);
-int fp4_stages(bool lora);
+int fp4_stages(bool lora, int bk);
 
 struct Fp8Params {
   const float* sfa;       // [K/128, M]
@@ -63,10 +64,17 @@ struct Fp8Launch {
 };
 
 cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream);
+int fp8_tile_n(long long M);
 
 // quantizers
 cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx,
                                const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream);
+cudaError_t launch_q4_lowrank_fused(const void* x, long long M, long long K, long long ldx, const int* gather,
+                                    const void* lora_a_t, uint8_t* codes, uint8_t* sf, void* lora_t,
+                                    cudaStream_t stream);
+cudaError_t launch_fp4_gather_rows(const uint8_t* codes_in, const uint8_t* sf_in, long long rows_in, long long K,
+                                   const int* gather, long long rows_out, uint8_t* codes_out, uint8_t* sf_out,
+                                   cudaStream_t stream);
 cudaError_t launch_lowrank_t(const void* x, long long M, long long K, long long ldx, const int* gather,
                              const void* lora_a_t, void* lora_t, cudaStream_t stream);
 cudaError_t launch_q8_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx, int mode,

@@ -272,3 +272,286 @@ cudaError_t launch_q8_quantize(const void* x, int x_bf16, long long M, long long
 }
 
 }  // namespace bsk
+
+namespace bsk {
+
+// ---------------------------------------------------------------------------
+// Fused FP4 quantization + low-rank left factor for bf16 rows.
+//
+// One CTA owns 64 rows and streams them through shared memory in K chunks of
+// 256 (3-stage cp.async ring, 32 KB of X + 16 KB of A^T per stage).  Each
+// 16-byte chunk j of row r is stored at chunk position j ^ (r % 8) so that
+// both consumers read conflict-free:
+//   - quantization: thread t owns row t % 64 and 64-element quarter t / 64 of
+//     the chunk: 4 group scales (one 32-bit word of the MMA scale layout) and
+//     32 bytes of codes;
+//   - low rank: warp w multiplies rows 16 (w % 4) .. +16 by A over the K half
+//     w / 4 of the chunk with ldmatrix + mma.sync m16n8k16 (bf16 -> fp32);
+//     the two K halves are summed through shared memory at the end and T is
+//     written as bf16 hi | lo.
+// X is read from HBM once for both results.
+// ---------------------------------------------------------------------------
+namespace fq {
+constexpr int R = 64;          // rows per CTA
+constexpr int KC = 256;        // K per stage
+constexpr int S = 3;           // stages
+constexpr int XB = R * KC * 2;       // 32 KB
+constexpr int AB = 32 * KC * 2;      // 16 KB
+constexpr int STAGE = XB + AB;
+constexpr int SMEM = S * STAGE + 2 * 4 * 16 * 32 * 4;  // + reduction buffer [4 rowgroups][16][32] x 2 halves
+}  // namespace fq
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, bool valid) {
+  const int n = valid ? 16 : 0;  // src-size 0 -> zero fill
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t saddr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(saddr));
+}
+
+// byte offset of 16-byte chunk `chunk` of row `row` in a [rows][KC] bf16 tile
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * (fq::KC * 2) + ((chunk ^ (row & 7)) * 16));
+}
+
+__global__ void __launch_bounds__(256) q4_lowrank_fused_kernel(
+    const __nv_bfloat16* __restrict__ x, long long M, long long Mpad, long long K, long long ldx,
+    const int* __restrict__ gather, const __nv_bfloat16* __restrict__ at, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ sf, __nv_bfloat16* __restrict__ t_out) {
+  extern __shared__ __align__(128) uint8_t fsm[];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const long long r0 = (long long)blockIdx.x * fq::R;
+  const int nchunks = (int)(K / fq::KC);
+  const uint32_t sbase = smem_u32(fsm);
+
+  // source row of each of this CTA's rows, resolved once per thread's load slots
+  auto src_row = [&](int r) -> long long {
+    const long long row = r0 + r;
+    if (row >= M) return -1;
+    return gather ? (long long)gather[row] : row;
+  };
+
+  // loader: X chunk = 64 rows x 32 chunks of 16 B = 2048 copies (8 per thread);
+  // A^T chunk = 32 rows x 32 chunks = 1024 copies (4 per thread)
+  long long my_src[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) my_src[i] = src_row((tid + i * 256) / 32);
+  auto load_stage = [&](int c, int s) {
+    const uint32_t xs = sbase + s * fq::STAGE, as = xs + fq::XB;
+    const long long k0 = (long long)c * fq::KC;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = tid + i * 256, r = idx / 32, ch = idx % 32;
+      const long long sr = my_src[i];
+      const __nv_bfloat16* g = x + (sr >= 0 ? sr * ldx + k0 + ch * 8 : 0);
+      cp_async16(xs + swz(r, ch), g, sr >= 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = tid + i * 256, r = idx / 32, ch = idx % 32;
+      cp_async16(as + swz(r, ch), at + (long long)r * K + k0 + ch * 8, true);
+    }
+  };
+
+  // quantization role of this thread
+  const int qrow = tid % fq::R, qquart = tid / fq::R;  // quarter = 64 elements = 8 chunks
+  const long long grow = r0 + qrow;
+  // low-rank role of this warp
+  const int rg = warp % 4, kh = warp / 4;
+  float d[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[i][j] = 0.0f;
+
+  for (int s = 0; s < fq::S - 1; ++s) {
+    if (s < nchunks) load_stage(s, s);
+    cp_async_commit();
+  }
+  for (int c = 0; c < nchunks; ++c) {
+    const int s = c % fq::S;
+    if (c + fq::S - 1 < nchunks) load_stage(c + fq::S - 1, (c + fq::S - 1) % fq::S);
+    cp_async_commit();
+    cp_async_wait<fq::S - 1>();
+    __syncthreads();
+    const uint32_t xs = sbase + s * fq::STAGE, as = xs + fq::XB;
+
+    // ---- quantize 64 elements (4 groups) of row qrow
+    {
+      float v[64];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint4 raw;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                     : "r"(xs + swz(qrow, qquart * 8 + j)));
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[8 * j + 2 * i] = __uint_as_float(w4[i] << 16);
+          v[8 * j + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+        }
+      }
+      uint32_t sfw = 0;
+      uint32_t cw[8];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[16 * g + i]));
+        const uint32_t sc = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
+        const float sv = e4m3_to_f32(sc);
+        sfw |= sc << (8 * g);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float q[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) q[i] = (sv == 0.0f) ? 0.0f : __fdiv_rn(v[16 * g + 8 * h + i], sv);
+          cw[2 * g + h] = f32x8_to_e2m1x8(q);
+        }
+      }
+      const long long kq = (long long)c * fq::KC + qquart * 64;  // first element of the quarter
+      if (grow < Mpad) {
+        const long long off = ((grow / 128) * (K / 64) + kq / 64) * 512 + (grow % 32) * 16 + ((grow % 128) / 32) * 4;
+        *reinterpret_cast<uint32_t*>(sf + off) = (grow < M) ? sfw : 0u;
+      }
+      if (grow < M) {
+        uint4* dst = reinterpret_cast<uint4*>(codes + grow * (K / 2) + kq / 2);
+        dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      }
+    }
+
+    // ---- low rank: rows 16 rg .. +16, K half kh of the chunk (8 k-steps)
+    {
+      const int arow = rg * 16 + (lane % 16);
+      const int ahalf = lane / 16;  // second 8 columns of the k-step
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int kchunk = kh * 16 + ks * 2;  // 16-byte chunk of this k-step's first 8 elements
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(xs + swz(arow, kchunk + ahalf), a0, a1, a2, a3);
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {  // pairs of n-tiles: rows 16 np .. +16 of A^T
+          const int brow = np * 16 + (lane % 8) + ((lane / 16) * 8);
+          const int bhalf = (lane / 8) % 2;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(as + swz(brow, kchunk + bhalf), b0, b1, b2, b3);
+          // b0/b1: n-tile 2np (k lo / k hi); b2/b3: n-tile 2np+1
+          asm volatile(
+              "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+              "{%0, %1, %2, %3};"
+              : "+f"(d[2 * np][0]), "+f"(d[2 * np][1]), "+f"(d[2 * np][2]), "+f"(d[2 * np][3])
+              : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+          asm volatile(
+              "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+              "{%0, %1, %2, %3};"
+              : "+f"(d[2 * np + 1][0]), "+f"(d[2 * np + 1][1]), "+f"(d[2 * np + 1][2]), "+f"(d[2 * np + 1][3])
+              : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b2), "r"(b3));
+        }
+      }
+    }
+    __syncthreads();  // stage s may be refilled next iteration
+  }
+  cp_async_wait<0>();
+
+  // ---- reduce the two K halves and write T as bf16 hi | lo
+  float* red = reinterpret_cast<float*>(fsm + fq::S * fq::STAGE);  // [2][4][16][32]
+  {
+    const int g = lane / 4, tq = lane % 4;
+    float* rb = red + ((kh * 4 + rg) * 16) * 32;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      rb[g * 32 + nt * 8 + 2 * tq] = d[nt][0];
+      rb[g * 32 + nt * 8 + 2 * tq + 1] = d[nt][1];
+      rb[(g + 8) * 32 + nt * 8 + 2 * tq] = d[nt][2];
+      rb[(g + 8) * 32 + nt * 8 + 2 * tq + 1] = d[nt][3];
+    }
+  }
+  __syncthreads();
+  for (int o = tid; o < fq::R * 32; o += 256) {
+    const int r = o / 32, j = o % 32;
+    const long long row = r0 + r;
+    if (row >= M) continue;
+    const float t = red[(0 * 4 * 16 + r) * 32 + j] + red[(1 * 4 * 16 + r) * 32 + j];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(t);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(t - __bfloat162float(hi));
+    t_out[row * 64 + j] = hi;
+    t_out[row * 64 + 32 + j] = lo;
+  }
+}
+
+cudaError_t launch_q4_lowrank_fused(const void* x, long long M, long long K, long long ldx, const int* gather,
+                                    const void* lora_a_t, uint8_t* codes, uint8_t* sf, void* lora_t,
+                                    cudaStream_t stream) {
+  const long long Mpad = (M + 127) / 128 * 128;
+  const long long blocks = Mpad / fq::R;  // covers the scale padding rows too
+  cudaError_t e = cudaFuncSetAttribute(q4_lowrank_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       fq::SMEM);
+  if (e != cudaSuccess) return e;
+  q4_lowrank_fused_kernel<<<(unsigned)blocks, 256, fq::SMEM, stream>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), M, Mpad, K, ldx, gather,
+      reinterpret_cast<const __nv_bfloat16*>(lora_a_t), codes, sf, reinterpret_cast<__nv_bfloat16*>(lora_t));
+  return cudaGetLastError();
+}
+
+}  // namespace bsk
+
+namespace bsk {
+
+// Gather rows of an already quantized FP4 matrix: out row i = in row
+// gather[i] (negative: zero row), codes copied as 16-byte vectors, each
+// 64-element chunk's scale word moved from the source row's place in the MMA
+// scale layout to the destination row's.  Equal, bit for bit, to quantizing
+// the gathered bf16 rows (quantization is row-local), at a fraction of the
+// traffic when rows repeat (MoE: each token feeds k experts).
+__global__ void __launch_bounds__(256) fp4_gather_rows_kernel(const uint8_t* __restrict__ codes_in,
+                                                              const uint8_t* __restrict__ sf_in, long long rows_in,
+                                                              long long K, const int* __restrict__ gather,
+                                                              long long rows_out, long long rows_out_pad,
+                                                              uint8_t* __restrict__ codes_out,
+                                                              uint8_t* __restrict__ sf_out) {
+  const int lane = threadIdx.x & 31;
+  const long long kv = K / 32;  // 16-byte vectors per row of codes
+  const long long kc = K / 64;  // scale words per row
+  for (long long row = (long long)blockIdx.x * 8 + threadIdx.x / 32; row < rows_out_pad;
+       row += (long long)gridDim.x * 8) {
+    long long src = -1;
+    if (row < rows_out) {
+      src = gather[row];
+      if (src >= rows_in) src = -1;
+    }
+    if (row < rows_out) {
+      const uint4* s = reinterpret_cast<const uint4*>(codes_in + (src >= 0 ? src : 0) * (K / 2));
+      uint4* d = reinterpret_cast<uint4*>(codes_out + row * (K / 2));
+      for (long long v = lane; v < kv; v += 32) d[v] = src >= 0 ? __ldg(s + v) : make_uint4(0, 0, 0, 0);
+    }
+    const long long doff = (row / 128) * kc * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4;
+    const long long soff = (src / 128) * kc * 512 + (src % 32) * 16 + ((src % 128) / 32) * 4;
+    for (long long c = lane; c < kc; c += 32) {
+      const uint32_t w = src >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(sf_in + soff + c * 512)) : 0u;
+      *reinterpret_cast<uint32_t*>(sf_out + doff + c * 512) = w;
+    }
+  }
+}
+
+cudaError_t launch_fp4_gather_rows(const uint8_t* codes_in, const uint8_t* sf_in, long long rows_in, long long K,
+                                   const int* gather, long long rows_out, uint8_t* codes_out, uint8_t* sf_out,
+                                   cudaStream_t stream) {
+  const long long pad = (rows_out + 127) / 128 * 128;
+  long long blocks = (pad + 7) / 8;
+  const long long cap = (long long)sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  fp4_gather_rows_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes_in, sf_in, rows_in, K, gather, rows_out, pad,
+                                                                codes_out, sf_out);
+  return cudaGetLastError();
+}
+
+}  // namespace bsk

@@ -5,7 +5,9 @@ teardown (FP8 GEMM)", section 5.3):
 
   1. bs_moe_dispatch     group the (token, slot) pairs by expert into
                          128-aligned contiguous segments
-  2. q4_quantize         gather each routed token's row and quantize it online
+  2. q4_quantize         quantize each token's row once (online), then
+     bs_fp4_gather_rows  gather the quantized rows into the expert segments
+                         (bit-identical to quantizing the gathered rows)
   3. bs_grouped_gemm     gate/up GEMM per expert with the SwiGLU epilogue
                          h = bf16(silu(x W_gate^T) * (x W_up^T))
   4. q4_quantize         re-quantize h online
@@ -22,8 +24,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import (EPI_COMBINE, EPI_SWIGLU, grouped_gemm_fp4, moe_dispatch, moe_finalize, moe_rows_bound,
-               q4_quantize, sf_bytes)
+from . import (EPI_COMBINE, EPI_SWIGLU, fp4_gather_rows, grouped_gemm_fp4, moe_dispatch, moe_finalize,
+               moe_rows_bound, q4_quantize, sf_bytes)
 
 
 @dataclass
@@ -66,6 +68,8 @@ class MoELayer:
         self.T, self.k = T, k
         E, H, F = weights.E, weights.H, weights.F
         self.rows = moe_rows_bound(T, k, E)
+        self.tq = torch.empty((T, H // 2), dtype=torch.uint8, device=device)
+        self.ts = torch.empty(sf_bytes(T, H), dtype=torch.uint8, device=device)
         self.xq = torch.empty((self.rows, H // 2), dtype=torch.uint8, device=device)
         self.xs = torch.empty(sf_bytes(self.rows, H), dtype=torch.uint8, device=device)
         self.h = torch.zeros((self.rows, F), dtype=torch.bfloat16, device=device)
@@ -74,16 +78,16 @@ class MoELayer:
         self.out32 = torch.zeros((T, H), dtype=torch.float32, device=device)
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
         self.disp = None
-        self.workspace = None
+        from . import load
+        wsb = int(load().bs_moe_dispatch_workspace_bytes(T, k, E))
+        self.workspace = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
 
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor) -> torch.Tensor:
         w = self.w
         self.disp = moe_dispatch(topk_ids, topk_w, w.E, out=self.disp, workspace=self.workspace)
-        if self.workspace is None:
-            # keep the workspace moe_dispatch allocated for later calls
-            pass
         d = self.disp
-        q4_quantize(x, gather=d["token_of"], rows=self.rows, out=(self.xq, self.xs, None))
+        q4_quantize(x, out=(self.tq, self.ts, None))
+        fp4_gather_rows(self.tq, self.ts, w.H, d["token_of"], out=(self.xq, self.xs))
         grouped_gemm_fp4(self.xq, self.xs, w.wgu_codes, w.wgu_sf, K=w.H, N=w.F, E=w.E, offsets=d["offsets"],
                          counts=d["counts"], epilogue=EPI_SWIGLU, out=self.h)
         q4_quantize(self.h, out=(self.hq, self.hs, None))

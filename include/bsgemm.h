@@ -108,6 +108,25 @@ bs_status q4_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t 
                       const void *lora_a_t, int r, void *lora_t, bs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * bs_fp4_gather_rows -- gather rows of an FP4 matrix that q4_quantize already
+ * wrote: output row i = input row gather[i] (a negative or out-of-range index
+ * gives a zero row with zero scales), codes copied and each row's scales moved
+ * to the output row's place in the MMA scale layout.  Bit-identical to
+ * q4_quantize with the same gather on the unquantized rows, because the
+ * quantization is row-local; used to group MoE activations by expert
+ * ("DeepGEMM teardown", section 5.3) after quantizing each token once.
+ *
+ *   codes_in, sf_in  [rows_in, K/2] codes and bs_sf_bytes(rows_in, K) scales
+ *   gather           int32 [rows_out]
+ *   codes_out, sf_out [rows_out, K/2] and bs_sf_bytes(rows_out, K); padding
+ *                    rows of the last 128-row block get zero scales
+ *   K % 64 == 0, every pointer 16-byte aligned
+ * ------------------------------------------------------------------------- */
+bs_status bs_fp4_gather_rows(const uint8_t *codes_in, const uint8_t *sf_in, int64_t rows_in, int64_t K,
+                             const int32_t *gather, int64_t rows_out, uint8_t *codes_out, uint8_t *sf_out,
+                             bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * q8_quantize -- FP8 e4m3 quantization with fp32 block scales ("DeepGEMM
  * teardown", section 2.2 per-token / per-block scaling, section 5.2 scale =
  * max_val / 448).  For every block (1 x 128 in BS_Q8_TOKEN_1x128 mode,

@@ -61,6 +61,19 @@ def test_q4_quantize_gather(cuda_lib):
     assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), 8, 256), os_)
 
 
+@pytest.mark.parametrize("rows_in,rows_out,K", [(50, 8, 256), (4096, 1000, 4096), (7, 300, 64)])
+def test_fp4_gather_rows_equals_quantize_with_gather(cuda_lib, rows_in, rows_out, K):
+    bs = cuda_lib
+    g = torch.Generator().manual_seed(rows_in + rows_out)
+    x = special_rows(torch.randn(rows_in, K, generator=g)).to(torch.bfloat16).cuda()
+    idx = torch.randint(-1, rows_in, (rows_out,), generator=g, dtype=torch.int32).cuda()
+    c, s, _ = bs.q4_quantize(x)
+    gc, gs = bs.fp4_gather_rows(c, s, K, idx)
+    rc, rs, _ = bs.q4_quantize(x, gather=idx)
+    torch.cuda.synchronize()
+    assert torch.equal(gc, rc) and torch.equal(gs, rs)
+
+
 def test_q4_quantize_full_size_activation(cuda_lib):
     """The 8192 x 8192 bf16 activation of the dense low-rank workload, every row."""
     bs = cuda_lib
@@ -73,18 +86,42 @@ def test_q4_quantize_full_size_activation(cuda_lib):
     assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), 8192, 8192)[rows], os_)
 
 
-def test_q4_lowrank_left_factor(cuda_lib):
+@pytest.mark.parametrize("M,K", [(200, 1024), (130, 320), (64, 8192)])
+def test_q4_lowrank_left_factor(cuda_lib, M, K):
+    """Codes, scales and T = X A from one call (fused pass when K % 256 == 0,
+    separate kernels otherwise)."""
     bs = cuda_lib
-    d = workloads.dense_lowrank(M=200, N=256, K=1024)
+    d = workloads.dense_lowrank(M=M, N=256, K=K)
     x, a = d["x"], d["lora_a"]
-    _, _, lt = bs.q4_quantize(x.cuda(), lora_a_t=a.t().contiguous().cuda())
+    codes, sf, lt = bs.q4_quantize(x.cuda(), lora_a_t=a.t().contiguous().cuda())
     torch.cuda.synchronize()
+    oc, os_ = oracle.q4_quantize(x)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    sfn = sf.cpu().numpy()
+    assert np.array_equal(sf_rowmajor(sfn, M, K), os_)
+    Mpad = (M + 127) // 128 * 128
+    assert np.all(sf_rowmajor(sfn, Mpad, K)[M:] == 0)
     t = lt.float().cpu().numpy().astype(np.float64)
     t_gpu = t[:, :32] + t[:, 32:]
     t_ref = oracle.lowrank_t(x, a)
     mag = np.abs(x.float().numpy().astype(np.float64)) @ np.abs(a.float().numpy().astype(np.float64))
     assert np.all(np.abs(t_gpu - t_ref) <= 1e-5 * mag + 2.0 ** -16 * np.abs(t_ref))
     assert np.all(t[:, 32:] == (t_gpu - t[:, :32]))  # lo is the bf16 remainder
+
+
+def test_q4_lowrank_gather(cuda_lib):
+    bs = cuda_lib
+    d = workloads.dense_lowrank(M=40, N=256, K=512)
+    x, a = d["x"], d["lora_a"]
+    gather = torch.tensor([5, -1, 39, 0, 5] * 30, dtype=torch.int32)
+    codes, sf, lt = bs.q4_quantize(x.cuda(), gather=gather.cuda(), lora_a_t=a.t().contiguous().cuda())
+    rows = torch.stack([x[i] if i >= 0 else torch.zeros(512, dtype=x.dtype) for i in gather.tolist()])
+    oc, os_ = oracle.q4_quantize(rows)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), len(gather), 512), os_)
+    t = lt.float().cpu().numpy().astype(np.float64)
+    t_ref = oracle.lowrank_t(rows, a)
+    assert np.allclose(t[:, :32] + t[:, 32:], t_ref, rtol=1e-4, atol=1e-4)
 
 
 @pytest.mark.parametrize("M,K,dtype", [(1, 4096, torch.bfloat16), (16, 4096, torch.bfloat16),
