@@ -240,9 +240,18 @@ static int fp4_bk() {
   return bk;
 }
 
-static bs_status fp4_maps(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows) {
+// FP4 GEMM on CTA pairs (cta_group::2): BSGEMM_FP4_PAIR=1 selects it.
+static bool fp4_pair() {
+  static bool on = [] {
+    const char* e = getenv("BSGEMM_FP4_PAIR");
+    return e && atoi(e) == 1;
+  }();
+  return on;
+}
+
+static bs_status fp4_maps(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int bk) {
   const uint64_t kb = (uint64_t)a->K / 2;
-  L.bk = fp4_bk();
+  L.bk = bk;
   const uint32_t box = (uint32_t)L.bk / 2;
   const CUtensorMapSwizzle sw = L.bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   bs_status st = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, kb, (uint64_t)a->M, kb, box, 128, sw);
@@ -260,6 +269,41 @@ static bs_status fp4_maps(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_ro
     memset(&L.tmT, 0, sizeof L.tmT);
     memset(&L.tmL, 0, sizeof L.tmL);
   }
+  return BS_OK;
+}
+
+// Scale tensors as uint32 rows: one row per 128-row block, K/64 tiles of 512
+// bytes each; a pair-kernel stage loads two tiles (256 words).
+static bs_status sf_map(CUtensorMap* m, const void* sf, int64_t rows, int64_t K) {
+  const uint64_t words = (uint64_t)(K / 64) * 128;
+  const uint64_t blocks = (uint64_t)((rows + 127) / 128);
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, sf, words, blocks, words * 4, 256, 1,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int sms, cudaStream_t s,
+                            long long pair_tiles, bool grouped) {
+  bs_status st;
+  if (fp4_pair()) {
+    bsk::Fp4PairLaunch P;
+    memset(&P, 0, sizeof P);
+    st = fp4_maps(L, a, b_rows, 128);
+    if (st != BS_OK) return st;
+    st = sf_map(&P.tmSfa, a->sfa, a->M, a->K);
+    if (st != BS_OK) return st;
+    st = sf_map(&P.tmSfb, a->sfb, b_rows, a->K);
+    if (st != BS_OK) return st;
+    P.base = L;
+    const int pairs = sms / 2;
+    P.grid = 2 * (int)(grouped ? pairs : (pair_tiles < pairs ? pair_tiles : pairs));
+    cudaError_t e = bsk::launch_fp4_pair_gemm(P, s);
+    if (e != cudaSuccess) return cuda_fail(e, "FP4 pair GEMM launch");
+    return BS_OK;
+  }
+  st = fp4_maps(L, a, b_rows, fp4_bk());
+  if (st != BS_OK) return st;
+  cudaError_t e = bsk::launch_fp4_gemm(L, s);
+  if (e != cudaSuccess) return cuda_fail(e, "FP4 GEMM launch");
   return BS_OK;
 }
 
@@ -283,8 +327,6 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     if (a->M == 0) return BS_OK;
     bsk::Fp4Launch L;
     memset(&L, 0, sizeof L);
-    st = fp4_maps(L, a, a->N);
-    if (st != BS_OK) return st;
     L.p.sfa = static_cast<const uint8_t*>(a->sfa);
     L.p.sfb = static_cast<const uint8_t*>(a->sfb);
     L.p.M = (int)a->M;
@@ -302,9 +344,8 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     L.epilogue = bsk::kEpiStore;
     const long long tiles = ((a->M + 127) / 128) * ((a->N + 255) / 256);
     L.grid = (int)(tiles < sms ? tiles : sms);
-    cudaError_t e = bsk::launch_fp4_gemm(L, s);
-    if (e != cudaSuccess) return cuda_fail(e, "FP4 GEMM launch");
-    return BS_OK;
+    const long long pair_tiles = ((a->M + 255) / 256) * ((a->N + 255) / 256);
+    return launch_fp4(L, a, a->N, sms, s, pair_tiles, false);
   }
   if (a->fmt == BS_FMT_FP8) {
     if (a->K % 128) return fail(BS_ERR_ALIGN, "FP8: K=%lld not a multiple of 128", (long long)a->K);
@@ -370,8 +411,6 @@ bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, 
   if (a->M == 0) return BS_OK;
   bsk::Fp4Launch L;
   memset(&L, 0, sizeof L);
-  st = fp4_maps(L, a, wrows);
-  if (st != BS_OK) return st;
   L.p.sfa = static_cast<const uint8_t*>(a->sfa);
   L.p.sfb = static_cast<const uint8_t*>(a->sfb);
   L.p.M = (int)a->M;
@@ -392,9 +431,7 @@ bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, 
   L.lora = false;
   L.epilogue = epilogue;
   L.grid = sms;
-  cudaError_t e = bsk::launch_fp4_gemm(L, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "grouped FP4 GEMM launch");
-  return BS_OK;
+  return launch_fp4(L, a, wrows, sms, reinterpret_cast<cudaStream_t>(stream), 0, true);
 }
 
 int64_t bs_moe_rows_bound(int64_t T, int k, int E) {

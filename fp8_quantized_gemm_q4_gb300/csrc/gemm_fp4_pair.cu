@@ -1,0 +1,489 @@
+// gemm_fp4_pair.cu -- block-scaled FP4 GEMM on CTA pairs (tcgen05 cta_group::2).
+//
+// "Warp-specialised W4A4 kernel on the newest GPU architecture", sections 4-6:
+// two CTAs form a pair that shares one 256 x 256 MMA; switching the MMA mode
+// alone gains nothing (section 4, 27 % -> 28 %): the data and sync flows are
+// split per CTA, and the shared-memory budget counts per CTA what each CTA
+// actually holds (section 6: the up-projection block of the low-rank branch
+// is split across the pair, not replicated).
+//
+// Per CTA of a pair (cluster of 2), per K stage of 128 FP4 elements:
+//   A      its own 128 rows                     8 KB  (64B swizzle)
+//   B      its own half (128 rows) of the 256   8 KB
+//   SFA    scales of its own rows               1 KB
+//   SFB    scales of all 256 B rows             2 KB  (replicated: each CTA's
+//          tensor core multiplies its rows by all 256 columns)
+// so a stage is 19 KB instead of 27 KB, and 10-11 stages fit.
+//
+// The leader CTA (rank 0) issues every tcgen05.mma / tcgen05.cp with
+// cta_group::2; the operands of the peer live at the same shared-memory
+// offsets in the peer.  Both CTAs' TMA loads signal the leader's "full"
+// barrier (the leader expects the bytes of both); the leader's commits
+// multicast to both CTAs' "empty" / "acc_full" barriers; both CTAs' epilogue
+// warps arrive on the leader's "acc_empty".  Each CTA's tensor memory holds
+// the fp32 accumulator of its own 128 rows x 256 columns.
+#include "budget.hpp"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bsk {
+namespace fp4pair {
+
+constexpr int BM = 128;        // rows per CTA (the pair covers 256)
+constexpr int BN = 256;        // MMA N; each CTA holds BN / 2 rows of B
+constexpr int BK = 128;        // K per stage
+constexpr int kRowBytes = BK / 2;
+constexpr int kSbo = 8 * kRowBytes;
+constexpr int kMmas = BK / 64;
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kMaxExperts = 1024;
+constexpr int kMisc = 2048 + (kMaxExperts + 1) * 4 + 1024;
+
+constexpr int kOffA = 0;
+constexpr int kOffB = BM * kRowBytes;                    // 8192
+constexpr int kOffSfa = kOffB + (BN / 2) * kRowBytes;    // 16384
+constexpr int kOffSfb = kOffSfa + kMmas * 512;           // 17408
+constexpr int kStageBytes = kOffSfb + 2 * kMmas * 512;   // 19456
+constexpr int kStageTx = kStageBytes;                    // bytes one CTA's loads deliver per stage
+
+constexpr Fp4TileShape kShapeLora{BM, BN, BK, 2, true, 32, kMisc};
+constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 2, false, 32, kMisc};
+static_assert(kStageBytes == fp4_stage_bytes(kShapeNoLora), "per-CTA stage layout matches the budget");
+static_assert(kStageBytes % kAlign == 0, "stage alignment");
+// low-rank slot per CTA: T hi / T lo of its own rows, its half of Bl^T
+constexpr int kLoraThi = 0, kLoraTlo = 8192, kLoraBl = 16384, kLoraBytes = 24576;
+static_assert(kLoraBytes == fp4_lora_bytes(kShapeLora), "low-rank slot: the up-projection block is split per CTA");
+constexpr int kStagesLora = fp4_main_stages(kShapeLora) < 16 ? fp4_main_stages(kShapeLora) : 16;
+constexpr int kStagesNoLora = fp4_main_stages(kShapeNoLora) < 16 ? fp4_main_stages(kShapeNoLora) : 16;
+static_assert(fp4_smem_total(kShapeLora, kStagesLora) + kAlign <= kSmemPerCta, "lora smem");
+static_assert(fp4_smem_total(kShapeNoLora, kStagesNoLora) + kAlign <= kSmemPerCta, "smem");
+
+constexpr int kSfBuffers = 2;
+constexpr int kTmemAcc = 0;
+constexpr int kTmemSf = BN;
+constexpr int kSfColsPerMma = 4 + BN / 32;
+constexpr int kSfColsPerStage = kMmas * kSfColsPerMma;
+static_assert(fp4_tmem_cols(kShapeLora, 1, kSfBuffers) <= kTmemCols, "tmem budget");
+constexpr int kTmemAlloc = pow2_cols(fp4_tmem_cols(kShapeLora, 1, kSfBuffers));
+
+constexpr uint32_t kIdescMain = idesc_mxf4nvf4(2 * BM, BN);
+constexpr uint32_t kIdescLora = idesc_bf16(2 * BM, BN);
+
+struct Tile {
+  int row0;      // first A row of the pair (this CTA's rows start at row0 + rank * 128)
+  int rows;      // valid rows of the pair tile (<= 256)
+  int brow0;     // first B row of accumulator columns [0, 128)   (leader's half)
+  int brow1;     // first B row of accumulator columns [128, 256) (peer's half)
+  int sfb_blk1;  // scale block of brow1 (valid even when brow1 is past the weights)
+  int col0;      // first output column
+};
+
+template <int kEpi>
+__device__ __forceinline__ int n_blocks(const Fp4Params& p) {
+  return kEpi == kEpiSwiglu ? p.N / 128 : (p.N + BN - 1) / BN;
+}
+
+template <int kEpi>
+__device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, int t) {
+  Tile tl;
+  if (p.E == 0) {
+    const int num_m = (p.M + 2 * BM - 1) / (2 * BM);
+    const int mb = t % num_m, nb = t / num_m;
+    tl.row0 = mb * 2 * BM;
+    tl.rows = min(2 * BM, p.M - tl.row0);
+    tl.col0 = nb * BN;
+    tl.brow0 = nb * BN;
+    tl.brow1 = tl.brow0 + 128;
+    tl.sfb_blk1 = (tl.brow1 < p.N) ? tl.brow1 / 128 : tl.brow0 / 128;
+    return tl;
+  }
+  int lo = 0, hi = p.E - 1;  // largest e with prefix[e] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int cnt = p.counts[e];
+  const int mblk = (cnt + 2 * BM - 1) / (2 * BM);
+  const int local = t - prefix[e];
+  const int nb = local / mblk, mb = local % mblk;
+  tl.row0 = p.offsets[e] + mb * 2 * BM;
+  tl.rows = min(2 * BM, cnt - mb * 2 * BM);
+  const int64_t wrows = (kEpi == kEpiSwiglu) ? 2LL * p.N : (int64_t)p.N;
+  if (kEpi == kEpiSwiglu) {
+    tl.col0 = nb * 128;
+    tl.brow0 = (int)(e * wrows + nb * 128);
+    tl.brow1 = (int)(e * wrows + p.N + nb * 128);
+    tl.sfb_blk1 = tl.brow1 / 128;
+  } else {
+    tl.col0 = nb * BN;
+    tl.brow0 = (int)(e * wrows + nb * BN);
+    tl.brow1 = tl.brow0 + 128;
+    tl.sfb_blk1 = (nb * BN + 128 < p.N) ? tl.brow1 / 128 : tl.brow0 / 128;
+  }
+  return tl;
+}
+
+template <int kStages, bool kLora, int kEpi>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmL,
+                    const __grid_constant__ CUtensorMap tmSfa, const __grid_constant__ CUtensorMap tmSfb,
+                    const Fp4Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kAlign - 1) &
+                                             ~static_cast<uintptr_t>(kAlign - 1));
+  uint8_t* stages = base;
+  uint8_t* lora = base + kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(lora + (kLora ? kLoraBytes : 0));
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* lora_full = acc_full + 2;
+  uint64_t* lora_empty = acc_full + 3;
+  uint64_t* drain = acc_full + 4;
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(acc_full + 5);
+  int* abort_i = reinterpret_cast<int*>(tmem_base + 1);
+  int* total_tiles = abort_i + 1;
+  int* prefix = total_tiles + 2;
+  volatile int* abort_flag = abort_i;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 16);  // 8 epilogue warps in each CTA of the pair
+    mbar_init(lora_full, 1);
+    mbar_init(lora_empty, 1);
+    mbar_init(drain, 1);
+    *abort_i = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSfa);
+    prefetch_tmap(&tmSfb);
+    if (kLora) {
+      prefetch_tmap(&tmT);
+      prefetch_tmap(&tmL);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_base, kTmemAlloc);
+    tmem_relinquish_pair();
+  }
+  if (warp == 3) {
+    if (p.E == 0) {
+      if (lane == 0) *total_tiles = ((p.M + 2 * BM - 1) / (2 * BM)) * ((p.N + BN - 1) / BN);
+    } else {
+      const int nb = n_blocks<kEpi>(p);
+      int running = 0;
+      bool bad = false;
+      for (int e0 = 0; e0 < p.E; e0 += 32) {
+        const int e = e0 + lane;
+        int tiles = 0;
+        if (e < p.E) {
+          const int off = p.offsets[e], cnt = p.counts[e], nxt = p.offsets[e + 1];
+          if (cnt < 0 || (off % BM) != 0 || off + cnt > nxt || nxt > p.M) bad = true;
+          tiles = ((max(cnt, 0) + 2 * BM - 1) / (2 * BM)) * nb;
+        }
+        int incl = tiles;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += v;
+        }
+        if (e < p.E) prefix[e] = running + incl - tiles;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      bad = __any_sync(0xffffffffu, bad) || p.offsets[0] != 0;
+      if (lane == 0) {
+        prefix[p.E] = running;
+        *total_tiles = bad ? 0 : running;
+        if (bad && blockIdx.x == 0) record_status(p.status, kStatusOffsets, 3);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either signals the other
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base;
+  const int total = *total_tiles;
+  const int kchunks = p.K / 64;
+  const int kstages = (kchunks + kMmas - 1) / kMmas;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    PipeState<kStages> ps;
+    uint32_t issued_mask = 0, last_phase = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs) {
+      const Tile tl = tile_of<kEpi>(p, prefix, t);
+      const int my_row0 = tl.row0 + (int)rank * BM;
+      const int my_brow = leader ? tl.brow0 : tl.brow1;
+      for (int ks = 0; ks < kstages; ++ks) {
+        if (!mbar_wait(&empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 110)) { ok = false; break; }
+        uint8_t* st = stages + ps.index * kStageBytes;
+        if (leader) mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(2 * kStageTx));
+        const uint32_t bar = mapa_shared(smem_u32(&full[ps.index]), 0);
+        tma_load_2d_pair(st + kOffA, &tmA, bar, ks * kRowBytes, my_row0);
+        tma_load_2d_pair(st + kOffB, &tmB, bar, ks * kRowBytes, my_brow);
+        tma_load_2d_pair(st + kOffSfa, &tmSfa, bar, ks * kMmas * 128, my_row0 / 128);
+        tma_load_2d_pair(st + kOffSfb, &tmSfb, bar, ks * kMmas * 128, tl.brow0 / 128);
+        tma_load_2d_pair(st + kOffSfb + kMmas * 512, &tmSfb, bar, ks * kMmas * 128, tl.sfb_blk1);
+        issued_mask |= 1u << ps.index;
+        last_phase = (last_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
+        ps.advance();
+      }
+    }
+    if (*abort_flag && leader) {
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(&full[s], (last_phase >> s) & 1u) && globaltimer() - t0 < 100000000ull) {
+          }
+        }
+    }
+  } else if (warp == 2 && lane == 0) {
+    // ------------------------------------------------------------------ low-rank producer (both CTAs)
+    if (kLora) {
+      uint32_t phase = 0;
+      for (int t = pair; t < total; t += npairs) {
+        const Tile tl = tile_of<kEpi>(p, prefix, t);
+        if (!mbar_wait(lora_empty, phase ^ 1u, abort_flag, p.status, 120)) break;
+        if (leader) mbar_arrive_expect_tx(lora_full, (uint32_t)(2 * kLoraBytes));
+        const uint32_t bar = mapa_shared(smem_u32(lora_full), 0);
+        const int my_row0 = tl.row0 + (int)rank * BM;
+        tma_load_2d_pair(lora + kLoraThi, &tmT, bar, 0, my_row0);
+        tma_load_2d_pair(lora + kLoraTlo, &tmT, bar, 32, my_row0);
+        tma_load_2d_pair(lora + kLoraBl, &tmL, bar, 0, leader ? tl.brow0 : tl.brow1);
+        phase ^= 1u;
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------------ MMA issuer (leader only)
+    PipeState<kStages> ps;
+    uint32_t acc_phase = 0, lora_phase = 0, sf_buf = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs) {
+      if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status, 130)) break;
+      tc_fence_after();
+      for (int ks = 0; ks < kstages; ++ks) {
+        if (!mbar_wait(&full[ps.index], ps.phase, abort_flag, p.status, 131)) { ok = false; break; }
+        tc_fence_after();
+        const int nmma = min(kMmas, kchunks - kMmas * ks);
+        uint8_t* st = stages + ps.index * kStageBytes;
+        const uint32_t sa = smem_u32(st + kOffA), sb = smem_u32(st + kOffB);
+        const uint32_t ssfa = smem_u32(st + kOffSfa), ssfb = smem_u32(st + kOffSfb);
+        const uint32_t sf_col = kTmemSf + sf_buf * kSfColsPerStage;
+        for (int j = 0; j < nmma; ++j) {
+          const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
+          tc_cp_32x128b_warpx4_pair(col, smem_desc(ssfa + 512 * j, 0, 128, kLayoutNone));
+          tc_cp_32x128b_warpx4_pair(col + 4, smem_desc(ssfb + 512 * j, 0, 128, kLayoutNone));
+          tc_cp_32x128b_warpx4_pair(col + 8, smem_desc(ssfb + kMmas * 512 + 512 * j, 0, 128, kLayoutNone));
+        }
+        for (int j = 0; j < nmma; ++j) {
+          const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
+          mma_mxf4nvf4_pair(tmem + kTmemAcc, smem_desc(sa + 32 * j, 16, kSbo, kLayoutSw64),
+                            smem_desc(sb + 32 * j, 16, kSbo, kLayoutSw64), kIdescMain, col, col + 4,
+                            (ks > 0 || j > 0) ? 1u : 0u);
+        }
+        tc_commit_pair_multicast(&empty[ps.index], 0x3);
+        sf_buf ^= 1u;
+        ps.advance();
+      }
+      if (!ok) break;
+      if (kLora) {
+        if (!mbar_wait(lora_full, lora_phase, abort_flag, p.status, 132)) break;
+        tc_fence_after();
+        const uint32_t thi = smem_u32(lora + kLoraThi), tlo = smem_u32(lora + kLoraTlo);
+        const uint32_t bl = smem_u32(lora + kLoraBl);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t ta = part == 0 ? thi : tlo;
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            mma_bf16_pair(tmem + kTmemAcc, smem_desc(ta + 32 * kk, 16, 512, kLayoutSw64),
+                          smem_desc(bl + 32 * kk, 16, 512, kLayoutSw64), kIdescLora, 1u);
+        }
+        tc_commit_pair_multicast(lora_empty, 0x3);
+        lora_phase ^= 1u;
+      }
+      tc_commit_pair_multicast(acc_full, 0x3);
+      acc_phase ^= 1u;
+    }
+    tc_commit_pair_local(drain);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 1000000000ull) {
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------------ epilogue (both CTAs, own rows)
+    const int q = warp % 4;
+    const int half = (warp - kEpiWarp0) / 4;
+    const int r_in_tile = (int)rank * BM + q * 32 + lane;  // row within the pair tile
+    const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
+    uint32_t acc_phase = 0;
+    for (int t = pair; t < total; t += npairs) {
+      const Tile tl = tile_of<kEpi>(p, prefix, t);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(acc_full, acc_phase, abort_flag, p.status, 140) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[4][32];
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      if (kEpi == kEpiSwiglu) {
+        tmem_ld32(lane_base + kTmemAcc + 64 * half, v[0]);
+        tmem_ld32(lane_base + kTmemAcc + 64 * half + 32, v[1]);
+        tmem_ld32(lane_base + kTmemAcc + 128 + 64 * half, v[2]);
+        tmem_ld32(lane_base + kTmemAcc + 128 + 64 * half + 32, v[3]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + kTmemAcc + 128 * half + 32 * c, v[c]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+      acc_phase ^= 1u;
+
+      const bool row_ok = r_in_tile < tl.rows;
+      const int64_t row = (int64_t)tl.row0 + r_in_tile;
+      if (kEpi == kEpiSwiglu) {
+        // padding rows of the segment inside the pair tile are written as zeros
+        const int col = tl.col0 + 64 * half;
+        const bool in_buf = row < p.M;
+        if (in_buf) {
+          uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * p.ldo + col;
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float hv[2];
+#pragma unroll
+              for (int k2 = 0; k2 < 2; ++k2) {
+                const int cc = c + 2 * i + k2;
+                const float g = __uint_as_float(v[cc / 32][cc % 32]);
+                const float u = __uint_as_float(v[2 + cc / 32][cc % 32]);
+                hv[k2] = row_ok ? (g / (1.0f + __expf(-g))) * u : 0.0f;
+              }
+              w[i] = pack_bf16x2(hv[0], hv[1]);
+            }
+            if (row_ok || r_in_tile < ((tl.rows + 127) / 128) * 128)
+              *reinterpret_cast<uint4*>(out + c) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      } else if (kEpi == kEpiCombine) {
+        const int col = tl.col0 + 128 * half;
+        if (row_ok && col < p.N) {
+          const int tok = p.token_of[row];
+          const float wt = p.weight_of[row];
+          if (tok >= 0) {
+            float* dst = p.out32 + (int64_t)tok * p.ld_out32 + col;
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+              const float a0 = wt * __uint_as_float(v[c / 32][c % 32]);
+              const float a1 = wt * __uint_as_float(v[c / 32][c % 32 + 1]);
+              const float a2 = wt * __uint_as_float(v[c / 32][c % 32 + 2]);
+              const float a3 = wt * __uint_as_float(v[c / 32][c % 32 + 3]);
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c), "f"(a0), "f"(a1),
+                           "f"(a2), "f"(a3)
+                           : "memory");
+            }
+          }
+        }
+      } else {
+        const int col = tl.col0 + 128 * half;
+        if (row_ok && col < p.N) {
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int n = col + c + i;
+              float a = __uint_as_float(v[(c + i) / 32][(c + i) % 32]);
+              float sc = p.alpha;
+              if (p.col_scale) sc *= p.col_scale[n];
+              a *= sc;
+              if (p.bias) a += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.bias)[n]);
+              y[i] = a;
+            }
+            if (p.out_bf16) {
+              uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * p.ldo + col + c;
+              *reinterpret_cast<uint4*>(out) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                          pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+            } else {
+              float* out = reinterpret_cast<float*>(p.out) + row * p.ldo + col + c;
+              *reinterpret_cast<float4*>(out) = make_float4(y[0], y[1], y[2], y[3]);
+              *reinterpret_cast<float4*>(out + 4) = make_float4(y[4], y[5], y[6], y[7]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA frees tensor memory or exits while the pair may still touch it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemAlloc);
+  }
+}
+
+template <bool kLora, int kEpi>
+static cudaError_t launch_one(const Fp4PairLaunch& L, cudaStream_t stream) {
+  constexpr int kStages = kLora ? kStagesLora : kStagesNoLora;
+  auto kern = fp4_pair_kernel<kStages, kLora, kEpi>;
+  const int smem = fp4_smem_total(kLora ? kShapeLora : kShapeNoLora, kStages) + kAlign;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)L.grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, L.base.tmA, L.base.tmB, L.base.tmT, L.base.tmL, L.tmSfa, L.tmSfb, L.base.p);
+}
+
+}  // namespace fp4pair
+
+cudaError_t launch_fp4_pair_gemm(const Fp4PairLaunch& L, cudaStream_t stream) {
+  using namespace fp4pair;
+  if (L.grid <= 0 || (L.grid & 1)) return cudaErrorInvalidValue;
+  if (L.base.lora) {
+    if (L.base.epilogue != kEpiStore) return cudaErrorInvalidValue;
+    return launch_one<true, kEpiStore>(L, stream);
+  }
+  switch (L.base.epilogue) {
+    case kEpiStore: return launch_one<false, kEpiStore>(L, stream);
+    case kEpiSwiglu: return launch_one<false, kEpiSwiglu>(L, stream);
+    case kEpiCombine: return launch_one<false, kEpiCombine>(L, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int fp4_pair_stages(bool lora) { return lora ? fp4pair::kStagesLora : fp4pair::kStagesNoLora; }
+
+}  // namespace bsk

@@ -36,12 +36,16 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kMisc = 2048;
 constexpr int kMaxStages = 12;
 
+constexpr int KBC = 32;   // K blocks whose scales are staged together
+
 template <int TN>
 struct Cfg {
   static constexpr int kStageBytes = round_up(BM * BK + TN * BK, kAlign);
-  static constexpr Fp8TileShape kShape{BM, TN, BK, kMisc};
+  // two staging buffers of [KBC][TN] activation scales + [KBC] weight scales
+  static constexpr int kScaleBytes = round_up(2 * (KBC * TN + KBC) * 4, kAlign);
+  static constexpr Fp8TileShape kShape{BM, TN, BK, kMisc + kScaleBytes + kAlign};
   static constexpr int kStages = fp8_main_stages(kShape) < kMaxStages ? fp8_main_stages(kShape) : kMaxStages;
-  static constexpr int kSmem = kStages * kStageBytes + kMisc + kAlign;
+  static constexpr int kSmem = kStages * kStageBytes + kScaleBytes + kMisc + kAlign;
   static constexpr int kTmemCols = pow2_cols(2 * TN);
   static constexpr int kColsPerWarp = TN / 2;
   static_assert(kStages >= 2, "ring too shallow");
@@ -58,7 +62,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kAlign - 1) &
                                              ~static_cast<uintptr_t>(kAlign - 1));
   uint8_t* stages = base;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kStages * C::kStageBytes);
+  float* ssa = reinterpret_cast<float*>(base + C::kStages * C::kStageBytes);  // [2][KBC][TN]
+  float* ssb = ssa + 2 * KBC * TN;                                            // [2][KBC]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kStages * C::kStageBytes + C::kScaleBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::kStages;
   uint64_t* pfull = bars + 2 * C::kStages;     // [2] partial slot written by the tensor core
@@ -157,62 +163,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ promotion + epilogue
+    // Walks (tile, chunk of KBC K blocks) in order.  The scales of the next
+    // chunk are staged into shared memory with cp.async while this chunk is
+    // promoted, so no K block waits on a global load.  Every epilogue warp runs
+    // the same sequence of named barriers; after an abort the warps keep
+    // walking (skipping the waits and the work) so the barriers still match.
     constexpr int NC = C::kColsPerWarp;
     const int q = warp % 4, half = (warp - kEpiWarp0) / 4;
     const int col0 = half * NC;
+    const int etid = threadIdx.x - kEpiWarp0 * 32;  // 0 .. 255
+    const int nchunk = (nkb + KBC - 1) / KBC;
     uint32_t slot = 0, slot_phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    auto stage_scales = [&](int t, int c, int buf) {
+      const int wb = t % n_wblk, tb = t / n_wblk;
+      float* da = ssa + buf * KBC * TN;
+      float* db = ssb + buf * KBC;
+      for (int i = etid; i < KBC * TN; i += 256) {
+        const int kbl = i / TN, m = i % TN;
+        const int kb = c * KBC + kbl, ma = tb * TN + m;
+        const bool valid = kb < nkb && ma < p.M;
+        const float* src = valid ? p.sfa + (size_t)kb * p.M + ma : p.sfa;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(da + i)), "l"(src),
+                     "r"(valid ? 4 : 0)
+                     : "memory");
+      }
+      for (int i = etid; i < KBC; i += 256) {
+        const int kb = c * KBC + i;
+        const bool valid = kb < nkb;
+        const float* src = valid ? p.sfb + (size_t)wb * nkb + kb : p.sfb;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(db + i)), "l"(src),
+                     "r"(valid ? 4 : 0)
+                     : "memory");
+      }
+    };
+    int t = blockIdx.x, c = 0, qi = 0;
+    if (t < total) stage_scales(t, 0, 0);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    float acc[NC];
+#pragma unroll
+    for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
+    while (t < total) {
+      int tn = t, cn = c + 1;
+      if (cn == nchunk) {
+        cn = 0;
+        tn = t + gridDim.x;
+      }
+      if (tn < total) stage_scales(tn, cn, (qi + 1) & 1);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const float* csa = ssa + (qi & 1) * KBC * TN;
+      const float* csb = ssb + (qi & 1) * KBC;
       const int wb = t % n_wblk, tb = t / n_wblk;
       const int n = wb * BM + q * 32 + lane;            // weight row = output column
       const int m0 = tb * TN + col0;                    // first token of this warp's columns
-      float acc[NC];
+      const int kb_end = min(nkb, (c + 1) * KBC);
+      for (int kb = c * KBC; kb < kb_end; ++kb) {
+        if (ok) {
+          int w_ok = 1;
+          if (lane == 0) w_ok = mbar_wait(&pfull[slot], slot_phase, abort_flag, p.status, 70) ? 1 : 0;
+          w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+          ok = w_ok != 0;
+        }
+        if (ok) {
+          tc_fence_after();
+          const float sbv = csb[kb - c * KBC];
+          const float* sa_row = csa + (kb - c * KBC) * TN + col0;
+          constexpr int CH = NC < 32 ? NC : 32;
 #pragma unroll
-      for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
-      for (int kb = 0; kb < nkb; ++kb) {
-        int w_ok = 1;
-        if (lane == 0) w_ok = mbar_wait(&pfull[slot], slot_phase, abort_flag, p.status, 70) ? 1 : 0;
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-        if (!w_ok) { ok = false; break; }
-        tc_fence_after();
-        const float sbv = (n < p.N) ? __ldg(p.sfb + (size_t)wb * nkb + kb) : 0.0f;
-        const float* sa_row = p.sfa + (size_t)kb * p.M;
-        constexpr int CH = NC < 32 ? NC : 32;
+          for (int c0 = 0; c0 < NC; c0 += CH) {
+            uint32_t v[CH];
+            tmem_ld_cols<CH>(tmem + ((uint32_t)(q * 32) << 16) + slot * TN + col0 + c0, v);
+            tmem_ld_wait();
+            if (c0 + CH == NC) {
+              // every column of the slot is in registers: hand the slot back
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&pempty[slot]);
+            }
 #pragma unroll
-        for (int c0 = 0; c0 < NC; c0 += CH) {
-          uint32_t v[CH];
-          tmem_ld_cols<CH>(tmem + ((uint32_t)(q * 32) << 16) + slot * TN + col0 + c0, v);
-          tmem_ld_wait();
-          if (c0 + CH == NC) {
-            // every column of the slot is in registers: hand the slot back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pempty[slot]);
-          }
-#pragma unroll
-          for (int i = 0; i < CH; ++i) {
-            const int m = m0 + c0 + i;
-            const float sav = (m < p.M) ? __ldg(sa_row + m) : 0.0f;
-            acc[c0 + i] = fmaf(__uint_as_float(v[i]), sbv * sav, acc[c0 + i]);
+            for (int i = 0; i < CH; ++i) acc[c0 + i] = fmaf(__uint_as_float(v[i]), sbv * sa_row[c0 + i], acc[c0 + i]);
           }
         }
         slot ^= 1u;
         if (slot == 0) slot_phase ^= 1u;
       }
-      if (!ok) break;
-      if (n < p.N) {
+      if (cn == 0) {
+        // the tile's last chunk: write it and reset the accumulators
+        if (ok && n < p.N) {
 #pragma unroll
-        for (int i = 0; i < NC; ++i) {
-          const int m = m0 + i;
-          if (m < p.M) {
-            if (p.out_bf16)
-              reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(acc[i]);
-            else
-              reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + n] = acc[i];
+          for (int i = 0; i < NC; ++i) {
+            const int m = m0 + i;
+            if (m < p.M) {
+              if (p.out_bf16)
+                reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(acc[i]);
+              else
+                reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + n] = acc[i];
+            }
           }
         }
+#pragma unroll
+        for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
       }
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // this buffer may be refilled next iteration
+      t = tn;
+      c = cn;
+      ++qi;
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
   }
 
   __syncwarp();

@@ -42,6 +42,16 @@ struct Fp4Launch {
 cudaError_t launch_fp4_gemm(const Fp4Launch& L, cudaStream_t stream);
 int fp4_stages(bool lora, int bk);
 
+// CTA-pair (cta_group::2) variant: K stages of 128, scales through TMA maps
+// (uint32 view of the MMA scale layout, one row per 128-row block).
+struct Fp4PairLaunch {
+  Fp4Launch base;         // tmA/tmB built for 128-element stages; base.grid unused
+  CUtensorMap tmSfa, tmSfb;
+  int grid;               // even: two CTAs per cluster
+};
+cudaError_t launch_fp4_pair_gemm(const Fp4PairLaunch& L, cudaStream_t stream);
+int fp4_pair_stages(bool lora);
+
 struct Fp8Params {
   const float* sfa;       // [K/128, M]
   const float* sfb;       // [ceil(N/128), K/128]

@@ -37,44 +37,54 @@ __device__ __forceinline__ void load8(const void* x, int x_bf16, long long off, 
   }
 }
 
-// One warp per (row, 256-element segment), grid-stride.  Rows in [M, Mpad)
-// (the 128-row padding of the scale tensor) get zero scales, no codes.
+// One warp per (row, 4 x 256-element segments), grid-stride: the four 16-byte
+// loads of a lane are issued before any arithmetic (memory-level parallelism).
+// Rows in [M, Mpad) (the 128-row padding of the scale tensor) get zero
+// scales, no codes.
+constexpr int kQ4Unroll = 4;
 __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict__ x, int x_bf16, long long M,
                                                           long long Mpad, long long K, long long ldx,
                                                           const int* __restrict__ gather,
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   const int lane = threadIdx.x & 31;
-  const long long nseg = (K + 255) / 256;
-  const long long total = Mpad * nseg;
+  const long long nblk = (K + 256 * kQ4Unroll - 1) / (256 * kQ4Unroll);
+  const long long total = Mpad * nblk;
   const long long kchunks = K / 64;
   for (long long w = (long long)blockIdx.x * 8 + threadIdx.x / 32; w < total; w += (long long)gridDim.x * 8) {
-    const long long row = w / nseg, seg = w % nseg;
-    const long long k0 = seg * 256 + lane * 8;
-    const bool active = k0 < K;
+    const long long row = w / nblk, blk = w % nblk;
     long long src = row < M ? row : -1;
     if (src >= 0 && gather) src = gather[row];
-    float v[8];
+    float v[kQ4Unroll][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-    if (active && src >= 0) load8(x, x_bf16, src * ldx + k0, v);
-    float amax = 0.0f;
+    for (int u = 0; u < kQ4Unroll; ++u) {
+      const long long k0 = (blk * kQ4Unroll + u) * 256 + lane * 8;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    const uint32_t s_code = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
-    const float s = e4m3_to_f32(s_code);
-    float q[8];
+      for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
+      if (k0 < K && src >= 0) load8(x, x_bf16, src * ldx + k0, v[u]);
+    }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = (s == 0.0f) ? 0.0f : __fdiv_rn(v[i], s);
-    const uint32_t word = f32x8_to_e2m1x8(q);
-    if (active && row < M) *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + k0 / 2) = word;
-    const uint32_t b1 = __shfl_down_sync(0xffffffffu, s_code, 2);
-    const uint32_t b2 = __shfl_down_sync(0xffffffffu, s_code, 4);
-    const uint32_t b3 = __shfl_down_sync(0xffffffffu, s_code, 6);
-    if (active && (lane & 7) == 0) {
-      const long long chunk = k0 / 64;
-      const long long off = ((row / 128) * kchunks + chunk) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4;
-      *reinterpret_cast<uint32_t*>(sf + off) = s_code | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    for (int u = 0; u < kQ4Unroll; ++u) {
+      const long long k0 = (blk * kQ4Unroll + u) * 256 + lane * 8;
+      const bool active = k0 < K;
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[u][i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      const uint32_t s_code = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
+      const float s = e4m3_to_f32(s_code);
+      float q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = (s == 0.0f) ? 0.0f : __fdiv_rn(v[u][i], s);
+      const uint32_t word = f32x8_to_e2m1x8(q);
+      if (active && row < M) *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + k0 / 2) = word;
+      const uint32_t b1 = __shfl_down_sync(0xffffffffu, s_code, 2);
+      const uint32_t b2 = __shfl_down_sync(0xffffffffu, s_code, 4);
+      const uint32_t b3 = __shfl_down_sync(0xffffffffu, s_code, 6);
+      if (active && (lane & 7) == 0) {
+        const long long chunk = k0 / 64;
+        const long long off = ((row / 128) * kchunks + chunk) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4;
+        *reinterpret_cast<uint32_t*>(sf + off) = s_code | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      }
     }
   }
 }
@@ -237,7 +247,7 @@ static int sm_count() {
 cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx,
                                const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream) {
   const long long Mpad = (M + 127) / 128 * 128;
-  const long long warps = Mpad * ((K + 255) / 256);
+  const long long warps = Mpad * ((K + 256 * kQ4Unroll - 1) / (256 * kQ4Unroll));
   long long blocks = (warps + 7) / 8;
   const long long cap = (long long)sm_count() * 16;
   if (blocks > cap) blocks = cap;
@@ -278,27 +288,29 @@ namespace bsk {
 // ---------------------------------------------------------------------------
 // Fused FP4 quantization + low-rank left factor for bf16 rows.
 //
-// One CTA owns 64 rows and streams them through shared memory in K chunks of
-// 256 (3-stage cp.async ring, 32 KB of X + 16 KB of A^T per stage).  Each
-// 16-byte chunk j of row r is stored at chunk position j ^ (r % 8) so that
-// both consumers read conflict-free:
-//   - quantization: thread t owns row t % 64 and 64-element quarter t / 64 of
-//     the chunk: 4 group scales (one 32-bit word of the MMA scale layout) and
-//     32 bytes of codes;
-//   - low rank: warp w multiplies rows 16 (w % 4) .. +16 by A over the K half
-//     w / 4 of the chunk with ldmatrix + mma.sync m16n8k16 (bf16 -> fp32);
-//     the two K halves are summed through shared memory at the end and T is
+// One CTA owns 32 rows and streams them through shared memory in K chunks of
+// 256 (3-stage cp.async ring: 16 KB of X + 16 KB of A^T per stage, ~104 KB per
+// CTA so two CTAs share an SM).  Each 16-byte chunk j of row r is stored at
+// chunk position j ^ (r % 8).  Per stage:
+//   - quantization: thread t owns row t % 32 and the 32-element piece t / 32
+//     of the chunk (two groups: half of a 32-bit word of the MMA scale layout,
+//     written as 16 bits, and 16 bytes of codes); the row swizzle keeps the
+//     lanes of a warp on distinct banks;
+//   - low rank: warp w multiplies rows 16 (w % 2) .. +16 by A over K quarter
+//     w / 2 of the chunk with ldmatrix + mma.sync m16n8k16 (bf16 -> fp32); the
+//     four K quarters are summed through shared memory at the end and T is
 //     written as bf16 hi | lo.
 // X is read from HBM once for both results.
 // ---------------------------------------------------------------------------
 namespace fq {
-constexpr int R = 64;          // rows per CTA
+constexpr int R = 32;          // rows per CTA
 constexpr int KC = 256;        // K per stage
 constexpr int S = 3;           // stages
-constexpr int XB = R * KC * 2;       // 32 KB
+constexpr int XB = R * KC * 2;       // 16 KB
 constexpr int AB = 32 * KC * 2;      // 16 KB
 constexpr int STAGE = XB + AB;
-constexpr int SMEM = S * STAGE + 2 * 4 * 16 * 32 * 4;  // + reduction buffer [4 rowgroups][16][32] x 2 halves
+constexpr int RED = 4 * R * 32 * 4;  // [4 K quarters][32 rows][32] fp32
+constexpr int SMEM = S * STAGE + RED;
 }  // namespace fq
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, bool valid) {
@@ -320,7 +332,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(row * (fq::KC * 2) + ((chunk ^ (row & 7)) * 16));
 }
 
-__global__ void __launch_bounds__(256) q4_lowrank_fused_kernel(
+__global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
     const __nv_bfloat16* __restrict__ x, long long M, long long Mpad, long long K, long long ldx,
     const int* __restrict__ gather, const __nv_bfloat16* __restrict__ at, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ sf, __nv_bfloat16* __restrict__ t_out) {
@@ -330,23 +342,19 @@ __global__ void __launch_bounds__(256) q4_lowrank_fused_kernel(
   const int nchunks = (int)(K / fq::KC);
   const uint32_t sbase = smem_u32(fsm);
 
-  // source row of each of this CTA's rows, resolved once per thread's load slots
-  auto src_row = [&](int r) -> long long {
-    const long long row = r0 + r;
-    if (row >= M) return -1;
-    return gather ? (long long)gather[row] : row;
-  };
-
-  // loader: X chunk = 64 rows x 32 chunks of 16 B = 2048 copies (8 per thread);
+  // loader: X chunk = 32 rows x 32 chunks of 16 B = 1024 copies (4 per thread);
   // A^T chunk = 32 rows x 32 chunks = 1024 copies (4 per thread)
-  long long my_src[8];
+  long long my_src[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) my_src[i] = src_row((tid + i * 256) / 32);
-  auto load_stage = [&](int c, int s) {
-    const uint32_t xs = sbase + s * fq::STAGE, as = xs + fq::XB;
+  for (int i = 0; i < 4; ++i) {
+    const long long row = r0 + (tid + i * 256) / 32;
+    my_src[i] = row >= M ? -1 : (gather ? (long long)gather[row] : row);
+  }
+  auto load_stage = [&](int c, int st) {
+    const uint32_t xs = sbase + st * fq::STAGE, as = xs + fq::XB;
     const long long k0 = (long long)c * fq::KC;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
       const int idx = tid + i * 256, r = idx / 32, ch = idx % 32;
       const long long sr = my_src[i];
       const __nv_bfloat16* g = x + (sr >= 0 ? sr * ldx + k0 + ch * 8 : 0);
@@ -359,38 +367,38 @@ __global__ void __launch_bounds__(256) q4_lowrank_fused_kernel(
     }
   };
 
-  // quantization role of this thread
-  const int qrow = tid % fq::R, qquart = tid / fq::R;  // quarter = 64 elements = 8 chunks
+  // quantization role: row qrow, 32-element piece qp (chunks 4 qp .. 4 qp + 3)
+  const int qrow = tid % 32, qp = tid / 32;
   const long long grow = r0 + qrow;
-  // low-rank role of this warp
-  const int rg = warp % 4, kh = warp / 4;
+  // low-rank role of this warp: rows 16 rg .. +16, K quarter kq (64 elements)
+  const int rg = warp % 2, kq = warp / 2;
   float d[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) d[i][j] = 0.0f;
 
-  for (int s = 0; s < fq::S - 1; ++s) {
-    if (s < nchunks) load_stage(s, s);
+  for (int st = 0; st < fq::S - 1; ++st) {
+    if (st < nchunks) load_stage(st, st);
     cp_async_commit();
   }
   for (int c = 0; c < nchunks; ++c) {
-    const int s = c % fq::S;
+    const int st = c % fq::S;
     if (c + fq::S - 1 < nchunks) load_stage(c + fq::S - 1, (c + fq::S - 1) % fq::S);
     cp_async_commit();
     cp_async_wait<fq::S - 1>();
     __syncthreads();
-    const uint32_t xs = sbase + s * fq::STAGE, as = xs + fq::XB;
+    const uint32_t xs = sbase + st * fq::STAGE, as = xs + fq::XB;
 
-    // ---- quantize 64 elements (4 groups) of row qrow
+    // ---- quantize 32 elements (2 groups) of row qrow
     {
-      float v[64];
+      float v[32];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         uint4 raw;
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
-                     : "r"(xs + swz(qrow, qquart * 8 + j)));
+                     : "r"(xs + swz(qrow, qp * 4 + j)));
         const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -398,16 +406,16 @@ __global__ void __launch_bounds__(256) q4_lowrank_fused_kernel(
           v[8 * j + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
         }
       }
-      uint32_t sfw = 0;
-      uint32_t cw[8];
+      uint32_t sfh = 0;
+      uint32_t cw[4];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < 2; ++g) {
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[16 * g + i]));
         const uint32_t sc = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
         const float sv = e4m3_to_f32(sc);
-        sfw |= sc << (8 * g);
+        sfh |= sc << (8 * g);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float q[8];
@@ -416,34 +424,32 @@ __global__ void __launch_bounds__(256) q4_lowrank_fused_kernel(
           cw[2 * g + h] = f32x8_to_e2m1x8(q);
         }
       }
-      const long long kq = (long long)c * fq::KC + qquart * 64;  // first element of the quarter
+      // two scale bytes = half of the 64-element chunk's scale word
+      const long long kp = (long long)c * fq::KC + qp * 32;  // first element of the piece
       if (grow < Mpad) {
-        const long long off = ((grow / 128) * (K / 64) + kq / 64) * 512 + (grow % 32) * 16 + ((grow % 128) / 32) * 4;
-        *reinterpret_cast<uint32_t*>(sf + off) = (grow < M) ? sfw : 0u;
+        const long long off = ((grow / 128) * (K / 64) + kp / 64) * 512 + (grow % 32) * 16 + ((grow % 128) / 32) * 4 +
+                              ((kp / 32) & 1) * 2;
+        *reinterpret_cast<uint16_t*>(sf + off) = (grow < M) ? (uint16_t)sfh : (uint16_t)0;
       }
-      if (grow < M) {
-        uint4* dst = reinterpret_cast<uint4*>(codes + grow * (K / 2) + kq / 2);
-        dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      }
+      if (grow < M)
+        *reinterpret_cast<uint4*>(codes + grow * (K / 2) + kp / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
     }
 
-    // ---- low rank: rows 16 rg .. +16, K half kh of the chunk (8 k-steps)
+    // ---- low rank: rows 16 rg .. +16, K quarter kq of the chunk (4 k-steps)
     {
       const int arow = rg * 16 + (lane % 16);
-      const int ahalf = lane / 16;  // second 8 columns of the k-step
+      const int ahalf = lane / 16;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int kchunk = kh * 16 + ks * 2;  // 16-byte chunk of this k-step's first 8 elements
+      for (int ks = 0; ks < 4; ++ks) {
+        const int kchunk = kq * 8 + ks * 2;  // 16-byte chunk of this k-step's first 8 elements
         uint32_t a0, a1, a2, a3;
         ldsm_x4(xs + swz(arow, kchunk + ahalf), a0, a1, a2, a3);
 #pragma unroll
-        for (int np = 0; np < 2; ++np) {  // pairs of n-tiles: rows 16 np .. +16 of A^T
+        for (int np = 0; np < 2; ++np) {
           const int brow = np * 16 + (lane % 8) + ((lane / 16) * 8);
           const int bhalf = (lane / 8) % 2;
           uint32_t b0, b1, b2, b3;
           ldsm_x4(as + swz(brow, kchunk + bhalf), b0, b1, b2, b3);
-          // b0/b1: n-tile 2np (k lo / k hi); b2/b3: n-tile 2np+1
           asm volatile(
               "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
               "{%0, %1, %2, %3};"
@@ -457,15 +463,15 @@ __global__ void __launch_bounds__(256) q4_lowrank_fused_kernel(
         }
       }
     }
-    __syncthreads();  // stage s may be refilled next iteration
+    __syncthreads();  // stage st may be refilled next iteration
   }
   cp_async_wait<0>();
 
-  // ---- reduce the two K halves and write T as bf16 hi | lo
-  float* red = reinterpret_cast<float*>(fsm + fq::S * fq::STAGE);  // [2][4][16][32]
+  // ---- reduce the four K quarters and write T as bf16 hi | lo
+  float* red = reinterpret_cast<float*>(fsm + fq::S * fq::STAGE);  // [4][32][32]
   {
     const int g = lane / 4, tq = lane % 4;
-    float* rb = red + ((kh * 4 + rg) * 16) * 32;
+    float* rb = red + (kq * fq::R + rg * 16) * 32;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       rb[g * 32 + nt * 8 + 2 * tq] = d[nt][0];
@@ -479,7 +485,9 @@ __global__ void __launch_bounds__(256) q4_lowrank_fused_kernel(
     const int r = o / 32, j = o % 32;
     const long long row = r0 + r;
     if (row >= M) continue;
-    const float t = red[(0 * 4 * 16 + r) * 32 + j] + red[(1 * 4 * 16 + r) * 32 + j];
+    float t = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) t += red[(w * fq::R + r) * 32 + j];
     const __nv_bfloat16 hi = __float2bfloat16_rn(t);
     const __nv_bfloat16 lo = __float2bfloat16_rn(t - __bfloat162float(hi));
     t_out[row * 64 + j] = hi;
