@@ -45,6 +45,7 @@ class GemmArgs(ctypes.Structure):
         ("alpha", ctypes.c_float), ("col_scale", ctypes.c_void_p), ("lora_t", ctypes.c_void_p),
         ("lora_b_t", ctypes.c_void_p), ("r", ctypes.c_int), ("bias", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("out_dtype", ctypes.c_int), ("ldo", ctypes.c_int64), ("num_sms", ctypes.c_int),
+        ("n_chunk_blocks", ctypes.c_int),
     ]
 
 
@@ -222,10 +223,12 @@ def gemm_fp8(a, sa, b, sb, out_dtype=torch.bfloat16, out=None, num_sms: int = 0,
 
 
 def grouped_gemm_fp4(a, sfa, b, sfb, K: int, N: int, E: int, offsets, counts, epilogue: int, out=None,
-                     token_of=None, weight_of=None, out32=None, num_sms: int = 0, stream=None):
+                     token_of=None, weight_of=None, out32=None, num_sms: int = 0, n_chunk_blocks: int = 0,
+                     stream=None):
     """FP4 GEMM grouped over experts (rows of ``a`` grouped by ``offsets``/``counts``)."""
     M = a.shape[0]
     g = _args(FMT_FP4, a, sfa, b, sfb, M, N, K, out, num_sms=num_sms)
+    g.n_chunk_blocks = n_chunk_blocks
     ld32 = 0 if out32 is None else out32.stride(0)
     _check(load().bs_grouped_gemm(ctypes.byref(g), E, _ptr(offsets), _ptr(counts), epilogue, _ptr(token_of),
                                   _ptr(weight_of), _ptr(out32), ld32, _stream(stream)))

@@ -226,6 +226,7 @@ static bs_status check_common(const bs_gemm_args* a, bool grouped) {
     if (!aligned16(a->out) || a->ldo % 8 || a->ldo < a->N) return fail(BS_ERR_ALIGN, "out must be 16-byte aligned, ldo %% 8 == 0, ldo >= N");
   }
   if (a->num_sms < 0) return fail(BS_ERR_INVALID, "num_sms < 0");
+  if (a->n_chunk_blocks < 0) return fail(BS_ERR_INVALID, "n_chunk_blocks < 0");
   return BS_OK;
 }
 
@@ -281,13 +282,33 @@ static bs_status sf_map(CUtensorMap* m, const void* sf, int64_t rows, int64_t K)
                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// FP8 decode split-K over CTA pairs (BSGEMM_FP8_SPLIT=0 disables it).
+static bool fp8_split_ok() {
+  static bool on = [] {
+    const char* e = getenv("BSGEMM_FP8_SPLIT");
+    return !(e && atoi(e) == 0);
+  }();
+  return on;
+}
+
+// Issue order of scale copies and MMAs in the FP4 kernel (BSGEMM_FP4_SCHED).
+static int fp4_sched() {
+  static int v = [] {
+    const char* e = getenv("BSGEMM_FP4_SCHED");
+    const int v = e ? atoi(e) : 0;
+    return (v >= 0 && v <= 2) ? v : 0;  // only the three complete issue orders exist
+  }();
+  return v;
+}
+
 static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int sms, cudaStream_t s,
                             long long pair_tiles, bool grouped) {
   bs_status st;
+  L.p.sched = fp4_sched();
   if (fp4_pair()) {
     bsk::Fp4PairLaunch P;
     memset(&P, 0, sizeof P);
-    st = fp4_maps(L, a, b_rows, 128);
+    st = fp4_maps(L, a, b_rows, fp4_bk());
     if (st != BS_OK) return st;
     st = sf_map(&P.tmSfa, a->sfa, a->M, a->K);
     if (st != BS_OK) return st;
@@ -376,6 +397,13 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     L.swap_ab = true;
     const long long tiles = ((a->N + 127) / 128) * ((a->M + L.tile_n - 1) / L.tile_n);
     L.grid = (int)(tiles < sms ? tiles : sms);
+    // Decode shapes with few tiles: two CTAs per tile, each streaming half of
+    // K (split-K over a 2-CTA cluster, partials reduced through DSMEM).
+    L.p.splits = 1;
+    if (L.tile_n <= 32 && tiles * 2 <= sms && a->K >= 256 && fp8_split_ok()) {
+      L.p.splits = 2;
+      L.grid = (int)(2 * tiles);
+    }
     cudaError_t e = bsk::launch_fp8_gemm(L, s);
     if (e != cudaSuccess) return cuda_fail(e, "FP8 GEMM launch");
     return BS_OK;
@@ -428,6 +456,7 @@ bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, 
   L.p.out32 = out32;
   L.p.ld_out32 = ld_out32;
   L.p.status = status;
+  L.p.n_chunk = a->n_chunk_blocks > 0 ? a->n_chunk_blocks : 0;
   L.lora = false;
   L.epilogue = epilogue;
   L.grid = sms;

@@ -135,7 +135,7 @@ __device__ __forceinline__ int n_blocks(const Fp4Params& p) {
 
 template <int kEpi>
 __device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, int t) {
-  Tile tl;
+  Tile tl = {};
   if (p.E == 0) {
     const int num_m = (p.M + BM - 1) / BM;
     const int mb = t % num_m, nb = t / num_m;
@@ -148,17 +148,25 @@ __device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, i
     tl.sfb_blk1 = (tl.brow1 < p.N) ? tl.brow1 / 128 : tl.brow0 / 128;
     return tl;
   }
-  // binary search: largest e with prefix[e] <= t
-  int lo = 0, hi = p.E - 1;
+  // Grouped: tiles walk chunks of n_chunk column blocks; inside a chunk,
+  // expert by expert, column block by column block, row block by row block.
+  // prefix[e] = row blocks of experts 0 .. e-1 (prefix[E] = all row blocks).
+  const int nbk = n_blocks<kEpi>(p);
+  const int nck = (p.n_chunk > 0 && p.n_chunk < nbk) ? p.n_chunk : nbk;
+  const int mbt = prefix[p.E];
+  const int c = t / (mbt * nck);
+  const int nbc = min(nck, nbk - c * nck);
+  const int rem = t - c * mbt * nck;
+  int lo = 0, hi = p.E - 1;  // largest e with prefix[e] * nbc <= rem
   while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] * nbc <= rem) lo = mid; else hi = mid - 1;
   }
   const int e = lo;
   const int cnt = p.counts[e];
-  const int mblk = (cnt + BM - 1) / BM;
-  const int local = t - prefix[e];
-  const int nb = local / mblk, mb = local % mblk;
+  const int mblk = prefix[e + 1] - prefix[e];
+  const int local = rem - prefix[e] * nbc;
+  const int nb = c * nck + local / mblk, mb = local % mblk;
   tl.expert = e;
   tl.row0 = p.offsets[e] + mb * BM;
   tl.rows = min(BM, cnt - mb * BM);
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (e < p.E) {
           const int off = p.offsets[e], cnt = p.counts[e], nxt = p.offsets[e + 1];
           if (cnt < 0 || (off % BM) != 0 || off + cnt > nxt || nxt > p.M) bad = true;
-          tiles = ((max(cnt, 0) + BM - 1) / BM) * nb;
+          tiles = (max(cnt, 0) + BM - 1) / BM;  // row blocks of expert e
         }
         int incl = tiles;
 #pragma unroll
@@ -244,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bad = __any_sync(0xffffffffu, bad) || p.offsets[0] != 0;
       if (lane == 0) {
         sm.prefix[p.E] = running;
-        *sm.total_tiles = bad ? 0 : running;
+        *sm.total_tiles = bad ? 0 : running * nb;
         if (bad && blockIdx.x == 0) record_status(p.status, kStatusOffsets, 1);
       }
     }
@@ -317,12 +325,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
+    // Scale copies (tcgen05.cp) and MMAs share the tensor core's in-order
+    // stream, so their order matters.  p.sched 0: a stage's copies, then its
+    // MMAs.  1: each MMA right after its own copies.  2: like 1, and the
+    // copies of the next stage are issued before the MMAs of this one (one
+    // stage of look-ahead; the scale buffers alternate by stage).
     PipeState<kStages> ps;
     uint32_t acc_phase = 0, lora_phase = 0, sf_buf = 0;
+    const int sched = p.sched;
     bool ok = true;
+    auto issue_cps = [&](uint8_t* st, int nmma, uint32_t buf) {
+      const uint32_t ssfa = smem_u32(st + G::kOffSfa), ssfb = smem_u32(st + G::kOffSfb);
+      for (int j = 0; j < nmma; ++j) {
+        const uint32_t col = tmem + kTmemSf + buf * G::kSfColsPerStage + j * kSfColsPerMma;
+        tc_cp_32x128b_warpx4(col, smem_desc(ssfa + 512 * j, 0, 128, kLayoutNone));
+        tc_cp_32x128b_warpx4(col + 4, smem_desc(ssfb + 512 * j, 0, 128, kLayoutNone));
+        tc_cp_32x128b_warpx4(col + 8, smem_desc(ssfb + G::kMmas * 512 + 512 * j, 0, 128, kLayoutNone));
+      }
+    };
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       if (!mbar_wait(sm.acc_empty, acc_phase ^ 1u, abort_flag, p.status, 30)) break;
       tc_fence_after();
+      bool next_cps_done = false;  // sched 2: copies of the current stage already issued
       for (int ks = 0; ks < kstages; ++ks) {
         if (!mbar_wait(&sm.full[ps.index], ps.phase, abort_flag, p.status, 31)) { ok = false; break; }
         tc_fence_after();
@@ -331,14 +355,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sa = smem_u32(st + G::kOffA), sb = smem_u32(st + G::kOffB);
         const uint32_t ssfa = smem_u32(st + G::kOffSfa), ssfb = smem_u32(st + G::kOffSfb);
         const uint32_t sf_col = kTmemSf + sf_buf * G::kSfColsPerStage;
-        for (int j = 0; j < nmma; ++j) {
-          const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
-          tc_cp_32x128b_warpx4(col, smem_desc(ssfa + 512 * j, 0, 128, kLayoutNone));
-          tc_cp_32x128b_warpx4(col + 4, smem_desc(ssfb + 512 * j, 0, 128, kLayoutNone));
-          tc_cp_32x128b_warpx4(col + 8, smem_desc(ssfb + G::kMmas * 512 + 512 * j, 0, 128, kLayoutNone));
+        if (sched == 0) {
+          issue_cps(st, nmma, sf_buf);
+        } else if (sched == 2) {
+          if (!next_cps_done) issue_cps(st, nmma, sf_buf);
+          next_cps_done = false;
+          // look ahead: the next stage of this tile, if its data is already there
+          if (ks + 1 < kstages) {
+            const uint32_t ni = ps.index + 1 == (uint32_t)kStages ? 0 : ps.index + 1;
+            const uint32_t nph = ps.index + 1 == (uint32_t)kStages ? ps.phase ^ 1u : ps.phase;
+            if (mbar_try_wait(&sm.full[ni], nph)) {
+              tc_fence_after();
+              issue_cps(sm.stages + ni * G::kStageBytes, min(G::kMmas, kchunks - G::kMmas * (ks + 1)), sf_buf ^ 1u);
+              next_cps_done = true;
+            }
+          }
         }
         for (int j = 0; j < nmma; ++j) {
           const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
+          if (sched == 1) {
+            tc_cp_32x128b_warpx4(col, smem_desc(ssfa + 512 * j, 0, 128, kLayoutNone));
+            tc_cp_32x128b_warpx4(col + 4, smem_desc(ssfb + 512 * j, 0, 128, kLayoutNone));
+            tc_cp_32x128b_warpx4(col + 8, smem_desc(ssfb + G::kMmas * 512 + 512 * j, 0, 128, kLayoutNone));
+          }
           mma_mxf4nvf4(tmem + kTmemAcc, smem_desc(sa + 32 * j, 16, G::kSbo, G::kLayout),
                        smem_desc(sb + 32 * j, 16, G::kSbo, G::kLayout), kIdescMain, col, col + 4,
                        (ks > 0 || j > 0) ? 1u : 0u);
@@ -405,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const bool row_ok = r_in_tile < tl.rows;
       const int64_t row = (int64_t)tl.row0 + r_in_tile;
-      if (kEpi == kEpiSwiglu) {
+      if (kEpi == kEpiSwiglu && row < p.M) {
         // h = bf16(silu(g) * u); padding rows of the segment are written as zeros.
         const int col = tl.col0 + 64 * half;
         uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * p.ldo + col;
@@ -428,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (kEpi == kEpiCombine) {
         const int col = tl.col0 + 128 * half;
-        if (row_ok && col < p.N) {
+        if (row_ok && row < p.M && col < p.N) {
           const int tok = p.token_of[row];
           const float wt = p.weight_of[row];
           if (tok >= 0) {
@@ -445,9 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else {
+      } else if (kEpi == kEpiStore) {
         const int col = tl.col0 + 128 * half;
-        if (row_ok && col < p.N) {
+        if (row_ok && row < p.M && col < p.N) {
 #pragma unroll
           for (int c = 0; c < 128; c += 8) {
             float y[8];

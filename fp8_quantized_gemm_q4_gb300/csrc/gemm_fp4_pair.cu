@@ -31,41 +31,46 @@ namespace fp4pair {
 
 constexpr int BM = 128;        // rows per CTA (the pair covers 256)
 constexpr int BN = 256;        // MMA N; each CTA holds BN / 2 rows of B
-constexpr int BK = 128;        // K per stage
-constexpr int kRowBytes = BK / 2;
-constexpr int kSbo = 8 * kRowBytes;
-constexpr int kMmas = BK / 64;
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
 constexpr int kMaxExperts = 1024;
 constexpr int kMisc = 2048 + (kMaxExperts + 1) * 4 + 1024;
-
-constexpr int kOffA = 0;
-constexpr int kOffB = BM * kRowBytes;                    // 8192
-constexpr int kOffSfa = kOffB + (BN / 2) * kRowBytes;    // 16384
-constexpr int kOffSfb = kOffSfa + kMmas * 512;           // 17408
-constexpr int kStageBytes = kOffSfb + 2 * kMmas * 512;   // 19456
-constexpr int kStageTx = kStageBytes;                    // bytes one CTA's loads deliver per stage
-
-constexpr Fp4TileShape kShapeLora{BM, BN, BK, 2, true, 32, kMisc};
-constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 2, false, 32, kMisc};
-static_assert(kStageBytes == fp4_stage_bytes(kShapeNoLora), "per-CTA stage layout matches the budget");
-static_assert(kStageBytes % kAlign == 0, "stage alignment");
 // low-rank slot per CTA: T hi / T lo of its own rows, its half of Bl^T
 constexpr int kLoraThi = 0, kLoraTlo = 8192, kLoraBl = 16384, kLoraBytes = 24576;
-static_assert(kLoraBytes == fp4_lora_bytes(kShapeLora), "low-rank slot: the up-projection block is split per CTA");
-constexpr int kStagesLora = fp4_main_stages(kShapeLora) < 16 ? fp4_main_stages(kShapeLora) : 16;
-constexpr int kStagesNoLora = fp4_main_stages(kShapeNoLora) < 16 ? fp4_main_stages(kShapeNoLora) : 16;
-static_assert(fp4_smem_total(kShapeLora, kStagesLora) + kAlign <= kSmemPerCta, "lora smem");
-static_assert(fp4_smem_total(kShapeNoLora, kStagesNoLora) + kAlign <= kSmemPerCta, "smem");
-
 constexpr int kSfBuffers = 2;
 constexpr int kTmemAcc = 0;
 constexpr int kTmemSf = BN;
 constexpr int kSfColsPerMma = 4 + BN / 32;
-constexpr int kSfColsPerStage = kMmas * kSfColsPerMma;
-static_assert(fp4_tmem_cols(kShapeLora, 1, kSfBuffers) <= kTmemCols, "tmem budget");
-constexpr int kTmemAlloc = pow2_cols(fp4_tmem_cols(kShapeLora, 1, kSfBuffers));
+
+// Per-CTA stage geometry for a K depth of BK FP4 elements per stage.
+template <int BK>
+struct PGeo {
+  static_assert(BK == 128 || BK == 256, "stage depth");
+  static constexpr int kRowBytes = BK / 2;
+  static constexpr uint32_t kLayout = BK == 256 ? kLayoutSw128 : kLayoutSw64;
+  static constexpr int kSbo = 8 * kRowBytes;
+  static constexpr int kMmas = BK / 64;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = BM * kRowBytes;
+  static constexpr int kOffSfa = kOffB + (BN / 2) * kRowBytes;
+  static constexpr int kOffSfb = kOffSfa + kMmas * 512;
+  static constexpr int kStageBytes = kOffSfb + 2 * kMmas * 512;
+  static constexpr int kStageTx = kStageBytes;  // bytes one CTA's loads deliver per stage
+  static constexpr int kSfWords = kMmas * 128;  // scale words of one 128-row block per stage
+  static constexpr int kSfBoxes = kSfWords / 256;  // TMA boxes of 256 words
+  static constexpr Fp4TileShape kShapeLora{BM, BN, BK, 2, true, 32, kMisc};
+  static constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 2, false, 32, kMisc};
+  static_assert(kStageBytes == fp4_stage_bytes(kShapeNoLora), "per-CTA stage layout matches the budget");
+  static_assert(kStageBytes % kAlign == 0, "stage alignment");
+  static_assert(kLoraBytes == fp4_lora_bytes(kShapeLora), "low-rank slot: the up-projection block is split per CTA");
+  static constexpr int kStagesLora = fp4_main_stages(kShapeLora) < 16 ? fp4_main_stages(kShapeLora) : 16;
+  static constexpr int kStagesNoLora = fp4_main_stages(kShapeNoLora) < 16 ? fp4_main_stages(kShapeNoLora) : 16;
+  static_assert(fp4_smem_total(kShapeLora, kStagesLora) + kAlign <= kSmemPerCta, "lora smem");
+  static_assert(fp4_smem_total(kShapeNoLora, kStagesNoLora) + kAlign <= kSmemPerCta, "smem");
+  static constexpr int kSfColsPerStage = kMmas * kSfColsPerMma;
+  static_assert(fp4_tmem_cols(kShapeLora, 1, kSfBuffers) <= kTmemCols, "tmem budget");
+  static constexpr int kTmemAlloc = pow2_cols(fp4_tmem_cols(kShapeLora, 1, kSfBuffers));
+};
 
 constexpr uint32_t kIdescMain = idesc_mxf4nvf4(2 * BM, BN);
 constexpr uint32_t kIdescLora = idesc_bf16(2 * BM, BN);
@@ -86,7 +91,7 @@ __device__ __forceinline__ int n_blocks(const Fp4Params& p) {
 
 template <int kEpi>
 __device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, int t) {
-  Tile tl;
+  Tile tl = {};
   if (p.E == 0) {
     const int num_m = (p.M + 2 * BM - 1) / (2 * BM);
     const int mb = t % num_m, nb = t / num_m;
@@ -98,16 +103,25 @@ __device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, i
     tl.sfb_blk1 = (tl.brow1 < p.N) ? tl.brow1 / 128 : tl.brow0 / 128;
     return tl;
   }
-  int lo = 0, hi = p.E - 1;  // largest e with prefix[e] <= t
+  // Grouped: tiles walk chunks of n_chunk column blocks; inside a chunk,
+  // expert by expert, column block by column block, row block by row block.
+  // prefix[e] = row blocks of experts 0 .. e-1 (prefix[E] = all row blocks).
+  const int nbk = n_blocks<kEpi>(p);
+  const int nck = (p.n_chunk > 0 && p.n_chunk < nbk) ? p.n_chunk : nbk;
+  const int mbt = prefix[p.E];
+  const int c = t / (mbt * nck);
+  const int nbc = min(nck, nbk - c * nck);
+  const int rem = t - c * mbt * nck;
+  int lo = 0, hi = p.E - 1;  // largest e with prefix[e] * nbc <= rem
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    if (prefix[mid] * nbc <= rem) lo = mid; else hi = mid - 1;
   }
   const int e = lo;
   const int cnt = p.counts[e];
-  const int mblk = (cnt + 2 * BM - 1) / (2 * BM);
-  const int local = t - prefix[e];
-  const int nb = local / mblk, mb = local % mblk;
+  const int mblk = prefix[e + 1] - prefix[e];
+  const int local = rem - prefix[e] * nbc;
+  const int nb = c * nck + local / mblk, mb = local % mblk;
   tl.row0 = p.offsets[e] + mb * 2 * BM;
   tl.rows = min(2 * BM, cnt - mb * 2 * BM);
   const int64_t wrows = (kEpi == kEpiSwiglu) ? 2LL * p.N : (int64_t)p.N;
@@ -125,12 +139,16 @@ __device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, i
   return tl;
 }
 
-template <int kStages, bool kLora, int kEpi>
+template <int BK, int kStages, bool kLora, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmL,
                     const __grid_constant__ CUtensorMap tmSfa, const __grid_constant__ CUtensorMap tmSfb,
                     const Fp4Params p) {
+  using G = PGeo<BK>;
+  constexpr int kStageBytes = G::kStageBytes, kRowBytes = G::kRowBytes, kMmas = G::kMmas;
+  constexpr int kOffA = G::kOffA, kOffB = G::kOffB, kOffSfa = G::kOffSfa, kOffSfb = G::kOffSfb;
+  constexpr int kSbo = G::kSbo, kSfColsPerStage = G::kSfColsPerStage, kTmemAlloc = G::kTmemAlloc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kAlign - 1) &
                                              ~static_cast<uintptr_t>(kAlign - 1));
@@ -195,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (e < p.E) {
           const int off = p.offsets[e], cnt = p.counts[e], nxt = p.offsets[e + 1];
           if (cnt < 0 || (off % BM) != 0 || off + cnt > nxt || nxt > p.M) bad = true;
-          tiles = ((max(cnt, 0) + 2 * BM - 1) / (2 * BM)) * nb;
+          tiles = (max(cnt, 0) + 2 * BM - 1) / (2 * BM);  // row blocks (pairs) of expert e
         }
         int incl = tiles;
 #pragma unroll
@@ -209,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bad = __any_sync(0xffffffffu, bad) || p.offsets[0] != 0;
       if (lane == 0) {
         prefix[p.E] = running;
-        *total_tiles = bad ? 0 : running;
+        *total_tiles = bad ? 0 : running * nb;
         if (bad && blockIdx.x == 0) record_status(p.status, kStatusOffsets, 3);
       }
     }
@@ -235,13 +253,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ks < kstages; ++ks) {
         if (!mbar_wait(&empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 110)) { ok = false; break; }
         uint8_t* st = stages + ps.index * kStageBytes;
-        if (leader) mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(2 * kStageTx));
+        if (leader) mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(2 * G::kStageTx));
         const uint32_t bar = mapa_shared(smem_u32(&full[ps.index]), 0);
         tma_load_2d_pair(st + kOffA, &tmA, bar, ks * kRowBytes, my_row0);
         tma_load_2d_pair(st + kOffB, &tmB, bar, ks * kRowBytes, my_brow);
-        tma_load_2d_pair(st + kOffSfa, &tmSfa, bar, ks * kMmas * 128, my_row0 / 128);
-        tma_load_2d_pair(st + kOffSfb, &tmSfb, bar, ks * kMmas * 128, tl.brow0 / 128);
-        tma_load_2d_pair(st + kOffSfb + kMmas * 512, &tmSfb, bar, ks * kMmas * 128, tl.sfb_blk1);
+#pragma unroll
+        for (int b = 0; b < G::kSfBoxes; ++b) {
+          const int x = ks * G::kSfWords + b * 256;
+          tma_load_2d_pair(st + kOffSfa + b * 1024, &tmSfa, bar, x, my_row0 / 128);
+          tma_load_2d_pair(st + kOffSfb + b * 1024, &tmSfb, bar, x, tl.brow0 / 128);
+          tma_load_2d_pair(st + kOffSfb + kMmas * 512 + b * 1024, &tmSfb, bar, x, tl.sfb_blk1);
+        }
         issued_mask |= 1u << ps.index;
         last_phase = (last_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
         ps.advance();
@@ -295,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j < nmma; ++j) {
           const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
-          mma_mxf4nvf4_pair(tmem + kTmemAcc, smem_desc(sa + 32 * j, 16, kSbo, kLayoutSw64),
-                            smem_desc(sb + 32 * j, 16, kSbo, kLayoutSw64), kIdescMain, col, col + 4,
+          mma_mxf4nvf4_pair(tmem + kTmemAcc, smem_desc(sa + 32 * j, 16, kSbo, G::kLayout),
+                            smem_desc(sb + 32 * j, 16, kSbo, G::kLayout), kIdescMain, col, col + 4,
                             (ks > 0 || j > 0) ? 1u : 0u);
         }
         tc_commit_pair_multicast(&empty[ps.index], 0x3);
@@ -387,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (kEpi == kEpiCombine) {
         const int col = tl.col0 + 128 * half;
-        if (row_ok && col < p.N) {
+        if (row_ok && row < p.M && col < p.N) {
           const int tok = p.token_of[row];
           const float wt = p.weight_of[row];
           if (tok >= 0) {
@@ -404,9 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else {
+      } else if (kEpi == kEpiStore) {
         const int col = tl.col0 + 128 * half;
-        if (row_ok && col < p.N) {
+        if (row_ok && row < p.M && col < p.N) {
 #pragma unroll
           for (int c = 0; c < 128; c += 8) {
             float y[8];
@@ -445,11 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kLora, int kEpi>
+template <int BK, bool kLora, int kEpi>
 static cudaError_t launch_one(const Fp4PairLaunch& L, cudaStream_t stream) {
-  constexpr int kStages = kLora ? kStagesLora : kStagesNoLora;
-  auto kern = fp4_pair_kernel<kStages, kLora, kEpi>;
-  const int smem = fp4_smem_total(kLora ? kShapeLora : kShapeNoLora, kStages) + kAlign;
+  using G = PGeo<BK>;
+  constexpr int kStages = kLora ? G::kStagesLora : G::kStagesNoLora;
+  auto kern = fp4_pair_kernel<BK, kStages, kLora, kEpi>;
+  const int smem = fp4_smem_total(kLora ? G::kShapeLora : G::kShapeNoLora, kStages) + kAlign;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -467,23 +490,32 @@ static cudaError_t launch_one(const Fp4PairLaunch& L, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kern, L.base.tmA, L.base.tmB, L.base.tmT, L.base.tmL, L.tmSfa, L.tmSfb, L.base.p);
 }
 
-}  // namespace fp4pair
-
-cudaError_t launch_fp4_pair_gemm(const Fp4PairLaunch& L, cudaStream_t stream) {
-  using namespace fp4pair;
-  if (L.grid <= 0 || (L.grid & 1)) return cudaErrorInvalidValue;
+template <int BK>
+static cudaError_t launch_bk(const Fp4PairLaunch& L, cudaStream_t stream) {
   if (L.base.lora) {
     if (L.base.epilogue != kEpiStore) return cudaErrorInvalidValue;
-    return launch_one<true, kEpiStore>(L, stream);
+    return launch_one<BK, true, kEpiStore>(L, stream);
   }
   switch (L.base.epilogue) {
-    case kEpiStore: return launch_one<false, kEpiStore>(L, stream);
-    case kEpiSwiglu: return launch_one<false, kEpiSwiglu>(L, stream);
-    case kEpiCombine: return launch_one<false, kEpiCombine>(L, stream);
+    case kEpiStore: return launch_one<BK, false, kEpiStore>(L, stream);
+    case kEpiSwiglu: return launch_one<BK, false, kEpiSwiglu>(L, stream);
+    case kEpiCombine: return launch_one<BK, false, kEpiCombine>(L, stream);
   }
   return cudaErrorInvalidValue;
 }
 
-int fp4_pair_stages(bool lora) { return lora ? fp4pair::kStagesLora : fp4pair::kStagesNoLora; }
+}  // namespace fp4pair
+
+cudaError_t launch_fp4_pair_gemm(const Fp4PairLaunch& L, cudaStream_t stream) {
+  if (L.grid <= 0 || (L.grid & 1)) return cudaErrorInvalidValue;
+  if (L.base.bk == 256) return fp4pair::launch_bk<256>(L, stream);
+  if (L.base.bk == 128) return fp4pair::launch_bk<128>(L, stream);
+  return cudaErrorInvalidValue;
+}
+
+int fp4_pair_stages(bool lora, int bk) {
+  if (bk == 256) return lora ? fp4pair::PGeo<256>::kStagesLora : fp4pair::PGeo<256>::kStagesNoLora;
+  return lora ? fp4pair::PGeo<128>::kStagesLora : fp4pair::PGeo<128>::kStagesNoLora;
+}
 
 }  // namespace bsk

@@ -8,9 +8,9 @@
 //
 // The fp32 scales are not a format the tensor core's block scaling takes, so
 // they are applied per 128-wide K block ("promotion"): the tensor core writes
-// the block's partial product into one of two tensor-memory slots and the
-// epilogue warps fold it into fp32 registers, acc += partial * sb * sa, while
-// the tensor core fills the other slot.
+// the block's partial product into a ring of tensor-memory slots (up to 16)
+// and the epilogue warps fold each into fp32 registers, acc += partial * sb *
+// sa, while the tensor core fills the next slots.
 //
 // Swap-AB orientation for every M: weight rows fill the MMA's M = 128 (one
 // weight-scale block per tile), the tokens are the MMA's N (16 .. 128), so the
@@ -43,17 +43,25 @@ struct Cfg {
   static constexpr int kStageBytes = round_up(BM * BK + TN * BK, kAlign);
   // two staging buffers of [KBC][TN] activation scales + [KBC] weight scales
   static constexpr int kScaleBytes = round_up(2 * (KBC * TN + KBC) * 4, kAlign);
-  static constexpr Fp8TileShape kShape{BM, TN, BK, kMisc + kScaleBytes + kAlign};
+  // split-K partner's partial sums [BM rows][TN], written through DSMEM
+  static constexpr int kRedBytes = round_up(BM * TN * 4, kAlign);
+  static constexpr Fp8TileShape kShape{BM, TN, BK, kMisc + kScaleBytes + kRedBytes + kAlign};
   static constexpr int kStages = fp8_main_stages(kShape) < kMaxStages ? fp8_main_stages(kShape) : kMaxStages;
-  static constexpr int kSmem = kStages * kStageBytes + kScaleBytes + kMisc + kAlign;
-  static constexpr int kTmemCols = pow2_cols(2 * TN);
+  static constexpr int kSmem = kStages * kStageBytes + kScaleBytes + kRedBytes + kMisc + kAlign;
+  // partial slots: as many K blocks as tensor memory holds (up to 16), so
+  // the tensor core can run that far ahead of the promotion warps
+  static constexpr int kSlots = (512 / TN) < 16 ? (512 / TN) : 16;
+  static constexpr int kTmemCols = pow2_cols(kSlots * TN);
   static constexpr int kColsPerWarp = TN / 2;
   static_assert(kStages >= 2, "ring too shallow");
   static_assert(kSmem <= kSmemPerCta, "smem budget");
-  static_assert(2 * TN <= kTmemCols && kTmemCols <= bsk::kTmemCols, "tmem budget");
+  static_assert(kSlots >= 2 && kSlots * TN <= kTmemCols && kTmemCols <= bsk::kTmemCols, "tmem budget");
 };
 
-template <int TN>
+// kSplit == 2: a cluster of two CTAs shares one tile, each streaming half of
+// the K blocks; the peer's fp32 partials reach the leader through distributed
+// shared memory at the end (decode shapes: twice as many SMs pull weights).
+template <int TN, int kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const Fp8Params p) {
@@ -64,13 +72,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stages = base;
   float* ssa = reinterpret_cast<float*>(base + C::kStages * C::kStageBytes);  // [2][KBC][TN]
   float* ssb = ssa + 2 * KBC * TN;                                            // [2][KBC]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kStages * C::kStageBytes + C::kScaleBytes);
+  float* red = reinterpret_cast<float*>(base + C::kStages * C::kStageBytes + C::kScaleBytes);  // [BM][TN]
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(base + C::kStages * C::kStageBytes + C::kScaleBytes + C::kRedBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::kStages;
-  uint64_t* pfull = bars + 2 * C::kStages;     // [2] partial slot written by the tensor core
-  uint64_t* pempty = pfull + 2;                // [2] partial slot read by the epilogue
-  uint64_t* drain = pfull + 4;
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(pfull + 5);
+  uint64_t* pfull = bars + 2 * C::kStages;     // [kSlots] partial slot written by the tensor core
+  uint64_t* pempty = pfull + C::kSlots;        // [kSlots] partial slot read by the epilogue
+  uint64_t* drain = pfull + 2 * C::kSlots;
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_i = reinterpret_cast<int*>(tmem_base + 1);
   volatile int* abort_flag = abort_i;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -80,7 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&pfull[i], 1);
       mbar_init(&pempty[i], 8);
     }
@@ -104,21 +114,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_wblk = (p.N + BM - 1) / BM;
   const int n_tblk = (p.M + TN - 1) / TN;
   const int total = n_wblk * n_tblk;
-  const int nkb = p.K / BK;
+  const int nkb_all = p.K / BK;
+  // split mode: this CTA's K blocks [kb0, kb0 + nkb); tiles are walked per cluster
+  const uint32_t srank = kSplit > 1 ? cluster_ctarank() : 0u;
+  const int kb0 = kSplit > 1 ? (int)srank * ((nkb_all + 1) / 2) : 0;
+  const int nkb = kSplit > 1 ? (srank == 0 ? (nkb_all + 1) / 2 : nkb_all / 2) : nkb_all;
+  const int t_first = kSplit > 1 ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int t_step = kSplit > 1 ? (int)gridDim.x / 2 : (int)gridDim.x;
+
+  // split mode: the tile's partial sums of this thread, kept for the exchange
+  float facc[C::kColsPerWarp];
+  int f_n = 0, f_m0 = 0;
+  bool f_have = false;
+#pragma unroll
+  for (int i = 0; i < C::kColsPerWarp; ++i) facc[i] = 0.0f;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
     PipeState<C::kStages> ps;
     uint32_t issued_mask = 0, last_phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int t = t_first; t < total && ok; t += t_step) {
       const int wb = t % n_wblk, tb = t / n_wblk;
       for (int kb = 0; kb < nkb; ++kb) {
         if (!mbar_wait(&empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 50)) { ok = false; break; }
         uint8_t* st = stages + ps.index * C::kStageBytes;
         mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(BM * BK + TN * BK));
-        tma_load_2d(st, &tmW, &full[ps.index], kb * BK, wb * BM);
-        tma_load_2d(st + BM * BK, &tmX, &full[ps.index], kb * BK, tb * TN);
+        tma_load_2d(st, &tmW, &full[ps.index], (kb0 + kb) * BK, wb * BM);
+        tma_load_2d(st + BM * BK, &tmX, &full[ps.index], (kb0 + kb) * BK, tb * TN);
         issued_mask |= 1u << ps.index;
         last_phase = (last_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
         ps.advance();
@@ -135,26 +158,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
     PipeState<C::kStages> ps;
-    uint32_t slot = 0, slot_phase = 0;  // partial slot ring (2 slots)
+    PipeState<C::kSlots> sl;  // partial slot ring
     constexpr uint32_t idesc = idesc_e4m3(BM, TN);
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int t = t_first; t < total && ok; t += t_step) {
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(&pempty[slot], slot_phase ^ 1u, abort_flag, p.status, 60)) { ok = false; break; }
+        if (!mbar_wait(&pempty[sl.index], sl.phase ^ 1u, abort_flag, p.status, 60)) { ok = false; break; }
         if (!mbar_wait(&full[ps.index], ps.phase, abort_flag, p.status, 61)) { ok = false; break; }
         tc_fence_after();
         uint8_t* st = stages + ps.index * C::kStageBytes;
         const uint32_t sw = smem_u32(st), sx = smem_u32(st + BM * BK);
-        const uint32_t d = tmem + slot * TN;
+        const uint32_t d = tmem + sl.index * TN;
 #pragma unroll
         for (int j = 0; j < BK / 32; ++j)
           mma_e4m3(d, smem_desc(sw + 32 * j, 16, 1024, kLayoutSw128), smem_desc(sx + 32 * j, 16, 1024, kLayoutSw128),
                    idesc, j > 0 ? 1u : 0u);
         tc_commit(&empty[ps.index]);
-        tc_commit(&pfull[slot]);
+        tc_commit(&pfull[sl.index]);
         ps.advance();
-        slot ^= 1u;
-        if (slot == 0) slot_phase ^= 1u;
+        sl.advance();
       }
     }
     tc_commit(drain);
@@ -173,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = half * NC;
     const int etid = threadIdx.x - kEpiWarp0 * 32;  // 0 .. 255
     const int nchunk = (nkb + KBC - 1) / KBC;
-    uint32_t slot = 0, slot_phase = 0;
+    PipeState<C::kSlots> sl;
     bool ok = true;
     auto stage_scales = [&](int t, int c, int buf) {
       const int wb = t % n_wblk, tb = t / n_wblk;
@@ -183,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kbl = i / TN, m = i % TN;
         const int kb = c * KBC + kbl, ma = tb * TN + m;
         const bool valid = kb < nkb && ma < p.M;
-        const float* src = valid ? p.sfa + (size_t)kb * p.M + ma : p.sfa;
+        const float* src = valid ? p.sfa + (size_t)(kb0 + kb) * p.M + ma : p.sfa;
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(da + i)), "l"(src),
                      "r"(valid ? 4 : 0)
                      : "memory");
@@ -191,13 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = etid; i < KBC; i += 256) {
         const int kb = c * KBC + i;
         const bool valid = kb < nkb;
-        const float* src = valid ? p.sfb + (size_t)wb * nkb + kb : p.sfb;
+        const float* src = valid ? p.sfb + (size_t)wb * nkb_all + kb0 + kb : p.sfb;
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(db + i)), "l"(src),
                      "r"(valid ? 4 : 0)
                      : "memory");
       }
     };
-    int t = blockIdx.x, c = 0, qi = 0;
+    int t = t_first, c = 0, qi = 0;
     if (t < total) stage_scales(t, 0, 0);
     asm volatile("cp.async.commit_group;" ::: "memory");
     float acc[NC];
@@ -207,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tn = t, cn = c + 1;
       if (cn == nchunk) {
         cn = 0;
-        tn = t + gridDim.x;
+        tn = t + t_step;
       }
       if (tn < total) stage_scales(tn, cn, (qi + 1) & 1);
       asm volatile("cp.async.commit_group;" ::: "memory");
@@ -219,10 +241,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = wb * BM + q * 32 + lane;            // weight row = output column
       const int m0 = tb * TN + col0;                    // first token of this warp's columns
       const int kb_end = min(nkb, (c + 1) * KBC);
-      for (int kb = c * KBC; kb < kb_end; ++kb) {
+      // Small tiles fold G partial slots per round trip (wait all, load all,
+      // one tcgen05.wait::ld, release all) so the latency of the hand-off is
+      // paid once per G K blocks.
+      constexpr int G = NC <= 32 ? (64 / NC < 8 ? 64 / NC : 8) : 1;
+      int kb = c * KBC;
+      if constexpr (G > 1) {
+        for (; kb + G <= kb_end; kb += G) {
+          uint32_t idx[G];
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            idx[i] = sl.index;
+            if (ok) {
+              int w_ok = 1;
+              if (lane == 0) w_ok = mbar_wait(&pfull[sl.index], sl.phase, abort_flag, p.status, 71) ? 1 : 0;
+              w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+              ok = w_ok != 0;
+            }
+            sl.advance();
+          }
+          if (ok) {
+            tc_fence_after();
+            uint32_t v[G][NC];
+#pragma unroll
+            for (int i = 0; i < G; ++i)
+              tmem_ld_cols<NC>(tmem + ((uint32_t)(q * 32) << 16) + idx[i] * TN + col0, v[i]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int i = 0; i < G; ++i) mbar_arrive(&pempty[idx[i]]);
+            }
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+              const float sbv = csb[kb + i - c * KBC];
+              const float* sa_row = csa + (kb + i - c * KBC) * TN + col0;
+#pragma unroll
+              for (int j = 0; j < NC; ++j) acc[j] = fmaf(__uint_as_float(v[i][j]), sbv * sa_row[j], acc[j]);
+            }
+          }
+        }
+      }
+      for (; kb < kb_end; ++kb) {
         if (ok) {
           int w_ok = 1;
-          if (lane == 0) w_ok = mbar_wait(&pfull[slot], slot_phase, abort_flag, p.status, 70) ? 1 : 0;
+          if (lane == 0) w_ok = mbar_wait(&pfull[sl.index], sl.phase, abort_flag, p.status, 70) ? 1 : 0;
           w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
           ok = w_ok != 0;
         }
@@ -234,22 +298,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < NC; c0 += CH) {
             uint32_t v[CH];
-            tmem_ld_cols<CH>(tmem + ((uint32_t)(q * 32) << 16) + slot * TN + col0 + c0, v);
+            tmem_ld_cols<CH>(tmem + ((uint32_t)(q * 32) << 16) + sl.index * TN + col0 + c0, v);
             tmem_ld_wait();
             if (c0 + CH == NC) {
               // every column of the slot is in registers: hand the slot back
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&pempty[slot]);
+              if (lane == 0) mbar_arrive(&pempty[sl.index]);
             }
 #pragma unroll
             for (int i = 0; i < CH; ++i) acc[c0 + i] = fmaf(__uint_as_float(v[i]), sbv * sa_row[c0 + i], acc[c0 + i]);
           }
         }
-        slot ^= 1u;
-        if (slot == 0) slot_phase ^= 1u;
+        sl.advance();
       }
-      if (cn == 0) {
+      if (cn == 0 && kSplit > 1) {
+        // split mode (one tile per cluster): keep the partial for the exchange
+#pragma unroll
+        for (int i = 0; i < NC; ++i) facc[i] = acc[i];
+        f_n = n;
+        f_m0 = m0;
+        f_have = ok;
+      } else if (cn == 0) {
         // the tile's last chunk: write it and reset the accumulators
         if (ok && n < p.N) {
 #pragma unroll
@@ -272,25 +342,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++qi;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (kSplit > 1 && srank == 1 && f_have) {
+      // hand the partial sums to the leader's reduction buffer (DSMEM)
+      const uint32_t dst = mapa_shared(smem_u32(red + (q * 32 + lane) * TN + col0), 0);
+#pragma unroll
+      for (int i = 0; i < NC; ++i)
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + 4 * i), "f"(facc[i]) : "memory");
+    }
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (kSplit > 1) {
+    cluster_sync();  // the peer's partials have landed in the leader's buffer
+    if (srank == 0 && warp >= kEpiWarp0 && f_have && f_n < p.N) {
+      const int q = warp % 4, col0 = ((warp - kEpiWarp0) / 4) * C::kColsPerWarp;
+      const float* other = red + (q * 32 + lane) * TN + col0;
+#pragma unroll
+      for (int i = 0; i < C::kColsPerWarp; ++i) {
+        const int m = f_m0 + i;
+        const float y = facc[i] + (nkb_all > 1 ? other[i] : 0.0f);
+        if (m < p.M) {
+          if (p.out_bf16)
+            reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + f_n] = __float2bfloat16_rn(y);
+          else
+            reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + f_n] = y;
+        }
+      }
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-template <int TN>
+template <int TN, int kSplit>
 static cudaError_t launch_tn(const Fp8Launch& L, cudaStream_t stream) {
   using C = Cfg<TN>;
-  auto kern = fp8_gemm_kernel<TN>;
+  auto kern = fp8_gemm_kernel<TN, kSplit>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, kThreads, C::kSmem, stream>>>(L.tmA, L.tmB, L.p);
-  return cudaGetLastError();
+  if (kSplit == 1) {
+    kern<<<L.grid, kThreads, C::kSmem, stream>>>(L.tmA, L.tmB, L.p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)L.grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.p);
 }
 
 }  // namespace fp8
@@ -303,11 +413,19 @@ int fp8_tile_n(long long M) {
 }
 
 cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream) {
+  if (L.p.splits == 2) {
+    if (L.grid <= 0 || (L.grid & 1)) return cudaErrorInvalidValue;
+    switch (L.tile_n) {
+      case 16: return fp8::launch_tn<16, 2>(L, stream);
+      case 32: return fp8::launch_tn<32, 2>(L, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (L.tile_n) {
-    case 16: return fp8::launch_tn<16>(L, stream);
-    case 32: return fp8::launch_tn<32>(L, stream);
-    case 64: return fp8::launch_tn<64>(L, stream);
-    case 128: return fp8::launch_tn<128>(L, stream);
+    case 16: return fp8::launch_tn<16, 1>(L, stream);
+    case 32: return fp8::launch_tn<32, 1>(L, stream);
+    case 64: return fp8::launch_tn<64, 1>(L, stream);
+    case 128: return fp8::launch_tn<128, 1>(L, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -28,6 +28,8 @@ struct Fp4Params {
   float* out32;
   long long ld_out32;
   int* status;
+  int sched;              // scale-copy / MMA issue order (see gemm_fp4.cu)
+  int n_chunk;            // grouped tile order: column blocks per chunk (0 = all)
 };
 
 struct Fp4Launch {
@@ -50,7 +52,7 @@ struct Fp4PairLaunch {
   int grid;               // even: two CTAs per cluster
 };
 cudaError_t launch_fp4_pair_gemm(const Fp4PairLaunch& L, cudaStream_t stream);
-int fp4_pair_stages(bool lora);
+int fp4_pair_stages(bool lora, int bk);
 
 struct Fp8Params {
   const float* sfa;       // [K/128, M]

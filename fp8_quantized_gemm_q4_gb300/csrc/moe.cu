@@ -4,13 +4,14 @@
 // Grouping ("DeepGEMM teardown (FP8 GEMM)", section 5.3: pass group offsets,
 // keep each expert's rows contiguous and movable in blocks) is a stable
 // counting sort over the flattened pair index p = t*k + slot:
-//   1. count:  one warp per chunk of 1024 pairs -> histogram [chunk][E]
+//   1. count:  one CTA per chunk of 1024 pairs -> histogram [chunk][E]
 //   2. scan:   one CTA: per-expert running sums over chunks (stable bases),
 //              counts, and 128-aligned segment offsets
-//   3. place:  one warp per chunk, pairs in order; ranks among equal experts
-//              inside each 32-pair round come from __match_any_sync, so the
-//              result is identical to a sequential stable sort; padding rows
-//              get pair/token -1 and weight 0
+//   3. place:  one CTA per chunk, each warp a 128-pair slice in order; ranks
+//              among equal experts inside each 32-pair round come from
+//              __match_any_sync and warp bases from a prefix over the warps,
+//              so the result is identical to a sequential stable sort;
+//              padding rows get pair/token -1 and weight 0
 #include <mutex>
 
 #include "kernels.h"
@@ -21,14 +22,15 @@ namespace bsk {
 constexpr int kChunk = 1024;
 constexpr int kSegAlign = 128;
 
-__global__ void __launch_bounds__(32) moe_count_kernel(const int* __restrict__ ids, long long P, int E,
-                                                       int* __restrict__ hist, int* status) {
+constexpr int kDispatchThreads = 256;  // 8 warps per chunk
+
+__global__ void __launch_bounds__(kDispatchThreads) moe_count_kernel(const int* __restrict__ ids, long long P, int E,
+                                                                     int* __restrict__ hist, int* status) {
   extern __shared__ int cnt[];
-  const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) cnt[e] = 0;
-  __syncwarp();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
   const long long p0 = (long long)blockIdx.x * kChunk;
-  for (int i = lane; i < kChunk; i += 32) {
+  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) {
     const long long p = p0 + i;
     if (p >= P) break;
     const int e = ids[p];
@@ -38,8 +40,8 @@ __global__ void __launch_bounds__(32) moe_count_kernel(const int* __restrict__ i
     }
     atomicAdd(&cnt[e], 1);
   }
-  __syncwarp();
-  for (int e = lane; e < E; e += 32) hist[(long long)blockIdx.x * E + e] = cnt[e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(long long)blockIdx.x * E + e] = cnt[e];
 }
 
 __global__ void __launch_bounds__(1024) moe_scan_kernel(int* __restrict__ hist, int nchunks, int E,
@@ -87,18 +89,41 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int* __restrict__ hist, 
     for (int c = 0; c < nchunks; ++c) hist[(long long)c * E + e] += padded[e];
 }
 
-__global__ void __launch_bounds__(32) moe_place_kernel(const int* __restrict__ ids, const float* __restrict__ w,
-                                                       long long P, int k, int E, const int* __restrict__ base,
-                                                       const int* __restrict__ counts,
-                                                       const int* __restrict__ offsets, int* __restrict__ pair_of_row,
-                                                       int* __restrict__ token_of, float* __restrict__ weight_of,
-                                                       long long rows_bound) {
-  extern __shared__ int pos[];
-  const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) pos[e] = base[(long long)blockIdx.x * E + e];
-  __syncwarp();
-  const long long p0 = (long long)blockIdx.x * kChunk;
-  for (int i = 0; i < kChunk; i += 32) {
+// Placement of one chunk by 8 warps: warp w owns pairs [128 w, 128 w + 128) of
+// the chunk.  Its first position for expert e is the chunk's base plus the
+// counts of warps 0 .. w-1 for e (a prefix over warps in shared memory); inside
+// the warp, 32-pair rounds in order with __match_any_sync ranks.  The result
+// equals a sequential stable sort.
+__global__ void __launch_bounds__(kDispatchThreads) moe_place_kernel(
+    const int* __restrict__ ids, const float* __restrict__ w, long long P, int k, int E, const int* __restrict__ base,
+    const int* __restrict__ counts, const int* __restrict__ offsets, int* __restrict__ pair_of_row,
+    int* __restrict__ token_of, float* __restrict__ weight_of, long long rows_bound) {
+  extern __shared__ int pos[];  // [8][E]: per-warp counts, then per-warp running positions
+  constexpr int kWarps = kDispatchThreads / 32;
+  constexpr int kPerWarp = kChunk / kWarps;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) pos[i] = 0;
+  __syncthreads();
+  const long long p0 = (long long)blockIdx.x * kChunk + (long long)warp * kPerWarp;
+  for (int i = lane; i < kPerWarp; i += 32) {
+    const long long p = p0 + i;
+    if (p < P) {
+      const int e = ids[p];
+      if (e >= 0 && e < E) atomicAdd(&pos[warp * E + e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = base[(long long)blockIdx.x * E + e];
+    for (int v = 0; v < kWarps; ++v) {
+      const int c = pos[v * E + e];
+      pos[v * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  int* my = pos + warp * E;
+  for (int i = 0; i < kPerWarp; i += 32) {
     const long long p = p0 + i + lane;
     const bool live = p < P;
     int e = live ? ids[p] : -1;
@@ -107,9 +132,9 @@ __global__ void __launch_bounds__(32) moe_place_kernel(const int* __restrict__ i
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const int leader = __ffs(peers) - 1;
     int slot = 0;
-    if (e >= 0) slot = pos[e] + rank;
+    if (e >= 0) slot = my[e] + rank;
     __syncwarp();
-    if (e >= 0 && lane == leader) pos[e] += __popc(peers);
+    if (e >= 0 && lane == leader) my[e] += __popc(peers);
     __syncwarp();
     if (e >= 0) {
       pair_of_row[slot] = (int)p;
@@ -117,11 +142,11 @@ __global__ void __launch_bounds__(32) moe_place_kernel(const int* __restrict__ i
       weight_of[slot] = w[p];
     }
   }
-  // padding rows: a share of [0, rows_bound) per warp
+  // padding rows: a share of [0, rows_bound) per CTA
   const long long per = (rows_bound + gridDim.x - 1) / gridDim.x;
   const long long r0 = (long long)blockIdx.x * per;
   const long long r1 = min(rows_bound, r0 + per);
-  for (long long r = r0 + lane; r < r1; r += 32) {
+  for (long long r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
     bool pad_row = r >= offsets[E];
     if (!pad_row) {
       int lo = 0, hi = E - 1;  // largest e with offsets[e] <= r
@@ -164,10 +189,11 @@ cudaError_t launch_moe_dispatch(const int* topk_ids, const float* topk_w, long l
   const long long P = T * k;
   const long long nch = moe_chunks(P) > 0 ? moe_chunks(P) : 1;
   const size_t smem = (size_t)E * sizeof(int);
-  moe_count_kernel<<<(unsigned)nch, 32, smem, stream>>>(topk_ids, P, E, work, status);
+  const size_t smem_place = (size_t)(kDispatchThreads / 32) * E * sizeof(int);  // <= 32 KB for E <= 1024
+  moe_count_kernel<<<(unsigned)nch, kDispatchThreads, smem, stream>>>(topk_ids, P, E, work, status);
   moe_scan_kernel<<<1, 1024, 0, stream>>>(work, (int)nch, E, counts, offsets);
-  moe_place_kernel<<<(unsigned)nch, 32, smem, stream>>>(topk_ids, topk_w, P, k, E, work, counts, offsets,
-                                                         pair_of_row, token_of, weight_of, rows_bound);
+  moe_place_kernel<<<(unsigned)nch, kDispatchThreads, smem_place, stream>>>(
+      topk_ids, topk_w, P, k, E, work, counts, offsets, pair_of_row, token_of, weight_of, rows_bound);
   return cudaGetLastError();
 }
 

@@ -20,6 +20,20 @@
 
 namespace bsk {
 
+// Correctly rounded x / s for the quantizers, where s is shared by a whole
+// group: with r = RN(1/s) (__frcp_rn), q0 = RN(x r) is within one ulp of x / s,
+// the remainder x - q0 s is exact in one FMA, and RN(q0 + r (x - q0 s)) is
+// RN(x / s) (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  copysign keeps
+// the sign of a zero quotient.  Three FP operations per element instead of a
+// full IEEE divide; tests/test_quant_gpu.py checks the codes against the
+// oracle for every bf16 value under every reachable e4m3 scale.
+__device__ __forceinline__ float quot_rn(float x, float s, float r) {
+  const float q0 = x * r;
+  const float rem = fmaf(-q0, s, x);
+  return copysignf(fmaf(rem, r, q0), x);
+}
+
 __device__ __forceinline__ void load8(const void* x, int x_bf16, long long off, float (&v)[8]) {
   if (x_bf16) {
     const uint4 raw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(x) + off));
@@ -72,9 +86,10 @@ __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       const uint32_t s_code = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
       const float s = e4m3_to_f32(s_code);
+      const float rs = __frcp_rn(s);
       float q[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = (s == 0.0f) ? 0.0f : __fdiv_rn(v[u][i], s);
+      for (int i = 0; i < 8; ++i) q[i] = (s == 0.0f) ? 0.0f : quot_rn(v[u][i], s, rs);
       const uint32_t word = f32x8_to_e2m1x8(q);
       if (active && row < M) *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + k0 / 2) = word;
       const uint32_t b1 = __shfl_down_sync(0xffffffffu, s_code, 2);
@@ -415,12 +430,13 @@ __global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[16 * g + i]));
         const uint32_t sc = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
         const float sv = e4m3_to_f32(sc);
+        const float rs = __frcp_rn(sv);
         sfh |= sc << (8 * g);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float q[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) q[i] = (sv == 0.0f) ? 0.0f : __fdiv_rn(v[16 * g + 8 * h + i], sv);
+          for (int i = 0; i < 8; ++i) q[i] = (sv == 0.0f) ? 0.0f : quot_rn(v[16 * g + 8 * h + i], sv, rs);
           cw[2 * g + h] = f32x8_to_e2m1x8(q);
         }
       }

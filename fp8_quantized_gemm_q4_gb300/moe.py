@@ -76,6 +76,10 @@ class MoELayer:
         self.hq = torch.empty((self.rows, F // 2), dtype=torch.uint8, device=device)
         self.hs = torch.empty(sf_bytes(self.rows, F), dtype=torch.uint8, device=device)
         self.out32 = torch.zeros((T, H), dtype=torch.float32, device=device)
+        # Down GEMM tile order: chunks of 256-column blocks small enough that
+        # the fp32 accumulator slab they reduce into (T x 256 x 4 bytes per
+        # block) stays within about half of the 129 MB L2.
+        self.combine_chunk = max(1, (64 << 20) // (T * 256 * 4))
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
         self.disp = None
         from . import load
@@ -93,6 +97,6 @@ class MoELayer:
         q4_quantize(self.h, out=(self.hq, self.hs, None))
         grouped_gemm_fp4(self.hq, self.hs, w.wd_codes, w.wd_sf, K=w.F, N=w.H, E=w.E, offsets=d["offsets"],
                          counts=d["counts"], epilogue=EPI_COMBINE, token_of=d["token_of"],
-                         weight_of=d["weight_of"], out32=self.out32)
+                         weight_of=d["weight_of"], out32=self.out32, n_chunk_blocks=self.combine_chunk)
         moe_finalize(self.out32, self.out)
         return self.out

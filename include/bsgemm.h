@@ -167,6 +167,7 @@ bs_status q8_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t 
  *   out        [M, ldo] fp32 or bf16 (out_dtype), 16-byte aligned, ldo % 8 == 0
  *   M >= 0, N % 128 == 0, K % 64 == 0 (FP4) or K % 128 == 0 (FP8)
  *   num_sms    persistent grid size limit (0 = all SMs)
+ *   n_chunk_blocks  ignored by bs_gemm (grouped tile-order knob)
  * ------------------------------------------------------------------------- */
 typedef struct {
     int fmt;                 /* bs_format */
@@ -185,6 +186,9 @@ typedef struct {
     int out_dtype;           /* bs_dtype */
     int64_t ldo;
     int num_sms;
+    int n_chunk_blocks;      /* grouped only: tile order walks chunks of this many output
+                                column blocks (256 columns; 128 for SWIGLU), all experts per
+                                chunk; 0 = one chunk.  Bounds the live out32 slab of COMBINE */
 } bs_gemm_args;
 
 bs_status bs_gemm(const bs_gemm_args *args, bs_stream_t stream);

@@ -61,13 +61,18 @@ def _small_moe(T=200, H=256, F=128, E=5, k=2, seed=3):
     return r, x, ws
 
 
-@pytest.mark.parametrize("T,H,F,E,k", [(200, 256, 128, 5, 2), (1000, 512, 256, 8, 4), (64, 256, 128, 16, 8)])
-def test_grouped_layer_staged(cuda_lib, T, H, F, E, k):
+@pytest.mark.parametrize("T,H,F,E,k,chunk", [(200, 256, 128, 5, 2, 0), (1000, 512, 256, 8, 4, 0),
+                                             (64, 256, 128, 16, 8, 0), (300, 1024, 256, 6, 2, 1),
+                                             (300, 1024, 256, 6, 2, 3)])
+def test_grouped_layer_staged(cuda_lib, T, H, F, E, k, chunk):
+    """chunk > 0: the down GEMM walks column chunks of that many 256-wide blocks."""
     bs = cuda_lib
     from fp8_quantized_gemm_q4_gb300.moe import MoELayer, quantize_expert_weights
     r, x, ws = _small_moe(T, H, F, E, k)
     W = quantize_expert_weights([a for a, _ in ws], [b for _, b in ws])
     layer = MoELayer(W, T, k)
+    if chunk:
+        layer.combine_chunk = chunk
     out = layer.forward(x.cuda(), torch.from_numpy(r["topk_ids"]).cuda(), torch.from_numpy(r["topk_w"]).cuda())
     torch.cuda.synchronize()
     assert bs.device_status()[0] == 0

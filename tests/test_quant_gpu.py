@@ -61,6 +61,52 @@ def test_q4_quantize_gather(cuda_lib):
     assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), 8, 256), os_)
 
 
+def _all_bf16_under_every_scale():
+    """Groups whose amax is 6 s for each finite positive e4m3 value s (so the
+    group scale is exactly s), filled with every bf16 value of magnitude in
+    (s / 8, 6 s] with both signs: every quotient x / s that can decide a code."""
+    e4 = oracle.e4m3_table()[1:127]
+    allbf = torch.arange(0, 1 << 15, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float()
+    allbf = allbf[torch.isfinite(allbf) & (allbf > 0)]
+    rows = []
+    for sv in e4:
+        sv = float(sv)
+        vals = allbf[(allbf > sv / 8) & (allbf <= 6 * sv)]
+        vals = torch.cat([vals, -vals])
+        n = (len(vals) + 14) // 15 * 15
+        vals = torch.cat([vals, torch.zeros(n - len(vals))]).view(-1, 15)
+        head = torch.full((vals.shape[0], 1), 6 * sv)
+        rows.append(torch.cat([head, vals], dim=1))
+    g = torch.cat(rows).reshape(-1)
+    pad = (-len(g)) % 256
+    return torch.cat([g, torch.zeros(pad)]).view(-1, 256)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_q4_quantize_exhaustive_bf16_quotients(cuda_lib, dtype):
+    bs = cuda_lib
+    x = _all_bf16_under_every_scale().to(dtype)
+    codes, sf, _ = bs.q4_quantize(x.cuda())
+    torch.cuda.synchronize()
+    oc, os_ = oracle.q4_quantize(x)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), x.shape[0], 256), os_)
+
+
+def test_q4_lowrank_fused_exhaustive_bf16_quotients(cuda_lib):
+    """The fused quantize + low-rank pass on the same exhaustive value set."""
+    bs = cuda_lib
+    x = _all_bf16_under_every_scale().to(torch.bfloat16)
+    x = x.reshape(-1, 1024) if x.numel() % 1024 == 0 else torch.cat(
+        [x.reshape(-1), torch.zeros((-x.numel()) % 1024, dtype=x.dtype)]).view(-1, 1024)
+    a = (torch.randn(1024, 32) * 0.02).to(torch.bfloat16)
+    codes, sf, _ = bs.q4_quantize(x.cuda(), lora_a_t=a.t().contiguous().cuda())
+    torch.cuda.synchronize()
+    oc, os_ = oracle.q4_quantize(x)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), x.shape[0], 1024), os_)
+
+
 @pytest.mark.parametrize("rows_in,rows_out,K", [(50, 8, 256), (4096, 1000, 4096), (7, 300, 64)])
 def test_fp4_gather_rows_equals_quantize_with_gather(cuda_lib, rows_in, rows_out, K):
     bs = cuda_lib
