@@ -315,8 +315,8 @@ class MoEWorkload:
         W = MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf)
         self.layer = MoELayer(W, self.T, self.k, device=dev)
         self.out = self.layer.out
-        # dispatch 3 + quantize 1 + gather 1 + gemm 1 + quantize 1 + gemm 1 + finalize 1
-        self.launches_per_step = 9
+        # dispatch 3 + quantize 1 + gather 1 + gemm 1 + quantize 1 + gemm 1 + finalize 2 (cast, zero)
+        self.launches_per_step = 10
         self.bytes_in = self.x.numel() * 2 + self.ids.numel() * 4 + self.w.numel() * 4
         self.bytes_out = self.out.numel() * 2
         counts = torch.bincount(self.ids.flatten().long(), minlength=E).cpu()

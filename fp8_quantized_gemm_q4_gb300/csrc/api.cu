@@ -291,20 +291,9 @@ static bool fp8_split_ok() {
   return on;
 }
 
-// Issue order of scale copies and MMAs in the FP4 kernel (BSGEMM_FP4_SCHED).
-static int fp4_sched() {
-  static int v = [] {
-    const char* e = getenv("BSGEMM_FP4_SCHED");
-    const int v = e ? atoi(e) : 0;
-    return (v >= 0 && v <= 2) ? v : 0;  // only the three complete issue orders exist
-  }();
-  return v;
-}
-
 static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int sms, cudaStream_t s,
                             long long pair_tiles, bool grouped) {
   bs_status st;
-  L.p.sched = fp4_sched();
   if (fp4_pair()) {
     bsk::Fp4PairLaunch P;
     memset(&P, 0, sizeof P);

@@ -87,6 +87,19 @@ struct Tile {
   int expert;
 };
 
+// Tile fields broadcast from lane 0 (warp-uniform for the issuing roles).
+__device__ __forceinline__ Tile bcast_tile(const Tile& t) {
+  Tile r;
+  r.row0 = warp_bcast(t.row0);
+  r.rows = warp_bcast(t.rows);
+  r.brow0 = warp_bcast(t.brow0);
+  r.brow1 = warp_bcast(t.brow1);
+  r.sfb_blk1 = warp_bcast(t.sfb_blk1);
+  r.col0 = warp_bcast(t.col0);
+  r.expert = warp_bcast(t.expert);
+  return r;
+}
+
 struct Smem {
   uint8_t* stages;
   uint8_t* lora;
@@ -195,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(kAlign - 1));
   using G = Geo<BK>;
   Smem sm = carve<kStages, kLora, G::kStageBytes>(base);
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int warp = warp_bcast((int)(threadIdx.x / 32)), lane = threadIdx.x % 32;
   volatile int* abort_flag = sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -260,39 +273,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *sm.tmem_base;
-  const int total = *sm.total_tiles;
+  const uint32_t tmem = warp_bcast(*sm.tmem_base);
+  const int total = warp_bcast(*sm.total_tiles);
   const int kchunks = p.K / 64;
   const int kstages = (kchunks + G::kMmas - 1) / G::kMmas;
 
-  if (warp == 0 && lane == 0) {
+  // The three issuing roles below run with the whole warp: lane 0 waits on
+  // the barriers (result broadcast), one elected lane issues.
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     PipeState<kStages> ps;
     uint32_t issued_mask = 0, last_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = tile_of<kEpi>(p, sm.prefix, t);
+      const Tile tl = bcast_tile(tile_of<kEpi>(p, sm.prefix, t));
       const uint8_t* sfa_src = p.sfa + (size_t)(tl.row0 / 128) * kchunks * 512;
       const uint8_t* sfb0_src = p.sfb + (size_t)(tl.brow0 / 128) * kchunks * 512;
       const uint8_t* sfb1_src = p.sfb + (size_t)tl.sfb_blk1 * kchunks * 512;
       for (int ks = 0; ks < kstages; ++ks) {
-        if (!mbar_wait(&sm.empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 10)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 10)) { ok = false; break; }
         const int nmma = min(G::kMmas, kchunks - G::kMmas * ks);
         uint8_t* st = sm.stages + ps.index * G::kStageBytes;
         uint64_t* bar = &sm.full[ps.index];
-        mbar_arrive_expect_tx(bar, (uint32_t)((BM + BN) * G::kRowBytes + nmma * 512 * 3));
-        tma_load_2d(st + G::kOffA, &tmA, bar, ks * G::kRowBytes, tl.row0);
-        tma_load_2d(st + G::kOffB, &tmB, bar, ks * G::kRowBytes, tl.brow0);
-        tma_load_2d(st + G::kOffB + 128 * G::kRowBytes, &tmB, bar, ks * G::kRowBytes, tl.brow1);
-        bulk_load(st + G::kOffSfa, sfa_src + ks * G::kMmas * 512, nmma * 512, bar);
-        bulk_load(st + G::kOffSfb, sfb0_src + ks * G::kMmas * 512, nmma * 512, bar);
-        bulk_load(st + G::kOffSfb + G::kMmas * 512, sfb1_src + ks * G::kMmas * 512, nmma * 512, bar);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar, (uint32_t)((BM + BN) * G::kRowBytes + nmma * 512 * 3));
+          tma_load_2d(st + G::kOffA, &tmA, bar, ks * G::kRowBytes, tl.row0);
+          tma_load_2d(st + G::kOffB, &tmB, bar, ks * G::kRowBytes, tl.brow0);
+          tma_load_2d(st + G::kOffB + 128 * G::kRowBytes, &tmB, bar, ks * G::kRowBytes, tl.brow1);
+          bulk_load(st + G::kOffSfa, sfa_src + ks * G::kMmas * 512, nmma * 512, bar);
+          bulk_load(st + G::kOffSfb, sfb0_src + ks * G::kMmas * 512, nmma * 512, bar);
+          bulk_load(st + G::kOffSfb + G::kMmas * 512, sfb1_src + ks * G::kMmas * 512, nmma * 512, bar);
+        }
+        __syncwarp();
         issued_mask |= 1u << ps.index;
         last_phase = (last_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
         ps.advance();
       }
     }
-    if (*abort_flag) {
+    if (*abort_flag && lane == 0) {
       // Let copies already in flight land before the CTA can exit.
       for (int s = 0; s < kStages; ++s)
         if (issued_mask & (1u << s)) {
@@ -301,116 +319,109 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
     }
-  } else if (warp == 2 && lane == 0) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------------ low-rank producer
     if (kLora) {
       uint32_t phase = 0;
       bool issued = false;
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const Tile tl = tile_of<kEpi>(p, sm.prefix, t);
-        if (!mbar_wait(sm.lora_empty, phase ^ 1u, abort_flag, p.status, 20)) break;
-        mbar_arrive_expect_tx(sm.lora_full, (uint32_t)kLoraBytes);
-        tma_load_2d(sm.lora + kLoraThi, &tmT, sm.lora_full, 0, tl.row0);
-        tma_load_2d(sm.lora + kLoraTlo, &tmT, sm.lora_full, 32, tl.row0);
-        tma_load_2d(sm.lora + kLoraBl, &tmL, sm.lora_full, 0, tl.brow0);
-        tma_load_2d(sm.lora + kLoraBl + 8192, &tmL, sm.lora_full, 0, tl.brow1);
+        const Tile tl = bcast_tile(tile_of<kEpi>(p, sm.prefix, t));
+        if (!mbar_wait_warp(sm.lora_empty, phase ^ 1u, abort_flag, p.status, 20)) break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(sm.lora_full, (uint32_t)kLoraBytes);
+          tma_load_2d(sm.lora + kLoraThi, &tmT, sm.lora_full, 0, tl.row0);
+          tma_load_2d(sm.lora + kLoraTlo, &tmT, sm.lora_full, 32, tl.row0);
+          tma_load_2d(sm.lora + kLoraBl, &tmL, sm.lora_full, 0, tl.brow0);
+          tma_load_2d(sm.lora + kLoraBl + 8192, &tmL, sm.lora_full, 0, tl.brow1);
+        }
+        __syncwarp();
         issued = true;
         phase ^= 1u;
       }
-      if (*abort_flag && issued) {
+      if (*abort_flag && issued && lane == 0) {
         const uint64_t t0 = globaltimer();
         while (!mbar_try_wait(sm.lora_full, phase ^ 1u) && globaltimer() - t0 < 100000000ull) {
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // Scale copies (tcgen05.cp) and MMAs share the tensor core's in-order
-    // stream, so their order matters.  p.sched 0: a stage's copies, then its
-    // MMAs.  1: each MMA right after its own copies.  2: like 1, and the
-    // copies of the next stage are issued before the MMAs of this one (one
-    // stage of look-ahead; the scale buffers alternate by stage).
+    // Per stage: the scale copies (tcgen05.cp, smem -> tensor memory), then the
+    // MMAs that read them; both go through the tensor core's in-order stream.
+    // Descriptors are built once for stage 0 and advanced by byte offset / 16
+    // in their start-address field.
     PipeState<kStages> ps;
     uint32_t acc_phase = 0, lora_phase = 0, sf_buf = 0;
-    const int sched = p.sched;
     bool ok = true;
-    auto issue_cps = [&](uint8_t* st, int nmma, uint32_t buf) {
-      const uint32_t ssfa = smem_u32(st + G::kOffSfa), ssfb = smem_u32(st + G::kOffSfb);
-      for (int j = 0; j < nmma; ++j) {
-        const uint32_t col = tmem + kTmemSf + buf * G::kSfColsPerStage + j * kSfColsPerMma;
-        tc_cp_32x128b_warpx4(col, smem_desc(ssfa + 512 * j, 0, 128, kLayoutNone));
-        tc_cp_32x128b_warpx4(col + 4, smem_desc(ssfb + 512 * j, 0, 128, kLayoutNone));
-        tc_cp_32x128b_warpx4(col + 8, smem_desc(ssfb + G::kMmas * 512 + 512 * j, 0, 128, kLayoutNone));
-      }
-    };
+    const uint64_t dA = smem_desc(smem_u32(sm.stages + G::kOffA), 16, G::kSbo, G::kLayout);
+    const uint64_t dB = smem_desc(smem_u32(sm.stages + G::kOffB), 16, G::kSbo, G::kLayout);
+    const uint64_t dSfa = smem_desc(smem_u32(sm.stages + G::kOffSfa), 0, 128, kLayoutNone);
+    const uint64_t dSfb = smem_desc(smem_u32(sm.stages + G::kOffSfb), 0, 128, kLayoutNone);
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      if (!mbar_wait(sm.acc_empty, acc_phase ^ 1u, abort_flag, p.status, 30)) break;
+      if (!mbar_wait_warp(sm.acc_empty, acc_phase ^ 1u, abort_flag, p.status, 30)) break;
       tc_fence_after();
-      bool next_cps_done = false;  // sched 2: copies of the current stage already issued
       for (int ks = 0; ks < kstages; ++ks) {
-        if (!mbar_wait(&sm.full[ps.index], ps.phase, abort_flag, p.status, 31)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.full[ps.index], ps.phase, abort_flag, p.status, 31)) { ok = false; break; }
         tc_fence_after();
         const int nmma = min(G::kMmas, kchunks - G::kMmas * ks);
-        uint8_t* st = sm.stages + ps.index * G::kStageBytes;
-        const uint32_t sa = smem_u32(st + G::kOffA), sb = smem_u32(st + G::kOffB);
-        const uint32_t ssfa = smem_u32(st + G::kOffSfa), ssfb = smem_u32(st + G::kOffSfb);
-        const uint32_t sf_col = kTmemSf + sf_buf * G::kSfColsPerStage;
-        if (sched == 0) {
-          issue_cps(st, nmma, sf_buf);
-        } else if (sched == 2) {
-          if (!next_cps_done) issue_cps(st, nmma, sf_buf);
-          next_cps_done = false;
-          // look ahead: the next stage of this tile, if its data is already there
-          if (ks + 1 < kstages) {
-            const uint32_t ni = ps.index + 1 == (uint32_t)kStages ? 0 : ps.index + 1;
-            const uint32_t nph = ps.index + 1 == (uint32_t)kStages ? ps.phase ^ 1u : ps.phase;
-            if (mbar_try_wait(&sm.full[ni], nph)) {
-              tc_fence_after();
-              issue_cps(sm.stages + ni * G::kStageBytes, min(G::kMmas, kchunks - G::kMmas * (ks + 1)), sf_buf ^ 1u);
-              next_cps_done = true;
+        const uint64_t so = (uint64_t)((ps.index * G::kStageBytes) >> 4);
+        const uint32_t sf_col = tmem + kTmemSf + sf_buf * G::kSfColsPerStage;
+        if (elect_one()) {
+#pragma unroll
+          for (int j = 0; j < G::kMmas; ++j) {
+            if (j < nmma) {
+              const uint32_t col = sf_col + j * kSfColsPerMma;
+              tc_cp_32x128b_warpx4(col, dSfa + so + 32 * j);                      // 512 B per block
+              tc_cp_32x128b_warpx4(col + 4, dSfb + so + 32 * j);
+              tc_cp_32x128b_warpx4(col + 8, dSfb + so + 32 * (G::kMmas + j));
             }
           }
-        }
-        for (int j = 0; j < nmma; ++j) {
-          const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
-          if (sched == 1) {
-            tc_cp_32x128b_warpx4(col, smem_desc(ssfa + 512 * j, 0, 128, kLayoutNone));
-            tc_cp_32x128b_warpx4(col + 4, smem_desc(ssfb + 512 * j, 0, 128, kLayoutNone));
-            tc_cp_32x128b_warpx4(col + 8, smem_desc(ssfb + G::kMmas * 512 + 512 * j, 0, 128, kLayoutNone));
+#pragma unroll
+          for (int j = 0; j < G::kMmas; ++j) {
+            if (j < nmma) {
+              const uint32_t col = sf_col + j * kSfColsPerMma;
+              mma_mxf4nvf4(tmem + kTmemAcc, dA + so + 2 * j, dB + so + 2 * j, kIdescMain, col, col + 4,
+                           (ks > 0 || j > 0) ? 1u : 0u);                         // 32 B of K per MMA
+            }
           }
-          mma_mxf4nvf4(tmem + kTmemAcc, smem_desc(sa + 32 * j, 16, G::kSbo, G::kLayout),
-                       smem_desc(sb + 32 * j, 16, G::kSbo, G::kLayout), kIdescMain, col, col + 4,
-                       (ks > 0 || j > 0) ? 1u : 0u);
+          tc_commit(&sm.empty[ps.index]);
         }
-        tc_commit(&sm.empty[ps.index]);
+        __syncwarp();
         sf_buf ^= 1u;
         ps.advance();
       }
       if (!ok) break;
       if (kLora) {
-        if (!mbar_wait(sm.lora_full, lora_phase, abort_flag, p.status, 32)) break;
+        if (!mbar_wait_warp(sm.lora_full, lora_phase, abort_flag, p.status, 32)) break;
         tc_fence_after();
-        const uint32_t thi = smem_u32(sm.lora + kLoraThi), tlo = smem_u32(sm.lora + kLoraTlo);
-        const uint32_t bl = smem_u32(sm.lora + kLoraBl);
+        if (elect_one()) {
+          const uint32_t thi = smem_u32(sm.lora + kLoraThi), tlo = smem_u32(sm.lora + kLoraTlo);
+          const uint32_t bl = smem_u32(sm.lora + kLoraBl);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t ta = part == 0 ? thi : tlo;
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t ta = part == 0 ? thi : tlo;
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma_bf16(tmem + kTmemAcc, smem_desc(ta + 32 * kk, 16, 512, kLayoutSw64),
-                     smem_desc(bl + 32 * kk, 16, 512, kLayoutSw64), kIdescLora, 1u);
+            for (int kk = 0; kk < 2; ++kk)
+              mma_bf16(tmem + kTmemAcc, smem_desc(ta + 32 * kk, 16, 512, kLayoutSw64),
+                       smem_desc(bl + 32 * kk, 16, 512, kLayoutSw64), kIdescLora, 1u);
+          }
+          tc_commit(sm.lora_empty);
         }
-        tc_commit(sm.lora_empty);
+        __syncwarp();
         lora_phase ^= 1u;
       }
-      tc_commit(sm.acc_full);
+      if (elect_one()) tc_commit(sm.acc_full);
+      __syncwarp();
       acc_phase ^= 1u;
     }
     // Drain: every tcgen05 op issued above has finished before TMEM is freed.
-    tc_commit(sm.drain);
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(sm.drain, 0) && globaltimer() - t0 < 1000000000ull) {
+    if (elect_one()) {
+      tc_commit(sm.drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(sm.drain, 0) && globaltimer() - t0 < 1000000000ull) {
+      }
     }
+    __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp % 4;               // tensor-memory lane quarter

@@ -84,6 +84,18 @@ struct Tile {
   int col0;      // first output column
 };
 
+// Tile fields broadcast from lane 0 (warp-uniform for the issuing roles).
+__device__ __forceinline__ Tile bcast_tile(const Tile& t) {
+  Tile r;
+  r.row0 = warp_bcast(t.row0);
+  r.rows = warp_bcast(t.rows);
+  r.brow0 = warp_bcast(t.brow0);
+  r.brow1 = warp_bcast(t.brow1);
+  r.sfb_blk1 = warp_bcast(t.sfb_blk1);
+  r.col0 = warp_bcast(t.col0);
+  return r;
+}
+
 template <int kEpi>
 __device__ __forceinline__ int n_blocks(const Fp4Params& p) {
   return kEpi == kEpiSwiglu ? p.N / 128 : (p.N + BN - 1) / BN;
@@ -168,8 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* prefix = total_tiles + 2;
   volatile int* abort_flag = abort_i;
 
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint32_t rank = cluster_ctarank();
+  const int warp = warp_bcast((int)(threadIdx.x / 32)), lane = threadIdx.x % 32;
+  const uint32_t rank = warp_bcast(cluster_ctarank());
   const bool leader = rank == 0;
   const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
 
@@ -236,40 +248,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
-  const uint32_t tmem = *tmem_base;
-  const int total = *total_tiles;
+  const uint32_t tmem = warp_bcast(*tmem_base);
+  const int total = warp_bcast(*total_tiles);
   const int kchunks = p.K / 64;
   const int kstages = (kchunks + kMmas - 1) / kMmas;
 
-  if (warp == 0 && lane == 0) {
+  // The three issuing roles below run with the whole warp: lane 0 waits on
+  // the barriers (result broadcast), one elected lane issues.
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     PipeState<kStages> ps;
     uint32_t issued_mask = 0, last_phase = 0;
     bool ok = true;
     for (int t = pair; t < total && ok; t += npairs) {
-      const Tile tl = tile_of<kEpi>(p, prefix, t);
+      const Tile tl = bcast_tile(tile_of<kEpi>(p, prefix, t));
       const int my_row0 = tl.row0 + (int)rank * BM;
       const int my_brow = leader ? tl.brow0 : tl.brow1;
       for (int ks = 0; ks < kstages; ++ks) {
-        if (!mbar_wait(&empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 110)) { ok = false; break; }
+        if (!mbar_wait_warp(&empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 110)) { ok = false; break; }
         uint8_t* st = stages + ps.index * kStageBytes;
-        if (leader) mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(2 * G::kStageTx));
-        const uint32_t bar = mapa_shared(smem_u32(&full[ps.index]), 0);
-        tma_load_2d_pair(st + kOffA, &tmA, bar, ks * kRowBytes, my_row0);
-        tma_load_2d_pair(st + kOffB, &tmB, bar, ks * kRowBytes, my_brow);
+        if (elect_one()) {
+          if (leader) mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(2 * G::kStageTx));
+          const uint32_t bar = mapa_shared(smem_u32(&full[ps.index]), 0);
+          tma_load_2d_pair(st + kOffA, &tmA, bar, ks * kRowBytes, my_row0);
+          tma_load_2d_pair(st + kOffB, &tmB, bar, ks * kRowBytes, my_brow);
 #pragma unroll
-        for (int b = 0; b < G::kSfBoxes; ++b) {
-          const int x = ks * G::kSfWords + b * 256;
-          tma_load_2d_pair(st + kOffSfa + b * 1024, &tmSfa, bar, x, my_row0 / 128);
-          tma_load_2d_pair(st + kOffSfb + b * 1024, &tmSfb, bar, x, tl.brow0 / 128);
-          tma_load_2d_pair(st + kOffSfb + kMmas * 512 + b * 1024, &tmSfb, bar, x, tl.sfb_blk1);
+          for (int b = 0; b < G::kSfBoxes; ++b) {
+            const int x = ks * G::kSfWords + b * 256;
+            tma_load_2d_pair(st + kOffSfa + b * 1024, &tmSfa, bar, x, my_row0 / 128);
+            tma_load_2d_pair(st + kOffSfb + b * 1024, &tmSfb, bar, x, tl.brow0 / 128);
+            tma_load_2d_pair(st + kOffSfb + kMmas * 512 + b * 1024, &tmSfb, bar, x, tl.sfb_blk1);
+          }
         }
+        __syncwarp();
         issued_mask |= 1u << ps.index;
         last_phase = (last_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
         ps.advance();
       }
     }
-    if (*abort_flag && leader) {
+    if (*abort_flag && leader && lane == 0) {
       for (int s = 0; s < kStages; ++s)
         if (issued_mask & (1u << s)) {
           const uint64_t t0 = globaltimer();
@@ -277,78 +294,100 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
     }
-  } else if (warp == 2 && lane == 0) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------------ low-rank producer (both CTAs)
     if (kLora) {
       uint32_t phase = 0;
       for (int t = pair; t < total; t += npairs) {
-        const Tile tl = tile_of<kEpi>(p, prefix, t);
-        if (!mbar_wait(lora_empty, phase ^ 1u, abort_flag, p.status, 120)) break;
-        if (leader) mbar_arrive_expect_tx(lora_full, (uint32_t)(2 * kLoraBytes));
-        const uint32_t bar = mapa_shared(smem_u32(lora_full), 0);
-        const int my_row0 = tl.row0 + (int)rank * BM;
-        tma_load_2d_pair(lora + kLoraThi, &tmT, bar, 0, my_row0);
-        tma_load_2d_pair(lora + kLoraTlo, &tmT, bar, 32, my_row0);
-        tma_load_2d_pair(lora + kLoraBl, &tmL, bar, 0, leader ? tl.brow0 : tl.brow1);
+        const Tile tl = bcast_tile(tile_of<kEpi>(p, prefix, t));
+        if (!mbar_wait_warp(lora_empty, phase ^ 1u, abort_flag, p.status, 120)) break;
+        if (elect_one()) {
+          if (leader) mbar_arrive_expect_tx(lora_full, (uint32_t)(2 * kLoraBytes));
+          const uint32_t bar = mapa_shared(smem_u32(lora_full), 0);
+          const int my_row0 = tl.row0 + (int)rank * BM;
+          tma_load_2d_pair(lora + kLoraThi, &tmT, bar, 0, my_row0);
+          tma_load_2d_pair(lora + kLoraTlo, &tmT, bar, 32, my_row0);
+          tma_load_2d_pair(lora + kLoraBl, &tmL, bar, 0, leader ? tl.brow0 : tl.brow1);
+        }
+        __syncwarp();
         phase ^= 1u;
       }
     }
-  } else if (warp == 1 && lane == 0 && leader) {
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------------ MMA issuer (leader only)
+    // Descriptors are built once for stage 0 and advanced by byte offset / 16
+    // in their start-address field.
     PipeState<kStages> ps;
     uint32_t acc_phase = 0, lora_phase = 0, sf_buf = 0;
     bool ok = true;
+    const uint64_t dA = smem_desc(smem_u32(stages + kOffA), 16, kSbo, G::kLayout);
+    const uint64_t dB = smem_desc(smem_u32(stages + kOffB), 16, kSbo, G::kLayout);
+    const uint64_t dSfa = smem_desc(smem_u32(stages + kOffSfa), 0, 128, kLayoutNone);
+    const uint64_t dSfb = smem_desc(smem_u32(stages + kOffSfb), 0, 128, kLayoutNone);
     for (int t = pair; t < total && ok; t += npairs) {
-      if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status, 130)) break;
+      if (!mbar_wait_warp(acc_empty, acc_phase ^ 1u, abort_flag, p.status, 130)) break;
       tc_fence_after();
       for (int ks = 0; ks < kstages; ++ks) {
-        if (!mbar_wait(&full[ps.index], ps.phase, abort_flag, p.status, 131)) { ok = false; break; }
+        if (!mbar_wait_warp(&full[ps.index], ps.phase, abort_flag, p.status, 131)) { ok = false; break; }
         tc_fence_after();
         const int nmma = min(kMmas, kchunks - kMmas * ks);
-        uint8_t* st = stages + ps.index * kStageBytes;
-        const uint32_t sa = smem_u32(st + kOffA), sb = smem_u32(st + kOffB);
-        const uint32_t ssfa = smem_u32(st + kOffSfa), ssfb = smem_u32(st + kOffSfb);
-        const uint32_t sf_col = kTmemSf + sf_buf * kSfColsPerStage;
-        for (int j = 0; j < nmma; ++j) {
-          const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
-          tc_cp_32x128b_warpx4_pair(col, smem_desc(ssfa + 512 * j, 0, 128, kLayoutNone));
-          tc_cp_32x128b_warpx4_pair(col + 4, smem_desc(ssfb + 512 * j, 0, 128, kLayoutNone));
-          tc_cp_32x128b_warpx4_pair(col + 8, smem_desc(ssfb + kMmas * 512 + 512 * j, 0, 128, kLayoutNone));
+        const uint64_t so = (uint64_t)((ps.index * kStageBytes) >> 4);
+        const uint32_t sf_col = tmem + kTmemSf + sf_buf * kSfColsPerStage;
+        if (elect_one()) {
+#pragma unroll
+          for (int j = 0; j < kMmas; ++j) {
+            if (j < nmma) {
+              const uint32_t col = sf_col + j * kSfColsPerMma;
+              tc_cp_32x128b_warpx4_pair(col, dSfa + so + 32 * j);               // 512 B per block
+              tc_cp_32x128b_warpx4_pair(col + 4, dSfb + so + 32 * j);
+              tc_cp_32x128b_warpx4_pair(col + 8, dSfb + so + 32 * (kMmas + j));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kMmas; ++j) {
+            if (j < nmma) {
+              const uint32_t col = sf_col + j * kSfColsPerMma;
+              mma_mxf4nvf4_pair(tmem + kTmemAcc, dA + so + 2 * j, dB + so + 2 * j, kIdescMain, col, col + 4,
+                                (ks > 0 || j > 0) ? 1u : 0u);                    // 32 B of K per MMA
+            }
+          }
+          tc_commit_pair_multicast(&empty[ps.index], 0x3);
         }
-        for (int j = 0; j < nmma; ++j) {
-          const uint32_t col = tmem + sf_col + j * kSfColsPerMma;
-          mma_mxf4nvf4_pair(tmem + kTmemAcc, smem_desc(sa + 32 * j, 16, kSbo, G::kLayout),
-                            smem_desc(sb + 32 * j, 16, kSbo, G::kLayout), kIdescMain, col, col + 4,
-                            (ks > 0 || j > 0) ? 1u : 0u);
-        }
-        tc_commit_pair_multicast(&empty[ps.index], 0x3);
+        __syncwarp();
         sf_buf ^= 1u;
         ps.advance();
       }
       if (!ok) break;
       if (kLora) {
-        if (!mbar_wait(lora_full, lora_phase, abort_flag, p.status, 132)) break;
+        if (!mbar_wait_warp(lora_full, lora_phase, abort_flag, p.status, 132)) break;
         tc_fence_after();
-        const uint32_t thi = smem_u32(lora + kLoraThi), tlo = smem_u32(lora + kLoraTlo);
-        const uint32_t bl = smem_u32(lora + kLoraBl);
+        if (elect_one()) {
+          const uint32_t thi = smem_u32(lora + kLoraThi), tlo = smem_u32(lora + kLoraTlo);
+          const uint32_t bl = smem_u32(lora + kLoraBl);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t ta = part == 0 ? thi : tlo;
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t ta = part == 0 ? thi : tlo;
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma_bf16_pair(tmem + kTmemAcc, smem_desc(ta + 32 * kk, 16, 512, kLayoutSw64),
-                          smem_desc(bl + 32 * kk, 16, 512, kLayoutSw64), kIdescLora, 1u);
+            for (int kk = 0; kk < 2; ++kk)
+              mma_bf16_pair(tmem + kTmemAcc, smem_desc(ta + 32 * kk, 16, 512, kLayoutSw64),
+                            smem_desc(bl + 32 * kk, 16, 512, kLayoutSw64), kIdescLora, 1u);
+          }
+          tc_commit_pair_multicast(lora_empty, 0x3);
         }
-        tc_commit_pair_multicast(lora_empty, 0x3);
+        __syncwarp();
         lora_phase ^= 1u;
       }
-      tc_commit_pair_multicast(acc_full, 0x3);
+      if (elect_one()) tc_commit_pair_multicast(acc_full, 0x3);
+      __syncwarp();
       acc_phase ^= 1u;
     }
-    tc_commit_pair_local(drain);
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 1000000000ull) {
+    if (elect_one()) {
+      tc_commit_pair_local(drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 1000000000ull) {
+      }
     }
+    __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ epilogue (both CTAs, own rows)
     const int q = warp % 4;

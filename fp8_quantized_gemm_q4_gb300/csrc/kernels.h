@@ -28,7 +28,6 @@ struct Fp4Params {
   float* out32;
   long long ld_out32;
   int* status;
-  int sched;              // scale-copy / MMA issue order (see gemm_fp4.cu)
   int n_chunk;            // grouped tile order: column blocks per chunk (0 = all)
 };
 

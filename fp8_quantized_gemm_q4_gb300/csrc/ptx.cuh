@@ -86,6 +86,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ---------------------------------------------------------------------------
+// Warp-uniform issue.  A role warp runs its loop with all 32 lanes; one lane
+// waits on a barrier and the result is broadcast, and one elected lane issues
+// each asynchronous copy / MMA.  Values broadcast from lane 0 are known to be
+// the same in every lane, so descriptors and coordinates built from them can
+// live in the warp's uniform registers, which is where tcgen05 and TMA
+// instructions take their operands from.
+// ---------------------------------------------------------------------------
+constexpr unsigned kFullMask = 0xffffffffu;
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_bcast(T v) {
+  return __shfl_sync(kFullMask, v, 0);
+}
+
+// mbar_wait by lane 0 of the calling warp, result broadcast to all lanes.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                               int* status, int site) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status, site) ? 1 : 0;
+  return warp_bcast(ok) != 0;
+}
+
 // Explicit per-role pipeline position: ring slot plus phase bit, advanced
 // explicitly ("Warp-specialised W4A4 kernel", section 5.1: per-warp PipeState).
 template <int kStages>
