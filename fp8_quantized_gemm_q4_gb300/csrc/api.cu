@@ -234,20 +234,16 @@ static bs_status check_common(const bs_gemm_args* a, bool grouped) {
 // faster than 128 (64-byte rows) on GB300 even though the finer ring holds
 // more stages; BSGEMM_FP4_BK=128 selects the finer ring (for measurements).
 static int fp4_bk() {
-  static int bk = [] {
-    const char* e = getenv("BSGEMM_FP4_BK");
-    return (e && atoi(e) == 128) ? 128 : 256;
-  }();
-  return bk;
+  const char* e = getenv("BSGEMM_FP4_BK");
+  return (e && atoi(e) == 128) ? 128 : 256;
 }
 
-// FP4 GEMM on CTA pairs (cta_group::2): BSGEMM_FP4_PAIR=1 selects it.
+// FP4 GEMM on CTA pairs (cta_group::2, 256 x 256 tiles) unless
+// BSGEMM_FP4_PAIR=0 selects the one-CTA kernel (128 x 256 tiles).  Read on
+// every call so one process can run both.
 static bool fp4_pair() {
-  static bool on = [] {
-    const char* e = getenv("BSGEMM_FP4_PAIR");
-    return e && atoi(e) == 1;
-  }();
-  return on;
+  const char* e = getenv("BSGEMM_FP4_PAIR");
+  return !(e && atoi(e) == 0);
 }
 
 static bs_status fp4_maps(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int bk) {
@@ -294,7 +290,7 @@ static bool fp8_split_ok() {
 static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int sms, cudaStream_t s,
                             long long pair_tiles, bool grouped) {
   bs_status st;
-  if (fp4_pair()) {
+  if (fp4_pair() && sms >= 2) {  // a pair needs two SMs
     bsk::Fp4PairLaunch P;
     memset(&P, 0, sizeof P);
     st = fp4_maps(L, a, b_rows, fp4_bk());

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_base = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_i = reinterpret_cast<int*>(tmem_base + 1);
   volatile int* abort_flag = abort_i;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int warp = warp_bcast((int)(threadIdx.x / 32)), lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -109,14 +109,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_base;
+  const uint32_t tmem = warp_bcast(*tmem_base);
 
   const int n_wblk = (p.N + BM - 1) / BM;
   const int n_tblk = (p.M + TN - 1) / TN;
   const int total = n_wblk * n_tblk;
   const int nkb_all = p.K / BK;
   // split mode: this CTA's K blocks [kb0, kb0 + nkb); tiles are walked per cluster
-  const uint32_t srank = kSplit > 1 ? cluster_ctarank() : 0u;
+  const uint32_t srank = kSplit > 1 ? warp_bcast(cluster_ctarank()) : 0u;
   const int kb0 = kSplit > 1 ? (int)srank * ((nkb_all + 1) / 2) : 0;
   const int nkb = kSplit > 1 ? (srank == 0 ? (nkb_all + 1) / 2 : nkb_all / 2) : nkb_all;
   const int t_first = kSplit > 1 ? (int)blockIdx.x / 2 : (int)blockIdx.x;
@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int i = 0; i < C::kColsPerWarp; ++i) facc[i] = 0.0f;
 
-  if (warp == 0 && lane == 0) {
+  // The producer and the MMA issuer run with the whole warp: lane 0 waits on
+  // the barriers (result broadcast), one elected lane issues.
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     PipeState<C::kStages> ps;
     uint32_t issued_mask = 0, last_phase = 0;
@@ -137,17 +139,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = t_first; t < total && ok; t += t_step) {
       const int wb = t % n_wblk, tb = t / n_wblk;
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(&empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 50)) { ok = false; break; }
+        if (!mbar_wait_warp(&empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 50)) { ok = false; break; }
         uint8_t* st = stages + ps.index * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(BM * BK + TN * BK));
-        tma_load_2d(st, &tmW, &full[ps.index], (kb0 + kb) * BK, wb * BM);
-        tma_load_2d(st + BM * BK, &tmX, &full[ps.index], (kb0 + kb) * BK, tb * TN);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(BM * BK + TN * BK));
+          tma_load_2d(st, &tmW, &full[ps.index], (kb0 + kb) * BK, wb * BM);
+          tma_load_2d(st + BM * BK, &tmX, &full[ps.index], (kb0 + kb) * BK, tb * TN);
+        }
+        __syncwarp();
         issued_mask |= 1u << ps.index;
         last_phase = (last_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
         ps.advance();
       }
     }
-    if (*abort_flag) {
+    if (*abort_flag && lane == 0) {
       for (int s = 0; s < C::kStages; ++s)
         if (issued_mask & (1u << s)) {
           const uint64_t t0 = globaltimer();
@@ -155,34 +160,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // Descriptors are built once for stage 0 and advanced by byte offset / 16.
     PipeState<C::kStages> ps;
     PipeState<C::kSlots> sl;  // partial slot ring
     constexpr uint32_t idesc = idesc_e4m3(BM, TN);
+    const uint64_t dW = smem_desc(smem_u32(stages), 16, 1024, kLayoutSw128);
+    const uint64_t dX = smem_desc(smem_u32(stages + BM * BK), 16, 1024, kLayoutSw128);
     bool ok = true;
     for (int t = t_first; t < total && ok; t += t_step) {
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(&pempty[sl.index], sl.phase ^ 1u, abort_flag, p.status, 60)) { ok = false; break; }
-        if (!mbar_wait(&full[ps.index], ps.phase, abort_flag, p.status, 61)) { ok = false; break; }
+        if (!mbar_wait_warp(&pempty[sl.index], sl.phase ^ 1u, abort_flag, p.status, 60)) { ok = false; break; }
+        if (!mbar_wait_warp(&full[ps.index], ps.phase, abort_flag, p.status, 61)) { ok = false; break; }
         tc_fence_after();
-        uint8_t* st = stages + ps.index * C::kStageBytes;
-        const uint32_t sw = smem_u32(st), sx = smem_u32(st + BM * BK);
+        const uint64_t so = (uint64_t)((ps.index * C::kStageBytes) >> 4);
         const uint32_t d = tmem + sl.index * TN;
+        if (elect_one()) {
 #pragma unroll
-        for (int j = 0; j < BK / 32; ++j)
-          mma_e4m3(d, smem_desc(sw + 32 * j, 16, 1024, kLayoutSw128), smem_desc(sx + 32 * j, 16, 1024, kLayoutSw128),
-                   idesc, j > 0 ? 1u : 0u);
-        tc_commit(&empty[ps.index]);
-        tc_commit(&pfull[sl.index]);
+          for (int j = 0; j < BK / 32; ++j)
+            mma_e4m3(d, dW + so + 2 * j, dX + so + 2 * j, idesc, j > 0 ? 1u : 0u);  // 32 B of K per MMA
+          tc_commit(&empty[ps.index]);
+          tc_commit(&pfull[sl.index]);
+        }
+        __syncwarp();
         ps.advance();
         sl.advance();
       }
     }
-    tc_commit(drain);
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 1000000000ull) {
+    if (elect_one()) {
+      tc_commit(drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 1000000000ull) {
+      }
     }
+    __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ promotion + epilogue
     // Walks (tile, chunk of KBC K blocks) in order.  The scales of the next
@@ -235,8 +247,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("cp.async.commit_group;" ::: "memory");
       asm volatile("cp.async.wait_group 1;" ::: "memory");
       asm volatile("bar.sync 1, 256;" ::: "memory");
+      {
+        // fold the weight block scale into the token scales once per chunk:
+        // csa[kb][m] = sb[kb] * sa[kb][m], the same factor for every row
+        float* wsa = ssa + (qi & 1) * KBC * TN;
+        const float* wsb = ssb + (qi & 1) * KBC;
+        for (int i = etid; i < KBC * TN; i += 256) wsa[i] *= wsb[i / TN];
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+      }
       const float* csa = ssa + (qi & 1) * KBC * TN;
-      const float* csb = ssb + (qi & 1) * KBC;
       const int wb = t % n_wblk, tb = t / n_wblk;
       const int n = wb * BM + q * 32 + lane;            // weight row = output column
       const int m0 = tb * TN + col0;                    // first token of this warp's columns
@@ -275,10 +294,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int i = 0; i < G; ++i) {
-              const float sbv = csb[kb + i - c * KBC];
-              const float* sa_row = csa + (kb + i - c * KBC) * TN + col0;
+              const float4* s4 = reinterpret_cast<const float4*>(csa + (kb + i - c * KBC) * TN + col0);
 #pragma unroll
-              for (int j = 0; j < NC; ++j) acc[j] = fmaf(__uint_as_float(v[i][j]), sbv * sa_row[j], acc[j]);
+              for (int j = 0; j < NC; j += 4) {
+                const float4 sc = s4[j / 4];  // same address in every lane: one broadcast
+                acc[j] = fmaf(__uint_as_float(v[i][j]), sc.x, acc[j]);
+                acc[j + 1] = fmaf(__uint_as_float(v[i][j + 1]), sc.y, acc[j + 1]);
+                acc[j + 2] = fmaf(__uint_as_float(v[i][j + 2]), sc.z, acc[j + 2]);
+                acc[j + 3] = fmaf(__uint_as_float(v[i][j + 3]), sc.w, acc[j + 3]);
+              }
             }
           }
         }
@@ -292,8 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
           tc_fence_after();
-          const float sbv = csb[kb - c * KBC];
-          const float* sa_row = csa + (kb - c * KBC) * TN + col0;
+          const float4* s4 = reinterpret_cast<const float4*>(csa + (kb - c * KBC) * TN + col0);
           constexpr int CH = NC < 32 ? NC : 32;
 #pragma unroll
           for (int c0 = 0; c0 < NC; c0 += CH) {
@@ -307,7 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (lane == 0) mbar_arrive(&pempty[sl.index]);
             }
 #pragma unroll
-            for (int i = 0; i < CH; ++i) acc[c0 + i] = fmaf(__uint_as_float(v[i]), sbv * sa_row[c0 + i], acc[c0 + i]);
+            for (int i = 0; i < CH; i += 4) {
+              const float4 sc = s4[(c0 + i) / 4];
+              acc[c0 + i] = fmaf(__uint_as_float(v[i]), sc.x, acc[c0 + i]);
+              acc[c0 + i + 1] = fmaf(__uint_as_float(v[i + 1]), sc.y, acc[c0 + i + 1]);
+              acc[c0 + i + 2] = fmaf(__uint_as_float(v[i + 2]), sc.z, acc[c0 + i + 2]);
+              acc[c0 + i + 3] = fmaf(__uint_as_float(v[i + 3]), sc.w, acc[c0 + i + 3]);
+            }
           }
         }
         sl.advance();

@@ -19,6 +19,13 @@ from tests.helpers import gemm_errors, sf_rowmajor
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["pair", "one_cta"])
+def fp4_kernel(request, monkeypatch):
+    """Grouped GEMMs on CTA pairs (default) or on the one-CTA kernel."""
+    monkeypatch.setenv("BSGEMM_FP4_PAIR", "1" if request.param == "pair" else "0")
+    return request.param
+
+
 def test_dispatch_hand_case(cuda_lib):
     bs = cuda_lib
     gold = {r[0]: [int(v) for v in r[1:]] for r in read_golden("moe_dispatch_2x8.txt")}
@@ -64,7 +71,7 @@ def _small_moe(T=200, H=256, F=128, E=5, k=2, seed=3):
 @pytest.mark.parametrize("T,H,F,E,k,chunk", [(200, 256, 128, 5, 2, 0), (1000, 512, 256, 8, 4, 0),
                                              (64, 256, 128, 16, 8, 0), (300, 1024, 256, 6, 2, 1),
                                              (300, 1024, 256, 6, 2, 3)])
-def test_grouped_layer_staged(cuda_lib, T, H, F, E, k, chunk):
+def test_grouped_layer_staged(cuda_lib, fp4_kernel, T, H, F, E, k, chunk):
     """chunk > 0: the down GEMM walks column chunks of that many 256-wide blocks."""
     bs = cuda_lib
     from fp8_quantized_gemm_q4_gb300.moe import MoELayer, quantize_expert_weights
