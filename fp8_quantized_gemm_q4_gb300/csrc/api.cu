@@ -299,6 +299,14 @@ static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_
     if (st != BS_OK) return st;
     st = sf_map(&P.tmSfb, a->sfb, b_rows, a->K);
     if (st != BS_OK) return st;
+    if (L.epilogue == bsk::kEpiSwiglu || (L.epilogue == bsk::kEpiStore && !grouped)) {
+      // 32 rows x 32 bytes per box, 32-byte swizzle (matches the kernel's staging layout)
+      const bool bf = a->out_dtype == BS_DTYPE_BF16;
+      const int es = bf ? 2 : 4;
+      st = make_map(&P.tmO, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, es, a->out,
+                    (uint64_t)a->N, (uint64_t)a->M, (uint64_t)a->ldo * es, 32 / es, 32, CU_TENSOR_MAP_SWIZZLE_32B);
+      if (st != BS_OK) return st;
+    }
     P.base = L;
     const int pairs = sms / 2;
     P.grid = 2 * (int)(grouped ? pairs : (pair_tiles < pairs ? pair_tiles : pairs));

@@ -34,7 +34,12 @@ constexpr int BN = 256;        // MMA N; each CTA holds BN / 2 rows of B
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
 constexpr int kMaxExperts = 1024;
-constexpr int kMisc = 2048 + (kMaxExperts + 1) * 4 + 1024;
+constexpr int kMiscBase = 2048 + 1024;                 // barriers, tile count + slack
+constexpr int kMiscTable = (kMaxExperts + 1) * 4;     // expert row-block prefix table (grouped only)
+// Output staging for TMA stores: one 1 KB buffer per epilogue warp, a box of
+// 32 rows x 32 bytes (16 bf16 or 8 fp32 columns) in the 32-byte swizzle
+// layout (the 16-byte half of row r sits at half ^ ((r >> 2) & 1)).
+constexpr int kEpiStageBytes = 8 * 1024;
 // low-rank slot per CTA: T hi / T lo of its own rows, its half of Bl^T
 constexpr int kLoraThi = 0, kLoraTlo = 8192, kLoraBl = 16384, kLoraBytes = 24576;
 constexpr int kSfBuffers = 2;
@@ -58,8 +63,9 @@ struct PGeo {
   static constexpr int kStageTx = kStageBytes;  // bytes one CTA's loads deliver per stage
   static constexpr int kSfWords = kMmas * 128;  // scale words of one 128-row block per stage
   static constexpr int kSfBoxes = kSfWords / 256;  // TMA boxes of 256 words
-  static constexpr Fp4TileShape kShapeLora{BM, BN, BK, 2, true, 32, kMisc};
-  static constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 2, false, 32, kMisc};
+  // the low-rank branch is dense-only, so its variant carries no expert table
+  static constexpr Fp4TileShape kShapeLora{BM, BN, BK, 2, true, 32, kMiscBase + kEpiStageBytes};
+  static constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 2, false, 32, kMiscBase + kMiscTable + kEpiStageBytes};
   static_assert(kStageBytes == fp4_stage_bytes(kShapeNoLora), "per-CTA stage layout matches the budget");
   static_assert(kStageBytes % kAlign == 0, "stage alignment");
   static_assert(kLoraBytes == fp4_lora_bytes(kShapeLora), "low-rank slot: the up-projection block is split per CTA");
@@ -156,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmL,
                     const __grid_constant__ CUtensorMap tmSfa, const __grid_constant__ CUtensorMap tmSfb,
-                    const Fp4Params p) {
+                    const __grid_constant__ CUtensorMap tmO, const Fp4Params p) {
   using G = PGeo<BK>;
   constexpr int kStageBytes = G::kStageBytes, kRowBytes = G::kRowBytes, kMmas = G::kMmas;
   constexpr int kOffA = G::kOffA, kOffB = G::kOffB, kOffSfa = G::kOffSfa, kOffSfb = G::kOffSfb;
@@ -166,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(kAlign - 1));
   uint8_t* stages = base;
   uint8_t* lora = base + kStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(lora + (kLora ? kLoraBytes : 0));
+  uint8_t* estage = lora + (kLora ? kLoraBytes : 0);  // [8 warps][1 KB]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(estage + kEpiStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
@@ -203,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmSfa);
     prefetch_tmap(&tmSfb);
+    if (kEpi == kEpiSwiglu || (kEpi == kEpiStore && p.E == 0)) prefetch_tmap(&tmO);
     if (kLora) {
       prefetch_tmap(&tmT);
       prefetch_tmap(&tmL);
@@ -215,6 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 3) {
     if (p.E == 0) {
       if (lane == 0) *total_tiles = ((p.M + 2 * BM - 1) / (2 * BM)) * ((p.N + BN - 1) / BN);
+    } else if (kLora) {
+      // the low-rank variant has no expert table: nothing to do (the host never asks for this)
+      if (lane == 0) {
+        *total_tiles = 0;
+        if (blockIdx.x == 0) record_status(p.status, kStatusOffsets, 4);
+      }
     } else {
       const int nb = n_blocks<kEpi>(p);
       int running = 0;
@@ -395,6 +409,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_in_tile = (int)rank * BM + q * 32 + lane;  // row within the pair tile
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t acc_phase = 0;
+    // One 32 x 32-byte box: each lane writes its row (two 16-byte halves in
+    // the swizzled order), then one lane hands the box to TMA.  The buffer is
+    // reused once TMA has read the previous box.
+    const uint32_t sbuf = smem_u32(estage + (warp - kEpiWarp0) * 1024);
+    const uint32_t swz = (uint32_t)((lane >> 2) & 1);
+    auto stage_and_store = [&](const uint32_t (&w)[8], int x, int y) {
+      if (elect_one()) bulk_wait_read_all();
+      __syncwarp();
+      st_shared_v4(sbuf + lane * 32 + (swz << 4), w[0], w[1], w[2], w[3]);
+      st_shared_v4(sbuf + lane * 32 + ((swz ^ 1u) << 4), w[4], w[5], w[6], w[7]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (elect_one()) {
+        tma_store_2d(&tmO, estage + (warp - kEpiWarp0) * 1024, x, y);
+        bulk_commit_group();
+      }
+      __syncwarp();
+    };
     for (int t = pair; t < total; t += npairs) {
       const Tile tl = tile_of<kEpi>(p, prefix, t);
       int ok = 1;
@@ -422,28 +454,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = r_in_tile < tl.rows;
       const int64_t row = (int64_t)tl.row0 + r_in_tile;
       if (kEpi == kEpiSwiglu) {
-        // padding rows of the segment inside the pair tile are written as zeros
+        // h = bf16(silu(g) * u); padding rows of the segment inside the pair
+        // tile are written as zeros.  Boxes of 32 rows past the segment's
+        // 128-aligned extent belong to the next expert and are skipped.
         const int col = tl.col0 + 64 * half;
-        const bool in_buf = row < p.M;
-        if (in_buf) {
-          uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * p.ldo + col;
+        const int box_r = (int)rank * BM + q * 32;  // first row of this warp's box, in the tile
+        const int row_box = tl.row0 + box_r;
+        if (box_r < ((tl.rows + 127) / 128) * 128 && row_box < p.M) {
 #pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            uint32_t w[4];
+          for (int cc = 0; cc < 4; ++cc) {  // 16 columns per box
+            uint32_t w[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
               float hv[2];
 #pragma unroll
               for (int k2 = 0; k2 < 2; ++k2) {
-                const int cc = c + 2 * i + k2;
-                const float g = __uint_as_float(v[cc / 32][cc % 32]);
-                const float u = __uint_as_float(v[2 + cc / 32][cc % 32]);
+                const int c = cc * 16 + 2 * i + k2;
+                const float g = __uint_as_float(v[c / 32][c % 32]);
+                const float u = __uint_as_float(v[2 + c / 32][c % 32]);
                 hv[k2] = row_ok ? (g / (1.0f + __expf(-g))) * u : 0.0f;
               }
               w[i] = pack_bf16x2(hv[0], hv[1]);
             }
-            if (row_ok || r_in_tile < ((tl.rows + 127) / 128) * 128)
-              *reinterpret_cast<uint4*>(out + c) = make_uint4(w[0], w[1], w[2], w[3]);
+            stage_and_store(w, col + cc * 16, row_box);
           }
         }
       } else if (kEpi == kEpiCombine) {
@@ -467,20 +500,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (kEpi == kEpiStore) {
         const int col = tl.col0 + 128 * half;
-        if (row_ok && row < p.M && col < p.N) {
+        auto value = [&](int c) {  // output column col + c of this lane's row
+          float a = __uint_as_float(v[c / 32][c % 32]);
+          float sc = p.alpha;
+          if (p.col_scale) sc *= p.col_scale[col + c];
+          a *= sc;
+          if (p.bias) a += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.bias)[col + c]);
+          return a;
+        };
+        if (p.E == 0) {
+          // dense: boxes of 32 rows x 32 bytes through the warp's staging buffer
+          const int row_box = tl.row0 + (int)rank * BM + q * 32;
+          if (row_box < p.M && col < p.N) {
+            if (p.out_bf16) {
+#pragma unroll
+              for (int cc = 0; cc < 8; ++cc) {  // 16 columns per box
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(value(cc * 16 + 2 * i), value(cc * 16 + 2 * i + 1));
+                stage_and_store(w, col + cc * 16, row_box);
+              }
+            } else {
+#pragma unroll
+              for (int cc = 0; cc < 16; ++cc) {  // 8 columns per box
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(value(cc * 8 + i));
+                stage_and_store(w, col + cc * 8, row_box);
+              }
+            }
+          }
+        } else if (row_ok && row < p.M && col < p.N) {
+          // grouped: rows past the expert's count are not written
 #pragma unroll
           for (int c = 0; c < 128; c += 8) {
             float y[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int n = col + c + i;
-              float a = __uint_as_float(v[(c + i) / 32][(c + i) % 32]);
-              float sc = p.alpha;
-              if (p.col_scale) sc *= p.col_scale[n];
-              a *= sc;
-              if (p.bias) a += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.bias)[n]);
-              y[i] = a;
-            }
+            for (int i = 0; i < 8; ++i) y[i] = value(c + i);
             if (p.out_bf16) {
               uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * p.ldo + col + c;
               *reinterpret_cast<uint4*>(out) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
@@ -494,6 +550,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // the output boxes handed to TMA are written before the CTA exits
+    if (elect_one()) bulk_wait_all();
+    __syncwarp();
   }
 
   __syncwarp();
@@ -526,7 +585,8 @@ static cudaError_t launch_one(const Fp4PairLaunch& L, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, L.base.tmA, L.base.tmB, L.base.tmT, L.base.tmL, L.tmSfa, L.tmSfb, L.base.p);
+  return cudaLaunchKernelEx(&cfg, kern, L.base.tmA, L.base.tmB, L.base.tmT, L.base.tmL, L.tmSfa, L.tmSfb, L.tmO,
+                            L.base.p);
 }
 
 template <int BK>

@@ -48,6 +48,7 @@ int fp4_stages(bool lora, int bk);
 struct Fp4PairLaunch {
   Fp4Launch base;         // tmA/tmB built for 128-element stages; base.grid unused
   CUtensorMap tmSfa, tmSfb;
+  CUtensorMap tmO;        // output boxes (dense STORE, SWIGLU); unused otherwise
   int grid;               // even: two CTAs per cluster
 };
 cudaError_t launch_fp4_pair_gemm(const Fp4PairLaunch& L, cudaStream_t stream);
