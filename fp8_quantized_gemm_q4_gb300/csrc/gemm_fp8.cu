@@ -38,13 +38,14 @@ constexpr int kMaxStages = 12;
 
 constexpr int KBC = 32;   // K blocks whose scales are staged together
 
-template <int TN>
+template <int TN, int kSplit>
 struct Cfg {
   static constexpr int kStageBytes = round_up(BM * BK + TN * BK, kAlign);
   // two staging buffers of [KBC][TN] activation scales + [KBC] weight scales
   static constexpr int kScaleBytes = round_up(2 * (KBC * TN + KBC) * 4, kAlign);
   // split-K partner's partial sums [BM rows][TN], written through DSMEM
-  static constexpr int kRedBytes = round_up(BM * TN * 4, kAlign);
+  // (split mode only: elsewhere the bytes go to the stage ring)
+  static constexpr int kRedBytes = kSplit > 1 ? round_up(BM * TN * 4, kAlign) : 0;
   static constexpr Fp8TileShape kShape{BM, TN, BK, kMisc + kScaleBytes + kRedBytes + kAlign};
   static constexpr int kStages = fp8_main_stages(kShape) < kMaxStages ? fp8_main_stages(kShape) : kMaxStages;
   static constexpr int kSmem = kStages * kStageBytes + kScaleBytes + kRedBytes + kMisc + kAlign;
@@ -65,7 +66,7 @@ template <int TN, int kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const Fp8Params p) {
-  using C = Cfg<TN>;
+  using C = Cfg<TN, kSplit>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kAlign - 1) &
                                              ~static_cast<uintptr_t>(kAlign - 1));
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int TN, int kSplit>
 static cudaError_t launch_tn(const Fp8Launch& L, cudaStream_t stream) {
-  using C = Cfg<TN>;
+  using C = Cfg<TN, kSplit>;
   auto kern = fp8_gemm_kernel<TN, kSplit>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;

@@ -48,7 +48,7 @@ def test_fp8_prefill_4096_sampled_rows(cuda_lib):
 
 
 @pytest.mark.parametrize("M,N,K", [(3, 256, 256), (100, 384, 512), (300, 128, 128), (17, 640, 1024),
-                                   (33, 128, 384)])
+                                   (33, 128, 384), (200, 640, 256)])
 def test_fp8_ragged(cuda_lib, M, N, K):
     g = torch.Generator().manual_seed(M + N + K)
     x = torch.randn(M, K, generator=g).to(torch.bfloat16)
