@@ -146,6 +146,7 @@ class DenseLowRank:
             self.at = self.bt = self.bias = self.lt = None
             self.out = torch.empty((M, N), dtype=torch.float32, device=dev)
         self.launches_per_step = 2 + (0 if self.tiny else 1)
+        self.kernel_src = "fp8_quantized_gemm_q4_gb300/csrc/gemm_fp4_pair.cu"
         self.bytes_in = self.x.numel() * self.x.element_size()
         self.bytes_out = self.out.numel() * self.out.element_size()
 
@@ -164,7 +165,7 @@ class DenseLowRank:
     def roofline(self, gemm_ms, peaks, source):
         tflops = self.flops / (gemm_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
-        return {"bound": "tensor", "kernel": "fp4_gemm_kernel", "achieved": round(tflops, 1),
+        return {"bound": "tensor", "kernel": "fp4_pair_kernel", "achieved": round(tflops, 1),
                 "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                 "peak_source": f"{source} bf16 burst x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/bf16)",
                 "algorithmic_flops_per_launch": self.flops, "kernel_ms": round(gemm_ms, 5)}
@@ -268,8 +269,9 @@ class MoEWorkload:
     """Grouped FP4 MoE layer: dispatch, gather + quantize, gate/up GEMM + SwiGLU,
     re-quantize, down GEMM + routed combine, bf16 cast (one step = one layer)."""
 
-    def __init__(self, large):
+    def __init__(self, large, combine="rows"):
         import workloads
+        self.combine = combine
         cfg = workloads.MOE_LARGE if large else workloads.MOE_SMALL
         self.index = 4 if large else 3
         self.T, self.H, self.E, self.k, self.F = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["F"]
@@ -313,10 +315,11 @@ class MoEWorkload:
             bs.q4_quantize(wd, out=(wd_codes[e * H:(e + 1) * H], wd_sf[e * pd:(e + 1) * pd], None))
         from fp8_quantized_gemm_q4_gb300.moe import MoEWeights
         W = MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf)
-        self.layer = MoELayer(W, self.T, self.k, device=dev)
+        self.layer = MoELayer(W, self.T, self.k, device=dev, combine=self.combine)
         self.out = self.layer.out
-        # dispatch 3 + quantize 1 + gather 1 + gemm 1 + quantize 1 + gemm 1 + finalize 2 (cast, zero)
-        self.launches_per_step = 10
+        # dispatch 3 + quantize 1 + gather 1 + gemm 1 + quantize 1 + gemm 1, then
+        # combine 3 (invert, init, sum) or finalize 2 (cast, zero)
+        self.launches_per_step = 11 if self.combine == "rows" else 10
         self.bytes_in = self.x.numel() * 2 + self.ids.numel() * 4 + self.w.numel() * 4
         self.bytes_out = self.out.numel() * 2
         counts = torch.bincount(self.ids.flatten().long(), minlength=E).cpu()
@@ -334,7 +337,7 @@ class MoEWorkload:
     def roofline(self, layer_ms, peaks, source):
         tflops = self.flops / (layer_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
-        return {"bound": "tensor", "kernel": "whole layer (grouped fp4_gemm_kernel x2 + quantize + dispatch)",
+        return {"bound": "tensor", "kernel": "whole layer (grouped fp4_pair_kernel x2 + quantize + dispatch + " + ("combine" if self.combine == "rows" else "finalize") + ")",
                 "achieved": round(tflops, 1), "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                 "peak_source": f"{source} bf16 burst x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/bf16)",
                 "algorithmic_flops_per_launch": self.flops, "kernel_ms": round(layer_ms, 5),
@@ -482,7 +485,8 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, pages' shapes)",
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   **({"moe_combine": wl.combine} if hasattr(wl, "combine") else {})},
         "e2e": {"value": round(job_throughput(wl.flops, world, e2e_ms) / 1e12, 2), "unit": wl.unit,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": wl.bytes_in,
                 "d2h_bytes_per_step": wl.bytes_out},
@@ -554,12 +558,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (default min(steps, 100))")
+    ap.add_argument("--moe-combine", choices=["rows", "atomic"], default="rows",
+                    help="MoE routed combine: weighted rows + per-token sum, or fp32 reductions")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     wl = WORKLOADS[args.workload]()
+    if isinstance(wl, MoEWorkload):
+        wl.combine = args.moe_combine
 
     if args.impl == "reference":
         if rank == 0:

@@ -21,14 +21,14 @@ from ._build import LIB as _LIB_PATH
 
 __all__ = [
     "load", "sf_bytes", "sf_offset", "q4_quantize", "fp4_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
-    "grouped_gemm_fp4", "moe_dispatch", "moe_finalize", "moe_rows_bound", "device_status",
-    "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE",
+    "grouped_gemm_fp4", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
+    "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE", "EPI_ROWS",
 ]
 
 BS_OK, BS_ERR_INVALID, BS_ERR_ALIGN, BS_ERR_UNSUPPORTED, BS_ERR_CUDA, BS_ERR_TIMEOUT, BS_ERR_OFFSETS = range(7)
 DTYPE_F32, DTYPE_BF16 = 0, 1
 FMT_FP4, FMT_FP8 = 0, 1
-EPI_STORE, EPI_SWIGLU, EPI_COMBINE = 0, 1, 2
+EPI_STORE, EPI_SWIGLU, EPI_COMBINE, EPI_ROWS = 0, 1, 2, 3
 Q8_TOKEN, Q8_BLOCK = 1, 128
 
 
@@ -88,6 +88,8 @@ def load(path: str | None = None):
         lib.bs_moe_dispatch_noalloc.argtypes = [P, P, I64, I, I, P, P, P, P, P, P]
         lib.bs_moe_finalize.restype = I
         lib.bs_moe_finalize.argtypes = [P, P, I64, P]
+        lib.bs_moe_combine.restype = I
+        lib.bs_moe_combine.argtypes = [P, I64, P, I64, I64, I, I64, P, P, I64, P]
         lib.bs_get_device_status.restype = I
         lib.bs_get_device_status.argtypes = [ctypes.POINTER(I)]
         lib.bs_clear_device_status.restype = I
@@ -264,6 +266,19 @@ def moe_dispatch(topk_ids, topk_w, E: int, out=None, workspace=None, stream=None
 def moe_finalize(out32, out_bf16, stream=None):
     _check(load().bs_moe_finalize(_ptr(out32), _ptr(out_bf16), out32.numel(), _stream(stream)))
     return out_bf16
+
+
+def moe_combine(rows, pair_of_row, T: int, k: int, out=None, row_of_pair=None, stream=None):
+    """out[t] = bf16(sum_j rows[row of pair t*k + j]) (fp32 sum in slot order);
+    ``rows`` fp32 [n_rows, H] from a grouped GEMM with EPI_ROWS."""
+    n_rows, H = rows.shape
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=rows.device)
+    if row_of_pair is None:
+        row_of_pair = torch.empty(max(T * k, 1), dtype=torch.int32, device=rows.device)
+    _check(load().bs_moe_combine(_ptr(rows), rows.stride(0), _ptr(pair_of_row), n_rows, T, k, H, _ptr(row_of_pair),
+                                 _ptr(out), out.stride(0), _stream(stream)))
+    return out
 
 
 def device_status() -> tuple[int, int]:

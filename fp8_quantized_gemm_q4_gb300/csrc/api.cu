@@ -299,12 +299,16 @@ static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_
     if (st != BS_OK) return st;
     st = sf_map(&P.tmSfb, a->sfb, b_rows, a->K);
     if (st != BS_OK) return st;
-    if (L.epilogue == bsk::kEpiSwiglu || (L.epilogue == bsk::kEpiStore && !grouped)) {
-      // 32 rows x 32 bytes per box, 32-byte swizzle (matches the kernel's staging layout)
+    if (L.epilogue == bsk::kEpiSwiglu || L.epilogue == bsk::kEpiRows ||
+        (L.epilogue == bsk::kEpiStore && !grouped)) {
+      // boxes of 32 rows x 64 bytes, 64-byte swizzle (32 bytes, 32-byte swizzle
+      // for the low-rank variant): the kernel's staging layout
       const bool bf = a->out_dtype == BS_DTYPE_BF16;
       const int es = bf ? 2 : 4;
+      const uint32_t row_bytes = L.lora ? 32 : 64;
       st = make_map(&P.tmO, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, es, a->out,
-                    (uint64_t)a->N, (uint64_t)a->M, (uint64_t)a->ldo * es, 32 / es, 32, CU_TENSOR_MAP_SWIZZLE_32B);
+                    (uint64_t)a->N, (uint64_t)a->M, (uint64_t)a->ldo * es, row_bytes / es, 32,
+                    L.lora ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
       if (st != BS_OK) return st;
     }
     P.base = L;
@@ -408,7 +412,8 @@ bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, 
                           int epilogue, const int32_t* token_of, const float* weight_of, float* out32,
                           int64_t ld_out32, bs_stream_t stream) {
   if (!a) return fail(BS_ERR_INVALID, "null args");
-  if (epilogue != BS_EPI_STORE && epilogue != BS_EPI_SWIGLU && epilogue != BS_EPI_COMBINE)
+  if (epilogue != BS_EPI_STORE && epilogue != BS_EPI_SWIGLU && epilogue != BS_EPI_COMBINE &&
+      epilogue != BS_EPI_ROWS)
     return fail(BS_ERR_INVALID, "epilogue %d", epilogue);
   bs_status st = check_common(a, epilogue == BS_EPI_COMBINE);
   if (st != BS_OK) return st;
@@ -419,6 +424,10 @@ bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, 
   if (a->lora_t || a->col_scale || a->bias || a->alpha != 1.0f)
     return fail(BS_ERR_UNSUPPORTED, "grouped GEMM takes no alpha/col_scale/bias/low-rank");
   if (epilogue == BS_EPI_SWIGLU && a->out_dtype != BS_DTYPE_BF16) return fail(BS_ERR_INVALID, "SWIGLU output is bf16");
+  if (epilogue == BS_EPI_ROWS) {
+    if (a->out_dtype != BS_DTYPE_F32) return fail(BS_ERR_INVALID, "ROWS output is fp32");
+    if (!weight_of) return fail(BS_ERR_INVALID, "ROWS needs weight_of");
+  }
   if (epilogue == BS_EPI_COMBINE) {
     if (!token_of || !weight_of || !out32) return fail(BS_ERR_INVALID, "COMBINE needs token_of, weight_of, out32");
     if (!aligned16(out32) || ld_out32 % 4 || ld_out32 < a->N) return fail(BS_ERR_ALIGN, "out32 misaligned or ld_out32 < N");
@@ -506,6 +515,24 @@ bs_status bs_moe_dispatch_noalloc(const int32_t* topk_ids, const float* topk_w, 
                                                    weight_of, bs_moe_rows_bound(T, k, E), status,
                                                    reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "dispatch_noalloc");
+  return BS_OK;
+}
+
+bs_status bs_moe_combine(const float* rows, int64_t ld_rows, const int32_t* pair_of_row, int64_t n_rows,
+                         int64_t T, int k, int64_t H, int32_t* row_of_pair, void* out, int64_t ldo,
+                         bs_stream_t stream) {
+  if (T < 0 || n_rows < 0 || H < 0) return fail(BS_ERR_INVALID, "combine: negative size");
+  if (k <= 0 || k > 32) return fail(BS_ERR_INVALID, "combine: k=%d outside [1, 32]", k);
+  if (T * (int64_t)k > INT32_MAX || n_rows > INT32_MAX) return fail(BS_ERR_INVALID, "combine: too many pairs / rows");
+  if (T == 0 || H == 0) return BS_OK;
+  if (!rows || !pair_of_row || !row_of_pair || !out) return fail(BS_ERR_INVALID, "combine: null pointer");
+  if (H % 8 || ld_rows < H || ld_rows % 4 || ldo < H || ldo % 8)
+    return fail(BS_ERR_ALIGN, "combine: H %% 8 == 0, ld_rows >= H (%% 4), ldo >= H (%% 8) required");
+  if (!aligned16(rows) || !aligned16(out)) return fail(BS_ERR_ALIGN, "combine: rows / out must be 16-byte aligned");
+  if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_moe_combine(rows, ld_rows, pair_of_row, n_rows, T, k, H, row_of_pair, out, ldo,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return BS_OK;
 }
 

@@ -495,6 +495,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      } else if (kEpi == kEpiRows) {
+        // out[r, n] = weight_of[r] * y[r, n] (fp32) by 32-row groups: a group
+        // holding only rows past the expert's count is not written (padding
+        // rows of a written group carry weight 0 and become zeros)
+        const int col = tl.col0 + 128 * half;
+        if (q * 32 < tl.rows && row < p.M && col < p.N) {
+          const float wt = p.weight_of[row];
+          float* out = reinterpret_cast<float*>(p.out) + row * p.ldo + col;
+#pragma unroll
+          for (int c = 0; c < 128; c += 4)
+            *reinterpret_cast<float4*>(out + c) =
+                make_float4(wt * __uint_as_float(v[c / 32][c % 32]), wt * __uint_as_float(v[c / 32][c % 32 + 1]),
+                            wt * __uint_as_float(v[c / 32][c % 32 + 2]), wt * __uint_as_float(v[c / 32][c % 32 + 3]));
+        }
       } else if (kEpi == kEpiStore) {
         const int col = tl.col0 + 128 * half;
         if (row_ok && row < p.M && col < p.N) {
@@ -557,6 +571,7 @@ static cudaError_t launch_bk(const Fp4Launch& L, cudaStream_t stream) {
     case kEpiStore: return launch_one<BK, false, kEpiStore>(L, stream);
     case kEpiSwiglu: return launch_one<BK, false, kEpiSwiglu>(L, stream);
     case kEpiCombine: return launch_one<BK, false, kEpiCombine>(L, stream);
+    case kEpiRows: return launch_one<BK, false, kEpiRows>(L, stream);
   }
   return cudaErrorInvalidValue;
 }

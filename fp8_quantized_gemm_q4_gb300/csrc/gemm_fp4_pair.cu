@@ -36,10 +36,21 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kMaxExperts = 1024;
 constexpr int kMiscBase = 2048 + 1024;                 // barriers, tile count + slack
 constexpr int kMiscTable = (kMaxExperts + 1) * 4;     // expert row-block prefix table (grouped only)
-// Output staging for TMA stores: one 1 KB buffer per epilogue warp, a box of
-// 32 rows x 32 bytes (16 bf16 or 8 fp32 columns) in the 32-byte swizzle
-// layout (the 16-byte half of row r sits at half ^ ((r >> 2) & 1)).
-constexpr int kEpiStageBytes = 8 * 1024;
+// Output staging for TMA stores: one buffer per epilogue warp holding a box
+// of 32 rows.  Without the low-rank branch a box row is 64 bytes (32 bf16 or
+// 16 fp32 columns) in the 64-byte swizzle layout (16-byte chunk j of row r at
+// j ^ ((r >> 1) & 3)); the low-rank variant, short of shared memory, uses
+// 32-byte rows in the 32-byte swizzle layout (chunk j at j ^ ((r >> 2) & 1)).
+// Either way the lanes' 16-byte writes fall in distinct banks.
+template <bool kLora>
+struct EpiBox {
+  static constexpr int kRowW = kLora ? 8 : 16;     // 32-bit words per box row
+  static constexpr int kRowBytes = 4 * kRowW;
+  static constexpr int kBytes = 32 * kRowBytes;    // per warp
+  static constexpr int kStage = 8 * kBytes;        // 8 epilogue warps
+};
+constexpr int kEpiStageLora = EpiBox<true>::kStage;
+constexpr int kEpiStageNoLora = EpiBox<false>::kStage;
 // low-rank slot per CTA: T hi / T lo of its own rows, its half of Bl^T
 constexpr int kLoraThi = 0, kLoraTlo = 8192, kLoraBl = 16384, kLoraBytes = 24576;
 constexpr int kSfBuffers = 2;
@@ -64,8 +75,8 @@ struct PGeo {
   static constexpr int kSfWords = kMmas * 128;  // scale words of one 128-row block per stage
   static constexpr int kSfBoxes = kSfWords / 256;  // TMA boxes of 256 words
   // the low-rank branch is dense-only, so its variant carries no expert table
-  static constexpr Fp4TileShape kShapeLora{BM, BN, BK, 2, true, 32, kMiscBase + kEpiStageBytes};
-  static constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 2, false, 32, kMiscBase + kMiscTable + kEpiStageBytes};
+  static constexpr Fp4TileShape kShapeLora{BM, BN, BK, 2, true, 32, kMiscBase + kEpiStageLora};
+  static constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 2, false, 32, kMiscBase + kMiscTable + kEpiStageNoLora};
   static_assert(kStageBytes == fp4_stage_bytes(kShapeNoLora), "per-CTA stage layout matches the budget");
   static_assert(kStageBytes % kAlign == 0, "stage alignment");
   static_assert(kLoraBytes == fp4_lora_bytes(kShapeLora), "low-rank slot: the up-projection block is split per CTA");
@@ -172,8 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(kAlign - 1));
   uint8_t* stages = base;
   uint8_t* lora = base + kStages * kStageBytes;
-  uint8_t* estage = lora + (kLora ? kLoraBytes : 0);  // [8 warps][1 KB]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(estage + kEpiStageBytes);
+  using Box = EpiBox<kLora>;
+  uint8_t* estage = lora + (kLora ? kLoraBytes : 0);  // [8 warps][Box::kBytes]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(estage + Box::kStage);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
@@ -210,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmSfa);
     prefetch_tmap(&tmSfb);
-    if (kEpi == kEpiSwiglu || (kEpi == kEpiStore && p.E == 0)) prefetch_tmap(&tmO);
+    if (kEpi == kEpiSwiglu || kEpi == kEpiRows || (kEpi == kEpiStore && p.E == 0)) prefetch_tmap(&tmO);
     if (kLora) {
       prefetch_tmap(&tmT);
       prefetch_tmap(&tmL);
@@ -412,17 +424,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One 32 x 32-byte box: each lane writes its row (two 16-byte halves in
     // the swizzled order), then one lane hands the box to TMA.  The buffer is
     // reused once TMA has read the previous box.
-    const uint32_t sbuf = smem_u32(estage + (warp - kEpiWarp0) * 1024);
-    const uint32_t swz = (uint32_t)((lane >> 2) & 1);
-    auto stage_and_store = [&](const uint32_t (&w)[8], int x, int y) {
+    constexpr int kRowW = Box::kRowW;
+    const uint32_t sbuf = smem_u32(estage + (warp - kEpiWarp0) * Box::kBytes);
+    const uint32_t swz = kLora ? (uint32_t)((lane >> 2) & 1) : (uint32_t)((lane >> 1) & 3);
+    auto stage_and_store = [&](const uint32_t (&w)[kRowW], int x, int y) {
       if (elect_one()) bulk_wait_read_all();
       __syncwarp();
-      st_shared_v4(sbuf + lane * 32 + (swz << 4), w[0], w[1], w[2], w[3]);
-      st_shared_v4(sbuf + lane * 32 + ((swz ^ 1u) << 4), w[4], w[5], w[6], w[7]);
+#pragma unroll
+      for (int j = 0; j < kRowW / 4; ++j)
+        st_shared_v4(sbuf + lane * Box::kRowBytes + (((uint32_t)j ^ swz) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                     w[4 * j + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (elect_one()) {
-        tma_store_2d(&tmO, estage + (warp - kEpiWarp0) * 1024, x, y);
+        tma_store_2d(&tmO, estage + (warp - kEpiWarp0) * Box::kBytes, x, y);
         bulk_commit_group();
       }
       __syncwarp();
@@ -462,21 +477,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_box = tl.row0 + box_r;
         if (box_r < ((tl.rows + 127) / 128) * 128 && row_box < p.M) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {  // 16 columns per box
-            uint32_t w[8];
+          for (int cc = 0; cc < 64 / (2 * kRowW); ++cc) {  // 2 kRowW columns per box
+            uint32_t w[kRowW];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < kRowW; ++i) {
               float hv[2];
 #pragma unroll
               for (int k2 = 0; k2 < 2; ++k2) {
-                const int c = cc * 16 + 2 * i + k2;
+                const int c = cc * 2 * kRowW + 2 * i + k2;
                 const float g = __uint_as_float(v[c / 32][c % 32]);
                 const float u = __uint_as_float(v[2 + c / 32][c % 32]);
                 hv[k2] = row_ok ? (g / (1.0f + __expf(-g))) * u : 0.0f;
               }
               w[i] = pack_bf16x2(hv[0], hv[1]);
             }
-            stage_and_store(w, col + cc * 16, row_box);
+            stage_and_store(w, col + cc * 2 * kRowW, row_box);
           }
         }
       } else if (kEpi == kEpiCombine) {
@@ -498,6 +513,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      } else if (kEpi == kEpiRows) {
+        // out[r, n] = weight_of[r] * y[r, n] (fp32) in 32-row boxes; boxes
+        // holding only rows past the expert's count are not written (padding
+        // rows inside a written box carry weight 0 and become zeros)
+        const int col = tl.col0 + 128 * half;
+        const int box_r = (int)rank * BM + q * 32;
+        const int row_box = tl.row0 + box_r;
+        if (box_r < tl.rows && row_box < p.M && col < p.N) {
+          const float wt = row < p.M ? p.weight_of[row] : 0.0f;
+#pragma unroll
+          for (int cc = 0; cc < 128 / kRowW; ++cc) {  // kRowW columns per box
+            uint32_t w[kRowW];
+#pragma unroll
+            for (int i = 0; i < kRowW; ++i)
+              w[i] = __float_as_uint(wt * __uint_as_float(v[(cc * kRowW + i) / 32][(cc * kRowW + i) % 32]));
+            stage_and_store(w, col + cc * kRowW, row_box);
+          }
+        }
       } else if (kEpi == kEpiStore) {
         const int col = tl.col0 + 128 * half;
         auto value = [&](int c) {  // output column col + c of this lane's row
@@ -514,19 +547,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (row_box < p.M && col < p.N) {
             if (p.out_bf16) {
 #pragma unroll
-              for (int cc = 0; cc < 8; ++cc) {  // 16 columns per box
-                uint32_t w[8];
+              for (int cc = 0; cc < 128 / (2 * kRowW); ++cc) {  // 2 kRowW columns per box
+                uint32_t w[kRowW];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(value(cc * 16 + 2 * i), value(cc * 16 + 2 * i + 1));
-                stage_and_store(w, col + cc * 16, row_box);
+                for (int i = 0; i < kRowW; ++i)
+                  w[i] = pack_bf16x2(value(cc * 2 * kRowW + 2 * i), value(cc * 2 * kRowW + 2 * i + 1));
+                stage_and_store(w, col + cc * 2 * kRowW, row_box);
               }
             } else {
 #pragma unroll
-              for (int cc = 0; cc < 16; ++cc) {  // 8 columns per box
-                uint32_t w[8];
+              for (int cc = 0; cc < 128 / kRowW; ++cc) {  // kRowW columns per box
+                uint32_t w[kRowW];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(value(cc * 8 + i));
-                stage_and_store(w, col + cc * 8, row_box);
+                for (int i = 0; i < kRowW; ++i) w[i] = __float_as_uint(value(cc * kRowW + i));
+                stage_and_store(w, col + cc * kRowW, row_box);
               }
             }
           }
@@ -599,6 +633,7 @@ static cudaError_t launch_bk(const Fp4PairLaunch& L, cudaStream_t stream) {
     case kEpiStore: return launch_one<BK, false, kEpiStore>(L, stream);
     case kEpiSwiglu: return launch_one<BK, false, kEpiSwiglu>(L, stream);
     case kEpiCombine: return launch_one<BK, false, kEpiCombine>(L, stream);
+    case kEpiRows: return launch_one<BK, false, kEpiRows>(L, stream);
   }
   return cudaErrorInvalidValue;
 }

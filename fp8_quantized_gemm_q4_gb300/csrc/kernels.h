@@ -7,7 +7,7 @@
 
 namespace bsk {
 
-enum { kEpiStore = 0, kEpiSwiglu = 1, kEpiCombine = 2 };
+enum { kEpiStore = 0, kEpiSwiglu = 1, kEpiCombine = 2, kEpiRows = 3 };
 
 struct Fp4Params {
   const uint8_t* sfa;
@@ -97,6 +97,9 @@ cudaError_t launch_moe_dispatch(const int* topk_ids, const float* topk_w, long l
                                 int* counts, int* offsets, int* pair_of_row, int* token_of, float* weight_of,
                                 int* work, long long rows_bound, int* status, cudaStream_t stream);
 cudaError_t launch_moe_finalize(float* out32, void* out_bf16, long long n, cudaStream_t stream);
+cudaError_t launch_moe_combine(const float* rows, long long ld_rows, const int* pair_of_row, long long n_rows,
+                               long long T, int k, long long H, int* row_of_pair, void* out, long long ldo,
+                               cudaStream_t stream);
 
 // Grouping whose histogram scratch is the library's static device array.
 constexpr size_t kNoAllocDispatchScratchBytes = size_t(1) << 20;

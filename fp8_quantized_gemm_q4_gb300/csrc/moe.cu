@@ -209,6 +209,75 @@ cudaError_t launch_moe_dispatch(const int* topk_ids, const float* topk_w, long l
   return cudaGetLastError();
 }
 
+// row_of_pair = inverse of pair_of_row (-1 where no row holds the pair)
+__global__ void moe_rows_init_kernel(int* __restrict__ row_of_pair, long long P) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x; p < P; p += stride) row_of_pair[p] = -1;
+}
+__global__ void moe_rows_invert_kernel(const int* __restrict__ pair_of_row, long long n_rows,
+                                       int* __restrict__ row_of_pair, long long P) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x; r < n_rows; r += stride) {
+    const int p = pair_of_row[r];
+    if (p >= 0 && p < P) row_of_pair[p] = (int)r;
+  }
+}
+
+// out[t, 8g .. 8g+8) = bf16(sum_j rows[row_of_pair[t*k + j], 8g .. 8g+8)), fp32
+// sum in slot order.  One thread per (token, 8 columns); the slots are read in
+// batches of 8 whose 16 loads are independent (that many 16-byte loads in
+// flight per thread), then added in order.
+constexpr int kCombineBatch = 8;
+__global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restrict__ rows, long long ld_rows,
+                                                          const int* __restrict__ row_of_pair, long long T, int k,
+                                                          long long G, __nv_bfloat16* __restrict__ out,
+                                                          long long ldo) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < T * G; i += stride) {
+    const long long t = i / G, g = i % G;
+    float acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+      float4 lo[kCombineBatch], hi[kCombineBatch];
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; ++j) {
+        const int r = j0 + j < k ? row_of_pair[t * k + j0 + j] : -1;
+        lo[j] = hi[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r >= 0) {
+          const float4* src = reinterpret_cast<const float4*>(rows + (long long)r * ld_rows + g * 8);
+          lo[j] = __ldg(src);
+          hi[j] = __ldg(src + 1);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; ++j) {  // slot order; absent slots add +0
+        acc[0] += lo[j].x; acc[1] += lo[j].y; acc[2] += lo[j].z; acc[3] += lo[j].w;
+        acc[4] += hi[j].x; acc[5] += hi[j].y; acc[6] += hi[j].z; acc[7] += hi[j].w;
+      }
+    }
+    *reinterpret_cast<uint4*>(out + t * ldo + g * 8) =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+cudaError_t launch_moe_combine(const float* rows, long long ld_rows, const int* pair_of_row, long long n_rows,
+                               long long T, int k, long long H, int* row_of_pair, void* out, long long ldo,
+                               cudaStream_t stream) {
+  auto grid = [](long long units) {
+    long long b = (units + 255) / 256;
+    return (unsigned)(b > 8192 ? 8192 : (b < 1 ? 1 : b));
+  };
+  const long long P = T * k;
+  moe_rows_init_kernel<<<grid(P), 256, 0, stream>>>(row_of_pair, P);
+  moe_rows_invert_kernel<<<grid(n_rows), 256, 0, stream>>>(pair_of_row, n_rows, row_of_pair, P);
+  const long long G = H / 8;
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+  moe_combine_kernel<<<grid(T * G), 256, 0, stream>>>(rows, ld_rows, row_of_pair, T, k, G, o, ldo);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_moe_finalize(float* out32, void* out_bf16, long long n, cudaStream_t stream) {
   auto grid = [](long long units) {
     long long b = (units + 255) / 256;

@@ -51,13 +51,49 @@ __device__ __forceinline__ void load8(const void* x, int x_bf16, long long off, 
   }
 }
 
-// One warp per (row, 4 x 256-element segments), grid-stride: the four 16-byte
-// loads of a lane are issued before any arithmetic (memory-level parallelism).
+// One warp per (row, kQ4Unroll x 256-element segments), grid-stride.  A
+// lane's kQ4Unroll 16-byte loads are all issued before any arithmetic and are
+// kept as raw words (bf16 pairs decode with a shift / mask when used), so a
+// warp holds 4 KB of loads in flight at 64 registers a thread (memory-level
+// parallelism: the kernel streams at HBM rate only with that much in flight).
 // Rows in [M, Mpad) (the 128-row padding of the scale tensor) get zero
 // scales, no codes.
-constexpr int kQ4Unroll = 4;
-__global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict__ x, int x_bf16, long long M,
-                                                          long long Mpad, long long K, long long ldx,
+constexpr int kQ4Unroll = 8;
+static int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+// 8 consecutive inputs as raw words: bf16 -> 4 words (pairs), fp32 -> 8 words.
+template <bool kBf16>
+struct Raw8 {
+  uint32_t w[kBf16 ? 4 : 8];
+};
+template <bool kBf16>
+__device__ __forceinline__ void load_raw8(const void* x, long long off, Raw8<kBf16>& r) {
+  if constexpr (kBf16) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(x) + off));
+    r.w[0] = u.x; r.w[1] = u.y; r.w[2] = u.z; r.w[3] = u.w;
+  } else {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(x) + off));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(x) + off + 4));
+    r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
+    r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+  }
+}
+template <bool kBf16>
+__device__ __forceinline__ float raw8_at(const Raw8<kBf16>& r, int i) {
+  if constexpr (kBf16)
+    return __uint_as_float((i & 1) ? (r.w[i / 2] & 0xFFFF0000u) : (r.w[i / 2] << 16));
+  else
+    return __uint_as_float(r.w[i]);
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict__ x, long long M, long long Mpad,
+                                                          long long K, long long ldx,
                                                           const int* __restrict__ gather,
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   const int lane = threadIdx.x & 31;
@@ -68,13 +104,13 @@ __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict
     const long long row = w / nblk, blk = w % nblk;
     long long src = row < M ? row : -1;
     if (src >= 0 && gather) src = gather[row];
-    float v[kQ4Unroll][8];
+    Raw8<kBf16> raw[kQ4Unroll];
 #pragma unroll
     for (int u = 0; u < kQ4Unroll; ++u) {
       const long long k0 = (blk * kQ4Unroll + u) * 256 + lane * 8;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
-      if (k0 < K && src >= 0) load8(x, x_bf16, src * ldx + k0, v[u]);
+      for (int i = 0; i < (kBf16 ? 4 : 8); ++i) raw[u].w[i] = 0u;
+      if (k0 < K && src >= 0) load_raw8<kBf16>(x, src * ldx + k0, raw[u]);
     }
 #pragma unroll
     for (int u = 0; u < kQ4Unroll; ++u) {
@@ -82,14 +118,14 @@ __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict
       const bool active = k0 < K;
       float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[u][i]));
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(raw8_at<kBf16>(raw[u], i)));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       const uint32_t s_code = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
       const float s = e4m3_to_f32(s_code);
       const float rs = __frcp_rn(s);
       float q[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = (s == 0.0f) ? 0.0f : quot_rn(v[u][i], s, rs);
+      for (int i = 0; i < 8; ++i) q[i] = (s == 0.0f) ? 0.0f : quot_rn(raw8_at<kBf16>(raw[u], i), s, rs);
       const uint32_t word = f32x8_to_e2m1x8(q);
       if (active && row < M) *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + k0 / 2) = word;
       const uint32_t b1 = __shfl_down_sync(0xffffffffu, s_code, 2);
@@ -252,13 +288,6 @@ __global__ void __launch_bounds__(256) q8_block_kernel(const void* __restrict__ 
   }
 }
 
-static int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 148;
-}
-
 cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx,
                                const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream) {
   const long long Mpad = (M + 127) / 128 * 128;
@@ -267,7 +296,10 @@ cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long
   const long long cap = (long long)sm_count() * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  q4_quantize_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, x_bf16, M, Mpad, K, ldx, gather, codes, sf);
+  if (x_bf16)
+    q4_quantize_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(x, M, Mpad, K, ldx, gather, codes, sf);
+  else
+    q4_quantize_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(x, M, Mpad, K, ldx, gather, codes, sf);
   return cudaGetLastError();
 }
 

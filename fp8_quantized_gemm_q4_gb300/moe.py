@@ -11,9 +11,16 @@ teardown (FP8 GEMM)", section 5.3):
   3. bs_grouped_gemm     gate/up GEMM per expert with the SwiGLU epilogue
                          h = bf16(silu(x W_gate^T) * (x W_up^T))
   4. q4_quantize         re-quantize h online
-  5. bs_grouped_gemm     down GEMM per expert with the routed combine epilogue
-                         out32[token] += w * (h W_down^T)   (fp32 reductions)
-  6. bs_moe_finalize     out = bf16(out32), out32 reset to zero
+  5. bs_grouped_gemm     down GEMM per expert; the routed combine ("Blackwell
+                         FP4 MoE TFLOPS optimisation", section 3.2, result
+                         aggregation) runs one of two ways:
+       combine="rows"    (default) the GEMM writes each row's weighted result
+                         w * (h W_down^T) in fp32 (coalesced TMA stores), then
+     6. bs_moe_combine   sums each token's k rows in slot order -> bf16 out
+                         (deterministic; no atomics)
+       combine="atomic"  the GEMM reduces w * (h W_down^T) into out32[token]
+     6. bs_moe_finalize  (fp32 reductions at L2), then out = bf16(out32) and
+                         out32 is reset to zero
 
 Every step is one or more of the library's kernels; this module only holds
 the buffers and calls them in order.
@@ -24,8 +31,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import (EPI_COMBINE, EPI_SWIGLU, fp4_gather_rows, grouped_gemm_fp4, moe_dispatch, moe_finalize,
-               moe_rows_bound, q4_quantize, sf_bytes)
+from . import (EPI_COMBINE, EPI_ROWS, EPI_SWIGLU, fp4_gather_rows, grouped_gemm_fp4, moe_combine, moe_dispatch,
+               moe_finalize, moe_rows_bound, q4_quantize, sf_bytes)
 
 
 @dataclass
@@ -63,9 +70,12 @@ class MoELayer:
     """Holds the per-call buffers of one layer shape so repeated calls (and a
     CUDA-graph capture) allocate nothing."""
 
-    def __init__(self, weights: MoEWeights, T: int, k: int, device="cuda"):
+    def __init__(self, weights: MoEWeights, T: int, k: int, device="cuda", combine: str = "rows"):
+        if combine not in ("rows", "atomic"):
+            raise ValueError(f"combine must be 'rows' or 'atomic', not {combine!r}")
         self.w = weights
         self.T, self.k = T, k
+        self.combine = combine
         E, H, F = weights.E, weights.H, weights.F
         self.rows = moe_rows_bound(T, k, E)
         self.tq = torch.empty((T, H // 2), dtype=torch.uint8, device=device)
@@ -75,10 +85,14 @@ class MoELayer:
         self.h = torch.zeros((self.rows, F), dtype=torch.bfloat16, device=device)
         self.hq = torch.empty((self.rows, F // 2), dtype=torch.uint8, device=device)
         self.hs = torch.empty(sf_bytes(self.rows, F), dtype=torch.uint8, device=device)
-        self.out32 = torch.zeros((T, H), dtype=torch.float32, device=device)
-        # Down GEMM tile order: chunks of 256-column blocks small enough that
-        # the fp32 accumulator slab they reduce into (T x 256 x 4 bytes per
-        # block) stays within about half of the 129 MB L2.
+        if combine == "rows":
+            self.yrows = torch.empty((self.rows, H), dtype=torch.float32, device=device)
+            self.row_of_pair = torch.empty(max(T * k, 1), dtype=torch.int32, device=device)
+        else:
+            self.out32 = torch.zeros((T, H), dtype=torch.float32, device=device)
+        # Atomic combine tile order: chunks of 256-column blocks small enough
+        # that the fp32 accumulator slab they reduce into (T x 256 x 4 bytes
+        # per block) stays within about half of the 129 MB L2.
         self.combine_chunk = max(1, (64 << 20) // (T * 256 * 4))
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
         self.disp = None
@@ -95,8 +109,13 @@ class MoELayer:
         grouped_gemm_fp4(self.xq, self.xs, w.wgu_codes, w.wgu_sf, K=w.H, N=w.F, E=w.E, offsets=d["offsets"],
                          counts=d["counts"], epilogue=EPI_SWIGLU, out=self.h)
         q4_quantize(self.h, out=(self.hq, self.hs, None))
-        grouped_gemm_fp4(self.hq, self.hs, w.wd_codes, w.wd_sf, K=w.F, N=w.H, E=w.E, offsets=d["offsets"],
-                         counts=d["counts"], epilogue=EPI_COMBINE, token_of=d["token_of"],
-                         weight_of=d["weight_of"], out32=self.out32, n_chunk_blocks=self.combine_chunk)
-        moe_finalize(self.out32, self.out)
+        if self.combine == "rows":
+            grouped_gemm_fp4(self.hq, self.hs, w.wd_codes, w.wd_sf, K=w.F, N=w.H, E=w.E, offsets=d["offsets"],
+                             counts=d["counts"], epilogue=EPI_ROWS, out=self.yrows, weight_of=d["weight_of"])
+            moe_combine(self.yrows, d["pair_of_row"], self.T, self.k, out=self.out, row_of_pair=self.row_of_pair)
+        else:
+            grouped_gemm_fp4(self.hq, self.hs, w.wd_codes, w.wd_sf, K=w.F, N=w.H, E=w.E, offsets=d["offsets"],
+                             counts=d["counts"], epilogue=EPI_COMBINE, token_of=d["token_of"],
+                             weight_of=d["weight_of"], out32=self.out32, n_chunk_blocks=self.combine_chunk)
+            moe_finalize(self.out32, self.out)
         return self.out

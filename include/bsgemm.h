@@ -57,7 +57,8 @@ typedef enum { BS_FMT_FP4 = 0, BS_FMT_FP8 = 1 } bs_format;
 typedef enum {
     BS_EPI_STORE = 0,  /* Y rows written to `out` */
     BS_EPI_SWIGLU = 1, /* grouped only: out[r, n] = bf16(silu(g[r,n]) * u[r,n]) */
-    BS_EPI_COMBINE = 2 /* grouped only: out32[token_of[r], n] += weight_of[r] * y[r, n] */
+    BS_EPI_COMBINE = 2, /* grouped only: out32[token_of[r], n] += weight_of[r] * y[r, n] */
+    BS_EPI_ROWS = 3     /* grouped only: out fp32 [r, n] = weight_of[r] * y[r, n] */
 } bs_epilogue;
 
 typedef enum { BS_Q8_TOKEN_1x128 = 1, BS_Q8_BLOCK_128x128 = 128 } bs_q8_mode;
@@ -217,7 +218,13 @@ bs_status bs_gemm(const bs_gemm_args *args, bs_stream_t stream);
  *                   BS_EPI_COMBINE: out32[token_of[r], n] += weight_of[r] * y[r, n]
  *                                   (fp32 reductions; out32 [*, ld_out32] must
  *                                   be zeroed by the caller or bs_moe_finalize)
- *   token_of, weight_of  int32 / fp32 [M] (COMBINE only)
+ *                   BS_EPI_ROWS:    out fp32 [M, ldo]: out[r, n] = weight_of[r] * y[r, n]
+ *                                   for the rows r < offsets[e] + counts[e]; rows
+ *                                   past a count may be left unwritten or get
+ *                                   weight_of[r] * y[r, n] (bs_moe_dispatch gives
+ *                                   them weight 0).  The first half of a
+ *                                   two-pass routed combine, see bs_moe_combine
+ *   token_of        int32 [M] (COMBINE only); weight_of fp32 [M] (COMBINE, ROWS)
  * Only alpha = 1, no col_scale, no lora and no bias are accepted here.
  * Offsets that break the contract set BS_ERR_OFFSETS in the device status and
  * the kernel writes nothing.
@@ -283,6 +290,32 @@ bs_status bs_moe_dispatch_noalloc(const int32_t *topk_ids, const float *topk_w, 
  * so the accumulator is ready for the next layer call ("DeepGEMM for Hopper
  * MoE", section 3: FP16-class output of the weighted sum). */
 bs_status bs_moe_finalize(float *out32, void *out_bf16, int64_t n, bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * bs_moe_combine -- second pass of the two-pass routed combine: the weighted
+ * top-k expert outputs of each token are summed into one bf16 row
+ * ("Blackwell FP4 MoE TFLOPS optimisation", section 3.2: result aggregation as
+ * a stage of its own after the expert matmuls; "DeepGEMM for Hopper MoE",
+ * section 3: the weighted sum of the selected experts' outputs).
+ *
+ *   out[t, n] = bf16( sum over j = 0 .. k-1 of rows[row_of(t, j), n] )
+ *
+ * summed in fp32 in slot order j (deterministic), where row_of(t, j) is the
+ * row bs_moe_dispatch placed pair t*k + j in; pairs the dispatch dropped
+ * (out-of-range expert ids) add nothing.
+ *
+ *   rows         fp32 [n_rows, ld_rows]: weight_of[r] * y[r, :] from
+ *                bs_grouped_gemm with BS_EPI_ROWS; 16-byte aligned, ld_rows % 4 == 0
+ *   pair_of_row  int32 [n_rows] from bs_moe_dispatch (-1 on padding rows)
+ *   T, k, H      tokens, slots per token, columns (H % 8 == 0, H <= ld_rows)
+ *   row_of_pair  int32 [T*k] device scratch owned by the caller; written here
+ *                (the inverse of pair_of_row, -1 for dropped pairs)
+ *   out          bf16 [T, ldo], 16-byte aligned, ldo % 8 == 0, ldo >= H
+ * Invalid sizes / pointers return BS_ERR_INVALID or BS_ERR_ALIGN before any launch.
+ * ------------------------------------------------------------------------- */
+bs_status bs_moe_combine(const float *rows, int64_t ld_rows, const int32_t *pair_of_row, int64_t n_rows,
+                         int64_t T, int k, int64_t H, int32_t *row_of_pair, void *out, int64_t ldo,
+                         bs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Status.

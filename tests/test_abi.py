@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("q4_quantize", "q8_quantize", "bs_gemm", "bs_grouped_gemm", "bs_moe_dispatch",
-              "bs_moe_finalize", "bs_sf_bytes", "bs_sf_offset", "bs_get_device_status"):
+              "bs_moe_finalize", "bs_moe_combine", "bs_sf_bytes", "bs_sf_offset", "bs_get_device_status"):
         assert n in names
 
 
@@ -100,6 +100,13 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.bs_moe_dispatch(fake, fake, 8, 2, 0, fake, fake, fake, fake, fake, fake, 1 << 20, None) == bs.BS_ERR_INVALID
     assert lib.bs_moe_rows_bound(8, 2, 2) == 16 + 2 * 127
     assert lib.bs_moe_finalize(P((1 << 20) + 4), fake, 8, None) == bs.BS_ERR_ALIGN
+    # ROWS needs fp32 output and weight_of (g.out_dtype is bf16 here)
+    assert lib.bs_grouped_gemm(ctypes.byref(g), 4, fake, fake, 3, None, fake, None, 0, None) == bs.BS_ERR_INVALID
+    # combine: bad k, H not a multiple of 8, misaligned rows; T = 0 is a no-op
+    assert lib.bs_moe_combine(fake, 64, fake, 128, 4, 0, 64, fake, fake, 64, None) == bs.BS_ERR_INVALID
+    assert lib.bs_moe_combine(fake, 64, fake, 128, 4, 2, 60, fake, fake, 64, None) == bs.BS_ERR_ALIGN
+    assert lib.bs_moe_combine(P((1 << 20) + 4), 64, fake, 128, 4, 2, 64, fake, fake, 64, None) == bs.BS_ERR_ALIGN
+    assert lib.bs_moe_combine(None, 64, None, 0, 0, 2, 64, None, None, 64, None) == bs.BS_OK
     assert lib.bs_status_string(5) == b"device pipeline wait timed out"
     assert b"K=100" in lib.bs_last_error() or lib.bs_last_error() != b""
 

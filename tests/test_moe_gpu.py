@@ -71,13 +71,16 @@ def _small_moe(T=200, H=256, F=128, E=5, k=2, seed=3):
 @pytest.mark.parametrize("T,H,F,E,k,chunk", [(200, 256, 128, 5, 2, 0), (1000, 512, 256, 8, 4, 0),
                                              (64, 256, 128, 16, 8, 0), (300, 1024, 256, 6, 2, 1),
                                              (300, 1024, 256, 6, 2, 3)])
-def test_grouped_layer_staged(cuda_lib, fp4_kernel, T, H, F, E, k, chunk):
-    """chunk > 0: the down GEMM walks column chunks of that many 256-wide blocks."""
+@pytest.mark.parametrize("combine", ["rows", "atomic"])
+def test_grouped_layer_staged(cuda_lib, fp4_kernel, combine, T, H, F, E, k, chunk):
+    """combine="rows": weighted fp32 rows, then a slot-order sum per token;
+    "atomic": fp32 reductions into out32.  chunk > 0 (atomic): the down GEMM
+    walks column chunks of that many 256-wide blocks."""
     bs = cuda_lib
     from fp8_quantized_gemm_q4_gb300.moe import MoELayer, quantize_expert_weights
     r, x, ws = _small_moe(T, H, F, E, k)
     W = quantize_expert_weights([a for a, _ in ws], [b for _, b in ws])
-    layer = MoELayer(W, T, k)
+    layer = MoELayer(W, T, k, combine=combine)
     if chunk:
         layer.combine_chunk = chunk
     out = layer.forward(x.cuda(), torch.from_numpy(r["topk_ids"]).cuda(), torch.from_numpy(r["topk_w"]).cuda())
@@ -127,8 +130,45 @@ def test_grouped_layer_staged(cuda_lib, fp4_kernel, T, H, F, E, k, chunk):
         np.add.at(S, pairs // k, np.abs(wflat[pairs][:, None]) * sy)
     ok, ratio, rel = gemm_errors(out.float().cpu().numpy(), ref, S, True)
     assert ok, (ratio, rel)
-    # out32 was reset by the finalize step
-    assert float(layer.out32.abs().max()) == 0.0
+    if combine == "atomic":
+        # out32 was reset by the finalize step
+        assert float(layer.out32.abs().max()) == 0.0
+    else:
+        # a written padding row (one sharing a 32-row box with real rows) is zero
+        yrows = layer.yrows[:rows].cpu().numpy()
+        shared = np.zeros(rows, dtype=bool)
+        for b0 in range(0, rows, 32):
+            shared[b0:b0 + 32] = real[b0:b0 + 32].any()
+        assert np.all(yrows[~real & shared] == 0)
+
+
+@pytest.mark.parametrize("T,k,H,n_rows,drop", [(1, 1, 8, 128, 0), (300, 4, 264, 1536, 7), (1000, 8, 1024, 8320, 31),
+                                               (50, 11, 64, 768, 3)])
+def test_combine_bit_exact(cuda_lib, T, k, H, n_rows, drop):
+    """bs_moe_combine against a float32 sum in slot order (absent slots add +0)
+    rounded once to bf16: bit-exact.  Pairs are placed on random rows; `drop`
+    pairs have no row (as for out-of-range expert ids)."""
+    bs = cuda_lib
+    rng = np.random.default_rng(T * 1000 + k)
+    P = T * k
+    rows_of = rng.permutation(n_rows)[:P].astype(np.int32)
+    dropped = rng.choice(P, size=drop, replace=False) if drop else np.zeros(0, dtype=np.int64)
+    pair_of_row = np.full(n_rows, -1, dtype=np.int32)
+    keep = np.setdiff1d(np.arange(P), dropped)
+    pair_of_row[rows_of[keep]] = keep
+    rows = rng.standard_normal((n_rows, H)).astype(np.float32)
+    acc = np.zeros((T, H), dtype=np.float32)
+    for j in range(k):
+        p = np.arange(T) * k + j
+        r = np.where(np.isin(p, dropped), -1, rows_of[p])
+        add = np.where((r >= 0)[:, None], rows[np.maximum(r, 0)], np.float32(0.0))
+        acc = (acc + add).astype(np.float32)
+    ref = torch.from_numpy(acc).to(torch.bfloat16)
+    out = bs.moe_combine(torch.from_numpy(rows).cuda(), torch.from_numpy(pair_of_row).cuda(), T, k)
+    out2 = bs.moe_combine(torch.from_numpy(rows).cuda(), torch.from_numpy(pair_of_row).cuda(), T, k)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu().view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(out2.cpu().view(torch.int16), ref.view(torch.int16))
 
 
 def test_layer_end_to_end_report(cuda_lib):
