@@ -62,6 +62,11 @@ double orc_e4m3_decode(uint8_t code)
  * go to the largest value (saturation).  Exhaustive search. */
 static uint8_t nearest_code(double mag, int ncodes, double (*dec)(uint8_t))
 {
+    /* Saturation: at or above the largest finite value the nearest finite
+     * value is that one.  (Tested first: for a magnitude ~2^53 times the
+     * maximum every distance below rounds to the same double.) */
+    if (mag >= dec((uint8_t)(ncodes - 1)))
+        return (uint8_t)(ncodes - 1);
     int best = 0;
     double best_d = INFINITY;
     for (int c = 0; c < ncodes; ++c) {

@@ -67,9 +67,27 @@ def test_e4m3_matches_torch_cast():
 
 
 def test_e4m3_saturates():
-    for v in (448.0, 449.0, 463.9, 464.0, 500.0, 1e6):
+    # up to the largest finite doubles: every value at or above 448 is 448
+    # (for magnitudes ~2^53 x 448 a distance-based search sees only ties)
+    for v in (448.0, 449.0, 463.9, 464.0, 500.0, 1e6, 2.0 ** 62, 1e30, 3.3895313892515355e38, 1e300):
         assert oracle.e4m3_encode(v) == 0x7E
         assert oracle.e4m3_encode(-v) == 0xFE
+
+
+def test_e2m1_saturates_at_any_magnitude():
+    for v in (6.0, 7.0, 1e6, 2.0 ** 60, 1e30, 1e300):
+        assert oracle.e2m1_encode(v) == 0x7
+        assert oracle.e2m1_encode(-v) == 0xF
+
+
+def test_q4_quantize_huge_groups_saturate():
+    # amax / 6 far above 448: the scale saturates to 448 and the codes of the
+    # group (x / 448, still far above 6) saturate to +-6
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, 0], x[0, 1], x[0, 16] = 3e38, -1e30, 1e20
+    c, s = oracle.q4_quantize(x)
+    assert list(s.ravel()) == [0x7E, 0x7E]
+    assert c[0, 0] == (0x7 | (0xF << 4)) and c[0, 8] == 0x7
 
 
 # ---------------------------------------------------------------------------
