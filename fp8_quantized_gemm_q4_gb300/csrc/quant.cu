@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict
                                                           const int* __restrict__ gather,
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   const int lane = threadIdx.x & 31;
+  const float r6 = __frcp_rn(6.0f);
   const long long nblk = (K + 256 * kQ4Unroll - 1) / (256 * kQ4Unroll);
   const long long total = Mpad * nblk;
   const long long kchunks = K / 64;
@@ -120,13 +121,15 @@ __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict
 #pragma unroll
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(raw8_at<kBf16>(raw[u], i)));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      const uint32_t s_code = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
+      // bf16 amax: the one-correction quotient is RN(amax / 6) (6 is an e4m3
+      // value, so the exhaustive GPU tests cover every case); fp32: IEEE divide
+      const uint32_t s_code = f32_to_e4m3(kBf16 ? quot_rn(amax, 6.0f, r6) : __fdiv_rn(amax, 6.0f));
       const float s = e4m3_to_f32(s_code);
       const float rs = __frcp_rn(s);
       float q[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = (s == 0.0f) ? 0.0f : quot_rn(raw8_at<kBf16>(raw[u], i), s, rs);
-      const uint32_t word = f32x8_to_e2m1x8(q);
+      for (int i = 0; i < 8; ++i) q[i] = quot_rn(raw8_at<kBf16>(raw[u], i), s, rs);
+      const uint32_t word = (s == 0.0f) ? 0u : f32x8_to_e2m1x8(q);  // zero group: all codes +0
       if (active && row < M) *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + k0 / 2) = word;
       const uint32_t b1 = __shfl_down_sync(0xffffffffu, s_code, 2);
       const uint32_t b2 = __shfl_down_sync(0xffffffffu, s_code, 4);
@@ -385,6 +388,7 @@ __global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
     uint8_t* __restrict__ sf, __nv_bfloat16* __restrict__ t_out) {
   extern __shared__ __align__(128) uint8_t fsm[];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float r6 = __frcp_rn(6.0f);
   const long long r0 = (long long)blockIdx.x * fq::R;
   const int nchunks = (int)(K / fq::KC);
   const uint32_t sbase = smem_u32(fsm);
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[16 * g + i]));
-        const uint32_t sc = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
+        const uint32_t sc = f32_to_e4m3(quot_rn(amax, 6.0f, r6));  // RN(amax / 6) for bf16 amax
         const float sv = e4m3_to_f32(sc);
         const float rs = __frcp_rn(sv);
         sfh |= sc << (8 * g);
@@ -468,8 +472,8 @@ __global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
         for (int h = 0; h < 2; ++h) {
           float q[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) q[i] = (sv == 0.0f) ? 0.0f : quot_rn(v[16 * g + 8 * h + i], sv, rs);
-          cw[2 * g + h] = f32x8_to_e2m1x8(q);
+          for (int i = 0; i < 8; ++i) q[i] = quot_rn(v[16 * g + 8 * h + i], sv, rs);
+          cw[2 * g + h] = (sv == 0.0f) ? 0u : f32x8_to_e2m1x8(q);  // zero group: all codes +0
         }
       }
       // two scale bytes = half of the 64-element chunk's scale word

@@ -107,6 +107,44 @@ def test_q4_lowrank_fused_exhaustive_bf16_quotients(cuda_lib):
     assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), x.shape[0], 1024), os_)
 
 
+def _every_bf16_amax(K):
+    """One 16-element group per finite positive bf16 value v: the group holds v
+    (its amax), -v/2 and 0.7 v (rounded to bf16, both below v in magnitude), so
+    the group scale e4m3(RN(v / 6)) is taken for every amax a bf16 input can
+    have.  Rows of K elements, zero groups as padding."""
+    allbf = torch.arange(1, 0x7F80, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float()
+    g = torch.zeros(allbf.numel(), 16)
+    g[:, 0] = allbf
+    g[:, 5] = -allbf / 2
+    g[:, 9] = allbf * 0.7
+    per_row = K // 16
+    pad = (-g.shape[0]) % per_row
+    g = torch.cat([g, torch.zeros(pad, 16)])
+    return g.reshape(-1, K).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_q4_quantize_every_bf16_amax(cuda_lib, dtype):
+    bs = cuda_lib
+    x = _every_bf16_amax(256).to(dtype)
+    codes, sf, _ = bs.q4_quantize(x.cuda())
+    torch.cuda.synchronize()
+    oc, os_ = oracle.q4_quantize(x)
+    assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), x.shape[0], 256), os_)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+def test_q4_lowrank_fused_every_bf16_amax(cuda_lib):
+    bs = cuda_lib
+    x = _every_bf16_amax(1024)
+    a = (torch.randn(1024, 32) * 0.02).to(torch.bfloat16)
+    codes, sf, _ = bs.q4_quantize(x.cuda(), lora_a_t=a.t().contiguous().cuda())
+    torch.cuda.synchronize()
+    oc, os_ = oracle.q4_quantize(x)
+    assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), x.shape[0], 1024), os_)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
+
 @pytest.mark.parametrize("rows_in,rows_out,K", [(50, 8, 256), (4096, 1000, 4096), (7, 300, 64)])
 def test_fp4_gather_rows_equals_quantize_with_gather(cuda_lib, rows_in, rows_out, K):
     bs = cuda_lib
