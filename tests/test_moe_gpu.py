@@ -191,3 +191,85 @@ def test_layer_end_to_end_report(cuda_lib):
     print(f"end-to-end MoE max |err| / max |ref| = {rel:.3g}")
     assert rel < 0.05
     assert bs.device_status()[0] == 0
+
+
+def _sf_rows(sf, rows, K):
+    """Scale bytes of the given rows from the MMA layout ([len(rows), K/16])."""
+    sf = np.asarray(sf).reshape(-1)
+    r = np.asarray(rows)[:, None]
+    g = np.arange(K // 16)[None, :]
+    off = ((r // 128) * (K // 64) + g // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + g % 4
+    return sf[off]
+
+
+@pytest.mark.parametrize("cfg,index", [("MOE_SMALL", 3), ("MOE_LARGE", 4)])
+def test_full_size_layer_sampled_tokens(cuda_lib, cfg, index):
+    """The benchmark's MoE layers at full size, through the same layer object
+    the bench times (two-pass combine, CTA pairs), checked on sampled tokens in
+    the same stages as the small-shape test: routed activation codes
+    bit-exact, h against the oracle's SwiGLU of its GEMMs on the GPU's codes,
+    re-quantized h bit-exact, and the combined output against the oracle's
+    down GEMMs on the GPU's quantized h."""
+    bs = cuda_lib
+    from fp8_quantized_gemm_q4_gb300.moe import MoELayer, MoEWeights
+    c = getattr(workloads, cfg)
+    T, H, E, k, F = c["T"], c["H"], c["E"], c["k"], c["F"]
+    r = workloads.moe_routing(T, E, k, index=index)
+    x = workloads.moe_activations(T, H, index=index)
+    ids = r["topk_ids"]
+    # tokens: first, middle, last, and one routed to the most loaded expert
+    heavy = int(np.bincount(ids.reshape(-1), minlength=E).argmax())
+    samples = sorted({0, T // 2, T - 1, int(np.nonzero((ids == heavy).any(axis=1))[0][0])})
+    experts = sorted({int(e) for t in samples for e in ids[t]})
+    F2 = 2 * F
+    wgu_codes = torch.empty((E * F2, H // 2), dtype=torch.uint8, device="cuda")
+    wgu_sf = torch.empty(bs.sf_bytes(E * F2, H), dtype=torch.uint8, device="cuda")
+    wd_codes = torch.empty((E * H, F // 2), dtype=torch.uint8, device="cuda")
+    wd_sf = torch.empty(bs.sf_bytes(E * H, F), dtype=torch.uint8, device="cuda")
+    pg, pd = bs.sf_bytes(F2, H), bs.sf_bytes(H, F)
+    host_w = {}
+    for e in range(E):
+        wgu, wd = workloads.moe_expert_weights(e, F, H, index=index, device="cuda")
+        bs.q4_quantize(wgu, out=(wgu_codes[e * F2:(e + 1) * F2], wgu_sf[e * pg:(e + 1) * pg], None))
+        bs.q4_quantize(wd, out=(wd_codes[e * H:(e + 1) * H], wd_sf[e * pd:(e + 1) * pd], None))
+        if e in experts:
+            host_w[e] = (wgu.cpu(), wd.cpu())
+        del wgu, wd
+    layer = MoELayer(MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf), T, k)
+    out = layer.forward(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(r["topk_w"]).cuda())
+    torch.cuda.synchronize()
+    assert bs.device_status()[0] == 0
+    rop = layer.row_of_pair.cpu().numpy()
+    rows = np.array([rop[t * k + j] for t in samples for j in range(k)])
+    assert np.all(rows >= 0)
+    xq = layer.xq[torch.from_numpy(rows).cuda().long()].cpu().numpy()
+    xs = _sf_rows(layer.xs.cpu().numpy(), rows, H)
+    oa, osa = oracle.q4_quantize(x[[t for t in samples for _ in range(k)]])
+    assert np.array_equal(xq, oa) and np.array_equal(xs, osa)
+    h = layer.h[torch.from_numpy(rows).cuda().long()].float().cpu().numpy()
+    hq = layer.hq[torch.from_numpy(rows).cuda().long()].cpu().numpy()
+    hs = _sf_rows(layer.hs.cpu().numpy(), rows, F)
+    ohq, ohs = oracle.q4_quantize(layer.h[torch.from_numpy(rows).cuda().long()].cpu())
+    assert np.array_equal(hq, ohq) and np.array_equal(hs, ohs)
+    oq = {e: (oracle.q4_quantize(host_w[e][0]), oracle.q4_quantize(host_w[e][1])) for e in experts}
+    got = out.float().cpu().numpy()
+    for i, t in enumerate(samples):
+        ref = np.zeros(H)
+        S = np.zeros(H)
+        for j in range(k):
+            n = i * k + j
+            e = int(ids[t, j])
+            (gu_c, gu_s), (d_c, d_s) = oq[e]
+            gu, s_gu = oracle.gemm_fp4(xq[n:n + 1], xs[n:n + 1], gu_c, gu_s, H)
+            g_, u_ = gu[:, :F], gu[:, F:]
+            h_ref = oracle.swiglu(g_, u_)
+            sig = 1.0 / (1.0 + np.exp(-g_))
+            dsilu = np.abs(sig * (1 + g_ * (1 - sig)))
+            bound = 1e-3 * (dsilu * np.abs(u_) * s_gu[:, :F] + np.abs(g_ * sig) * s_gu[:, F:]) + 2.0 ** -8 * np.abs(h_ref)
+            assert np.all(np.abs(h[n:n + 1] - h_ref) <= bound + 1e-30), (t, j)
+            y, sy = oracle.gemm_fp4(hq[n:n + 1], hs[n:n + 1], d_c, d_s, F)
+            wgt = float(r["topk_w"][t, j])
+            ref += wgt * y[0]
+            S += abs(wgt) * sy[0]
+        ok, ratio, rel = gemm_errors(got[t:t + 1], ref[None], S[None], True)
+        assert ok, (t, ratio, rel)
