@@ -269,9 +269,10 @@ class MoEWorkload:
     """Grouped FP4 MoE layer: dispatch, gather + quantize, gate/up GEMM + SwiGLU,
     re-quantize, down GEMM + routed combine, bf16 cast (one step = one layer)."""
 
-    def __init__(self, large, combine="rows"):
+    def __init__(self, large, combine="rows", graph=True):
         import workloads
         self.combine = combine
+        self.graph = graph  # the layer replayed as one CUDA graph
         cfg = workloads.MOE_LARGE if large else workloads.MOE_SMALL
         self.index = 4 if large else 3
         self.T, self.H, self.E, self.k, self.F = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["F"]
@@ -317,6 +318,10 @@ class MoEWorkload:
         W = MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf)
         self.layer = MoELayer(W, self.T, self.k, device=dev, combine=self.combine)
         self.out = self.layer.out
+        if self.graph:
+            # capture once; from here on the workload's inputs are the graph's static ones
+            self.layer.capture(self.x, self.ids, self.w)
+            self.x, self.ids, self.w = self.layer.static_x, self.layer.static_ids, self.layer.static_w
         # dispatch 3 + quantize 1 + gather 1 + gemm 1 + quantize 1 + gemm 1, then
         # combine 3 (invert, init, sum) or finalize 2 (cast, zero)
         self.launches_per_step = 11 if self.combine == "rows" else 10
@@ -325,11 +330,20 @@ class MoEWorkload:
         counts = torch.bincount(self.ids.flatten().long(), minlength=E).cpu()
         self.load_hist = {"max": int(counts.max()), "min": int(counts.min()), "empty": int((counts == 0).sum())}
 
+    def e2e_buffers(self):
+        import torch
+        return [(self.x.cpu().pin_memory(), self.x if self.graph else torch.empty_like(self.x)),
+                (self.ids.cpu().pin_memory(), self.ids), (self.w.cpu().pin_memory(), self.w)]
+
     def step(self, x=None, gemm_events=None):
         x = self.x if x is None else x
         if gemm_events:
             gemm_events[0].record()
-        out = self.layer.forward(x, self.ids, self.w)
+        if self.graph:
+            # the graph reads the static inputs (self.x / ids / w are those)
+            out = self.layer.replay(None if x is self.x else x)
+        else:
+            out = self.layer.forward(x, self.ids, self.w)
         if gemm_events:
             gemm_events[1].record()
         return out
@@ -452,20 +466,28 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
     gemm_ms = sum(a.elapsed_time(b) for a, b in gev) / K
     step_ms, gemm_ms = max_over_ranks([step_ms, gemm_ms], dev)
 
-    # end to end through the public API with pinned host buffers
-    xh = wl.x.cpu().pin_memory()
+    # end to end through the public API with pinned host buffers: every input
+    # of the step is copied host -> device (workloads with several inputs name
+    # them as (host, device) pairs, the first being the activations)
+    if hasattr(wl, "e2e_buffers"):
+        pairs = wl.e2e_buffers()
+    else:
+        pairs = [(wl.x.cpu().pin_memory(), torch.empty_like(wl.x))]
     yh = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
-    xd = torch.empty_like(wl.x)
     Ke = args.e2e_steps if args.e2e_steps > 0 else max(1, min(K, 100))
+
+    def e2e_step():
+        for h, d in pairs:
+            d.copy_(h, non_blocking=True)
+        yh.copy_(wl.step(pairs[0][1]), non_blocking=True)
+
     for _ in range(3):
-        xd.copy_(xh, non_blocking=True)
-        yh.copy_(wl.step(xd), non_blocking=True)
+        e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(Ke):
-        xd.copy_(xh, non_blocking=True)
-        yh.copy_(wl.step(xd), non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
@@ -486,7 +508,7 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
                    "parallelism": f"replicas x{world}",
-                   **({"moe_combine": wl.combine} if hasattr(wl, "combine") else {})},
+                   **({"moe_combine": wl.combine, "cuda_graph": wl.graph} if hasattr(wl, "combine") else {})},
         "e2e": {"value": round(job_throughput(wl.flops, world, e2e_ms) / 1e12, 2), "unit": wl.unit,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": wl.bytes_in,
                 "d2h_bytes_per_step": wl.bytes_out},
@@ -560,6 +582,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (default min(steps, 100))")
     ap.add_argument("--moe-combine", choices=["rows", "atomic"], default="rows",
                     help="MoE routed combine: weighted rows + per-token sum, or fp32 reductions")
+    ap.add_argument("--moe-eager", action="store_true",
+                    help="MoE: launch the layer's kernels one by one instead of replaying its CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -568,6 +592,7 @@ def main():
     wl = WORKLOADS[args.workload]()
     if isinstance(wl, MoEWorkload):
         wl.combine = args.moe_combine
+        wl.graph = not args.moe_eager
 
     if args.impl == "reference":
         if rank == 0:

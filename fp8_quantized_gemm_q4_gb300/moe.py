@@ -119,3 +119,34 @@ class MoELayer:
                              weight_of=d["weight_of"], out32=self.out32, n_chunk_blocks=self.combine_chunk)
             moe_finalize(self.out32, self.out)
         return self.out
+
+    def capture(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor) -> None:
+        """Record the whole layer (all its launches) as one CUDA graph ("Blackwell
+        FP4 MoE TFLOPS optimisation", section 3.2: the compute flow captured in a
+        CUDA Graph).  The graph reads static copies of the inputs; replay()
+        refreshes them and runs the layer with one graph launch."""
+        self.static_x = x.clone()
+        self.static_ids = topk_ids.clone()
+        self.static_w = topk_w.clone()
+        self.forward(self.static_x, self.static_ids, self.static_w)  # sizes the dispatch tables
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                self.forward(self.static_x, self.static_ids, self.static_w)
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = g
+
+    def replay(self, x: torch.Tensor | None = None, topk_ids: torch.Tensor | None = None,
+               topk_w: torch.Tensor | None = None) -> torch.Tensor:
+        """Run the captured layer; given inputs are first copied into the static ones."""
+        if x is not None:
+            self.static_x.copy_(x, non_blocking=True)
+        if topk_ids is not None:
+            self.static_ids.copy_(topk_ids, non_blocking=True)
+        if topk_w is not None:
+            self.static_w.copy_(topk_w, non_blocking=True)
+        self.graph.replay()
+        return self.out

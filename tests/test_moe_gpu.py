@@ -273,3 +273,27 @@ def test_full_size_layer_sampled_tokens(cuda_lib, cfg, index):
             S += abs(wgt) * sy[0]
         ok, ratio, rel = gemm_errors(got[t:t + 1], ref[None], S[None], True)
         assert ok, (t, ratio, rel)
+
+
+def test_layer_graph_replay_matches_forward(cuda_lib):
+    """The layer captured as one CUDA graph: replays give the eager forward's
+    output bit for bit (the combine is deterministic), also after new
+    activations are copied in."""
+    from fp8_quantized_gemm_q4_gb300.moe import MoELayer, quantize_expert_weights
+    T, H, F, E, k = 300, 512, 256, 6, 4
+    r, x, ws = _small_moe(T, H, F, E, k)
+    W = quantize_expert_weights([a for a, _ in ws], [b for _, b in ws])
+    ids = torch.from_numpy(r["topk_ids"]).cuda()
+    w = torch.from_numpy(r["topk_w"]).cuda()
+    xd = x.cuda()
+    ref = MoELayer(W, T, k).forward(xd, ids, w).clone()
+    x2 = (x.float() * 0.5 + 0.125).to(torch.bfloat16).cuda()
+    ref2 = MoELayer(W, T, k).forward(x2, ids, w).clone()
+    layer = MoELayer(W, T, k)
+    layer.capture(xd, ids, w)
+    out1 = layer.replay().clone()
+    out2 = layer.replay(x2).clone()
+    out3 = layer.replay(xd).clone()
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status()[0] == 0
+    assert torch.equal(out1, ref) and torch.equal(out2, ref2) and torch.equal(out3, ref)
