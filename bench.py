@@ -322,9 +322,14 @@ class MoEWorkload:
             # capture once; from here on the workload's inputs are the graph's static ones
             self.layer.capture(self.x, self.ids, self.w)
             self.x, self.ids, self.w = self.layer.static_x, self.layer.static_ids, self.layer.static_w
-        # dispatch 3 + quantize 1 + gather 1 + gemm 1 + quantize 1 + gemm 1, then
-        # combine 3 (invert, init, sum) or finalize 2 (cast, zero)
-        self.launches_per_step = 11 if self.combine == "rows" else 10
+        # dispatch 3 + quantize 1 + gather 1 + gate/up GEMM + quantize 1 + down GEMM,
+        # then combine 3 (invert, init, sum) or finalize 2 (cast, zero); each
+        # grouped GEMM is two launches on CTA pairs with the small experts
+        # split off (the library's default), one otherwise
+        pair = os.environ.get("BSGEMM_FP4_PAIR", "1") != "0"
+        tails = os.environ.get("BSGEMM_FP4_TAILS", "1") != "0"
+        g = 2 if (pair and tails) else 1
+        self.launches_per_step = 5 + 2 * g + (3 if self.combine == "rows" else 2)
         self.bytes_in = self.x.numel() * 2 + self.ids.numel() * 4 + self.w.numel() * 4
         self.bytes_out = self.out.numel() * 2
         counts = torch.bincount(self.ids.flatten().long(), minlength=E).cpu()

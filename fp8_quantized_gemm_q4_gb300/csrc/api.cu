@@ -287,10 +287,20 @@ static bool fp8_split_ok() {
   return on;
 }
 
+// Grouped GEMMs on CTA pairs hand experts of at most 128 rows to a second,
+// one-CTA launch (BSGEMM_FP4_TAILS=0 keeps them in the pair launch).
+// Read on every call.
+static bool fp4_split_tails() {
+  const char* e = getenv("BSGEMM_FP4_TAILS");
+  return !(e && atoi(e) == 0);
+}
+
 static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int sms, cudaStream_t s,
                             long long pair_tiles, bool grouped) {
   bs_status st;
   if (fp4_pair() && sms >= 2) {  // a pair needs two SMs
+    const bool split = grouped && fp4_split_tails();
+    L.p.part = split ? 1 : 0;
     bsk::Fp4PairLaunch P;
     memset(&P, 0, sizeof P);
     st = fp4_maps(L, a, b_rows, fp4_bk());
@@ -316,6 +326,12 @@ static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_
     P.grid = 2 * (int)(grouped ? pairs : (pair_tiles < pairs ? pair_tiles : pairs));
     cudaError_t e = bsk::launch_fp4_pair_gemm(P, s);
     if (e != cudaSuccess) return cuda_fail(e, "FP4 pair GEMM launch");
+    if (split) {
+      // the small experts: one CTA per 128-row tile, same operand maps
+      L.p.part = 2;
+      e = bsk::launch_fp4_gemm(L, s);
+      if (e != cudaSuccess) return cuda_fail(e, "FP4 tail GEMM launch");
+    }
     return BS_OK;
   }
   st = fp4_maps(L, a, b_rows, fp4_bk());

@@ -176,12 +176,13 @@ __device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, i
     if (prefix[mid] * nbc <= rem) lo = mid; else hi = mid - 1;
   }
   const int e = lo;
-  const int cnt = p.counts[e];
+  int eoff, cnt;
+  expert_part(p, e, eoff, cnt);
   const int mblk = prefix[e + 1] - prefix[e];
   const int local = rem - prefix[e] * nbc;
   const int nb = c * nck + local / mblk, mb = local % mblk;
   tl.expert = e;
-  tl.row0 = p.offsets[e] + mb * BM;
+  tl.row0 = eoff + mb * BM;
   tl.rows = min(BM, cnt - mb * BM);
   const int64_t wrows = (kEpi == kEpiSwiglu) ? 2LL * p.N : (int64_t)p.N;  // weight rows per expert
   if (kEpi == kEpiSwiglu) {
@@ -251,7 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (e < p.E) {
           const int off = p.offsets[e], cnt = p.counts[e], nxt = p.offsets[e + 1];
           if (cnt < 0 || (off % BM) != 0 || off + cnt > nxt || nxt > p.M) bad = true;
-          tiles = (max(cnt, 0) + BM - 1) / BM;  // row blocks of expert e
+          int eoff, ecnt;
+          expert_part(p, e, eoff, ecnt);
+          tiles = (max(ecnt, 0) + BM - 1) / BM;  // row blocks of expert e in this launch
         }
         int incl = tiles;
 #pragma unroll

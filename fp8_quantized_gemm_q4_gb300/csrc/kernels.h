@@ -29,8 +29,22 @@ struct Fp4Params {
   long long ld_out32;
   int* status;
   int n_chunk;            // grouped tile order: column blocks per chunk (0 = all)
+  int part;               // grouped rows covered: 0 all, 1 experts > 128 rows, 2 the others (expert_part)
 };
 
+// Rows of expert e that one grouped launch covers.  part 0: all of them.  A
+// grouped GEMM on CTA pairs is split in two launches so that small experts do
+// not fill 256-row pair tiles with padding: part 1 (CTA pairs) takes the
+// experts with more than 128 rows, part 2 (one CTA per 128-row tile) those
+// with at most 128.  Whole experts move, so each expert's weights are still
+// streamed by one launch only.
+__device__ __forceinline__ void expert_part(const Fp4Params& p, int e, int& off, int& cnt) {
+  off = p.offsets[e];
+  cnt = p.counts[e];
+  if (p.part == 0) return;
+  const bool small = cnt <= 128;
+  if ((p.part == 1 && small) || (p.part == 2 && !small)) cnt = 0;
+}
 struct Fp4Launch {
   CUtensorMap tmA, tmB, tmT, tmL;
   Fp4Params p;

@@ -19,10 +19,13 @@ from tests.helpers import gemm_errors, sf_rowmajor
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["pair", "one_cta"])
+@pytest.fixture(params=["pair", "pair_whole", "one_cta"])
 def fp4_kernel(request, monkeypatch):
-    """Grouped GEMMs on CTA pairs (default) or on the one-CTA kernel."""
-    monkeypatch.setenv("BSGEMM_FP4_PAIR", "1" if request.param == "pair" else "0")
+    """Grouped GEMMs on CTA pairs with the small experts (<= 128 rows) in a
+    second one-CTA launch (default), on CTA pairs alone, or on the one-CTA
+    kernel alone."""
+    monkeypatch.setenv("BSGEMM_FP4_PAIR", "0" if request.param == "one_cta" else "1")
+    monkeypatch.setenv("BSGEMM_FP4_TAILS", "0" if request.param == "pair_whole" else "1")
     return request.param
 
 
