@@ -51,9 +51,22 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int* __restrict__ hist, 
   const int e = threadIdx.x;
   int total = 0;
   if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
+    // exclusive base of chunk c inside expert e; the counts of 16 chunks are
+    // loaded together so their round trips overlap
+    int c = 0;
+    for (; c + 16 <= nchunks; c += 16) {
+      int h[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) h[i] = hist[(long long)(c + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        hist[(long long)(c + i) * E + e] = total;
+        total += h[i];
+      }
+    }
+    for (; c < nchunks; ++c) {
       const int h = hist[(long long)c * E + e];
-      hist[(long long)c * E + e] = total;  // exclusive base of chunk c inside expert e
+      hist[(long long)c * E + e] = total;
       total += h;
     }
     counts[e] = total;
