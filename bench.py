@@ -401,17 +401,30 @@ WORKLOADS = {
 }
 
 
+KERNEL_HEADERS = ("budget.hpp", "kernels.h", "ptx.cuh")
+
+
+def kernel_source_sha1(kernel_src: str) -> str:
+    """sha1 over a kernel's translation unit followed by the shared device
+    headers it includes (in KERNEL_HEADERS order): a change to either makes a
+    recorded profile stale."""
+    h = hashlib.sha1(open(os.path.join(ROOT, kernel_src), "rb").read())
+    csrc = os.path.dirname(os.path.join(ROOT, kernel_src))
+    for name in KERNEL_HEADERS:
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()
+
+
 def traffic_for(kernel_src: str, workload: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source and this workload
-    (else None)."""
+    summary, if it was taken on the current kernel source (and headers) and
+    this workload (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    src = os.path.join(ROOT, kernel_src)
-    h = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    h = kernel_source_sha1(kernel_src)
     for ent in d.get("entries", []):
         if ent.get("kernel_src") == kernel_src and ent.get("source_sha1") == h and ent.get("workload") == workload:
             return ent.get("dram_bytes_per_launch")

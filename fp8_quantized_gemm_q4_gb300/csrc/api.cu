@@ -295,12 +295,21 @@ static bool fp4_split_tails() {
   return !(e && atoi(e) == 0);
 }
 
+// Dense GEMMs on CTA pairs split a last wave that fills at most half the pairs
+// into 256 x 128 half tiles (BSGEMM_FP4_HALF_TAIL=0 keeps whole tiles).  Read
+// on every call.
+static bool fp4_half_tail() {
+  const char* e = getenv("BSGEMM_FP4_HALF_TAIL");
+  return !(e && atoi(e) == 0);
+}
+
 static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int sms, cudaStream_t s,
                             long long pair_tiles, bool grouped) {
   bs_status st;
   if (fp4_pair() && sms >= 2) {  // a pair needs two SMs
     const bool split = grouped && fp4_split_tails();
     L.p.part = split ? 1 : 0;
+    L.p.half_tail = (!grouped && fp4_half_tail()) ? 1 : 0;
     bsk::Fp4PairLaunch P;
     memset(&P, 0, sizeof P);
     st = fp4_maps(L, a, b_rows, fp4_bk());

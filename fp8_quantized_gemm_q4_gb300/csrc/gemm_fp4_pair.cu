@@ -91,6 +91,9 @@ struct PGeo {
 
 constexpr uint32_t kIdescMain = idesc_mxf4nvf4(2 * BM, BN);
 constexpr uint32_t kIdescLora = idesc_bf16(2 * BM, BN);
+// half tiles (256 x 128) of the dense tail, see dense_work()
+constexpr uint32_t kIdescMainHalf = idesc_mxf4nvf4(2 * BM, BN / 2);
+constexpr uint32_t kIdescLoraHalf = idesc_bf16(2 * BM, BN / 2);
 
 struct Tile {
   int row0;      // first A row of the pair (this CTA's rows start at row0 + rank * 128)
@@ -99,6 +102,7 @@ struct Tile {
   int brow1;     // first B row of accumulator columns [128, 256) (peer's half)
   int sfb_blk1;  // scale block of brow1 (valid even when brow1 is past the weights)
   int col0;      // first output column
+  int narrow;    // 1: a 256 x 128 half tile (MMA N = 128, accumulator columns [0, 128))
 };
 
 // Tile fields broadcast from lane 0 (warp-uniform for the issuing roles).
@@ -110,6 +114,7 @@ __device__ __forceinline__ Tile bcast_tile(const Tile& t) {
   r.brow1 = warp_bcast(t.brow1);
   r.sfb_blk1 = warp_bcast(t.sfb_blk1);
   r.col0 = warp_bcast(t.col0);
+  r.narrow = warp_bcast(t.narrow);
   return r;
 }
 
@@ -118,18 +123,53 @@ __device__ __forceinline__ int n_blocks(const Fp4Params& p) {
   return kEpi == kEpiSwiglu ? p.N / 128 : (p.N + BN - 1) / BN;
 }
 
+// Dense work list.  With T pair tiles on P pairs, the last T mod P tiles
+// would run as a partial wave while the other pairs idle (8192^3: 1024 tiles
+// on 76 pairs, 36 pairs doing 14 tiles and 40 doing 13).  When that tail
+// fits in half the pairs, each tail tile is split into two 256 x 128 halves
+// (MMA N = 128) so that the tail spreads over twice as many pairs.
+// Returns the number of work items; `full` receives the count of whole tiles.
+// Only the plain dense epilogue (kEpiStore) splits.
+template <int kEpi>
+__device__ __forceinline__ int dense_work(const Fp4Params& p, int npairs, int& full) {
+  const int tiles = ((p.M + 2 * BM - 1) / (2 * BM)) * ((p.N + BN - 1) / BN);
+  const int tail = tiles % npairs;
+  full = tiles;
+  if (kEpi != kEpiStore || !p.half_tail || tail == 0 || 2 * tail > npairs) return tiles;
+  full = tiles - tail;
+  return tiles + tail;
+}
+
 template <int kEpi>
 __device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, int t) {
   Tile tl = {};
   if (p.E == 0) {
+    int nfull;
+    dense_work<kEpi>(p, (int)(gridDim.x / 2), nfull);
+    int half = -1;
+    if (t >= nfull) {  // half tile: item nfull + 2 i + h is half h of tile nfull + i
+      half = (t - nfull) & 1;
+      t = nfull + (t - nfull) / 2;
+    }
     const int num_m = (p.M + 2 * BM - 1) / (2 * BM);
     const int mb = t % num_m, nb = t / num_m;
     tl.row0 = mb * 2 * BM;
     tl.rows = min(2 * BM, p.M - tl.row0);
-    tl.col0 = nb * BN;
-    tl.brow0 = nb * BN;
-    tl.brow1 = tl.brow0 + 128;
-    tl.sfb_blk1 = (tl.brow1 < p.N) ? tl.brow1 / 128 : tl.brow0 / 128;
+    if (half < 0) {
+      tl.col0 = nb * BN;
+      tl.brow0 = nb * BN;
+      tl.brow1 = tl.brow0 + 128;
+      tl.sfb_blk1 = (tl.brow1 < p.N) ? tl.brow1 / 128 : tl.brow0 / 128;
+    } else {
+      // each CTA supplies 64 of the 128 B rows at its B offset: the leader
+      // rows [brow0, brow0 + 64), the peer [brow0 + 64, brow0 + 128); the
+      // other 64 rows of each CTA's 128-row box are loaded but not used
+      tl.narrow = 1;
+      tl.col0 = nb * BN + 128 * half;
+      tl.brow0 = tl.col0;
+      tl.brow1 = tl.brow0 + 64;
+      tl.sfb_blk1 = tl.brow0 / 128;
+    }
     return tl;
   }
   // Grouped: tiles walk chunks of n_chunk column blocks; inside a chunk,
@@ -235,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 3) {
     if (p.E == 0) {
-      if (lane == 0) *total_tiles = ((p.M + 2 * BM - 1) / (2 * BM)) * ((p.N + BN - 1) / BN);
+      int nfull;
+      const int items = dense_work<kEpi>(p, npairs, nfull);
+      if (lane == 0) *total_tiles = items;
     } else if (kLora) {
       // the low-rank variant has no expert table: nothing to do (the host never asks for this)
       if (lane == 0) {
@@ -354,6 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dSfa = smem_desc(smem_u32(stages + kOffSfa), 0, 128, kLayoutNone);
     const uint64_t dSfb = smem_desc(smem_u32(stages + kOffSfb), 0, 128, kLayoutNone);
     for (int t = pair; t < total && ok; t += npairs) {
+      const bool narrow = (kEpi == kEpiStore && p.E == 0) && warp_bcast(tile_of<kEpi>(p, prefix, t).narrow) != 0;
+      const uint32_t idesc_main = narrow ? kIdescMainHalf : kIdescMain;
       if (!mbar_wait_warp(acc_empty, acc_phase ^ 1u, abort_flag, p.status, 130)) break;
       tc_fence_after();
       for (int ks = 0; ks < kstages; ++ks) {
@@ -376,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kMmas; ++j) {
             if (j < nmma) {
               const uint32_t col = sf_col + j * kSfColsPerMma;
-              mma_mxf4nvf4_pair(tmem + kTmemAcc, dA + so + 2 * j, dB + so + 2 * j, kIdescMain, col, col + 4,
+              mma_mxf4nvf4_pair(tmem + kTmemAcc, dA + so + 2 * j, dB + so + 2 * j, idesc_main, col, col + 4,
                                 (ks > 0 || j > 0) ? 1u : 0u);                    // 32 B of K per MMA
             }
           }
@@ -399,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk)
               mma_bf16_pair(tmem + kTmemAcc, smem_desc(ta + 32 * kk, 16, 512, kLayoutSw64),
-                            smem_desc(bl + 32 * kk, 16, 512, kLayoutSw64), kIdescLora, 1u);
+                            smem_desc(bl + 32 * kk, 16, 512, kLayoutSw64), narrow ? kIdescLoraHalf : kIdescLora, 1u);
           }
           tc_commit_pair_multicast(lora_empty, 0x3);
         }
@@ -546,8 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if (p.E == 0) {
           // dense: boxes of 32 rows x 32 bytes through the warp's staging buffer
+          // (a half tile has only accumulator columns [0, 128))
           const int row_box = tl.row0 + (int)rank * BM + q * 32;
-          if (row_box < p.M && col < p.N) {
+          if (row_box < p.M && col < p.N && !(tl.narrow && half)) {
             if (p.out_bf16) {
 #pragma unroll
               for (int cc = 0; cc < 128 / (2 * kRowW); ++cc) {  // 2 kRowW columns per box

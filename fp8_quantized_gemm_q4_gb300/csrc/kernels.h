@@ -30,6 +30,7 @@ struct Fp4Params {
   int* status;
   int n_chunk;            // grouped tile order: column blocks per chunk (0 = all)
   int part;               // grouped rows covered: 0 all, 1 experts > 128 rows, 2 the others (expert_part)
+  int half_tail;          // dense, CTA pairs: split a short last wave into 256 x 128 half tiles
 };
 
 // Rows of expert e that one grouped launch covers.  part 0: all of them.  A

@@ -112,6 +112,20 @@ def test_full_size_lowrank_sampled_rows(cuda_lib, fp4_variant):
     assert ok and tok, (ratio, rel, tratio)
 
 
+@pytest.mark.parametrize("half_tail", ["1", "0"])
+def test_short_last_wave_half_tiles(cuda_lib, monkeypatch, half_tail):
+    """80 pair tiles (2560 x 2048) on at most 76 pairs: the last 4 tiles run as
+    eight 256 x 128 half tiles on CTA pairs (BSGEMM_FP4_HALF_TAIL=0: whole tiles)."""
+    monkeypatch.setenv("BSGEMM_FP4_HALF_TAIL", half_tail)
+    d = workloads.dense_lowrank(M=2560, N=2048, K=256)
+    for kw in ({}, {"lora": (d["lora_a"], d["lora_b"]), "bias": d["bias"]}):
+        for dt in (torch.bfloat16, torch.float32):
+            if kw and dt == torch.float32:
+                continue
+            ok, ratio, rel, tok, tratio = run_case(cuda_lib, d["x"], d["w"], dt, **kw)
+            assert ok and tok, (dt, bool(kw), ratio, rel, tratio)
+
+
 def test_empty_m_is_noop(cuda_lib):
     bs = cuda_lib
     a = torch.empty((0, 32), dtype=torch.uint8, device="cuda")
