@@ -271,10 +271,13 @@ static bs_status fp4_maps(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_ro
 
 // Scale tensors as uint32 rows: one row per 128-row block, K/64 tiles of 512
 // bytes each; a pair-kernel stage loads two tiles (256 words).
-static bs_status sf_map(CUtensorMap* m, const void* sf, int64_t rows, int64_t K) {
-  const uint64_t words = (uint64_t)(K / 64) * 128;
+// Scales of the FP4 pair kernel as 8-byte elements, one row per 128-row
+// block (K/64 chunks of 512 bytes = K elements); a box is one K stage of `bk`
+// elements (bk/64 chunks).
+static bs_status sf_map(CUtensorMap* m, const void* sf, int64_t rows, int64_t K, int bk) {
+  const uint64_t elems = (uint64_t)K;
   const uint64_t blocks = (uint64_t)((rows + 127) / 128);
-  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, sf, words, blocks, words * 4, 256, 1,
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, sf, elems, blocks, elems * 8, (uint32_t)bk, 1,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -314,9 +317,9 @@ static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_
     memset(&P, 0, sizeof P);
     st = fp4_maps(L, a, b_rows, fp4_bk());
     if (st != BS_OK) return st;
-    st = sf_map(&P.tmSfa, a->sfa, a->M, a->K);
+    st = sf_map(&P.tmSfa, a->sfa, a->M, a->K, fp4_bk());
     if (st != BS_OK) return st;
-    st = sf_map(&P.tmSfb, a->sfb, b_rows, a->K);
+    st = sf_map(&P.tmSfb, a->sfb, b_rows, a->K, fp4_bk());
     if (st != BS_OK) return st;
     if (L.epilogue == bsk::kEpiSwiglu || L.epilogue == bsk::kEpiRows ||
         (L.epilogue == bsk::kEpiStore && !grouped)) {

@@ -73,7 +73,7 @@ struct PGeo {
   static constexpr int kStageBytes = kOffSfb + 2 * kMmas * 512;
   static constexpr int kStageTx = kStageBytes;  // bytes one CTA's loads deliver per stage
   static constexpr int kSfWords = kMmas * 128;  // scale words of one 128-row block per stage
-  static constexpr int kSfBoxes = kSfWords / 256;  // TMA boxes of 256 words
+  static constexpr int kSfBox = kSfWords / 2;     // one TMA box per stage: BK 8-byte elements
   // the low-rank branch is dense-only, so its variant carries no expert table
   static constexpr Fp4TileShape kShapeLora{BM, BN, BK, 2, true, 32, kMiscBase + kEpiStageLora};
   static constexpr Fp4TileShape kShapeNoLora{BM, BN, BK, 2, false, 32, kMiscBase + kMiscTable + kEpiStageNoLora};
@@ -343,13 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bar = mapa_shared(smem_u32(&full[ps.index]), 0);
           tma_load_2d_pair(st + kOffA, &tmA, bar, ks * kRowBytes, my_row0);
           tma_load_2d_pair(st + kOffB, &tmB, bar, ks * kRowBytes, my_brow);
-#pragma unroll
-          for (int b = 0; b < G::kSfBoxes; ++b) {
-            const int x = ks * G::kSfWords + b * 256;
-            tma_load_2d_pair(st + kOffSfa + b * 1024, &tmSfa, bar, x, my_row0 / 128);
-            tma_load_2d_pair(st + kOffSfb + b * 1024, &tmSfb, bar, x, tl.brow0 / 128);
-            tma_load_2d_pair(st + kOffSfb + kMmas * 512 + b * 1024, &tmSfb, bar, x, tl.sfb_blk1);
-          }
+          // scales: each CTA loads its own rows' block of A scales, and one of
+          // the two B scale blocks that both CTAs' tensor cores need (the
+          // leader the first, the peer the second), multicast to the pair
+          const int x = ks * G::kSfBox;
+          tma_load_2d_pair(st + kOffSfa, &tmSfa, bar, x, my_row0 / 128);
+          if (leader)
+            tma_load_2d_pair_mc(st + kOffSfb, &tmSfb, bar, x, tl.brow0 / 128, 0x3);
+          else
+            tma_load_2d_pair_mc(st + kOffSfb + kMmas * 512, &tmSfb, bar, x, tl.sfb_blk1, 0x3);
         }
         __syncwarp();
         issued_mask |= 1u << ps.index;

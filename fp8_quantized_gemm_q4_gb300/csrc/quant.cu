@@ -571,32 +571,61 @@ namespace bsk {
 // scale layout to the destination row's.  Equal, bit for bit, to quantizing
 // the gathered bf16 rows (quantization is row-local), at a fraction of the
 // traffic when rows repeat (MoE: each token feeds k experts).
+// One CTA per 128-row block of the output.  Codes: each warp copies 16 rows,
+// a lane's 16-byte vectors of a row issued together.  Scales: the block's
+// 512-byte word groups (one per 64-element chunk) are written whole — lane l
+// of a chunk's warp stores the 16 bytes holding rows l, l + 32, l + 64 and
+// l + 96 — so every store is a full coalesced line, and the four source
+// words come from the (cache-resident) input scale rows.
+constexpr int kGatherVec = 8;  // 16-byte code vectors in flight per lane and pass
 __global__ void __launch_bounds__(256) fp4_gather_rows_kernel(const uint8_t* __restrict__ codes_in,
                                                               const uint8_t* __restrict__ sf_in, long long rows_in,
                                                               long long K, const int* __restrict__ gather,
                                                               long long rows_out, long long rows_out_pad,
                                                               uint8_t* __restrict__ codes_out,
                                                               uint8_t* __restrict__ sf_out) {
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long kv = K / 32;  // 16-byte vectors per row of codes
   const long long kc = K / 64;  // scale words per row
-  for (long long row = (long long)blockIdx.x * 8 + threadIdx.x / 32; row < rows_out_pad;
-       row += (long long)gridDim.x * 8) {
-    long long src = -1;
-    if (row < rows_out) {
-      src = gather[row];
+  for (long long blk = blockIdx.x; blk * 128 < rows_out_pad; blk += gridDim.x) {
+    const long long r0 = blk * 128;
+    // codes: warp w copies rows r0 + 16 w .. + 16
+    for (int i = 0; i < 16; ++i) {
+      const long long row = r0 + warp * 16 + i;
+      if (row >= rows_out) break;
+      long long src = gather[row];
       if (src >= rows_in) src = -1;
+      const uint4* sp = reinterpret_cast<const uint4*>(codes_in + (src >= 0 ? src : 0) * (K / 2));
+      uint4* dp = reinterpret_cast<uint4*>(codes_out + row * (K / 2));
+      for (long long v0 = 0; v0 < kv; v0 += 32 * kGatherVec) {
+        uint4 buf[kGatherVec];
+#pragma unroll
+        for (int u = 0; u < kGatherVec; ++u) {
+          const long long v = v0 + u * 32 + lane;
+          buf[u] = (src >= 0 && v < kv) ? __ldg(sp + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kGatherVec; ++u) {
+          const long long v = v0 + u * 32 + lane;
+          if (v < kv) dp[v] = buf[u];
+        }
+      }
     }
-    if (row < rows_out) {
-      const uint4* s = reinterpret_cast<const uint4*>(codes_in + (src >= 0 ? src : 0) * (K / 2));
-      uint4* d = reinterpret_cast<uint4*>(codes_out + row * (K / 2));
-      for (long long v = lane; v < kv; v += 32) d[v] = src >= 0 ? __ldg(s + v) : make_uint4(0, 0, 0, 0);
+    // scales: lane l serves rows r0 + l + 32 q (q = 0..3) of every chunk
+    long long soff[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const long long row = r0 + lane + 32 * q;
+      long long src = row < rows_out ? (long long)gather[row] : -1;
+      if (src >= rows_in) src = -1;
+      soff[q] = src < 0 ? -1 : (src / 128) * kc * 512 + (src % 32) * 16 + ((src % 128) / 32) * 4;
     }
-    const long long doff = (row / 128) * kc * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4;
-    const long long soff = (src / 128) * kc * 512 + (src % 32) * 16 + ((src % 128) / 32) * 4;
-    for (long long c = lane; c < kc; c += 32) {
-      const uint32_t w = src >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(sf_in + soff + c * 512)) : 0u;
-      *reinterpret_cast<uint32_t*>(sf_out + doff + c * 512) = w;
+    for (long long c = warp; c < kc; c += 8) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w[q] = soff[q] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(sf_in + soff[q] + c * 512)) : 0u;
+      *reinterpret_cast<uint4*>(sf_out + (blk * kc + c) * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
@@ -605,8 +634,8 @@ cudaError_t launch_fp4_gather_rows(const uint8_t* codes_in, const uint8_t* sf_in
                                    const int* gather, long long rows_out, uint8_t* codes_out, uint8_t* sf_out,
                                    cudaStream_t stream) {
   const long long pad = (rows_out + 127) / 128 * 128;
-  long long blocks = (pad + 7) / 8;
-  const long long cap = (long long)sm_count() * 16;
+  long long blocks = pad / 128;
+  const long long cap = (long long)sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   fp4_gather_rows_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes_in, sf_in, rows_in, K, gather, rows_out, pad,

@@ -170,10 +170,11 @@ def test_q4_quantize_full_size_activation(cuda_lib):
     assert np.array_equal(sf_rowmajor(sf.cpu().numpy(), 8192, 8192)[rows], os_)
 
 
-@pytest.mark.parametrize("M,K", [(200, 1024), (130, 320), (64, 8192)])
+@pytest.mark.parametrize("M,K", [(200, 1024), (130, 320), (64, 8192), (1000, 512), (20000, 256)])
 def test_q4_lowrank_left_factor(cuda_lib, M, K):
     """Codes, scales and T = X A from one call (fused pass when K % 256 == 0,
-    separate kernels otherwise)."""
+    separate kernels otherwise), including row counts that leave the last
+    32-row CTA of the fused pass partly empty."""
     bs = cuda_lib
     d = workloads.dense_lowrank(M=M, N=256, K=K)
     x, a = d["x"], d["lora_a"]
