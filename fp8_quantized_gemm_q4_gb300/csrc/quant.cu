@@ -589,12 +589,17 @@ __global__ void __launch_bounds__(256) fp4_gather_rows_kernel(const uint8_t* __r
   const long long kc = K / 64;  // scale words per row
   for (long long blk = blockIdx.x; blk * 128 < rows_out_pad; blk += gridDim.x) {
     const long long r0 = blk * 128;
-    // codes: warp w copies rows r0 + 16 w .. + 16
-    for (int i = 0; i < 16; ++i) {
+    // codes: warp w copies rows r0 + 16 w .. + 16 (their sources read up front)
+    long long my_src = -1;
+    if (lane < 16 && r0 + warp * 16 + lane < rows_out) {
+      my_src = gather[r0 + warp * 16 + lane];
+      if (my_src >= rows_in) my_src = -1;
+    }
+    const long long left = rows_out - (r0 + warp * 16);
+    const int nrows = left < 16 ? (left > 0 ? (int)left : 0) : 16;
+    for (int i = 0; i < nrows; ++i) {
       const long long row = r0 + warp * 16 + i;
-      if (row >= rows_out) break;
-      long long src = gather[row];
-      if (src >= rows_in) src = -1;
+      const long long src = __shfl_sync(0xffffffffu, my_src, i);
       const uint4* sp = reinterpret_cast<const uint4*>(codes_in + (src >= 0 ? src : 0) * (K / 2));
       uint4* dp = reinterpret_cast<uint4*>(codes_out + row * (K / 2));
       for (long long v0 = 0; v0 < kv; v0 += 32 * kGatherVec) {
