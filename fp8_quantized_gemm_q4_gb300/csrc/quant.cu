@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(256) fp4_gather_rows_kernel(const uint8_t* __r
 #pragma unroll
         for (int u = 0; u < kGatherVec; ++u) {
           const long long v = v0 + u * 32 + lane;
-          if (v < kv) dp[v] = buf[u];
+          if (v < kv) __stcs(dp + v, buf[u]);  // streaming: keep the source rows in L2
         }
       }
     }
@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(256) fp4_gather_rows_kernel(const uint8_t* __r
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         w[q] = soff[q] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(sf_in + soff[q] + c * 512)) : 0u;
-      *reinterpret_cast<uint4*>(sf_out + (blk * kc + c) * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      __stcs(reinterpret_cast<uint4*>(sf_out + (blk * kc + c) * 512 + lane * 16), make_uint4(w[0], w[1], w[2], w[3]));
     }
   }
 }
