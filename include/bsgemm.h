@@ -44,7 +44,7 @@ typedef enum {
     BS_OK = 0,
     BS_ERR_INVALID = 1,     /* null pointer, bad size or enum value */
     BS_ERR_ALIGN = 2,       /* pointer / leading dimension not 16-byte aligned, K or N not a multiple of the block */
-    BS_ERR_UNSUPPORTED = 3, /* valid request this build does not implement */
+    BS_ERR_UNSUPPORTED = 3, /* valid request this library does not implement */
     BS_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute, tensor-map encode) */
     BS_ERR_TIMEOUT = 5,     /* device status: a bounded pipeline wait gave up */
     BS_ERR_OFFSETS = 6      /* device status: expert offsets / counts inconsistent */

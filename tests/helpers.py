@@ -15,7 +15,7 @@ def sf_rowmajor(sf, rows, K):
 
 
 def gemm_errors(y, y_ref, S, bf16_out):
-    """Spec bound: |y - y_ref| <= 1e-3 * S + 2^-8 |y_ref| (last term bf16 only).
+    """GEMM tolerance: |y - y_ref| <= 1e-3 * S + 2^-8 |y_ref| (last term bf16 only).
     Returns (ok, max ratio err / bound, max err / S)."""
     y = np.asarray(y, dtype=np.float64)
     err = np.abs(y - y_ref)

@@ -1,6 +1,6 @@
 """Dense block-scaled FP4 GEMM on the GPU vs the FP64 oracle.
 
-Bound (the benchmark spec): |y - y_ref| <= 1e-3 * S + 2^-8 |y_ref| (bf16 output only),
+Tolerance: |y - y_ref| <= 1e-3 * S + 2^-8 |y_ref| (bf16 output only),
 S = sum_k |a_k b_k| (+ low-rank and bias magnitudes).  A tighter diagnostic
 bound (1e-4 S) is asserted too, so a dropped K group cannot hide in the slack.
 """
