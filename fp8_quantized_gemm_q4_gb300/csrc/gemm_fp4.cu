@@ -370,6 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t so = (uint64_t)((ps.index * G::kStageBytes) >> 4);
         const uint32_t sf_col = tmem + kTmemSf + sf_buf * G::kSfColsPerStage;
         if (elect_one()) {
+          // each MMA right behind the scale copies it reads (copies and MMAs
+          // run in issue order, so the stage's first MMA need not wait for
+          // every copy of the stage)
 #pragma unroll
           for (int j = 0; j < G::kMmas; ++j) {
             if (j < nmma) {
@@ -377,12 +380,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_cp_32x128b_warpx4(col, dSfa + so + 32 * j);                      // 512 B per block
               tc_cp_32x128b_warpx4(col + 4, dSfb + so + 32 * j);
               tc_cp_32x128b_warpx4(col + 8, dSfb + so + 32 * (G::kMmas + j));
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < G::kMmas; ++j) {
-            if (j < nmma) {
-              const uint32_t col = sf_col + j * kSfColsPerMma;
               mma_mxf4nvf4(tmem + kTmemAcc, dA + so + 2 * j, dB + so + 2 * j, kIdescMain, col, col + 4,
                            (ks > 0 || j > 0) ? 1u : 0u);                         // 32 B of K per MMA
             }

@@ -409,6 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t so = (uint64_t)((ps.index * kStageBytes) >> 4);
         const uint32_t sf_col = tmem + kTmemSf + sf_buf * kSfColsPerStage;
         if (elect_one()) {
+          // each MMA right behind the three scale copies it reads (copies
+          // and MMAs run in issue order): with all twelve copies of a stage
+          // first, every stage's first MMA waited for all of them
+          // (8192^3: 0.1826 -> 0.1764 ms with the low-rank branch)
 #pragma unroll
           for (int j = 0; j < kMmas; ++j) {
             if (j < nmma) {
@@ -416,12 +420,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_cp_32x128b_warpx4_pair(col, dSfa + so + 32 * j);               // 512 B per block
               tc_cp_32x128b_warpx4_pair(col + 4, dSfb + so + 32 * j);
               tc_cp_32x128b_warpx4_pair(col + 8, dSfb + so + 32 * (kMmas + j));
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < kMmas; ++j) {
-            if (j < nmma) {
-              const uint32_t col = sf_col + j * kSfColsPerMma;
               mma_mxf4nvf4_pair(tmem + kTmemAcc, dA + so + 2 * j, dB + so + 2 * j, idesc_main, col, col + 4,
                                 (ks > 0 || j > 0) ? 1u : 0u);                    // 32 B of K per MMA
             }
