@@ -404,14 +404,24 @@ WORKLOADS = {
 KERNEL_HEADERS = ("budget.hpp", "kernels.h", "ptx.cuh")
 
 
+def _code_only(path: str) -> bytes:
+    """Source text without comments or blank lines (comment edits do not
+    change the kernel a profile was taken on)."""
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip()).encode()
+
+
 def kernel_source_sha1(kernel_src: str) -> str:
-    """sha1 over a kernel's translation unit followed by the shared device
-    headers it includes (in KERNEL_HEADERS order): a change to either makes a
-    recorded profile stale."""
-    h = hashlib.sha1(open(os.path.join(ROOT, kernel_src), "rb").read())
+    """sha1 over the code of a kernel's translation unit followed by the shared
+    device headers it includes (in KERNEL_HEADERS order), comments removed: a
+    change to either makes a recorded profile stale."""
+    h = hashlib.sha1(_code_only(os.path.join(ROOT, kernel_src)))
     csrc = os.path.dirname(os.path.join(ROOT, kernel_src))
     for name in KERNEL_HEADERS:
-        h.update(open(os.path.join(csrc, name), "rb").read())
+        h.update(_code_only(os.path.join(csrc, name)))
     return h.hexdigest()
 
 

@@ -7,13 +7,15 @@
 // actually holds (section 6: the up-projection block of the low-rank branch
 // is split across the pair, not replicated).
 //
-// Per CTA of a pair (cluster of 2), per K stage of 128 FP4 elements:
+// Per CTA of a pair (cluster of 2), per K stage of 128 FP4 elements (the
+// default 256-element stage holds twice each):
 //   A      its own 128 rows                     8 KB  (64B swizzle)
 //   B      its own half (128 rows) of the 256   8 KB
 //   SFA    scales of its own rows               1 KB
-//   SFB    scales of all 256 B rows             2 KB  (replicated: each CTA's
-//          tensor core multiplies its rows by all 256 columns)
-// so a stage is 19 KB instead of 27 KB, and 10-11 stages fit.
+//   SFB    scales of all 256 B rows             2 KB  (held by both: each CTA's
+//          tensor core multiplies its rows by all 256 columns; each CTA
+//          loads one 128-row block and multicasts it to the pair)
+// so a 128-deep stage is 19 KB instead of 27 KB, and 10-11 stages fit.
 //
 // The leader CTA (rank 0) issues every tcgen05.mma / tcgen05.cp with
 // cta_group::2; the operands of the peer live at the same shared-memory
