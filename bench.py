@@ -269,9 +269,10 @@ class MoEWorkload:
     """Grouped FP4 MoE layer: dispatch, gather + quantize, gate/up GEMM + SwiGLU,
     re-quantize, down GEMM + routed combine, bf16 cast (one step = one layer)."""
 
-    def __init__(self, large, combine="rows", graph=True):
+    def __init__(self, large, combine="rows", graph=True, h_quant="fused"):
         import workloads
         self.combine = combine
+        self.h_quant = h_quant
         self.graph = graph  # the layer replayed as one CUDA graph
         cfg = workloads.MOE_LARGE if large else workloads.MOE_SMALL
         self.index = 4 if large else 3
@@ -316,20 +317,22 @@ class MoEWorkload:
             bs.q4_quantize(wd, out=(wd_codes[e * H:(e + 1) * H], wd_sf[e * pd:(e + 1) * pd], None))
         from fp8_quantized_gemm_q4_gb300.moe import MoEWeights
         W = MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf)
-        self.layer = MoELayer(W, self.T, self.k, device=dev, combine=self.combine)
+        self.layer = MoELayer(W, self.T, self.k, device=dev, combine=self.combine, h_quant=self.h_quant)
         self.out = self.layer.out
         if self.graph:
             # capture once; from here on the workload's inputs are the graph's static ones
             self.layer.capture(self.x, self.ids, self.w)
             self.x, self.ids, self.w = self.layer.static_x, self.layer.static_ids, self.layer.static_w
-        # dispatch 3 + quantize 1 + gather 1 + gate/up GEMM + quantize 1 + down GEMM,
-        # then combine 3 (invert, init, sum) or finalize 2 (cast, zero); each
-        # grouped GEMM is two launches on CTA pairs with the small experts
-        # split off (the library's default), one otherwise
+        # dispatch 3 + quantize 1 + gather 1 + gate/up GEMM (+ quantize h 1 on the
+        # separate path) + down GEMM, then combine 3 (invert, init, sum) or
+        # finalize 2 (cast, zero); each grouped GEMM is two launches on CTA
+        # pairs with the small experts split off (the library's default), one
+        # otherwise
         pair = os.environ.get("BSGEMM_FP4_PAIR", "1") != "0"
         tails = os.environ.get("BSGEMM_FP4_TAILS", "1") != "0"
         g = 2 if (pair and tails) else 1
-        self.launches_per_step = 5 + 2 * g + (3 if self.combine == "rows" else 2)
+        self.launches_per_step = (5 if self.layer.h_quant == "fused" else 6) + 2 * g + \
+            (3 if self.combine == "rows" else 2)
         self.bytes_in = self.x.numel() * 2 + self.ids.numel() * 4 + self.w.numel() * 4
         self.bytes_out = self.out.numel() * 2
         counts = torch.bincount(self.ids.flatten().long(), minlength=E).cpu()
@@ -536,7 +539,8 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
                    "parallelism": f"replicas x{world}",
-                   **({"moe_combine": wl.combine, "cuda_graph": wl.graph} if hasattr(wl, "combine") else {})},
+                   **({"moe_combine": wl.combine, "cuda_graph": wl.graph, "h_quant": wl.layer.h_quant}
+                      if hasattr(wl, "combine") else {})},
         "e2e": {"value": round(job_throughput(wl.flops, world, e2e_ms) / 1e12, 2), "unit": wl.unit,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": wl.bytes_in,
                 "d2h_bytes_per_step": wl.bytes_out},
@@ -610,6 +614,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (default min(steps, 100))")
     ap.add_argument("--moe-combine", choices=["rows", "atomic"], default="rows",
                     help="MoE routed combine: weighted rows + per-token sum, or fp32 reductions")
+    ap.add_argument("--moe-h-quant", choices=["fused", "separate"], default="fused",
+                    help="MoE: quantize h in the gate/up epilogue (default) or in a separate pass")
     ap.add_argument("--moe-eager", action="store_true",
                     help="MoE: launch the layer's kernels one by one instead of replaying its CUDA graph")
     args = ap.parse_args()
@@ -621,6 +627,7 @@ def main():
     if isinstance(wl, MoEWorkload):
         wl.combine = args.moe_combine
         wl.graph = not args.moe_eager
+        wl.h_quant = args.moe_h_quant
 
     if args.impl == "reference":
         if rank == 0:

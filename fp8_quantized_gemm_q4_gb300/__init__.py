@@ -79,6 +79,8 @@ def load(path: str | None = None):
         lib.bs_grouped_gemm.restype = I
         lib.bs_grouped_gemm.argtypes = [ctypes.POINTER(GemmArgs), I, P, P, I, P, P, P, I64, P]
         lib.bs_moe_rows_bound.restype = I64
+        lib.bs_grouped_gemm_swiglu_q4.restype = I
+        lib.bs_grouped_gemm_swiglu_q4.argtypes = [ctypes.POINTER(GemmArgs), I, P, P, P, P, P]
         lib.bs_moe_rows_bound.argtypes = [I64, I, I]
         lib.bs_moe_dispatch_workspace_bytes.restype = SZ
         lib.bs_moe_dispatch_workspace_bytes.argtypes = [I64, I, I]
@@ -235,6 +237,23 @@ def grouped_gemm_fp4(a, sfa, b, sfb, K: int, N: int, E: int, offsets, counts, ep
     _check(load().bs_grouped_gemm(ctypes.byref(g), E, _ptr(offsets), _ptr(counts), epilogue, _ptr(token_of),
                                   _ptr(weight_of), _ptr(out32), ld32, _stream(stream)))
     return out
+
+
+def grouped_gemm_fp4_swiglu_q4(a, sfa, b, sfb, K: int, N: int, E: int, offsets, counts, h_codes=None, h_sf=None,
+                               num_sms: int = 0, n_chunk_blocks: int = 0, stream=None):
+    """Grouped gate/up GEMM with h = bf16(silu(g) * u) quantized to FP4 in the
+    epilogue: returns (h_codes uint8 [M, N/2], h_sf scale bytes), as
+    q4_quantize would write them for the segment rows."""
+    M = a.shape[0]
+    if h_codes is None:
+        h_codes = torch.empty((M, N // 2), dtype=torch.uint8, device=a.device)
+    if h_sf is None:
+        h_sf = torch.empty(sf_bytes(M, N), dtype=torch.uint8, device=a.device)
+    g = _args(FMT_FP4, a, sfa, b, sfb, M, N, K, None, num_sms=num_sms)
+    g.n_chunk_blocks = n_chunk_blocks
+    _check(load().bs_grouped_gemm_swiglu_q4(ctypes.byref(g), E, _ptr(offsets), _ptr(counts), _ptr(h_codes),
+                                            _ptr(h_sf), _stream(stream)))
+    return h_codes, h_sf
 
 
 def moe_rows_bound(T: int, k: int, E: int) -> int:

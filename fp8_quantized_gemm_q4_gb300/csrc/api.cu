@@ -493,6 +493,49 @@ bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, 
   return launch_fp4(L, a, wrows, sms, reinterpret_cast<cudaStream_t>(stream), 0, true);
 }
 
+bs_status bs_grouped_gemm_swiglu_q4(const bs_gemm_args* a, int E, const int32_t* offsets, const int32_t* counts,
+                                    uint8_t* h_codes, uint8_t* h_sf, bs_stream_t stream) {
+  if (!a) return fail(BS_ERR_INVALID, "null args");
+  if (a->out) return fail(BS_ERR_INVALID, "SWIGLU_Q4 writes h_codes / h_sf: args->out must be NULL");
+  bs_status st = check_common(a, true);
+  if (st != BS_OK) return st;
+  if (a->fmt != BS_FMT_FP4) return fail(BS_ERR_UNSUPPORTED, "grouped GEMM is FP4 only");
+  if (a->K % 64) return fail(BS_ERR_ALIGN, "FP4: K=%lld not a multiple of 64", (long long)a->K);
+  if (E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "E=%d outside [1, 1024]", E);
+  if (!offsets || !counts) return fail(BS_ERR_INVALID, "null offsets/counts");
+  if (a->lora_t || a->col_scale || a->bias || a->alpha != 1.0f)
+    return fail(BS_ERR_UNSUPPORTED, "grouped GEMM takes no alpha/col_scale/bias/low-rank");
+  const int64_t wrows = 2 * a->N * (int64_t)E;
+  if (wrows > (1LL << 30)) return fail(BS_ERR_INVALID, "stacked weights too large");
+  int* status = nullptr;
+  int sms = 0;
+  if (!device_info(&status, &sms)) return fail(BS_ERR_CUDA, "no current device");
+  if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
+  if (a->M == 0) return BS_OK;
+  if (!h_codes || !h_sf) return fail(BS_ERR_INVALID, "null h_codes / h_sf");
+  if (!aligned16(h_codes) || !aligned16(h_sf)) return fail(BS_ERR_ALIGN, "h_codes / h_sf must be 16-byte aligned");
+  bsk::Fp4Launch L;
+  memset(&L, 0, sizeof L);
+  L.p.sfa = static_cast<const uint8_t*>(a->sfa);
+  L.p.sfb = static_cast<const uint8_t*>(a->sfb);
+  L.p.M = (int)a->M;
+  L.p.N = (int)a->N;
+  L.p.K = (int)a->K;
+  L.p.alpha = 1.0f;
+  L.p.out = h_codes;
+  L.p.ldo = a->N / 2;
+  L.p.out_sf = h_sf;
+  L.p.E = E;
+  L.p.offsets = offsets;
+  L.p.counts = counts;
+  L.p.status = status;
+  L.p.n_chunk = a->n_chunk_blocks > 0 ? a->n_chunk_blocks : 0;
+  L.lora = false;
+  L.epilogue = bsk::kEpiSwigluQ4;
+  L.grid = sms;
+  return launch_fp4(L, a, wrows, sms, reinterpret_cast<cudaStream_t>(stream), 0, true);
+}
+
 int64_t bs_moe_rows_bound(int64_t T, int k, int E) {
   if (T < 0 || k <= 0 || E <= 0) return 0;
   return T * k + (int64_t)E * 127;

@@ -122,7 +122,7 @@ __device__ __forceinline__ Tile bcast_tile(const Tile& t) {
 
 template <int kEpi>
 __device__ __forceinline__ int n_blocks(const Fp4Params& p) {
-  return kEpi == kEpiSwiglu ? p.N / 128 : (p.N + BN - 1) / BN;
+  return epi_is_swiglu(kEpi) ? p.N / 128 : (p.N + BN - 1) / BN;
 }
 
 // Dense work list.  With T pair tiles on P pairs, the last T mod P tiles
@@ -196,8 +196,8 @@ __device__ __forceinline__ Tile tile_of(const Fp4Params& p, const int* prefix, i
   const int nb = c * nck + local / mblk, mb = local % mblk;
   tl.row0 = eoff + mb * 2 * BM;
   tl.rows = min(2 * BM, cnt - mb * 2 * BM);
-  const int64_t wrows = (kEpi == kEpiSwiglu) ? 2LL * p.N : (int64_t)p.N;
-  if (kEpi == kEpiSwiglu) {
+  const int64_t wrows = epi_is_swiglu(kEpi) ? 2LL * p.N : (int64_t)p.N;
+  if (epi_is_swiglu(kEpi)) {
     tl.col0 = nb * 128;
     tl.brow0 = (int)(e * wrows + nb * 128);
     tl.brow1 = (int)(e * wrows + p.N + nb * 128);
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t v[4][32];
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      if (kEpi == kEpiSwiglu) {
+      if (epi_is_swiglu(kEpi)) {
         tmem_ld32(lane_base + kTmemAcc + 64 * half, v[0]);
         tmem_ld32(lane_base + kTmemAcc + 64 * half + 32, v[1]);
         tmem_ld32(lane_base + kTmemAcc + 128 + 64 * half, v[2]);
@@ -542,6 +542,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             stage_and_store(w, col + cc * 2 * kRowW, row_box);
           }
+        }
+      } else if (kEpi == kEpiSwigluQ4) {
+        // h = bf16(silu(g) * u) quantized in place, as q4_quantize would do
+        // it: this warp's 64 columns are one 64-element chunk of h, four
+        // groups of 16 per lane (its row).  Codes: 32 bytes per row; scales:
+        // one 32-bit word (group g in byte g) at the row's place in the MMA
+        // scale layout.  Rows follow the SWIGLU rule (padding rows of the
+        // segment get zero codes and scales; rows past its 128-aligned end
+        // belong to the next expert).
+        const int col = tl.col0 + 64 * half;
+        if (r_in_tile < ((tl.rows + 127) / 128) * 128 && row < p.M) {
+          uint32_t cw[8];
+          uint32_t sfw = 0;
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) {
+            float hx[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int c = 16 * g4 + i;
+              const float g = __uint_as_float(v[c / 32][c % 32]);
+              const float u = __uint_as_float(v[2 + c / 32][c % 32]);
+              hx[i] = row_ok ? __bfloat162float(__float2bfloat16_rn((g / (1.0f + __expf(-g))) * u)) : 0.0f;
+            }
+            uint32_t w2[2];
+            sfw |= q4_group16_bf16(hx, w2) << (8 * g4);
+            cw[2 * g4] = w2[0];
+            cw[2 * g4 + 1] = w2[1];
+          }
+          uint4* dc = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out) + row * (int64_t)(p.N / 2) + col / 2);
+          dc[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          dc[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+          const int64_t so = ((row / 128) * (int64_t)(p.N / 64) + col / 64) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4;
+          *reinterpret_cast<uint32_t*>(p.out_sf + so) = sfw;
         }
       } else if (kEpi == kEpiCombine) {
         const int col = tl.col0 + 128 * half;
@@ -682,6 +715,7 @@ static cudaError_t launch_bk(const Fp4PairLaunch& L, cudaStream_t stream) {
   switch (L.base.epilogue) {
     case kEpiStore: return launch_one<BK, false, kEpiStore>(L, stream);
     case kEpiSwiglu: return launch_one<BK, false, kEpiSwiglu>(L, stream);
+    case kEpiSwigluQ4: return launch_one<BK, false, kEpiSwigluQ4>(L, stream);
     case kEpiCombine: return launch_one<BK, false, kEpiCombine>(L, stream);
     case kEpiRows: return launch_one<BK, false, kEpiRows>(L, stream);
   }

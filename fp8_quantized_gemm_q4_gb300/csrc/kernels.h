@@ -7,7 +7,10 @@
 
 namespace bsk {
 
-enum { kEpiStore = 0, kEpiSwiglu = 1, kEpiCombine = 2, kEpiRows = 3 };
+enum { kEpiStore = 0, kEpiSwiglu = 1, kEpiCombine = 2, kEpiRows = 3, kEpiSwigluQ4 = 4 };
+// SWIGLU and SWIGLU_Q4 share the tile map (gate / up column blocks); Q4 then
+// quantizes h in the epilogue instead of storing it.
+constexpr bool epi_is_swiglu(int e) { return e == kEpiSwiglu || e == kEpiSwigluQ4; }
 
 struct Fp4Params {
   const uint8_t* sfa;
@@ -31,6 +34,7 @@ struct Fp4Params {
   int n_chunk;            // grouped tile order: column blocks per chunk (0 = all)
   int part;               // grouped rows covered: 0 all, 1 experts > 128 rows, 2 the others (expert_part)
   int half_tail;          // dense, CTA pairs: split a short last wave into 256 x 128 half tiles
+  uint8_t* out_sf;        // SWIGLU_Q4: scales of h (MMA layout for [M, N]); out holds its codes [M, N/2]
 };
 
 // Rows of expert e that one grouped launch covers.  part 0: all of them.  A

@@ -436,6 +436,42 @@ __device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float (&v)[8]) {
   return r;
 }
 
+// Correctly rounded x / s for the FP4 quantizers, where s is shared by a
+// whole group: with r = RN(1/s) (__frcp_rn), q0 = RN(x r) is within one ulp
+// of x / s, the remainder x - q0 s is exact in one FMA, and
+// RN(q0 + r (x - q0 s)) is RN(x / s) (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990).  copysign keeps the sign of a zero quotient.  Three FP operations per
+// element instead of a full IEEE divide; tests/test_quant_gpu.py checks the
+// codes against the oracle for every bf16 value under every reachable e4m3
+// scale.
+__device__ __forceinline__ float quot_rn(float x, float s, float r) {
+  const float q0 = x * r;
+  const float rem = fmaf(-q0, s, x);
+  return copysignf(fmaf(rem, r, q0), x);
+}
+
+// FP4 quantization of one 16-element group of bf16 values (passed as exact
+// floats), as q4_quantize does it: scale code e4m3(RN(amax / 6)), codes
+// E2M1 RNE of x / scale (all +0 when the scale is 0), element i in nibble
+// i % 8 of w[i / 8].  Returns the scale code.
+__device__ __forceinline__ uint32_t q4_group16_bf16(const float (&x)[16], uint32_t (&w)[2]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const uint32_t sc = f32_to_e4m3(quot_rn(amax, 6.0f, __frcp_rn(6.0f)));
+  const float s = e4m3_to_f32(sc);
+  const float rs = __frcp_rn(s);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = quot_rn(x[8 * h + i], s, rs);
+    w[h] = (s == 0.0f) ? 0u : f32x8_to_e2m1x8(q);
+  }
+  return sc;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

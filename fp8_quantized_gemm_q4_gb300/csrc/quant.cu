@@ -20,19 +20,8 @@
 
 namespace bsk {
 
-// Correctly rounded x / s for the quantizers, where s is shared by a whole
-// group: with r = RN(1/s) (__frcp_rn), q0 = RN(x r) is within one ulp of x / s,
-// the remainder x - q0 s is exact in one FMA, and RN(q0 + r (x - q0 s)) is
-// RN(x / s) (P. Markstein, "Computation of elementary functions on the IBM
-// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  copysign keeps
-// the sign of a zero quotient.  Three FP operations per element instead of a
-// full IEEE divide; tests/test_quant_gpu.py checks the codes against the
-// oracle for every bf16 value under every reachable e4m3 scale.
-__device__ __forceinline__ float quot_rn(float x, float s, float r) {
-  const float q0 = x * r;
-  const float rem = fmaf(-q0, s, x);
-  return copysignf(fmaf(rem, r, q0), x);
-}
+// quot_rn (correctly rounded group quotient) lives in ptx.cuh, shared with
+// the GEMM epilogue that quantizes h.
 
 __device__ __forceinline__ void load8(const void* x, int x_bf16, long long off, float (&v)[8]) {
   if (x_bf16) {

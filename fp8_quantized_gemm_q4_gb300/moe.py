@@ -8,9 +8,13 @@ teardown (FP8 GEMM)", section 5.3):
   2. q4_quantize         quantize each token's row once (online), then
      bs_fp4_gather_rows  gather the quantized rows into the expert segments
                          (bit-identical to quantizing the gathered rows)
-  3. bs_grouped_gemm     gate/up GEMM per expert with the SwiGLU epilogue
-                         h = bf16(silu(x W_gate^T) * (x W_up^T))
-  4. q4_quantize         re-quantize h online
+  3. bs_grouped_gemm_swiglu_q4
+                         gate/up GEMM per expert whose epilogue forms
+                         h = bf16(silu(x W_gate^T) * (x W_up^T)) and
+  4.                     re-quantizes it to FP4 in place ("DeepGEMM for
+                         Hopper MoE", section 3: h never goes through memory
+                         as bf16); h_quant="separate" runs the SWIGLU
+                         epilogue (bf16 h) and q4_quantize instead
   5. bs_grouped_gemm     down GEMM per expert; the routed combine ("Blackwell
                          FP4 MoE TFLOPS optimisation", section 3.2, result
                          aggregation) runs one of two ways:
@@ -31,8 +35,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import (EPI_COMBINE, EPI_ROWS, EPI_SWIGLU, fp4_gather_rows, grouped_gemm_fp4, moe_combine, moe_dispatch,
-               moe_finalize, moe_rows_bound, q4_quantize, sf_bytes)
+from . import (EPI_COMBINE, EPI_ROWS, EPI_SWIGLU, fp4_gather_rows, grouped_gemm_fp4, grouped_gemm_fp4_swiglu_q4,
+               moe_combine, moe_dispatch, moe_finalize, moe_rows_bound, q4_quantize, sf_bytes)
 
 
 @dataclass
@@ -70,19 +74,24 @@ class MoELayer:
     """Holds the per-call buffers of one layer shape so repeated calls (and a
     CUDA-graph capture) allocate nothing."""
 
-    def __init__(self, weights: MoEWeights, T: int, k: int, device="cuda", combine: str = "rows"):
+    def __init__(self, weights: MoEWeights, T: int, k: int, device="cuda", combine: str = "rows",
+                 h_quant: str = "fused"):
         if combine not in ("rows", "atomic"):
             raise ValueError(f"combine must be 'rows' or 'atomic', not {combine!r}")
+        if h_quant not in ("fused", "separate"):
+            raise ValueError(f"h_quant must be 'fused' or 'separate', not {h_quant!r}")
         self.w = weights
         self.T, self.k = T, k
         self.combine = combine
+        self.h_quant = h_quant
         E, H, F = weights.E, weights.H, weights.F
         self.rows = moe_rows_bound(T, k, E)
         self.tq = torch.empty((T, H // 2), dtype=torch.uint8, device=device)
         self.ts = torch.empty(sf_bytes(T, H), dtype=torch.uint8, device=device)
         self.xq = torch.empty((self.rows, H // 2), dtype=torch.uint8, device=device)
         self.xs = torch.empty(sf_bytes(self.rows, H), dtype=torch.uint8, device=device)
-        self.h = torch.zeros((self.rows, F), dtype=torch.bfloat16, device=device)
+        # bf16 h only on the separate path
+        self.h = torch.zeros((self.rows, F), dtype=torch.bfloat16, device=device) if h_quant == "separate" else None
         self.hq = torch.empty((self.rows, F // 2), dtype=torch.uint8, device=device)
         self.hs = torch.empty(sf_bytes(self.rows, F), dtype=torch.uint8, device=device)
         if combine == "rows":
@@ -106,9 +115,13 @@ class MoELayer:
         d = self.disp
         q4_quantize(x, out=(self.tq, self.ts, None))
         fp4_gather_rows(self.tq, self.ts, w.H, d["token_of"], out=(self.xq, self.xs))
-        grouped_gemm_fp4(self.xq, self.xs, w.wgu_codes, w.wgu_sf, K=w.H, N=w.F, E=w.E, offsets=d["offsets"],
-                         counts=d["counts"], epilogue=EPI_SWIGLU, out=self.h)
-        q4_quantize(self.h, out=(self.hq, self.hs, None))
+        if self.h_quant == "fused":
+            grouped_gemm_fp4_swiglu_q4(self.xq, self.xs, w.wgu_codes, w.wgu_sf, K=w.H, N=w.F, E=w.E,
+                                       offsets=d["offsets"], counts=d["counts"], h_codes=self.hq, h_sf=self.hs)
+        else:
+            grouped_gemm_fp4(self.xq, self.xs, w.wgu_codes, w.wgu_sf, K=w.H, N=w.F, E=w.E, offsets=d["offsets"],
+                             counts=d["counts"], epilogue=EPI_SWIGLU, out=self.h)
+            q4_quantize(self.h, out=(self.hq, self.hs, None))
         if self.combine == "rows":
             grouped_gemm_fp4(self.hq, self.hs, w.wd_codes, w.wd_sf, K=w.F, N=w.H, E=w.E, offsets=d["offsets"],
                              counts=d["counts"], epilogue=EPI_ROWS, out=self.yrows, weight_of=d["weight_of"])

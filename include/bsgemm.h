@@ -235,6 +235,24 @@ bs_status bs_grouped_gemm(const bs_gemm_args *args, int E, const int32_t *offset
                           bs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * bs_grouped_gemm_swiglu_q4 -- the SWIGLU grouped GEMM with h re-quantized in
+ * its epilogue, so h never goes through memory as bf16 (the "Mega MoE"
+ * fusion of "DeepGEMM for Hopper MoE", section 3; FP4 format of the
+ * "Warp-specialised W4A4 kernel", section 2).  Same operands and offsets
+ * contract as bs_grouped_gemm with BS_EPI_SWIGLU, but args->out must be NULL:
+ *   h_codes   uint8 [M, N/2]: the E2M1 codes q4_quantize would write for
+ *             h = bf16(silu(g) * u), 16-byte aligned
+ *   h_sf      bs_sf_bytes(M, N) bytes: their e4m3 group scales (MMA layout)
+ * Rows of each expert's 128-aligned segment are written (padding rows as
+ * zero codes and zero scales, like the zero rows of BS_EPI_SWIGLU); rows
+ * outside every segment are left untouched.  Bit-identical to BS_EPI_SWIGLU
+ * followed by q4_quantize of the segment rows.
+ * ------------------------------------------------------------------------- */
+bs_status bs_grouped_gemm_swiglu_q4(const bs_gemm_args *args, int E, const int32_t *offsets,
+                                    const int32_t *counts, uint8_t *h_codes, uint8_t *h_sf,
+                                    bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * bs_moe_dispatch -- group the T*k (token, slot) pairs of a top-k routing by
  * expert ("DeepGEMM teardown", section 5.3: each expert's rows contiguous and
  * movable in whole blocks).  Rows of expert e, in increasing pair index

@@ -78,12 +78,14 @@ def _small_moe(T=200, H=256, F=128, E=5, k=2, seed=3):
 def test_grouped_layer_staged(cuda_lib, fp4_kernel, combine, T, H, F, E, k, chunk):
     """combine="rows": weighted fp32 rows, then a slot-order sum per token;
     "atomic": fp32 reductions into out32.  chunk > 0 (atomic): the down GEMM
-    walks column chunks of that many 256-wide blocks."""
+    walks column chunks of that many 256-wide blocks.  The stages run on the
+    separate-h path (bf16 h visible); the default path, h quantized in the
+    gate/up epilogue, must then give the same codes, scales and output."""
     bs = cuda_lib
     from fp8_quantized_gemm_q4_gb300.moe import MoELayer, quantize_expert_weights
     r, x, ws = _small_moe(T, H, F, E, k)
     W = quantize_expert_weights([a for a, _ in ws], [b for _, b in ws])
-    layer = MoELayer(W, T, k, combine=combine)
+    layer = MoELayer(W, T, k, combine=combine, h_quant="separate")
     if chunk:
         layer.combine_chunk = chunk
     out = layer.forward(x.cuda(), torch.from_numpy(r["topk_ids"]).cuda(), torch.from_numpy(r["topk_w"]).cuda())
@@ -133,6 +135,18 @@ def test_grouped_layer_staged(cuda_lib, fp4_kernel, combine, T, H, F, E, k, chun
         np.add.at(S, pairs // k, np.abs(wflat[pairs][:, None]) * sy)
     ok, ratio, rel = gemm_errors(out.float().cpu().numpy(), ref, S, True)
     assert ok, (ratio, rel)
+    # the fused path: h quantized in the gate/up epilogue
+    fused = MoELayer(W, T, k, combine=combine)
+    if chunk:
+        fused.combine_chunk = chunk
+    assert fused.h_quant == "fused" and fused.h is None
+    out_f = fused.forward(x.cuda(), torch.from_numpy(r["topk_ids"]).cuda(), torch.from_numpy(r["topk_w"]).cuda())
+    torch.cuda.synchronize()
+    assert bs.device_status()[0] == 0
+    assert np.array_equal(fused.hq.cpu().numpy()[:rows], hq)
+    assert np.array_equal(sf_rowmajor(fused.hs.cpu().numpy(), rows, F), sf_rowmajor(layer.hs.cpu().numpy(), rows, F))
+    if combine == "rows":  # the atomic combine's reduction order may differ between runs
+        assert torch.equal(out_f.view(torch.int16), out.view(torch.int16))
     if combine == "atomic":
         # out32 was reset by the finalize step
         assert float(layer.out32.abs().max()) == 0.0
@@ -238,10 +252,24 @@ def test_full_size_layer_sampled_tokens(cuda_lib, cfg, index):
         if e in experts:
             host_w[e] = (wgu.cpu(), wd.cpu())
         del wgu, wd
-    layer = MoELayer(MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf), T, k)
+    Wt = MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf)
+    layer = MoELayer(Wt, T, k, h_quant="separate")  # bf16 h visible for the stages
     out = layer.forward(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(r["topk_w"]).cuda())
     torch.cuda.synchronize()
     assert bs.device_status()[0] == 0
+    # the bench's path (h quantized in the gate/up epilogue): same codes and
+    # scales on every row of the expert segments, same output bit for bit
+    fused = MoELayer(Wt, T, k)
+    out_f = fused.forward(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(r["topk_w"]).cuda())
+    torch.cuda.synchronize()
+    assert bs.device_status()[0] == 0
+    seg_rows = int(fused.disp["offsets"][E])
+    assert torch.equal(fused.hq[:seg_rows], layer.hq[:seg_rows])
+    nblk = (seg_rows + 127) // 128
+    per_blk = bs.sf_bytes(128, F)
+    assert torch.equal(fused.hs[:nblk * per_blk], layer.hs[:nblk * per_blk])
+    assert torch.equal(out_f.view(torch.int16), out.view(torch.int16))
+    del fused
     rop = layer.row_of_pair.cpu().numpy()
     rows = np.array([rop[t * k + j] for t in samples for j in range(k)])
     assert np.all(rows >= 0)
