@@ -507,13 +507,15 @@ bs_status bs_grouped_gemm_swiglu_q4(const bs_gemm_args* a, int E, const int32_t*
     return fail(BS_ERR_UNSUPPORTED, "grouped GEMM takes no alpha/col_scale/bias/low-rank");
   const int64_t wrows = 2 * a->N * (int64_t)E;
   if (wrows > (1LL << 30)) return fail(BS_ERR_INVALID, "stacked weights too large");
+  if (a->M > 0) {
+    if (!h_codes || !h_sf) return fail(BS_ERR_INVALID, "null h_codes / h_sf");
+    if (!aligned16(h_codes) || !aligned16(h_sf)) return fail(BS_ERR_ALIGN, "h_codes / h_sf must be 16-byte aligned");
+  }
   int* status = nullptr;
   int sms = 0;
   if (!device_info(&status, &sms)) return fail(BS_ERR_CUDA, "no current device");
   if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
   if (a->M == 0) return BS_OK;
-  if (!h_codes || !h_sf) return fail(BS_ERR_INVALID, "null h_codes / h_sf");
-  if (!aligned16(h_codes) || !aligned16(h_sf)) return fail(BS_ERR_ALIGN, "h_codes / h_sf must be 16-byte aligned");
   bsk::Fp4Launch L;
   memset(&L, 0, sizeof L);
   L.p.sfa = static_cast<const uint8_t*>(a->sfa);

@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("q4_quantize", "q8_quantize", "bs_gemm", "bs_grouped_gemm", "bs_moe_dispatch",
+    for n in ("q4_quantize", "q8_quantize", "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_swiglu_q4",
+              "bs_moe_dispatch",
               "bs_moe_finalize", "bs_moe_combine", "bs_sf_bytes", "bs_sf_offset", "bs_get_device_status"):
         assert n in names
 
@@ -102,6 +103,16 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.bs_moe_finalize(P((1 << 20) + 4), fake, 8, None) == bs.BS_ERR_ALIGN
     # ROWS needs fp32 output and weight_of (g.out_dtype is bf16 here)
     assert lib.bs_grouped_gemm(ctypes.byref(g), 4, fake, fake, 3, None, fake, None, 0, None) == bs.BS_ERR_INVALID
+    # gate/up GEMM with h quantized in the epilogue: out must be NULL (h goes
+    # to h_codes / h_sf), both present and 16-byte aligned, E in range
+    q4 = lib.bs_grouped_gemm_swiglu_q4
+    assert q4(ctypes.byref(g), 4, fake, fake, fake, fake, None) == bs.BS_ERR_INVALID   # g.out is set
+    g.out = None
+    assert q4(ctypes.byref(g), 4, fake, fake, None, fake, None) == bs.BS_ERR_INVALID
+    assert q4(ctypes.byref(g), 4, fake, fake, fake, P((1 << 20) + 4), None) == bs.BS_ERR_ALIGN
+    assert q4(ctypes.byref(g), 0, fake, fake, fake, fake, None) == bs.BS_ERR_INVALID
+    assert q4(ctypes.byref(g), 4, None, fake, fake, fake, None) == bs.BS_ERR_INVALID
+    g.out = 1 << 20
     # combine: bad k, H not a multiple of 8, misaligned rows; T = 0 is a no-op
     assert lib.bs_moe_combine(fake, 64, fake, 128, 4, 0, 64, fake, fake, 64, None) == bs.BS_ERR_INVALID
     assert lib.bs_moe_combine(fake, 64, fake, 128, 4, 2, 60, fake, fake, 64, None) == bs.BS_ERR_ALIGN
