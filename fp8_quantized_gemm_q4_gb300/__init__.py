@@ -21,7 +21,7 @@ from ._build import LIB as _LIB_PATH
 
 __all__ = [
     "load", "sf_bytes", "sf_offset", "q4_quantize", "fp4_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
-    "grouped_gemm_fp4", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
+    "grouped_gemm_fp4", "grouped_gemm_fp4_swiglu_q4", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
     "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE", "EPI_ROWS",
 ]
 
