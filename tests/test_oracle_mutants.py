@@ -24,6 +24,13 @@ MUTANTS = {
                            "int32_t padded = counts[e];"),
     "lowrank_sign": ("y += prod;\n                    s += fabs(prod);", "y -= prod;\n                    s += fabs(prod);"),
     "swiglu_sign": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(g[i])) * u[i];"),
+    "negative_zero_code": ("return signbit(v) ? (uint8_t)(c | 8) : c;", "return (v < 0) ? (uint8_t)(c | 8) : c;"),
+    "e4m3_subnormal_scale": ("? ldexp((double)m / 8.0, -6)", "? ldexp((double)m / 8.0, -7)"),
+    "scale_not_rounded": ("float s = (float)orc_e4m3_decode(sc);", "float s = div_f32(amax, 6.0f);"),
+    "dispatch_reversed": ("for (int64_t p = 0; p < T * k; ++p)\n            if (topk_ids[p] == e)",
+                          "for (int64_t p = T * k - 1; p >= 0; --p)\n            if (topk_ids[p] == e)"),
+    "bias_dropped": ("if (j->bias) { y += j->bias[n]; s += fabs(j->bias[n]); }",
+                     "if (j->bias) { s += fabs(j->bias[n]); }"),
 }
 
 

@@ -47,6 +47,20 @@ def test_e2m1_matches_ml_dtypes_sweep():
     assert np.array_equal(ref, got)
 
 
+def test_e2m1_signed_zero():
+    """E2M1 carries a sign bit, so -0 is its own code (0b1000); a -0.0 input
+    divided by a positive group scale is -0.0 (IEEE division), so its code
+    is 0b1000 in a quantized group too, as the library cast gives."""
+    ml = pytest.importorskip("ml_dtypes")
+    assert oracle.e2m1_encode(-0.0) == 0b1000 and oracle.e2m1_encode(0.0) == 0
+    assert int(np.array([-0.0], dtype=np.float32).astype(ml.float4_e2m1fn).view(np.uint8)[0]) & 0xF == 0b1000
+    x = np.zeros((1, 16), dtype=np.float32)
+    x[0, 0], x[0, 3], x[0, 5] = 3.0, -0.0, -1e-3   # -1e-3 / 0.5 rounds to -0 as well
+    codes, sf = oracle.q4_quantize(torch.from_numpy(x))
+    nib = lambda k: (int(codes[0, k // 2]) >> (4 * (k & 1))) & 0xF
+    assert nib(0) == 0b0111 and nib(3) == 0b1000 and nib(5) == 0b1000 and nib(1) == 0  # 3.0 / 0.5 = 6
+
+
 def test_e4m3_facts():
     for code, val in read_golden("e4m3_facts.txt"):
         got = oracle.e4m3_decode(int(code))
