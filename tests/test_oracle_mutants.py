@@ -49,3 +49,33 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+# Mistakes planted in the Python half of the oracle (the MoE layer's order of
+# steps): the pin suite runs from a scratch tree whose `oracle` package is
+# the mutated copy (the C library is the unchanged one, via ORACLE_SO).
+PY_MUTANTS = {
+    "gate_up_swapped": ("g, u = gu[0, :F], gu[0, F:]", "u, g = gu[0, :F], gu[0, F:]"),
+    "h_not_rounded": ("h = round_bf16(swiglu(g, u))", "h = swiglu(g, u)"),
+    "routing_weight_dropped": ("acc += w[t, slot] * y[0]", "acc += y[0]"),
+    "output_not_rounded": ("out[i] = round_bf16(acc)", "out[i] = acc"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_pins_catch_planted_mistake_in_layer(name, tmp_path):
+    import oracle as real_oracle
+    old, new = PY_MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    assert src.count(old) == 1, name
+    pkg = tmp_path / "oracle"
+    pkg.mkdir()
+    (pkg / "__init__.py").write_text(src.replace(old, new))
+    for d in ("tests", "workloads"):
+        os.symlink(os.path.join(ROOT, d), tmp_path / d)
+    env = dict(os.environ, ORACLE_SO=real_oracle.build())
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join("tests", "test_oracle_pins.py")],
+                       cwd=str(tmp_path), env=env, capture_output=True, text=True, timeout=600)
+    # a pin must fail on an assertion (not the tree failing to import)
+    assert "ERROR" not in r.stdout and " failed" in r.stdout, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
