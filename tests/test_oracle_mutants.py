@@ -31,6 +31,12 @@ MUTANTS = {
                           "for (int64_t p = T * k - 1; p >= 0; --p)\n            if (topk_ids[p] == e)"),
     "bias_dropped": ("if (j->bias) { y += j->bias[n]; s += fabs(j->bias[n]); }",
                      "if (j->bias) { s += fabs(j->bias[n]); }"),
+    "fp8_token_scale_index": ("double sa = j->sa8[m * KB + kb];", "double sa = j->sa8[m * KB];"),
+    "fp8_block_amax_one_row": ("for (int64_t m = r0; m < r1; ++m)\n                for (int j = 0; j < 128; ++j) {\n"
+                               "                    float a = fabsf",
+                               "for (int64_t m = r0; m < r0 + 1; ++m)\n                for (int j = 0; j < 128; ++j) {\n"
+                               "                    float a = fabsf"),
+    "ties_away_from_zero": ("(d == best_d && (c & 1) == 0 && (best & 1) == 1)", "(d == best_d && c > best)"),
 }
 
 
