@@ -13,8 +13,8 @@
 //   B      its own half (128 rows) of the 256   8 KB
 //   SFA    scales of its own rows               1 KB
 //   SFB    scales of all 256 B rows             2 KB  (held by both: each CTA's
-//          tensor core multiplies its rows by all 256 columns; each CTA
-//          loads one 128-row block and multicasts it to the pair)
+//          tensor core multiplies its rows by all 256 columns, so each CTA
+//          loads both 128-row blocks itself)
 // so a 128-deep stage is 19 KB instead of 27 KB, and 10-11 stages fit.
 //
 // The leader CTA (rank 0) issues every tcgen05.mma / tcgen05.cp with
@@ -345,15 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bar = mapa_shared(smem_u32(&full[ps.index]), 0);
           tma_load_2d_pair(st + kOffA, &tmA, bar, ks * kRowBytes, my_row0);
           tma_load_2d_pair(st + kOffB, &tmB, bar, ks * kRowBytes, my_brow);
-          // scales: each CTA loads its own rows' block of A scales, and one of
-          // the two B scale blocks that both CTAs' tensor cores need (the
-          // leader the first, the peer the second), multicast to the pair
+          // scales: each CTA loads its own rows' block of A scales and both
+          // B scale blocks, since each CTA's tensor core reads all 256 of them
           const int x = ks * G::kSfBox;
           tma_load_2d_pair(st + kOffSfa, &tmSfa, bar, x, my_row0 / 128);
-          if (leader)
-            tma_load_2d_pair_mc(st + kOffSfb, &tmSfb, bar, x, tl.brow0 / 128, 0x3);
-          else
-            tma_load_2d_pair_mc(st + kOffSfb + kMmas * 512, &tmSfb, bar, x, tl.sfb_blk1, 0x3);
+          tma_load_2d_pair(st + kOffSfb, &tmSfb, bar, x, tl.brow0 / 128);
+          tma_load_2d_pair(st + kOffSfb + kMmas * 512, &tmSfb, bar, x, tl.sfb_blk1);
         }
         __syncwarp();
         issued_mask |= 1u << ps.index;
