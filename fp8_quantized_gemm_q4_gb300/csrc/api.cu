@@ -16,6 +16,41 @@
 static_assert(BS_MOE_DISPATCH_NOALLOC_MAX_BYTES == bsk::kNoAllocDispatchScratchBytes,
               "header limit and static scratch size must agree");
 
+namespace bsk {
+
+// Unique id of the CUDA context current on the calling thread, 0 if none.
+// Device addresses of the library's __device__ variables belong to a context
+// (a non-primary context, or the primary context re-created after
+// cudaDeviceReset, has its own), so address caches are keyed on this id, which
+// the driver never reuses within a process.  The driver calls are reached
+// through the runtime's entry-point query (no libcuda link).
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id + 1;  // never 0 for a live context
+}
+
+}  // namespace bsk
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -35,28 +70,36 @@ bs_status cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Device status word: one per device, address looked up once per device.
+// Device status word: one per context, its address looked up once per
+// context (see bsk::current_context_id).
 __device__ int g_device_status;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int* g_status_ptr[kMaxDevices] = {};
-int g_sm_count[kMaxDevices] = {};
+struct DeviceInfo {
+  unsigned long long ctx_id;  // context the address below belongs to (0: not looked up)
+  int* status;
+  int sms;
+};
+DeviceInfo g_info[kMaxDevices] = {};
 
 bool device_info(int** status, int* sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[dev]) {
+  unsigned long long ctx = bsk::current_context_id();
+  if (ctx == 0 || g_info[dev].ctx_id != ctx) {
+    // first call in this context (or a context other than the cached one):
+    // the lookup also makes the runtime's primary context current if none is
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return false;
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    g_status_ptr[dev] = static_cast<int*>(p);
-    g_sm_count[dev] = n;
+    ctx = bsk::current_context_id();
+    g_info[dev] = DeviceInfo{ctx, static_cast<int*>(p), n};
   }
-  if (status) *status = g_status_ptr[dev];
-  if (sms) *sms = g_sm_count[dev];
+  if (status) *status = g_info[dev].status;
+  if (sms) *sms = g_info[dev].sms;
   return true;
 }
 

@@ -120,6 +120,10 @@ cudaError_t launch_moe_combine(const float* rows, long long ld_rows, const int* 
                                long long T, int k, long long H, int* row_of_pair, void* out, long long ldo,
                                cudaStream_t stream);
 
+// Unique id of the CUDA context current on this thread (0 if none); keys the
+// caches of device addresses of the library's __device__ variables.
+unsigned long long current_context_id();
+
 // Grouping whose histogram scratch is the library's static device array.
 constexpr size_t kNoAllocDispatchScratchBytes = size_t(1) << 20;
 cudaError_t launch_moe_dispatch_noalloc(const int* topk_ids, const float* topk_w, long long T, int k, int E,

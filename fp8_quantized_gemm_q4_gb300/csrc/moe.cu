@@ -320,25 +320,33 @@ static __device__ __align__(256) int g_dispatch_scratch[kNoAllocDispatchScratchB
 
 namespace {
 std::mutex g_scratch_mu;
-int* g_scratch_ptr[64] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id;  // context the address belongs to (0: not looked up)
+  int* ptr;
+};
+ScratchAddr g_scratch[64] = {};
 }  // namespace
 
-// Device address of the array on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// Device address of the array in the current context.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per context (a device's primary context, or any
+// other context the caller makes current on it) and cached under the
+// context's unique id; a call from a context other than the cached one looks
+// the address up again.
 cudaError_t dispatch_scratch_ptr(int** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  unsigned long long ctx = current_context_id();
+  if (ctx == 0 || g_scratch[dev].ctx_id != ctx) {
     int* p = nullptr;
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_dispatch_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+    g_scratch[dev] = ScratchAddr{current_context_id(), p};
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 

@@ -291,9 +291,14 @@ bs_status bs_moe_dispatch(const int32_t *topk_ids, const float *topk_w, int64_t 
  *   Memory: every GPU that loads the library holds the 1 MiB array until the
  *          process exits.  It calls no cudaMalloc / cudaFree or other
  *          allocating routine.
- *   Set-up: the first call on a device looks up the array's device address
- *          (once per device, with that device current); make that first call
- *          before any stream capture.
+ *   Set-up: the first call in a CUDA context looks up the array's device
+ *          address (cudaGetSymbolAddress, with that context current) and
+ *          caches it under the context's unique id; the runtime's primary
+ *          context of each device is one such context, and a call from another
+ *          context (a driver-API context of the caller's, or a primary
+ *          context re-created after cudaDeviceReset) looks the address up
+ *          again.  Make the first call in each context before any stream
+ *          capture.
  *   Sharing: all calls share the array and it keeps the last call's
  *          contents (each call overwrites everything it reads).  Calls whose
  *          kernels can overlap on the GPU -- different streams or host threads
