@@ -23,6 +23,11 @@ int main() {
   constexpr int stages_split = max_main_stages(round_up(fp4_stage_bytes(pair), kAlign), round_up(split, kAlign), misc);
   constexpr int stages_repl = max_main_stages(round_up(fp4_stage_bytes(pair), kAlign), round_up(repl, kAlign), misc);
   static_assert(split < repl, "split accounting must be smaller");
+  constexpr int kmisc = 2048 + 1024 + 8 * 32 * 32;
+  constexpr Fp4TileShape kpair{128, 256, 256, 2, true, 32, kmisc};
+  constexpr int kstages_split = fp4_main_stages(kpair);
+  constexpr int kstages_repl =
+      max_main_stages(round_up(fp4_stage_bytes(kpair), kAlign), round_up(fp4_lora_bytes_replicated(kpair), kAlign), kmisc);
   printf("stage_one %d\n", fp4_stage_bytes(one));
   printf("stage_pair %d\n", fp4_stage_bytes(pair));
   printf("lora_one %d\n", fp4_lora_bytes(one));
@@ -32,6 +37,8 @@ int main() {
   printf("stages_one_nolora %d\n", fp4_main_stages(one_nl));
   printf("stages_pair_split %d\n", stages_split);
   printf("stages_pair_repl %d\n", stages_repl);
+  printf("kernel_stages_split %d\n", kstages_split);
+  printf("kernel_stages_repl %d\n", kstages_repl);
   printf("smem_one %d\n", fp4_smem_total(one, fp4_main_stages(one)));
   printf("smem_one_nolora %d\n", fp4_smem_total(one_nl, fp4_main_stages(one_nl)));
   printf("tmem_one %d\n", fp4_tmem_cols(one, 1, 2));
@@ -72,8 +79,15 @@ def test_stage_solver_fits_and_is_maximal(budget):
     assert budget["smem_one_nolora"] + 1024 <= 232448
     # one more stage would not fit
     assert budget["smem_one"] + budget["stage_one"] > 232448 - 1024
-    # the double-counted up-projection never buys stages; the split one may
-    assert budget["stages_pair_split"] >= budget["stages_pair_repl"]
+    # the page's split-or-replicate decision (section 6): counting each CTA's
+    # half of the up-projection block gives the pair five main stages;
+    # counting the whole block in every CTA (the page's bug) gives four
+    assert budget["stages_pair_split"] == 5
+    assert budget["stages_pair_repl"] == 4
+    # the same decision with the pair kernel's own low-rank shape (its misc
+    # bytes: barriers 3 KiB + eight 32 x 32-byte output staging boxes)
+    assert budget["kernel_stages_split"] == 5
+    assert budget["kernel_stages_repl"] == 4
 
 
 def test_tmem_budget(budget):
