@@ -22,7 +22,8 @@ from ._build import LIB as _LIB_PATH
 __all__ = [
     "load", "sf_bytes", "sf_offset", "q4_quantize", "fp4_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
     "grouped_gemm_fp4", "grouped_gemm_fp4_swiglu_q4", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
-    "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE", "EPI_ROWS",
+    "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE", "EPI_ROWS", "kernel_options",
+    "current_kernel_options", "FP4_ONE_CTA", "FP4_PAIR",
 ]
 
 BS_OK, BS_ERR_INVALID, BS_ERR_ALIGN, BS_ERR_UNSUPPORTED, BS_ERR_CUDA, BS_ERR_TIMEOUT, BS_ERR_OFFSETS = range(7)
@@ -45,8 +46,44 @@ class GemmArgs(ctypes.Structure):
         ("alpha", ctypes.c_float), ("col_scale", ctypes.c_void_p), ("lora_t", ctypes.c_void_p),
         ("lora_b_t", ctypes.c_void_p), ("r", ctypes.c_int), ("bias", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("out_dtype", ctypes.c_int), ("ldo", ctypes.c_int64), ("num_sms", ctypes.c_int),
-        ("n_chunk_blocks", ctypes.c_int),
+        ("n_chunk_blocks", ctypes.c_int), ("fp4_kernel", ctypes.c_int), ("fp4_stage_k", ctypes.c_int),
+        ("fp4_small_experts", ctypes.c_int), ("fp4_half_tail", ctypes.c_int), ("fp8_split_k", ctypes.c_int),
+        ("wait_timeout_us", ctypes.c_int),
     ]
+
+
+# Per-call kernel choices of bs_gemm_args (0 = the library's default), see
+# include/bsgemm.h.  Every GEMM call of this binding fills them from the
+# options active on the calling thread: the defaults, or those of an enclosing
+# ``with kernel_options(...)`` block.
+_CHOICES = ("fp4_kernel", "fp4_stage_k", "fp4_small_experts", "fp4_half_tail", "fp8_split_k", "wait_timeout_us")
+FP4_ONE_CTA, FP4_PAIR = 1, 2
+_tls = threading.local()
+
+
+def current_kernel_options() -> dict:
+    return dict(getattr(_tls, "opts", {}))
+
+
+class kernel_options:
+    """Context manager: GEMM calls made on this thread inside the block pass
+    these kernel choices in their bs_gemm_args (unnamed fields keep the value
+    of any enclosing block, else 0 = default)."""
+
+    def __init__(self, **choices):
+        bad = set(choices) - set(_CHOICES)
+        if bad:
+            raise TypeError(f"unknown kernel choices {sorted(bad)}")
+        self.choices = {k: int(v) for k, v in choices.items()}
+
+    def __enter__(self):
+        self.saved = getattr(_tls, "opts", {})
+        _tls.opts = {**self.saved, **self.choices}
+        return self
+
+    def __exit__(self, *exc):
+        _tls.opts = self.saved
+        return False
 
 
 _lib = None
@@ -201,6 +238,8 @@ def _args(fmt, a, sfa, b, sfb, M, N, K, out, alpha=1.0, col_scale=None, lora_t=N
         g.out_dtype = _dt(out)
         g.ldo = out.stride(0)
     g.num_sms = num_sms
+    for k, v in getattr(_tls, "opts", {}).items():
+        setattr(g, k, v)
     return g
 
 

@@ -253,12 +253,28 @@ bs_status q8_quantize(const void* x, bs_dtype dt, int64_t M, int64_t K, int64_t 
   return BS_OK;
 }
 
+// Range checks of the per-call kernel choices (0 = default everywhere).
+static bs_status check_choices(const bs_gemm_args* a) {
+  if (a->fp4_kernel < 0 || a->fp4_kernel > 2) return fail(BS_ERR_INVALID, "fp4_kernel=%d (0, 1 or 2)", a->fp4_kernel);
+  if (a->fp4_stage_k != 0 && a->fp4_stage_k != 128 && a->fp4_stage_k != 256)
+    return fail(BS_ERR_INVALID, "fp4_stage_k=%d (0, 128 or 256)", a->fp4_stage_k);
+  if (a->fp4_small_experts < 0 || a->fp4_small_experts > 2)
+    return fail(BS_ERR_INVALID, "fp4_small_experts=%d (0, 1 or 2)", a->fp4_small_experts);
+  if (a->fp4_half_tail < 0 || a->fp4_half_tail > 2)
+    return fail(BS_ERR_INVALID, "fp4_half_tail=%d (0, 1 or 2)", a->fp4_half_tail);
+  if (a->fp8_split_k < 0 || a->fp8_split_k > 2) return fail(BS_ERR_INVALID, "fp8_split_k=%d (0, 1 or 2)", a->fp8_split_k);
+  if (a->wait_timeout_us < 0) return fail(BS_ERR_INVALID, "wait_timeout_us < 0");
+  return BS_OK;
+}
+
 static bs_status check_common(const bs_gemm_args* a, bool grouped) {
   if (!a) return fail(BS_ERR_INVALID, "null args");
   if (a->M < 0 || a->N <= 0 || a->K <= 0) return fail(BS_ERR_INVALID, "bad sizes M=%lld N=%lld K=%lld",
                                                     (long long)a->M, (long long)a->N, (long long)a->K);
   if (a->M > (1LL << 30) || a->N > (1LL << 30) || a->K > (1LL << 30)) return fail(BS_ERR_INVALID, "sizes too large");
   if (a->N % 128) return fail(BS_ERR_ALIGN, "N=%lld not a multiple of 128", (long long)a->N);
+  bs_status st = check_choices(a);
+  if (st != BS_OK) return st;
   if (a->M == 0) return BS_OK;  // nothing to compute; operands may be empty (null)
   if (!a->a || !a->b || !a->sfa || !a->sfb) return fail(BS_ERR_INVALID, "null operand");
   if (!aligned16(a->a) || !aligned16(a->b) || !aligned16(a->sfa) || !aligned16(a->sfb))
@@ -273,21 +289,16 @@ static bs_status check_common(const bs_gemm_args* a, bool grouped) {
   return BS_OK;
 }
 
-// FP4 stage depth: 256 K elements (128-byte rows, 128B swizzle) measured
-// faster than 128 (64-byte rows) on GB300 even though the finer ring holds
-// more stages; BSGEMM_FP4_BK=128 selects the finer ring (for measurements).
-static int fp4_bk() {
-  const char* e = getenv("BSGEMM_FP4_BK");
-  return (e && atoi(e) == 128) ? 128 : 256;
+// Pipeline-wait bound of the kernels launched for `a` (nanoseconds).
+constexpr unsigned long long kDefaultWaitNs = 4000000000ull;  // 4 s
+static unsigned long long wait_ns(const bs_gemm_args* a) {
+  return a->wait_timeout_us > 0 ? (unsigned long long)a->wait_timeout_us * 1000ull : kDefaultWaitNs;
 }
 
-// FP4 GEMM on CTA pairs (cta_group::2, 256 x 256 tiles) unless
-// BSGEMM_FP4_PAIR=0 selects the one-CTA kernel (128 x 256 tiles).  Read on
-// every call so one process can run both.
-static bool fp4_pair() {
-  const char* e = getenv("BSGEMM_FP4_PAIR");
-  return !(e && atoi(e) == 0);
-}
+// FP4 stage depth: 256 K elements (128-byte rows, 128B swizzle) measured
+// faster than 128 (64-byte rows) on GB300 even though the finer ring holds
+// more stages.
+static int fp4_bk(const bs_gemm_args* a) { return a->fp4_stage_k == 128 ? 128 : 256; }
 
 static bs_status fp4_maps(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int bk) {
   const uint64_t kb = (uint64_t)a->K / 2;
@@ -324,45 +335,21 @@ static bs_status sf_map(CUtensorMap* m, const void* sf, int64_t rows, int64_t K,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// FP8 decode split-K over CTA pairs (BSGEMM_FP8_SPLIT=0 disables it).
-static bool fp8_split_ok() {
-  static bool on = [] {
-    const char* e = getenv("BSGEMM_FP8_SPLIT");
-    return !(e && atoi(e) == 0);
-  }();
-  return on;
-}
-
-// Grouped GEMMs on CTA pairs hand experts of at most 128 rows to a second,
-// one-CTA launch (BSGEMM_FP4_TAILS=0 keeps them in the pair launch).
-// Read on every call.
-static bool fp4_split_tails() {
-  const char* e = getenv("BSGEMM_FP4_TAILS");
-  return !(e && atoi(e) == 0);
-}
-
-// Dense GEMMs on CTA pairs split a last wave that fills at most half the pairs
-// into 256 x 128 half tiles (BSGEMM_FP4_HALF_TAIL=0 keeps whole tiles).  Read
-// on every call.
-static bool fp4_half_tail() {
-  const char* e = getenv("BSGEMM_FP4_HALF_TAIL");
-  return !(e && atoi(e) == 0);
-}
-
 static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_rows, int sms, cudaStream_t s,
                             long long pair_tiles, bool grouped) {
   bs_status st;
-  if (fp4_pair() && sms >= 2) {  // a pair needs two SMs
-    const bool split = grouped && fp4_split_tails();
+  L.p.wait_ns = wait_ns(a);
+  if (a->fp4_kernel != 1 && sms >= 2) {  // a pair needs two SMs
+    const bool split = grouped && a->fp4_small_experts != 2;
     L.p.part = split ? 1 : 0;
-    L.p.half_tail = (!grouped && fp4_half_tail()) ? 1 : 0;
+    L.p.half_tail = (!grouped && a->fp4_half_tail != 2) ? 1 : 0;
     bsk::Fp4PairLaunch P;
     memset(&P, 0, sizeof P);
-    st = fp4_maps(L, a, b_rows, fp4_bk());
+    st = fp4_maps(L, a, b_rows, fp4_bk(a));
     if (st != BS_OK) return st;
-    st = sf_map(&P.tmSfa, a->sfa, a->M, a->K, fp4_bk());
+    st = sf_map(&P.tmSfa, a->sfa, a->M, a->K, fp4_bk(a));
     if (st != BS_OK) return st;
-    st = sf_map(&P.tmSfb, a->sfb, b_rows, a->K, fp4_bk());
+    st = sf_map(&P.tmSfb, a->sfb, b_rows, a->K, fp4_bk(a));
     if (st != BS_OK) return st;
     if (L.epilogue == bsk::kEpiSwiglu || L.epilogue == bsk::kEpiRows ||
         (L.epilogue == bsk::kEpiStore && !grouped)) {
@@ -389,7 +376,7 @@ static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_
     }
     return BS_OK;
   }
-  st = fp4_maps(L, a, b_rows, fp4_bk());
+  st = fp4_maps(L, a, b_rows, fp4_bk(a));
   if (st != BS_OK) return st;
   cudaError_t e = bsk::launch_fp4_gemm(L, s);
   if (e != cudaSuccess) return cuda_fail(e, "FP4 GEMM launch");
@@ -468,7 +455,8 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     // Decode shapes with few tiles: two CTAs per tile, each streaming half of
     // K (split-K over a 2-CTA cluster, partials reduced through DSMEM).
     L.p.splits = 1;
-    if (L.tile_n <= 32 && tiles * 2 <= sms && a->K >= 256 && fp8_split_ok()) {
+    L.p.wait_ns = wait_ns(a);
+    if (L.tile_n <= 32 && tiles * 2 <= sms && a->K >= 256 && a->fp8_split_k != 2) {
       L.p.splits = 2;
       L.grid = (int)(2 * tiles);
     }

@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem sm = carve<kStages, kLora, G::kStageBytes>(base);
   const int warp = warp_bcast((int)(threadIdx.x / 32)), lane = threadIdx.x % 32;
   volatile int* abort_flag = sm.abort_flag;
+  const WaitGuard wg{abort_flag, p.status, p.wait_ns};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* sfb0_src = p.sfb + (size_t)(tl.brow0 / 128) * kchunks * 512;
       const uint8_t* sfb1_src = p.sfb + (size_t)tl.sfb_blk1 * kchunks * 512;
       for (int ks = 0; ks < kstages; ++ks) {
-        if (!mbar_wait_warp(&sm.empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 10)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.empty[ps.index], ps.phase ^ 1u, wg, 10)) { ok = false; break; }
         const int nmma = min(G::kMmas, kchunks - G::kMmas * ks);
         uint8_t* st = sm.stages + ps.index * G::kStageBytes;
         uint64_t* bar = &sm.full[ps.index];
@@ -313,14 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ps.advance();
       }
     }
-    if (*abort_flag && lane == 0) {
-      // Let copies already in flight land before the CTA can exit.
+    if (lane == 0) {
+      // Copies already in flight land before the CTA can exit (after an
+      // abort; on the normal path every issued stage has completed already).
       for (int s = 0; s < kStages; ++s)
-        if (issued_mask & (1u << s)) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(&sm.full[s], (last_phase >> s) & 1u) && globaltimer() - t0 < 100000000ull) {
-          }
-        }
+        if (issued_mask & (1u << s)) mbar_drain(&sm.full[s], (last_phase >> s) & 1u, 100000000ull);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ low-rank producer
@@ -329,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued = false;
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
         const Tile tl = bcast_tile(tile_of<kEpi>(p, sm.prefix, t));
-        if (!mbar_wait_warp(sm.lora_empty, phase ^ 1u, abort_flag, p.status, 20)) break;
+        if (!mbar_wait_warp(sm.lora_empty, phase ^ 1u, wg, 20)) break;
         if (elect_one()) {
           mbar_arrive_expect_tx(sm.lora_full, (uint32_t)kLoraBytes);
           tma_load_2d(sm.lora + kLoraThi, &tmT, sm.lora_full, 0, tl.row0);
@@ -341,11 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = true;
         phase ^= 1u;
       }
-      if (*abort_flag && issued && lane == 0) {
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(sm.lora_full, phase ^ 1u) && globaltimer() - t0 < 100000000ull) {
-        }
-      }
+      if (issued && lane == 0) mbar_drain(sm.lora_full, phase ^ 1u, 100000000ull);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -361,10 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dSfa = smem_desc(smem_u32(sm.stages + G::kOffSfa), 0, 128, kLayoutNone);
     const uint64_t dSfb = smem_desc(smem_u32(sm.stages + G::kOffSfb), 0, 128, kLayoutNone);
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      if (!mbar_wait_warp(sm.acc_empty, acc_phase ^ 1u, abort_flag, p.status, 30)) break;
+      if (!mbar_wait_warp(sm.acc_empty, acc_phase ^ 1u, wg, 30)) break;
       tc_fence_after();
       for (int ks = 0; ks < kstages; ++ks) {
-        if (!mbar_wait_warp(&sm.full[ps.index], ps.phase, abort_flag, p.status, 31)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.full[ps.index], ps.phase, wg, 31)) { ok = false; break; }
         tc_fence_after();
         const int nmma = min(G::kMmas, kchunks - G::kMmas * ks);
         const uint64_t so = (uint64_t)((ps.index * G::kStageBytes) >> 4);
@@ -392,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (kLora) {
-        if (!mbar_wait_warp(sm.lora_full, lora_phase, abort_flag, p.status, 32)) break;
+        if (!mbar_wait_warp(sm.lora_full, lora_phase, wg, 32)) break;
         tc_fence_after();
         if (elect_one()) {
           const uint32_t thi = smem_u32(sm.lora + kLoraThi), tlo = smem_u32(sm.lora + kLoraTlo);
@@ -417,9 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Drain: every tcgen05 op issued above has finished before TMEM is freed.
     if (elect_one()) {
       tc_commit(sm.drain);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(sm.drain, 0) && globaltimer() - t0 < 1000000000ull) {
-      }
+      mbar_drain(sm.drain, 0, 1000000000ull);
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
@@ -432,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile tl = tile_of<kEpi>(p, sm.prefix, t);
       // one lane polls, the warp follows (keeps the .sync.aligned loads convergent)
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(sm.acc_full, acc_phase, abort_flag, p.status, 40) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(sm.acc_full, acc_phase, wg, 40) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();

@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* total_tiles = abort_i + 1;
   int* prefix = total_tiles + 2;
   volatile int* abort_flag = abort_i;
+  const WaitGuard wg{abort_flag, p.status, p.wait_ns};
 
   const int warp = warp_bcast((int)(threadIdx.x / 32)), lane = threadIdx.x % 32;
   const uint32_t rank = warp_bcast(cluster_ctarank());
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int my_row0 = tl.row0 + (int)rank * BM;
       const int my_brow = leader ? tl.brow0 : tl.brow1;
       for (int ks = 0; ks < kstages; ++ks) {
-        if (!mbar_wait_warp(&empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 110)) { ok = false; break; }
+        if (!mbar_wait_warp(&empty[ps.index], ps.phase ^ 1u, wg, 110)) { ok = false; break; }
         uint8_t* st = stages + ps.index * kStageBytes;
         if (elect_one()) {
           if (leader) mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(2 * G::kStageTx));
@@ -358,21 +359,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         ps.advance();
       }
     }
-    if (*abort_flag && leader && lane == 0) {
+    if (leader && lane == 0) {
+      // Copies already in flight (both CTAs' loads signal the leader's
+      // barriers) land before the pair can exit (after an abort; on the
+      // normal path every issued stage has completed already).
       for (int s = 0; s < kStages; ++s)
-        if (issued_mask & (1u << s)) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(&full[s], (last_phase >> s) & 1u) && globaltimer() - t0 < 100000000ull) {
-          }
-        }
+        if (issued_mask & (1u << s)) mbar_drain(&full[s], (last_phase >> s) & 1u, 100000000ull);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ low-rank producer (both CTAs)
     if (kLora) {
       uint32_t phase = 0;
+      bool issued = false;
       for (int t = pair; t < total; t += npairs) {
         const Tile tl = bcast_tile(tile_of<kEpi>(p, prefix, t));
-        if (!mbar_wait_warp(lora_empty, phase ^ 1u, abort_flag, p.status, 120)) break;
+        if (!mbar_wait_warp(lora_empty, phase ^ 1u, wg, 120)) break;
         if (elect_one()) {
           if (leader) mbar_arrive_expect_tx(lora_full, (uint32_t)(2 * kLoraBytes));
           const uint32_t bar = mapa_shared(smem_u32(lora_full), 0);
@@ -382,8 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d_pair(lora + kLoraBl, &tmL, bar, 0, leader ? tl.brow0 : tl.brow1);
         }
         __syncwarp();
+        issued = true;
         phase ^= 1u;
       }
+      // the last low-rank copies (both CTAs') land before the pair can exit
+      if (issued && leader && lane == 0) mbar_drain(lora_full, phase ^ 1u, 100000000ull);
     }
   } else if (warp == 1 && leader) {
     // ------------------------------------------------------------------ MMA issuer (leader only)
@@ -399,10 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = pair; t < total && ok; t += npairs) {
       const bool narrow = (kEpi == kEpiStore && p.E == 0) && warp_bcast(tile_of<kEpi>(p, prefix, t).narrow) != 0;
       const uint32_t idesc_main = narrow ? kIdescMainHalf : kIdescMain;
-      if (!mbar_wait_warp(acc_empty, acc_phase ^ 1u, abort_flag, p.status, 130)) break;
+      if (!mbar_wait_warp(acc_empty, acc_phase ^ 1u, wg, 130)) break;
       tc_fence_after();
       for (int ks = 0; ks < kstages; ++ks) {
-        if (!mbar_wait_warp(&full[ps.index], ps.phase, abort_flag, p.status, 131)) { ok = false; break; }
+        if (!mbar_wait_warp(&full[ps.index], ps.phase, wg, 131)) { ok = false; break; }
         tc_fence_after();
         const int nmma = min(kMmas, kchunks - kMmas * ks);
         const uint64_t so = (uint64_t)((ps.index * kStageBytes) >> 4);
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (kLora) {
-        if (!mbar_wait_warp(lora_full, lora_phase, abort_flag, p.status, 132)) break;
+        if (!mbar_wait_warp(lora_full, lora_phase, wg, 132)) break;
         tc_fence_after();
         if (elect_one()) {
           const uint32_t thi = smem_u32(lora + kLoraThi), tlo = smem_u32(lora + kLoraTlo);
@@ -455,9 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (elect_one()) {
       tc_commit_pair_local(drain);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 1000000000ull) {
-      }
+      mbar_drain(drain, 0, 1000000000ull);
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = pair; t < total; t += npairs) {
       const Tile tl = tile_of<kEpi>(p, prefix, t);
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(acc_full, acc_phase, abort_flag, p.status, 140) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(acc_full, acc_phase, wg, 140) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();

@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_base = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_i = reinterpret_cast<int*>(tmem_base + 1);
   volatile int* abort_flag = abort_i;
+  const WaitGuard wg{abort_flag, p.status, p.wait_ns};
   const int warp = warp_bcast((int)(threadIdx.x / 32)), lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = t_first; t < total && ok; t += t_step) {
       const int wb = t % n_wblk, tb = t / n_wblk;
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait_warp(&empty[ps.index], ps.phase ^ 1u, abort_flag, p.status, 50)) { ok = false; break; }
+        if (!mbar_wait_warp(&empty[ps.index], ps.phase ^ 1u, wg, 50)) { ok = false; break; }
         uint8_t* st = stages + ps.index * C::kStageBytes;
         if (elect_one()) {
           mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(BM * BK + TN * BK));
@@ -153,13 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ps.advance();
       }
     }
-    if (*abort_flag && lane == 0) {
+    if (lane == 0) {
+      // copies already in flight land before the CTA can exit
       for (int s = 0; s < C::kStages; ++s)
-        if (issued_mask & (1u << s)) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(&full[s], (last_phase >> s) & 1u) && globaltimer() - t0 < 100000000ull) {
-          }
-        }
+        if (issued_mask & (1u << s)) mbar_drain(&full[s], (last_phase >> s) & 1u, 100000000ull);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -172,8 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = t_first; t < total && ok; t += t_step) {
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait_warp(&pempty[sl.index], sl.phase ^ 1u, abort_flag, p.status, 60)) { ok = false; break; }
-        if (!mbar_wait_warp(&full[ps.index], ps.phase, abort_flag, p.status, 61)) { ok = false; break; }
+        if (!mbar_wait_warp(&pempty[sl.index], sl.phase ^ 1u, wg, 60)) { ok = false; break; }
+        if (!mbar_wait_warp(&full[ps.index], ps.phase, wg, 61)) { ok = false; break; }
         tc_fence_after();
         const uint64_t so = (uint64_t)((ps.index * C::kStageBytes) >> 4);
         const uint32_t d = tmem + sl.index * TN;
@@ -191,9 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (elect_one()) {
       tc_commit(drain);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < 1000000000ull) {
-      }
+      mbar_drain(drain, 0, 1000000000ull);
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
@@ -274,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             idx[i] = sl.index;
             if (ok) {
               int w_ok = 1;
-              if (lane == 0) w_ok = mbar_wait(&pfull[sl.index], sl.phase, abort_flag, p.status, 71) ? 1 : 0;
+              if (lane == 0) w_ok = mbar_wait(&pfull[sl.index], sl.phase, wg, 71) ? 1 : 0;
               w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
               ok = w_ok != 0;
             }
@@ -311,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; kb < kb_end; ++kb) {
         if (ok) {
           int w_ok = 1;
-          if (lane == 0) w_ok = mbar_wait(&pfull[sl.index], sl.phase, abort_flag, p.status, 70) ? 1 : 0;
+          if (lane == 0) w_ok = mbar_wait(&pfull[sl.index], sl.phase, wg, 70) ? 1 : 0;
           w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
           ok = w_ok != 0;
         }

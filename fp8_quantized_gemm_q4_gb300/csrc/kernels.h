@@ -35,6 +35,7 @@ struct Fp4Params {
   int part;               // grouped rows covered: 0 all, 1 experts > 128 rows, 2 the others (expert_part)
   int half_tail;          // dense, CTA pairs: split a short last wave into 256 x 128 half tiles
   uint8_t* out_sf;        // SWIGLU_Q4: scales of h (MMA layout for [M, N]); out holds its codes [M, N/2]
+  unsigned long long wait_ns;  // bound of every pipeline wait (%globaltimer ns)
 };
 
 // Rows of expert e that one grouped launch covers.  part 0: all of them.  A
@@ -84,6 +85,7 @@ struct Fp8Params {
   int* counters;          // split-K tile counters (decode), may be null
   int splits;
   int* status;
+  unsigned long long wait_ns;  // bound of every pipeline wait (%globaltimer ns)
 };
 
 struct Fp8Launch {

@@ -1,20 +1,17 @@
 // ptx.cuh -- inline-PTX wrappers for sm_103a: mbarriers with bounded waits,
 // TMA bulk-tensor loads, and the tcgen05 tensor-core / tensor-memory ops.
 //
-// Every wait in this library is bounded: after BSK_WAIT_TIMEOUT_NS of
-// %globaltimer without progress the waiter raises the CTA-wide abort flag,
-// records BS_ERR_TIMEOUT plus a site id in the device status word and
-// returns false; every other waiter in the CTA sees the flag and returns too,
-// so a broken pipeline ends the kernel instead of hanging the GPU.
+// Every wait in this library is bounded: after the launch's wait limit
+// (WaitGuard::limit_ns of %globaltimer, 4 s unless the caller sets another)
+// without progress the waiter raises the CTA-wide abort flag, records
+// BS_ERR_TIMEOUT plus a site id in the device status word and returns false;
+// every other waiter in the CTA sees the flag and returns too, so a broken
+// pipeline ends the kernel instead of hanging the GPU.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#ifndef BSK_WAIT_TIMEOUT_NS
-#define BSK_WAIT_TIMEOUT_NS 4000000000ull  // 4 s
-#endif
 
 namespace bsk {
 
@@ -66,23 +63,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// What a bounded wait of one CTA needs: the CTA-wide abort flag (shared
+// memory), the device status word and the launch's wait limit.
+struct WaitGuard {
+  volatile int* abort_flag;
+  int* status;
+  uint64_t limit_ns;
+};
+
 // Waits until the phase with the given parity has completed.  Returns false
 // (and leaves the CTA abort flag set) on timeout or when another waiter of
 // the CTA already gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, int site) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitGuard& wg, int site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > BSK_WAIT_TIMEOUT_NS) {
-        *abort_flag = 1;
-        record_status(status, kStatusTimeout, site);
+      if (*wg.abort_flag) return false;
+      if (globaltimer() - t0 > wg.limit_ns) {
+        *wg.abort_flag = 1;
+        record_status(wg.status, kStatusTimeout, site);
         return false;
       }
     }
+  }
+}
+
+// Bounded wait used on the way out of a kernel (draining copies or tensor-core
+// work already issued): returns when the phase completes or after `limit_ns`.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < limit_ns) {
   }
 }
 
@@ -112,10 +124,9 @@ __device__ __forceinline__ T warp_bcast(T v) {
 }
 
 // mbar_wait by lane 0 of the calling warp, result broadcast to all lanes.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                               int* status, int site) {
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitGuard& wg, int site) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status, site) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, wg, site) ? 1 : 0;
   return warp_bcast(ok) != 0;
 }
 

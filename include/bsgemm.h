@@ -169,6 +169,10 @@ bs_status q8_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t 
  *   M >= 0, N % 128 == 0, K % 64 == 0 (FP4) or K % 128 == 0 (FP8)
  *   num_sms    persistent grid size limit (0 = all SMs)
  *   n_chunk_blocks  ignored by bs_gemm (grouped tile-order knob)
+ *   fp4_kernel, fp4_stage_k, fp4_small_experts, fp4_half_tail, fp8_split_k,
+ *   wait_timeout_us
+ *              per-call kernel choices, described at the fields; 0 = the
+ *              library's default.  A zero-initialised struct gets every default.
  * ------------------------------------------------------------------------- */
 typedef struct {
     int fmt;                 /* bs_format */
@@ -190,6 +194,21 @@ typedef struct {
     int n_chunk_blocks;      /* grouped only: tile order walks chunks of this many output
                                 column blocks (256 columns; 128 for SWIGLU), all experts per
                                 chunk; 0 = one chunk.  Bounds the live out32 slab of COMBINE */
+    /* Per-call kernel choices (0 = default).  Other values return BS_ERR_INVALID. */
+    int fp4_kernel;          /* FP4: 1 = one CTA per 128 x 256 output tile; 2 = CTA pairs
+                                (cta_group::2) on 256 x 256 tiles.  Default: 2 when the call may
+                                use two or more SMs, else 1 */
+    int fp4_stage_k;         /* FP4: K elements per pipeline stage, 128 or 256 (default 256) */
+    int fp4_small_experts;   /* grouped FP4 on CTA pairs: 1 = experts of at most 128 rows run in a
+                                second, one-CTA launch (default); 2 = every expert in the pair launch */
+    int fp4_half_tail;       /* dense FP4 on CTA pairs: 1 = a last wave that fills at most half of
+                                the pairs runs as 256 x 128 half tiles (default); 2 = whole tiles */
+    int fp8_split_k;         /* FP8 decode shapes (at most 32 token columns per tile, few tiles):
+                                1 = each tile's K split over a CTA pair (default); 2 = no split */
+    int wait_timeout_us;     /* bound of every pipeline wait inside the kernels, in microseconds
+                                (default 4,000,000 = 4 s).  A wait that runs out ends the kernel
+                                early (outputs undefined) and sets BS_ERR_TIMEOUT in the device
+                                status word; it never hangs the GPU */
 } bs_gemm_args;
 
 bs_status bs_gemm(const bs_gemm_args *args, bs_stream_t stream);

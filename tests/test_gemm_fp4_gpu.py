@@ -15,18 +15,17 @@ from tests.helpers import gemm_errors, tight_errors
 pytestmark = pytest.mark.gpu
 
 # The library runs FP4 GEMMs on CTA pairs (256 x 256 tiles) by default; the
-# one-CTA kernel (128 x 256) and the 128-deep K stages are selected per call
-# through the environment.  Every case runs on each kernel variant.
-VARIANTS = {"pair": ("1", "256"), "one_cta": ("0", "256"), "pair_bk128": ("1", "128"),
-            "one_cta_bk128": ("0", "128")}
+# one-CTA kernel (128 x 256) and the 128-deep K stages are per-call choices
+# (bs_gemm_args.fp4_kernel / fp4_stage_k).  Every case runs on each variant.
+VARIANTS = {"pair": (2, 256), "one_cta": (1, 256), "pair_bk128": (2, 128), "one_cta_bk128": (1, 128)}
 
 
 @pytest.fixture(autouse=True, params=sorted(VARIANTS))
-def fp4_variant(request, monkeypatch):
-    pair, bk = VARIANTS[request.param]
-    monkeypatch.setenv("BSGEMM_FP4_PAIR", pair)
-    monkeypatch.setenv("BSGEMM_FP4_BK", bk)
-    return request.param
+def fp4_variant(request):
+    kernel, bk = VARIANTS[request.param]
+    import fp8_quantized_gemm_q4_gb300 as bs
+    with bs.kernel_options(fp4_kernel=kernel, fp4_stage_k=bk):
+        yield request.param
 
 
 def run_case(bs, x, w, out_dtype, alpha=1.0, col_scale=None, lora=None, bias=None, rows=None):
@@ -112,18 +111,19 @@ def test_full_size_lowrank_sampled_rows(cuda_lib, fp4_variant):
     assert ok and tok, (ratio, rel, tratio)
 
 
-@pytest.mark.parametrize("half_tail", ["1", "0"])
-def test_short_last_wave_half_tiles(cuda_lib, monkeypatch, half_tail):
+@pytest.mark.parametrize("half_tail", [1, 2])
+def test_short_last_wave_half_tiles(cuda_lib, half_tail):
     """80 pair tiles (2560 x 2048) on at most 76 pairs: the last 4 tiles run as
-    eight 256 x 128 half tiles on CTA pairs (BSGEMM_FP4_HALF_TAIL=0: whole tiles)."""
-    monkeypatch.setenv("BSGEMM_FP4_HALF_TAIL", half_tail)
+    eight 256 x 128 half tiles on CTA pairs (fp4_half_tail = 1, the default;
+    2 keeps whole tiles)."""
     d = workloads.dense_lowrank(M=2560, N=2048, K=256)
-    for kw in ({}, {"lora": (d["lora_a"], d["lora_b"]), "bias": d["bias"]}):
-        for dt in (torch.bfloat16, torch.float32):
-            if kw and dt == torch.float32:
-                continue
-            ok, ratio, rel, tok, tratio = run_case(cuda_lib, d["x"], d["w"], dt, **kw)
-            assert ok and tok, (dt, bool(kw), ratio, rel, tratio)
+    with cuda_lib.kernel_options(fp4_half_tail=half_tail):
+        for kw in ({}, {"lora": (d["lora_a"], d["lora_b"]), "bias": d["bias"]}):
+            for dt in (torch.bfloat16, torch.float32):
+                if kw and dt == torch.float32:
+                    continue
+                ok, ratio, rel, tok, tratio = run_case(cuda_lib, d["x"], d["w"], dt, **kw)
+                assert ok and tok, (dt, bool(kw), ratio, rel, tratio)
 
 
 def test_empty_m_is_noop(cuda_lib):

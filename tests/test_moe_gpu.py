@@ -20,13 +20,14 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(params=["pair", "pair_whole", "one_cta"])
-def fp4_kernel(request, monkeypatch):
+def fp4_kernel(request):
     """Grouped GEMMs on CTA pairs with the small experts (<= 128 rows) in a
     second one-CTA launch (default), on CTA pairs alone, or on the one-CTA
-    kernel alone."""
-    monkeypatch.setenv("BSGEMM_FP4_PAIR", "0" if request.param == "one_cta" else "1")
-    monkeypatch.setenv("BSGEMM_FP4_TAILS", "0" if request.param == "pair_whole" else "1")
-    return request.param
+    kernel alone (bs_gemm_args.fp4_kernel / fp4_small_experts)."""
+    import fp8_quantized_gemm_q4_gb300 as bs
+    with bs.kernel_options(fp4_kernel=1 if request.param == "one_cta" else 2,
+                           fp4_small_experts=2 if request.param == "pair_whole" else 1):
+        yield request.param
 
 
 def test_dispatch_hand_case(cuda_lib):
