@@ -30,6 +30,8 @@ sys.path.insert(0, ROOT)
 
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # dense tensor peaks, profiling recipe table
 NOMINAL_FP8_OVER_BF16 = 4.5 / 2.25
+NOMINAL_FP4_TFLOPS = 13500.0           # GB300 dense FP4 / FP8 tensor peaks (nominal, per GPU)
+NOMINAL_FP8_TFLOPS = 4500.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -98,6 +100,31 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------
+def tensor_roofline(kernel, flops, ms, peaks, source, ratio, nominal_tflops, fmt):
+    """Tensor-bound roofline: the FLOPs of one launch over its measured time,
+    against the measured bf16 peak times the nominal ratio of `fmt` to bf16,
+    with the fraction of the nominal dense peak beside it."""
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"] * ratio
+    return {"bound": "tensor", "kernel": kernel, "achieved": round(tflops, 1), "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+            "peak_source": f"{source} bf16 burst x {ratio:g} (nominal {fmt}/bf16)",
+            "nominal": {"peak": nominal_tflops, "frac": round(tflops / nominal_tflops, 4),
+                        "source": f"GB300 nominal dense {fmt}"},
+            "algorithmic_flops_per_launch": flops, "kernel_ms": round(ms, 5)}
+
+
+def hbm_roofline(kernel, nbytes, ms, peaks, source):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak = peaks["hbm_gbs"]
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(gbs / peak, 4), "peak_source": f"{source} HBM copy",
+            "algorithmic_bytes_per_launch": nbytes, "kernel_ms": round(ms, 5)}
+
+
+# ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
 class DenseLowRank:
@@ -145,7 +172,7 @@ class DenseLowRank:
         else:
             self.at = self.bt = self.bias = self.lt = None
             self.out = torch.empty((M, N), dtype=torch.float32, device=dev)
-        self.launches_per_step = 2 + (0 if self.tiny else 1)
+        self.launches_per_step = 2   # fused quantizer (+ low-rank factor), GEMM
         self.kernel_src = "fp8_quantized_gemm_q4_gb300/csrc/gemm_fp4_pair.cu"
         self.bytes_in = self.x.numel() * self.x.element_size()
         self.bytes_out = self.out.numel() * self.out.element_size()
@@ -163,12 +190,8 @@ class DenseLowRank:
         return self.out
 
     def roofline(self, gemm_ms, peaks, source):
-        tflops = self.flops / (gemm_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
-        return {"bound": "tensor", "kernel": "fp4_pair_kernel", "achieved": round(tflops, 1),
-                "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                "peak_source": f"{source} bf16 burst x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/bf16)",
-                "algorithmic_flops_per_launch": self.flops, "kernel_ms": round(gemm_ms, 5)}
+        return tensor_roofline("fp4_pair_kernel", self.flops, gemm_ms, peaks, source, NOMINAL_FP4_OVER_BF16,
+                               NOMINAL_FP4_TFLOPS, "FP4")
 
     # --- CPU oracle arm
     def oracle_sample(self, rows, cols, nthreads):
@@ -239,17 +262,9 @@ class Fp8Sweep:
 
     def roofline(self, gemm_ms, peaks, source):
         if self.M <= 128:
-            gbs = self.gemm_bytes / (gemm_ms * 1e-3) / 1e9
-            peak = peaks["hbm_gbs"]
-            return {"bound": "hbm", "kernel": "fp8_gemm_kernel", "achieved": round(gbs, 1), "peak": peak,
-                    "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": f"{source} HBM copy",
-                    "algorithmic_bytes_per_launch": self.gemm_bytes, "kernel_ms": round(gemm_ms, 5)}
-        tflops = self.flops / (gemm_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
-        return {"bound": "tensor", "kernel": "fp8_gemm_kernel", "achieved": round(tflops, 1), "peak": round(peak, 1),
-                "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                "peak_source": f"{source} bf16 burst x {NOMINAL_FP8_OVER_BF16:g} (nominal FP8/bf16)",
-                "algorithmic_flops_per_launch": self.flops, "kernel_ms": round(gemm_ms, 5)}
+            return hbm_roofline("fp8_gemm_kernel", self.gemm_bytes, gemm_ms, peaks, source)
+        return tensor_roofline("fp8_gemm_kernel", self.flops, gemm_ms, peaks, source, NOMINAL_FP8_OVER_BF16,
+                               NOMINAL_FP8_TFLOPS, "FP8")
 
     def oracle_sample(self, rows, cols, nthreads):
         import oracle
@@ -328,9 +343,7 @@ class MoEWorkload:
         # finalize 2 (cast, zero); each grouped GEMM is two launches on CTA
         # pairs with the small experts split off (the library's default), one
         # otherwise
-        pair = os.environ.get("BSGEMM_FP4_PAIR", "1") != "0"
-        tails = os.environ.get("BSGEMM_FP4_TAILS", "1") != "0"
-        g = 2 if (pair and tails) else 1
+        g = 2   # CTA pairs plus the one-CTA launch for experts of <= 128 rows (the library's default)
         self.launches_per_step = (5 if self.layer.h_quant == "fused" else 6) + 2 * g + \
             (3 if self.combine == "rows" else 2)
         self.bytes_in = self.x.numel() * 2 + self.ids.numel() * 4 + self.w.numel() * 4
@@ -356,14 +369,24 @@ class MoEWorkload:
             gemm_events[1].record()
         return out
 
+    def algorithmic_bytes(self):
+        """Bytes the layer must move at least: every expert's FP4 weights and
+        their scales (read once), the bf16 activations in, the routing, the
+        bf16 output."""
+        E, H, F, T, k = self.E, self.H, self.F, self.T, self.k
+        w = E * (2 * F * H + H * F)
+        return w // 2 + w // 16 + T * H * 2 + T * k * 8 + T * H * 2
+
     def roofline(self, layer_ms, peaks, source):
-        tflops = self.flops / (layer_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
-        return {"bound": "tensor", "kernel": "whole layer (grouped fp4_pair_kernel x2 + quantize + dispatch + " + ("combine" if self.combine == "rows" else "finalize") + ")",
-                "achieved": round(tflops, 1), "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                "peak_source": f"{source} bf16 burst x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4/bf16)",
-                "algorithmic_flops_per_launch": self.flops, "kernel_ms": round(layer_ms, 5),
-                "expert_load": getattr(self, "load_hist", None)}
+        kern = ("whole layer (grouped fp4_pair_kernel x2 + quantize + dispatch + " +
+                ("combine" if self.combine == "rows" else "finalize") + ")")
+        r = tensor_roofline(kern, self.flops, layer_ms, peaks, source, NOMINAL_FP4_OVER_BF16, NOMINAL_FP4_TFLOPS,
+                            "FP4")
+        h = hbm_roofline(kern, self.algorithmic_bytes(), layer_ms, peaks, source)
+        r["hbm"] = {k: h[k] for k in ("achieved", "peak", "unit", "frac", "peak_source",
+                                      "algorithmic_bytes_per_launch")}
+        r["expert_load"] = getattr(self, "load_hist", None)
+        return r
 
     def oracle_sample(self, rows, cols, nthreads):
         """`rows` tokens through the oracle's layer (cols ignored)."""
@@ -462,10 +485,13 @@ def job_throughput(work_per_rank, world, step_ms):
     return world * work_per_rank / (step_ms * 1e-3)
 
 
-def run_ours(args, wl, rank, world, dev, peaks, source):
+def time_steps(args, wl, world, dev):
+    """W untimed warm-up steps, then K steps each bracketed by CUDA events on
+    the launching stream (L2 flushed before every step, outside the events),
+    with the GPU clocks sampled during the timed region.  Returns (step ms,
+    dominant-kernel ms, clocks, wall seconds), the times max-over-ranks."""
     import torch
     import torch.distributed as dist
-    wl.setup(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -493,9 +519,50 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
+    del flush
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     gemm_ms = sum(a.elapsed_time(b) for a, b in gev) / K
     step_ms, gemm_ms = max_over_ranks([step_ms, gemm_ms], dev)
+    return step_ms, gemm_ms, clk, wall
+
+
+def check_device_status():
+    import fp8_quantized_gemm_q4_gb300 as bs
+    st, detail = bs.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
+
+
+# The other configurations of the metric ("block-scaled FP4/FP8 GEMM TFLOPS &
+# % of GB300 dense peak; MoE layer us"), timed in the same run as the dense
+# headline and reported beside it.
+EXTRAS = ("moe_small", "moe_large", "fp8_m16", "fp8_m4096")
+
+
+def run_extra(args, name, world, dev, peaks, source):
+    import torch
+    wl = WORKLOADS[name]()
+    wl.setup(dev)
+    step_ms, kern_ms, clk, wall = time_steps(args, wl, world, dev)
+    check_device_status()
+    roof = wl.roofline(kern_ms, peaks, source)
+    roof["traffic"] = traffic_for(wl.kernel_src, wl.name) if hasattr(wl, "kernel_src") else None
+    d = {"metric": wl.metric, "value": round(job_throughput(wl.flops, world, step_ms) / 1e12, 2), "unit": wl.unit,
+         "workload": wl.name, "ms_per_step": round(step_ms, 5), "us_per_step": round(step_ms * 1e3, 2),
+         "kernel_ms": round(kern_ms, 5), "gpu_launches": args.steps * wl.launches_per_step,
+         "roofline": roof, "clocks": clk, "timed_wall_s": round(wall, 3)}
+    del wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return d
+
+
+def run_ours(args, wl, rank, world, dev, peaks, source):
+    import torch
+    wl.setup(dev)
+    stream = torch.cuda.current_stream()
+    K = args.steps
+    step_ms, gemm_ms, clk, wall = time_steps(args, wl, world, dev)
 
     # end to end through the public API with pinned host buffers: every input
     # of the step is copied host -> device (workloads with several inputs name
@@ -524,10 +591,7 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
     e2e_ms = e0.elapsed_time(e1) / Ke
     (e2e_ms,) = max_over_ranks([e2e_ms], dev)
 
-    import fp8_quantized_gemm_q4_gb300 as bs
-    st, detail = bs.device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
+    check_device_status()
     value = job_throughput(wl.flops, world, step_ms) / 1e12
     roof = wl.roofline(gemm_ms, peaks, source)
     roof["traffic"] = traffic_for(getattr(wl, "kernel_src", "fp8_quantized_gemm_q4_gb300/csrc/gemm_fp4.cu"),
@@ -551,6 +615,12 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    if args.workload == "dense_lowrank" and not args.no_extras:
+        h = getattr(wl, "h", None)
+        del wl, h
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["extra"] = {name: run_extra(args, name, world, dev, peaks, source) for name in EXTRAS}
     return line
 
 
@@ -611,6 +681,9 @@ def main():
     ap.add_argument("--workload", default="dense_lowrank", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="dense headline only (by default the MoE layers and the FP8 M=16 / M=4096 shapes are "
+                         "timed in the same run and reported under 'extra')")
     ap.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (default min(steps, 100))")
     ap.add_argument("--moe-combine", choices=["rows", "atomic"], default="rows",
                     help="MoE routed combine: weighted rows + per-token sum, or fp32 reductions")
