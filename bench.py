@@ -34,6 +34,7 @@ NOMINAL_FP4_TFLOPS = 13500.0           # GB300 dense FP4 / FP8 tensor peaks (nom
 NOMINAL_FP8_TFLOPS = 4500.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+SPIN_HZ = 2.1e9                        # spin-kernel cycles per second (SM clock, upper bound)
 
 
 def load_peaks():
@@ -255,7 +256,9 @@ class Fp8Sweep:
         bs.q8_quantize(x, out=(self.xq, self.xs))
         if gemm_events:
             gemm_events[0].record()
-        bs.gemm_fp8(self.xq, self.xs, self.wq, self.ws, out=self.out)
+        # the weights are quantized once, offline: the GEMM may start loading
+        # them while the activation quantizer still runs
+        bs.gemm_fp8(self.xq, self.xs, self.wq, self.ws, out=self.out, weights_ready=True)
         if gemm_events:
             gemm_events[1].record()
         return self.out
@@ -486,20 +489,37 @@ def job_throughput(work_per_rank, world, step_ms):
 
 
 def time_steps(args, wl, world, dev):
-    """W untimed warm-up steps, then K steps each bracketed by CUDA events on
-    the launching stream (L2 flushed before every step, outside the events),
-    with the GPU clocks sampled during the timed region.  Returns (step ms,
-    dominant-kernel ms, clocks, wall seconds), the times max-over-ranks."""
+    """W untimed warm-up steps, then two timed passes of K steps, each step
+    bracketed by CUDA events on the launching stream (L2 flushed before every
+    step, outside the events), with the GPU clocks sampled during both:
+      - the step pass records no event inside a step, so a kernel may start
+        under the tail of the one before it (programmatic dependent launch)
+        exactly as in use: its times give ms_per_step;
+      - the kernel pass also records events around the dominant kernel (which
+        serialises it against its neighbours): its times give the kernel's
+        own duration for the roofline.
+    Returns (step ms, dominant-kernel ms, clocks, wall seconds), the times
+    max-over-ranks."""
     import torch
     import torch.distributed as dist
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
+
+    def flush_l2(i):
+        # Write a buffer larger than L2, then read another one: the step's
+        # operands are evicted, and what L2 holds afterwards is clean, so the
+        # timed kernels do not pay for writing back the flush's dirty lines.
+        flush.fill_(float(i))
+        clean.sum()
+
+    for i in range(args.warmup):
+        flush_l2(i)
         wl.step()
     torch.cuda.synchronize()
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[torch.cuda.current_device()]))
@@ -509,17 +529,25 @@ def time_steps(args, wl, world, dev):
     clocks.start()
     time.sleep(0.3)  # let the sampler start before the timed region
     wall0 = time.perf_counter()
-    for i in range(K):
-        flush.fill_(float(i))          # L2 flush, outside the per-step events
-        ev[i][0].record(stream)
-        wl.step(gemm_events=gev[i])
-        ev[i][1].record(stream)
+    for events, kernel_events in ((ev, None), (kev, gev)):
+        # Hold the stream with a spin kernel while the host enqueues the K
+        # steps, so that the steps then run back to back: the events time the
+        # GPU's work, not gaps in which the device waited for host-side
+        # launches (binding and tensor-map set-up take tens of microseconds
+        # per call, as long as a whole decode step).  The end-to-end figure
+        # keeps them.
+        torch.cuda._sleep(int((K * 400e-6 + 5e-3) * SPIN_HZ))
+        for i in range(K):
+            flush_l2(i)                    # L2 flush, outside the per-step events
+            events[i][0].record(stream)
+            wl.step(gemm_events=None if kernel_events is None else kernel_events[i])
+            events[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    del flush
+    del flush, clean
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     gemm_ms = sum(a.elapsed_time(b) for a, b in gev) / K
     step_ms, gemm_ms = max_over_ranks([step_ms, gemm_ms], dev)
@@ -549,7 +577,7 @@ def run_extra(args, name, world, dev, peaks, source):
     roof["traffic"] = traffic_for(wl.kernel_src, wl.name) if hasattr(wl, "kernel_src") else None
     d = {"metric": wl.metric, "value": round(job_throughput(wl.flops, world, step_ms) / 1e12, 2), "unit": wl.unit,
          "workload": wl.name, "ms_per_step": round(step_ms, 5), "us_per_step": round(step_ms * 1e3, 2),
-         "kernel_ms": round(kern_ms, 5), "gpu_launches": args.steps * wl.launches_per_step,
+         "kernel_ms": round(kern_ms, 5), "gpu_launches": 2 * args.steps * wl.launches_per_step,
          "roofline": roof, "clocks": clk, "timed_wall_s": round(wall, 3)}
     del wl
     torch.cuda.synchronize()
@@ -601,14 +629,16 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": wl.higher_is_better,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, pages' shapes)",
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
-                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, then {L2_FLUSH_BYTES >> 20} MiB "
+                         "read so L2 holds clean lines; outside the step events)",
+                   "enqueue": "timed steps queued behind a GPU spin (device time without host launch gaps)",
                    "parallelism": f"replicas x{world}",
                    **({"moe_combine": wl.combine, "cuda_graph": wl.graph, "h_quant": wl.layer.h_quant}
                       if hasattr(wl, "combine") else {})},
         "e2e": {"value": round(job_throughput(wl.flops, world, e2e_ms) / 1e12, 2), "unit": wl.unit,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": wl.bytes_in,
                 "d2h_bytes_per_step": wl.bytes_out},
-        "gpu_launches": K * wl.launches_per_step,
+        "gpu_launches": 2 * K * wl.launches_per_step,   # two timed passes
         "roofline": roof,
         "clocks": clk,
         "timed_wall_s": round(wall, 3),

@@ -47,8 +47,9 @@ class GemmArgs(ctypes.Structure):
         ("lora_b_t", ctypes.c_void_p), ("r", ctypes.c_int), ("bias", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("out_dtype", ctypes.c_int), ("ldo", ctypes.c_int64), ("num_sms", ctypes.c_int),
         ("n_chunk_blocks", ctypes.c_int), ("fp4_kernel", ctypes.c_int), ("fp4_stage_k", ctypes.c_int),
-        ("fp4_small_experts", ctypes.c_int), ("fp4_half_tail", ctypes.c_int), ("fp8_split_k", ctypes.c_int),
-        ("wait_timeout_us", ctypes.c_int),
+        ("fp4_small_experts", ctypes.c_int), ("fp4_half_tail", ctypes.c_int), ("fp8_stream_k", ctypes.c_int),
+        ("wait_timeout_us", ctypes.c_int), ("weights_ready", ctypes.c_int), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -56,7 +57,7 @@ class GemmArgs(ctypes.Structure):
 # include/bsgemm.h.  Every GEMM call of this binding fills them from the
 # options active on the calling thread: the defaults, or those of an enclosing
 # ``with kernel_options(...)`` block.
-_CHOICES = ("fp4_kernel", "fp4_stage_k", "fp4_small_experts", "fp4_half_tail", "fp8_split_k", "wait_timeout_us")
+_CHOICES = ("fp4_kernel", "fp4_stage_k", "fp4_small_experts", "fp4_half_tail", "fp8_stream_k", "wait_timeout_us")
 FP4_ONE_CTA, FP4_PAIR = 1, 2
 _tls = threading.local()
 
@@ -113,6 +114,8 @@ def load(path: str | None = None):
         lib.q8_quantize.argtypes = [P, I, I64, I64, I64, I, P, P, P]
         lib.bs_gemm.restype = I
         lib.bs_gemm.argtypes = [ctypes.POINTER(GemmArgs), P]
+        lib.bs_gemm_workspace_bytes.restype = SZ
+        lib.bs_gemm_workspace_bytes.argtypes = [ctypes.POINTER(GemmArgs)]
         lib.bs_grouped_gemm.restype = I
         lib.bs_grouped_gemm.argtypes = [ctypes.POINTER(GemmArgs), I, P, P, I, P, P, P, I64, P]
         lib.bs_moe_rows_bound.restype = I64
@@ -254,14 +257,39 @@ def gemm_fp4(a, sfa, b, sfb, K: int, out_dtype=torch.bfloat16, alpha: float = 1.
     return out
 
 
-def gemm_fp8(a, sa, b, sb, out_dtype=torch.bfloat16, out=None, num_sms: int = 0, stream=None):
-    """Dense FP8 GEMM with 1x128 A scales [K/128, M] and 128x128 B scales."""
+# Workspaces of the FP8 stream-K schedule, one per (device, stream): calls on
+# one stream run in order, so they may share it; the library leaves it zeroed
+# where the next call reads it.
+_workspaces: dict = {}
+
+
+def _workspace(device, stream, nbytes: int):
+    key = (device.index, stream.cuda_stream)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def gemm_fp8(a, sa, b, sb, out_dtype=torch.bfloat16, out=None, num_sms: int = 0, weights_ready: bool = False,
+             stream=None):
+    """Dense FP8 GEMM with 1x128 A scales [K/128, M] and 128x128 B scales.
+    ``weights_ready``: the kernel just before this call on the stream does not
+    write ``b`` / ``sb``, so the weight loads may start before it finishes."""
     M, K = a.shape
     N = b.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
     g = _args(FMT_FP8, a, sa, b, sb, M, N, K, out, num_sms=num_sms)
-    _check(load().bs_gemm(ctypes.byref(g), _stream(stream)))
+    g.weights_ready = 1 if weights_ready else 0
+    lib = load()
+    nbytes = int(lib.bs_gemm_workspace_bytes(ctypes.byref(g)))
+    if nbytes:
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        ws = _workspace(a.device, s, nbytes)
+        g.workspace, g.workspace_bytes = ws.data_ptr(), ws.numel()
+    _check(lib.bs_gemm(ctypes.byref(g), _stream(stream)))
     return out
 
 

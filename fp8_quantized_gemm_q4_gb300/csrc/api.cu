@@ -262,7 +262,9 @@ static bs_status check_choices(const bs_gemm_args* a) {
     return fail(BS_ERR_INVALID, "fp4_small_experts=%d (0, 1 or 2)", a->fp4_small_experts);
   if (a->fp4_half_tail < 0 || a->fp4_half_tail > 2)
     return fail(BS_ERR_INVALID, "fp4_half_tail=%d (0, 1 or 2)", a->fp4_half_tail);
-  if (a->fp8_split_k < 0 || a->fp8_split_k > 2) return fail(BS_ERR_INVALID, "fp8_split_k=%d (0, 1 or 2)", a->fp8_split_k);
+  if (a->fp8_stream_k < 0 || a->fp8_stream_k > 2)
+    return fail(BS_ERR_INVALID, "fp8_stream_k=%d (0, 1 or 2)", a->fp8_stream_k);
+  if (a->weights_ready < 0 || a->weights_ready > 1) return fail(BS_ERR_INVALID, "weights_ready=%d (0 or 1)", a->weights_ready);
   if (a->wait_timeout_us < 0) return fail(BS_ERR_INVALID, "wait_timeout_us < 0");
   return BS_OK;
 }
@@ -383,6 +385,56 @@ static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_
   return BS_OK;
 }
 
+// Launch plan of an FP8 GEMM: tile width (token columns), tile count, and
+// for fewer tiles than SMs the stream-K split: grid G = min(SMs, units), the
+// most CTAs sharing one tile (maxc) and the workspace it needs (partials,
+// then one counter per tile).
+constexpr size_t kStreamKCounterBytes = 4096;
+struct Fp8Plan {
+  int tile_n;
+  long long tiles;
+  int grid;
+  bool stream_k;
+  int maxc;
+  size_t ws_bytes, counters_off;  // counters at the start, then the partials
+};
+static Fp8Plan fp8_plan(const bs_gemm_args* a, int sms) {
+  Fp8Plan P;
+  memset(&P, 0, sizeof P);
+  P.tile_n = bsk::fp8_tile_n(a->M);
+  P.tiles = ((a->N + 127) / 128) * ((a->M + P.tile_n - 1) / P.tile_n);
+  const long long nkb = a->K / 128;
+  P.grid = (int)(P.tiles < sms ? P.tiles : sms);
+  P.stream_k = a->fp8_stream_k != 2 && P.tiles < sms && P.tiles <= (long long)(kStreamKCounterBytes / sizeof(int)) &&
+               nkb > 1;
+  if (!P.stream_k) return P;
+  const long long U = P.tiles * nkb;
+  const long long G = U < sms ? U : sms;
+  P.grid = (int)G;
+  auto owner = [&](long long u) { return ((u + 1) * G - 1) / U; };
+  for (long long t = 0; t < P.tiles; ++t) {
+    const long long n = owner(t * nkb + nkb - 1) - owner(t * nkb) + 1;
+    if (n > P.maxc) P.maxc = (int)n;
+  }
+  // The counters sit in a fixed region at the start of the workspace (one per
+  // tile; stream-K runs only with fewer tiles than SMs, so 1024 always
+  // suffice) and the partials after it, so calls of different shapes sharing
+  // one workspace never find another call's partials where their counters go.
+  P.counters_off = 0;
+  const size_t parts = (size_t)P.tiles * (size_t)P.maxc * 128 * (size_t)P.tile_n * sizeof(float);
+  P.ws_bytes = kStreamKCounterBytes + parts;
+  return P;
+}
+
+size_t bs_gemm_workspace_bytes(const bs_gemm_args* a) {
+  if (!a || a->fmt != BS_FMT_FP8 || a->M <= 0 || a->N <= 0 || a->K < 128 || a->num_sms < 0) return 0;
+  int sms = 0;
+  if (!device_info(nullptr, &sms)) return 0;
+  if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
+  const Fp8Plan P = fp8_plan(a, sms);
+  return P.stream_k ? P.ws_bytes : 0;
+}
+
 bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
   bs_status st = check_common(a, false);
   if (st != BS_OK) return st;
@@ -449,16 +501,20 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     L.p.out_bf16 = a->out_dtype == BS_DTYPE_BF16;
     L.p.ldo = a->ldo;
     L.p.status = status;
-    L.swap_ab = true;
-    const long long tiles = ((a->N + 127) / 128) * ((a->M + L.tile_n - 1) / L.tile_n);
-    L.grid = (int)(tiles < sms ? tiles : sms);
-    // Decode shapes with few tiles: two CTAs per tile, each streaming half of
-    // K (split-K over a 2-CTA cluster, partials reduced through DSMEM).
-    L.p.splits = 1;
+    const Fp8Plan P = fp8_plan(a, sms);
     L.p.wait_ns = wait_ns(a);
-    if (L.tile_n <= 32 && tiles * 2 <= sms && a->K >= 256 && a->fp8_split_k != 2) {
-      L.p.splits = 2;
-      L.grid = (int)(2 * tiles);
+    L.p.pre_b = a->weights_ready == 1 ? bsk::fp8_stages(P.tile_n) : 0;
+    L.grid = P.grid;
+    if (P.stream_k && a->workspace) {
+      if (!aligned16(a->workspace)) return fail(BS_ERR_ALIGN, "workspace must be 16-byte aligned");
+      if (a->workspace_bytes < P.ws_bytes)
+        return fail(BS_ERR_INVALID, "workspace too small (%zu < %zu bytes)", a->workspace_bytes, P.ws_bytes);
+      L.p.stream_k = 1;
+      L.p.maxc = P.maxc;
+      L.p.counters = static_cast<int*>(a->workspace);
+      L.p.work = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + kStreamKCounterBytes);
+    } else {
+      L.grid = (int)(P.tiles < sms ? P.tiles : sms);  // one CTA per tile
     }
     cudaError_t e = bsk::launch_fp8_gemm(L, s);
     if (e != cudaSuccess) return cuda_fail(e, "FP8 GEMM launch");

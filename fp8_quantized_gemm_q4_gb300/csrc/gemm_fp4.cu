@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitGuard wg{abort_flag, p.status, p.wait_ns};
 
   if (threadIdx.x == 0) {
+    griddep_launch_dependents();
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
@@ -238,6 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(sm.tmem_base, G::kTmemAlloc);
     tmem_relinquish();
   }
+  // Everything above only touched this CTA's own resources: the operands,
+  // expert tables and outputs may belong to the kernel just before this one
+  // on the stream (programmatic dependent launch), so wait for it here.
+  griddep_wait();
   if (warp == 3) {
     // Tile table.  Dense: closed form.  Grouped: validate the offset table and
     // prefix-sum the tiles of each expert.
@@ -576,8 +581,7 @@ static cudaError_t launch_one(const Fp4Launch& L, cudaStream_t stream) {
   const int smem = fp4_smem_total(kLora ? G::kShapeLora : G::kShapeNoLora, kStages) + kAlign;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, kThreads, smem, stream>>>(L.tmA, L.tmB, L.tmT, L.tmL, L.p);
-  return cudaGetLastError();
+  return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)smem, stream, 1, L.tmA, L.tmB, L.tmT, L.tmL, L.p);
 }
 
 template <int BK>

@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
 
   if (threadIdx.x == 0) {
+    griddep_launch_dependents();
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -276,6 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(tmem_base, kTmemAlloc);
     tmem_relinquish_pair();
   }
+  // Everything above only touched this CTA's own resources: the operands,
+  // expert tables and outputs may belong to the kernel just before this one
+  // on the stream (programmatic dependent launch), so wait for it here.
+  griddep_wait();
   if (warp == 3) {
     if (p.E == 0) {
       int nfull;
@@ -689,20 +694,8 @@ static cudaError_t launch_one(const Fp4PairLaunch& L, cudaStream_t stream) {
   const int smem = fp4_smem_total(kLora ? G::kShapeLora : G::kShapeNoLora, kStages) + kAlign;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)L.grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, L.base.tmA, L.base.tmB, L.base.tmT, L.base.tmL, L.tmSfa, L.tmSfb, L.tmO,
-                            L.base.p);
+  return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)smem, stream, 2, L.base.tmA, L.base.tmB, L.base.tmT,
+                       L.base.tmL, L.tmSfa, L.tmSfb, L.tmO, L.base.p);
 }
 
 template <int BK>

@@ -16,12 +16,32 @@
 // weight-scale block per tile), the tokens are the MMA's N (16 .. 128), so the
 // decode shapes (M = 1 .. 16, "DeepGEMM teardown" section 1.2: M of 1 to 16
 // idles most of a normal tile) stream the weights through full 128-row MMAs.
-// One persistent CTA per SM walks (weight block, token block) tiles.
+//
+// Work is a list of (tile, K-block range) segments per CTA:
+//  - tiles >= CTAs: each persistent CTA takes whole tiles t = c, c + G, ...
+//  - tiles <  CTAs (decode: N = 7168 gives 56 weight tiles for 152 SMs):
+//    stream-K ("DeepGEMM teardown" sections 1.2 and 3.2: small M leaves SMs
+//    idle; wave scheduling).  The tiles' K blocks form one sequence of units
+//    u = t * nkb + kb that is cut into G equal contiguous ranges, one per CTA,
+//    so every SM streams the same share of the weights.  A tile cut between
+//    CTAs is finished by whichever of them arrives last: each writes its fp32
+//    partial to the caller's workspace and counts itself in on the tile's
+//    counter; the last one sums the partials in the fixed order of their K
+//    ranges (deterministic whatever the arrival order), writes the output and
+//    resets the counter to zero for the next call.  Nobody waits for anybody.
+//
+// Roles (384 threads):
 //   warp 0      TMA producer: weight tile [128 x 128] + token tile [TN x 128]
-//   warp 1      tensor-memory allocator, single-lane MMA issuer
-//               (tcgen05.mma kind::f8f6f4, K = 32 per instruction)
+//   warp 1      tensor-memory allocator, MMA issuer (tcgen05.mma kind::f8f6f4,
+//               K = 32 per instruction)
 //   warps 4-11  promotion / epilogue: two warps per 32-lane quarter, each
 //               owning half of the TN token columns of its weight rows
+//
+// Programmatic dependent launch: the prologue runs before griddep_wait().
+// With p.pre_b > 0 the producer also issues the weight loads of its first
+// p.pre_b stages before waiting (the caller has promised that the kernel
+// before this one on the stream does not write the weights or their scales),
+// so the weight stream starts while the activation quantizer still runs.
 #include "budget.hpp"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -38,17 +58,14 @@ constexpr int kMaxStages = 12;
 
 constexpr int KBC = 32;   // K blocks whose scales are staged together
 
-template <int TN, int kSplit>
+template <int TN>
 struct Cfg {
   static constexpr int kStageBytes = round_up(BM * BK + TN * BK, kAlign);
   // two staging buffers of [KBC][TN] activation scales + [KBC] weight scales
   static constexpr int kScaleBytes = round_up(2 * (KBC * TN + KBC) * 4, kAlign);
-  // split-K partner's partial sums [BM rows][TN], written through DSMEM
-  // (split mode only: elsewhere the bytes go to the stage ring)
-  static constexpr int kRedBytes = kSplit > 1 ? round_up(BM * TN * 4, kAlign) : 0;
-  static constexpr Fp8TileShape kShape{BM, TN, BK, kMisc + kScaleBytes + kRedBytes + kAlign};
+  static constexpr Fp8TileShape kShape{BM, TN, BK, kMisc + kScaleBytes + kAlign};
   static constexpr int kStages = fp8_main_stages(kShape) < kMaxStages ? fp8_main_stages(kShape) : kMaxStages;
-  static constexpr int kSmem = kStages * kStageBytes + kScaleBytes + kRedBytes + kMisc + kAlign;
+  static constexpr int kSmem = kStages * kStageBytes + kScaleBytes + kMisc + kAlign;
   // partial slots: as many K blocks as tensor memory holds (up to 16), so
   // the tensor core can run that far ahead of the promotion warps
   static constexpr int kSlots = (512 / TN) < 16 ? (512 / TN) : 16;
@@ -59,23 +76,60 @@ struct Cfg {
   static_assert(kSlots >= 2 && kSlots * TN <= kTmemCols && kTmemCols <= bsk::kTmemCols, "tmem budget");
 };
 
-// kSplit == 2: a cluster of two CTAs shares one tile, each streaming half of
-// the K blocks; the peer's fp32 partials reach the leader through distributed
-// shared memory at the end (decode shapes: twice as many SMs pull weights).
-template <int TN, int kSplit>
+// A CTA's piece of work: K blocks [kb0, kb1) of tile t.
+struct Seg {
+  int t, kb0, kb1;
+};
+
+// The CTA's segments in order; every role walks the same sequence.
+template <bool kStreamK>
+struct Walk {
+  long long cur, end;
+  int step;
+  __device__ __forceinline__ Walk(const Fp8Params& p, int total, int nkb) {
+    if (kStreamK) {
+      const long long U = (long long)total * nkb;
+      cur = (long long)blockIdx.x * U / gridDim.x;
+      end = (long long)(blockIdx.x + 1) * U / gridDim.x;
+      step = 0;
+    } else {
+      cur = blockIdx.x;
+      end = total;
+      step = (int)gridDim.x;
+    }
+  }
+  __device__ __forceinline__ bool next(const Fp8Params& p, int nkb, Seg& s) {
+    if (cur >= end) return false;
+    if (kStreamK) {
+      s.t = (int)(cur / nkb);
+      s.kb0 = (int)(cur % nkb);
+      s.kb1 = (int)min((long long)nkb, s.kb0 + (end - cur));
+      cur += s.kb1 - s.kb0;
+    } else {
+      s.t = (int)cur;
+      s.kb0 = 0;
+      s.kb1 = nkb;
+      cur += step;
+    }
+    return true;
+  }
+};
+
+// CTA whose stream-K range holds unit u (ranges [c U / G, (c + 1) U / G)).
+__device__ __forceinline__ int sk_owner(long long u, long long U, int G) { return (int)(((u + 1) * G - 1) / U); }
+
+template <int TN, bool kStreamK>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const Fp8Params p) {
-  using C = Cfg<TN, kSplit>;
+  using C = Cfg<TN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kAlign - 1) &
                                              ~static_cast<uintptr_t>(kAlign - 1));
   uint8_t* stages = base;
   float* ssa = reinterpret_cast<float*>(base + C::kStages * C::kStageBytes);  // [2][KBC][TN]
   float* ssb = ssa + 2 * KBC * TN;                                            // [2][KBC]
-  float* red = reinterpret_cast<float*>(base + C::kStages * C::kStageBytes + C::kScaleBytes);  // [BM][TN]
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(base + C::kStages * C::kStageBytes + C::kScaleBytes + C::kRedBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kStages * C::kStageBytes + C::kScaleBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::kStages;
   uint64_t* pfull = bars + 2 * C::kStages;     // [kSlots] partial slot written by the tensor core
@@ -83,53 +137,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = pfull + 2 * C::kSlots;
   uint32_t* tmem_base = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_i = reinterpret_cast<int*>(tmem_base + 1);
+  int* fix_flag = abort_i + 1;                 // stream-K: this CTA finishes the tile
   volatile int* abort_flag = abort_i;
   const WaitGuard wg{abort_flag, p.status, p.wait_ns};
   const int warp = warp_bcast((int)(threadIdx.x / 32)), lane = threadIdx.x % 32;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+  // Prologue.  The producer (warp 0) initialises the barriers itself and
+  // starts loading at once; it signals named barrier 2 without waiting, so the
+  // tensor-memory allocation (warp 1) overlaps its first loads.  The other
+  // warps wait on barrier 2 for both the barriers and the allocation.
+  uint32_t tmem = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      griddep_launch_dependents();
+      for (int s = 0; s < C::kStages; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+      }
+      for (int i = 0; i < C::kSlots; ++i) {
+        mbar_init(&pfull[i], 1);
+        mbar_init(&pempty[i], 8);
+      }
+      mbar_init(drain, 1);
+      *abort_i = 0;
+      fence_barrier_init();
+      prefetch_tmap(&tmW);
+      prefetch_tmap(&tmX);
     }
-    for (int i = 0; i < C::kSlots; ++i) {
-      mbar_init(&pfull[i], 1);
-      mbar_init(&pempty[i], 8);
+    __syncwarp();
+    asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
+  } else {
+    if (warp == 1) {
+      tmem_alloc(tmem_base, C::kTmemCols);
+      tmem_relinquish();
     }
-    mbar_init(drain, 1);
-    *abort_i = 0;
-    fence_barrier_init();
+    tc_fence_before();
+    asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");
+    tc_fence_after();
+    tmem = warp_bcast(*tmem_base);
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmW);
-    prefetch_tmap(&tmX);
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_base, C::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = warp_bcast(*tmem_base);
 
   const int n_wblk = (p.N + BM - 1) / BM;
   const int n_tblk = (p.M + TN - 1) / TN;
   const int total = n_wblk * n_tblk;
-  const int nkb_all = p.K / BK;
-  // split mode: this CTA's K blocks [kb0, kb0 + nkb); tiles are walked per cluster
-  const uint32_t srank = kSplit > 1 ? warp_bcast(cluster_ctarank()) : 0u;
-  const int kb0 = kSplit > 1 ? (int)srank * ((nkb_all + 1) / 2) : 0;
-  const int nkb = kSplit > 1 ? (srank == 0 ? (nkb_all + 1) / 2 : nkb_all / 2) : nkb_all;
-  const int t_first = kSplit > 1 ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-  const int t_step = kSplit > 1 ? (int)gridDim.x / 2 : (int)gridDim.x;
-
-  // split mode: the tile's partial sums of this thread, kept for the exchange
-  float facc[C::kColsPerWarp];
-  int f_n = 0, f_m0 = 0;
-  bool f_have = false;
-#pragma unroll
-  for (int i = 0; i < C::kColsPerWarp; ++i) facc[i] = 0.0f;
+  const int nkb = p.K / BK;
 
   // The producer and the MMA issuer run with the whole warp: lane 0 waits on
   // the barriers (result broadcast), one elected lane issues.
@@ -138,22 +189,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     PipeState<C::kStages> ps;
     uint32_t issued_mask = 0, last_phase = 0;
     bool ok = true;
-    for (int t = t_first; t < total && ok; t += t_step) {
-      const int wb = t % n_wblk, tb = t / n_wblk;
-      for (int kb = 0; kb < nkb; ++kb) {
+    const int pre = p.pre_b < C::kStages ? p.pre_b : C::kStages;
+    int item = 0;
+    // The token tiles of the first `issued` items, issued once the preceding
+    // kernel (the activation quantizer) has finished.  Those items sit in
+    // ring slots 0 .. issued-1 of the fresh ring.
+    auto late_token_loads = [&](int issued) {
+      griddep_wait();
+      Walk<kStreamK> w2(p, total, nkb);
+      Seg s2;
+      int i = 0;
+      while (i < issued && w2.next(p, nkb, s2))
+        for (int kb = s2.kb0; kb < s2.kb1 && i < issued; ++kb, ++i)
+          if (elect_one())
+            tma_load_2d(stages + i * C::kStageBytes + BM * BK, &tmX, &full[i], kb * BK, (s2.t / n_wblk) * TN);
+      __syncwarp();
+    };
+    if (pre == 0) griddep_wait();
+    Walk<kStreamK> w(p, total, nkb);
+    Seg sg;
+    while (ok && w.next(p, nkb, sg)) {
+      const int wb = sg.t % n_wblk, tb = sg.t / n_wblk;
+      for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
         if (!mbar_wait_warp(&empty[ps.index], ps.phase ^ 1u, wg, 50)) { ok = false; break; }
         uint8_t* st = stages + ps.index * C::kStageBytes;
         if (elect_one()) {
           mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(BM * BK + TN * BK));
-          tma_load_2d(st, &tmW, &full[ps.index], (kb0 + kb) * BK, wb * BM);
-          tma_load_2d(st + BM * BK, &tmX, &full[ps.index], (kb0 + kb) * BK, tb * TN);
+          tma_load_2d(st, &tmW, &full[ps.index], kb * BK, wb * BM);
+          if (item >= pre) tma_load_2d(st + BM * BK, &tmX, &full[ps.index], kb * BK, tb * TN);
         }
         __syncwarp();
         issued_mask |= 1u << ps.index;
         last_phase = (last_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
         ps.advance();
+        if (++item == pre) late_token_loads(pre);
       }
     }
+    if (item < pre) late_token_loads(item);   // fewer items than early weight loads (or an abort)
     if (lane == 0) {
       // copies already in flight land before the CTA can exit
       for (int s = 0; s < C::kStages; ++s)
@@ -168,8 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dW = smem_desc(smem_u32(stages), 16, 1024, kLayoutSw128);
     const uint64_t dX = smem_desc(smem_u32(stages + BM * BK), 16, 1024, kLayoutSw128);
     bool ok = true;
-    for (int t = t_first; t < total && ok; t += t_step) {
-      for (int kb = 0; kb < nkb; ++kb) {
+    Walk<kStreamK> w(p, total, nkb);
+    Seg sg;
+    while (ok && w.next(p, nkb, sg)) {
+      for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
         if (!mbar_wait_warp(&pempty[sl.index], sl.phase ^ 1u, wg, 60)) { ok = false; break; }
         if (!mbar_wait_warp(&full[ps.index], ps.phase, wg, 61)) { ok = false; break; }
         tc_fence_after();
@@ -194,53 +268,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ promotion + epilogue
-    // Walks (tile, chunk of KBC K blocks) in order.  The scales of the next
+    // Walks (segment, chunk of KBC K blocks) in order.  The scales of the next
     // chunk are staged into shared memory with cp.async while this chunk is
     // promoted, so no K block waits on a global load.  Every epilogue warp runs
     // the same sequence of named barriers; after an abort the warps keep
-    // walking (skipping the waits and the work) so the barriers still match.
+    // walking (skipping the waits and the work) so the barriers still match,
+    // and stream-K tiles are still counted in so the counters return to zero.
     constexpr int NC = C::kColsPerWarp;
     const int q = warp % 4, half = (warp - kEpiWarp0) / 4;
     const int col0 = half * NC;
+    const int r = q * 32 + lane;                     // weight row within the tile
     const int etid = threadIdx.x - kEpiWarp0 * 32;  // 0 .. 255
-    const int nchunk = (nkb + KBC - 1) / KBC;
+    griddep_wait();                                 // activation scales come from the preceding kernel
     PipeState<C::kSlots> sl;
     bool ok = true;
-    auto stage_scales = [&](int t, int c, int buf) {
-      const int wb = t % n_wblk, tb = t / n_wblk;
+    auto nchunks = [&](const Seg& s) { return (s.kb1 - s.kb0 + KBC - 1) / KBC; };
+    auto stage_scales = [&](const Seg& s, int c, int buf) {
+      const int wb = s.t % n_wblk, tb = s.t / n_wblk;
       float* da = ssa + buf * KBC * TN;
       float* db = ssb + buf * KBC;
       for (int i = etid; i < KBC * TN; i += 256) {
         const int kbl = i / TN, m = i % TN;
-        const int kb = c * KBC + kbl, ma = tb * TN + m;
-        const bool valid = kb < nkb && ma < p.M;
-        const float* src = valid ? p.sfa + (size_t)(kb0 + kb) * p.M + ma : p.sfa;
+        const int kb = s.kb0 + c * KBC + kbl, ma = tb * TN + m;
+        const bool valid = kb < s.kb1 && ma < p.M;
+        const float* src = valid ? p.sfa + (size_t)kb * p.M + ma : p.sfa;
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(da + i)), "l"(src),
                      "r"(valid ? 4 : 0)
                      : "memory");
       }
       for (int i = etid; i < KBC; i += 256) {
-        const int kb = c * KBC + i;
-        const bool valid = kb < nkb;
-        const float* src = valid ? p.sfb + (size_t)wb * nkb_all + kb0 + kb : p.sfb;
+        const int kb = s.kb0 + c * KBC + i;
+        const bool valid = kb < s.kb1;
+        const float* src = valid ? p.sfb + (size_t)wb * nkb + kb : p.sfb;
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(db + i)), "l"(src),
                      "r"(valid ? 4 : 0)
                      : "memory");
       }
     };
-    int t = t_first, c = 0, qi = 0;
-    if (t < total) stage_scales(t, 0, 0);
+    auto store_out = [&](const Seg& s, const float (&y)[NC]) {
+      const int n = (s.t % n_wblk) * BM + r;            // weight row = output column
+      const int m0 = (s.t / n_wblk) * TN + col0;        // first token of this warp's columns
+      if (n >= p.N) return;
+#pragma unroll
+      for (int i = 0; i < NC; ++i) {
+        const int m = m0 + i;
+        if (m < p.M) {
+          if (p.out_bf16)
+            reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(y[i]);
+          else
+            reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + n] = y[i];
+        }
+      }
+    };
+    Walk<kStreamK> w(p, total, nkb);
+    Seg sg;
+    bool have = w.next(p, nkb, sg);
+    int c = 0, qi = 0;
+    if (have) stage_scales(sg, 0, 0);
     asm volatile("cp.async.commit_group;" ::: "memory");
     float acc[NC];
 #pragma unroll
     for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
-    while (t < total) {
-      int tn = t, cn = c + 1;
-      if (cn == nchunk) {
+    while (have) {
+      Seg sn = sg;
+      int cn = c + 1;
+      bool haven = true;
+      if (cn == nchunks(sg)) {
         cn = 0;
-        tn = t + t_step;
+        haven = w.next(p, nkb, sn);
       }
-      if (tn < total) stage_scales(tn, cn, (qi + 1) & 1);
+      if (haven) stage_scales(sn, cn, (qi + 1) & 1);
       asm volatile("cp.async.commit_group;" ::: "memory");
       asm volatile("cp.async.wait_group 1;" ::: "memory");
       asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -253,15 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 1, 256;" ::: "memory");
       }
       const float* csa = ssa + (qi & 1) * KBC * TN;
-      const int wb = t % n_wblk, tb = t / n_wblk;
-      const int n = wb * BM + q * 32 + lane;            // weight row = output column
-      const int m0 = tb * TN + col0;                    // first token of this warp's columns
-      const int kb_end = min(nkb, (c + 1) * KBC);
+      const int kc0 = sg.kb0 + c * KBC;                // first K block of the chunk
+      const int kb_end = min(sg.kb1, kc0 + KBC);
       // Small tiles fold G partial slots per round trip (wait all, load all,
       // one tcgen05.wait::ld, release all) so the latency of the hand-off is
       // paid once per G K blocks.
       constexpr int G = NC <= 32 ? (64 / NC < 8 ? 64 / NC : 8) : 1;
-      int kb = c * KBC;
+      int kb = kc0;
       if constexpr (G > 1) {
         for (; kb + G <= kb_end; kb += G) {
           uint32_t idx[G];
@@ -291,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int i = 0; i < G; ++i) {
-              const float4* s4 = reinterpret_cast<const float4*>(csa + (kb + i - c * KBC) * TN + col0);
+              const float4* s4 = reinterpret_cast<const float4*>(csa + (kb + i - kc0) * TN + col0);
 #pragma unroll
               for (int j = 0; j < NC; j += 4) {
                 const float4 sc = s4[j / 4];  // same address in every lane: one broadcast
@@ -313,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
           tc_fence_after();
-          const float4* s4 = reinterpret_cast<const float4*>(csa + (kb - c * KBC) * TN + col0);
+          const float4* s4 = reinterpret_cast<const float4*>(csa + (kb - kc0) * TN + col0);
           constexpr int CH = NC < 32 ? NC : 32;
 #pragma unroll
           for (int c0 = 0; c0 < NC; c0 += CH) {
@@ -338,95 +433,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         sl.advance();
       }
-      if (cn == 0 && kSplit > 1) {
-        // split mode (one tile per cluster): keep the partial for the exchange
+      if (cn == 0) {
+        // the segment's last chunk
+        if (!kStreamK || (sg.kb0 == 0 && sg.kb1 == nkb)) {
+          if (ok) store_out(sg, acc);
+        } else {
+          // stream-K piece of a tile: partial to the workspace, count in; the
+          // last of the tile's CTAs sums the pieces in K order
+          const long long U = (long long)total * nkb, u0 = (long long)sg.t * nkb;
+          const int c_first = sk_owner(u0, U, (int)gridDim.x);
+          const int n_parts = sk_owner(u0 + nkb - 1, U, (int)gridDim.x) - c_first + 1;
+          const int j = (int)blockIdx.x - c_first;
+          float* parts = p.work + (size_t)sg.t * p.maxc * (BM * TN);
+          float4* mine = reinterpret_cast<float4*>(parts + (size_t)j * (BM * TN) + r * TN + col0);
 #pragma unroll
-        for (int i = 0; i < NC; ++i) facc[i] = acc[i];
-        f_n = n;
-        f_m0 = m0;
-        f_have = ok;
-      } else if (cn == 0) {
-        // the tile's last chunk: write it and reset the accumulators
-        if (ok && n < p.N) {
+          for (int i = 0; i < NC; i += 4) mine[i / 4] = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+          // One thread counts the CTA in with an acquire-release add: the
+          // barrier orders every thread's partial before its release, and if
+          // it is the last piece its acquire (passed on by the second barrier)
+          // orders the other CTAs' partials before the reads below.
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          if (etid == 0) {
+            int old;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + sg.t) : "memory");
+            *fix_flag = old == n_parts - 1;
+          }
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          if (*fix_flag) {
+            // every piece, this CTA's own included, summed from the workspace
+            // (L2) in K order
 #pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            const int m = m0 + i;
-            if (m < p.M) {
-              if (p.out_bf16)
-                reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(acc[i]);
-              else
-                reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + n] = acc[i];
+            for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
+            for (int jj = 0; jj < n_parts; ++jj) {
+              const float4* src = reinterpret_cast<const float4*>(parts + (size_t)jj * (BM * TN) + r * TN + col0);
+#pragma unroll
+              for (int i = 0; i < NC; i += 4) {
+                const float4 v4 = __ldcg(src + i / 4);
+                acc[i] += v4.x;
+                acc[i + 1] += v4.y;
+                acc[i + 2] += v4.z;
+                acc[i + 3] += v4.w;
+              }
             }
+            if (ok) store_out(sg, acc);
+            if (etid == 0) p.counters[sg.t] = 0;
           }
         }
 #pragma unroll
         for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");  // this buffer may be refilled next iteration
-      t = tn;
+      sg = sn;
       c = cn;
+      have = haven;
       ++qi;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    if (kSplit > 1 && srank == 1 && f_have) {
-      // hand the partial sums to the leader's reduction buffer (DSMEM)
-      const uint32_t dst = mapa_shared(smem_u32(red + (q * 32 + lane) * TN + col0), 0);
-#pragma unroll
-      for (int i = 0; i < NC; ++i)
-        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + 4 * i), "f"(facc[i]) : "memory");
-    }
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (kSplit > 1) {
-    cluster_sync();  // the peer's partials have landed in the leader's buffer
-    if (srank == 0 && warp >= kEpiWarp0 && f_have && f_n < p.N) {
-      const int q = warp % 4, col0 = ((warp - kEpiWarp0) / 4) * C::kColsPerWarp;
-      const float* other = red + (q * 32 + lane) * TN + col0;
-#pragma unroll
-      for (int i = 0; i < C::kColsPerWarp; ++i) {
-        const int m = f_m0 + i;
-        const float y = facc[i] + (nkb_all > 1 ? other[i] : 0.0f);
-        if (m < p.M) {
-          if (p.out_bf16)
-            reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + f_n] = __float2bfloat16_rn(y);
-          else
-            reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + f_n] = y;
-        }
-      }
-    }
-  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-template <int TN, int kSplit>
+template <int TN, bool kStreamK>
 static cudaError_t launch_tn(const Fp8Launch& L, cudaStream_t stream) {
-  using C = Cfg<TN, kSplit>;
-  auto kern = fp8_gemm_kernel<TN, kSplit>;
+  using C = Cfg<TN>;
+  auto kern = fp8_gemm_kernel<TN, kStreamK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  if (kSplit == 1) {
-    kern<<<L.grid, kThreads, C::kSmem, stream>>>(L.tmA, L.tmB, L.p);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)L.grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)C::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.p);
+  return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmA, L.tmB, L.p);
 }
 
 }  // namespace fp8
@@ -438,20 +518,32 @@ int fp8_tile_n(long long M) {
   return 128;
 }
 
+int fp8_stages(int tile_n) {
+  switch (tile_n) {
+    case 16: return fp8::Cfg<16>::kStages;
+    case 32: return fp8::Cfg<32>::kStages;
+    case 64: return fp8::Cfg<64>::kStages;
+    case 128: return fp8::Cfg<128>::kStages;
+  }
+  return 0;
+}
+
 cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream) {
-  if (L.p.splits == 2) {
-    if (L.grid <= 0 || (L.grid & 1)) return cudaErrorInvalidValue;
+  if (L.grid <= 0) return cudaErrorInvalidValue;
+  if (L.p.stream_k) {
     switch (L.tile_n) {
-      case 16: return fp8::launch_tn<16, 2>(L, stream);
-      case 32: return fp8::launch_tn<32, 2>(L, stream);
+      case 16: return fp8::launch_tn<16, true>(L, stream);
+      case 32: return fp8::launch_tn<32, true>(L, stream);
+      case 64: return fp8::launch_tn<64, true>(L, stream);
+      case 128: return fp8::launch_tn<128, true>(L, stream);
     }
     return cudaErrorInvalidValue;
   }
   switch (L.tile_n) {
-    case 16: return fp8::launch_tn<16, 1>(L, stream);
-    case 32: return fp8::launch_tn<32, 1>(L, stream);
-    case 64: return fp8::launch_tn<64, 1>(L, stream);
-    case 128: return fp8::launch_tn<128, 1>(L, stream);
+    case 16: return fp8::launch_tn<16, false>(L, stream);
+    case 32: return fp8::launch_tn<32, false>(L, stream);
+    case 64: return fp8::launch_tn<64, false>(L, stream);
+    case 128: return fp8::launch_tn<128, false>(L, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -5,7 +5,38 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace bsk {
+
+// Launch with the library's attributes: programmatic stream serialization
+// (the kernel may start while the previous kernel on the stream finishes; each
+// kernel waits with griddepcontrol.wait before touching global memory another
+// kernel may use) and, for cluster > 1, a 1-D cluster shape.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                          int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 enum { kEpiStore = 0, kEpiSwiglu = 1, kEpiCombine = 2, kEpiRows = 3, kEpiSwigluQ4 = 4 };
 // SWIGLU and SWIGLU_Q4 share the tile map (gate / up column blocks); Q4 then
@@ -81,9 +112,11 @@ struct Fp8Params {
   void* out;
   int out_bf16;
   long long ldo;
-  float* work;            // split-K partials (decode), may be null
-  int* counters;          // split-K tile counters (decode), may be null
-  int splits;
+  float* work;            // stream-K: fp32 partials [tiles][maxc][128][TN]
+  int* counters;          // stream-K: one arrival counter per tile (zero between calls)
+  int stream_k;           // 1: the tiles' K blocks are shared out evenly over the grid
+  int maxc;               // stream-K: most CTAs that share one tile
+  int pre_b;              // weight stages loaded before waiting on the preceding kernel
   int* status;
   unsigned long long wait_ns;  // bound of every pipeline wait (%globaltimer ns)
 };
@@ -91,13 +124,13 @@ struct Fp8Params {
 struct Fp8Launch {
   CUtensorMap tmA, tmB;
   Fp8Params p;
-  bool swap_ab;           // decode: weight rows fill the MMA M dimension
-  int tile_n;             // MMA N of the swap-AB kernel (16..256)
+  int tile_n;             // MMA N (token columns per tile): 16, 32, 64 or 128
   int grid;
 };
 
 cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream);
 int fp8_tile_n(long long M);
+int fp8_stages(int tile_n);
 
 // quantizers
 cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx,

@@ -26,6 +26,8 @@ constexpr int kDispatchThreads = 256;  // 8 warps per chunk
 
 __global__ void __launch_bounds__(kDispatchThreads) moe_count_kernel(const int* __restrict__ ids, long long P, int E,
                                                                      int* __restrict__ hist, int* status) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   extern __shared__ int cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -46,6 +48,8 @@ __global__ void __launch_bounds__(kDispatchThreads) moe_count_kernel(const int* 
 
 __global__ void __launch_bounds__(1024) moe_scan_kernel(int* __restrict__ hist, int nchunks, int E,
                                                         int* __restrict__ counts, int* __restrict__ offsets) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   __shared__ int padded[1024];
   __shared__ int warp_sums[32];
   const int e = threadIdx.x;
@@ -111,6 +115,8 @@ __global__ void __launch_bounds__(kDispatchThreads) moe_place_kernel(
     const int* __restrict__ ids, const float* __restrict__ w, long long P, int k, int E, const int* __restrict__ base,
     const int* __restrict__ counts, const int* __restrict__ offsets, int* __restrict__ pair_of_row,
     int* __restrict__ token_of, float* __restrict__ weight_of, long long rows_bound) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   extern __shared__ int pos[];  // [8][E]: per-warp counts, then per-warp running positions
   constexpr int kWarps = kDispatchThreads / 32;
   constexpr int kPerWarp = kChunk / kWarps;
@@ -182,6 +188,8 @@ __global__ void __launch_bounds__(kDispatchThreads) moe_place_kernel(
 // over the lines a thread has just read, in the same kernel, ran several
 // times slower than the two streaming passes together on GB300.
 __global__ void moe_cast_kernel(const float* __restrict__ out32, __nv_bfloat16* __restrict__ out, long long n) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   const long long n8 = n / 8;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
@@ -199,6 +207,8 @@ __global__ void moe_cast_kernel(const float* __restrict__ out32, __nv_bfloat16* 
 }
 
 __global__ void moe_zero_kernel(float* __restrict__ out32, long long n) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   const long long n4 = n / 4;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
@@ -215,20 +225,27 @@ cudaError_t launch_moe_dispatch(const int* topk_ids, const float* topk_w, long l
   const long long nch = moe_chunks(P) > 0 ? moe_chunks(P) : 1;
   const size_t smem = (size_t)E * sizeof(int);
   const size_t smem_place = (size_t)(kDispatchThreads / 32) * E * sizeof(int);  // <= 32 KB for E <= 1024
-  moe_count_kernel<<<(unsigned)nch, kDispatchThreads, smem, stream>>>(topk_ids, P, E, work, status);
-  moe_scan_kernel<<<1, 1024, 0, stream>>>(work, (int)nch, E, counts, offsets);
-  moe_place_kernel<<<(unsigned)nch, kDispatchThreads, smem_place, stream>>>(
-      topk_ids, topk_w, P, k, E, work, counts, offsets, pair_of_row, token_of, weight_of, rows_bound);
-  return cudaGetLastError();
+  cudaError_t e = launch_kernel(moe_count_kernel, (unsigned)nch, kDispatchThreads, smem, stream, 1, topk_ids, P, E,
+                                work, status);
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(moe_scan_kernel, 1, 1024, 0, stream, 1, work, (int)nch, E, counts, offsets);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(moe_place_kernel, (unsigned)nch, kDispatchThreads, smem_place, stream, 1, topk_ids, topk_w, P, k,
+                       E, (const int*)work, (const int*)counts, (const int*)offsets, pair_of_row, token_of, weight_of,
+                       rows_bound);
 }
 
 // row_of_pair = inverse of pair_of_row (-1 where no row holds the pair)
 __global__ void moe_rows_init_kernel(int* __restrict__ row_of_pair, long long P) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x; p < P; p += stride) row_of_pair[p] = -1;
 }
 __global__ void moe_rows_invert_kernel(const int* __restrict__ pair_of_row, long long n_rows,
                                        int* __restrict__ row_of_pair, long long P) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x; r < n_rows; r += stride) {
     const int p = pair_of_row[r];
@@ -245,6 +262,8 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restric
                                                           const int* __restrict__ row_of_pair, long long T, int k,
                                                           long long G, __nv_bfloat16* __restrict__ out,
                                                           long long ldo) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < T * G; i += stride) {
     const long long t = i / G, g = i % G;
@@ -283,12 +302,14 @@ cudaError_t launch_moe_combine(const float* rows, long long ld_rows, const int* 
     return (unsigned)(b > 8192 ? 8192 : (b < 1 ? 1 : b));
   };
   const long long P = T * k;
-  moe_rows_init_kernel<<<grid(P), 256, 0, stream>>>(row_of_pair, P);
-  moe_rows_invert_kernel<<<grid(n_rows), 256, 0, stream>>>(pair_of_row, n_rows, row_of_pair, P);
+  cudaError_t e = launch_kernel(moe_rows_init_kernel, grid(P), 256, 0, stream, 1, row_of_pair, P);
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(moe_rows_invert_kernel, grid(n_rows), 256, 0, stream, 1, pair_of_row, n_rows, row_of_pair, P);
+  if (e != cudaSuccess) return e;
   const long long G = H / 8;
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
-  moe_combine_kernel<<<grid(T * G), 256, 0, stream>>>(rows, ld_rows, row_of_pair, T, k, G, o, ldo);
-  return cudaGetLastError();
+  return launch_kernel(moe_combine_kernel, grid(T * G), 256, 0, stream, 1, rows, ld_rows, (const int*)row_of_pair, T,
+                       k, G, o, ldo);
 }
 
 cudaError_t launch_moe_finalize(float* out32, void* out_bf16, long long n, cudaStream_t stream) {
@@ -296,9 +317,10 @@ cudaError_t launch_moe_finalize(float* out32, void* out_bf16, long long n, cudaS
     long long b = (units + 255) / 256;
     return (unsigned)(b > 4096 ? 4096 : (b < 1 ? 1 : b));
   };
-  moe_cast_kernel<<<grid(n / 8), 256, 0, stream>>>(out32, reinterpret_cast<__nv_bfloat16*>(out_bf16), n);
-  moe_zero_kernel<<<grid(n / 4), 256, 0, stream>>>(out32, n);
-  return cudaGetLastError();
+  cudaError_t e = launch_kernel(moe_cast_kernel, grid(n / 8), 256, 0, stream, 1, (const float*)out32,
+                                reinterpret_cast<__nv_bfloat16*>(out_bf16), n);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(moe_zero_kernel, grid(n / 4), 256, 0, stream, 1, out32, n);
 }
 
 }  // namespace bsk

@@ -99,6 +99,19 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint6
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch ("DeepGEMM for Hopper MoE", section 4.1: a
+// kernel's launch and prologue overlap the tail of the kernel before it).
+// Every kernel of the library is launched as a programmatic dependent of the
+// previous kernel on its stream and calls griddep_wait() before it reads or
+// writes global memory that another kernel may touch; griddep_wait returns
+// once the preceding grid has completed and its writes are visible (at once
+// when there is none).  griddep_launch_dependents() lets the next kernel on
+// the stream begin its own prologue early.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// ---------------------------------------------------------------------------
 // Warp-uniform issue.  A role warp runs its loop with all 32 lanes; one lane
 // waits on a barrier and the result is broadcast, and one elected lane issues
 // each asynchronous copy / MMA.  Values broadcast from lane 0 are known to be

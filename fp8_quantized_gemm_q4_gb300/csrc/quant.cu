@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict
                                                           long long K, long long ldx,
                                                           const int* __restrict__ gather,
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const float r6 = __frcp_rn(6.0f);
   const long long nblk = (K + 256 * kQ4Unroll - 1) / (256 * kQ4Unroll);
@@ -140,6 +142,8 @@ __global__ void __launch_bounds__(256) lowrank_t_kernel(const __nv_bfloat16* __r
                                                         const int* __restrict__ gather,
                                                         const __nv_bfloat16* __restrict__ at,
                                                         __nv_bfloat16* __restrict__ t_out) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   __shared__ float red[8][16][33];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int g = lane / 4, tq = lane % 4;
@@ -193,37 +197,57 @@ __global__ void __launch_bounds__(256) lowrank_t_kernel(const __nv_bfloat16* __r
   }
 }
 
-// FP8 1x128: one warp per (row, 128-block), 4 elements per lane.
-__global__ void __launch_bounds__(256) q8_token_kernel(const void* __restrict__ x, int x_bf16, long long M,
-                                                       long long K, long long ldx, uint8_t* __restrict__ codes,
+// FP8 1x128 per token.  Each lane owns 8 consecutive elements (one 16-byte
+// bf16 load, two for fp32), 16 lanes a 128-element block, so a warp covers
+// two blocks of one row per 256-element unit; a warp takes kQ8Unroll units of
+// a row and issues all their loads before any arithmetic (4 KB of bf16 in
+// flight per warp).  The block amax is a 4-step shuffle over the 16 lanes;
+// s = fl32(amax / 448) and every code's quotient x / s use IEEE division.
+// (The one-correction quotient of the FP4 quantizers is exact for their e4m3
+// scales, checked exhaustively; for arbitrary fp32 scales it is not always
+// correctly rounded, which the quotient sweep over 512 scales shows.)
+constexpr int kQ8Unroll = 8;
+template <bool kBf16>
+__global__ void __launch_bounds__(256) q8_token_kernel(const void* __restrict__ x, long long M, long long K,
+                                                       long long ldx, uint8_t* __restrict__ codes,
                                                        float* __restrict__ scales) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
-  const long long nkb = K / 128;
-  const long long total = M * nkb;
+  const long long units = (K + 255) / 256;
+  const long long ngrp = (units + kQ8Unroll - 1) / kQ8Unroll;
+  const long long total = M * ngrp;
   for (long long w = (long long)blockIdx.x * 8 + threadIdx.x / 32; w < total; w += (long long)gridDim.x * 8) {
-    const long long row = w / nkb, kb = w % nkb;
-    const long long off = row * ldx + kb * 128 + lane * 4;
-    float v[4];
-    if (x_bf16) {
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(x) + off));
-      v[0] = __uint_as_float(raw.x << 16);
-      v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-      v[2] = __uint_as_float(raw.y << 16);
-      v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-    } else {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + off));
-      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    const long long row = w / ngrp, g = w % ngrp;
+    Raw8<kBf16> raw[kQ8Unroll];
+#pragma unroll
+    for (int u = 0; u < kQ8Unroll; ++u) {
+      const long long k0 = (g * kQ8Unroll + u) * 256 + lane * 8;
+#pragma unroll
+      for (int i = 0; i < (kBf16 ? 4 : 8); ++i) raw[u].w[i] = 0u;
+      if (k0 < K) load_raw8<kBf16>(x, row * ldx + k0, raw[u]);
     }
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-    const float s = __fdiv_rn(amax, 448.0f);
-    float q[4];
+    for (int u = 0; u < kQ8Unroll; ++u) {
+      const long long k0 = (g * kQ8Unroll + u) * 256 + lane * 8;
+      float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = (s == 0.0f) ? 0.0f : __fdiv_rn(v[i], s);
-    const uint32_t c = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
-    *reinterpret_cast<uint32_t*>(codes + row * K + kb * 128 + lane * 4) = c;
-    if (lane == 0) scales[kb * M + row] = s;
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(raw8_at<kBf16>(raw[u], i)));
+#pragma unroll
+      for (int d = 1; d < 16; d <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+      if (k0 >= K) continue;  // after the shuffles: the whole warp takes part in them
+      const float s = __fdiv_rn(amax, 448.0f);
+      uint32_t c[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = s == 0.0f ? 0.0f : __fdiv_rn(raw8_at<kBf16>(raw[u], 4 * h + i), s);
+        c[h] = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
+      }
+      *reinterpret_cast<uint2*>(codes + row * K + k0) = make_uint2(c[0], c[1]);
+      if ((lane & 15) == 0) scales[(k0 / 128) * M + row] = s;
+    }
   }
 }
 
@@ -232,7 +256,9 @@ __global__ void __launch_bounds__(256) q8_block_kernel(const void* __restrict__ 
                                                        long long K, long long ldx, uint8_t* __restrict__ codes,
                                                        float* __restrict__ scales) {
   __shared__ float wmax[8];
-  const long long rb = blockIdx.y, kb = blockIdx.x;
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long rb = blockIdx.x / (K / 128), kb = blockIdx.x % (K / 128);
   const int tid = threadIdx.x;
   // thread -> (row r = tid / 2 .. in 2 passes of 64 rows? keep it simple: 64 elements each)
   const int r_local = tid / 2, c_local = (tid % 2) * 64;
@@ -289,35 +315,34 @@ cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (x_bf16)
-    q4_quantize_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(x, M, Mpad, K, ldx, gather, codes, sf);
-  else
-    q4_quantize_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(x, M, Mpad, K, ldx, gather, codes, sf);
-  return cudaGetLastError();
+    return launch_kernel(q4_quantize_kernel<true>, (unsigned)blocks, 256, 0, stream, 1, x, M, Mpad, K, ldx, gather,
+                         codes, sf);
+  return launch_kernel(q4_quantize_kernel<false>, (unsigned)blocks, 256, 0, stream, 1, x, M, Mpad, K, ldx, gather,
+                       codes, sf);
 }
 
 cudaError_t launch_lowrank_t(const void* x, long long M, long long K, long long ldx, const int* gather,
                              const void* lora_a_t, void* lora_t, cudaStream_t stream) {
   const long long blocks = (M + 15) / 16;
-  lowrank_t_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(x), M, K, ldx,
-                                                          gather, reinterpret_cast<const __nv_bfloat16*>(lora_a_t),
-                                                          reinterpret_cast<__nv_bfloat16*>(lora_t));
-  return cudaGetLastError();
+  return launch_kernel(lowrank_t_kernel, (unsigned)blocks, 256, 0, stream, 1,
+                       reinterpret_cast<const __nv_bfloat16*>(x), M, K, ldx, gather,
+                       reinterpret_cast<const __nv_bfloat16*>(lora_a_t), reinterpret_cast<__nv_bfloat16*>(lora_t));
 }
 
 cudaError_t launch_q8_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx, int mode,
                                uint8_t* codes, float* scales, cudaStream_t stream) {
   if (mode == 1) {
-    const long long warps = M * (K / 128);
+    const long long warps = M * (((K + 255) / 256 + kQ8Unroll - 1) / kQ8Unroll);
     long long blocks = (warps + 7) / 8;
-    const long long cap = (long long)sm_count() * 16;
+    const long long cap = (long long)sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    q8_token_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, x_bf16, M, K, ldx, codes, scales);
-  } else {
-    dim3 grid((unsigned)(K / 128), (unsigned)((M + 127) / 128));
-    q8_block_kernel<<<grid, 256, 0, stream>>>(x, x_bf16, M, K, ldx, codes, scales);
+    if (x_bf16) return launch_kernel(q8_token_kernel<true>, (unsigned)blocks, 256, 0, stream, 1, x, M, K, ldx, codes, scales);
+    return launch_kernel(q8_token_kernel<false>, (unsigned)blocks, 256, 0, stream, 1, x, M, K, ldx, codes, scales);
   }
-  return cudaGetLastError();
+  // one CTA per 128 x 128 block, numbered kb + (K / 128) * rb
+  return launch_kernel(q8_block_kernel, (unsigned)((K / 128) * ((M + 127) / 128)), 256, 0, stream, 1, x, x_bf16, M,
+                       K, ldx, codes, scales);
 }
 
 }  // namespace bsk
@@ -376,6 +401,8 @@ __global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
     const int* __restrict__ gather, const __nv_bfloat16* __restrict__ at, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ sf, __nv_bfloat16* __restrict__ t_out) {
   extern __shared__ __align__(128) uint8_t fsm[];
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const float r6 = __frcp_rn(6.0f);
   const long long r0 = (long long)blockIdx.x * fq::R;
@@ -544,10 +571,10 @@ cudaError_t launch_q4_lowrank_fused(const void* x, long long M, long long K, lon
   cudaError_t e = cudaFuncSetAttribute(q4_lowrank_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        fq::SMEM);
   if (e != cudaSuccess) return e;
-  q4_lowrank_fused_kernel<<<(unsigned)blocks, 256, fq::SMEM, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(x), M, Mpad, K, ldx, gather,
-      reinterpret_cast<const __nv_bfloat16*>(lora_a_t), codes, sf, reinterpret_cast<__nv_bfloat16*>(lora_t));
-  return cudaGetLastError();
+  return launch_kernel(q4_lowrank_fused_kernel, (unsigned)blocks, 256, (size_t)fq::SMEM, stream, 1,
+                       reinterpret_cast<const __nv_bfloat16*>(x), M, Mpad, K, ldx, gather,
+                       reinterpret_cast<const __nv_bfloat16*>(lora_a_t), codes, sf,
+                       reinterpret_cast<__nv_bfloat16*>(lora_t));
 }
 
 }  // namespace bsk
@@ -573,6 +600,8 @@ __global__ void __launch_bounds__(256) fp4_gather_rows_kernel(const uint8_t* __r
                                                               long long rows_out, long long rows_out_pad,
                                                               uint8_t* __restrict__ codes_out,
                                                               uint8_t* __restrict__ sf_out) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long kv = K / 32;  // 16-byte vectors per row of codes
   const long long kc = K / 64;  // scale words per row
@@ -632,9 +661,8 @@ cudaError_t launch_fp4_gather_rows(const uint8_t* codes_in, const uint8_t* sf_in
   const long long cap = (long long)sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  fp4_gather_rows_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes_in, sf_in, rows_in, K, gather, rows_out, pad,
-                                                                codes_out, sf_out);
-  return cudaGetLastError();
+  return launch_kernel(fp4_gather_rows_kernel, (unsigned)blocks, 256, 0, stream, 1, codes_in, sf_in, rows_in, K, gather,
+                       rows_out, pad, codes_out, sf_out);
 }
 
 }  // namespace bsk

@@ -169,10 +169,13 @@ bs_status q8_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t 
  *   M >= 0, N % 128 == 0, K % 64 == 0 (FP4) or K % 128 == 0 (FP8)
  *   num_sms    persistent grid size limit (0 = all SMs)
  *   n_chunk_blocks  ignored by bs_gemm (grouped tile-order knob)
- *   fp4_kernel, fp4_stage_k, fp4_small_experts, fp4_half_tail, fp8_split_k,
- *   wait_timeout_us
+ *   fp4_kernel, fp4_stage_k, fp4_small_experts, fp4_half_tail, fp8_stream_k,
+ *   wait_timeout_us, weights_ready
  *              per-call kernel choices, described at the fields; 0 = the
  *              library's default.  A zero-initialised struct gets every default.
+ *   workspace, workspace_bytes
+ *              optional caller-owned device scratch (FP8 decode shapes), see
+ *              bs_gemm_workspace_bytes.
  * ------------------------------------------------------------------------- */
 typedef struct {
     int fmt;                 /* bs_format */
@@ -203,13 +206,35 @@ typedef struct {
                                 second, one-CTA launch (default); 2 = every expert in the pair launch */
     int fp4_half_tail;       /* dense FP4 on CTA pairs: 1 = a last wave that fills at most half of
                                 the pairs runs as 256 x 128 half tiles (default); 2 = whole tiles */
-    int fp8_split_k;         /* FP8 decode shapes (at most 32 token columns per tile, few tiles):
-                                1 = each tile's K split over a CTA pair (default); 2 = no split */
+    int fp8_stream_k;        /* FP8 with fewer output tiles than SMs (decode shapes): 1 = the
+                                tiles' K blocks are shared out evenly over all SMs and the pieces
+                                of a tile summed in K order by the last CTA to finish one
+                                (stream-K; default, needs `workspace`); 2 = one CTA per tile */
     int wait_timeout_us;     /* bound of every pipeline wait inside the kernels, in microseconds
                                 (default 4,000,000 = 4 s).  A wait that runs out ends the kernel
                                 early (outputs undefined) and sets BS_ERR_TIMEOUT in the device
                                 status word; it never hangs the GPU */
+    int weights_ready;       /* 1 = the kernel launched just before this call on `stream` does not
+                                write b or sfb, so the GEMM may start loading them before that
+                                kernel has finished (FP8; 0 = wait for it like for every other
+                                operand).  Every call is a programmatic dependent launch: its
+                                prologue overlaps the tail of the previous kernel on the stream */
+    void *workspace;         /* device scratch owned by the caller, 16-byte aligned, of at least
+                                bs_gemm_workspace_bytes(args) bytes and ZEROED before its first
+                                use; every call leaves it zeroed where the next call reads it.
+                                Calls that overlap on the GPU must not share one.  NULL: no
+                                scratch (FP8 stream-K then runs one CTA per tile) */
+    size_t workspace_bytes;
 } bs_gemm_args;
+
+/* Bytes of `workspace` bs_gemm would use for these arguments (sizes, format,
+ * num_sms, fp8_stream_k) on the current device; 0 when it needs none.  FP8
+ * stream-K keeps one arrival counter per tile in the first 4096 bytes (zero
+ * between calls) and one fp32 partial tile per CTA share of a tile after
+ * them (e.g. M <= 16, N = 7168, K = 4096 on 152 SMs: < 2 MB).  Because the
+ * counters always sit at the same place, calls of different shapes may share
+ * one workspace as long as they do not overlap on the GPU. */
+size_t bs_gemm_workspace_bytes(const bs_gemm_args *args);
 
 bs_status bs_gemm(const bs_gemm_args *args, bs_stream_t stream);
 

@@ -90,10 +90,10 @@ def test_host_validation_rejects_before_launch(lib):
     g.ldo = 128
     # per-call kernel choices out of range, and a negative wait limit
     for field, bad in (("fp4_kernel", 3), ("fp4_stage_k", 64), ("fp4_small_experts", -1), ("fp4_half_tail", 5),
-                       ("fp8_split_k", 9), ("wait_timeout_us", -1)):
+                       ("fp8_stream_k", 9), ("wait_timeout_us", -1), ("weights_ready", 2)):
         setattr(g, field, bad)
         assert lib.bs_gemm(ctypes.byref(g), None) == bs.BS_ERR_INVALID, field
-        assert field.encode() in lib.bs_last_error() or b"wait_timeout_us" in lib.bs_last_error()
+        assert field.encode() in lib.bs_last_error()
         setattr(g, field, 0)
     g.fmt = 9
     assert lib.bs_gemm(ctypes.byref(g), None) in (bs.BS_ERR_INVALID, bs.BS_ERR_CUDA)

@@ -11,13 +11,32 @@ from tests.helpers import gemm_errors, tight_errors
 
 pytestmark = pytest.mark.gpu
 
+# Decode shapes (fewer output tiles than SMs) run stream-K by default: the
+# tiles' K blocks shared out over every SM, a tile's pieces summed by the last
+# CTA to finish one (bs_gemm_args.fp8_stream_k = 1); 2 runs one CTA per tile.
+# Every case runs both ways.
+SCHEDULES = {"stream_k": 1, "per_tile": 2}
 
-def run_fp8(bs, x, w, rows=None, out_dtype=torch.bfloat16):
+
+@pytest.fixture(autouse=True, params=sorted(SCHEDULES))
+def fp8_schedule(request):
+    import fp8_quantized_gemm_q4_gb300 as bs
+    with bs.kernel_options(fp8_stream_k=SCHEDULES[request.param]):
+        yield request.param
+
+
+def run_fp8(bs, x, w, rows=None, out_dtype=torch.bfloat16, num_sms=0):
     xq, xs = bs.q8_quantize(x.cuda(), mode=bs.Q8_TOKEN)
     wq, ws = bs.q8_quantize(w.cuda(), mode=bs.Q8_BLOCK)
-    y = bs.gemm_fp8(xq, xs, wq, ws, out_dtype=out_dtype)
+    y = bs.gemm_fp8(xq, xs, wq, ws, out_dtype=out_dtype, num_sms=num_sms)
+    # the same call again, now as the weights-ready programmatic launch right
+    # behind the activation quantizer: the same result bit for bit, and the
+    # stream-K counters the first call left must have been reset to zero
+    xq2, xs2 = bs.q8_quantize(x.cuda(), mode=bs.Q8_TOKEN)
+    y2 = bs.gemm_fp8(xq2, xs2, wq, ws, out_dtype=out_dtype, num_sms=num_sms, weights_ready=True)
     torch.cuda.synchronize()
     assert bs.device_status()[0] == 0
+    assert torch.equal(y, y2)
     M = x.shape[0]
     rows = np.arange(M) if rows is None else np.asarray(rows)
     oa, osa = oracle.q8_quantize(x[rows], rows_per_block=1)
@@ -56,6 +75,16 @@ def test_fp8_ragged(cuda_lib, M, N, K):
     for dt in (torch.bfloat16, torch.float32):
         ok, info = run_fp8(cuda_lib, x, w, out_dtype=dt)
         assert ok, (dt, info)
+
+
+@pytest.mark.parametrize("num_sms", [3, 57, 100, 151])
+def test_fp8_stream_k_grid_sizes(cuda_lib, num_sms):
+    """Decode shape on grids that cut the 56 x 32 K blocks unevenly: pieces
+    of one tile spread over 1 to 4 CTAs, ranges that start and end inside
+    tiles (3 SMs: fewer CTAs than tiles, whole tiles only)."""
+    d = workloads.fp8_sweep(16)
+    ok, info = run_fp8(cuda_lib, d["x"], d["w"], num_sms=num_sms)
+    assert ok, info
 
 
 def test_fp8_rejects_fp4_only_options(cuda_lib):

@@ -237,3 +237,53 @@ def test_q8_block_bit_exact(cuda_lib, N, K):
     oc, os_ = oracle.q8_quantize(w, rows_per_block=128)
     assert np.array_equal(codes.cpu().numpy(), oc)
     assert np.array_equal(scales.cpu().numpy(), os_)
+
+
+def _q8_quotient_sweep(dtype, n_scales=512, seed=3):
+    """1 x 128 blocks whose first element A is the block amax, so the block
+    scale is s = fl32(A / 448), for a spread of A over the positive finite
+    bf16 range; the other 127 elements take every bf16 value of magnitude in
+    [A 2^-12, A] with both signs (fp32 input: as many random fp32 values in
+    that range).  These are the quotients x / s that decide the e4m3 codes,
+    under n_scales different scales; rows of 32 blocks."""
+    allbf = torch.arange(1, 0x7F80, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float()
+    A = allbf[::len(allbf) // n_scales][:n_scales]
+    g = torch.Generator().manual_seed(seed)
+    blocks = []
+    for a in A.tolist():
+        if dtype == torch.bfloat16:
+            vals = allbf[(allbf >= a * 2.0 ** -12) & (allbf <= a)]
+        else:
+            vals = a * torch.exp2(-12.0 * torch.rand(3000, generator=g))
+        vals = torch.cat([vals, -vals])
+        n = (len(vals) + 126) // 127 * 127
+        vals = torch.cat([vals, torch.zeros(n - len(vals))]).view(-1, 127)
+        blocks.append(torch.cat([torch.full((vals.shape[0], 1), a), vals], dim=1))
+    b = torch.cat(blocks)
+    b = torch.cat([b, torch.zeros((-b.shape[0]) % 32, 128)])
+    return b.reshape(-1, 4096).to(dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_q8_token_quotient_sweep(cuda_lib, dtype):
+    """FP8 1 x 128 codes and scales bit-exact against the oracle's correctly
+    rounded division over every bf16 quotient under 512 block scales."""
+    bs = cuda_lib
+    x = _q8_quotient_sweep(dtype)
+    codes, scales = bs.q8_quantize(x.cuda(), mode=bs.Q8_TOKEN)
+    torch.cuda.synchronize()
+    oc, os_ = oracle.q8_quantize(x, rows_per_block=1)
+    assert np.array_equal(scales.cpu().numpy().T, os_)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+@pytest.mark.parametrize("K", [128, 384, 4096 + 128])
+def test_q8_token_odd_block_counts(cuda_lib, K):
+    """K % 256 == 128: the last 256-element unit of a row holds one block."""
+    bs = cuda_lib
+    x = special_rows(torch.randn(37, K)).to(torch.bfloat16)
+    codes, scales = bs.q8_quantize(x.cuda(), mode=bs.Q8_TOKEN)
+    torch.cuda.synchronize()
+    oc, os_ = oracle.q8_quantize(x, rows_per_block=1)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(scales.cpu().numpy().T, os_)
