@@ -72,6 +72,9 @@ def _load():
             lib.orc_moe_rows_bound.argtypes = [I64, I, I, I]
             lib.orc_moe_dispatch.argtypes = [P, I64, I, I, I, P, P, P]
             lib.orc_swiglu.argtypes = [P, P, I64, P]
+            lib.orc_moe_router.argtypes = [P, I64, I, I, P, P]
+            lib.orc_round_bf16.restype = D
+            lib.orc_round_bf16.argtypes = [D]
             _lib = lib
     return _lib
 
@@ -255,11 +258,27 @@ def swiglu(g, u) -> np.ndarray:
     return h
 
 
-def round_bf16(y: np.ndarray) -> np.ndarray:
-    """Round FP64 values to bf16 (RNE, via fp32: exact for the tolerance used) and
-    return them as fp64."""
-    import torch
-    return torch.from_numpy(np.asarray(y, dtype=np.float64)).to(torch.bfloat16).to(torch.float64).numpy()
+def round_bf16(y) -> np.ndarray:
+    """Round FP64 values to bf16 in one step (round to nearest, ties to even;
+    orc_round_bf16) and return them as fp64."""
+    y = np.asarray(y, dtype=np.float64)
+    f = _load().orc_round_bf16
+    return np.vectorize(f, otypes=[np.float64])(y) if y.size else y.copy()
+
+
+def moe_router(logits, k: int):
+    """Top-k routing of every token from its fp32 router logits ("DeepGEMM for
+    Hopper MoE" section 1): expert ids int32 [T, k] in descending order of
+    logit (ties to the lower id) and the softmax of the chosen logits, fp64
+    [T, k]."""
+    lg = _f32(logits)
+    T, E = lg.shape
+    assert 1 <= k <= E
+    ids = np.zeros((T, k), dtype=np.int32)
+    w = np.zeros((T, k), dtype=np.float64)
+    if T:
+        _load().orc_moe_router(_p(lg), T, E, k, _p(ids), _p(w))
+    return ids, w
 
 
 def moe_layer(x, topk_ids, topk_w, wgu_codes, wgu_sf, wd_codes, wd_sf, F: int,

@@ -22,7 +22,8 @@
  *             2.2 (per-token / per-block scales), 2.3 (FP32 accumulation),
  *             5.2 (scale = max_val / 448), 5.3 (MoE grouping, contiguous
  *             per-expert rows).
- *   [DG-MOE]  "DeepGEMM for Hopper MoE", section 2.1 (C = TC(A,B) * (sA*sB)),
+ *   [DG-MOE]  "DeepGEMM for Hopper MoE", section 1 (gate -> top-k ->
+ *             experts -> weighted sum), section 2.1 (C = TC(A,B) * (sA*sB)),
  *             section 3.1 (fused swish).
  */
 #include <math.h>
@@ -363,4 +364,53 @@ void orc_moe_dispatch(const int32_t *topk_ids, int64_t T, int k, int E,
 void orc_swiglu(const double *g, const double *u, int64_t n, double *h)
 {
     for (int64_t i = 0; i < n; ++i) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+}
+
+/* Top-k router ([DG-MOE] section 1: the gate's scores pick each token's
+ * top-k experts, whose outputs are summed with softmax weights).  For token
+ * t the k experts with the largest logits, in descending order of logit,
+ * ties going to the lower expert id; weights w[t,j] = exp(l_j - l_0) /
+ * sum_i exp(l_i - l_0) over the k chosen logits (l_0 the largest), in FP64.
+ * Logits are finite; 1 <= k <= E. */
+void orc_moe_router(const float *logits, int64_t T, int E, int k,
+                    int32_t *ids, double *w)
+{
+    unsigned char *taken = (unsigned char *)malloc((size_t)E);
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;   /* strict: the lower id keeps a tie */
+            }
+            taken[best] = 1;
+            ids[t * k + j] = best;
+        }
+        const double top = l[ids[t * k]];
+        double sum = 0.0;
+        for (int j = 0; j < k; ++j) sum += exp((double)l[ids[t * k + j]] - top);
+        for (int j = 0; j < k; ++j) w[t * k + j] = exp((double)l[ids[t * k + j]] - top) / sum;
+    }
+    free(taken);
+}
+
+/* Round a double to the nearest bf16 value (8 significant bits, exponent
+ * range of fp32), ties to even, in one step: the significand is scaled to
+ * an integer in [128, 256) and rounded with rint() in the default
+ * round-to-nearest-even mode.  Values below 2^-126 round to a multiple of
+ * 2^-133 (bf16 subnormals); results beyond the largest finite bf16 become
+ * infinite.  Returned as a double. */
+double orc_round_bf16(double v)
+{
+    if (v == 0.0 || !isfinite(v)) return v;
+    const double a = fabs(v);
+    int e;
+    frexp(a, &e);                      /* a = f * 2^e, f in [0.5, 1) */
+    int q = e - 8;                     /* the unit of the 8th significant bit */
+    if (q < -133) q = -133;            /* subnormal spacing */
+    const double r = rint(ldexp(a, -q)) * ldexp(1.0, q);
+    if (r > 3.3895313892515355e38) return v < 0 ? -INFINITY : INFINITY;
+    return v < 0 ? -r : r;
 }

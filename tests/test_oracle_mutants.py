@@ -37,6 +37,12 @@ MUTANTS = {
                                "for (int64_t m = r0; m < r0 + 1; ++m)\n                for (int j = 0; j < 128; ++j) {\n"
                                "                    float a = fabsf"),
     "ties_away_from_zero": ("(d == best_d && (c & 1) == 0 && (best & 1) == 1)", "(d == best_d && c > best)"),
+    "router_ties_to_higher_id": ("if (best < 0 || l[e] > l[best]) best = e;", "if (best < 0 || l[e] >= l[best]) best = e;"),
+    "router_ascending": ("if (best < 0 || l[e] > l[best]) best = e;", "if (best < 0 || l[e] < l[best]) best = e;"),
+    "router_softmax_over_all_experts": ("for (int j = 0; j < k; ++j) sum += exp((double)l[ids[t * k + j]] - top);",
+                                        "for (int e = 0; e < E; ++e) sum += exp((double)l[e] - top);"),
+    "bf16_truncates": ("const double r = rint(ldexp(a, -q))", "const double r = trunc(ldexp(a, -q))"),
+    "bf16_nine_bits": ("int q = e - 8;", "int q = e - 9;"),
 }
 
 

@@ -414,3 +414,63 @@ def test_moe_layer_top1_single_expert_is_dense_ffn():
     y = _dequant_fp4_lib(hq, hs, F) @ _dequant_fp4_lib(dw, ds, F).T
     ref = torch.from_numpy(y).to(torch.bfloat16).double().numpy()
     assert np.array_equal(res["out"], ref)
+
+
+# ---------------------------------------------------------------------------
+# top-k router ("DeepGEMM for Hopper MoE", section 1) and bf16 rounding
+# ---------------------------------------------------------------------------
+
+def test_moe_router_hand_case():
+    rows = {r[0]: r[1:] for r in read_golden("moe_router_hand.txt")}
+    for t in range(3):
+        lg = np.array([[float(v) for v in rows[f"logits{t}"]]], dtype=np.float32)
+        ids, w = oracle.moe_router(lg, 3)
+        assert ids[0].tolist() == [int(v) for v in rows[f"ids{t}"]]
+        assert np.allclose(w[0], [float(v) for v in rows[f"w{t}"]], rtol=1e-14, atol=0)
+
+
+def test_moe_router_matches_numpy_brute_force():
+    """numpy's stable sort of -logits (ties keep the lower index first) and a
+    float64 softmax of the chosen logits, on logits rounded to one decimal so
+    that ties are frequent."""
+    g = np.random.default_rng(7)
+    for E, k in ((8, 2), (64, 8), (256, 8), (13, 13)):
+        lg = np.round(g.standard_normal((200, E)), 1).astype(np.float32)
+        ids, w = oracle.moe_router(lg, k)
+        ref = np.argsort(-lg, axis=1, kind="stable")[:, :k]
+        assert np.array_equal(ids, ref)
+        ch = np.take_along_axis(lg.astype(np.float64), ref, axis=1)
+        ex = np.exp(ch - ch.max(axis=1, keepdims=True))
+        assert np.allclose(w, ex / ex.sum(axis=1, keepdims=True), rtol=1e-13, atol=0)
+
+
+def test_moe_router_invariants():
+    g = np.random.default_rng(8)
+    # multiples of 2^-10 below 2^12 in magnitude: adding 4 below is exact in fp32
+    lg = (np.round(g.standard_normal((50, 32)) * 3 * 1024) / 1024).astype(np.float32)
+    ids, w = oracle.moe_router(lg, 8)
+    assert np.allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    assert np.all(np.diff(w, axis=1) <= 0)                 # descending logit -> descending weight
+    ids2, w2 = oracle.moe_router(lg + np.float32(4.0), 8)   # a shift of every logit changes nothing
+    assert np.array_equal(ids, ids2) and np.allclose(w, w2, rtol=1e-12)
+    ids3, w3 = oracle.moe_router(lg, 32)                    # k = E: the full softmax over all experts
+    full = np.exp(lg.astype(np.float64) - lg.max(axis=1, keepdims=True))
+    full /= full.sum(axis=1, keepdims=True)
+    assert np.allclose(np.take_along_axis(full, ids3, axis=1), w3, rtol=1e-13)
+
+
+def test_round_bf16_single_rounding():
+    import torch
+    # fp32-representable values: torch's fp32 -> bf16 cast is one rounding
+    g = np.random.default_rng(9)
+    v = np.concatenate([g.standard_normal(4000) * 10.0 ** g.integers(-30, 30, 4000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875, -2.5, 3.0e38]]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_bf16(v.astype(np.float64)), ref)
+    # a value just above a bf16 midpoint that fp32 rounds onto the midpoint:
+    # rounding twice (fp64 -> fp32 -> bf16) would go down to 1, once goes up
+    assert oracle.round_bf16([1 + 2.0 ** -8 + 2.0 ** -30])[0] == 1 + 2.0 ** -7
+    assert oracle.round_bf16([1 + 2.0 ** -8])[0] == 1.0                    # tie to even
+    assert oracle.round_bf16([1 + 3 * 2.0 ** -8])[0] == 1 + 2.0 ** -6      # tie to even (up)
+    assert oracle.round_bf16([1e-40])[0] == 2.0 ** -133                    # bf16 subnormal spacing
+    assert np.isinf(oracle.round_bf16([3.4e38])[0])
