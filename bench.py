@@ -284,8 +284,9 @@ class Fp8Sweep:
 
 
 class MoEWorkload:
-    """Grouped FP4 MoE layer: dispatch, gather + quantize, gate/up GEMM + SwiGLU,
-    re-quantize, down GEMM + routed combine, bf16 cast (one step = one layer)."""
+    """Grouped FP4 MoE layer from router logits: top-k router, dispatch, quantize +
+    gather, gate/up GEMM + SwiGLU with h re-quantized, down GEMM, routed combine
+    (one step = one layer)."""
 
     def __init__(self, large, combine="rows", graph=True, h_quant="fused"):
         import workloads
@@ -307,8 +308,8 @@ class MoEWorkload:
 
     def host_inputs(self):
         import workloads
-        r = workloads.moe_routing(self.T, self.E, self.k, index=self.index)
-        return dict(x=workloads.moe_activations(self.T, self.H, index=self.index), routing=r)
+        return dict(x=workloads.moe_activations(self.T, self.H, index=self.index),
+                    logits=workloads.moe_logits(self.T, self.E, index=self.index))
 
     def setup(self, dev):
         import torch
@@ -317,8 +318,7 @@ class MoEWorkload:
         d = self.host_inputs()
         self.h = d
         self.x = d["x"].to(dev)
-        self.ids = torch.from_numpy(d["routing"]["topk_ids"]).to(dev)
-        self.w = torch.from_numpy(d["routing"]["topk_w"]).to(dev)
+        self.logits = torch.from_numpy(d["logits"]).to(dev)
         gu, dn = [], []
         W = None
         # quantize expert by expert so the bf16 weights never all sit on the device
@@ -338,47 +338,49 @@ class MoEWorkload:
         self.layer = MoELayer(W, self.T, self.k, device=dev, combine=self.combine, h_quant=self.h_quant)
         self.out = self.layer.out
         if self.graph:
-            # capture once; from here on the workload's inputs are the graph's static ones
-            self.layer.capture(self.x, self.ids, self.w)
-            self.x, self.ids, self.w = self.layer.static_x, self.layer.static_ids, self.layer.static_w
-        # dispatch 3 + quantize 1 + gather 1 + gate/up GEMM (+ quantize h 1 on the
-        # separate path) + down GEMM, then combine 3 (invert, init, sum) or
-        # finalize 2 (cast, zero); each grouped GEMM is two launches on CTA
-        # pairs with the small experts split off (the library's default), one
-        # otherwise
+            # capture once (router included); from here on the workload's
+            # inputs are the graph's static ones
+            self.layer.capture(self.x, logits=self.logits)
+            self.x, self.logits = self.layer.static_x, self.layer.static_logits
+        # router 1 + dispatch 3 + quantize 1 + gather 1 + gate/up GEMM (+ quantize
+        # h 1 on the separate path) + down GEMM, then combine 3 (invert, init,
+        # sum) or finalize 2 (cast, zero); each grouped GEMM is two launches on
+        # CTA pairs with the small experts split off (the library's default)
         g = 2   # CTA pairs plus the one-CTA launch for experts of <= 128 rows (the library's default)
-        self.launches_per_step = (5 if self.layer.h_quant == "fused" else 6) + 2 * g + \
+        self.launches_per_step = 1 + (5 if self.layer.h_quant == "fused" else 6) + 2 * g + \
             (3 if self.combine == "rows" else 2)
-        self.bytes_in = self.x.numel() * 2 + self.ids.numel() * 4 + self.w.numel() * 4
+        self.bytes_in = self.x.numel() * 2 + self.logits.numel() * 4
         self.bytes_out = self.out.numel() * 2
-        counts = torch.bincount(self.ids.flatten().long(), minlength=E).cpu()
+        # expert loads of this routing, from the layer's own router output
+        self.layer.replay() if self.graph else self.layer.forward_logits(self.x, self.logits)
+        counts = torch.bincount(self.layer.topk_ids.flatten().long(), minlength=E).cpu()
         self.load_hist = {"max": int(counts.max()), "min": int(counts.min()), "empty": int((counts == 0).sum())}
 
     def e2e_buffers(self):
         import torch
         return [(self.x.cpu().pin_memory(), self.x if self.graph else torch.empty_like(self.x)),
-                (self.ids.cpu().pin_memory(), self.ids), (self.w.cpu().pin_memory(), self.w)]
+                (self.logits.cpu().pin_memory(), self.logits)]
 
     def step(self, x=None, gemm_events=None):
         x = self.x if x is None else x
         if gemm_events:
             gemm_events[0].record()
         if self.graph:
-            # the graph reads the static inputs (self.x / ids / w are those)
+            # the graph reads the static inputs (self.x / logits are those)
             out = self.layer.replay(None if x is self.x else x)
         else:
-            out = self.layer.forward(x, self.ids, self.w)
+            out = self.layer.forward_logits(x, self.logits)
         if gemm_events:
             gemm_events[1].record()
         return out
 
     def algorithmic_bytes(self):
         """Bytes the layer must move at least: every expert's FP4 weights and
-        their scales (read once), the bf16 activations in, the routing, the
-        bf16 output."""
-        E, H, F, T, k = self.E, self.H, self.F, self.T, self.k
+        their scales (read once), the bf16 activations and fp32 router logits
+        in, the bf16 output."""
+        E, H, F, T = self.E, self.H, self.F, self.T
         w = E * (2 * F * H + H * F)
-        return w // 2 + w // 16 + T * H * 2 + T * k * 8 + T * H * 2
+        return w // 2 + w // 16 + T * H * 2 + T * E * 4 + T * H * 2
 
     def roofline(self, layer_ms, peaks, source):
         kern = ("whole layer (grouped fp4_pair_kernel x2 + quantize + dispatch + " +
@@ -396,9 +398,11 @@ class MoEWorkload:
         import oracle
         import workloads
         h = self.h
-        r = h["routing"]
+        t0 = time.perf_counter()
+        ids, wts = oracle.moe_router(h["logits"][:rows], self.k)
+        t_router = time.perf_counter() - t0
         toks = list(range(rows))
-        experts = sorted(set(int(e) for t in toks for e in r["topk_ids"][t]))
+        experts = sorted(set(int(e) for t in toks for e in ids[t]))
         if not hasattr(self, "_ow"):
             self._ow = {}
         for e in experts:
@@ -411,10 +415,9 @@ class MoEWorkload:
         dc = [self._ow[e][1][0] if e in self._ow else None for e in range(E)]
         ds = [self._ow[e][1][1] if e in self._ow else None for e in range(E)]
         t0 = time.perf_counter()
-        oracle.moe_layer(h["x"][:rows], r["topk_ids"][:rows], r["topk_w"][:rows], gc, gs, dc, ds, F=self.F,
-                         nthreads=nthreads)
+        oracle.moe_layer(h["x"][:rows], ids, wts.astype("float32"), gc, gs, dc, ds, F=self.F, nthreads=nthreads)
         fl = 2.0 * rows * self.k * (self.H * 2 * self.F + self.F * self.H)
-        return time.perf_counter() - t0, fl
+        return time.perf_counter() - t0 + t_router, fl
 
 
 WORKLOADS = {

@@ -21,7 +21,7 @@ from ._build import LIB as _LIB_PATH
 
 __all__ = [
     "load", "sf_bytes", "sf_offset", "q4_quantize", "fp4_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
-    "grouped_gemm_fp4", "grouped_gemm_fp4_swiglu_q4", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
+    "grouped_gemm_fp4", "grouped_gemm_fp4_swiglu_q4", "moe_router_topk", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
     "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE", "EPI_ROWS", "kernel_options",
     "current_kernel_options", "FP4_ONE_CTA", "FP4_PAIR",
 ]
@@ -124,6 +124,8 @@ def load(path: str | None = None):
         lib.bs_moe_rows_bound.argtypes = [I64, I, I]
         lib.bs_moe_dispatch_workspace_bytes.restype = SZ
         lib.bs_moe_dispatch_workspace_bytes.argtypes = [I64, I, I]
+        lib.bs_moe_router_topk.restype = I
+        lib.bs_moe_router_topk.argtypes = [P, I64, I, I, P, P, P]
         lib.bs_moe_dispatch.restype = I
         lib.bs_moe_dispatch.argtypes = [P, P, I64, I, I, P, P, P, P, P, P, SZ, P]
         lib.bs_moe_dispatch_noalloc.restype = I
@@ -325,6 +327,18 @@ def grouped_gemm_fp4_swiglu_q4(a, sfa, b, sfb, K: int, N: int, E: int, offsets, 
 
 def moe_rows_bound(T: int, k: int, E: int) -> int:
     return int(load().bs_moe_rows_bound(T, k, E))
+
+
+def moe_router_topk(logits, k: int, out=None, stream=None):
+    """Top-k routing from fp32 router logits [T, E]: (topk_ids int32 [T, k] in
+    descending order of logit, ties to the lower id; topk_w fp32 [T, k], the
+    softmax of the chosen logits)."""
+    T, E = logits.shape
+    if out is None:
+        out = (torch.empty((T, k), dtype=torch.int32, device=logits.device),
+               torch.empty((T, k), dtype=torch.float32, device=logits.device))
+    _check(load().bs_moe_router_topk(_ptr(logits), T, E, k, _ptr(out[0]), _ptr(out[1]), _stream(stream)))
+    return out
 
 
 def moe_dispatch(topk_ids, topk_w, E: int, out=None, workspace=None, stream=None):

@@ -625,6 +625,22 @@ bs_status bs_grouped_gemm_swiglu_q4(const bs_gemm_args* a, int E, const int32_t*
   return launch_fp4(L, a, wrows, sms, reinterpret_cast<cudaStream_t>(stream), 0, true);
 }
 
+bs_status bs_moe_router_topk(const float* logits, int64_t T, int E, int k, int32_t* topk_ids, float* topk_w,
+                             bs_stream_t stream) {
+  if (T < 0 || E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "router: T=%lld E=%d", (long long)T, E);
+  if (k <= 0 || k > E || k > 32) return fail(BS_ERR_INVALID, "router: k=%d outside [1, min(E, 32)]", k);
+  if (T > (1LL << 31) / 8) return fail(BS_ERR_INVALID, "router: too many tokens");
+  if (T == 0) return BS_OK;
+  if (!logits || !topk_ids || !topk_w) return fail(BS_ERR_INVALID, "router: null pointer");
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(topk_ids) |
+       reinterpret_cast<uintptr_t>(topk_w)) & 3)
+    return fail(BS_ERR_ALIGN, "router: buffers must be 4-byte aligned");
+  if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_moe_router(logits, T, E, k, topk_ids, topk_w, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "router launch");
+  return BS_OK;
+}
+
 int64_t bs_moe_rows_bound(int64_t T, int k, int E) {
   if (T < 0 || k <= 0 || E <= 0) return 0;
   return T * k + (int64_t)E * 127;

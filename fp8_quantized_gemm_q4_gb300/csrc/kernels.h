@@ -147,6 +147,8 @@ cudaError_t launch_q8_quantize(const void* x, int x_bf16, long long M, long long
                                uint8_t* codes, float* scales, cudaStream_t stream);
 
 // MoE
+cudaError_t launch_moe_router(const float* logits, long long T, int E, int k, int* ids, float* w,
+                              cudaStream_t stream);
 cudaError_t launch_moe_dispatch(const int* topk_ids, const float* topk_w, long long T, int k, int E,
                                 int* counts, int* offsets, int* pair_of_row, int* token_of, float* weight_of,
                                 int* work, long long rows_bound, int* status, cudaStream_t stream);

@@ -216,6 +216,81 @@ __global__ void moe_zero_kernel(float* __restrict__ out32, long long n) {
   for (long long i = n4 * 4 + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) out32[i] = 0.0f;
 }
 
+// Top-k routing of each token from its fp32 router logits ("DeepGEMM for
+// Hopper MoE", section 1: the gate scores the experts, the top k are chosen
+// and weighted by a softmax of their scores).  One warp per token; lane l
+// holds logits l, l + 32, ... (E <= 1024, so at most 32 per lane) and a mask
+// of those not yet chosen.  Round j takes the warp's arg-max -- the larger
+// logit, the lower expert id between equal ones -- so the experts come out in
+// descending order exactly as a stable sort would give them; lane j keeps
+// the j-th pick.  Weights: exp(l_j - l_0) / sum over the k picks, in fp32.
+template <int NV>  // logits per lane: ceil(E / 32) rounded up to a power of two
+__global__ void __launch_bounds__(256) moe_router_kernel(const float* __restrict__ logits, long long T, int E, int k,
+                                                         int* __restrict__ ids, float* __restrict__ w) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const long long t = (long long)blockIdx.x * 8 + threadIdx.x / 32;
+  if (t >= T) return;
+  const float* row = logits + t * E;
+  float v[NV];
+  uint32_t live = 0;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldg(row + e) : 0.0f;
+    live |= (e < E ? 1u : 0u) << i;
+  }
+  constexpr int kNone = 0x7fffffff;
+  float my_v = 0.0f;
+  int my_e = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.0f;
+    int be = kNone;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)  // increasing expert id: strict > keeps the lower id of equal logits
+      if (((live >> i) & 1u) && (be == kNone || v[i] > bv)) {
+        bv = v[i];
+        be = lane + 32 * i;
+      }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, d);
+      if (oe != kNone && (be == kNone || ov > bv || (ov == bv && oe < be))) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) live &= ~(1u << (be >> 5));
+    if (lane == j) {
+      my_v = bv;
+      my_e = be;
+    }
+  }
+  const float top = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < k ? expf(my_v - top) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+  if (lane < k) {
+    ids[t * k + lane] = my_e;
+    w[t * k + lane] = __fdiv_rn(ex, sum);
+  }
+}
+
+cudaError_t launch_moe_router(const float* logits, long long T, int E, int k, int* ids, float* w,
+                              cudaStream_t stream) {
+  const unsigned blocks = (unsigned)((T + 7) / 8 > 0 ? (T + 7) / 8 : 1);
+  const int per_lane = (E + 31) / 32;
+  if (per_lane <= 1) return launch_kernel(moe_router_kernel<1>, blocks, 256, 0, stream, 1, logits, T, E, k, ids, w);
+  if (per_lane <= 2) return launch_kernel(moe_router_kernel<2>, blocks, 256, 0, stream, 1, logits, T, E, k, ids, w);
+  if (per_lane <= 4) return launch_kernel(moe_router_kernel<4>, blocks, 256, 0, stream, 1, logits, T, E, k, ids, w);
+  if (per_lane <= 8) return launch_kernel(moe_router_kernel<8>, blocks, 256, 0, stream, 1, logits, T, E, k, ids, w);
+  if (per_lane <= 16) return launch_kernel(moe_router_kernel<16>, blocks, 256, 0, stream, 1, logits, T, E, k, ids, w);
+  return launch_kernel(moe_router_kernel<32>, blocks, 256, 0, stream, 1, logits, T, E, k, ids, w);
+}
+
 long long moe_chunks(long long P) { return (P + kChunk - 1) / kChunk; }
 
 cudaError_t launch_moe_dispatch(const int* topk_ids, const float* topk_w, long long T, int k, int E, int* counts,

@@ -3,6 +3,8 @@
 Order of the layer ("DeepGEMM for Hopper MoE", sections 1 and 3; "DeepGEMM
 teardown (FP8 GEMM)", section 5.3):
 
+  0. bs_moe_router_topk  (forward_logits) top-k experts of every token from
+                         its router logits, softmax weights of the chosen
   1. bs_moe_dispatch     group the (token, slot) pairs by expert into
                          128-aligned contiguous segments
   2. q4_quantize         quantize each token's row once (online), then
@@ -36,7 +38,7 @@ from dataclasses import dataclass
 import torch
 
 from . import (EPI_COMBINE, EPI_ROWS, EPI_SWIGLU, fp4_gather_rows, grouped_gemm_fp4, grouped_gemm_fp4_swiglu_q4,
-               moe_combine, moe_dispatch, moe_finalize, moe_rows_bound, q4_quantize, sf_bytes)
+               moe_combine, moe_dispatch, moe_finalize, moe_router_topk, moe_rows_bound, q4_quantize, sf_bytes)
 
 
 @dataclass
@@ -104,6 +106,9 @@ class MoELayer:
         # per block) stays within about half of the 129 MB L2.
         self.combine_chunk = max(1, (64 << 20) // (T * 256 * 4))
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        # routing of forward_logits (the router's outputs, the dispatch's inputs)
+        self.topk_ids = torch.empty((T, k), dtype=torch.int32, device=device)
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=device)
         self.disp = None
         from . import load
         wsb = int(load().bs_moe_dispatch_workspace_bytes(T, k, E))
@@ -133,33 +138,47 @@ class MoELayer:
             moe_finalize(self.out32, self.out)
         return self.out
 
-    def capture(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor) -> None:
+    def forward_logits(self, x: torch.Tensor, logits: torch.Tensor) -> torch.Tensor:
+        """The layer from the router's fp32 logits [T, E]: top-k routing on the
+        GPU, then forward()."""
+        moe_router_topk(logits, self.k, out=(self.topk_ids, self.topk_w))
+        return self.forward(x, self.topk_ids, self.topk_w)
+
+    def capture(self, x: torch.Tensor, topk_ids: torch.Tensor | None = None, topk_w: torch.Tensor | None = None,
+                logits: torch.Tensor | None = None) -> None:
         """Record the whole layer (all its launches) as one CUDA graph ("Blackwell
         FP4 MoE TFLOPS optimisation", section 3.2: the compute flow captured in a
-        CUDA Graph).  The graph reads static copies of the inputs; replay()
-        refreshes them and runs the layer with one graph launch."""
+        CUDA Graph), from the routing or, given ``logits``, from the router.
+        The graph reads static copies of the inputs; replay() refreshes them and
+        runs the layer with one graph launch."""
         self.static_x = x.clone()
-        self.static_ids = topk_ids.clone()
-        self.static_w = topk_w.clone()
-        self.forward(self.static_x, self.static_ids, self.static_w)  # sizes the dispatch tables
+        self.static_logits = None if logits is None else logits.clone()
+        self.static_ids = None if topk_ids is None else topk_ids.clone()
+        self.static_w = None if topk_w is None else topk_w.clone()
+
+        def run():
+            if self.static_logits is not None:
+                self.forward_logits(self.static_x, self.static_logits)
+            else:
+                self.forward(self.static_x, self.static_ids, self.static_w)
+
+        run()  # sizes the dispatch tables
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             with torch.cuda.graph(g, stream=side):
-                self.forward(self.static_x, self.static_ids, self.static_w)
+                run()
         torch.cuda.current_stream().wait_stream(side)
         self.graph = g
 
     def replay(self, x: torch.Tensor | None = None, topk_ids: torch.Tensor | None = None,
-               topk_w: torch.Tensor | None = None) -> torch.Tensor:
+               topk_w: torch.Tensor | None = None, logits: torch.Tensor | None = None) -> torch.Tensor:
         """Run the captured layer; given inputs are first copied into the static ones."""
-        if x is not None:
-            self.static_x.copy_(x, non_blocking=True)
-        if topk_ids is not None:
-            self.static_ids.copy_(topk_ids, non_blocking=True)
-        if topk_w is not None:
-            self.static_w.copy_(topk_w, non_blocking=True)
+        for src, dst in ((x, self.static_x), (topk_ids, self.static_ids), (topk_w, self.static_w),
+                         (logits, self.static_logits)):
+            if src is not None:
+                dst.copy_(src, non_blocking=True)
         self.graph.replay()
         return self.out

@@ -297,6 +297,23 @@ bs_status bs_grouped_gemm_swiglu_q4(const bs_gemm_args *args, int E, const int32
                                     bs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * bs_moe_router_topk -- top-k routing of every token from its router logits
+ * ("DeepGEMM for Hopper MoE", section 1: the gate scores every expert for a
+ * token, the top k are chosen and their outputs summed with softmax weights).
+ * For token t: topk_ids[t, 0..k) are the k experts with the largest logits in
+ * descending order, ties going to the lower expert id (the order a stable sort
+ * gives), and topk_w[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k
+ * chosen logits, in fp32 (within a few ulp of the exact softmax).
+ *
+ *   logits    fp32 [T, E], finite; topk_ids int32 [T, k]; topk_w fp32 [T, k]
+ *   1 <= E <= 1024, 1 <= k <= min(E, 32); buffers 4-byte aligned
+ * The outputs are bs_moe_dispatch's inputs.  Invalid sizes or pointers return
+ * BS_ERR_INVALID / BS_ERR_ALIGN before any launch.
+ * ------------------------------------------------------------------------- */
+bs_status bs_moe_router_topk(const float *logits, int64_t T, int E, int k, int32_t *topk_ids,
+                             float *topk_w, bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * bs_moe_dispatch -- group the T*k (token, slot) pairs of a top-k routing by
  * expert ("DeepGEMM teardown", section 5.3: each expert's rows contiguous and
  * movable in whole blocks).  Rows of expert e, in increasing pair index

@@ -33,3 +33,13 @@ def tight_errors(y, y_ref, S, bf16_out):
     err = np.abs(y - y_ref)
     bound = 1e-4 * S + (2.0 ** -8 * np.abs(y_ref) if bf16_out else 0.0) + 1e-30
     return bool(np.all(err <= bound)), float((err / bound).max(initial=0.0))
+
+
+def routing(T, E, k, index=3):
+    """Seeded router logits and the oracle's top-k routing of them: dict with
+    logits fp32 [T, E], topk_ids int32 [T, k], topk_w fp32 [T, k]."""
+    import oracle
+    import workloads
+    logits = workloads.moe_logits(T, E, index=index)
+    ids, w = oracle.moe_router(logits, k)
+    return dict(logits=logits, topk_ids=ids, topk_w=w.astype(np.float32))

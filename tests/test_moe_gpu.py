@@ -14,9 +14,15 @@ import torch
 import oracle
 import workloads
 from tests.conftest import read_golden
-from tests.helpers import gemm_errors, sf_rowmajor
+from tests.helpers import gemm_errors, sf_rowmajor, routing
 
 pytestmark = pytest.mark.gpu
+
+# Router weights: the GPU takes exp(l_j - l_0) in fp32 (one rounding of the
+# difference, scaled by |l_j - l_0| <= 32 here, plus expf's <= 2 ulp), sums k
+# <= 32 terms and divides once: relative error below (32 + 2 + 32 + 1) 2^-24
+# < 4e-6 of the FP64 softmax.
+ROUTER_RTOL = 4e-6
 
 
 @pytest.fixture(params=["pair", "pair_whole", "one_cta"])
@@ -47,7 +53,7 @@ def test_dispatch_hand_case(cuda_lib):
 @pytest.mark.parametrize("T,E,k", [(1, 4, 2), (300, 9, 4), (4096, 64, 8), (16384, 256, 8)])
 def test_dispatch_bit_exact(cuda_lib, T, E, k):
     bs = cuda_lib
-    r = workloads.moe_routing(T, E, k)
+    r = routing(T, E, k)
     ids, w = torch.from_numpy(r["topk_ids"]), torch.from_numpy(r["topk_w"])
     d = bs.moe_dispatch(ids.cuda(), w.cuda(), E=E)
     torch.cuda.synchronize()
@@ -66,7 +72,7 @@ def test_dispatch_bit_exact(cuda_lib, T, E, k):
 
 
 def _small_moe(T=200, H=256, F=128, E=5, k=2, seed=3):
-    r = workloads.moe_routing(T, E, k, index=seed)
+    r = routing(T, E, k, index=seed)
     x = workloads.moe_activations(T, H, index=seed)
     ws = [workloads.moe_expert_weights(e, F, H, index=seed) for e in range(E)]
     return r, x, ws
@@ -232,12 +238,22 @@ def test_full_size_layer_sampled_tokens(cuda_lib, cfg, index):
     from fp8_quantized_gemm_q4_gb300.moe import MoELayer, MoEWeights
     c = getattr(workloads, cfg)
     T, H, E, k, F = c["T"], c["H"], c["E"], c["k"], c["F"]
-    r = workloads.moe_routing(T, E, k, index=index)
+    r = routing(T, E, k, index=index)
     x = workloads.moe_activations(T, H, index=index)
     ids = r["topk_ids"]
-    # tokens: first, middle, last, and one routed to the most loaded expert
-    heavy = int(np.bincount(ids.reshape(-1), minlength=E).argmax())
-    samples = sorted({0, T // 2, T - 1, int(np.nonzero((ids == heavy).any(axis=1))[0][0])})
+    # tokens: first, middle, last; one routed to the most loaded expert; one
+    # routed to an expert of at most 128 rows (served by the one-CTA launch);
+    # the last token of an expert whose last 256-row pair tile is partly full
+    cnt = np.bincount(ids.reshape(-1), minlength=E)
+    heavy = int(cnt.argmax())
+    small = [e for e in range(E) if 1 <= cnt[e] <= 128]
+    partial = [e for e in range(E) if cnt[e] > 128 and cnt[e] % 256 != 0]
+    assert small and partial
+
+    def token_of(e, last=False):
+        return int(np.nonzero((ids == e).any(axis=1))[0][-1 if last else 0])
+
+    samples = sorted({0, T // 2, T - 1, token_of(heavy), token_of(small[0]), token_of(partial[0], last=True)})
     experts = sorted({int(e) for t in samples for e in ids[t]})
     F2 = 2 * F
     wgu_codes = torch.empty((E * F2, H // 2), dtype=torch.uint8, device="cuda")
@@ -255,13 +271,19 @@ def test_full_size_layer_sampled_tokens(cuda_lib, cfg, index):
         del wgu, wd
     Wt = MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf)
     layer = MoELayer(Wt, T, k, h_quant="separate")  # bf16 h visible for the stages
-    out = layer.forward(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(r["topk_w"]).cuda())
+    # from the router's logits, as the bench runs it: the GPU router's experts
+    # equal the oracle's, its weights are within the fp32 softmax's rounding
+    out = layer.forward_logits(x.cuda(), torch.from_numpy(r["logits"]).cuda())
     torch.cuda.synchronize()
     assert bs.device_status()[0] == 0
+    assert np.array_equal(layer.topk_ids.cpu().numpy(), ids)
+    _, w64 = oracle.moe_router(r["logits"], k)
+    wts = layer.topk_w.cpu().numpy()
+    assert np.allclose(wts, w64, rtol=ROUTER_RTOL, atol=0)
     # the bench's path (h quantized in the gate/up epilogue): same codes and
     # scales on every row of the expert segments, same output bit for bit
     fused = MoELayer(Wt, T, k)
-    out_f = fused.forward(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(r["topk_w"]).cuda())
+    out_f = fused.forward_logits(x.cuda(), torch.from_numpy(r["logits"]).cuda())
     torch.cuda.synchronize()
     assert bs.device_status()[0] == 0
     seg_rows = int(fused.disp["offsets"][E])
@@ -300,7 +322,7 @@ def test_full_size_layer_sampled_tokens(cuda_lib, cfg, index):
             bound = 1e-3 * (dsilu * np.abs(u_) * s_gu[:, :F] + np.abs(g_ * sig) * s_gu[:, F:]) + 2.0 ** -8 * np.abs(h_ref)
             assert np.all(np.abs(h[n:n + 1] - h_ref) <= bound + 1e-30), (t, j)
             y, sy = oracle.gemm_fp4(hq[n:n + 1], hs[n:n + 1], d_c, d_s, F)
-            wgt = float(r["topk_w"][t, j])
+            wgt = float(wts[t, j])
             ref += wgt * y[0]
             S += abs(wgt) * sy[0]
         ok, ratio, rel = gemm_errors(got[t:t + 1], ref[None], S[None], True)
@@ -329,3 +351,33 @@ def test_layer_graph_replay_matches_forward(cuda_lib):
     torch.cuda.synchronize()
     assert cuda_lib.device_status()[0] == 0
     assert torch.equal(out1, ref) and torch.equal(out2, ref2) and torch.equal(out3, ref)
+
+
+@pytest.mark.parametrize("T,E,k,ties", [(4096, 64, 8, False), (16384, 256, 8, False), (37, 13, 13, True),
+                                        (300, 1024, 32, False), (5, 33, 1, True), (700, 256, 8, True),
+                                        (0, 64, 8, False)])
+def test_router_topk_matches_oracle(cuda_lib, T, E, k, ties):
+    """Top-k experts bit-exact against the oracle (the same fp32 logits decide
+    both), weights within ROUTER_RTOL of its FP64 softmax.  `ties`: logits
+    rounded to one decimal, so equal logits are common and the lower expert
+    id must win every tie."""
+    bs = cuda_lib
+    logits = workloads.moe_logits(max(T, 1), E, index=T + E)[:T]
+    if ties:
+        logits = np.round(logits, 1).astype(np.float32)
+    ids, w = bs.moe_router_topk(torch.from_numpy(logits).cuda(), k)
+    torch.cuda.synchronize()
+    oids, ow = oracle.moe_router(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    assert np.allclose(w.cpu().numpy(), ow, rtol=ROUTER_RTOL, atol=0)
+
+
+def test_router_rejects_bad_sizes(cuda_lib):
+    bs = cuda_lib
+    lg = torch.zeros((4, 8), device="cuda")
+    for k in (0, 9):
+        with pytest.raises(bs.BSError) as e:
+            bs.moe_router_topk(lg, k)
+        assert e.value.status == bs.BS_ERR_INVALID
+    with pytest.raises(bs.BSError):
+        bs.moe_router_topk(torch.zeros((4, 40), device="cuda"), 33)   # k > 32

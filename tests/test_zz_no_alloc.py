@@ -16,6 +16,7 @@ import pytest
 import torch
 
 import workloads
+from tests.helpers import routing
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +44,7 @@ def test_noalloc_dispatch_matches_workspace_dispatch():
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     # two different routings, the second with more pairs and a different E
     for (T, E, k, seed) in [(4096, 64, 8, 11), (16384, 256, 8, 12)]:
-        r = workloads.moe_routing(T, E, k, index=seed)
+        r = routing(T, E, k, index=seed)
         ids = torch.from_numpy(r["topk_ids"]).to(dev)
         w = torch.from_numpy(r["topk_w"]).to(dev)
         ref = bs.moe_dispatch(ids, w, E)

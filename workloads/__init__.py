@@ -15,9 +15,8 @@ Workloads (sizes and distributions of the pages' configurations):
                           x50; W bf16 [7168,4096] ~ N(0,0.02)
   3  MoE T=4096 H=4096 E=64 k=8 F=1536
   4  MoE T=16384 H=7168 E=256 k=8 F=2048
-  MoE router logits ~ N(0,1) + beta_e, beta_e = -1.2 ln(rank_e) for a seeded
-  permutation rank of 1..E (log-Zipf, alpha = 1.2); top-k by logit with ties
-  to the lower expert id; routing weights = softmax over the k chosen logits.
+  MoE router logits (fp32) ~ N(0,1) + beta_e, beta_e = -1.2 ln(rank_e) for a
+  seeded permutation rank of 1..E (log-Zipf, alpha = 1.2).
 """
 from __future__ import annotations
 
@@ -72,17 +71,15 @@ def fp8_sweep(M, N=7168, K=4096, index: int = 2, outlier_frac=0.01, outlier_mult
     return dict(x=to_bf16(x), w=to_bf16(w), outlier_channels=np.sort(ch))
 
 
-def moe_routing(T, E, k, index: int = 3, zipf_alpha=1.2):
-    """Router logits and the top-k routing of each token (inputs to the MoE path)."""
+def moe_logits(T, E, index: int = 3, zipf_alpha=1.2):
+    """Router logits [T, E] fp32: N(0, 1) plus a log-Zipf expert bias
+    beta_e = -alpha ln(rank_e) over a seeded permutation rank of 1..E (skewed
+    expert loads, some experts empty).  The routing itself (top-k, softmax)
+    is part of the path: the GPU router, or the oracle's."""
     g = rng(index, salt=2)
     rank = g.permutation(E) + 1
     beta = -zipf_alpha * np.log(rank.astype(np.float64))
-    logits = g.standard_normal((T, E)) + beta[None, :]
-    order = np.argsort(-logits, axis=1, kind="stable")[:, :k]
-    chosen = np.take_along_axis(logits, order, axis=1)
-    ex = np.exp(chosen - chosen.max(axis=1, keepdims=True))
-    w = ex / ex.sum(axis=1, keepdims=True)
-    return dict(topk_ids=order.astype(np.int32), topk_w=w.astype(np.float32), logits=logits)
+    return (g.standard_normal((T, E)) + beta[None, :]).astype(np.float32)
 
 
 def moe_activations(T, H, index: int = 3):
