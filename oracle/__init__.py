@@ -75,6 +75,11 @@ def _load():
             lib.orc_moe_router.argtypes = [P, I64, I, I, P, P]
             lib.orc_round_bf16.restype = D
             lib.orc_round_bf16.argtypes = [D]
+            lib.orc_q4_two_level_exp.restype = I
+            lib.orc_q4_two_level_exp.argtypes = [ctypes.c_float]
+            lib.orc_q4_quantize_two_level.argtypes = [P, I64, I64, I64, P, P, P]
+            lib.orc_q8_quantize_rowwise.argtypes = [P, I64, I64, I64, P, P]
+            lib.orc_gemm_fp8_rowwise.argtypes = [P, P, P, P, I64, I64, I64, P, P]
             _lib = lib
     return _lib
 
@@ -176,6 +181,37 @@ def q8_quantize(x, rows_per_block: int = 1):
     return codes, scales
 
 
+def q4_two_level_exp(amax: float) -> int:
+    """Exponent e of the two-level FP4 tensor scale 2^e: the smallest e with
+    amax <= 6 * 448 * 2^e (0 for a zero tensor)."""
+    return int(_load().orc_q4_two_level_exp(float(np.float32(amax))))
+
+
+def q4_quantize_two_level(x):
+    """Two-level FP4: a power-of-two tensor scale 2^e above the e4m3 group
+    scales.  Returns (codes [M, K/2], group scales [M, K/16], tensor scale
+    2^e as a float)."""
+    x = _f32(x)
+    M, K = x.shape
+    codes = np.zeros((M, K // 2), dtype=np.uint8)
+    sf = np.zeros((M, K // 16), dtype=np.uint8)
+    ts = np.zeros(1, dtype=np.float32)
+    _load().orc_q4_quantize_two_level(_p(x), M, K, K, _p(codes), _p(sf), _p(ts))
+    return codes, sf, float(ts[0])
+
+
+def q8_quantize_rowwise(x):
+    """FP8 with one fp32 scale per row over all of K (W8A8: per-token
+    activations, per-channel weights).  Returns (codes [M, K], scales [M])."""
+    x = _f32(x)
+    M, K = x.shape
+    codes = np.zeros((M, K), dtype=np.uint8)
+    scales = np.zeros(M, dtype=np.float32)
+    if M:
+        _load().orc_q8_quantize_rowwise(_p(x), M, K, K, _p(codes), _p(scales))
+    return codes, scales
+
+
 # ---------------------------------------------------------------------------
 # GEMMs
 # ---------------------------------------------------------------------------
@@ -228,6 +264,21 @@ def gemm_fp8(a_codes, sa, b_codes, sb, nthreads=None):
     if M and N:
         _load().orc_gemm_fp8(_p(a_codes), _p(sa), _p(b_codes), _p(sb), M, N, K, _p(y), _p(s),
                              nthreads or default_threads())
+    return y, s
+
+
+def gemm_fp8_rowwise(a_codes, sa, b_codes, sb):
+    """W8A8 GEMM y = sa[m] sb[n] sum_k a b in FP64 (plus the error scale)."""
+    a_codes = np.ascontiguousarray(a_codes, dtype=np.uint8)
+    b_codes = np.ascontiguousarray(b_codes, dtype=np.uint8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32).reshape(-1)
+    sb = np.ascontiguousarray(sb, dtype=np.float32).reshape(-1)
+    M, K = a_codes.shape
+    N = b_codes.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    s = np.zeros((M, N), dtype=np.float64)
+    if M and N:
+        _load().orc_gemm_fp8_rowwise(_p(a_codes), _p(sa), _p(b_codes), _p(sb), M, N, K, _p(y), _p(s))
     return y, s
 
 

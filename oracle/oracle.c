@@ -22,6 +22,10 @@
  *             2.2 (per-token / per-block scales), 2.3 (FP32 accumulation),
  *             5.2 (scale = max_val / 448), 5.3 (MoE grouping, contiguous
  *             per-expert rows).
+ *   [INFRA-G] "Tencent AI Infra interview notes" -- the scale-granularity
+ *             table (per-tensor [1], per-channel [N], per-token [M], per-group)
+ *             and W8A8 SmoothQuant: X per-token scale_x [M,1], W per-channel
+ *             scale_w [1,N], Y = acc * scale_x * scale_w^T.
  *   [DG-MOE]  "DeepGEMM for Hopper MoE", section 1 (gate -> top-k ->
  *             experts -> weighted sum), section 2.1 (C = TC(A,B) * (sA*sB)),
  *             section 3.1 (fused swish).
@@ -413,4 +417,85 @@ double orc_round_bf16(double v)
     const double r = rint(ldexp(a, -q)) * ldexp(1.0, q);
     if (r > 3.3895313892515355e38) return v < 0 ? -INFINITY : INFINITY;
     return v < 0 ? -r : r;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Format variants                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Two-level FP4 scaling: a per-tensor scale ([INFRA-G] per-tensor row of the
+ * granularity table) above the per-group e4m3 scales.  Reading: the tensor
+ * scale is the power of two 2^e with the smallest e such that
+ * amax_tensor <= 6 * 448 * 2^e, so that the largest group scale
+ * amax / (6 * 2^e) fills e4m3's top binade without saturating and applying
+ * the tensor scale is exact.  The tensor is divided by 2^e (x' = fl32(x 2^-e))
+ * and quantized group by group as orc_q4_quantize does; the value a code
+ * stands for is code * s_group * 2^e.  A zero tensor takes e = 0.         */
+int orc_q4_two_level_exp(float amax)
+{
+    if (!(amax > 0.0f)) return 0;
+    int e = 0;
+    while ((double)amax > 2688.0 * ldexp(1.0, e)) ++e;
+    while ((double)amax <= 2688.0 * ldexp(1.0, e - 1)) --e;
+    return e;
+}
+
+void orc_q4_quantize_two_level(const float *x, int64_t M, int64_t K, int64_t ldx,
+                               uint8_t *codes, uint8_t *sf, float *tensor_scale)
+{
+    float amax = 0.0f;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(x[m * ldx + k]);
+            if (a > amax) amax = a;
+        }
+    const int e = orc_q4_two_level_exp(amax);
+    float *xs = (float *)malloc((size_t)(M * K > 0 ? M * K : 1) * sizeof(float));
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) xs[m * K + k] = (float)ldexp((double)x[m * ldx + k], -e);
+    orc_q4_quantize(xs, M, K, K, codes, sf);
+    free(xs);
+    *tensor_scale = (float)ldexp(1.0, e);
+}
+
+/* FP8 with one fp32 scale per row over all of K ([INFRA-G] W8A8: per-token
+ * scale_x [M,1] for activations, per-channel scale_w [1,N] for weights, the
+ * weights held as [N, K] so a channel is a row):
+ *   s[m]    = fl32(amax_row / 448)
+ *   code    = e4m3(fl32(x / s[m])),  or 0 when s[m] == 0                  */
+void orc_q8_quantize_rowwise(const float *x, int64_t M, int64_t K, int64_t ldx,
+                             uint8_t *codes, float *scales)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(x[m * ldx + k]);
+            if (a > amax) amax = a;
+        }
+        const float srow = div_f32(amax, 448.0f);
+        scales[m] = srow;
+        for (int64_t k = 0; k < K; ++k)
+            codes[m * K + k] = (srow == 0.0f) ? 0 : orc_e4m3_encode(div_f32(x[m * ldx + k], srow));
+    }
+}
+
+/* W8A8 GEMM ([INFRA-G] Y = acc * scale_x * scale_w^T):
+ *   y[m,n] = sa[m] * sb[n] * sum_k dec(a[m,k]) dec(b[n,k])   in FP64, and
+ *   s[m,n] = sum_k |sa[m] dec(a) sb[n] dec(b)|  (the error scale).        */
+void orc_gemm_fp8_rowwise(const uint8_t *a8, const float *sa, const uint8_t *b8,
+                          const float *sb, int64_t M, int64_t N, int64_t K,
+                          double *y, double *s)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double prod = orc_e4m3_decode(a8[m * K + k]) * orc_e4m3_decode(b8[n * K + k]);
+                acc += prod;
+                mag += fabs(prod);
+            }
+            const double f = (double)sa[m] * (double)sb[n];
+            y[m * N + n] = f * acc;
+            s[m * N + n] = fabs(f) * mag;
+        }
 }

@@ -43,6 +43,14 @@ MUTANTS = {
                                         "for (int e = 0; e < E; ++e) sum += exp((double)l[e] - top);"),
     "bf16_truncates": ("const double r = rint(ldexp(a, -q))", "const double r = trunc(ldexp(a, -q))"),
     "bf16_nine_bits": ("int q = e - 8;", "int q = e - 9;"),
+    "two_level_fits_448_not_6x448": ("while ((double)amax <= 2688.0 * ldexp(1.0, e - 1)) --e;",
+                                     "while ((double)amax <= 448.0 * ldexp(1.0, e - 1)) --e;"),
+    "two_level_scale_off_by_one": ("*tensor_scale = (float)ldexp(1.0, e);", "*tensor_scale = (float)ldexp(1.0, e + 1);"),
+    "two_level_unscaled_input": ("xs[m * K + k] = (float)ldexp((double)x[m * ldx + k], -e);",
+                                 "xs[m * K + k] = x[m * ldx + k];"),
+    "rowwise_scale_447": ("const float srow = div_f32(amax, 448.0f);", "const float srow = div_f32(amax, 447.0f);"),
+    "rowwise_gemm_drops_weight_scale": ("const double f = (double)sa[m] * (double)sb[n];",
+                                        "const double f = (double)sa[m];"),
 }
 
 

@@ -474,3 +474,80 @@ def test_round_bf16_single_rounding():
     assert oracle.round_bf16([1 + 3 * 2.0 ** -8])[0] == 1 + 2.0 ** -6      # tie to even (up)
     assert oracle.round_bf16([1e-40])[0] == 2.0 ** -133                    # bf16 subnormal spacing
     assert np.isinf(oracle.round_bf16([3.4e38])[0])
+
+
+# ---------------------------------------------------------------------------
+# format variants: two-level FP4, W8A8 per-row FP8 ("Tencent AI Infra
+# interview notes": scale-granularity table, W8A8 SmoothQuant)
+# ---------------------------------------------------------------------------
+
+def test_q4_two_level_exponent_is_the_smallest_that_fits():
+    assert oracle.q4_two_level_exp(0.0) == 0
+    for amax in (2688.0, 2688.0001, 1344.0, 1344.0001, 0.1, 0.02, 3.0e-30, 1.0e30, 6.0, 448.0 * 6 * 2 ** -20):
+        e = oracle.q4_two_level_exp(amax)
+        a = float(np.float32(amax))
+        assert a <= 6 * 448 * 2.0 ** e          # the largest group scale does not exceed 448
+        assert a > 6 * 448 * 2.0 ** (e - 1)     # and one power of two less would
+
+
+def test_q4_two_level_is_one_level_on_the_scaled_tensor():
+    """Codes and group scales equal the library casts' quantization of the
+    tensor divided (exactly) by its power-of-two scale."""
+    g = np.random.default_rng(11)
+    for std in (0.02, 1.0, 300.0):
+        x = (g.standard_normal((6, 128)) * std).astype(np.float32)
+        x[1, 16:32] = 0
+        codes, sf, ts = oracle.q4_quantize_two_level(x)
+        e = oracle.q4_two_level_exp(np.abs(x).max())
+        assert ts == 2.0 ** e
+        ref_codes, ref_sf = _lib_q4(np.ldexp(x, -e).astype(np.float32))
+        assert np.array_equal(sf, ref_sf)
+        assert np.array_equal(oracle.unpack_e2m1(codes, 128), ref_codes)
+
+
+def test_q4_two_level_scales_use_the_top_binade_and_dequantize():
+    g = np.random.default_rng(12)
+    x = (g.standard_normal((16, 256)) * 0.02).astype(np.float32)
+    codes, sf, ts = oracle.q4_quantize_two_level(x)
+    smax = oracle.e4m3_decode(int(sf.max()))
+    assert 256.0 <= smax <= 448.0
+    c = oracle.unpack_e2m1(codes, 256)
+    s = np.vectorize(oracle.e4m3_decode)(sf).repeat(16, axis=1)
+    deq = np.vectorize(oracle.e2m1_decode)(c) * s * ts
+    assert np.all(np.abs(deq - x) <= s * ts + 1e-30)     # within one unit of the local grid
+    # the point of the second level: N(0, 0.02) weights, whose one-level group
+    # scales are e4m3 subnormals with 2-3 significant bits, lose less (over
+    # 256 groups the mean error drops by about 6 %)
+    c1, sf1 = oracle.q4_quantize(x)
+    s1 = np.vectorize(oracle.e4m3_decode)(sf1).repeat(16, axis=1)
+    deq1 = np.vectorize(oracle.e2m1_decode)(oracle.unpack_e2m1(c1, 256)) * s1
+    assert np.abs(deq - x).mean() < 0.97 * np.abs(deq1 - x).mean()
+
+
+def test_q8_rowwise_matches_library_casts():
+    g = np.random.default_rng(13)
+    x = g.standard_normal((5, 384)).astype(np.float32)
+    x[:, 7] *= 50
+    x[3, :] = 0
+    codes, scales = oracle.q8_quantize_rowwise(x)
+    s = (np.abs(x).max(axis=1) / np.float32(448)).astype(np.float32)
+    assert np.array_equal(scales, s)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = (x / s[:, None]).astype(np.float32)
+    q[s == 0] = 0
+    ref = torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+
+
+def test_gemm_fp8_rowwise_matches_matmul_of_dequantized():
+    g = np.random.default_rng(14)
+    xa = g.standard_normal((9, 256)).astype(np.float32)
+    xb = (g.standard_normal((130, 256)) * 0.02).astype(np.float32)
+    a, sa = oracle.q8_quantize_rowwise(xa)
+    b, sb = oracle.q8_quantize_rowwise(xb)
+    y, s = oracle.gemm_fp8_rowwise(a, sa, b, sb)
+    da = torch.from_numpy(a).view(torch.float8_e4m3fn).to(torch.float64).numpy() * sa[:, None]
+    db = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy() * sb[:, None]
+    ref = da @ db.T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert np.all(s >= np.abs(y) - 1e-12)
