@@ -283,6 +283,119 @@ class Fp8Sweep:
         return time.perf_counter() - t0, 2.0 * rows * cols * self.K
 
 
+class Fp8W8A8(Fp8Sweep):
+    """FP8 W8A8 ("Tencent AI Infra interview notes", SmoothQuant): one fp32
+    scale per token row of X and per channel of W, Y = s_x[m] s_w[n] sum_k a b
+    (no per-block promotion).  Step = q8_quantize(X, per row) + GEMM."""
+
+    def __init__(self, M):
+        super().__init__(M)
+        self.name = f"fp8_w8a8_M{M}_N7168_K4096_outliers"
+        self.metric = f"FP8 W8A8 GEMM TFLOPS (M={M}, N=7168, K=4096, per-token x per-channel scales)"
+        self.dtype = "e4m3 x e4m3 (fp32 per-token / per-channel scales), fp32 accumulate, bf16 out"
+        self.gemm_bytes = self.N * self.K + self.N * 4 + self.M * self.K + self.M * 4 + self.M * self.N * 2
+
+    def setup(self, dev):
+        import torch
+        import fp8_quantized_gemm_q4_gb300 as bs
+        d = self.host_inputs()
+        self.h = d
+        self.x = d["x"].to(dev)
+        self.wq, self.ws = bs.q8_quantize(d["w"].to(dev), mode=bs.Q8_ROW)
+        self.xq = torch.empty((self.M, self.K), dtype=torch.uint8, device=dev)
+        self.xs = torch.empty((self.M,), dtype=torch.float32, device=dev)
+        self.out = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 2
+        self.bytes_in = self.x.numel() * 2
+        self.bytes_out = self.out.numel() * 2
+
+    def step(self, x=None, gemm_events=None):
+        import fp8_quantized_gemm_q4_gb300 as bs
+        x = self.x if x is None else x
+        bs.q8_quantize(x, mode=bs.Q8_ROW, out=(self.xq, self.xs))
+        if gemm_events:
+            gemm_events[0].record()
+        bs.gemm_fp8(self.xq, self.xs, self.wq, self.ws, out=self.out, weights_ready=True, rowwise=True)
+        if gemm_events:
+            gemm_events[1].record()
+        return self.out
+
+    def oracle_sample(self, rows, cols, nthreads):
+        import oracle
+        h = self.h
+        if not hasattr(self, "_ow"):
+            self._ow = {}
+        if cols not in self._ow:
+            self._ow[cols] = oracle.q8_quantize_rowwise(h["w"][:cols])
+        ob, osb = self._ow[cols]
+        t0 = time.perf_counter()
+        oa, osa = oracle.q8_quantize_rowwise(h["x"][:rows])
+        oracle.gemm_fp8_rowwise(oa, osa, ob, osb)
+        return time.perf_counter() - t0, 2.0 * rows * cols * self.K
+
+
+class DenseTwoLevel(DenseLowRank):
+    """Dense W4A4 8192^3 with two-level FP4 operands (power-of-two tensor
+    scale above the e4m3 group scales; weights N(0, 0.02)), bf16 out, no
+    low-rank branch.  Step = tensor amax + two-level quantize of X + GEMM."""
+
+    def __init__(self):
+        super().__init__(tiny=False)
+        self.name = "dense_w4a4_two_level_8192x8192x8192_bf16out"
+        self.metric = "block-scaled FP4 GEMM TFLOPS (dense W4A4, two-level scales)"
+        self.dtype = "e2m1 x e2m1 (e4m3 group-16 x power-of-two tensor scales), fp32 accumulate, bf16 out"
+
+    def host_inputs(self):
+        import workloads
+        d = workloads.dense_lowrank(lowrank=False, bias=False)
+        d["w"] = (d["w"].float() * 0.02).to(d["w"].dtype)
+        return d
+
+    def setup(self, dev):
+        import torch
+        import fp8_quantized_gemm_q4_gb300 as bs
+        d = self.host_inputs()
+        self.h = d
+        self.x = d["x"].to(dev)
+        self.wq, self.ws, self.wts = bs.q4_quantize_two_level(d["w"].to(dev))
+        M, N, K = self.M, self.N, self.K
+        self.xq = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+        self.xs = torch.empty(bs.sf_bytes(M, K), dtype=torch.uint8, device=dev)
+        self.xts = torch.empty(1, dtype=torch.float32, device=dev)
+        self.amax = torch.empty(1, dtype=torch.float32, device=dev)
+        self.out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 4   # amax (zero + reduce), quantize, GEMM
+        self.kernel_src = "fp8_quantized_gemm_q4_gb300/csrc/gemm_fp4_pair.cu"
+        self.bytes_in = self.x.numel() * 2
+        self.bytes_out = self.out.numel() * 2
+
+    def step(self, x=None, gemm_events=None):
+        import fp8_quantized_gemm_q4_gb300 as bs
+        x = self.x if x is None else x
+        bs.tensor_amax(x, out=self.amax)
+        bs.q4_quantize_two_level(x, amax=self.amax, out=(self.xq, self.xs, self.xts))
+        if gemm_events:
+            gemm_events[0].record()
+        bs.gemm_fp4(self.xq, self.xs, self.wq, self.ws, self.K, out=self.out, a_tensor_scale=self.xts,
+                    b_tensor_scale=self.wts)
+        if gemm_events:
+            gemm_events[1].record()
+        return self.out
+
+    def oracle_sample(self, rows, cols, nthreads):
+        import oracle
+        h = self.h
+        if not hasattr(self, "_ow"):
+            self._ow = {}
+        if cols not in self._ow:
+            self._ow[cols] = oracle.q4_quantize_two_level(h["w"][:cols])
+        ob, osb, tb = self._ow[cols]
+        t0 = time.perf_counter()
+        oa, osa, ta = oracle.q4_quantize_two_level(h["x"][:rows])
+        oracle.gemm_fp4(oa, osa, ob, osb, self.K, alpha=ta * tb, nthreads=nthreads)
+        return time.perf_counter() - t0, 2.0 * rows * cols * self.K
+
+
 class MoEWorkload:
     """Grouped FP4 MoE layer from router logits: top-k router, dispatch, quantize +
     gather, gate/up GEMM + SwiGLU with h re-quantized, down GEMM, routed combine
@@ -428,6 +541,9 @@ WORKLOADS = {
     "fp8_m64": lambda: Fp8Sweep(64),
     "fp8_m128": lambda: Fp8Sweep(128),
     "fp8_m4096": lambda: Fp8Sweep(4096),
+    "fp8_w8a8_m16": lambda: Fp8W8A8(16),
+    "fp8_w8a8_m4096": lambda: Fp8W8A8(4096),
+    "dense_two_level": lambda: DenseTwoLevel(),
     "moe_small": lambda: MoEWorkload(large=False),
     "moe_large": lambda: MoEWorkload(large=True),
 }
@@ -567,7 +683,7 @@ def check_device_status():
 # The other configurations of the metric ("block-scaled FP4/FP8 GEMM TFLOPS &
 # % of GB300 dense peak; MoE layer us"), timed in the same run as the dense
 # headline and reported beside it.
-EXTRAS = ("moe_small", "moe_large", "fp8_m16", "fp8_m4096")
+EXTRAS = ("moe_small", "moe_large", "fp8_m16", "fp8_m4096", "fp8_w8a8_m16", "fp8_w8a8_m4096")
 
 
 def run_extra(args, name, world, dev, peaks, source):

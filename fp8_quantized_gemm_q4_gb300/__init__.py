@@ -20,7 +20,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 
 __all__ = [
-    "load", "sf_bytes", "sf_offset", "q4_quantize", "fp4_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
+    "load", "sf_bytes", "sf_offset", "q4_quantize", "tensor_amax", "q4_quantize_two_level", "fp4_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
     "grouped_gemm_fp4", "grouped_gemm_fp4_swiglu_q4", "moe_router_topk", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
     "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE", "EPI_ROWS", "kernel_options",
     "current_kernel_options", "FP4_ONE_CTA", "FP4_PAIR",
@@ -30,7 +30,7 @@ BS_OK, BS_ERR_INVALID, BS_ERR_ALIGN, BS_ERR_UNSUPPORTED, BS_ERR_CUDA, BS_ERR_TIM
 DTYPE_F32, DTYPE_BF16 = 0, 1
 FMT_FP4, FMT_FP8 = 0, 1
 EPI_STORE, EPI_SWIGLU, EPI_COMBINE, EPI_ROWS = 0, 1, 2, 3
-Q8_TOKEN, Q8_BLOCK = 1, 128
+Q8_TOKEN, Q8_BLOCK, Q8_ROW = 1, 128, 3
 
 
 class BSError(RuntimeError):
@@ -48,8 +48,8 @@ class GemmArgs(ctypes.Structure):
         ("out_dtype", ctypes.c_int), ("ldo", ctypes.c_int64), ("num_sms", ctypes.c_int),
         ("n_chunk_blocks", ctypes.c_int), ("fp4_kernel", ctypes.c_int), ("fp4_stage_k", ctypes.c_int),
         ("fp4_small_experts", ctypes.c_int), ("fp4_half_tail", ctypes.c_int), ("fp8_stream_k", ctypes.c_int),
-        ("wait_timeout_us", ctypes.c_int), ("weights_ready", ctypes.c_int), ("workspace", ctypes.c_void_p),
-        ("workspace_bytes", ctypes.c_size_t),
+        ("fp8_scaling", ctypes.c_int), ("wait_timeout_us", ctypes.c_int), ("weights_ready", ctypes.c_int), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t), ("a_tensor_scale", ctypes.c_void_p), ("b_tensor_scale", ctypes.c_void_p),
     ]
 
 
@@ -108,6 +108,10 @@ def load(path: str | None = None):
         lib.bs_sf_offset.argtypes = [I64, I64, I64]
         lib.q4_quantize.restype = I
         lib.q4_quantize.argtypes = [P, I, I64, I64, I64, P, P, P, P, I, P, P]
+        lib.bs_tensor_amax.restype = I
+        lib.bs_tensor_amax.argtypes = [P, I, I64, I64, I64, P, P]
+        lib.q4_quantize_two_level.restype = I
+        lib.q4_quantize_two_level.argtypes = [P, I, I64, I64, I64, P, P, P, P, P]
         lib.bs_fp4_gather_rows.restype = I
         lib.bs_fp4_gather_rows.argtypes = [P, P, I64, I64, P, I64, P, P, P]
         lib.q8_quantize.restype = I
@@ -199,6 +203,31 @@ def q4_quantize(x: torch.Tensor, gather: torch.Tensor | None = None, rows: int |
     return codes, sf, lt
 
 
+def tensor_amax(x: torch.Tensor, out=None, stream=None):
+    """max |x| over the whole [M, K] tensor, as a device fp32 tensor [1]."""
+    amax = out if out is not None else torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(load().bs_tensor_amax(_ptr(x), _dt(x), x.shape[0], x.shape[1], x.stride(0), _ptr(amax), _stream(stream)))
+    return amax
+
+
+def q4_quantize_two_level(x: torch.Tensor, amax=None, out=None, stream=None):
+    """Two-level FP4: power-of-two tensor scale above the e4m3 group scales.
+    Returns (codes [M, K/2], sf, tensor_scale device fp32 [1]); ``amax``
+    (device fp32 [1]) defaults to tensor_amax(x)."""
+    assert x.is_cuda and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if amax is None:
+        amax = tensor_amax(x, stream=stream)
+    if out is None:
+        out = (torch.empty((M, K // 2), dtype=torch.uint8, device=x.device),
+               torch.empty(sf_bytes(M, K), dtype=torch.uint8, device=x.device),
+               torch.empty(1, dtype=torch.float32, device=x.device))
+    codes, sf, ts = out
+    _check(load().q4_quantize_two_level(_ptr(x), _dt(x), M, K, x.stride(0), _ptr(amax), _ptr(codes), _ptr(sf),
+                                        _ptr(ts), _stream(stream)))
+    return codes, sf, ts
+
+
 def fp4_gather_rows(codes, sf, K: int, gather, out=None, stream=None):
     """Rows gather[i] of an FP4 matrix (codes + MMA-layout scales); -1 -> zero row."""
     rows_out = gather.numel()
@@ -212,12 +241,12 @@ def fp4_gather_rows(codes, sf, K: int, gather, out=None, stream=None):
 
 def q8_quantize(x: torch.Tensor, mode: int = Q8_TOKEN, out=None, stream=None):
     """FP8 e4m3 quantization.  TOKEN mode: scales fp32 [K/128, M]; BLOCK mode:
-    scales fp32 [ceil(M/128), K/128]."""
+    scales fp32 [ceil(M/128), K/128]; ROW mode (W8A8): scales fp32 [M]."""
     assert x.is_cuda and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     if out is None:
         codes = torch.empty((M, K), dtype=torch.uint8, device=x.device)
-        shape = (K // 128, M) if mode == Q8_TOKEN else ((M + 127) // 128, K // 128)
+        shape = {Q8_TOKEN: (K // 128, M), Q8_BLOCK: ((M + 127) // 128, K // 128), Q8_ROW: (M,)}[mode]
         scales = torch.empty(shape, dtype=torch.float32, device=x.device)
     else:
         codes, scales = out
@@ -249,12 +278,16 @@ def _args(fmt, a, sfa, b, sfb, M, N, K, out, alpha=1.0, col_scale=None, lora_t=N
 
 
 def gemm_fp4(a, sfa, b, sfb, K: int, out_dtype=torch.bfloat16, alpha: float = 1.0, col_scale=None,
-             lora_t=None, lora_b_t=None, bias=None, out=None, num_sms: int = 0, stream=None):
-    """Dense block-scaled FP4 GEMM: Y[M, N] from A codes [M, K/2] and B codes [N, K/2]."""
+             lora_t=None, lora_b_t=None, bias=None, out=None, num_sms: int = 0, a_tensor_scale=None,
+             b_tensor_scale=None, stream=None):
+    """Dense block-scaled FP4 GEMM: Y[M, N] from A codes [M, K/2] and B codes [N, K/2]
+    (two-level operands: their device tensor scales from q4_quantize_two_level)."""
     M, N = a.shape[0], b.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
     g = _args(FMT_FP4, a, sfa, b, sfb, M, N, K, out, alpha, col_scale, lora_t, lora_b_t, bias, num_sms)
+    g.a_tensor_scale = None if a_tensor_scale is None else a_tensor_scale.data_ptr()
+    g.b_tensor_scale = None if b_tensor_scale is None else b_tensor_scale.data_ptr()
     _check(load().bs_gemm(ctypes.byref(g), _stream(stream)))
     return out
 
@@ -275,7 +308,7 @@ def _workspace(device, stream, nbytes: int):
 
 
 def gemm_fp8(a, sa, b, sb, out_dtype=torch.bfloat16, out=None, num_sms: int = 0, weights_ready: bool = False,
-             stream=None):
+             rowwise: bool = False, stream=None):
     """Dense FP8 GEMM with 1x128 A scales [K/128, M] and 128x128 B scales.
     ``weights_ready``: the kernel just before this call on the stream does not
     write ``b`` / ``sb``, so the weight loads may start before it finishes."""
@@ -285,6 +318,7 @@ def gemm_fp8(a, sa, b, sb, out_dtype=torch.bfloat16, out=None, num_sms: int = 0,
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
     g = _args(FMT_FP8, a, sa, b, sb, M, N, K, out, num_sms=num_sms)
     g.weights_ready = 1 if weights_ready else 0
+    g.fp8_scaling = 2 if rowwise else 0   # W8A8: sa [M] per token, sb [N] per channel
     lib = load()
     nbytes = int(lib.bs_gemm_workspace_bytes(ctypes.byref(g)))
     if nbytes:

@@ -219,6 +219,40 @@ bs_status q4_quantize(const void* x, bs_dtype dt, int64_t M, int64_t K, int64_t 
   return BS_OK;
 }
 
+bs_status bs_tensor_amax(const void* x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx, float* amax,
+                         bs_stream_t stream) {
+  if (M < 0 || K <= 0) return fail(BS_ERR_INVALID, "tensor_amax: M=%lld K=%lld", (long long)M, (long long)K);
+  if (dt != BS_DTYPE_F32 && dt != BS_DTYPE_BF16) return fail(BS_ERR_INVALID, "tensor_amax: dtype %d", (int)dt);
+  if (K % 8) return fail(BS_ERR_ALIGN, "tensor_amax: K=%lld not a multiple of 8", (long long)K);
+  if (!amax || (M > 0 && !x)) return fail(BS_ERR_INVALID, "tensor_amax: null pointer");
+  if ((M > 0 && (!aligned16(x) || ldx < K || ldx % 8)) || (reinterpret_cast<uintptr_t>(amax) & 3))
+    return fail(BS_ERR_ALIGN, "tensor_amax: x 16-byte aligned with ldx %% 8 == 0 and ldx >= K, amax 4-byte aligned");
+  if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_tensor_amax(x, dt == BS_DTYPE_BF16, M, K, ldx, amax, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "tensor_amax launch");
+  return BS_OK;
+}
+
+bs_status q4_quantize_two_level(const void* x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx, const float* amax,
+                                uint8_t* codes, uint8_t* sf, float* tensor_scale, bs_stream_t stream) {
+  if (M < 0 || K <= 0) return fail(BS_ERR_INVALID, "q4_quantize_two_level: M=%lld K=%lld", (long long)M, (long long)K);
+  if (dt != BS_DTYPE_F32 && dt != BS_DTYPE_BF16)
+    return fail(BS_ERR_INVALID, "q4_quantize_two_level: dtype %d", (int)dt);
+  if (K % 64) return fail(BS_ERR_ALIGN, "q4_quantize_two_level: K=%lld not a multiple of 64", (long long)K);
+  if (!amax || !tensor_scale) return fail(BS_ERR_INVALID, "q4_quantize_two_level: null amax / tensor_scale");
+  if ((reinterpret_cast<uintptr_t>(amax) | reinterpret_cast<uintptr_t>(tensor_scale)) & 3)
+    return fail(BS_ERR_ALIGN, "q4_quantize_two_level: amax / tensor_scale must be 4-byte aligned");
+  if (M == 0) return BS_OK;
+  if (!x || !codes || !sf) return fail(BS_ERR_INVALID, "q4_quantize_two_level: null pointer");
+  if (ldx < K || ldx % 8 || !aligned16(x) || !aligned16(codes) || !aligned16(sf))
+    return fail(BS_ERR_ALIGN, "q4_quantize_two_level: x/codes/sf must be 16-byte aligned and ldx %% 8 == 0, ldx >= K");
+  if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_q4_quantize(x, dt == BS_DTYPE_BF16, M, K, ldx, nullptr, codes, sf,
+                                          reinterpret_cast<cudaStream_t>(stream), amax, tensor_scale);
+  if (e != cudaSuccess) return cuda_fail(e, "q4_quantize_two_level launch");
+  return BS_OK;
+}
+
 bs_status bs_fp4_gather_rows(const uint8_t* codes_in, const uint8_t* sf_in, int64_t rows_in, int64_t K,
                              const int32_t* gather, int64_t rows_out, uint8_t* codes_out, uint8_t* sf_out,
                              bs_stream_t stream) {
@@ -240,7 +274,8 @@ bs_status q8_quantize(const void* x, bs_dtype dt, int64_t M, int64_t K, int64_t 
                       float* scales, bs_stream_t stream) {
   if (M < 0 || K <= 0) return fail(BS_ERR_INVALID, "q8_quantize: M=%lld K=%lld", (long long)M, (long long)K);
   if (dt != BS_DTYPE_F32 && dt != BS_DTYPE_BF16) return fail(BS_ERR_INVALID, "q8_quantize: dtype %d", (int)dt);
-  if (mode != BS_Q8_TOKEN_1x128 && mode != BS_Q8_BLOCK_128x128) return fail(BS_ERR_INVALID, "q8_quantize: mode %d", mode);
+  if (mode != BS_Q8_TOKEN_1x128 && mode != BS_Q8_BLOCK_128x128 && mode != BS_Q8_ROW)
+    return fail(BS_ERR_INVALID, "q8_quantize: mode %d", mode);
   if (K % 128) return fail(BS_ERR_ALIGN, "q8_quantize: K=%lld not a multiple of 128", (long long)K);
   if (M == 0) return BS_OK;
   if (!x || !codes || !scales) return fail(BS_ERR_INVALID, "q8_quantize: null pointer");
@@ -265,6 +300,7 @@ static bs_status check_choices(const bs_gemm_args* a) {
   if (a->fp8_stream_k < 0 || a->fp8_stream_k > 2)
     return fail(BS_ERR_INVALID, "fp8_stream_k=%d (0, 1 or 2)", a->fp8_stream_k);
   if (a->weights_ready < 0 || a->weights_ready > 1) return fail(BS_ERR_INVALID, "weights_ready=%d (0 or 1)", a->weights_ready);
+  if (a->fp8_scaling < 0 || a->fp8_scaling > 2) return fail(BS_ERR_INVALID, "fp8_scaling=%d (0, 1 or 2)", a->fp8_scaling);
   if (a->wait_timeout_us < 0) return fail(BS_ERR_INVALID, "wait_timeout_us < 0");
   return BS_OK;
 }
@@ -452,6 +488,10 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
         return fail(BS_ERR_UNSUPPORTED, "low-rank branch with alpha != 1 or col_scale");
       if (!aligned16(a->lora_t) || !aligned16(a->lora_b_t)) return fail(BS_ERR_ALIGN, "low-rank buffers misaligned");
     }
+    if ((a->a_tensor_scale || a->b_tensor_scale) && lora)
+      return fail(BS_ERR_UNSUPPORTED, "low-rank branch with two-level tensor scales");
+    if ((reinterpret_cast<uintptr_t>(a->a_tensor_scale) | reinterpret_cast<uintptr_t>(a->b_tensor_scale)) & 3)
+      return fail(BS_ERR_ALIGN, "tensor scales must be 4-byte aligned");
     if (a->M == 0) return BS_OK;
     bsk::Fp4Launch L;
     memset(&L, 0, sizeof L);
@@ -461,6 +501,8 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     L.p.N = (int)a->N;
     L.p.K = (int)a->K;
     L.p.alpha = a->alpha;
+    L.p.a_ts = a->a_tensor_scale;
+    L.p.b_ts = a->b_tensor_scale;
     L.p.col_scale = a->col_scale;
     L.p.bias = a->bias;
     L.p.out = a->out;
@@ -477,8 +519,8 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
   }
   if (a->fmt == BS_FMT_FP8) {
     if (a->K % 128) return fail(BS_ERR_ALIGN, "FP8: K=%lld not a multiple of 128", (long long)a->K);
-    if (a->alpha != 1.0f || a->col_scale || a->lora_t || a->bias)
-      return fail(BS_ERR_UNSUPPORTED, "FP8 GEMM takes no alpha/col_scale/low-rank/bias");
+    if (a->alpha != 1.0f || a->col_scale || a->lora_t || a->bias || a->a_tensor_scale || a->b_tensor_scale)
+      return fail(BS_ERR_UNSUPPORTED, "FP8 GEMM takes no alpha/col_scale/low-rank/bias/tensor scales");
     if (reinterpret_cast<uintptr_t>(a->sfa) & 3 || reinterpret_cast<uintptr_t>(a->sfb) & 3)
       return fail(BS_ERR_ALIGN, "FP8 scales must be 4-byte aligned");
     if (a->M == 0) return BS_OK;
@@ -504,6 +546,7 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     const Fp8Plan P = fp8_plan(a, sms);
     L.p.wait_ns = wait_ns(a);
     L.p.pre_b = a->weights_ready == 1 ? bsk::fp8_stages(P.tile_n) : 0;
+    L.p.rowwise = a->fp8_scaling == 2;
     L.grid = P.grid;
     if (P.stream_k && a->workspace) {
       if (!aligned16(a->workspace)) return fail(BS_ERR_ALIGN, "workspace must be 16-byte aligned");
@@ -536,8 +579,8 @@ bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, 
   if (a->K % 64) return fail(BS_ERR_ALIGN, "FP4: K=%lld not a multiple of 64", (long long)a->K);
   if (E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "E=%d outside [1, 1024]", E);
   if (!offsets || !counts) return fail(BS_ERR_INVALID, "null offsets/counts");
-  if (a->lora_t || a->col_scale || a->bias || a->alpha != 1.0f)
-    return fail(BS_ERR_UNSUPPORTED, "grouped GEMM takes no alpha/col_scale/bias/low-rank");
+  if (a->lora_t || a->col_scale || a->bias || a->alpha != 1.0f || a->a_tensor_scale || a->b_tensor_scale)
+    return fail(BS_ERR_UNSUPPORTED, "grouped GEMM takes no alpha/col_scale/bias/low-rank/tensor scales");
   if (epilogue == BS_EPI_SWIGLU && a->out_dtype != BS_DTYPE_BF16) return fail(BS_ERR_INVALID, "SWIGLU output is bf16");
   if (epilogue == BS_EPI_ROWS) {
     if (a->out_dtype != BS_DTYPE_F32) return fail(BS_ERR_INVALID, "ROWS output is fp32");
@@ -590,8 +633,8 @@ bs_status bs_grouped_gemm_swiglu_q4(const bs_gemm_args* a, int E, const int32_t*
   if (a->K % 64) return fail(BS_ERR_ALIGN, "FP4: K=%lld not a multiple of 64", (long long)a->K);
   if (E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "E=%d outside [1, 1024]", E);
   if (!offsets || !counts) return fail(BS_ERR_INVALID, "null offsets/counts");
-  if (a->lora_t || a->col_scale || a->bias || a->alpha != 1.0f)
-    return fail(BS_ERR_UNSUPPORTED, "grouped GEMM takes no alpha/col_scale/bias/low-rank");
+  if (a->lora_t || a->col_scale || a->bias || a->alpha != 1.0f || a->a_tensor_scale || a->b_tensor_scale)
+    return fail(BS_ERR_UNSUPPORTED, "grouped GEMM takes no alpha/col_scale/bias/low-rank/tensor scales");
   const int64_t wrows = 2 * a->N * (int64_t)E;
   if (wrows > (1LL << 30)) return fail(BS_ERR_INVALID, "stacked weights too large");
   if (a->M > 0) {

@@ -243,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // expert tables and outputs may belong to the kernel just before this one
   // on the stream (programmatic dependent launch), so wait for it here.
   griddep_wait();
+  // alpha times the two-level FP4 tensor scales (powers of two: exact)
+  const float alpha_ts = p.alpha * (p.a_ts ? __ldg(p.a_ts) : 1.0f) * (p.b_ts ? __ldg(p.b_ts) : 1.0f);
   if (warp == 3) {
     // Tile table.  Dense: closed form.  Grouped: validate the offset table and
     // prefix-sum the tiles of each expert.
@@ -543,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 8; ++i) {
               const int n = col + c + i;
               float a = __uint_as_float(v[(c + i) / 32][(c + i) % 32]);
-              float sc = p.alpha;
+              float sc = alpha_ts;
               if (p.col_scale) sc *= p.col_scale[n];
               a *= sc;
               if (p.bias) a += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.bias)[n]);

@@ -281,6 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // expert tables and outputs may belong to the kernel just before this one
   // on the stream (programmatic dependent launch), so wait for it here.
   griddep_wait();
+  // alpha times the two-level FP4 tensor scales (powers of two: exact)
+  const float alpha_ts = p.alpha * (p.a_ts ? __ldg(p.a_ts) : 1.0f) * (p.b_ts ? __ldg(p.b_ts) : 1.0f);
   if (warp == 3) {
     if (p.E == 0) {
       int nfull;
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col = tl.col0 + 128 * half;
         auto value = [&](int c) {  // output column col + c of this lane's row
           float a = __uint_as_float(v[c / 32][c % 32]);
-          float sc = p.alpha;
+          float sc = alpha_ts;
           if (p.col_scale) sc *= p.col_scale[col + c];
           a *= sc;
           if (p.bias) a += __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.bias)[col + c]);

@@ -118,7 +118,7 @@ struct Walk {
 // CTA whose stream-K range holds unit u (ranges [c U / G, (c + 1) U / G)).
 __device__ __forceinline__ int sk_owner(long long u, long long U, int G) { return (int)(((u + 1) * G - 1) / U); }
 
-template <int TN, bool kStreamK>
+template <int TN, bool kStreamK, bool kRowwise>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const Fp8Params p) {
@@ -243,6 +243,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     Walk<kStreamK> w(p, total, nkb);
     Seg sg;
     while (ok && w.next(p, nkb, sg)) {
+      if constexpr (kRowwise) {
+        // W8A8: the segment's K blocks accumulate into one slot, handed to the
+        // epilogue once
+        if (!mbar_wait_warp(&pempty[sl.index], sl.phase ^ 1u, wg, 62)) { ok = false; break; }
+        const uint32_t d = tmem + sl.index * TN;
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+          if (!mbar_wait_warp(&full[ps.index], ps.phase, wg, 63)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t so = (uint64_t)((ps.index * C::kStageBytes) >> 4);
+          if (elect_one()) {
+#pragma unroll
+            for (int j = 0; j < BK / 32; ++j)
+              mma_e4m3(d, dW + so + 2 * j, dX + so + 2 * j, idesc, (kb > sg.kb0 || j > 0) ? 1u : 0u);
+            tc_commit(&empty[ps.index]);
+          }
+          __syncwarp();
+          ps.advance();
+        }
+        if (!ok) break;
+        if (elect_one()) tc_commit(&pfull[sl.index]);
+        __syncwarp();
+        sl.advance();
+        continue;
+      }
       for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
         if (!mbar_wait_warp(&pempty[sl.index], sl.phase ^ 1u, wg, 60)) { ok = false; break; }
         if (!mbar_wait_warp(&full[ps.index], ps.phase, wg, 61)) { ok = false; break; }
@@ -309,17 +333,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = (s.t % n_wblk) * BM + r;            // weight row = output column
       const int m0 = (s.t / n_wblk) * TN + col0;        // first token of this warp's columns
       if (n >= p.N) return;
+      const float sw = kRowwise ? __ldg(p.sfb + n) : 1.0f;   // W8A8: channel scale of this row
 #pragma unroll
       for (int i = 0; i < NC; ++i) {
         const int m = m0 + i;
         if (m < p.M) {
+          const float v = kRowwise ? y[i] * (__ldg(p.sfa + m) * sw) : y[i];
           if (p.out_bf16)
-            reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(y[i]);
+            reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(v);
           else
-            reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + n] = y[i];
+            reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + n] = v;
         }
       }
     };
+    // End of a segment: a whole tile is stored; a stream-K piece goes to the
+    // workspace and the last of the tile's CTAs sums the pieces (in K order)
+    // and stores them.  Every epilogue warp takes part (named barrier 1).
+    // acc is reset for the next segment.
+    auto finish = [&](const Seg& sg, float (&acc)[NC], bool ok) {
+      if (!kStreamK || (sg.kb0 == 0 && sg.kb1 == nkb)) {
+        if (ok) store_out(sg, acc);
+      } else {
+        // stream-K piece of a tile: partial to the workspace, count in; the
+        // last of the tile's CTAs sums the pieces in K order
+        const long long U = (long long)total * nkb, u0 = (long long)sg.t * nkb;
+        const int c_first = sk_owner(u0, U, (int)gridDim.x);
+        const int n_parts = sk_owner(u0 + nkb - 1, U, (int)gridDim.x) - c_first + 1;
+        const int j = (int)blockIdx.x - c_first;
+        float* parts = p.work + (size_t)sg.t * p.maxc * (BM * TN);
+        float4* mine = reinterpret_cast<float4*>(parts + (size_t)j * (BM * TN) + r * TN + col0);
+#pragma unroll
+        for (int i = 0; i < NC; i += 4) mine[i / 4] = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+        // One thread counts the CTA in with an acquire-release add: the
+        // barrier orders every thread's partial before its release, and if
+        // it is the last piece its acquire (passed on by the second barrier)
+        // orders the other CTAs' partials before the reads below.
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (etid == 0) {
+          int old;
+          asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + sg.t) : "memory");
+          *fix_flag = old == n_parts - 1;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (*fix_flag) {
+          // every piece, this CTA's own included, summed from the workspace
+          // (L2) in K order
+#pragma unroll
+          for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
+          for (int jj = 0; jj < n_parts; ++jj) {
+            const float4* src = reinterpret_cast<const float4*>(parts + (size_t)jj * (BM * TN) + r * TN + col0);
+#pragma unroll
+            for (int i = 0; i < NC; i += 4) {
+              const float4 v4 = __ldcg(src + i / 4);
+              acc[i] += v4.x;
+              acc[i + 1] += v4.y;
+              acc[i + 2] += v4.z;
+              acc[i + 3] += v4.w;
+            }
+          }
+          if (ok) store_out(sg, acc);
+          if (etid == 0) p.counters[sg.t] = 0;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
+    };
+    if constexpr (kRowwise) {
+      // W8A8: one accumulator per segment, scaled once at the store
+      Walk<kStreamK> w(p, total, nkb);
+      Seg sg;
+      float acc[NC];
+#pragma unroll
+      for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
+      while (w.next(p, nkb, sg)) {
+        if (ok) {
+          int w_ok = 1;
+          if (lane == 0) w_ok = mbar_wait(&pfull[sl.index], sl.phase, wg, 72) ? 1 : 0;
+          ok = __shfl_sync(0xffffffffu, w_ok, 0) != 0;
+        }
+        if (ok) {
+          tc_fence_after();
+          constexpr int CH = NC < 32 ? NC : 32;
+#pragma unroll
+          for (int c0 = 0; c0 < NC; c0 += CH) {
+            uint32_t v[CH];
+            tmem_ld_cols<CH>(tmem + ((uint32_t)(q * 32) << 16) + sl.index * TN + col0 + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < CH; ++i) acc[c0 + i] = __uint_as_float(v[i]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pempty[sl.index]);
+        }
+        sl.advance();
+        finish(sg, acc, ok);
+      }
+    } else {
     Walk<kStreamK> w(p, total, nkb);
     Seg sg;
     bool have = w.next(p, nkb, sg);
@@ -433,55 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         sl.advance();
       }
-      if (cn == 0) {
-        // the segment's last chunk
-        if (!kStreamK || (sg.kb0 == 0 && sg.kb1 == nkb)) {
-          if (ok) store_out(sg, acc);
-        } else {
-          // stream-K piece of a tile: partial to the workspace, count in; the
-          // last of the tile's CTAs sums the pieces in K order
-          const long long U = (long long)total * nkb, u0 = (long long)sg.t * nkb;
-          const int c_first = sk_owner(u0, U, (int)gridDim.x);
-          const int n_parts = sk_owner(u0 + nkb - 1, U, (int)gridDim.x) - c_first + 1;
-          const int j = (int)blockIdx.x - c_first;
-          float* parts = p.work + (size_t)sg.t * p.maxc * (BM * TN);
-          float4* mine = reinterpret_cast<float4*>(parts + (size_t)j * (BM * TN) + r * TN + col0);
-#pragma unroll
-          for (int i = 0; i < NC; i += 4) mine[i / 4] = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-          // One thread counts the CTA in with an acquire-release add: the
-          // barrier orders every thread's partial before its release, and if
-          // it is the last piece its acquire (passed on by the second barrier)
-          // orders the other CTAs' partials before the reads below.
-          asm volatile("bar.sync 1, 256;" ::: "memory");
-          if (etid == 0) {
-            int old;
-            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + sg.t) : "memory");
-            *fix_flag = old == n_parts - 1;
-          }
-          asm volatile("bar.sync 1, 256;" ::: "memory");
-          if (*fix_flag) {
-            // every piece, this CTA's own included, summed from the workspace
-            // (L2) in K order
-#pragma unroll
-            for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
-            for (int jj = 0; jj < n_parts; ++jj) {
-              const float4* src = reinterpret_cast<const float4*>(parts + (size_t)jj * (BM * TN) + r * TN + col0);
-#pragma unroll
-              for (int i = 0; i < NC; i += 4) {
-                const float4 v4 = __ldcg(src + i / 4);
-                acc[i] += v4.x;
-                acc[i + 1] += v4.y;
-                acc[i + 2] += v4.z;
-                acc[i + 3] += v4.w;
-              }
-            }
-            if (ok) store_out(sg, acc);
-            if (etid == 0) p.counters[sg.t] = 0;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < NC; ++i) acc[i] = 0.0f;
-      }
+      if (cn == 0) finish(sg, acc, ok);  // the segment's last chunk
       asm volatile("bar.sync 1, 256;" ::: "memory");  // this buffer may be refilled next iteration
       sg = sn;
       c = cn;
@@ -489,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++qi;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
   }
 
   __syncwarp();
@@ -500,10 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int TN, bool kStreamK>
+template <int TN, bool kStreamK, bool kRowwise>
 static cudaError_t launch_tn(const Fp8Launch& L, cudaStream_t stream) {
   using C = Cfg<TN>;
-  auto kern = fp8_gemm_kernel<TN, kStreamK>;
+  auto kern = fp8_gemm_kernel<TN, kStreamK, kRowwise>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmA, L.tmB, L.p);
@@ -528,24 +591,21 @@ int fp8_stages(int tile_n) {
   return 0;
 }
 
-cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream) {
-  if (L.grid <= 0) return cudaErrorInvalidValue;
-  if (L.p.stream_k) {
-    switch (L.tile_n) {
-      case 16: return fp8::launch_tn<16, true>(L, stream);
-      case 32: return fp8::launch_tn<32, true>(L, stream);
-      case 64: return fp8::launch_tn<64, true>(L, stream);
-      case 128: return fp8::launch_tn<128, true>(L, stream);
-    }
-    return cudaErrorInvalidValue;
-  }
+template <bool kStreamK, bool kRowwise>
+static cudaError_t launch_sk(const Fp8Launch& L, cudaStream_t stream) {
   switch (L.tile_n) {
-    case 16: return fp8::launch_tn<16, false>(L, stream);
-    case 32: return fp8::launch_tn<32, false>(L, stream);
-    case 64: return fp8::launch_tn<64, false>(L, stream);
-    case 128: return fp8::launch_tn<128, false>(L, stream);
+    case 16: return fp8::launch_tn<16, kStreamK, kRowwise>(L, stream);
+    case 32: return fp8::launch_tn<32, kStreamK, kRowwise>(L, stream);
+    case 64: return fp8::launch_tn<64, kStreamK, kRowwise>(L, stream);
+    case 128: return fp8::launch_tn<128, kStreamK, kRowwise>(L, stream);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream) {
+  if (L.grid <= 0) return cudaErrorInvalidValue;
+  if (L.p.rowwise) return L.p.stream_k ? launch_sk<true, true>(L, stream) : launch_sk<false, true>(L, stream);
+  return L.p.stream_k ? launch_sk<true, false>(L, stream) : launch_sk<false, false>(L, stream);
 }
 
 }  // namespace bsk

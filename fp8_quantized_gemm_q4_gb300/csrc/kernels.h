@@ -67,6 +67,8 @@ struct Fp4Params {
   int half_tail;          // dense, CTA pairs: split a short last wave into 256 x 128 half tiles
   uint8_t* out_sf;        // SWIGLU_Q4: scales of h (MMA layout for [M, N]); out holds its codes [M, N/2]
   unsigned long long wait_ns;  // bound of every pipeline wait (%globaltimer ns)
+  const float* a_ts;      // two-level FP4: tensor scales of A / B (device fp32, or null = 1)
+  const float* b_ts;
 };
 
 // Rows of expert e that one grouped launch covers.  part 0: all of them.  A
@@ -117,6 +119,7 @@ struct Fp8Params {
   int stream_k;           // 1: the tiles' K blocks are shared out evenly over the grid
   int maxc;               // stream-K: most CTAs that share one tile
   int pre_b;              // weight stages loaded before waiting on the preceding kernel
+  int rowwise;            // W8A8: sfa fp32 [M] per token, sfb fp32 [N] per channel; no per-block promotion
   int* status;
   unsigned long long wait_ns;  // bound of every pipeline wait (%globaltimer ns)
 };
@@ -134,7 +137,10 @@ int fp8_stages(int tile_n);
 
 // quantizers
 cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx,
-                               const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream);
+                               const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream,
+                               const float* tensor_amax = nullptr, float* tensor_scale = nullptr);
+cudaError_t launch_tensor_amax(const void* x, int x_bf16, long long M, long long K, long long ldx, float* amax,
+                               cudaStream_t stream);
 cudaError_t launch_q4_lowrank_fused(const void* x, long long M, long long K, long long ldx, const int* gather,
                                     const void* lora_a_t, uint8_t* codes, uint8_t* sf, void* lora_t,
                                     cudaStream_t stream);

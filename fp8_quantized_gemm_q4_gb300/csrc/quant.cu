@@ -80,15 +80,40 @@ __device__ __forceinline__ float raw8_at(const Raw8<kBf16>& r, int i) {
     return __uint_as_float(r.w[i]);
 }
 
-template <bool kBf16>
+// Two-level FP4 tensor scale 2^e: the smallest e with amax <= 6 * 448 * 2^e
+// (0 for a zero tensor), decided with exact double comparisons.
+__device__ __forceinline__ int two_level_exp(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int e = ilogbf(amax) - 11;  // 2688 lies in [2^11, 2^12): at most a step or two off
+  while ((double)amax > ldexp(2688.0, e)) ++e;
+  while ((double)amax <= ldexp(2688.0, e - 1)) --e;
+  return e;
+}
+
+// kScaled: two-level FP4, the input divided by the tensor scale 2^e first
+// (exact: a multiply by an fp32 power of two, or ldexpf where 2^-e is not an
+// fp32 normal), e derived from *tensor_amax; CTA 0 stores 2^e.
+template <bool kBf16, bool kScaled>
 __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict__ x, long long M, long long Mpad,
                                                           long long K, long long ldx,
                                                           const int* __restrict__ gather,
-                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                          const float* __restrict__ tensor_amax,
+                                                          float* __restrict__ tensor_scale) {
   griddep_wait();  // inputs may come from the kernel just before on the stream
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const float r6 = __frcp_rn(6.0f);
+  int e2 = 0;
+  float down = 1.0f;
+  bool fast = true;
+  if constexpr (kScaled) {
+    e2 = two_level_exp(__ldg(tensor_amax));
+    fast = e2 >= -126 && e2 <= 126;
+    down = fast ? ldexpf(1.0f, -e2) : 1.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = (float)ldexp(1.0, e2);
+  }
+  auto in = [&](float v) { return kScaled ? (fast ? v * down : ldexpf(v, -e2)) : v; };
   const long long nblk = (K + 256 * kQ4Unroll - 1) / (256 * kQ4Unroll);
   const long long total = Mpad * nblk;
   const long long kchunks = K / 64;
@@ -110,7 +135,7 @@ __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict
       const bool active = k0 < K;
       float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(raw8_at<kBf16>(raw[u], i)));
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(in(raw8_at<kBf16>(raw[u], i))));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       // bf16 amax: the one-correction quotient is RN(amax / 6) (6 is an e4m3
       // value, so the exhaustive GPU tests cover every case); fp32: IEEE divide
@@ -119,7 +144,7 @@ __global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict
       const float rs = __frcp_rn(s);
       float q[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = quot_rn(raw8_at<kBf16>(raw[u], i), s, rs);
+      for (int i = 0; i < 8; ++i) q[i] = quot_rn(in(raw8_at<kBf16>(raw[u], i)), s, rs);
       const uint32_t word = (s == 0.0f) ? 0u : f32x8_to_e2m1x8(q);  // zero group: all codes +0
       if (active && row < M) *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + k0 / 2) = word;
       const uint32_t b1 = __shfl_down_sync(0xffffffffu, s_code, 2);
@@ -251,6 +276,52 @@ __global__ void __launch_bounds__(256) q8_token_kernel(const void* __restrict__ 
   }
 }
 
+// FP8 with one scale per row over all of K (W8A8: per-token activations,
+// per-channel weights held as [N, K] rows).  One CTA per row: a first pass
+// takes the row's amax (16-byte loads, block reduction), s = fl32(amax / 448);
+// a second pass (the row is now in L2) writes the codes, IEEE division.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) q8_row_kernel(const void* __restrict__ x, long long M, long long K,
+                                                     long long ldx, uint8_t* __restrict__ codes,
+                                                     float* __restrict__ scales) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
+  __shared__ float wmax[8];
+  for (long long row = blockIdx.x; row < M; row += gridDim.x) {
+    const long long base = row * ldx;
+    float m = 0.0f;
+    for (long long k = (long long)threadIdx.x * 8; k < K; k += 256 * 8) {
+      Raw8<kBf16> r;
+      load_raw8<kBf16>(x, base + k, r);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(raw8_at<kBf16>(r, i)));
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x / 32] = m;
+    __syncthreads();
+    float amax = wmax[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
+    __syncthreads();  // wmax is reused by the next row
+    const float s = __fdiv_rn(amax, 448.0f);
+    if (threadIdx.x == 0) scales[row] = s;
+    for (long long k = (long long)threadIdx.x * 8; k < K; k += 256 * 8) {
+      Raw8<kBf16> r;
+      load_raw8<kBf16>(x, base + k, r);
+      uint32_t c[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = s == 0.0f ? 0.0f : __fdiv_rn(raw8_at<kBf16>(r, 4 * h + i), s);
+        c[h] = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
+      }
+      *reinterpret_cast<uint2*>(codes + row * K + k) = make_uint2(c[0], c[1]);
+    }
+  }
+}
+
 // FP8 128x128 blocks: one CTA (256 threads) per block.
 __global__ void __launch_bounds__(256) q8_block_kernel(const void* __restrict__ x, int x_bf16, long long M,
                                                        long long K, long long ldx, uint8_t* __restrict__ codes,
@@ -306,19 +377,71 @@ __global__ void __launch_bounds__(256) q8_block_kernel(const void* __restrict__ 
   }
 }
 
+// max |x| over an [M, K] tensor into *amax: a one-thread kernel zeroes it,
+// then every CTA reduces its grid-stride share and merges with an integer
+// atomicMax (non-negative floats order like their bit patterns).
+__global__ void tensor_amax_init_kernel(float* amax) {
+  griddep_wait();
+  griddep_launch_dependents();
+  *amax = 0.0f;
+}
+template <bool kBf16>
+__global__ void __launch_bounds__(256) tensor_amax_kernel(const void* __restrict__ x, long long M, long long K,
+                                                          long long ldx, float* __restrict__ amax) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float wmax[8];
+  const long long per_row = K / 8, total = M * per_row;
+  float m = 0.0f;
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (long long)gridDim.x * blockDim.x) {
+    Raw8<kBf16> r;
+    load_raw8<kBf16>(x, (v / per_row) * ldx + (v % per_row) * 8, r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(raw8_at<kBf16>(r, i)));
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x / 32] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, wmax[w]);
+    atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(m));
+  }
+}
+
+cudaError_t launch_tensor_amax(const void* x, int x_bf16, long long M, long long K, long long ldx, float* amax,
+                               cudaStream_t stream) {
+  cudaError_t e = launch_kernel(tensor_amax_init_kernel, 1, 1, 0, stream, 1, amax);
+  if (e != cudaSuccess) return e;
+  long long blocks = (M * (K / 8) + 255) / 256;
+  const long long cap = (long long)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (x_bf16) return launch_kernel(tensor_amax_kernel<true>, (unsigned)blocks, 256, 0, stream, 1, x, M, K, ldx, amax);
+  return launch_kernel(tensor_amax_kernel<false>, (unsigned)blocks, 256, 0, stream, 1, x, M, K, ldx, amax);
+}
+
 cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx,
-                               const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream) {
+                               const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream,
+                               const float* tensor_amax, float* tensor_scale) {
   const long long Mpad = (M + 127) / 128 * 128;
   const long long warps = Mpad * ((K + 256 * kQ4Unroll - 1) / (256 * kQ4Unroll));
   long long blocks = (warps + 7) / 8;
   const long long cap = (long long)sm_count() * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  if (tensor_amax) {
+    if (x_bf16)
+      return launch_kernel(q4_quantize_kernel<true, true>, (unsigned)blocks, 256, 0, stream, 1, x, M, Mpad, K, ldx,
+                           gather, codes, sf, tensor_amax, tensor_scale);
+    return launch_kernel(q4_quantize_kernel<false, true>, (unsigned)blocks, 256, 0, stream, 1, x, M, Mpad, K, ldx,
+                         gather, codes, sf, tensor_amax, tensor_scale);
+  }
   if (x_bf16)
-    return launch_kernel(q4_quantize_kernel<true>, (unsigned)blocks, 256, 0, stream, 1, x, M, Mpad, K, ldx, gather,
-                         codes, sf);
-  return launch_kernel(q4_quantize_kernel<false>, (unsigned)blocks, 256, 0, stream, 1, x, M, Mpad, K, ldx, gather,
-                       codes, sf);
+    return launch_kernel(q4_quantize_kernel<true, false>, (unsigned)blocks, 256, 0, stream, 1, x, M, Mpad, K, ldx,
+                         gather, codes, sf, tensor_amax, tensor_scale);
+  return launch_kernel(q4_quantize_kernel<false, false>, (unsigned)blocks, 256, 0, stream, 1, x, M, Mpad, K, ldx,
+                       gather, codes, sf, tensor_amax, tensor_scale);
 }
 
 cudaError_t launch_lowrank_t(const void* x, long long M, long long K, long long ldx, const int* gather,
@@ -339,6 +462,12 @@ cudaError_t launch_q8_quantize(const void* x, int x_bf16, long long M, long long
     if (blocks < 1) blocks = 1;
     if (x_bf16) return launch_kernel(q8_token_kernel<true>, (unsigned)blocks, 256, 0, stream, 1, x, M, K, ldx, codes, scales);
     return launch_kernel(q8_token_kernel<false>, (unsigned)blocks, 256, 0, stream, 1, x, M, K, ldx, codes, scales);
+  }
+  if (mode == 3) {  // one scale per row over all of K
+    long long blocks = M < (long long)sm_count() * 8 ? M : (long long)sm_count() * 8;
+    if (blocks < 1) blocks = 1;
+    if (x_bf16) return launch_kernel(q8_row_kernel<true>, (unsigned)blocks, 256, 0, stream, 1, x, M, K, ldx, codes, scales);
+    return launch_kernel(q8_row_kernel<false>, (unsigned)blocks, 256, 0, stream, 1, x, M, K, ldx, codes, scales);
   }
   // one CTA per 128 x 128 block, numbered kb + (K / 128) * rb
   return launch_kernel(q8_block_kernel, (unsigned)((K / 128) * ((M + 127) / 128)), 256, 0, stream, 1, x, x_bf16, M,

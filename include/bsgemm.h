@@ -61,7 +61,12 @@ typedef enum {
     BS_EPI_ROWS = 3     /* grouped only: out fp32 [r, n] = weight_of[r] * y[r, n] */
 } bs_epilogue;
 
-typedef enum { BS_Q8_TOKEN_1x128 = 1, BS_Q8_BLOCK_128x128 = 128 } bs_q8_mode;
+typedef enum {
+    BS_Q8_TOKEN_1x128 = 1,     /* one scale per row and 128-wide K block (activations) */
+    BS_Q8_BLOCK_128x128 = 128, /* one scale per 128 x 128 block (weights) */
+    BS_Q8_ROW = 3              /* one scale per row over all of K (W8A8: per-token activations,
+                                  per-channel weights) */
+} bs_q8_mode;
 
 /* ---------------------------------------------------------------------------
  * FP4 scale-factor layout ("MMA layout").
@@ -109,6 +114,30 @@ bs_status q4_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t 
                       const void *lora_a_t, int r, void *lora_t, bs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Two-level FP4 scaling: a per-tensor scale above the e4m3 group scales
+ * ("Tencent AI Infra interview notes", scale-granularity table: per-tensor,
+ * per-channel, per-token, per-group).  The tensor scale is the power of two
+ * 2^e with the smallest e such that amax <= 6 * 448 * 2^e; the tensor is
+ * divided by it (exactly) and quantized as q4_quantize does, so the largest
+ * group scale falls in e4m3's top binade [256, 448] and small weights
+ * (N(0, 0.02): one-level group scales are e4m3 subnormals with 2-3
+ * significant bits) keep full 3-bit scale mantissas.  A code stands for
+ * code * s_group * 2^e; bs_gemm multiplies Y by the two tensor scales
+ * (bs_gemm_args.a_tensor_scale / b_tensor_scale).
+ *
+ * bs_tensor_amax: *amax (device fp32) = max |x| over x [M, K] (K % 8 == 0,
+ *   x 16-byte aligned, ldx % 8 == 0).
+ * q4_quantize_two_level: codes / sf as q4_quantize (no gather, no low-rank)
+ *   of x / 2^e, e from *amax (device, e.g. from bs_tensor_amax); writes
+ *   *tensor_scale = 2^e (device fp32).  A zero tensor gets e = 0.
+ * ------------------------------------------------------------------------- */
+bs_status bs_tensor_amax(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx, float *amax,
+                         bs_stream_t stream);
+bs_status q4_quantize_two_level(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx,
+                                const float *amax, uint8_t *codes, uint8_t *sf, float *tensor_scale,
+                                bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * bs_fp4_gather_rows -- gather rows of an FP4 matrix that q4_quantize already
  * wrote: output row i = input row gather[i] (a negative or out-of-range index
  * gives a zero row with zero scales), codes copied and each row's scales moved
@@ -139,7 +168,10 @@ bs_status bs_fp4_gather_rows(const uint8_t *codes_in, const uint8_t *sf_in, int6
  *   codes   [M, K] bytes
  *   scales  TOKEN mode: fp32 [K/128, M] (K-block major: the scales of one K
  *           block are contiguous over rows);
- *           BLOCK mode: fp32 [ceil(M/128), K/128]
+ *           BLOCK mode: fp32 [ceil(M/128), K/128];
+ *           ROW mode: fp32 [M] ("Tencent AI Infra interview notes", W8A8
+ *           SmoothQuant: scale_x [M, 1] per token, scale_w [1, N] per output
+ *           channel, i.e. per row of the [N, K] weights)
  * ------------------------------------------------------------------------- */
 bs_status q8_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx,
                       int mode, uint8_t *codes, float *scales, bs_stream_t stream);
@@ -170,7 +202,7 @@ bs_status q8_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t 
  *   num_sms    persistent grid size limit (0 = all SMs)
  *   n_chunk_blocks  ignored by bs_gemm (grouped tile-order knob)
  *   fp4_kernel, fp4_stage_k, fp4_small_experts, fp4_half_tail, fp8_stream_k,
- *   wait_timeout_us, weights_ready
+ *   fp8_scaling, wait_timeout_us, weights_ready
  *              per-call kernel choices, described at the fields; 0 = the
  *              library's default.  A zero-initialised struct gets every default.
  *   workspace, workspace_bytes
@@ -210,6 +242,12 @@ typedef struct {
                                 tiles' K blocks are shared out evenly over all SMs and the pieces
                                 of a tile summed in K order by the last CTA to finish one
                                 (stream-K; default, needs `workspace`); 2 = one CTA per tile */
+    int fp8_scaling;         /* FP8 scales: 0 or 1 = block-scaled (sfa 1x128 per token, sfb
+                                128x128, promoted per 128-wide K block); 2 = W8A8 per row
+                                ("Tencent AI Infra interview notes", SmoothQuant): sfa fp32 [M]
+                                and sfb fp32 [N] from q8_quantize BS_Q8_ROW,
+                                Y = sfa[m] sfb[n] sum_k a b, accumulated over all of K in tensor
+                                memory and scaled once */
     int wait_timeout_us;     /* bound of every pipeline wait inside the kernels, in microseconds
                                 (default 4,000,000 = 4 s).  A wait that runs out ends the kernel
                                 early (outputs undefined) and sets BS_ERR_TIMEOUT in the device
@@ -225,6 +263,10 @@ typedef struct {
                                 Calls that overlap on the GPU must not share one.  NULL: no
                                 scratch (FP8 stream-K then runs one CTA per tile) */
     size_t workspace_bytes;
+    const float *a_tensor_scale; /* FP4 dense: device fp32 tensor scales of A and B from
+                                    q4_quantize_two_level, or NULL (= 1); Y is multiplied by
+                                    both.  Not with the low-rank branch */
+    const float *b_tensor_scale;
 } bs_gemm_args;
 
 /* Bytes of `workspace` bs_gemm would use for these arguments (sizes, format,

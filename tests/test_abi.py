@@ -76,7 +76,15 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.q4_quantize(None, 1, 0, 64, 64, None, None, None, None, 0, None, None) == bs.BS_OK
     # q8: K % 128
     assert lib.q8_quantize(fake, 1, 4, 64, 64, 1, fake, fake, None) == bs.BS_ERR_ALIGN
-    assert lib.q8_quantize(fake, 1, 4, 128, 128, 3, fake, fake, None) == bs.BS_ERR_INVALID
+    assert lib.q8_quantize(fake, 1, 4, 128, 128, 7, fake, fake, None) == bs.BS_ERR_INVALID   # no such mode
+    # two-level FP4: K % 64, null amax / tensor scale; tensor amax: K % 8
+    assert lib.q4_quantize_two_level(fake, 1, 4, 96, 96, fake, fake, fake, fake, None) == bs.BS_ERR_ALIGN
+    assert lib.q4_quantize_two_level(fake, 1, 4, 64, 64, None, fake, fake, fake, None) == bs.BS_ERR_INVALID
+    assert lib.bs_tensor_amax(fake, 1, 4, 12, 12, fake, None) == bs.BS_ERR_ALIGN
+    # router: k outside [1, min(E, 32)], E outside [1, 1024]
+    assert lib.bs_moe_router_topk(fake, 4, 8, 9, fake, fake, None) == bs.BS_ERR_INVALID
+    assert lib.bs_moe_router_topk(fake, 4, 2048, 8, fake, fake, None) == bs.BS_ERR_INVALID
+    assert lib.bs_moe_router_topk(None, 0, 64, 8, None, None, None) == bs.BS_OK
     g = bs.GemmArgs()
     g.fmt, g.a, g.sfa, g.b, g.sfb, g.out = 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20
     g.M, g.N, g.K, g.alpha, g.ldo, g.out_dtype = 64, 100, 128, 1.0, 128, 1
@@ -90,7 +98,7 @@ def test_host_validation_rejects_before_launch(lib):
     g.ldo = 128
     # per-call kernel choices out of range, and a negative wait limit
     for field, bad in (("fp4_kernel", 3), ("fp4_stage_k", 64), ("fp4_small_experts", -1), ("fp4_half_tail", 5),
-                       ("fp8_stream_k", 9), ("wait_timeout_us", -1), ("weights_ready", 2)):
+                       ("fp8_stream_k", 9), ("wait_timeout_us", -1), ("weights_ready", 2), ("fp8_scaling", 3)):
         setattr(g, field, bad)
         assert lib.bs_gemm(ctypes.byref(g), None) == bs.BS_ERR_INVALID, field
         assert field.encode() in lib.bs_last_error()
