@@ -334,6 +334,63 @@ class Fp8W8A8(Fp8Sweep):
         return time.perf_counter() - t0, 2.0 * rows * cols * self.K
 
 
+class Fp4Decode(Fp8Sweep):
+    """Dense W4A4 decode: M tokens (<= 32) against N = 7168, K = 4096 FP4
+    weights ("Tencent AI Infra interview notes", decode intensity: 2KN FLOPs
+    per KN/2 weight bytes).  X bf16 N(0, 1) with the FP8 sweep's outlier
+    channels, W N(0, 0.02).  Step = q4_quantize(X) + the decode GEMM."""
+
+    def __init__(self, M):
+        super().__init__(M)
+        self.name = f"fp4_decode_M{M}_N7168_K4096"
+        self.metric = f"FP4 decode GEMM TFLOPS (M={M}, N=7168, K=4096)"
+        self.dtype = "e2m1 x e2m1 (e4m3 group-16 scales), fp32 accumulate, bf16 out"
+        self.kernel_src = "fp8_quantized_gemm_q4_gb300/csrc/gemm_fp4_decode.cu"
+        N, K, M = self.N, self.K, self.M
+        self.gemm_bytes = N * K // 2 + N * K // 16 + M * K // 2 + 128 * K // 16 + M * N * 2
+
+    def setup(self, dev):
+        import torch
+        import fp8_quantized_gemm_q4_gb300 as bs
+        d = self.host_inputs()
+        self.h = d
+        self.x = d["x"].to(dev)
+        self.wq, self.ws, _ = bs.q4_quantize(d["w"].to(dev))
+        self.xq = torch.empty((self.M, self.K // 2), dtype=torch.uint8, device=dev)
+        self.xs = torch.empty(bs.sf_bytes(self.M, self.K), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
+        self.launches_per_step = 2
+        self.bytes_in = self.x.numel() * 2
+        self.bytes_out = self.out.numel() * 2
+
+    def step(self, x=None, gemm_events=None):
+        import fp8_quantized_gemm_q4_gb300 as bs
+        x = self.x if x is None else x
+        bs.q4_quantize(x, out=(self.xq, self.xs, None))
+        if gemm_events:
+            gemm_events[0].record()
+        bs.gemm_fp4(self.xq, self.xs, self.wq, self.ws, self.K, out=self.out, weights_ready=True)
+        if gemm_events:
+            gemm_events[1].record()
+        return self.out
+
+    def roofline(self, gemm_ms, peaks, source):
+        return hbm_roofline("fp4_decode_kernel", self.gemm_bytes, gemm_ms, peaks, source)
+
+    def oracle_sample(self, rows, cols, nthreads):
+        import oracle
+        h = self.h
+        if not hasattr(self, "_ow"):
+            self._ow = {}
+        if cols not in self._ow:
+            self._ow[cols] = oracle.q4_quantize(h["w"][:cols])
+        ob, osb = self._ow[cols]
+        t0 = time.perf_counter()
+        oa, osa = oracle.q4_quantize(h["x"][:rows])
+        oracle.gemm_fp4(oa, osa, ob, osb, self.K, nthreads=nthreads)
+        return time.perf_counter() - t0, 2.0 * rows * cols * self.K
+
+
 class DenseTwoLevel(DenseLowRank):
     """Dense W4A4 8192^3 with two-level FP4 operands (power-of-two tensor
     scale above the e4m3 group scales; weights N(0, 0.02)), bf16 out, no
@@ -544,6 +601,8 @@ WORKLOADS = {
     "fp8_w8a8_m16": lambda: Fp8W8A8(16),
     "fp8_w8a8_m4096": lambda: Fp8W8A8(4096),
     "dense_two_level": lambda: DenseTwoLevel(),
+    "fp4_decode_m1": lambda: Fp4Decode(1),
+    "fp4_decode_m16": lambda: Fp4Decode(16),
     "moe_small": lambda: MoEWorkload(large=False),
     "moe_large": lambda: MoEWorkload(large=True),
 }
@@ -683,7 +742,7 @@ def check_device_status():
 # The other configurations of the metric ("block-scaled FP4/FP8 GEMM TFLOPS &
 # % of GB300 dense peak; MoE layer us"), timed in the same run as the dense
 # headline and reported beside it.
-EXTRAS = ("moe_small", "moe_large", "fp8_m16", "fp8_m4096", "fp8_w8a8_m16", "fp8_w8a8_m4096")
+EXTRAS = ("moe_small", "moe_large", "fp8_m16", "fp8_m4096", "fp8_w8a8_m16", "fp8_w8a8_m4096", "fp4_decode_m16")
 
 
 def run_extra(args, name, world, dev, peaks, source):

@@ -50,6 +50,7 @@ class GemmArgs(ctypes.Structure):
         ("fp4_small_experts", ctypes.c_int), ("fp4_half_tail", ctypes.c_int), ("fp8_stream_k", ctypes.c_int),
         ("fp8_scaling", ctypes.c_int), ("wait_timeout_us", ctypes.c_int), ("weights_ready", ctypes.c_int), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t), ("a_tensor_scale", ctypes.c_void_p), ("b_tensor_scale", ctypes.c_void_p),
+        ("fp4_decode", ctypes.c_int),
     ]
 
 
@@ -57,7 +58,8 @@ class GemmArgs(ctypes.Structure):
 # include/bsgemm.h.  Every GEMM call of this binding fills them from the
 # options active on the calling thread: the defaults, or those of an enclosing
 # ``with kernel_options(...)`` block.
-_CHOICES = ("fp4_kernel", "fp4_stage_k", "fp4_small_experts", "fp4_half_tail", "fp8_stream_k", "wait_timeout_us")
+_CHOICES = ("fp4_kernel", "fp4_stage_k", "fp4_small_experts", "fp4_half_tail", "fp4_decode", "fp8_stream_k",
+            "wait_timeout_us")
 FP4_ONE_CTA, FP4_PAIR = 1, 2
 _tls = threading.local()
 
@@ -279,7 +281,7 @@ def _args(fmt, a, sfa, b, sfb, M, N, K, out, alpha=1.0, col_scale=None, lora_t=N
 
 def gemm_fp4(a, sfa, b, sfb, K: int, out_dtype=torch.bfloat16, alpha: float = 1.0, col_scale=None,
              lora_t=None, lora_b_t=None, bias=None, out=None, num_sms: int = 0, a_tensor_scale=None,
-             b_tensor_scale=None, stream=None):
+             b_tensor_scale=None, weights_ready: bool = False, stream=None):
     """Dense block-scaled FP4 GEMM: Y[M, N] from A codes [M, K/2] and B codes [N, K/2]
     (two-level operands: their device tensor scales from q4_quantize_two_level)."""
     M, N = a.shape[0], b.shape[0]
@@ -288,6 +290,13 @@ def gemm_fp4(a, sfa, b, sfb, K: int, out_dtype=torch.bfloat16, alpha: float = 1.
     g = _args(FMT_FP4, a, sfa, b, sfb, M, N, K, out, alpha, col_scale, lora_t, lora_b_t, bias, num_sms)
     g.a_tensor_scale = None if a_tensor_scale is None else a_tensor_scale.data_ptr()
     g.b_tensor_scale = None if b_tensor_scale is None else b_tensor_scale.data_ptr()
+    g.weights_ready = 1 if weights_ready else 0
+    lib = load()
+    nbytes = int(lib.bs_gemm_workspace_bytes(ctypes.byref(g)))
+    if nbytes:   # the decode kernel (M <= 32): stream-K scratch
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        ws = _workspace(a.device, s, nbytes)
+        g.workspace, g.workspace_bytes = ws.data_ptr(), ws.numel()
     _check(load().bs_gemm(ctypes.byref(g), _stream(stream)))
     return out
 

@@ -301,6 +301,7 @@ static bs_status check_choices(const bs_gemm_args* a) {
     return fail(BS_ERR_INVALID, "fp8_stream_k=%d (0, 1 or 2)", a->fp8_stream_k);
   if (a->weights_ready < 0 || a->weights_ready > 1) return fail(BS_ERR_INVALID, "weights_ready=%d (0 or 1)", a->weights_ready);
   if (a->fp8_scaling < 0 || a->fp8_scaling > 2) return fail(BS_ERR_INVALID, "fp8_scaling=%d (0, 1 or 2)", a->fp8_scaling);
+  if (a->fp4_decode < 0 || a->fp4_decode > 2) return fail(BS_ERR_INVALID, "fp4_decode=%d (0, 1 or 2)", a->fp4_decode);
   if (a->wait_timeout_us < 0) return fail(BS_ERR_INVALID, "wait_timeout_us < 0");
   return BS_OK;
 }
@@ -426,6 +427,36 @@ static bs_status launch_fp4(bsk::Fp4Launch& L, const bs_gemm_args* a, int64_t b_
 // most CTAs sharing one tile (maxc) and the workspace it needs (partials,
 // then one counter per tile).
 constexpr size_t kStreamKCounterBytes = 4096;
+
+// Stream-K split of `tiles` output tiles of `units` K steps each over at most
+// `sms` CTAs: the grid, the most CTAs sharing one tile, and the workspace
+// (counter head, then one fp32 partial of 128 x tile_n per share of a tile).
+struct SkSplit {
+  int grid;
+  int maxc;
+  size_t ws_bytes;
+};
+static SkSplit sk_split(long long tiles, long long units, int tile_n, int sms) {
+  SkSplit k;
+  const long long U = tiles * units;
+  const long long G = U < sms ? U : sms;
+  k.grid = (int)G;
+  k.maxc = 0;
+  auto owner = [&](long long u) { return ((u + 1) * G - 1) / U; };
+  for (long long t = 0; t < tiles; ++t) {
+    const long long n = owner(t * units + units - 1) - owner(t * units) + 1;
+    if (n > k.maxc) k.maxc = (int)n;
+  }
+  k.ws_bytes = kStreamKCounterBytes + (size_t)tiles * (size_t)k.maxc * 128 * (size_t)tile_n * sizeof(float);
+  return k;
+}
+
+// FP4 decode kernel (M <= 32, swap-AB, stream-K): used unless the caller
+// turns it off, there is a low-rank branch, or K is not a multiple of 256.
+static bool fp4_decode_applies(const bs_gemm_args* a) {
+  return a->fmt == BS_FMT_FP4 && a->M > 0 && a->M <= 32 && !a->lora_t && a->K % 256 == 0 && a->fp4_decode != 2;
+}
+
 struct Fp8Plan {
   int tile_n;
   long long tiles;
@@ -463,12 +494,64 @@ static Fp8Plan fp8_plan(const bs_gemm_args* a, int sms) {
 }
 
 size_t bs_gemm_workspace_bytes(const bs_gemm_args* a) {
-  if (!a || a->fmt != BS_FMT_FP8 || a->M <= 0 || a->N <= 0 || a->K < 128 || a->num_sms < 0) return 0;
+  if (!a || a->M <= 0 || a->N <= 0 || a->K < 128 || a->num_sms < 0) return 0;
   int sms = 0;
   if (!device_info(nullptr, &sms)) return 0;
   if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
+  if (fp4_decode_applies(a)) return sk_split((a->N + 127) / 128, a->K / 256, a->M <= 16 ? 16 : 32, sms).ws_bytes;
+  if (a->fmt != BS_FMT_FP8) return 0;
   const Fp8Plan P = fp8_plan(a, sms);
   return P.stream_k ? P.ws_bytes : 0;
+}
+
+// FP4 decode launch (see fp4_decode_applies).
+static bs_status launch_fp4_decode(const bs_gemm_args* a, int sms, int* status, cudaStream_t s) {
+  bsk::Fp4DecodeLaunch L;
+  memset(&L, 0, sizeof L);
+  L.tile_n = a->M <= 16 ? 16 : 32;
+  const uint64_t kb = (uint64_t)a->K / 2;
+  bs_status st = make_map(&L.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->b, kb, (uint64_t)a->N, kb, 128, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != BS_OK) return st;
+  st = make_map(&L.tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, kb, (uint64_t)a->M, kb, 128, (uint32_t)L.tile_n,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != BS_OK) return st;
+  bsk::Fp4DecodeParams& p = L.p;
+  p.sfw = static_cast<const uint8_t*>(a->sfb);
+  p.sfx = static_cast<const uint8_t*>(a->sfa);
+  p.M = (int)a->M;
+  p.N = (int)a->N;
+  p.K = (int)a->K;
+  p.alpha = a->alpha;
+  p.col_scale = a->col_scale;
+  p.bias = a->bias;
+  p.a_ts = a->a_tensor_scale;
+  p.b_ts = a->b_tensor_scale;
+  p.out = a->out;
+  p.out_bf16 = a->out_dtype == BS_DTYPE_BF16;
+  p.ldo = a->ldo;
+  p.status = status;
+  p.wait_ns = wait_ns(a);
+  p.pre_b = a->weights_ready == 1 ? bsk::fp4_decode_stages(L.tile_n) : 0;
+  const long long tiles = (a->N + 127) / 128, units = a->K / 256;
+  const SkSplit k = sk_split(tiles, units, L.tile_n, sms);
+  if (a->workspace) {
+    if (!aligned16(a->workspace)) return fail(BS_ERR_ALIGN, "workspace must be 16-byte aligned");
+    if (a->workspace_bytes < k.ws_bytes)
+      return fail(BS_ERR_INVALID, "workspace too small (%zu < %zu bytes)", a->workspace_bytes, k.ws_bytes);
+    L.grid = k.grid;
+    p.maxc = k.maxc;
+    p.counters = static_cast<int*>(a->workspace);
+    p.work = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + kStreamKCounterBytes);
+  } else {
+    // no workspace: whole tiles only, on the largest grid that divides them
+    int g = (int)(tiles < sms ? tiles : sms);
+    while (tiles % g) --g;
+    L.grid = g;
+  }
+  cudaError_t e = bsk::launch_fp4_decode(L, s);
+  if (e != cudaSuccess) return cuda_fail(e, "FP4 decode GEMM launch");
+  return BS_OK;
 }
 
 bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
@@ -493,6 +576,7 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     if ((reinterpret_cast<uintptr_t>(a->a_tensor_scale) | reinterpret_cast<uintptr_t>(a->b_tensor_scale)) & 3)
       return fail(BS_ERR_ALIGN, "tensor scales must be 4-byte aligned");
     if (a->M == 0) return BS_OK;
+    if (fp4_decode_applies(a)) return launch_fp4_decode(a, sms, status, s);
     bsk::Fp4Launch L;
     memset(&L, 0, sizeof L);
     L.p.sfa = static_cast<const uint8_t*>(a->sfa);

@@ -265,8 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) tc_commit(&pfull[sl.index]);
         __syncwarp();
         sl.advance();
-        continue;
-      }
+      } else {
       for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
         if (!mbar_wait_warp(&pempty[sl.index], sl.phase ^ 1u, wg, 60)) { ok = false; break; }
         if (!mbar_wait_warp(&full[ps.index], ps.phase, wg, 61)) { ok = false; break; }
@@ -283,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         ps.advance();
         sl.advance();
+      }
       }
     }
     if (elect_one()) {

@@ -107,6 +107,35 @@ struct Fp4PairLaunch {
 cudaError_t launch_fp4_pair_gemm(const Fp4PairLaunch& L, cudaStream_t stream);
 int fp4_pair_stages(bool lora, int bk);
 
+// FP4 decode shapes (M <= 32): swap-AB, stream-K over all SMs.
+struct Fp4DecodeParams {
+  const uint8_t* sfw;     // weight scales, MMA layout for [N, K]
+  const uint8_t* sfx;     // token scales, MMA layout for [M, K] (block 0 holds every row)
+  int M, N, K;
+  float alpha;
+  const float* col_scale; // [N] or null
+  const void* bias;       // bf16 [N] or null
+  const float* a_ts;      // two-level tensor scales (device, or null = 1)
+  const float* b_ts;
+  void* out;
+  int out_bf16;
+  long long ldo;
+  float* work;            // stream-K partials [tiles][maxc][128][TN]
+  int* counters;          // one arrival counter per tile (zero between calls)
+  int maxc;
+  int pre_b;              // weight stages loaded before waiting on the preceding kernel
+  int* status;
+  unsigned long long wait_ns;
+};
+struct Fp4DecodeLaunch {
+  CUtensorMap tmW, tmX;
+  Fp4DecodeParams p;
+  int tile_n;             // 16 or 32 token columns
+  int grid;
+};
+cudaError_t launch_fp4_decode(const Fp4DecodeLaunch& L, cudaStream_t stream);
+int fp4_decode_stages(int tile_n);
+
 struct Fp8Params {
   const float* sfa;       // [K/128, M]
   const float* sfb;       // [ceil(N/128), K/128]

@@ -201,13 +201,13 @@ bs_status q8_quantize(const void *x, bs_dtype dt, int64_t M, int64_t K, int64_t 
  *   M >= 0, N % 128 == 0, K % 64 == 0 (FP4) or K % 128 == 0 (FP8)
  *   num_sms    persistent grid size limit (0 = all SMs)
  *   n_chunk_blocks  ignored by bs_gemm (grouped tile-order knob)
- *   fp4_kernel, fp4_stage_k, fp4_small_experts, fp4_half_tail, fp8_stream_k,
- *   fp8_scaling, wait_timeout_us, weights_ready
+ *   fp4_kernel, fp4_stage_k, fp4_small_experts, fp4_half_tail, fp4_decode,
+ *   fp8_stream_k, fp8_scaling, wait_timeout_us, weights_ready
  *              per-call kernel choices, described at the fields; 0 = the
  *              library's default.  A zero-initialised struct gets every default.
  *   workspace, workspace_bytes
- *              optional caller-owned device scratch (FP8 decode shapes), see
- *              bs_gemm_workspace_bytes.
+ *              optional caller-owned device scratch (FP8 and FP4 decode
+ *              shapes), see bs_gemm_workspace_bytes.
  * ------------------------------------------------------------------------- */
 typedef struct {
     int fmt;                 /* bs_format */
@@ -267,11 +267,15 @@ typedef struct {
                                     q4_quantize_two_level, or NULL (= 1); Y is multiplied by
                                     both.  Not with the low-rank branch */
     const float *b_tensor_scale;
+    int fp4_decode;          /* FP4 with M <= 32 and K % 256 == 0, no low-rank branch: 1 = the
+                                decode kernel (swap-AB: weight rows fill the MMA's 128 rows, the
+                                tokens its N = 16 or 32; stream-K over every SM through
+                                `workspace`; default); 2 = the regular tile kernels */
 } bs_gemm_args;
 
 /* Bytes of `workspace` bs_gemm would use for these arguments (sizes, format,
- * num_sms, fp8_stream_k) on the current device; 0 when it needs none.  FP8
- * stream-K keeps one arrival counter per tile in the first 4096 bytes (zero
+ * num_sms, fp8_stream_k, fp4_decode) on the current device; 0 when it needs
+ * none.  Stream-K keeps one arrival counter per tile in the first 4096 bytes (zero
  * between calls) and one fp32 partial tile per CTA share of a tile after
  * them (e.g. M <= 16, N = 7168, K = 4096 on 152 SMs: < 2 MB).  Because the
  * counters always sit at the same place, calls of different shapes may share
