@@ -333,17 +333,23 @@ def moe_router(logits, k: int):
 
 
 def moe_layer(x, topk_ids, topk_w, wgu_codes, wgu_sf, wd_codes, wd_sf, F: int,
-              tokens=None, nthreads=None):
+              tokens=None, nthreads=None, fmt: str = "fp4"):
     """FP64 MoE layer ("DeepGEMM for Hopper MoE" section 1: experts then weighted
     sum; section 3.1 swish; "DeepGEMM teardown" 5.3 grouping), in the pages' order:
 
       1. group (token, slot) pairs by expert            (moe_dispatch)
-      2. quantize each routed token's activations       (q4_quantize)
-      3. g = x^ Wg^T, u = x^ Wu^T per expert            (gemm_fp4; Wg = rows [0,F), Wu = [F,2F))
+      2. quantize each routed token's activations       (q4_quantize | q8_quantize)
+      3. g = x^ Wg^T, u = x^ Wu^T per expert            (gemm_fp4 | gemm_fp8; Wg = rows [0,F), Wu = [F,2F))
       4. h = bf16(silu(g) * u)                          (swiglu + bf16 rounding)
-      5. requantize h                                   (q4_quantize)
-      6. y = h^ Wd^T per expert                         (gemm_fp4)
+      5. requantize h                                   (q4_quantize | q8_quantize)
+      6. y = h^ Wd^T per expert                         (gemm_fp4 | gemm_fp8)
       7. out[t] = bf16(sum_slot w[t,slot] * y[t,slot])
+
+    Formats: fmt "fp4" quantizes with q4_quantize and multiplies with gemm_fp4
+    (E2M1 codes, e4m3 group-16 scales); fmt "fp8" quantizes x and h with
+    q8_quantize per 1x128 token block and multiplies with gemm_fp8, the expert
+    weights carrying 128x128 block scales ("DeepGEMM teardown" sections 2.2 and
+    5.3; "DeepGEMM for Hopper MoE" section 2.1: FP8 grouped expert GEMMs).
 
     wgu_codes/wgu_sf: per-expert lists (or arrays) of the quantized [2F,H] gate/up
     weights; wd_codes/wd_sf: per-expert quantized [H,F] down weights.  Only the
@@ -359,18 +365,30 @@ def moe_layer(x, topk_ids, topk_w, wgu_codes, wgu_sf, wd_codes, wd_sf, F: int,
     if tokens is None:
         tokens = np.arange(T)
     tokens = np.asarray(tokens)
+    if fmt == "fp4":
+        quantize = q4_quantize
+
+        def gemm(a, sa, b, sb, K):
+            return gemm_fp4(a, sa, b, sb, K, nthreads=nthreads)
+    elif fmt == "fp8":
+        quantize = q8_quantize
+
+        def gemm(a, sa, b, sb, K):
+            return gemm_fp8(a, sa, b, sb, nthreads=nthreads)
+    else:
+        raise ValueError(f"fmt must be 'fp4' or 'fp8', not {fmt!r}")
     out = np.zeros((len(tokens), H), dtype=np.float64)
     inter = {}
     for i, t in enumerate(tokens):
-        xq, xs = q4_quantize(x[t:t + 1])
+        xq, xs = quantize(x[t:t + 1])
         acc = np.zeros(H, dtype=np.float64)
         for slot in range(k):
             e = int(ids[t, slot])
-            gu, gu_s = gemm_fp4(xq, xs, wgu_codes[e], wgu_sf[e], H, nthreads=nthreads)
+            gu, gu_s = gemm(xq, xs, wgu_codes[e], wgu_sf[e], H)
             g, u = gu[0, :F], gu[0, F:]
             h = round_bf16(swiglu(g, u))
-            hq, hs = q4_quantize(h.astype(np.float32)[None, :])
-            y, ys = gemm_fp4(hq, hs, wd_codes[e], wd_sf[e], F, nthreads=nthreads)
+            hq, hs = quantize(h.astype(np.float32)[None, :])
+            y, ys = gemm(hq, hs, wd_codes[e], wd_sf[e], F)
             acc += w[t, slot] * y[0]
             inter[int(t) * k + slot] = dict(g=g, u=u, h=h, y=y[0], s_gu=gu_s[0], s_y=ys[0])
         out[i] = round_bf16(acc)

@@ -79,6 +79,7 @@ PY_MUTANTS = {
     "h_not_rounded": ("h = round_bf16(swiglu(g, u))", "h = swiglu(g, u)"),
     "routing_weight_dropped": ("acc += w[t, slot] * y[0]", "acc += y[0]"),
     "output_not_rounded": ("out[i] = round_bf16(acc)", "out[i] = acc"),
+    "fp8_layer_with_fp4_quantizer": ("quantize = q8_quantize", "quantize = q4_quantize"),
 }
 
 

@@ -416,6 +416,83 @@ def test_moe_layer_top1_single_expert_is_dense_ffn():
     assert np.array_equal(res["out"], ref)
 
 
+def _quantized_experts_fp8(weights):
+    """Expert weights in FP8 e4m3 with 128x128 block scales (oracle quantizer)."""
+    gu = [oracle.q8_quantize(wgu, 128) for wgu, _ in weights]
+    dn = [oracle.q8_quantize(wd, 128) for _, wd in weights]
+    return [c for c, _ in gu], [s for _, s in gu], [c for c, _ in dn], [s for _, s in dn]
+
+
+def test_moe_layer_fp8_all_ones_hand_case():
+    gold = {r[0]: float(r[1]) for r in read_golden("moe_layer_fp8_allones.txt")}
+    H = F = 128
+    weights = [(np.full((2 * F, H), v, np.float32), np.full((H, F), v, np.float32)) for v in (1.0, 2.0)]
+    x = np.ones((2, H), np.float32)
+    ids = np.array([[0, 1]] * 2, dtype=np.int32)
+    w = np.full((2, 2), 0.5, np.float32)
+    res = oracle.moe_layer(x, ids, w, *_quantized_experts_fp8(weights), F=F, fmt="fp8")
+    assert np.all(res["out"] == gold["out"])
+    for e in (0, 1):
+        it = res["inter"][e]
+        assert np.all(it["g"] == gold[f"g_expert{e}"]) and np.all(it["u"] == gold[f"g_expert{e}"])
+        assert np.all(it["h"] == gold[f"h_expert{e}"])
+        assert np.all(it["y"] == gold[f"y_expert{e}"])
+
+
+def test_moe_layer_fp8_top1_single_expert_is_dense_ffn():
+    """The FP8 layer with one expert and weight 1 is the dense FFN written with
+    library pieces: torch's e4m3 cast to dequantize, numpy matmul, silu."""
+    g = np.random.default_rng(17)
+    T, H, F = 3, 256, 128
+    x = g.standard_normal((T, H)).astype(np.float32)
+    x[:, 5] *= 40
+    wgu = (g.standard_normal((2 * F, H)) * 0.05).astype(np.float32)
+    wd = (g.standard_normal((H, F)) * 0.05).astype(np.float32)
+    res = oracle.moe_layer(x, np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32),
+                           *_quantized_experts_fp8([(wgu, wd)]), F=F, fmt="fp8")
+    dq = lambda c: torch.from_numpy(np.ascontiguousarray(c)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+    def tok(v):            # per 1x128 token block
+        c, s_ = oracle.q8_quantize(v, 1)
+        return dq(c) * np.repeat(s_.astype(np.float64), 128, axis=1)
+
+    def blk(v):            # per 128x128 weight block
+        c, s_ = oracle.q8_quantize(v, 128)
+        return dq(c) * np.repeat(np.repeat(s_.astype(np.float64), 128, axis=1), 128, axis=0)[:v.shape[0]]
+
+    gu = tok(x) @ blk(wgu).T
+    gg, uu = gu[:, :F], gu[:, F:]
+    for t in range(T):
+        assert np.allclose(res["inter"][t]["g"], gg[t], rtol=1e-12, atol=1e-12)
+        assert np.allclose(res["inter"][t]["u"], uu[t], rtol=1e-12, atol=1e-12)
+    h = torch.from_numpy(gg / (1 + np.exp(-gg)) * uu).to(torch.bfloat16).float().numpy()
+    y = tok(h) @ blk(wd).T
+    for t in range(T):
+        assert np.array_equal(res["inter"][t]["h"], h[t].astype(np.float64))
+        assert np.allclose(res["inter"][t]["y"], y[t], rtol=1e-12, atol=1e-12)
+    ref = torch.from_numpy(y).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(res["out"], ref)
+
+
+def test_moe_layer_fp8_expert_relabel_invariance():
+    g = np.random.default_rng(18)
+    T, H, F, E, k = 4, 128, 128, 3, 2
+    x = g.standard_normal((T, H)).astype(np.float32)
+    weights = [((g.standard_normal((2 * F, H)) * 0.3).astype(np.float32),
+                (g.standard_normal((H, F)) * 0.3).astype(np.float32)) for _ in range(E)]
+    ids = np.array([[0, 1], [2, 0], [1, 2], [0, 2]], dtype=np.int32)
+    w = g.uniform(0.1, 1, (T, k)).astype(np.float32)
+    base = oracle.moe_layer(x, ids, w, *_quantized_experts_fp8(weights), F=F, fmt="fp8")["out"]
+    perm = np.array([1, 2, 0])
+    inv = np.argsort(perm)
+    relab = oracle.moe_layer(x, perm[ids], w, *_quantized_experts_fp8([weights[i] for i in inv]), F=F,
+                             fmt="fp8")["out"]
+    assert np.array_equal(base, relab)
+    # the FP8 layer differs from the FP4 one on the same weights (the format is used)
+    fp4 = oracle.moe_layer(x, ids, w, *_quantized_experts(weights), F=F)["out"]
+    assert not np.array_equal(base, fp4)
+
+
 # ---------------------------------------------------------------------------
 # top-k router ("DeepGEMM for Hopper MoE", section 1) and bf16 rounding
 # ---------------------------------------------------------------------------
