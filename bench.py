@@ -590,6 +590,93 @@ class MoEWorkload:
         return time.perf_counter() - t0 + t_router, fl
 
 
+class Fp8MoEWorkload(MoEWorkload):
+    """Grouped FP8 MoE layer from router logits (e4m3 with fp32 scales per 1x128
+    token block and 128x128 expert weight block): router, dispatch, quantize +
+    gather, gate/up GEMM with the SwiGLU epilogue, h quantize, down GEMM with
+    weighted rows, routed combine (one step = one layer, one CUDA graph)."""
+
+    def __init__(self, large=False):
+        super().__init__(large)
+        self.name = f"moe_fp8_T{self.T}_H{self.H}_E{self.E}_k{self.k}_F{self.F}"
+        self.metric = f"MoE grouped FP8 layer TFLOPS (T={self.T}, H={self.H}, E={self.E}, k={self.k}, F={self.F})"
+        self.dtype = "e4m3 x e4m3 (fp32 1x128 / 128x128 block scales), fp32 accumulate, bf16 out"
+
+    def setup(self, dev):
+        import torch
+        import workloads
+        from fp8_quantized_gemm_q4_gb300.moe import Fp8MoELayer, Fp8MoEWeights
+        import fp8_quantized_gemm_q4_gb300 as bs
+        d = self.host_inputs()
+        self.h = d
+        self.x = d["x"].to(dev)
+        self.logits = torch.from_numpy(d["logits"]).to(dev)
+        F2, H, F, E = 2 * self.F, self.H, self.F, self.E
+        wgu_codes = torch.empty((E * F2, H), dtype=torch.uint8, device=dev)
+        wgu_sf = torch.empty((E * F2 // 128, H // 128), dtype=torch.float32, device=dev)
+        wd_codes = torch.empty((E * H, F), dtype=torch.uint8, device=dev)
+        wd_sf = torch.empty((E * H // 128, F // 128), dtype=torch.float32, device=dev)
+        bg, bd = F2 // 128, H // 128
+        # quantize expert by expert so the bf16 weights never all sit on the device
+        for e in range(E):
+            wgu, wd = workloads.moe_expert_weights(e, F, H, index=self.index, device=dev)
+            bs.q8_quantize(wgu, mode=bs.Q8_BLOCK, out=(wgu_codes[e * F2:(e + 1) * F2], wgu_sf[e * bg:(e + 1) * bg]))
+            bs.q8_quantize(wd, mode=bs.Q8_BLOCK, out=(wd_codes[e * H:(e + 1) * H], wd_sf[e * bd:(e + 1) * bd]))
+        W = Fp8MoEWeights(E, H, F, wgu_codes, wgu_sf, wd_codes, wd_sf)
+        self.layer = Fp8MoELayer(W, self.T, self.k, device=dev)
+        self.out = self.layer.out
+        self.layer.capture(self.x, logits=self.logits)
+        self.x, self.logits = self.layer.static_x, self.layer.static_logits
+        # router 1 + dispatch 3 + quantize 1 + gather 1 + gate/up GEMM 1 +
+        # quantize h 1 + down GEMM 1 + combine 3
+        self.launches_per_step = 12
+        self.bytes_in = self.x.numel() * 2 + self.logits.numel() * 4
+        self.bytes_out = self.out.numel() * 2
+        self.layer.replay()
+        counts = torch.bincount(self.layer.topk_ids.flatten().long(), minlength=E).cpu()
+        self.load_hist = {"max": int(counts.max()), "min": int(counts.min()), "empty": int((counts == 0).sum())}
+
+    def algorithmic_bytes(self):
+        """Every expert's FP8 weights and their 128x128 block scales (read
+        once), the bf16 activations and fp32 router logits in, the bf16 output."""
+        E, H, F, T = self.E, self.H, self.F, self.T
+        w = E * (2 * F * H + H * F)
+        return w + (w // (128 * 128)) * 4 + T * H * 2 + T * E * 4 + T * H * 2
+
+    def roofline(self, layer_ms, peaks, source):
+        kern = "whole layer (fp8_grouped_kernel x2 + quantize x2 + gather + router + dispatch + combine)"
+        r = tensor_roofline(kern, self.flops, layer_ms, peaks, source, NOMINAL_FP8_OVER_BF16, NOMINAL_FP8_TFLOPS,
+                            "FP8")
+        h = hbm_roofline(kern, self.algorithmic_bytes(), layer_ms, peaks, source)
+        r["hbm"] = {k: h[k] for k in ("achieved", "peak", "unit", "frac", "peak_source",
+                                      "algorithmic_bytes_per_launch")}
+        r["expert_load"] = getattr(self, "load_hist", None)
+        return r
+
+    def oracle_sample(self, rows, cols, nthreads):
+        """`rows` tokens through the oracle's FP8 layer (cols ignored)."""
+        import oracle
+        import workloads
+        h = self.h
+        t0 = time.perf_counter()
+        ids, wts = oracle.moe_router(h["logits"][:rows], self.k)
+        t_router = time.perf_counter() - t0
+        experts = sorted(set(int(e) for t in range(rows) for e in ids[t]))
+        if not hasattr(self, "_ow8"):
+            self._ow8 = {}
+        for e in experts:
+            if e not in self._ow8:
+                wgu, wd = workloads.moe_expert_weights(e, self.F, self.H, index=self.index, device="cuda")
+                self._ow8[e] = (oracle.q8_quantize(wgu.cpu(), 128), oracle.q8_quantize(wd.cpu(), 128))
+        E = self.E
+        pick = lambda i, j: [self._ow8[e][i][j] if e in self._ow8 else None for e in range(E)]
+        t0 = time.perf_counter()
+        oracle.moe_layer(h["x"][:rows], ids, wts.astype("float32"), pick(0, 0), pick(0, 1), pick(1, 0), pick(1, 1),
+                         F=self.F, nthreads=nthreads, fmt="fp8")
+        fl = 2.0 * rows * self.k * (self.H * 2 * self.F + self.F * self.H)
+        return time.perf_counter() - t0 + t_router, fl
+
+
 WORKLOADS = {
     "dense_lowrank": lambda: DenseLowRank(tiny=False),
     "dense_tiny": lambda: DenseLowRank(tiny=True),
@@ -605,6 +692,7 @@ WORKLOADS = {
     "fp4_decode_m16": lambda: Fp4Decode(16),
     "moe_small": lambda: MoEWorkload(large=False),
     "moe_large": lambda: MoEWorkload(large=True),
+    "moe_fp8_small": lambda: Fp8MoEWorkload(large=False),
 }
 
 
@@ -742,7 +830,8 @@ def check_device_status():
 # The other configurations of the metric ("block-scaled FP4/FP8 GEMM TFLOPS &
 # % of GB300 dense peak; MoE layer us"), timed in the same run as the dense
 # headline and reported beside it.
-EXTRAS = ("moe_small", "moe_large", "fp8_m16", "fp8_m4096", "fp8_w8a8_m16", "fp8_w8a8_m4096", "fp4_decode_m16")
+EXTRAS = ("moe_small", "moe_large", "moe_fp8_small", "fp8_m16", "fp8_m4096", "fp8_w8a8_m16", "fp8_w8a8_m4096",
+          "fp4_decode_m16")
 
 
 def run_extra(args, name, world, dev, peaks, source):
@@ -811,7 +900,8 @@ def run_ours(args, wl, rank, world, dev, peaks, source):
                          "read so L2 holds clean lines; outside the step events)",
                    "enqueue": "timed steps queued behind a GPU spin (device time without host launch gaps)",
                    "parallelism": f"replicas x{world}",
-                   **({"moe_combine": wl.combine, "cuda_graph": wl.graph, "h_quant": wl.layer.h_quant}
+                   **({"moe_combine": wl.combine, "cuda_graph": wl.graph,
+                       "h_quant": getattr(wl.layer, "h_quant", "separate")}
                       if hasattr(wl, "combine") else {})},
         "e2e": {"value": round(job_throughput(wl.flops, world, e2e_ms) / 1e12, 2), "unit": wl.unit,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": wl.bytes_in,

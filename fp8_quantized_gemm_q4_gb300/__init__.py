@@ -20,8 +20,8 @@ import torch
 from ._build import LIB as _LIB_PATH
 
 __all__ = [
-    "load", "sf_bytes", "sf_offset", "q4_quantize", "tensor_amax", "q4_quantize_two_level", "fp4_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
-    "grouped_gemm_fp4", "grouped_gemm_fp4_swiglu_q4", "moe_router_topk", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
+    "load", "sf_bytes", "sf_offset", "q4_quantize", "tensor_amax", "q4_quantize_two_level", "fp4_gather_rows", "fp8_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
+    "grouped_gemm_fp4", "grouped_gemm_fp4_swiglu_q4", "grouped_gemm_fp8", "moe_router_topk", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
     "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE", "EPI_ROWS", "kernel_options",
     "current_kernel_options", "FP4_ONE_CTA", "FP4_PAIR",
 ]
@@ -116,6 +116,8 @@ def load(path: str | None = None):
         lib.q4_quantize_two_level.argtypes = [P, I, I64, I64, I64, P, P, P, P, P]
         lib.bs_fp4_gather_rows.restype = I
         lib.bs_fp4_gather_rows.argtypes = [P, P, I64, I64, P, I64, P, P, P]
+        lib.bs_fp8_gather_rows.restype = I
+        lib.bs_fp8_gather_rows.argtypes = [P, P, I64, I64, P, I64, P, P, P]
         lib.q8_quantize.restype = I
         lib.q8_quantize.argtypes = [P, I, I64, I64, I64, I, P, P, P]
         lib.bs_gemm.restype = I
@@ -241,6 +243,19 @@ def fp4_gather_rows(codes, sf, K: int, gather, out=None, stream=None):
     return out
 
 
+def fp8_gather_rows(codes, scales, gather, out=None, stream=None):
+    """Rows gather[i] of an FP8 matrix (codes [rows, K] + TOKEN-mode scales
+    [K/128, rows]); -1 -> zero row with zero scales."""
+    rows_in, K = codes.shape
+    rows_out = gather.numel()
+    if out is None:
+        out = (torch.empty((rows_out, K), dtype=torch.uint8, device=codes.device),
+               torch.empty((K // 128, rows_out), dtype=torch.float32, device=codes.device))
+    _check(load().bs_fp8_gather_rows(_ptr(codes), _ptr(scales), rows_in, K, _ptr(gather), rows_out,
+                                     _ptr(out[0]), _ptr(out[1]), _stream(stream)))
+    return out
+
+
 def q8_quantize(x: torch.Tensor, mode: int = Q8_TOKEN, out=None, stream=None):
     """FP8 e4m3 quantization.  TOKEN mode: scales fp32 [K/128, M]; BLOCK mode:
     scales fp32 [ceil(M/128), K/128]; ROW mode (W8A8): scales fp32 [M]."""
@@ -348,6 +363,22 @@ def grouped_gemm_fp4(a, sfa, b, sfb, K: int, N: int, E: int, offsets, counts, ep
     ld32 = 0 if out32 is None else out32.stride(0)
     _check(load().bs_grouped_gemm(ctypes.byref(g), E, _ptr(offsets), _ptr(counts), epilogue, _ptr(token_of),
                                   _ptr(weight_of), _ptr(out32), ld32, _stream(stream)))
+    return out
+
+
+def grouped_gemm_fp8(a, sfa, b, sfb, N: int, E: int, offsets, counts, epilogue: int, out=None, weight_of=None,
+                     num_sms: int = 0, stream=None):
+    """FP8 GEMM grouped over experts: ``a`` e4m3 [M, K] with TOKEN-mode scales
+    ``sfa`` [K/128, M] (rows grouped by ``offsets``/``counts``), ``b`` the
+    stacked expert weights [E*Nw, K] with 128x128 block scales ``sfb``.
+    Epilogues EPI_STORE, EPI_SWIGLU (bf16 h) and EPI_ROWS (fp32, weight_of)."""
+    M, K = a.shape
+    if out is None:
+        dt = torch.float32 if epilogue == EPI_ROWS else torch.bfloat16
+        out = torch.empty((M, N), dtype=dt, device=a.device)
+    g = _args(FMT_FP8, a, sfa, b, sfb, M, N, K, out, num_sms=num_sms)
+    _check(load().bs_grouped_gemm(ctypes.byref(g), E, _ptr(offsets), _ptr(counts), epilogue, None,
+                                  _ptr(weight_of), None, 0, _stream(stream)))
     return out
 
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libbsgemm.so")
-SOURCES = ["api.cu", "quant.cu", "gemm_fp4.cu", "gemm_fp4_pair.cu", "gemm_fp4_decode.cu", "gemm_fp8.cu", "moe.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm_fp4.cu", "gemm_fp4_pair.cu", "gemm_fp4_decode.cu", "gemm_fp8.cu", "gemm_fp8_grouped.cu", "moe.cu"]
 HEADERS = ["ptx.cuh", "kernels.h", "budget.hpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -270,6 +270,24 @@ bs_status bs_fp4_gather_rows(const uint8_t* codes_in, const uint8_t* sf_in, int6
   return BS_OK;
 }
 
+bs_status bs_fp8_gather_rows(const uint8_t* codes_in, const float* scales_in, int64_t rows_in, int64_t K,
+                             const int32_t* gather, int64_t rows_out, uint8_t* codes_out, float* scales_out,
+                             bs_stream_t stream) {
+  if (rows_in < 0 || rows_out < 0 || K <= 0) return fail(BS_ERR_INVALID, "fp8_gather_rows: bad sizes");
+  if (K % 128) return fail(BS_ERR_ALIGN, "fp8_gather_rows: K=%lld not a multiple of 128", (long long)K);
+  if (rows_out == 0) return BS_OK;
+  if (!gather || !codes_out || !scales_out || (rows_in > 0 && (!codes_in || !scales_in)))
+    return fail(BS_ERR_INVALID, "fp8_gather_rows: null pointer");
+  if (!aligned16(codes_out) || (codes_in && !aligned16(codes_in)) ||
+      ((reinterpret_cast<uintptr_t>(scales_out) | reinterpret_cast<uintptr_t>(scales_in)) & 3))
+    return fail(BS_ERR_ALIGN, "fp8_gather_rows: codes must be 16-byte and scales 4-byte aligned");
+  if (!device_info(nullptr, nullptr)) return fail(BS_ERR_CUDA, "no current device");
+  cudaError_t e = bsk::launch_fp8_gather_rows(codes_in, scales_in, rows_in, K, gather, rows_out, codes_out,
+                                              scales_out, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_gather_rows launch");
+  return BS_OK;
+}
+
 bs_status q8_quantize(const void* x, bs_dtype dt, int64_t M, int64_t K, int64_t ldx, int mode, uint8_t* codes,
                       float* scales, bs_stream_t stream) {
   if (M < 0 || K <= 0) return fail(BS_ERR_INVALID, "q8_quantize: M=%lld K=%lld", (long long)M, (long long)K);
@@ -650,6 +668,63 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
   return fail(BS_ERR_INVALID, "fmt %d", a->fmt);
 }
 
+// FP8 grouped GEMM (tokens as the MMA's M, see gemm_fp8_grouped.cu); args
+// already passed check_common.
+static bs_status grouped_fp8(const bs_gemm_args* a, int E, const int32_t* offsets, const int32_t* counts,
+                             int epilogue, const float* weight_of, cudaStream_t s) {
+  if (a->K % 128) return fail(BS_ERR_ALIGN, "FP8: K=%lld not a multiple of 128", (long long)a->K);
+  if (epilogue == BS_EPI_COMBINE) return fail(BS_ERR_UNSUPPORTED, "FP8 grouped GEMM: COMBINE epilogue (use ROWS)");
+  if (E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "E=%d outside [1, 1024]", E);
+  if (!offsets || !counts) return fail(BS_ERR_INVALID, "null offsets/counts");
+  if (a->lora_t || a->col_scale || a->bias || a->alpha != 1.0f || a->a_tensor_scale || a->b_tensor_scale ||
+      a->fp8_scaling == 2)
+    return fail(BS_ERR_UNSUPPORTED, "FP8 grouped GEMM takes no alpha/col_scale/bias/low-rank/tensor scales/W8A8");
+  if (epilogue == BS_EPI_SWIGLU && a->out_dtype != BS_DTYPE_BF16) return fail(BS_ERR_INVALID, "SWIGLU output is bf16");
+  if (epilogue == BS_EPI_ROWS) {
+    if (a->out_dtype != BS_DTYPE_F32) return fail(BS_ERR_INVALID, "ROWS output is fp32");
+    if (!weight_of) return fail(BS_ERR_INVALID, "ROWS needs weight_of");
+  }
+  if (reinterpret_cast<uintptr_t>(a->sfa) & 3 || reinterpret_cast<uintptr_t>(a->sfb) & 3)
+    return fail(BS_ERR_ALIGN, "FP8 scales must be 4-byte aligned");
+  const int64_t wrows = (epilogue == BS_EPI_SWIGLU ? 2 : 1) * a->N * (int64_t)E;
+  if (wrows > (1LL << 30)) return fail(BS_ERR_INVALID, "stacked weights too large");
+  const int64_t nbk = epilogue == BS_EPI_SWIGLU ? a->N / (bsk::kFp8GroupedBN / 2)
+                                                : (a->N + bsk::kFp8GroupedBN - 1) / bsk::kFp8GroupedBN;
+  if ((a->M / 128 + E) * nbk >= (1LL << 31)) return fail(BS_ERR_INVALID, "too many tiles");
+  int* status = nullptr;
+  int sms = 0;
+  if (!device_info(&status, &sms)) return fail(BS_ERR_CUDA, "no current device");
+  if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
+  if (a->M == 0) return BS_OK;
+  bsk::Fp8GroupedLaunch L;
+  memset(&L, 0, sizeof L);
+  bs_status st = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, (uint64_t)a->K, (uint64_t)a->M,
+                          (uint64_t)a->K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != BS_OK) return st;
+  st = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->b, (uint64_t)a->K, (uint64_t)wrows, (uint64_t)a->K, 128,
+                bsk::kFp8GroupedBN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != BS_OK) return st;
+  L.p.sfa = static_cast<const float*>(a->sfa);
+  L.p.sfb = static_cast<const float*>(a->sfb);
+  L.p.M = (int)a->M;
+  L.p.N = (int)a->N;
+  L.p.K = (int)a->K;
+  L.p.E = E;
+  L.p.offsets = offsets;
+  L.p.counts = counts;
+  L.p.weight_of = weight_of;
+  L.p.out = a->out;
+  L.p.out_bf16 = a->out_dtype == BS_DTYPE_BF16;
+  L.p.ldo = a->ldo;
+  L.p.status = status;
+  L.p.wait_ns = wait_ns(a);
+  L.epilogue = epilogue == BS_EPI_STORE ? bsk::kEpiStore : epilogue == BS_EPI_SWIGLU ? bsk::kEpiSwiglu : bsk::kEpiRows;
+  L.grid = sms;
+  cudaError_t e = bsk::launch_fp8_grouped(L, s);
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 grouped GEMM launch");
+  return BS_OK;
+}
+
 bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, const int32_t* counts,
                           int epilogue, const int32_t* token_of, const float* weight_of, float* out32,
                           int64_t ld_out32, bs_stream_t stream) {
@@ -659,7 +734,9 @@ bs_status bs_grouped_gemm(const bs_gemm_args* a, int E, const int32_t* offsets, 
     return fail(BS_ERR_INVALID, "epilogue %d", epilogue);
   bs_status st = check_common(a, epilogue == BS_EPI_COMBINE);
   if (st != BS_OK) return st;
-  if (a->fmt != BS_FMT_FP4) return fail(BS_ERR_UNSUPPORTED, "grouped GEMM is FP4 only");
+  if (a->fmt == BS_FMT_FP8)
+    return grouped_fp8(a, E, offsets, counts, epilogue, weight_of, reinterpret_cast<cudaStream_t>(stream));
+  if (a->fmt != BS_FMT_FP4) return fail(BS_ERR_INVALID, "fmt %d", a->fmt);
   if (a->K % 64) return fail(BS_ERR_ALIGN, "FP4: K=%lld not a multiple of 64", (long long)a->K);
   if (E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "E=%d outside [1, 1024]", E);
   if (!offsets || !counts) return fail(BS_ERR_INVALID, "null offsets/counts");
@@ -713,7 +790,7 @@ bs_status bs_grouped_gemm_swiglu_q4(const bs_gemm_args* a, int E, const int32_t*
   if (a->out) return fail(BS_ERR_INVALID, "SWIGLU_Q4 writes h_codes / h_sf: args->out must be NULL");
   bs_status st = check_common(a, true);
   if (st != BS_OK) return st;
-  if (a->fmt != BS_FMT_FP4) return fail(BS_ERR_UNSUPPORTED, "grouped GEMM is FP4 only");
+  if (a->fmt != BS_FMT_FP4) return fail(BS_ERR_UNSUPPORTED, "SWIGLU_Q4 is FP4 only");
   if (a->K % 64) return fail(BS_ERR_ALIGN, "FP4: K=%lld not a multiple of 64", (long long)a->K);
   if (E <= 0 || E > 1024) return fail(BS_ERR_INVALID, "E=%d outside [1, 1024]", E);
   if (!offsets || !counts) return fail(BS_ERR_INVALID, "null offsets/counts");

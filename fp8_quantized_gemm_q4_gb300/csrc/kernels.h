@@ -164,6 +164,32 @@ cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream);
 int fp8_tile_n(long long M);
 int fp8_stages(int tile_n);
 
+// FP8 grouped over MoE experts: the tokens of a 128-row block of an expert
+// segment are the MMA's M, kFp8GroupedBN weight rows its N.
+constexpr int kFp8GroupedBN = 128;
+struct Fp8GroupedParams {
+  const float* sfa;       // [K/128, M]
+  const float* sfb;       // [E * Nw / 128, K/128] (Nw = 2N for SWIGLU, else N)
+  int M, N, K, E;         // N: output columns per row (SWIGLU: h columns)
+  const int* offsets;     // [E+1]
+  const int* counts;      // [E]
+  const float* weight_of; // ROWS: [M]
+  void* out;
+  int out_bf16;
+  long long ldo;
+  int* status;
+  unsigned long long wait_ns;  // bound of every pipeline wait (%globaltimer ns)
+};
+struct Fp8GroupedLaunch {
+  CUtensorMap tmA;        // token codes [M, K], box 128 rows x 128 bytes
+  CUtensorMap tmB;        // stacked weights [E * Nw, K], box kFp8GroupedBN / 2 rows x 128 bytes
+  Fp8GroupedParams p;
+  int epilogue;           // kEpiStore, kEpiSwiglu or kEpiRows
+  int grid;
+};
+cudaError_t launch_fp8_grouped(const Fp8GroupedLaunch& L, cudaStream_t stream);
+int fp8_grouped_stages();
+
 // quantizers
 cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long K, long long ldx,
                                const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream,
@@ -175,6 +201,9 @@ cudaError_t launch_q4_lowrank_fused(const void* x, long long M, long long K, lon
                                     cudaStream_t stream);
 cudaError_t launch_fp4_gather_rows(const uint8_t* codes_in, const uint8_t* sf_in, long long rows_in, long long K,
                                    const int* gather, long long rows_out, uint8_t* codes_out, uint8_t* sf_out,
+                                   cudaStream_t stream);
+cudaError_t launch_fp8_gather_rows(const uint8_t* codes_in, const float* scales_in, long long rows_in, long long K,
+                                   const int* gather, long long rows_out, uint8_t* codes_out, float* scales_out,
                                    cudaStream_t stream);
 cudaError_t launch_lowrank_t(const void* x, long long M, long long K, long long ldx, const int* gather,
                              const void* lora_a_t, void* lora_t, cudaStream_t stream);

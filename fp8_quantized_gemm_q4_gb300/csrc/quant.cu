@@ -794,4 +794,72 @@ cudaError_t launch_fp4_gather_rows(const uint8_t* codes_in, const uint8_t* sf_in
                        rows_out, pad, codes_out, sf_out);
 }
 
+// Rows of an FP8 matrix written by q8_quantize in 1x128 token mode, gathered:
+// output row i = input row gather[i] (negative or out of range: a zero row
+// with zero scales).  The scales are K-block major ([K/128, rows]), so for
+// each K block the 128 scales of an output row block are one coalesced
+// 512-byte store.  Used to group MoE activations by expert after quantizing
+// each token once ("DeepGEMM teardown", section 5.3).
+__global__ void __launch_bounds__(256) fp8_gather_rows_kernel(const uint8_t* __restrict__ codes_in,
+                                                              const float* __restrict__ scales_in,
+                                                              long long rows_in, long long K,
+                                                              const int* __restrict__ gather, long long rows_out,
+                                                              uint8_t* __restrict__ codes_out,
+                                                              float* __restrict__ scales_out) {
+  griddep_wait();  // inputs may come from the kernel just before on the stream
+  griddep_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long kv = K / 16;   // 16-byte vectors per row of codes
+  const long long nkb = K / 128;
+  for (long long blk = blockIdx.x; blk * 128 < rows_out; blk += gridDim.x) {
+    const long long r0 = blk * 128;
+    // codes: warp w copies rows r0 + 16 w .. + 16 (their sources read up front)
+    long long my_src = -1;
+    if (lane < 16 && r0 + warp * 16 + lane < rows_out) {
+      my_src = gather[r0 + warp * 16 + lane];
+      if (my_src >= rows_in) my_src = -1;
+    }
+    const long long left = rows_out - (r0 + warp * 16);
+    const int nrows = left < 16 ? (left > 0 ? (int)left : 0) : 16;
+    for (int i = 0; i < nrows; ++i) {
+      const long long row = r0 + warp * 16 + i;
+      const long long src = __shfl_sync(0xffffffffu, my_src, i);
+      const uint4* sp = reinterpret_cast<const uint4*>(codes_in + (src >= 0 ? src : 0) * K);
+      uint4* dp = reinterpret_cast<uint4*>(codes_out + row * K);
+      for (long long v0 = 0; v0 < kv; v0 += 32 * kGatherVec) {
+        uint4 buf[kGatherVec];
+#pragma unroll
+        for (int u = 0; u < kGatherVec; ++u) {
+          const long long v = v0 + u * 32 + lane;
+          buf[u] = (src >= 0 && v < kv) ? __ldg(sp + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kGatherVec; ++u) {
+          const long long v = v0 + u * 32 + lane;
+          if (v < kv) dp[v] = buf[u];
+        }
+      }
+    }
+    // scales: thread j serves row r0 + (j % 128) of every other K block
+    const long long row = r0 + (tid & 127);
+    long long src = row < rows_out ? (long long)gather[row] : -1;
+    if (src >= rows_in) src = -1;
+    if (row < rows_out) {
+      for (long long kb = tid >> 7; kb < nkb; kb += 2)
+        scales_out[kb * rows_out + row] = src >= 0 ? __ldg(scales_in + kb * rows_in + src) : 0.0f;
+    }
+  }
+}
+
+cudaError_t launch_fp8_gather_rows(const uint8_t* codes_in, const float* scales_in, long long rows_in, long long K,
+                                   const int* gather, long long rows_out, uint8_t* codes_out, float* scales_out,
+                                   cudaStream_t stream) {
+  long long blocks = (rows_out + 127) / 128;
+  const long long cap = (long long)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_kernel(fp8_gather_rows_kernel, (unsigned)blocks, 256, 0, stream, 1, codes_in, scales_in, rows_in, K,
+                       gather, rows_out, codes_out, scales_out);
+}
+
 }  // namespace bsk

@@ -157,6 +157,24 @@ bs_status bs_fp4_gather_rows(const uint8_t *codes_in, const uint8_t *sf_in, int6
                              bs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * bs_fp8_gather_rows -- gather rows of an FP8 matrix that q8_quantize wrote in
+ * TOKEN (1x128) mode: output row i = input row gather[i] (a negative or
+ * out-of-range index gives a zero row with zero scales), codes copied and the
+ * row's K-block scales moved to the output row's place.  Bit-identical to
+ * q8_quantize of the gathered unquantized rows, because the 1x128 blocks are
+ * row-local; groups MoE activations by expert ("DeepGEMM teardown",
+ * section 5.3) after quantizing each token once.
+ *
+ *   codes_in, scales_in    [rows_in, K] e4m3 codes and fp32 [K/128, rows_in]
+ *   gather                 int32 [rows_out]
+ *   codes_out, scales_out  [rows_out, K] and fp32 [K/128, rows_out]
+ *   K % 128 == 0; codes 16-byte aligned, scales 4-byte aligned
+ * ------------------------------------------------------------------------- */
+bs_status bs_fp8_gather_rows(const uint8_t *codes_in, const float *scales_in, int64_t rows_in, int64_t K,
+                             const int32_t *gather, int64_t rows_out, uint8_t *codes_out, float *scales_out,
+                             bs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * q8_quantize -- FP8 e4m3 quantization with fp32 block scales ("DeepGEMM
  * teardown", section 2.2 per-token / per-block scaling, section 5.2 scale =
  * max_val / 448).  For every block (1 x 128 in BS_Q8_TOKEN_1x128 mode,
@@ -285,9 +303,10 @@ size_t bs_gemm_workspace_bytes(const bs_gemm_args *args);
 bs_status bs_gemm(const bs_gemm_args *args, bs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * bs_grouped_gemm -- FP4 GEMM grouped over E experts in one persistent
+ * bs_grouped_gemm -- FP4 or FP8 GEMM grouped over E experts in one persistent
  * launch ("DeepGEMM teardown", section 1.2 grouped/segmented GEMM and 5.3
- * group offsets; "DeepGEMM for Hopper MoE", section 3 fused expert compute).
+ * group offsets; "DeepGEMM for Hopper MoE", section 3 fused expert compute,
+ * section 2.1 FP8 expert GEMMs).
  *
  * Rows of A are grouped by expert: expert e owns rows
  * [offsets[e], offsets[e] + counts[e]); every offsets[e] is a multiple of 128
@@ -316,6 +335,17 @@ bs_status bs_gemm(const bs_gemm_args *args, bs_stream_t stream);
  *                                   two-pass routed combine, see bs_moe_combine
  *   token_of        int32 [M] (COMBINE only); weight_of fp32 [M] (COMBINE, ROWS)
  * Only alpha = 1, no col_scale, no lora and no bias are accepted here.
+ *
+ * FP8 (args->fmt = BS_FMT_FP8; "DeepGEMM teardown", sections 2.2 and 5.3):
+ *   Y[r, n] = sum_kb sa[kb, r] * sb[(e*Nw + n)/128, kb] * sum_{k in kb} a[r,k] b[e*Nw + n, k]
+ *   args->a/sfa     e4m3 codes [M, K] and fp32 scales [K/128, M] of all rows
+ *                   (q8_quantize TOKEN mode, or bs_fp8_gather_rows)
+ *   args->b/sfb     stacked e4m3 weights [E*Nw, K] and their 128x128 block
+ *                   scales fp32 [E*Nw/128, K/128] (q8_quantize BLOCK mode of
+ *                   the stacked matrix; Nw % 128 == 0, so no block straddles
+ *                   two experts)
+ *   K % 128 == 0; epilogues STORE, SWIGLU and ROWS as above (COMBINE returns
+ *   BS_ERR_UNSUPPORTED); fp8_scaling must not be 2 (W8A8 is dense only).
  * Offsets that break the contract set BS_ERR_OFFSETS in the device status and
  * the kernel writes nothing.
  * ------------------------------------------------------------------------- */
