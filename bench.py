@@ -590,6 +590,82 @@ class MoEWorkload:
         return time.perf_counter() - t0 + t_router, fl
 
 
+class QuantWorkload:
+    """Activation quantizer alone, an HBM-bound kernel: "q4" = FP4 (E2M1 codes,
+    e4m3 group-16 scales) of the 8192 x 8192 bf16 activations of the dense
+    workload; "q8" = FP8 1x128 token blocks of the 4096 x 4096 bf16
+    activations of the FP8 prefill workload.  value = algorithmic bytes per
+    second (TB/s; the bytes take the place of FLOPs in the common fields)."""
+
+    def __init__(self, kind):
+        self.kind = kind
+        if kind == "q4":
+            self.M = self.K = 8192
+            self.name = "q4_quantize_bf16_8192x8192"
+            self.metric = "FP4 activation quantizer HBM throughput (8192 x 8192 bf16)"
+            per_elem = 2 + 0.5 + 1 / 16
+            self.kernel = "q4_quantize_kernel"
+        else:
+            self.M, self.K = 4096, 4096
+            self.name = "q8_quantize_token_bf16_4096x4096_outliers"
+            self.metric = "FP8 1x128 token quantizer HBM throughput (4096 x 4096 bf16)"
+            per_elem = 2 + 1 + 4 / 128
+            self.kernel = "q8_token_kernel"
+        self.N = self.K
+        self.flops = per_elem * self.M * self.K   # algorithmic bytes
+        self.unit = "TB/s"
+        self.higher_is_better = True
+        self.dtype = "bf16 in; e2m1 codes + e4m3 scales out" if kind == "q4" else "bf16 in; e4m3 codes + fp32 scales out"
+        self.launches_per_step = 1
+
+    def host_inputs(self):
+        import workloads
+        return workloads.dense_lowrank() if self.kind == "q4" else workloads.fp8_sweep(4096)
+
+    def setup(self, dev):
+        import torch
+        import fp8_quantized_gemm_q4_gb300 as bs
+        d = self.host_inputs()
+        self.h = d
+        self.x = d["x"].to(dev)
+        M, K = self.M, self.K
+        if self.kind == "q4":
+            self.outs = (torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+                         torch.empty(bs.sf_bytes(M, K), dtype=torch.uint8, device=dev), None)
+        else:
+            self.outs = (torch.empty((M, K), dtype=torch.uint8, device=dev),
+                         torch.empty((K // 128, M), dtype=torch.float32, device=dev))
+        self.out = self.outs[0]   # the codes: what the end-to-end pass reads back
+        self.bytes_in = self.x.numel() * 2
+        self.bytes_out = self.out.numel()
+
+    def step(self, x=None, gemm_events=None):
+        import fp8_quantized_gemm_q4_gb300 as bs
+        x = self.x if x is None else x
+        if gemm_events:
+            gemm_events[0].record()
+        if self.kind == "q4":
+            bs.q4_quantize(x, out=self.outs)
+        else:
+            bs.q8_quantize(x, out=self.outs)
+        if gemm_events:
+            gemm_events[1].record()
+        return self.out
+
+    def roofline(self, kern_ms, peaks, source):
+        return hbm_roofline(self.kernel, self.flops, kern_ms, peaks, source)
+
+    def oracle_sample(self, rows, cols, nthreads):
+        import oracle
+        x = self.h["x"][:rows]
+        t0 = time.perf_counter()
+        if self.kind == "q4":
+            oracle.q4_quantize(x)
+        else:
+            oracle.q8_quantize(x, 1)
+        return time.perf_counter() - t0, self.flops * rows / self.M
+
+
 class Fp8MoEWorkload(MoEWorkload):
     """Grouped FP8 MoE layer from router logits (e4m3 with fp32 scales per 1x128
     token block and 128x128 expert weight block): router, dispatch, quantize +
@@ -693,6 +769,8 @@ WORKLOADS = {
     "moe_small": lambda: MoEWorkload(large=False),
     "moe_large": lambda: MoEWorkload(large=True),
     "moe_fp8_small": lambda: Fp8MoEWorkload(large=False),
+    "q4_quantize": lambda: QuantWorkload("q4"),
+    "q8_quantize": lambda: QuantWorkload("q8"),
 }
 
 
@@ -831,7 +909,7 @@ def check_device_status():
 # % of GB300 dense peak; MoE layer us"), timed in the same run as the dense
 # headline and reported beside it.
 EXTRAS = ("moe_small", "moe_large", "moe_fp8_small", "fp8_m16", "fp8_m4096", "fp8_w8a8_m16", "fp8_w8a8_m4096",
-          "fp4_decode_m16")
+          "fp4_decode_m16", "q4_quantize", "q8_quantize")
 
 
 def run_extra(args, name, world, dev, peaks, source):

@@ -2,12 +2,11 @@
 //
 // FP4: per group of 16 K elements s = e4m3(fl32(amax / 6)), code =
 // e2m1(fl32(x / s)) ("Tencent AI Infra interview notes": E2M1 format table,
-// per-group quantization, online activation quantization).  Each thread owns 8
-// consecutive elements (one 128-bit bf16 load), a group is a lane pair (one
-// shuffle for its amax), and the four scales of a 64-element chunk are
-// gathered by shuffles into the 32-bit word the tensor core reads, written at
-// its place in the MMA scale layout.  Codes use the hardware cvt with round to
-// nearest even and saturation; the divisions are IEEE.
+// per-group quantization, online activation quantization).  One lane owns one
+// 16-element group; the quotients x / s are correctly rounded (one-correction
+// form on packed fp32 pairs, or IEEE division), scales and codes are written
+// at their places in the MMA layouts.  Codes use the hardware cvt with round
+// to nearest even and saturation.
 //
 // FP8: s = fl32(amax / 448), code = e4m3(fl32(x / s)) per 1x128 token block or
 // 128x128 weight block ("DeepGEMM teardown (FP8 GEMM)", sections 2.2 and 5.2).
@@ -40,14 +39,6 @@ __device__ __forceinline__ void load8(const void* x, int x_bf16, long long off, 
   }
 }
 
-// One warp per (row, kQ4Unroll x 256-element segments), grid-stride.  A
-// lane's kQ4Unroll 16-byte loads are all issued before any arithmetic and are
-// kept as raw words (bf16 pairs decode with a shift / mask when used), so a
-// warp holds 4 KB of loads in flight at 64 registers a thread (memory-level
-// parallelism: the kernel streams at HBM rate only with that much in flight).
-// Rows in [M, Mpad) (the 128-row padding of the scale tensor) get zero
-// scales, no codes.
-constexpr int kQ4Unroll = 8;
 static int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -82,79 +73,167 @@ __device__ __forceinline__ float raw8_at(const Raw8<kBf16>& r, int i) {
 
 // Two-level FP4 tensor scale 2^e: the smallest e with amax <= 6 * 448 * 2^e
 // (0 for a zero tensor), decided with exact double comparisons.
+// With 2688 = 21 * 2^7: amax <= 2688 * 2^e  <=>  amax * 2^-(e+7) <= 21, and the
+// scaled value stays near 21, a normal fp32 number, so ldexpf is exact.
 __device__ __forceinline__ int two_level_exp(float amax) {
   if (!(amax > 0.0f)) return 0;
   int e = ilogbf(amax) - 11;  // 2688 lies in [2^11, 2^12): at most a step or two off
-  while ((double)amax > ldexp(2688.0, e)) ++e;
-  while ((double)amax <= ldexp(2688.0, e - 1)) --e;
+  while (ldexpf(amax, -(e + 7)) > 21.0f) ++e;
+  while (ldexpf(amax, -(e + 6)) <= 21.0f) --e;  // amax <= 2688 * 2^(e-1)
   return e;
 }
 
+// (s, RN(1/s)) of every e4m3 scale code, one table per CTA in shared memory
+// (codes 0x7F / 0xFF are NaN and never produced by the saturating scale
+// conversion; code 0 gives s = 0, whose groups are all zero codes).
+__device__ __forceinline__ void fill_scale_table(float2* tab) {
+  for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+    const float s = e4m3_to_f32((uint32_t)c);
+    tab[c] = make_float2(s, __frcp_rn(s));
+  }
+}
+
+// FP4 quantization of one 16-element group held as eight fp32 pairs (exact
+// values of the input): scale code e4m3(RN(amax / 6)), codes E2M1 RNE of
+// RN(x / s) (all +0 when s == 0), element i in nibble i of the result.
+//
+// The quotient is quot_rn's one-correction form on pairs (packed fp32x2
+// multiply-add): p = RN(x r), rem = x - p s (exact), q = RN(p + r rem).  The
+// remainder is rounded downward: its value is exact either way, but an exact
+// zero then comes out as -0, so that q keeps the sign of a -0 input (the
+// zero remainder of +0 gives -0 * r + 0 = +0), with no copysign per element.
+// kBf16Amax: amax is a bf16 value and RN(amax / 6) is quot_rn's form (checked
+// exhaustively on the GPU); otherwise IEEE division.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {  // three-input max (sm_100 family)
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+template <bool kBf16Amax>
+__device__ __forceinline__ uint64_t q4_group16_x2(const float2 (&x)[8], const float2* tab, uint32_t& sc) {
+  // |x| max as a tree of three-input maxes (depth 3, not a chain of 8)
+  float m[6];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) {
+    const int a = 3 * i, b = 3 * i + 1, c = 3 * i + 2;
+    m[i] = fmax3(fabsf(a % 2 ? x[a / 2].y : x[a / 2].x), fabsf(b % 2 ? x[b / 2].y : x[b / 2].x),
+                 fabsf(c % 2 ? x[c / 2].y : x[c / 2].x));
+  }
+  m[5] = fabsf(x[7].y);
+  const float amax = fmax3(fmax3(m[0], m[1], m[2]), m[3], fmaxf(m[4], m[5]));
+  float a6;
+  if constexpr (kBf16Amax) {
+    const float r6 = __frcp_rn(6.0f);
+    const float p = amax * r6;
+    a6 = fmaf(fmaf(-p, 6.0f, amax), r6, p);  // amax >= 0: no sign of zero to keep
+  } else {
+    a6 = __fdiv_rn(amax, 6.0f);
+  }
+  sc = f32_to_e4m3(a6);
+  const float2 sr = tab[sc];
+  const float2 r2 = make_float2(sr.y, sr.y), ns2 = make_float2(-sr.x, -sr.x);
+  float q[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 p = __fmul2_rn(x[i], r2);
+    const float2 rem = __ffma2_rd(p, ns2, x[i]);
+    const float2 qq = __ffma2_rn(rem, r2, p);
+    q[2 * i] = qq.x;
+    q[2 * i + 1] = qq.y;
+  }
+  const float(&lo)[8] = *reinterpret_cast<const float(*)[8]>(&q[0]);
+  const float(&hi)[8] = *reinterpret_cast<const float(*)[8]>(&q[8]);
+  if (sr.x == 0.0f) return 0ull;  // zero group: all codes +0
+  return (uint64_t)f32x8_to_e2m1x8(lo) | ((uint64_t)f32x8_to_e2m1x8(hi) << 32);
+}
+
+// One lane per 16-element group: a warp covers 512 consecutive elements of a
+// row per segment and kQ4Seg segments per work item, every load of the item
+// issued before any arithmetic (4 KB in flight per warp for bf16 input).
+// Codes: 8 bytes per lane (a warp's 256 bytes contiguous); scales: one byte
+// per lane at its place in the MMA scale layout.  Rows in [M, Mpad) (the
+// 128-row padding of the scale tensor) get zero scales, no codes.
+//
 // kScaled: two-level FP4, the input divided by the tensor scale 2^e first
 // (exact: a multiply by an fp32 power of two, or ldexpf where 2^-e is not an
 // fp32 normal), e derived from *tensor_amax; CTA 0 stores 2^e.
+constexpr int kQ4Seg = 4;
 template <bool kBf16, bool kScaled>
-__global__ void __launch_bounds__(256) q4_quantize_kernel(const void* __restrict__ x, long long M, long long Mpad,
+__global__ void __launch_bounds__(256, kBf16 ? 3 : 2) q4_quantize_kernel(const void* __restrict__ x, long long M, long long Mpad,
                                                           long long K, long long ldx,
                                                           const int* __restrict__ gather,
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                           const float* __restrict__ tensor_amax,
                                                           float* __restrict__ tensor_scale) {
-  griddep_wait();  // inputs may come from the kernel just before on the stream
+  __shared__ float2 tab[256];
+  __shared__ int e2_s;
+  fill_scale_table(tab);  // before the dependency wait: touches no global memory
+  griddep_wait();         // inputs may come from the kernel just before on the stream
   griddep_launch_dependents();
+  if (kScaled && threadIdx.x == 0) {
+    e2_s = two_level_exp(__ldg(tensor_amax));  // once per CTA
+    if (blockIdx.x == 0) *tensor_scale = ldexpf(1.0f, e2_s);
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const float r6 = __frcp_rn(6.0f);
   int e2 = 0;
   float down = 1.0f;
   bool fast = true;
   if constexpr (kScaled) {
-    e2 = two_level_exp(__ldg(tensor_amax));
+    e2 = e2_s;
     fast = e2 >= -126 && e2 <= 126;
     down = fast ? ldexpf(1.0f, -e2) : 1.0f;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = (float)ldexp(1.0, e2);
   }
-  auto in = [&](float v) { return kScaled ? (fast ? v * down : ldexpf(v, -e2)) : v; };
-  const long long nblk = (K + 256 * kQ4Unroll - 1) / (256 * kQ4Unroll);
-  const long long total = Mpad * nblk;
+  constexpr int NW = kBf16 ? 8 : 16;  // 32-bit words per group
+  const long long nseg = (K + 512 * kQ4Seg - 1) / (512 * kQ4Seg);
+  const long long total = Mpad * nseg;
   const long long kchunks = K / 64;
   for (long long w = (long long)blockIdx.x * 8 + threadIdx.x / 32; w < total; w += (long long)gridDim.x * 8) {
-    const long long row = w / nblk, blk = w % nblk;
+    const long long row = w / nseg, seg = w % nseg;
     long long src = row < M ? row : -1;
     if (src >= 0 && gather) src = gather[row];
-    Raw8<kBf16> raw[kQ4Unroll];
+    uint32_t raw[kQ4Seg][NW];
 #pragma unroll
-    for (int u = 0; u < kQ4Unroll; ++u) {
-      const long long k0 = (blk * kQ4Unroll + u) * 256 + lane * 8;
+    for (int u = 0; u < kQ4Seg; ++u) {
+      const long long k0 = ((seg * kQ4Seg + u) * 32 + lane) * 16;
 #pragma unroll
-      for (int i = 0; i < (kBf16 ? 4 : 8); ++i) raw[u].w[i] = 0u;
-      if (k0 < K && src >= 0) load_raw8<kBf16>(x, src * ldx + k0, raw[u]);
+      for (int i = 0; i < NW; ++i) raw[u][i] = 0u;
+      if (k0 < K && src >= 0) {
+        const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(x) +
+                                                        (src * ldx + k0) * (kBf16 ? 2 : 4));
+#pragma unroll
+        for (int j = 0; j < NW / 4; ++j) {
+          const uint4 v = __ldg(p + j);
+          raw[u][4 * j] = v.x;
+          raw[u][4 * j + 1] = v.y;
+          raw[u][4 * j + 2] = v.z;
+          raw[u][4 * j + 3] = v.w;
+        }
+      }
     }
 #pragma unroll
-    for (int u = 0; u < kQ4Unroll; ++u) {
-      const long long k0 = (blk * kQ4Unroll + u) * 256 + lane * 8;
-      const bool active = k0 < K;
-      float amax = 0.0f;
+    for (int u = 0; u < kQ4Seg; ++u) {
+      const long long g = (seg * kQ4Seg + u) * 32 + lane;  // group index within the row
+      const long long k0 = g * 16;
+      if (k0 >= K) continue;
+      float2 v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(in(raw8_at<kBf16>(raw[u], i))));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      // bf16 amax: the one-correction quotient is RN(amax / 6) (6 is an e4m3
-      // value, so the exhaustive GPU tests cover every case); fp32: IEEE divide
-      const uint32_t s_code = f32_to_e4m3(kBf16 ? quot_rn(amax, 6.0f, r6) : __fdiv_rn(amax, 6.0f));
-      const float s = e4m3_to_f32(s_code);
-      const float rs = __frcp_rn(s);
-      float q[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = quot_rn(in(raw8_at<kBf16>(raw[u], i)), s, rs);
-      const uint32_t word = (s == 0.0f) ? 0u : f32x8_to_e2m1x8(q);  // zero group: all codes +0
-      if (active && row < M) *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + k0 / 2) = word;
-      const uint32_t b1 = __shfl_down_sync(0xffffffffu, s_code, 2);
-      const uint32_t b2 = __shfl_down_sync(0xffffffffu, s_code, 4);
-      const uint32_t b3 = __shfl_down_sync(0xffffffffu, s_code, 6);
-      if (active && (lane & 7) == 0) {
-        const long long chunk = k0 / 64;
-        const long long off = ((row / 128) * kchunks + chunk) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4;
-        *reinterpret_cast<uint32_t*>(sf + off) = s_code | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      for (int i = 0; i < 8; ++i) {
+        if constexpr (kBf16)
+          v[i] = make_float2(__uint_as_float(raw[u][i] << 16), __uint_as_float(raw[u][i] & 0xFFFF0000u));
+        else
+          v[i] = make_float2(__uint_as_float(raw[u][2 * i]), __uint_as_float(raw[u][2 * i + 1]));
+        if constexpr (kScaled) {
+          if (fast) v[i] = __fmul2_rn(v[i], make_float2(down, down));
+          else v[i] = make_float2(ldexpf(v[i].x, -e2), ldexpf(v[i].y, -e2));
+        }
       }
+      uint32_t sc;
+      const uint64_t cw = q4_group16_x2<kBf16>(v, tab, sc);
+      if (row < M) *reinterpret_cast<uint2*>(codes + row * (K / 2) + k0 / 2) = make_uint2((uint32_t)cw, (uint32_t)(cw >> 32));
+      const long long off = ((row / 128) * kchunks + g / 4) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + g % 4;
+      sf[off] = (uint8_t)sc;  // padding rows: an all-zero group, scale code 0
     }
   }
 }
@@ -425,7 +504,7 @@ cudaError_t launch_q4_quantize(const void* x, int x_bf16, long long M, long long
                                const int* gather, uint8_t* codes, uint8_t* sf, cudaStream_t stream,
                                const float* tensor_amax, float* tensor_scale) {
   const long long Mpad = (M + 127) / 128 * 128;
-  const long long warps = Mpad * ((K + 256 * kQ4Unroll - 1) / (256 * kQ4Unroll));
+  const long long warps = Mpad * ((K + 512 * kQ4Seg - 1) / (512 * kQ4Seg));
   long long blocks = (warps + 7) / 8;
   const long long cap = (long long)sm_count() * 16;
   if (blocks > cap) blocks = cap;
@@ -481,29 +560,36 @@ namespace bsk {
 // ---------------------------------------------------------------------------
 // Fused FP4 quantization + low-rank left factor for bf16 rows.
 //
-// One CTA owns 32 rows and streams them through shared memory in K chunks of
-// 256 (3-stage cp.async ring: 16 KB of X + 16 KB of A^T per stage, ~104 KB per
-// CTA so two CTAs share an SM).  Each 16-byte chunk j of row r is stored at
+// One CTA of 8 R threads owns R = 16 rows and streams them through shared
+// memory in K chunks of 256 (2-stage cp.async ring: 8 KB of X + 16 KB of A^T
+// per stage, ~50 KB per CTA so four CTAs share an SM and all 512 CTAs of an
+// 8192-row matrix are resident at once: each does half the work of a 32-row
+// CTA, with as many warps per SM).  Each 16-byte chunk j of row r is stored at
 // chunk position j ^ (r % 8).  Per stage:
-//   - quantization: thread t owns row t % 32 and the 32-element piece t / 32
-//     of the chunk (two groups: half of a 32-bit word of the MMA scale layout,
+//   - quantization: thread t owns row t % R and the 32-element piece t / R of
+//     the chunk (two groups: half of a 32-bit word of the MMA scale layout,
 //     written as 16 bits, and 16 bytes of codes); the row swizzle keeps the
 //     lanes of a warp on distinct banks;
-//   - low rank: warp w multiplies rows 16 (w % 2) .. +16 by A over K quarter
-//     w / 2 of the chunk with ldmatrix + mma.sync m16n8k16 (bf16 -> fp32); the
+//   - low rank: warp w multiplies rows 16 (w % RG) .. +16 by A over K quarter
+//     w / RG of the chunk with ldmatrix + mma.sync m16n8k16 (bf16 -> fp32); the
 //     four K quarters are summed through shared memory at the end and T is
 //     written as bf16 hi | lo.
 // X is read from HBM once for both results.
 // ---------------------------------------------------------------------------
 namespace fq {
-constexpr int R = 32;          // rows per CTA
+constexpr int R = 16;          // rows per CTA
+constexpr int NT = 8 * R;      // threads: eight 32-element pieces of a K chunk per row
 constexpr int KC = 256;        // K per stage
-constexpr int S = 3;           // stages
-constexpr int XB = R * KC * 2;       // 16 KB
+constexpr int S = 2;           // stages
+constexpr int XB = R * KC * 2;       // 8 KB
 constexpr int AB = 32 * KC * 2;      // 16 KB
+constexpr int RG = R / 16;           // 16-row groups of the low-rank MMA; each has 4 K-quarter warps
+static_assert(NT / 32 == 4 * RG, "four K quarters per row group");
 constexpr int STAGE = XB + AB;
-constexpr int RED = 4 * R * 32 * 4;  // [4 K quarters][32 rows][32] fp32
-constexpr int SMEM = S * STAGE + RED;
+constexpr int RED = 4 * R * 32 * 4;  // [4 K quarters][R rows][32] fp32, in the stage buffers after the loop
+constexpr int TAB = 256 * 8;         // (s, 1/s) of every e4m3 scale code
+constexpr int SMEM = S * STAGE + TAB;
+static_assert(RED <= S * STAGE, "reduction buffer reuses the stages");
 }  // namespace fq
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, bool valid) {
@@ -525,49 +611,51 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(row * (fq::KC * 2) + ((chunk ^ (row & 7)) * 16));
 }
 
-__global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
+__global__ void __launch_bounds__(fq::NT, 4) q4_lowrank_fused_kernel(
     const __nv_bfloat16* __restrict__ x, long long M, long long Mpad, long long K, long long ldx,
     const int* __restrict__ gather, const __nv_bfloat16* __restrict__ at, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ sf, __nv_bfloat16* __restrict__ t_out) {
   extern __shared__ __align__(128) uint8_t fsm[];
-  griddep_wait();  // inputs may come from the kernel just before on the stream
+  float2* tab = reinterpret_cast<float2*>(fsm + fq::S * fq::STAGE);
+  fill_scale_table(tab);  // read after the first stage barrier below
+  griddep_wait();         // inputs may come from the kernel just before on the stream
   griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const float r6 = __frcp_rn(6.0f);
   const long long r0 = (long long)blockIdx.x * fq::R;
   const int nchunks = (int)(K / fq::KC);
   const uint32_t sbase = smem_u32(fsm);
 
-  // loader: X chunk = 32 rows x 32 chunks of 16 B = 1024 copies (4 per thread);
-  // A^T chunk = 32 rows x 32 chunks = 1024 copies (4 per thread)
-  long long my_src[4];
+  // loader: X chunk = R rows x 32 chunks of 16 B (4 copies per thread);
+  // A^T chunk = 32 rows x 32 chunks (1024 / NT copies per thread)
+  constexpr int XC = fq::R * 32 / fq::NT, AC = 32 * 32 / fq::NT;
+  long long my_src[XC];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const long long row = r0 + (tid + i * 256) / 32;
+  for (int i = 0; i < XC; ++i) {
+    const long long row = r0 + (tid + i * fq::NT) / 32;
     my_src[i] = row >= M ? -1 : (gather ? (long long)gather[row] : row);
   }
   auto load_stage = [&](int c, int st) {
     const uint32_t xs = sbase + st * fq::STAGE, as = xs + fq::XB;
     const long long k0 = (long long)c * fq::KC;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int idx = tid + i * 256, r = idx / 32, ch = idx % 32;
+    for (int i = 0; i < XC; ++i) {
+      const int idx = tid + i * fq::NT, r = idx / 32, ch = idx % 32;
       const long long sr = my_src[i];
       const __nv_bfloat16* g = x + (sr >= 0 ? sr * ldx + k0 + ch * 8 : 0);
       cp_async16(xs + swz(r, ch), g, sr >= 0);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int idx = tid + i * 256, r = idx / 32, ch = idx % 32;
+    for (int i = 0; i < AC; ++i) {
+      const int idx = tid + i * fq::NT, r = idx / 32, ch = idx % 32;
       cp_async16(as + swz(r, ch), at + (long long)r * K + k0 + ch * 8, true);
     }
   };
 
   // quantization role: row qrow, 32-element piece qp (chunks 4 qp .. 4 qp + 3)
-  const int qrow = tid % 32, qp = tid / 32;
+  const int qrow = tid % fq::R, qp = tid / fq::R;
   const long long grow = r0 + qrow;
   // low-rank role of this warp: rows 16 rg .. +16, K quarter kq (64 elements)
-  const int rg = warp % 2, kq = warp / 2;
+  const int rg = warp % fq::RG, kq = warp / fq::RG;
   float d[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -588,38 +676,29 @@ __global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
 
     // ---- quantize 32 elements (2 groups) of row qrow
     {
-      float v[32];
+      uint32_t raw[16];
+      const uint8_t* xg = fsm + st * fq::STAGE;  // generic view of this stage's X tile
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint4 raw;
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
-                     : "r"(xs + swz(qrow, qp * 4 + j)));
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[8 * j + 2 * i] = __uint_as_float(w4[i] << 16);
-          v[8 * j + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
-        }
+        const uint4 u = *reinterpret_cast<const uint4*>(xg + swz(qrow, qp * 4 + j));
+        raw[4 * j] = u.x;
+        raw[4 * j + 1] = u.y;
+        raw[4 * j + 2] = u.z;
+        raw[4 * j + 3] = u.w;
       }
       uint32_t sfh = 0;
       uint32_t cw[4];
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
-        float amax = 0.0f;
+        float2 v[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[16 * g + i]));
-        const uint32_t sc = f32_to_e4m3(quot_rn(amax, 6.0f, r6));  // RN(amax / 6) for bf16 amax
-        const float sv = e4m3_to_f32(sc);
-        const float rs = __frcp_rn(sv);
+        for (int i = 0; i < 8; ++i)
+          v[i] = make_float2(__uint_as_float(raw[8 * g + i] << 16), __uint_as_float(raw[8 * g + i] & 0xFFFF0000u));
+        uint32_t sc;
+        const uint64_t c2 = q4_group16_x2<true>(v, tab, sc);
         sfh |= sc << (8 * g);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float q[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) q[i] = quot_rn(v[16 * g + 8 * h + i], sv, rs);
-          cw[2 * g + h] = (sv == 0.0f) ? 0u : f32x8_to_e2m1x8(q);  // zero group: all codes +0
-        }
+        cw[2 * g] = (uint32_t)c2;
+        cw[2 * g + 1] = (uint32_t)(c2 >> 32);
       }
       // two scale bytes = half of the 64-element chunk's scale word
       const long long kp = (long long)c * fq::KC + qp * 32;  // first element of the piece
@@ -664,8 +743,10 @@ __global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
   }
   cp_async_wait<0>();
 
-  // ---- reduce the four K quarters and write T as bf16 hi | lo
-  float* red = reinterpret_cast<float*>(fsm + fq::S * fq::STAGE);  // [4][32][32]
+  // ---- reduce the four K quarters and write T as bf16 hi | lo (the last
+  // loop iteration ended with a barrier and no copy is in flight, so the
+  // stage buffers are free)
+  float* red = reinterpret_cast<float*>(fsm);  // [4][32][32]
   {
     const int g = lane / 4, tq = lane % 4;
     float* rb = red + (kq * fq::R + rg * 16) * 32;
@@ -678,7 +759,7 @@ __global__ void __launch_bounds__(256, 2) q4_lowrank_fused_kernel(
     }
   }
   __syncthreads();
-  for (int o = tid; o < fq::R * 32; o += 256) {
+  for (int o = tid; o < fq::R * 32; o += fq::NT) {
     const int r = o / 32, j = o % 32;
     const long long row = r0 + r;
     if (row >= M) continue;
@@ -700,7 +781,7 @@ cudaError_t launch_q4_lowrank_fused(const void* x, long long M, long long K, lon
   cudaError_t e = cudaFuncSetAttribute(q4_lowrank_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        fq::SMEM);
   if (e != cudaSuccess) return e;
-  return launch_kernel(q4_lowrank_fused_kernel, (unsigned)blocks, 256, (size_t)fq::SMEM, stream, 1,
+  return launch_kernel(q4_lowrank_fused_kernel, (unsigned)blocks, fq::NT, (size_t)fq::SMEM, stream, 1,
                        reinterpret_cast<const __nv_bfloat16*>(x), M, Mpad, K, ldx, gather,
                        reinterpret_cast<const __nv_bfloat16*>(lora_a_t), codes, sf,
                        reinterpret_cast<__nv_bfloat16*>(lora_t));
