@@ -391,6 +391,88 @@ class Fp4Decode(Fp8Sweep):
         return time.perf_counter() - t0, 2.0 * rows * cols * self.K
 
 
+class DecodeChain(Fp8Sweep):
+    """Decode GEMMs back to back: one activation quantization of M = 16 tokens,
+    then G = 8 GEMMs of [16 x 4096] by different [7168 x 4096] weight sets (as
+    the projections of a decode step that read the same activation), each a
+    programmatic dependent launch with weights_ready, so its weight stream
+    starts under the tail of the GEMM before it.  fmt "fp8": block-scaled FP8
+    (swap-AB stream-K kernel); "fp4": the FP4 decode kernel.  Roofline: the G
+    GEMMs' algorithmic bytes over the time from the first GEMM's start to the
+    last one's end (the quantizer excluded)."""
+
+    G = 8
+
+    def __init__(self, fmt):
+        super().__init__(16)
+        self.fmt = fmt
+        G = self.G
+        self.name = f"{fmt}_decode_chain_{G}x_M16_N7168_K4096"
+        self.metric = f"{fmt.upper()} decode GEMM chain TFLOPS ({G} GEMMs, M=16, N=7168, K=4096)"
+        self.flops = G * 2.0 * self.M * self.N * self.K
+        N, K, M = self.N, self.K, self.M
+        if fmt == "fp4":
+            self.dtype = "e2m1 x e2m1 (e4m3 group-16 scales), fp32 accumulate, bf16 out"
+            self.kernel_src = "fp8_quantized_gemm_q4_gb300/csrc/gemm_fp4_decode.cu"
+            one = N * K // 2 + N * K // 16 + M * K // 2 + 128 * K // 16 + M * N * 2
+        else:
+            one = self.gemm_bytes
+        self.gemm_bytes = G * one
+
+    def setup(self, dev):
+        import torch
+        import fp8_quantized_gemm_q4_gb300 as bs
+        import workloads
+        d = self.host_inputs()
+        self.h = d
+        self.x = d["x"].to(dev)
+        M, N, K = self.M, self.N, self.K
+        self.ws_list = []
+        for g in range(self.G):
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(workloads.SEED_BASE + 7919 * (g + 1))
+            w = (torch.randn(N, K, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+            if self.fmt == "fp4":
+                wq, wsf, _ = bs.q4_quantize(w)
+            else:
+                wq, wsf = bs.q8_quantize(w, mode=bs.Q8_BLOCK)
+            self.ws_list.append((wq, wsf))
+            del w
+        if self.fmt == "fp4":
+            self.xq = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+            self.xs = torch.empty(bs.sf_bytes(M, K), dtype=torch.uint8, device=dev)
+        else:
+            self.xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+            self.xs = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        self.outs = torch.empty((self.G, M, N), dtype=torch.bfloat16, device=dev)
+        self.out = self.outs[-1]
+        self.launches_per_step = 1 + self.G
+        self.bytes_in = self.x.numel() * 2
+        self.bytes_out = self.out.numel() * 2
+
+    def step(self, x=None, gemm_events=None):
+        import fp8_quantized_gemm_q4_gb300 as bs
+        x = self.x if x is None else x
+        if self.fmt == "fp4":
+            bs.q4_quantize(x, out=(self.xq, self.xs, None))
+        else:
+            bs.q8_quantize(x, out=(self.xq, self.xs))
+        if gemm_events:
+            gemm_events[0].record()
+        for g, (wq, wsf) in enumerate(self.ws_list):
+            if self.fmt == "fp4":
+                bs.gemm_fp4(self.xq, self.xs, wq, wsf, self.K, out=self.outs[g], weights_ready=True)
+            else:
+                bs.gemm_fp8(self.xq, self.xs, wq, wsf, out=self.outs[g], weights_ready=True)
+        if gemm_events:
+            gemm_events[1].record()
+        return self.out
+
+    def roofline(self, gemm_ms, peaks, source):
+        kern = ("fp4_decode_kernel" if self.fmt == "fp4" else "fp8_gemm_kernel") + f" x{self.G} (chain)"
+        return hbm_roofline(kern, self.gemm_bytes, gemm_ms, peaks, source)
+
+
 class DenseTwoLevel(DenseLowRank):
     """Dense W4A4 8192^3 with two-level FP4 operands (power-of-two tensor
     scale above the e4m3 group scales; weights N(0, 0.02)), bf16 out, no
@@ -769,6 +851,8 @@ WORKLOADS = {
     "moe_small": lambda: MoEWorkload(large=False),
     "moe_large": lambda: MoEWorkload(large=True),
     "moe_fp8_small": lambda: Fp8MoEWorkload(large=False),
+    "fp8_decode_chain": lambda: DecodeChain("fp8"),
+    "fp4_decode_chain": lambda: DecodeChain("fp4"),
     "q4_quantize": lambda: QuantWorkload("q4"),
     "q8_quantize": lambda: QuantWorkload("q8"),
 }
@@ -909,7 +993,7 @@ def check_device_status():
 # % of GB300 dense peak; MoE layer us"), timed in the same run as the dense
 # headline and reported beside it.
 EXTRAS = ("moe_small", "moe_large", "moe_fp8_small", "fp8_m16", "fp8_m4096", "fp8_w8a8_m16", "fp8_w8a8_m4096",
-          "fp4_decode_m16", "q4_quantize", "q8_quantize")
+          "fp4_decode_m16", "fp8_decode_chain", "fp4_decode_chain", "q4_quantize", "q8_quantize")
 
 
 def run_extra(args, name, world, dev, peaks, source):

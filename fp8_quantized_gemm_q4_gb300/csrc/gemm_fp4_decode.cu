@@ -50,9 +50,12 @@ struct Cfg {
   static constexpr int kOffSfx = kOffSfw + kMmas * 512;
   static constexpr int kStageBytes = round_up(kOffSfx + kMmas * 512, kAlign);
   static constexpr int kTx = kOffSfx + kMmas * 512;   // bytes one stage's copies deliver
+  // TN 16: a 5-stage ring (about 113 KB) and at most 85 registers a thread,
+  // so that two CTAs share an SM and a GEMM launched behind this one streams
+  // its first weight stages while this one finishes
+  static constexpr int kMax = TN == 16 ? 5 : kMaxStages;
   static constexpr int kStages =
-      (kSmemPerCta - kMisc - kAlign) / kStageBytes < kMaxStages ? (kSmemPerCta - kMisc - kAlign) / kStageBytes
-                                                                : kMaxStages;
+      (kSmemPerCta - kMisc - kAlign) / kStageBytes < kMax ? (kSmemPerCta - kMisc - kAlign) / kStageBytes : kMax;
   static constexpr int kSmem = kStages * kStageBytes + kMisc + kAlign;
   static constexpr int kSlots = 8;                     // accumulator slots (one per segment)
   static constexpr int kTmemAcc = 0;
@@ -89,7 +92,7 @@ struct Walk {
 __device__ __forceinline__ int sk_owner(long long u, long long U, int G) { return (int)(((u + 1) * G - 1) / U); }
 
 template <int TN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
     fp4_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const Fp4DecodeParams p) {
   using C = Cfg<TN>;
@@ -351,6 +354,9 @@ static cudaError_t launch_tn(const Fp4DecodeLaunch& L, cudaStream_t stream) {
   using C = Cfg<TN>;
   auto kern = fp4_decode_kernel<TN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  // all of the SM's unified memory as shared memory, so two decode CTAs fit
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmW, L.tmX, L.p);
 }

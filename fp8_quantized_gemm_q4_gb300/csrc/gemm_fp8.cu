@@ -57,6 +57,7 @@ constexpr int kMisc = 2048;
 constexpr int kMaxStages = 12;
 
 constexpr int KBC = 32;   // K blocks whose scales are staged together
+constexpr int kDecodeStages = 5;
 
 template <int TN>
 struct Cfg {
@@ -64,7 +65,11 @@ struct Cfg {
   // two staging buffers of [KBC][TN] activation scales + [KBC] weight scales
   static constexpr int kScaleBytes = round_up(2 * (KBC * TN + KBC) * 4, kAlign);
   static constexpr Fp8TileShape kShape{BM, TN, BK, kMisc + kScaleBytes + kAlign};
-  static constexpr int kStages = fp8_main_stages(kShape) < kMaxStages ? fp8_main_stages(kShape) : kMaxStages;
+  // M <= 16 (decode): a 5-stage ring (98 KB) and at most 85 registers a
+  // thread, so that two CTAs share an SM and a GEMM launched behind this one
+  // streams its first weight stages while this one finishes
+  static constexpr int kMax = TN == 16 ? kDecodeStages : kMaxStages;
+  static constexpr int kStages = fp8_main_stages(kShape) < kMax ? fp8_main_stages(kShape) : kMax;
   static constexpr int kSmem = kStages * kStageBytes + kScaleBytes + kMisc + kAlign;
   // partial slots: as many K blocks as tensor memory holds (up to 16), so
   // the tensor core can run that far ahead of the promotion warps
@@ -119,7 +124,7 @@ struct Walk {
 __device__ __forceinline__ int sk_owner(long long u, long long U, int G) { return (int)(((u + 1) * G - 1) / U); }
 
 template <int TN, bool kStreamK, bool kRowwise>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const Fp8Params p) {
   using C = Cfg<TN>;
@@ -465,7 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Small tiles fold G partial slots per round trip (wait all, load all,
       // one tcgen05.wait::ld, release all) so the latency of the hand-off is
       // paid once per G K blocks.
-      constexpr int G = NC <= 32 ? (64 / NC < 8 ? 64 / NC : 8) : 1;
+      constexpr int kFold = TN == 16 ? 16 : 64;   // registers for the folded slots (two CTAs per SM at TN 16)
+      constexpr int G = NC <= 32 ? (kFold / NC < 8 ? kFold / NC : 8) : 1;
       int kb = kc0;
       if constexpr (G > 1) {
         for (; kb + G <= kb_end; kb += G) {
@@ -568,6 +574,9 @@ static cudaError_t launch_tn(const Fp8Launch& L, cudaStream_t stream) {
   using C = Cfg<TN>;
   auto kern = fp8_gemm_kernel<TN, kStreamK, kRowwise>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  // all of the SM's unified memory as shared memory, so two decode CTAs fit
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmA, L.tmB, L.p);
 }
