@@ -825,22 +825,31 @@ __global__ void __launch_bounds__(256) fp4_gather_rows_kernel(const uint8_t* __r
     }
     const long long left = rows_out - (r0 + warp * 16);
     const int nrows = left < 16 ? (left > 0 ? (int)left : 0) : 16;
-    for (int i = 0; i < nrows; ++i) {
+    // two rows per pass: both rows' loads are in flight before either is stored
+    for (int i = 0; i < nrows; i += 2) {
+      const bool two = i + 1 < nrows;
       const long long row = r0 + warp * 16 + i;
-      const long long src = __shfl_sync(0xffffffffu, my_src, i);
-      const uint4* sp = reinterpret_cast<const uint4*>(codes_in + (src >= 0 ? src : 0) * (K / 2));
-      uint4* dp = reinterpret_cast<uint4*>(codes_out + row * (K / 2));
+      const long long src0 = __shfl_sync(0xffffffffu, my_src, i);
+      const long long src1 = __shfl_sync(0xffffffffu, my_src, two ? i + 1 : i);
+      const uint4* sp0 = reinterpret_cast<const uint4*>(codes_in + (src0 >= 0 ? src0 : 0) * (K / 2));
+      const uint4* sp1 = reinterpret_cast<const uint4*>(codes_in + (src1 >= 0 ? src1 : 0) * (K / 2));
+      uint4* dp0 = reinterpret_cast<uint4*>(codes_out + row * (K / 2));
+      uint4* dp1 = dp0 + kv;
       for (long long v0 = 0; v0 < kv; v0 += 32 * kGatherVec) {
-        uint4 buf[kGatherVec];
+        uint4 buf[2][kGatherVec];
 #pragma unroll
         for (int u = 0; u < kGatherVec; ++u) {
           const long long v = v0 + u * 32 + lane;
-          buf[u] = (src >= 0 && v < kv) ? __ldg(sp + v) : make_uint4(0, 0, 0, 0);
+          buf[0][u] = (src0 >= 0 && v < kv) ? __ldg(sp0 + v) : make_uint4(0, 0, 0, 0);
+          buf[1][u] = (two && src1 >= 0 && v < kv) ? __ldg(sp1 + v) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kGatherVec; ++u) {
           const long long v = v0 + u * 32 + lane;
-          if (v < kv) __stcs(dp + v, buf[u]);  // streaming: keep the source rows in L2
+          if (v < kv) {
+            __stcs(dp0 + v, buf[0][u]);  // streaming: keep the source rows in L2
+            if (two) __stcs(dp1 + v, buf[1][u]);
+          }
         }
       }
     }
@@ -902,22 +911,31 @@ __global__ void __launch_bounds__(256) fp8_gather_rows_kernel(const uint8_t* __r
     }
     const long long left = rows_out - (r0 + warp * 16);
     const int nrows = left < 16 ? (left > 0 ? (int)left : 0) : 16;
-    for (int i = 0; i < nrows; ++i) {
+    // two rows per pass: both rows' loads are in flight before either is stored
+    for (int i = 0; i < nrows; i += 2) {
+      const bool two = i + 1 < nrows;
       const long long row = r0 + warp * 16 + i;
-      const long long src = __shfl_sync(0xffffffffu, my_src, i);
-      const uint4* sp = reinterpret_cast<const uint4*>(codes_in + (src >= 0 ? src : 0) * K);
-      uint4* dp = reinterpret_cast<uint4*>(codes_out + row * K);
+      const long long src0 = __shfl_sync(0xffffffffu, my_src, i);
+      const long long src1 = __shfl_sync(0xffffffffu, my_src, two ? i + 1 : i);
+      const uint4* sp0 = reinterpret_cast<const uint4*>(codes_in + (src0 >= 0 ? src0 : 0) * K);
+      const uint4* sp1 = reinterpret_cast<const uint4*>(codes_in + (src1 >= 0 ? src1 : 0) * K);
+      uint4* dp0 = reinterpret_cast<uint4*>(codes_out + row * K);
+      uint4* dp1 = dp0 + kv;
       for (long long v0 = 0; v0 < kv; v0 += 32 * kGatherVec) {
-        uint4 buf[kGatherVec];
+        uint4 buf[2][kGatherVec];
 #pragma unroll
         for (int u = 0; u < kGatherVec; ++u) {
           const long long v = v0 + u * 32 + lane;
-          buf[u] = (src >= 0 && v < kv) ? __ldg(sp + v) : make_uint4(0, 0, 0, 0);
+          buf[0][u] = (src0 >= 0 && v < kv) ? __ldg(sp0 + v) : make_uint4(0, 0, 0, 0);
+          buf[1][u] = (two && src1 >= 0 && v < kv) ? __ldg(sp1 + v) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kGatherVec; ++u) {
           const long long v = v0 + u * 32 + lane;
-          if (v < kv) dp[v] = buf[u];
+          if (v < kv) {
+            dp0[v] = buf[0][u];
+            if (two) dp1[v] = buf[1][u];
+          }
         }
       }
     }
