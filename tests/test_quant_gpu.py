@@ -239,7 +239,7 @@ def test_q8_block_bit_exact(cuda_lib, N, K):
     assert np.array_equal(scales.cpu().numpy(), os_)
 
 
-def _q8_quotient_sweep(dtype, n_scales=512, seed=3):
+def _q8_quotient_sweep(dtype, n_scales=512, seed=3, lo_exp=-12):
     """1 x 128 blocks whose first element A is the block amax, so the block
     scale is s = fl32(A / 448), for a spread of A over the positive finite
     bf16 range; the other 127 elements take every bf16 value of magnitude in
@@ -252,9 +252,9 @@ def _q8_quotient_sweep(dtype, n_scales=512, seed=3):
     blocks = []
     for a in A.tolist():
         if dtype == torch.bfloat16:
-            vals = allbf[(allbf >= a * 2.0 ** -12) & (allbf <= a)]
+            vals = allbf[(allbf >= a * 2.0 ** lo_exp) & (allbf <= a)]
         else:
-            vals = a * torch.exp2(-12.0 * torch.rand(3000, generator=g))
+            vals = a * torch.exp2(lo_exp * torch.rand(3000, generator=g))
         vals = torch.cat([vals, -vals])
         n = (len(vals) + 126) // 127 * 127
         vals = torch.cat([vals, torch.zeros(n - len(vals))]).view(-1, 127)
@@ -274,6 +274,73 @@ def test_q8_token_quotient_sweep(cuda_lib, dtype):
     torch.cuda.synchronize()
     oc, os_ = oracle.q8_quantize(x, rows_per_block=1)
     assert np.array_equal(scales.cpu().numpy().T, os_)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_q8_token_small_quotient_sweep(cuda_lib, dtype):
+    """The same sweep down to quotients of 448 * 2^-20 (below half the
+    smallest e4m3 subnormal): every decision point of the e4m3 subnormal
+    range, under 64 scales."""
+    bs = cuda_lib
+    x = _q8_quotient_sweep(dtype, n_scales=64, seed=4, lo_exp=-20)
+    codes, scales = bs.q8_quantize(x.cuda(), mode=bs.Q8_TOKEN)
+    torch.cuda.synchronize()
+    oc, os_ = oracle.q8_quantize(x, rows_per_block=1)
+    assert np.array_equal(scales.cpu().numpy().T, os_)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+def _q8_midpoint_rows(n_scales=64, seed=5):
+    """fp32 blocks [A, x ...] whose x make x / s land on and within three fp32
+    ulps of every e4m3 decision point (midpoints between consecutive e4m3
+    values up to 448, normal and subnormal), both signs, s = fl32(A / 448)
+    for n_scales random A."""
+    g = np.random.default_rng(seed)
+    mags = np.unique(np.abs(oracle.e4m3_table()))
+    mags = mags[np.isfinite(mags) & (mags <= 448)]
+    mids = (mags[:-1] + mags[1:]) / 2
+    blocks = []
+    for _ in range(n_scales):
+        a = np.float32(g.uniform(0.5, 4.0) * 2.0 ** int(g.integers(-8, 9)))
+        sc = np.float32(np.float64(a) / 448.0)
+        xs = []
+        for m in mids:
+            x0 = np.float32(m * np.float64(sc))
+            up, dn = x0, x0
+            xs.append(x0)
+            for _ in range(3):
+                up = np.nextafter(up, np.float32(np.inf), dtype=np.float32)
+                dn = np.nextafter(dn, np.float32(0), dtype=np.float32)
+                xs += [up, dn]
+        xs = np.array([v for v in xs if 0 < v <= a], dtype=np.float32)
+        xs = np.concatenate([xs, -xs])
+        n = (len(xs) + 126) // 127 * 127
+        xs = np.concatenate([xs, np.zeros(n - len(xs), np.float32)]).reshape(-1, 127)
+        blocks.append(np.concatenate([np.full((xs.shape[0], 1), a, np.float32), xs], axis=1))
+    b = np.concatenate(blocks)
+    b = np.concatenate([b, np.zeros(((-b.shape[0]) % 32, 128), np.float32)])
+    return torch.from_numpy(b.reshape(-1, 4096))
+
+
+@pytest.mark.parametrize("mode", ["token", "row", "block"])
+def test_q8_decision_points(cuda_lib, mode):
+    """Quotients on and next to every e4m3 decision point (the cases the fast
+    quotient hands to IEEE division), for the token, row and block modes."""
+    bs = cuda_lib
+    x = _q8_midpoint_rows()
+    if mode == "token":
+        codes, scales = bs.q8_quantize(x.cuda(), mode=bs.Q8_TOKEN)
+        oc, os_ = oracle.q8_quantize(x, rows_per_block=1)
+        os_ = os_.T
+    elif mode == "block":
+        codes, scales = bs.q8_quantize(x.cuda(), mode=bs.Q8_BLOCK)
+        oc, os_ = oracle.q8_quantize(x, rows_per_block=128)
+    else:
+        codes, scales = bs.q8_quantize(x.cuda(), mode=bs.Q8_ROW)
+        oc, os_ = oracle.q8_quantize_rowwise(x)
+    torch.cuda.synchronize()
+    assert np.array_equal(scales.cpu().numpy(), os_)
     assert np.array_equal(codes.cpu().numpy(), oc)
 
 
