@@ -10,6 +10,10 @@ BS_ERR_TIMEOUT with the id of the wait that ran out, and the next call with
 the default limit computes the right result in the same context.  No fault,
 trap or hang is involved: every wait of the kernels is bounded.
 """
+import ctypes
+import os
+import subprocess
+
 import pytest
 import torch
 
@@ -50,4 +54,99 @@ def test_wait_runs_out_then_the_context_stays_usable(cuda_lib, kernel):
     yr, s = oracle.gemm_fp4(oa, osa, ob, osb, K)
     ok, ratio, rel = gemm_errors(y.cpu().numpy(), yr, s, False)
     assert ok, (ratio, rel)
+
+
+# wait sites of the FP8 and FP4-decode kernels.  (The grouped FP8 kernel
+# orders all its warps behind griddepcontrol.wait -- its tile table needs the
+# expert offsets first -- and afterwards hands off every 128-wide K block, so
+# none of its waits can be made to run past a limit without withholding a
+# producer; its timeout exits share the helpers exercised here.)
+SITES_FP8 = {50, 60, 61, 62, 63, 70, 71, 72}
+SITES_DECODE = {210, 220, 221, 230}
+
+HOLD_NS = 5_000_000      # upstream kernel's hold: 5 ms, far past the limit
+LIMIT_US = 10
+
+
+@pytest.fixture(scope="module")
+def pdl_hold(tmp_path_factory):
+    """hold() enqueues, on the current stream, tests/native/pdl_hold.cu's
+    kernel: it lets the next kernel start early (programmatic dependent
+    launch) and keeps the stream's previous grid alive for HOLD_NS.  The
+    library's kernels order their first reads of another kernel's data behind
+    griddepcontrol.wait, so the tensor-core and epilogue waits of a kernel
+    launched right behind the hold last the whole hold."""
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "native", "pdl_hold.cu")
+    so = str(tmp_path_factory.mktemp("pdl_hold") / "pdl_hold.so")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-shared",
+                    "-Xcompiler", "-fPIC", "-o", so, src], check=True)
+    lib = ctypes.CDLL(so)
+    lib.pdl_hold.restype = ctypes.c_int
+    lib.pdl_hold.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
+
+    def hold():
+        assert lib.pdl_hold(HOLD_NS, torch.cuda.current_stream().cuda_stream) == 0
+    return hold
+
+
+def _timeout_then_same_result(bs, hold, run, sites):
+    """run(opts, before) -> output tensor, calling before() right before the
+    library call (nothing else may be enqueued in between, or the early
+    start is lost).  A normal call; then one launched behind the hold with a
+    short wait limit, which must end by itself with BS_ERR_TIMEOUT at one of
+    `sites`; then a normal call that must reproduce the first result bit for
+    bit (stream-K counters back at zero, nothing left behind in the
+    context)."""
+    bs.clear_device_status()
+    ref = run({}, lambda: None).clone()
+    torch.cuda.synchronize()
+    assert bs.device_status()[0] == bs.BS_OK
+    run({"wait_timeout_us": LIMIT_US}, hold)
+    torch.cuda.synchronize()           # returns: the kernel ended by itself
+    st, detail = bs.device_status()
+    assert st == bs.BS_ERR_TIMEOUT, (st, hex(detail))
+    assert (detail >> 8) in sites, hex(detail)
+    bs.clear_device_status()
+    again = run({}, lambda: None)
+    torch.cuda.synchronize()
+    assert bs.device_status()[0] == bs.BS_OK
+    assert torch.equal(again, ref)
+
+
+@pytest.mark.parametrize("case", ["fp8_stream_k", "fp8_tiles", "w8a8", "fp8_prefill"])
+def test_wait_runs_out_fp8(cuda_lib, pdl_hold, case):
+    bs = cuda_lib
+    g = torch.Generator().manual_seed(3)
+    M = 256 if case == "fp8_prefill" else 16
+    K, N = 8192, 1024
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    rowwise = case == "w8a8"
+    mode = bs.Q8_ROW if rowwise else bs.Q8_TOKEN
+    xq, xs = bs.q8_quantize(x, mode=mode)
+    wq, ws = bs.q8_quantize(w, mode=bs.Q8_ROW if rowwise else bs.Q8_BLOCK)
+
+    def run(opts, before):
+        with bs.kernel_options(fp8_stream_k=2 if case == "fp8_tiles" else 1, **opts):
+            before()
+            return bs.gemm_fp8(xq, xs, wq, ws, rowwise=rowwise)
+
+    _timeout_then_same_result(bs, pdl_hold, run, SITES_FP8)
+
+
+def test_wait_runs_out_fp4_decode(cuda_lib, pdl_hold):
+    bs = cuda_lib
+    g = torch.Generator().manual_seed(4)
+    K, N = 8192, 1024
+    x = torch.randn(16, K, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    xq, xs, _ = bs.q4_quantize(x)
+    wq, ws, _ = bs.q4_quantize(w)
+
+    def run(opts, before):
+        with bs.kernel_options(fp4_decode=1, **opts):
+            before()
+            return bs.gemm_fp4(xq, xs, wq, ws, K)
+
+    _timeout_then_same_result(bs, pdl_hold, run, SITES_DECODE)
 
