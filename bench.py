@@ -413,12 +413,18 @@ class DecodeChain(Fp8Sweep):
 
     G = 8
 
-    def __init__(self, fmt):
+    def __init__(self, fmt, multi=False):
         super().__init__(16)
         self.fmt = fmt
+        self.multi = multi  # fp8: the G products in one bs_gemm_multi launch
         G = self.G
-        self.name = f"{fmt}_decode_chain_{G}x_M16_N7168_K4096"
-        self.metric = f"{fmt.upper()} decode GEMM chain TFLOPS ({G} GEMMs, M=16, N=7168, K=4096)"
+        if multi:
+            self.name = f"{fmt}_decode_multi_{G}x_M16_N7168_K4096"
+            self.metric = f"{fmt.upper()} decode multi-weight GEMM TFLOPS ({G} weight sets in one launch, " \
+                          f"M=16, N=7168, K=4096)"
+        else:
+            self.name = f"{fmt}_decode_chain_{G}x_M16_N7168_K4096"
+            self.metric = f"{fmt.upper()} decode GEMM chain TFLOPS ({G} GEMMs, M=16, N=7168, K=4096)"
         self.flops = G * 2.0 * self.M * self.N * self.K
         N, K, M = self.N, self.K, self.M
         if fmt == "fp4":
@@ -455,8 +461,9 @@ class DecodeChain(Fp8Sweep):
             self.xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
             self.xs = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
         self.outs = torch.empty((self.G, M, N), dtype=torch.bfloat16, device=dev)
+        self.out_list = [self.outs[g] for g in range(self.G)]
         self.out = self.outs[-1]
-        self.launches_per_step = 1 + self.G
+        self.launches_per_step = 2 if self.multi else 1 + self.G
         self.bytes_in = self.x.numel() * 2
         self.bytes_out = self.out.numel() * 2
 
@@ -469,6 +476,11 @@ class DecodeChain(Fp8Sweep):
             bs.q8_quantize(x, out=(self.xq, self.xs))
         if gemm_events:
             gemm_events[0].record()
+        if self.multi:
+            bs.gemm_fp8_multi(self.xq, self.xs, self.ws_list, outs=self.out_list, weights_ready=True)
+            if gemm_events:
+                gemm_events[1].record()
+            return self.out
         for g, (wq, wsf) in enumerate(self.ws_list):
             if self.fmt == "fp4":
                 bs.gemm_fp4(self.xq, self.xs, wq, wsf, self.K, out=self.outs[g], weights_ready=True)
@@ -479,7 +491,10 @@ class DecodeChain(Fp8Sweep):
         return self.out
 
     def roofline(self, gemm_ms, peaks, source):
-        kern = ("fp4_decode_kernel" if self.fmt == "fp4" else "fp8_gemm_kernel") + f" x{self.G} (chain)"
+        if self.multi:
+            kern = f"fp8_gemm_kernel (multi-weight: {self.G} products, one launch)"
+        else:
+            kern = ("fp4_decode_kernel" if self.fmt == "fp4" else "fp8_gemm_kernel") + f" x{self.G} (chain)"
         return hbm_roofline(kern, self.gemm_bytes, gemm_ms, peaks, source)
 
 
@@ -862,6 +877,7 @@ WORKLOADS = {
     "moe_large": lambda: MoEWorkload(large=True),
     "moe_fp8_small": lambda: Fp8MoEWorkload(large=False),
     "fp8_decode_chain": lambda: DecodeChain("fp8"),
+    "fp8_decode_multi": lambda: DecodeChain("fp8", multi=True),
     "fp4_decode_chain": lambda: DecodeChain("fp4"),
     "q4_quantize": lambda: QuantWorkload("q4"),
     "q8_quantize": lambda: QuantWorkload("q8"),
@@ -1003,7 +1019,7 @@ def check_device_status():
 # % of GB300 dense peak; MoE layer us"), timed in the same run as the dense
 # headline and reported beside it.
 EXTRAS = ("moe_small", "moe_large", "moe_fp8_small", "fp8_m16", "fp8_m4096", "fp8_w8a8_m16", "fp8_w8a8_m4096",
-          "fp4_decode_m16", "fp8_decode_chain", "fp4_decode_chain", "q4_quantize", "q8_quantize")
+          "fp4_decode_m16", "fp8_decode_chain", "fp8_decode_multi", "fp4_decode_chain", "q4_quantize", "q8_quantize")
 
 
 def run_extra(args, name, world, dev, peaks, source):

@@ -20,7 +20,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 
 __all__ = [
-    "load", "sf_bytes", "sf_offset", "q4_quantize", "tensor_amax", "q4_quantize_two_level", "fp4_gather_rows", "fp8_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8",
+    "load", "sf_bytes", "sf_offset", "q4_quantize", "tensor_amax", "q4_quantize_two_level", "fp4_gather_rows", "fp8_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8", "gemm_fp8_multi",
     "grouped_gemm_fp4", "grouped_gemm_fp4_swiglu_q4", "grouped_gemm_fp8", "moe_router_topk", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
     "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE", "EPI_ROWS", "kernel_options",
     "current_kernel_options", "FP4_ONE_CTA", "FP4_PAIR",
@@ -124,6 +124,10 @@ def load(path: str | None = None):
         lib.bs_gemm.argtypes = [ctypes.POINTER(GemmArgs), P]
         lib.bs_gemm_workspace_bytes.restype = SZ
         lib.bs_gemm_workspace_bytes.argtypes = [ctypes.POINTER(GemmArgs)]
+        lib.bs_gemm_multi.restype = I
+        lib.bs_gemm_multi.argtypes = [ctypes.POINTER(GemmArgs), I, P, P, P, P]
+        lib.bs_gemm_multi_workspace_bytes.restype = SZ
+        lib.bs_gemm_multi_workspace_bytes.argtypes = [ctypes.POINTER(GemmArgs), I]
         lib.bs_grouped_gemm.restype = I
         lib.bs_grouped_gemm.argtypes = [ctypes.POINTER(GemmArgs), I, P, P, I, P, P, P, I64, P]
         lib.bs_moe_rows_bound.restype = I64
@@ -351,6 +355,34 @@ def gemm_fp8(a, sa, b, sb, out_dtype=torch.bfloat16, out=None, num_sms: int = 0,
         g.workspace, g.workspace_bytes = ws.data_ptr(), ws.numel()
     _check(lib.bs_gemm(ctypes.byref(g), _stream(stream)))
     return out
+
+
+def gemm_fp8_multi(a, sa, weights, out_dtype=torch.bfloat16, outs=None, num_sms: int = 0,
+                   weights_ready: bool = False, stream=None):
+    """G block-scaled FP8 GEMMs that share the tokens ``a`` [M, K] (M <= 32,
+    TOKEN-mode scales ``sa``) in one launch: ``weights`` is a list of (codes
+    [N, K], BLOCK-mode scales) pairs, one per product; returns the G outputs
+    [M, N] (or fills ``outs``)."""
+    M, K = a.shape
+    G = len(weights)
+    N = weights[0][0].shape[0]
+    if outs is None:
+        outs = [torch.empty((M, N), dtype=out_dtype, device=a.device) for _ in range(G)]
+    b0, sb0 = weights[0]
+    g = _args(FMT_FP8, a, sa, b0, sb0, M, N, K, outs[0], num_sms=num_sms)
+    g.weights_ready = 1 if weights_ready else 0
+    arr = ctypes.c_void_p * max(G, 1)
+    bp = arr(*[w[0].data_ptr() for w in weights])
+    sp = arr(*[w[1].data_ptr() for w in weights])
+    op = arr(*[o.data_ptr() for o in outs])
+    lib = load()
+    nbytes = int(lib.bs_gemm_multi_workspace_bytes(ctypes.byref(g), G))
+    if nbytes:
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        ws = _workspace(a.device, s, nbytes)
+        g.workspace, g.workspace_bytes = ws.data_ptr(), ws.numel()
+    _check(lib.bs_gemm_multi(ctypes.byref(g), G, bp, sp, op, _stream(stream)))
+    return outs
 
 
 def grouped_gemm_fp4(a, sfa, b, sfb, K: int, N: int, E: int, offsets, counts, epilogue: int, out=None,

@@ -483,11 +483,11 @@ struct Fp8Plan {
   int maxc;
   size_t ws_bytes, counters_off;  // counters at the start, then the partials
 };
-static Fp8Plan fp8_plan(const bs_gemm_args* a, int sms) {
+static Fp8Plan fp8_plan(const bs_gemm_args* a, int sms, int products = 1) {
   Fp8Plan P;
   memset(&P, 0, sizeof P);
   P.tile_n = bsk::fp8_tile_n(a->M);
-  P.tiles = ((a->N + 127) / 128) * ((a->M + P.tile_n - 1) / P.tile_n);
+  P.tiles = (long long)products * ((a->N + 127) / 128) * ((a->M + P.tile_n - 1) / P.tile_n);
   const long long nkb = a->K / 128;
   P.grid = (int)(P.tiles < sms ? P.tiles : sms);
   P.stream_k = a->fp8_stream_k != 2 && P.tiles < sms && P.tiles <= (long long)(kStreamKCounterBytes / sizeof(int)) &&
@@ -572,6 +572,69 @@ static bs_status launch_fp4_decode(const bs_gemm_args* a, int sms, int* status, 
   return BS_OK;
 }
 
+// FP8 restrictions shared by bs_gemm and bs_gemm_multi (after check_common).
+static bs_status check_fp8(const bs_gemm_args* a) {
+  if (a->K % 128) return fail(BS_ERR_ALIGN, "FP8: K=%lld not a multiple of 128", (long long)a->K);
+  if (a->alpha != 1.0f || a->col_scale || a->lora_t || a->bias || a->a_tensor_scale || a->b_tensor_scale)
+    return fail(BS_ERR_UNSUPPORTED, "FP8 GEMM takes no alpha/col_scale/low-rank/bias/tensor scales");
+  if (reinterpret_cast<uintptr_t>(a->sfa) & 3 || reinterpret_cast<uintptr_t>(a->sfb) & 3)
+    return fail(BS_ERR_ALIGN, "FP8 scales must be 4-byte aligned");
+  return BS_OK;
+}
+
+// FP8 launch of G >= 1 products that share the token operand a->a: product g
+// multiplies by weights b[g] (scales sfb[g]) into out[g].  G == 1 is bs_gemm's
+// kernel; G > 1 the multi-weight variant (one tile list over all products).
+// Arguments already checked, M > 0.
+static bs_status launch_fp8(const bs_gemm_args* a, int G, const uint8_t* const* b, const float* const* sfb,
+                            void* const* out, int sms, int* status, cudaStream_t s) {
+  bsk::Fp8Launch L;
+  memset(&L, 0, sizeof L);
+  L.tile_n = bsk::fp8_tile_n(a->M);
+  // swap-AB: the weights [N, K] are the MMA's A operand, the tokens [M, K] its B
+  for (int g = 0; g < G; ++g) {
+    bs_status st = make_map(G == 1 ? &L.tmA : &L.tmA_g.m[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b[g],
+                            (uint64_t)a->K, (uint64_t)a->N, (uint64_t)a->K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BS_OK) return st;
+  }
+  bs_status st = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, (uint64_t)a->K, (uint64_t)a->M,
+                          (uint64_t)a->K, 128, (uint32_t)L.tile_n, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != BS_OK) return st;
+  L.p.sfa = static_cast<const float*>(a->sfa);
+  L.p.sfb = sfb[0];
+  L.p.M = (int)a->M;
+  L.p.N = (int)a->N;
+  L.p.K = (int)a->K;
+  L.p.out = out[0];
+  L.p.out_bf16 = a->out_dtype == BS_DTYPE_BF16;
+  L.p.ldo = a->ldo;
+  L.p.status = status;
+  L.p.G = G;
+  for (int g = 0; g < G; ++g) {
+    L.p.sfb_g[g] = sfb[g];
+    L.p.out_g[g] = out[g];
+  }
+  const Fp8Plan P = fp8_plan(a, sms, G);
+  L.p.wait_ns = wait_ns(a);
+  L.p.pre_b = a->weights_ready == 1 ? bsk::fp8_stages(P.tile_n) : 0;
+  L.p.rowwise = a->fp8_scaling == 2;
+  L.grid = P.grid;
+  if (P.stream_k && a->workspace) {
+    if (!aligned16(a->workspace)) return fail(BS_ERR_ALIGN, "workspace must be 16-byte aligned");
+    if (a->workspace_bytes < P.ws_bytes)
+      return fail(BS_ERR_INVALID, "workspace too small (%zu < %zu bytes)", a->workspace_bytes, P.ws_bytes);
+    L.p.stream_k = 1;
+    L.p.maxc = P.maxc;
+    L.p.counters = static_cast<int*>(a->workspace);
+    L.p.work = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + kStreamKCounterBytes);
+  } else {
+    L.grid = (int)(P.tiles < sms ? P.tiles : sms);  // one CTA per tile
+  }
+  cudaError_t e = bsk::launch_fp8_gemm(L, s);
+  if (e != cudaSuccess) return cuda_fail(e, G == 1 ? "FP8 GEMM launch" : "FP8 multi-weight GEMM launch");
+  return BS_OK;
+}
+
 bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
   bs_status st = check_common(a, false);
   if (st != BS_OK) return st;
@@ -620,52 +683,55 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     return launch_fp4(L, a, a->N, sms, s, pair_tiles, false);
   }
   if (a->fmt == BS_FMT_FP8) {
-    if (a->K % 128) return fail(BS_ERR_ALIGN, "FP8: K=%lld not a multiple of 128", (long long)a->K);
-    if (a->alpha != 1.0f || a->col_scale || a->lora_t || a->bias || a->a_tensor_scale || a->b_tensor_scale)
-      return fail(BS_ERR_UNSUPPORTED, "FP8 GEMM takes no alpha/col_scale/low-rank/bias/tensor scales");
-    if (reinterpret_cast<uintptr_t>(a->sfa) & 3 || reinterpret_cast<uintptr_t>(a->sfb) & 3)
-      return fail(BS_ERR_ALIGN, "FP8 scales must be 4-byte aligned");
+    st = check_fp8(a);
+    if (st != BS_OK) return st;
     if (a->M == 0) return BS_OK;
-    bsk::Fp8Launch L;
-    memset(&L, 0, sizeof L);
-    L.tile_n = bsk::fp8_tile_n(a->M);
-    // swap-AB: the weights [N, K] are the MMA's A operand, the tokens [M, K] its B
-    st = make_map(&L.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->b, (uint64_t)a->K, (uint64_t)a->N, (uint64_t)a->K,
-                  128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != BS_OK) return st;
-    st = make_map(&L.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, (uint64_t)a->K, (uint64_t)a->M, (uint64_t)a->K,
-                  128, (uint32_t)L.tile_n, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != BS_OK) return st;
-    L.p.sfa = static_cast<const float*>(a->sfa);
-    L.p.sfb = static_cast<const float*>(a->sfb);
-    L.p.M = (int)a->M;
-    L.p.N = (int)a->N;
-    L.p.K = (int)a->K;
-    L.p.out = a->out;
-    L.p.out_bf16 = a->out_dtype == BS_DTYPE_BF16;
-    L.p.ldo = a->ldo;
-    L.p.status = status;
-    const Fp8Plan P = fp8_plan(a, sms);
-    L.p.wait_ns = wait_ns(a);
-    L.p.pre_b = a->weights_ready == 1 ? bsk::fp8_stages(P.tile_n) : 0;
-    L.p.rowwise = a->fp8_scaling == 2;
-    L.grid = P.grid;
-    if (P.stream_k && a->workspace) {
-      if (!aligned16(a->workspace)) return fail(BS_ERR_ALIGN, "workspace must be 16-byte aligned");
-      if (a->workspace_bytes < P.ws_bytes)
-        return fail(BS_ERR_INVALID, "workspace too small (%zu < %zu bytes)", a->workspace_bytes, P.ws_bytes);
-      L.p.stream_k = 1;
-      L.p.maxc = P.maxc;
-      L.p.counters = static_cast<int*>(a->workspace);
-      L.p.work = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + kStreamKCounterBytes);
-    } else {
-      L.grid = (int)(P.tiles < sms ? P.tiles : sms);  // one CTA per tile
-    }
-    cudaError_t e = bsk::launch_fp8_gemm(L, s);
-    if (e != cudaSuccess) return cuda_fail(e, "FP8 GEMM launch");
-    return BS_OK;
+    const uint8_t* b = a->b;
+    const float* sfb = static_cast<const float*>(a->sfb);
+    void* out = a->out;
+    return launch_fp8(a, 1, &b, &sfb, &out, sms, status, s);
   }
   return fail(BS_ERR_INVALID, "fmt %d", a->fmt);
+}
+
+size_t bs_gemm_multi_workspace_bytes(const bs_gemm_args* a, int G) {
+  if (!a || G < 1 || G > bsk::kFp8MaxWeights || a->fmt != BS_FMT_FP8 || a->M <= 0 || a->M > 32 || a->N <= 0 ||
+      a->K < 128 || a->num_sms < 0)
+    return 0;
+  int sms = 0;
+  if (!device_info(nullptr, &sms)) return 0;
+  if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
+  const Fp8Plan P = fp8_plan(a, sms, G);
+  return P.stream_k ? P.ws_bytes : 0;
+}
+
+bs_status bs_gemm_multi(const bs_gemm_args* a, int G, const uint8_t* const* b, const float* const* sfb,
+                        void* const* out, bs_stream_t stream) {
+  if (!a) return fail(BS_ERR_INVALID, "null args");
+  if (G < 1 || G > bsk::kFp8MaxWeights) return fail(BS_ERR_INVALID, "G=%d outside [1, %d]", G, bsk::kFp8MaxWeights);
+  if (!b || !sfb || !out) return fail(BS_ERR_INVALID, "null weight / scale / output array");
+  if (a->fmt != BS_FMT_FP8) return fail(BS_ERR_UNSUPPORTED, "bs_gemm_multi: FP8 only");
+  if (a->fp8_scaling == 2) return fail(BS_ERR_UNSUPPORTED, "bs_gemm_multi: block scaling only (not W8A8)");
+  if (a->M > 32) return fail(BS_ERR_UNSUPPORTED, "bs_gemm_multi: M=%lld > 32 (decode shapes)", (long long)a->M);
+  bs_gemm_args one = *a;
+  one.b = b[0];
+  one.sfb = sfb[0];
+  one.out = out[0];
+  bs_status st = check_common(&one, false);
+  if (st != BS_OK) return st;
+  st = check_fp8(&one);
+  if (st != BS_OK) return st;
+  if (a->M == 0) return BS_OK;
+  for (int g = 0; g < G; ++g) {
+    if (!b[g] || !sfb[g] || !out[g]) return fail(BS_ERR_INVALID, "null operand of product %d", g);
+    if (!aligned16(b[g]) || !aligned16(sfb[g]) || !aligned16(out[g]))
+      return fail(BS_ERR_ALIGN, "operands of product %d must be 16-byte aligned", g);
+  }
+  int* status = nullptr;
+  int sms = 0;
+  if (!device_info(&status, &sms)) return fail(BS_ERR_CUDA, "no current device");
+  if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
+  return launch_fp8(a, G, b, sfb, out, sms, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // FP8 grouped GEMM (tokens as the MMA's M, see gemm_fp8_grouped.cu); args

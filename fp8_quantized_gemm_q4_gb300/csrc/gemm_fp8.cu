@@ -123,10 +123,36 @@ struct Walk {
 // CTA whose stream-K range holds unit u (ranges [c U / G, (c + 1) U / G)).
 __device__ __forceinline__ int sk_owner(long long u, long long U, int G) { return (int)(((u + 1) * G - 1) / U); }
 
-template <int TN, bool kStreamK, bool kRowwise>
+// The weight operand of the kernel: one tensor map, or one per product for the
+// multi-weight variant.
+template <bool kMulti>
+struct WArg {
+  using type = CUtensorMap;
+};
+template <>
+struct WArg<true> {
+  using type = Fp8WMaps;
+};
+
+// a[g] of a per-product parameter array, read with constant indices only
+template <typename T>
+__device__ __forceinline__ T pick(const T (&a)[kFp8MaxWeights], int g) {
+  T r = a[0];
+#pragma unroll
+  for (int i = 1; i < kFp8MaxWeights; ++i)
+    if (g == i) r = a[i];
+  return r;
+}
+
+// kMulti: G products Y_g = X W_g^T that share the token operand run as one
+// list of tiles, product-major (tile t is tile t mod T of product t / T, T =
+// tiles of one product), so a decode step's projections stream their weights
+// through one grid and pay its launch, first loads and fix-ups once.
+template <int TN, bool kStreamK, bool kRowwise, bool kMulti>
 __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
-    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    const Fp8Params p) {
+    fp8_gemm_kernel(const __grid_constant__ typename WArg<kMulti>::type tmW,
+                    const __grid_constant__ CUtensorMap tmX, const Fp8Params p) {
+  static_assert(!(kMulti && kRowwise), "the multi-weight kernel is block-scaled");
   using C = Cfg<TN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kAlign - 1) &
@@ -166,7 +192,11 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
       mbar_init(drain, 1);
       *abort_i = 0;
       fence_barrier_init();
-      prefetch_tmap(&tmW);
+      if constexpr (kMulti) {
+        for (int g = 0; g < p.G; ++g) prefetch_tmap(&tmW.m[g]);
+      } else {
+        prefetch_tmap(&tmW);
+      }
       prefetch_tmap(&tmX);
     }
     __syncwarp();
@@ -184,8 +214,17 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
 
   const int n_wblk = (p.N + BM - 1) / BM;
   const int n_tblk = (p.M + TN - 1) / TN;
-  const int total = n_wblk * n_tblk;
+  const int per = n_wblk * n_tblk;              // tiles of one product
+  const int total = (kMulti ? p.G : 1) * per;
   const int nkb = p.K / BK;
+  // tile t: product, weight-row block, token block
+  auto t_g = [&](int t) { return kMulti ? t / per : 0; };
+  auto t_w = [&](int t) { return (kMulti ? t % per : t) % n_wblk; };
+  auto t_tok = [&](int t) { return (kMulti ? t % per : t) / n_wblk; };
+  auto wmap = [&](int g) -> const CUtensorMap* {
+    if constexpr (kMulti) return &tmW.m[g];
+    else return &tmW;
+  };
 
   // The producer and the MMA issuer run with the whole warp: lane 0 waits on
   // the barriers (result broadcast), one elected lane issues.
@@ -207,20 +246,21 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
       while (i < issued && w2.next(p, nkb, s2))
         for (int kb = s2.kb0; kb < s2.kb1 && i < issued; ++kb, ++i)
           if (elect_one())
-            tma_load_2d(stages + i * C::kStageBytes + BM * BK, &tmX, &full[i], kb * BK, (s2.t / n_wblk) * TN);
+            tma_load_2d(stages + i * C::kStageBytes + BM * BK, &tmX, &full[i], kb * BK, t_tok(s2.t) * TN);
       __syncwarp();
     };
     if (pre == 0) griddep_wait();
     Walk<kStreamK> w(p, total, nkb);
     Seg sg;
     while (ok && w.next(p, nkb, sg)) {
-      const int wb = sg.t % n_wblk, tb = sg.t / n_wblk;
+      const int wb = t_w(sg.t), tb = t_tok(sg.t);
+      const CUtensorMap* mw = wmap(t_g(sg.t));
       for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
         if (!mbar_wait_warp(&empty[ps.index], ps.phase ^ 1u, wg, 50)) { ok = false; break; }
         uint8_t* st = stages + ps.index * C::kStageBytes;
         if (elect_one()) {
           mbar_arrive_expect_tx(&full[ps.index], (uint32_t)(BM * BK + TN * BK));
-          tma_load_2d(st, &tmW, &full[ps.index], kb * BK, wb * BM);
+          tma_load_2d(st, mw, &full[ps.index], kb * BK, wb * BM);
           if (item >= pre) tma_load_2d(st + BM * BK, &tmX, &full[ps.index], kb * BK, tb * TN);
         }
         __syncwarp();
@@ -313,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
     bool ok = true;
     auto nchunks = [&](const Seg& s) { return (s.kb1 - s.kb0 + KBC - 1) / KBC; };
     auto stage_scales = [&](const Seg& s, int c, int buf) {
-      const int wb = s.t % n_wblk, tb = s.t / n_wblk;
+      const int wb = t_w(s.t), tb = t_tok(s.t);
+      const float* sfb = kMulti ? pick(p.sfb_g, t_g(s.t)) : p.sfb;
       float* da = ssa + buf * KBC * TN;
       float* db = ssb + buf * KBC;
       for (int i = etid; i < KBC * TN; i += 256) {
@@ -328,15 +369,16 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
       for (int i = etid; i < KBC; i += 256) {
         const int kb = s.kb0 + c * KBC + i;
         const bool valid = kb < s.kb1;
-        const float* src = valid ? p.sfb + (size_t)wb * nkb + kb : p.sfb;
+        const float* src = valid ? sfb + (size_t)wb * nkb + kb : sfb;
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(db + i)), "l"(src),
                      "r"(valid ? 4 : 0)
                      : "memory");
       }
     };
     auto store_out = [&](const Seg& s, const float (&y)[NC]) {
-      const int n = (s.t % n_wblk) * BM + r;            // weight row = output column
-      const int m0 = (s.t / n_wblk) * TN + col0;        // first token of this warp's columns
+      const int n = t_w(s.t) * BM + r;                  // weight row = output column
+      const int m0 = t_tok(s.t) * TN + col0;            // first token of this warp's columns
+      void* const out = kMulti ? pick(p.out_g, t_g(s.t)) : p.out;
       if (n >= p.N) return;
       const float sw = kRowwise ? __ldg(p.sfb + n) : 1.0f;   // W8A8: channel scale of this row
 #pragma unroll
@@ -345,9 +387,9 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
         if (m < p.M) {
           const float v = kRowwise ? y[i] * (__ldg(p.sfa + m) * sw) : y[i];
           if (p.out_bf16)
-            reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(v);
+            reinterpret_cast<__nv_bfloat16*>(out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(v);
           else
-            reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + n] = v;
+            reinterpret_cast<float*>(out)[(size_t)m * p.ldo + n] = v;
         }
       }
     };
@@ -525,25 +567,49 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
         if (ok) {
           tc_fence_after();
           const float4* s4 = reinterpret_cast<const float4*>(csa + (kb - kc0) * TN + col0);
-          constexpr int CH = NC < 32 ? NC : 32;
-#pragma unroll
-          for (int c0 = 0; c0 < NC; c0 += CH) {
-            uint32_t v[CH];
-            tmem_ld_cols<CH>(tmem + ((uint32_t)(q * 32) << 16) + sl.index * TN + col0 + c0, v);
+          if constexpr (!kStreamK) {
+            // the warp's whole slot in registers with one wait, the slot handed
+            // back, then the fold (two columns per packed FMA)
+            uint32_t v[NC];
+            tmem_ld_cols<NC>(tmem + ((uint32_t)(q * 32) << 16) + sl.index * TN + col0, v);
             tmem_ld_wait();
-            if (c0 + CH == NC) {
-              // every column of the slot is in registers: hand the slot back
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&pempty[sl.index]);
-            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[sl.index]);
 #pragma unroll
-            for (int i = 0; i < CH; i += 4) {
-              const float4 sc = s4[(c0 + i) / 4];
-              acc[c0 + i] = fmaf(__uint_as_float(v[i]), sc.x, acc[c0 + i]);
-              acc[c0 + i + 1] = fmaf(__uint_as_float(v[i + 1]), sc.y, acc[c0 + i + 1]);
-              acc[c0 + i + 2] = fmaf(__uint_as_float(v[i + 2]), sc.z, acc[c0 + i + 2]);
-              acc[c0 + i + 3] = fmaf(__uint_as_float(v[i + 3]), sc.w, acc[c0 + i + 3]);
+            for (int i = 0; i < NC; i += 4) {
+              const float4 sc = s4[i / 4];
+              const float2 lo = __ffma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                           make_float2(sc.x, sc.y), make_float2(acc[i], acc[i + 1]));
+              const float2 hi = __ffma2_rn(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])),
+                                           make_float2(sc.z, sc.w), make_float2(acc[i + 2], acc[i + 3]));
+              acc[i] = lo.x;
+              acc[i + 1] = lo.y;
+              acc[i + 2] = hi.x;
+              acc[i + 3] = hi.y;
+            }
+          } else {
+            // stream-K (registers also hold the fix-up): two halves, one wait each
+            constexpr int CH = NC < 32 ? NC : 32;
+#pragma unroll
+            for (int c0 = 0; c0 < NC; c0 += CH) {
+              uint32_t v[CH];
+              tmem_ld_cols<CH>(tmem + ((uint32_t)(q * 32) << 16) + sl.index * TN + col0 + c0, v);
+              tmem_ld_wait();
+              if (c0 + CH == NC) {
+                // every column of the slot is in registers: hand the slot back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pempty[sl.index]);
+              }
+#pragma unroll
+              for (int i = 0; i < CH; i += 4) {
+                const float4 sc = s4[(c0 + i) / 4];
+                acc[c0 + i] = fmaf(__uint_as_float(v[i]), sc.x, acc[c0 + i]);
+                acc[c0 + i + 1] = fmaf(__uint_as_float(v[i + 1]), sc.y, acc[c0 + i + 1]);
+                acc[c0 + i + 2] = fmaf(__uint_as_float(v[i + 2]), sc.z, acc[c0 + i + 2]);
+                acc[c0 + i + 3] = fmaf(__uint_as_float(v[i + 3]), sc.w, acc[c0 + i + 3]);
+              }
             }
           }
         }
@@ -569,16 +635,19 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
   }
 }
 
-template <int TN, bool kStreamK, bool kRowwise>
+template <int TN, bool kStreamK, bool kRowwise, bool kMulti = false>
 static cudaError_t launch_tn(const Fp8Launch& L, cudaStream_t stream) {
   using C = Cfg<TN>;
-  auto kern = fp8_gemm_kernel<TN, kStreamK, kRowwise>;
+  auto kern = fp8_gemm_kernel<TN, kStreamK, kRowwise, kMulti>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   // all of the SM's unified memory as shared memory, so two decode CTAs fit
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmA, L.tmB, L.p);
+  if constexpr (kMulti)
+    return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmA_g, L.tmB, L.p);
+  else
+    return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmA, L.tmB, L.p);
 }
 
 }  // namespace fp8
@@ -611,8 +680,22 @@ static cudaError_t launch_sk(const Fp8Launch& L, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
+// Multi-weight launches: block-scaled, decode tiles (M <= 32) only.
+template <bool kStreamK>
+static cudaError_t launch_multi(const Fp8Launch& L, cudaStream_t stream) {
+  switch (L.tile_n) {
+    case 16: return fp8::launch_tn<16, kStreamK, false, true>(L, stream);
+    case 32: return fp8::launch_tn<32, kStreamK, false, true>(L, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream) {
   if (L.grid <= 0) return cudaErrorInvalidValue;
+  if (L.p.G > 1) {
+    if (L.p.G > kFp8MaxWeights || L.p.rowwise) return cudaErrorInvalidValue;
+    return L.p.stream_k ? launch_multi<true>(L, stream) : launch_multi<false>(L, stream);
+  }
   if (L.p.rowwise) return L.p.stream_k ? launch_sk<true, true>(L, stream) : launch_sk<false, true>(L, stream);
   return L.p.stream_k ? launch_sk<true, false>(L, stream) : launch_sk<false, false>(L, stream);
 }

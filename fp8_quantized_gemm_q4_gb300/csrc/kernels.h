@@ -136,6 +136,13 @@ struct Fp4DecodeLaunch {
 cudaError_t launch_fp4_decode(const Fp4DecodeLaunch& L, cudaStream_t stream);
 int fp4_decode_stages(int tile_n);
 
+// Products one multi-weight FP8 launch computes (G weight sets that share the
+// activation operand).
+constexpr int kFp8MaxWeights = 8;
+struct Fp8WMaps {
+  CUtensorMap m[kFp8MaxWeights];
+};
+
 struct Fp8Params {
   const float* sfa;       // [K/128, M]
   const float* sfb;       // [ceil(N/128), K/128]
@@ -151,10 +158,15 @@ struct Fp8Params {
   int rowwise;            // W8A8: sfa fp32 [M] per token, sfb fp32 [N] per channel; no per-block promotion
   int* status;
   unsigned long long wait_ns;  // bound of every pipeline wait (%globaltimer ns)
+  int G;                  // products sharing the activation: 1 = one GEMM (sfb, out); > 1 = the
+                          // multi-weight kernel (sfb_g, out_g; block scaling, M <= 32)
+  const float* sfb_g[kFp8MaxWeights];
+  void* out_g[kFp8MaxWeights];
 };
 
 struct Fp8Launch {
   CUtensorMap tmA, tmB;
+  Fp8WMaps tmA_g;         // G > 1: the weight map of every product (tmA unused)
   Fp8Params p;
   int tile_n;             // MMA N (token columns per tile): 16, 32, 64 or 128
   int grid;

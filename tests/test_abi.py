@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("q4_quantize", "q8_quantize", "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_swiglu_q4",
+    for n in ("q4_quantize", "q8_quantize", "bs_gemm", "bs_gemm_multi", "bs_grouped_gemm", "bs_grouped_gemm_swiglu_q4",
               "bs_moe_dispatch",
               "bs_moe_finalize", "bs_moe_combine", "bs_sf_bytes", "bs_sf_offset", "bs_get_device_status"):
         assert n in names
@@ -133,6 +133,33 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.bs_moe_combine(fake, 64, fake, 128, 4, 2, 60, fake, fake, 64, None) == bs.BS_ERR_ALIGN
     assert lib.bs_moe_combine(P((1 << 20) + 4), 64, fake, 128, 4, 2, 64, fake, fake, 64, None) == bs.BS_ERR_ALIGN
     assert lib.bs_moe_combine(None, 64, None, 0, 0, 2, 64, None, None, 64, None) == bs.BS_OK
+    # multi-weight FP8: G out of range, null arrays, FP4, W8A8, M > 32, a null or
+    # misaligned product operand -- all rejected before any device query
+    arr3 = (P * 3)(fake, fake, fake)
+    bad = (P * 3)(fake, None, fake)
+    mis = (P * 3)(fake, P((1 << 20) + 8), fake)
+    g.fmt, g.M, g.N, g.K, g.ldo = 1, 16, 128, 256, 128
+    multi = lib.bs_gemm_multi
+    assert multi(ctypes.byref(g), 0, arr3, arr3, arr3, None) == bs.BS_ERR_INVALID
+    assert multi(ctypes.byref(g), 9, arr3, arr3, arr3, None) == bs.BS_ERR_INVALID
+    assert multi(ctypes.byref(g), 3, None, arr3, arr3, None) == bs.BS_ERR_INVALID
+    assert multi(ctypes.byref(g), 3, bad, arr3, arr3, None) == bs.BS_ERR_INVALID
+    assert multi(ctypes.byref(g), 3, arr3, arr3, mis, None) == bs.BS_ERR_ALIGN
+    g.K = 192
+    assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_ERR_ALIGN     # K % 128
+    g.K = 256
+    g.M = 33
+    assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_ERR_UNSUPPORTED
+    g.M = 16
+    g.fp8_scaling = 2
+    assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_ERR_UNSUPPORTED
+    g.fp8_scaling = 0
+    g.fmt = 0
+    assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_ERR_UNSUPPORTED
+    g.fmt, g.M = 1, 0
+    assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_OK           # M == 0: nothing to do
+    assert lib.bs_gemm_multi_workspace_bytes(ctypes.byref(g), 3) == 0
+    g.fmt, g.M, g.N, g.K, g.ldo = 0, 64, 128, 128, 128
     assert lib.bs_status_string(5) == b"device pipeline wait timed out"
     assert b"K=100" in lib.bs_last_error() or lib.bs_last_error() != b""
 

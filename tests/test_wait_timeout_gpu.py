@@ -150,3 +150,21 @@ def test_wait_runs_out_fp4_decode(cuda_lib, pdl_hold):
 
     _timeout_then_same_result(bs, pdl_hold, run, SITES_DECODE)
 
+
+
+def test_wait_runs_out_fp8_multi(cuda_lib, pdl_hold):
+    """The multi-weight kernel (three decode products in one grid)."""
+    bs = cuda_lib
+    g = torch.Generator().manual_seed(6)
+    K, N = 4096, 1024
+    x = torch.randn(16, K, generator=g).to(torch.bfloat16).cuda()
+    xq, xs = bs.q8_quantize(x, mode=bs.Q8_TOKEN)
+    wqs = [bs.q8_quantize((torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda(), mode=bs.Q8_BLOCK)
+           for _ in range(3)]
+
+    def run(opts, before):
+        with bs.kernel_options(**opts):
+            before()
+            return torch.stack(bs.gemm_fp8_multi(xq, xs, wqs))
+
+    _timeout_then_same_result(bs, pdl_hold, run, SITES_FP8)
