@@ -407,16 +407,17 @@ class DecodeChain(Fp8Sweep):
     the projections of a decode step that read the same activation), each a
     programmatic dependent launch with weights_ready, so its weight stream
     starts under the tail of the GEMM before it.  fmt "fp8": block-scaled FP8
-    (swap-AB stream-K kernel); "fp4": the FP4 decode kernel.  Roofline: the G
-    GEMMs' algorithmic bytes over the time from the first GEMM's start to the
-    last one's end (the quantizer excluded)."""
+    (swap-AB stream-K kernel); "fp4": the FP4 decode kernel.  multi: the same
+    G products as one bs_gemm_multi launch (one tile list on one grid).
+    Roofline: the G GEMMs' algorithmic bytes over the time from the first
+    GEMM's start to the last one's end (the quantizer excluded)."""
 
     G = 8
 
     def __init__(self, fmt, multi=False):
         super().__init__(16)
         self.fmt = fmt
-        self.multi = multi  # fp8: the G products in one bs_gemm_multi launch
+        self.multi = multi  # the G products in one bs_gemm_multi launch
         G = self.G
         if multi:
             self.name = f"{fmt}_decode_multi_{G}x_M16_N7168_K4096"
@@ -477,7 +478,10 @@ class DecodeChain(Fp8Sweep):
         if gemm_events:
             gemm_events[0].record()
         if self.multi:
-            bs.gemm_fp8_multi(self.xq, self.xs, self.ws_list, outs=self.out_list, weights_ready=True)
+            if self.fmt == "fp4":
+                bs.gemm_fp4_multi(self.xq, self.xs, self.ws_list, self.K, outs=self.out_list, weights_ready=True)
+            else:
+                bs.gemm_fp8_multi(self.xq, self.xs, self.ws_list, outs=self.out_list, weights_ready=True)
             if gemm_events:
                 gemm_events[1].record()
             return self.out
@@ -492,7 +496,8 @@ class DecodeChain(Fp8Sweep):
 
     def roofline(self, gemm_ms, peaks, source):
         if self.multi:
-            kern = f"fp8_gemm_kernel (multi-weight: {self.G} products, one launch)"
+            kern = ("fp4_decode_kernel" if self.fmt == "fp4" else "fp8_gemm_kernel") + \
+                f" (multi-weight: {self.G} products, one launch)"
         else:
             kern = ("fp4_decode_kernel" if self.fmt == "fp4" else "fp8_gemm_kernel") + f" x{self.G} (chain)"
         return hbm_roofline(kern, self.gemm_bytes, gemm_ms, peaks, source)
@@ -878,6 +883,7 @@ WORKLOADS = {
     "moe_fp8_small": lambda: Fp8MoEWorkload(large=False),
     "fp8_decode_chain": lambda: DecodeChain("fp8"),
     "fp8_decode_multi": lambda: DecodeChain("fp8", multi=True),
+    "fp4_decode_multi": lambda: DecodeChain("fp4", multi=True),
     "fp4_decode_chain": lambda: DecodeChain("fp4"),
     "q4_quantize": lambda: QuantWorkload("q4"),
     "q8_quantize": lambda: QuantWorkload("q8"),
@@ -1019,7 +1025,7 @@ def check_device_status():
 # % of GB300 dense peak; MoE layer us"), timed in the same run as the dense
 # headline and reported beside it.
 EXTRAS = ("moe_small", "moe_large", "moe_fp8_small", "fp8_m16", "fp8_m4096", "fp8_w8a8_m16", "fp8_w8a8_m4096",
-          "fp4_decode_m16", "fp8_decode_chain", "fp8_decode_multi", "fp4_decode_chain", "q4_quantize", "q8_quantize")
+          "fp4_decode_m16", "fp8_decode_chain", "fp8_decode_multi", "fp4_decode_chain", "fp4_decode_multi", "q4_quantize", "q8_quantize")
 
 
 def run_extra(args, name, world, dev, peaks, source):

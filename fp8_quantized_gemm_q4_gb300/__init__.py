@@ -20,7 +20,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 
 __all__ = [
-    "load", "sf_bytes", "sf_offset", "q4_quantize", "tensor_amax", "q4_quantize_two_level", "fp4_gather_rows", "fp8_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8", "gemm_fp8_multi",
+    "load", "sf_bytes", "sf_offset", "q4_quantize", "tensor_amax", "q4_quantize_two_level", "fp4_gather_rows", "fp8_gather_rows", "q8_quantize", "gemm_fp4", "gemm_fp8", "gemm_fp8_multi", "gemm_fp4_multi",
     "grouped_gemm_fp4", "grouped_gemm_fp4_swiglu_q4", "grouped_gemm_fp8", "moe_router_topk", "moe_dispatch", "moe_finalize", "moe_combine", "moe_rows_bound", "device_status",
     "clear_device_status", "BSError", "EPI_STORE", "EPI_SWIGLU", "EPI_COMBINE", "EPI_ROWS", "kernel_options",
     "current_kernel_options", "FP4_ONE_CTA", "FP4_PAIR",
@@ -357,20 +357,15 @@ def gemm_fp8(a, sa, b, sb, out_dtype=torch.bfloat16, out=None, num_sms: int = 0,
     return out
 
 
-def gemm_fp8_multi(a, sa, weights, out_dtype=torch.bfloat16, outs=None, num_sms: int = 0,
-                   weights_ready: bool = False, stream=None):
-    """G block-scaled FP8 GEMMs that share the tokens ``a`` [M, K] (M <= 32,
-    TOKEN-mode scales ``sa``) in one launch: ``weights`` is a list of (codes
-    [N, K], BLOCK-mode scales) pairs, one per product; returns the G outputs
-    [M, N] (or fills ``outs``)."""
-    M, K = a.shape
+def _gemm_multi(fmt, a, sa, weights, M, N, K, out_dtype, outs, num_sms, weights_ready, alpha=1.0,
+                a_tensor_scale=None, stream=None):
     G = len(weights)
-    N = weights[0][0].shape[0]
     if outs is None:
         outs = [torch.empty((M, N), dtype=out_dtype, device=a.device) for _ in range(G)]
     b0, sb0 = weights[0]
-    g = _args(FMT_FP8, a, sa, b0, sb0, M, N, K, outs[0], num_sms=num_sms)
+    g = _args(fmt, a, sa, b0, sb0, M, N, K, outs[0], alpha=alpha, num_sms=num_sms)
     g.weights_ready = 1 if weights_ready else 0
+    g.a_tensor_scale = None if a_tensor_scale is None else a_tensor_scale.data_ptr()
     arr = ctypes.c_void_p * max(G, 1)
     bp = arr(*[w[0].data_ptr() for w in weights])
     sp = arr(*[w[1].data_ptr() for w in weights])
@@ -383,6 +378,27 @@ def gemm_fp8_multi(a, sa, weights, out_dtype=torch.bfloat16, outs=None, num_sms:
         g.workspace, g.workspace_bytes = ws.data_ptr(), ws.numel()
     _check(lib.bs_gemm_multi(ctypes.byref(g), G, bp, sp, op, _stream(stream)))
     return outs
+
+
+def gemm_fp8_multi(a, sa, weights, out_dtype=torch.bfloat16, outs=None, num_sms: int = 0,
+                   weights_ready: bool = False, stream=None):
+    """G block-scaled FP8 GEMMs that share the tokens ``a`` [M, K] (M <= 32,
+    TOKEN-mode scales ``sa``) in one launch: ``weights`` is a list of (codes
+    [N, K], BLOCK-mode scales) pairs, one per product; returns the G outputs
+    [M, N] (or fills ``outs``)."""
+    M, K = a.shape
+    return _gemm_multi(FMT_FP8, a, sa, weights, M, weights[0][0].shape[0], K, out_dtype, outs, num_sms,
+                       weights_ready, stream=stream)
+
+
+def gemm_fp4_multi(a, sfa, weights, K: int, out_dtype=torch.bfloat16, outs=None, alpha: float = 1.0,
+                   a_tensor_scale=None, num_sms: int = 0, weights_ready: bool = False, stream=None):
+    """G FP4 decode GEMMs that share the tokens ``a`` (codes [M, K/2], M <= 32,
+    scales ``sfa``) in one launch: ``weights`` is a list of (codes [N, K/2],
+    scales) pairs from q4_quantize; returns the G outputs [M, N]."""
+    M = a.shape[0]
+    return _gemm_multi(FMT_FP4, a, sfa, weights, M, weights[0][0].shape[0], K, out_dtype, outs, num_sms,
+                       weights_ready, alpha=alpha, a_tensor_scale=a_tensor_scale, stream=stream)
 
 
 def grouped_gemm_fp4(a, sfa, b, sfb, K: int, N: int, E: int, offsets, counts, epilogue: int, out=None,

@@ -474,6 +474,10 @@ static SkSplit sk_split(long long tiles, long long units, int tile_n, int sms) {
 static bool fp4_decode_applies(const bs_gemm_args* a) {
   return a->fmt == BS_FMT_FP4 && a->M > 0 && a->M <= 32 && !a->lora_t && a->K % 256 == 0 && a->fp4_decode != 2;
 }
+// Stream-K keeps one arrival counter per tile in the workspace's fixed head.
+static bool fp4_decode_stream_k(long long tiles) {
+  return tiles <= (long long)(kStreamKCounterBytes / sizeof(int));
+}
 
 struct Fp8Plan {
   int tile_n;
@@ -516,26 +520,35 @@ size_t bs_gemm_workspace_bytes(const bs_gemm_args* a) {
   int sms = 0;
   if (!device_info(nullptr, &sms)) return 0;
   if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
-  if (fp4_decode_applies(a)) return sk_split((a->N + 127) / 128, a->K / 256, a->M <= 16 ? 16 : 32, sms).ws_bytes;
+  if (fp4_decode_applies(a)) {
+    const long long tiles = (a->N + 127) / 128;
+    return fp4_decode_stream_k(tiles) ? sk_split(tiles, a->K / 256, a->M <= 16 ? 16 : 32, sms).ws_bytes : 0;
+  }
   if (a->fmt != BS_FMT_FP8) return 0;
   const Fp8Plan P = fp8_plan(a, sms);
   return P.stream_k ? P.ws_bytes : 0;
 }
 
-// FP4 decode launch (see fp4_decode_applies).
-static bs_status launch_fp4_decode(const bs_gemm_args* a, int sms, int* status, cudaStream_t s) {
+// FP4 decode launch (see fp4_decode_applies) of G >= 1 products that share the
+// tokens a->a: product g multiplies by weights b[g] (scales sfb[g]) into
+// out[g].  G > 1 takes no per-column scale, bias or weight tensor scale
+// (checked by the caller).
+static bs_status launch_fp4_decode(const bs_gemm_args* a, int G, const uint8_t* const* b, const uint8_t* const* sfb,
+                                   void* const* out, int sms, int* status, cudaStream_t s) {
   bsk::Fp4DecodeLaunch L;
   memset(&L, 0, sizeof L);
   L.tile_n = a->M <= 16 ? 16 : 32;
   const uint64_t kb = (uint64_t)a->K / 2;
-  bs_status st = make_map(&L.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->b, kb, (uint64_t)a->N, kb, 128, 128,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != BS_OK) return st;
-  st = make_map(&L.tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, kb, (uint64_t)a->M, kb, 128, (uint32_t)L.tile_n,
-                CU_TENSOR_MAP_SWIZZLE_128B);
+  for (int g = 0; g < G; ++g) {
+    bs_status st = make_map(G == 1 ? &L.tmW : &L.tmW_g.m[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b[g], kb,
+                            (uint64_t)a->N, kb, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BS_OK) return st;
+  }
+  bs_status st = make_map(&L.tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a->a, kb, (uint64_t)a->M, kb, 128,
+                          (uint32_t)L.tile_n, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != BS_OK) return st;
   bsk::Fp4DecodeParams& p = L.p;
-  p.sfw = static_cast<const uint8_t*>(a->sfb);
+  p.sfw = sfb[0];
   p.sfx = static_cast<const uint8_t*>(a->sfa);
   p.M = (int)a->M;
   p.N = (int)a->N;
@@ -545,15 +558,20 @@ static bs_status launch_fp4_decode(const bs_gemm_args* a, int sms, int* status, 
   p.bias = a->bias;
   p.a_ts = a->a_tensor_scale;
   p.b_ts = a->b_tensor_scale;
-  p.out = a->out;
+  p.out = out[0];
   p.out_bf16 = a->out_dtype == BS_DTYPE_BF16;
   p.ldo = a->ldo;
   p.status = status;
   p.wait_ns = wait_ns(a);
   p.pre_b = a->weights_ready == 1 ? bsk::fp4_decode_stages(L.tile_n) : 0;
-  const long long tiles = (a->N + 127) / 128, units = a->K / 256;
-  const SkSplit k = sk_split(tiles, units, L.tile_n, sms);
-  if (a->workspace) {
+  p.G = G;
+  for (int g = 0; g < G; ++g) {
+    p.sfw_g[g] = sfb[g];
+    p.out_g[g] = out[g];
+  }
+  const long long tiles = (long long)G * ((a->N + 127) / 128), units = a->K / 256;
+  if (a->workspace && fp4_decode_stream_k(tiles)) {
+    const SkSplit k = sk_split(tiles, units, L.tile_n, sms);
     if (!aligned16(a->workspace)) return fail(BS_ERR_ALIGN, "workspace must be 16-byte aligned");
     if (a->workspace_bytes < k.ws_bytes)
       return fail(BS_ERR_INVALID, "workspace too small (%zu < %zu bytes)", a->workspace_bytes, k.ws_bytes);
@@ -568,7 +586,7 @@ static bs_status launch_fp4_decode(const bs_gemm_args* a, int sms, int* status, 
     L.grid = g;
   }
   cudaError_t e = bsk::launch_fp4_decode(L, s);
-  if (e != cudaSuccess) return cuda_fail(e, "FP4 decode GEMM launch");
+  if (e != cudaSuccess) return cuda_fail(e, G == 1 ? "FP4 decode GEMM launch" : "FP4 multi-weight decode launch");
   return BS_OK;
 }
 
@@ -657,7 +675,11 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
     if ((reinterpret_cast<uintptr_t>(a->a_tensor_scale) | reinterpret_cast<uintptr_t>(a->b_tensor_scale)) & 3)
       return fail(BS_ERR_ALIGN, "tensor scales must be 4-byte aligned");
     if (a->M == 0) return BS_OK;
-    if (fp4_decode_applies(a)) return launch_fp4_decode(a, sms, status, s);
+    if (fp4_decode_applies(a)) {
+      const uint8_t* sfb = static_cast<const uint8_t*>(a->sfb);
+      void* out = a->out;
+      return launch_fp4_decode(a, 1, &a->b, &sfb, &out, sms, status, s);
+    }
     bsk::Fp4Launch L;
     memset(&L, 0, sizeof L);
     L.p.sfa = static_cast<const uint8_t*>(a->sfa);
@@ -695,23 +717,29 @@ bs_status bs_gemm(const bs_gemm_args* a, bs_stream_t stream) {
 }
 
 size_t bs_gemm_multi_workspace_bytes(const bs_gemm_args* a, int G) {
-  if (!a || G < 1 || G > bsk::kFp8MaxWeights || a->fmt != BS_FMT_FP8 || a->M <= 0 || a->M > 32 || a->N <= 0 ||
-      a->K < 128 || a->num_sms < 0)
+  if (!a || G < 1 || G > bsk::kMaxProducts || (a->fmt != BS_FMT_FP8 && a->fmt != BS_FMT_FP4) || a->M <= 0 ||
+      a->M > 32 || a->N <= 0 || a->K < 128 || a->num_sms < 0)
     return 0;
   int sms = 0;
   if (!device_info(nullptr, &sms)) return 0;
   if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
+  if (a->fmt == BS_FMT_FP4) {
+    if (a->K % 256) return 0;
+    const long long tiles = (long long)G * ((a->N + 127) / 128);
+    return fp4_decode_stream_k(tiles) ? sk_split(tiles, a->K / 256, a->M <= 16 ? 16 : 32, sms).ws_bytes : 0;
+  }
   const Fp8Plan P = fp8_plan(a, sms, G);
   return P.stream_k ? P.ws_bytes : 0;
 }
 
-bs_status bs_gemm_multi(const bs_gemm_args* a, int G, const uint8_t* const* b, const float* const* sfb,
+bs_status bs_gemm_multi(const bs_gemm_args* a, int G, const uint8_t* const* b, const void* const* sfb,
                         void* const* out, bs_stream_t stream) {
   if (!a) return fail(BS_ERR_INVALID, "null args");
-  if (G < 1 || G > bsk::kFp8MaxWeights) return fail(BS_ERR_INVALID, "G=%d outside [1, %d]", G, bsk::kFp8MaxWeights);
+  if (G < 1 || G > bsk::kMaxProducts) return fail(BS_ERR_INVALID, "G=%d outside [1, %d]", G, bsk::kMaxProducts);
   if (!b || !sfb || !out) return fail(BS_ERR_INVALID, "null weight / scale / output array");
-  if (a->fmt != BS_FMT_FP8) return fail(BS_ERR_UNSUPPORTED, "bs_gemm_multi: FP8 only");
-  if (a->fp8_scaling == 2) return fail(BS_ERR_UNSUPPORTED, "bs_gemm_multi: block scaling only (not W8A8)");
+  if (a->fmt != BS_FMT_FP8 && a->fmt != BS_FMT_FP4) return fail(BS_ERR_INVALID, "fmt %d", a->fmt);
+  if (a->fmt == BS_FMT_FP8 && a->fp8_scaling == 2)
+    return fail(BS_ERR_UNSUPPORTED, "bs_gemm_multi: FP8 block scaling only (not W8A8)");
   if (a->M > 32) return fail(BS_ERR_UNSUPPORTED, "bs_gemm_multi: M=%lld > 32 (decode shapes)", (long long)a->M);
   bs_gemm_args one = *a;
   one.b = b[0];
@@ -719,8 +747,16 @@ bs_status bs_gemm_multi(const bs_gemm_args* a, int G, const uint8_t* const* b, c
   one.out = out[0];
   bs_status st = check_common(&one, false);
   if (st != BS_OK) return st;
-  st = check_fp8(&one);
-  if (st != BS_OK) return st;
+  if (a->fmt == BS_FMT_FP8) {
+    st = check_fp8(&one);
+    if (st != BS_OK) return st;
+  } else {
+    if (a->K % 256) return fail(BS_ERR_ALIGN, "bs_gemm_multi FP4: K=%lld not a multiple of 256", (long long)a->K);
+    if (a->lora_t || a->col_scale || a->bias || a->b_tensor_scale || a->fp4_decode == 2)
+      return fail(BS_ERR_UNSUPPORTED,
+                  "bs_gemm_multi FP4: no low-rank branch, col_scale, bias or weight tensor scale; decode kernel only");
+    if (reinterpret_cast<uintptr_t>(a->a_tensor_scale) & 3) return fail(BS_ERR_ALIGN, "tensor scale misaligned");
+  }
   if (a->M == 0) return BS_OK;
   for (int g = 0; g < G; ++g) {
     if (!b[g] || !sfb[g] || !out[g]) return fail(BS_ERR_INVALID, "null operand of product %d", g);
@@ -731,7 +767,10 @@ bs_status bs_gemm_multi(const bs_gemm_args* a, int G, const uint8_t* const* b, c
   int sms = 0;
   if (!device_info(&status, &sms)) return fail(BS_ERR_CUDA, "no current device");
   if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
-  return launch_fp8(a, G, b, sfb, out, sms, status, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (a->fmt == BS_FMT_FP4)
+    return launch_fp4_decode(a, G, b, reinterpret_cast<const uint8_t* const*>(sfb), out, sms, status, s);
+  return launch_fp8(a, G, b, reinterpret_cast<const float* const*>(sfb), out, sms, status, s);
 }
 
 // FP8 grouped GEMM (tokens as the MMA's M, see gemm_fp8_grouped.cu); args

@@ -11,9 +11,10 @@
 // runs full-height block-scaled MMAs (kind::mxf4nvf4, block16 ue4m3 scales
 // applied by the tensor core: no promotion) over the weights.
 //
-// Work units are (weight tile of 128 rows, K stage of 256) pairs; they form
-// one sequence shared out evenly over the grid (stream-K, "DeepGEMM teardown"
-// sections 1.2 and 3.2: small M leaves SMs idle).  A CTA accumulates its K
+// Work units are (weight tile of 128 rows, K stage of 256) pairs; with fewer
+// tiles than CTAs they form one sequence shared out evenly over the grid
+// (stream-K, "DeepGEMM teardown" sections 1.2 and 3.2: small M leaves SMs
+// idle), otherwise each CTA takes a contiguous run of whole tiles.  A CTA accumulates its K
 // range of a tile in one tensor-memory slot; a tile cut between CTAs is
 // finished by the last of them (acquire-release counter in the caller's
 // workspace, pieces summed in K order, counter reset), as in the FP8 kernel.
@@ -24,6 +25,12 @@
 // of one stage contiguous) with bulk copies.  The MMA warp stages the scales
 // in tensor memory with tcgen05.cp (token row n sits at lane n % 32, column
 // n / 32 of its tile, so N = TN <= 32 reads column 0) and issues four MMAs.
+//
+// kMulti: G products Y_g = X W_g^T that share the tokens form one list of
+// weight tiles (tile t is tile t mod T of product t / T, T = tiles of one
+// product) under one stream-K schedule, each product with its own weight map,
+// scales and output, so a decode step's projections pay the launch, first
+// loads and fix-up tail once.
 #include "budget.hpp"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -72,12 +79,20 @@ struct Seg {
   int t, kb0, kb1;  // weight tile t, K stages [kb0, kb1)
 };
 
+// A CTA's range of the (tile, K stage) sequence.  With at least as many tiles
+// as CTAs the ranges are whole tiles (contiguous, balanced to within one
+// tile), so no tile is cut and no fix-up runs; with fewer, stream-K.
 struct Walk {
   long long cur, end;
   __device__ __forceinline__ Walk(int total, int nks) {
-    const long long U = (long long)total * nks;
-    cur = (long long)blockIdx.x * U / gridDim.x;
-    end = (long long)(blockIdx.x + 1) * U / gridDim.x;
+    if (total >= (int)gridDim.x) {
+      cur = (long long)blockIdx.x * total / gridDim.x * nks;
+      end = (long long)(blockIdx.x + 1) * total / gridDim.x * nks;
+    } else {
+      const long long U = (long long)total * nks;
+      cur = (long long)blockIdx.x * U / gridDim.x;
+      end = (long long)(blockIdx.x + 1) * U / gridDim.x;
+    }
   }
   __device__ __forceinline__ bool next(int nks, Seg& s) {
     if (cur >= end) return false;
@@ -91,10 +106,10 @@ struct Walk {
 
 __device__ __forceinline__ int sk_owner(long long u, long long U, int G) { return (int)(((u + 1) * G - 1) / U); }
 
-template <int TN>
+template <int TN, bool kMulti>
 __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
-    fp4_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                      const Fp4DecodeParams p) {
+    fp4_decode_kernel(const __grid_constant__ typename WArg<kMulti>::type tmW,
+                      const __grid_constant__ CUtensorMap tmX, const Fp4DecodeParams p) {
   using C = Cfg<TN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kAlign - 1) &
@@ -130,7 +145,11 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
       mbar_init(drain, 1);
       *abort_i = 0;
       fence_barrier_init();
-      prefetch_tmap(&tmW);
+      if constexpr (kMulti) {
+        for (int g = 0; g < p.G; ++g) prefetch_tmap(&tmW.m[g]);
+      } else {
+        prefetch_tmap(&tmW);
+      }
       prefetch_tmap(&tmX);
     }
     __syncwarp();
@@ -146,8 +165,12 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
     tmem = warp_bcast(*tmem_base);
   }
 
-  const int total = (p.N + BM - 1) / BM;   // weight tiles (one token block: M <= TN)
+  const int per = (p.N + BM - 1) / BM;     // weight tiles of one product (one token block: M <= TN)
+  const int total = (kMulti ? p.G : 1) * per;
   const int nks = p.K / BK;                // K stages (K % 256 == 0)
+  // tile t: product and weight-row block within it
+  auto t_g = [&](int t) { return kMulti ? t / per : 0; };
+  auto t_w = [&](int t) { return kMulti ? t % per : t; };
   const int kchunks = p.K / 64;            // 512-byte scale tiles per 128-row block
 
   if (warp == 0) {
@@ -182,8 +205,13 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
         uint8_t* st = stages + ps.index * C::kStageBytes;
         if (elect_one()) {
           mbar_arrive_expect_tx(&full[ps.index], (uint32_t)C::kTx);
-          tma_load_2d(st + C::kOffW, &tmW, &full[ps.index], kb * kRowBytes, sg.t * BM);
-          bulk_load(st + C::kOffSfw, p.sfw + ((size_t)sg.t * kchunks + (size_t)kb * kMmas) * 512, kMmas * 512,
+          const int g = t_g(sg.t), wt = t_w(sg.t);
+          const CUtensorMap* mw;
+          if constexpr (kMulti) mw = &tmW.m[g];
+          else mw = &tmW;
+          const uint8_t* sfw = kMulti ? pick(p.sfw_g, g) : p.sfw;
+          tma_load_2d(st + C::kOffW, mw, &full[ps.index], kb * kRowBytes, wt * BM);
+          bulk_load(st + C::kOffSfw, sfw + ((size_t)wt * kchunks + (size_t)kb * kMmas) * 512, kMmas * 512,
                     &full[ps.index]);
           if (item >= pre) {
             tma_load_2d(st + C::kOffX, &tmX, &full[ps.index], kb * kRowBytes, 0);
@@ -259,8 +287,9 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
     PipeState<C::kSlots> sl;
     bool ok = true;
     auto store_out = [&](const Seg& s, const float (&y)[NC]) {
-      const int n = s.t * BM + r;  // weight row = output column
+      const int n = t_w(s.t) * BM + r;  // weight row = output column
       if (n >= p.N) return;
+      void* const out = kMulti ? pick(p.out_g, t_g(s.t)) : p.out;
       const float sc = alpha_ts * (p.col_scale ? __ldg(p.col_scale + n) : 1.0f);
       const float b = p.bias ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.bias)[n]) : 0.0f;
 #pragma unroll
@@ -269,9 +298,9 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
         if (m < p.M) {
           const float v = y[i] * sc + b;
           if (p.out_bf16)
-            reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(v);
+            reinterpret_cast<__nv_bfloat16*>(out)[(size_t)m * p.ldo + n] = __float2bfloat16_rn(v);
           else
-            reinterpret_cast<float*>(p.out)[(size_t)m * p.ldo + n] = v;
+            reinterpret_cast<float*>(out)[(size_t)m * p.ldo + n] = v;
         }
       }
     };
@@ -349,16 +378,19 @@ __global__ void __launch_bounds__(kThreads, TN == 16 ? 2 : 1)
   }
 }
 
-template <int TN>
+template <int TN, bool kMulti>
 static cudaError_t launch_tn(const Fp4DecodeLaunch& L, cudaStream_t stream) {
   using C = Cfg<TN>;
-  auto kern = fp4_decode_kernel<TN>;
+  auto kern = fp4_decode_kernel<TN, kMulti>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   // all of the SM's unified memory as shared memory, so two decode CTAs fit
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmW, L.tmX, L.p);
+  if constexpr (kMulti)
+    return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmW_g, L.tmX, L.p);
+  else
+    return launch_kernel(kern, (unsigned)L.grid, kThreads, (size_t)C::kSmem, stream, 1, L.tmW, L.tmX, L.p);
 }
 
 }  // namespace fp4dec
@@ -368,9 +400,10 @@ int fp4_decode_stages(int tile_n) {
 }
 
 cudaError_t launch_fp4_decode(const Fp4DecodeLaunch& L, cudaStream_t stream) {
-  if (L.grid <= 0) return cudaErrorInvalidValue;
-  if (L.tile_n == 16) return fp4dec::launch_tn<16>(L, stream);
-  if (L.tile_n == 32) return fp4dec::launch_tn<32>(L, stream);
+  if (L.grid <= 0 || L.p.G < 1 || L.p.G > kMaxProducts) return cudaErrorInvalidValue;
+  const bool multi = L.p.G > 1;
+  if (L.tile_n == 16) return multi ? fp4dec::launch_tn<16, true>(L, stream) : fp4dec::launch_tn<16, false>(L, stream);
+  if (L.tile_n == 32) return multi ? fp4dec::launch_tn<32, true>(L, stream) : fp4dec::launch_tn<32, false>(L, stream);
   return cudaErrorInvalidValue;
 }
 

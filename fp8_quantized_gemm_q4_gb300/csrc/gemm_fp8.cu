@@ -123,27 +123,6 @@ struct Walk {
 // CTA whose stream-K range holds unit u (ranges [c U / G, (c + 1) U / G)).
 __device__ __forceinline__ int sk_owner(long long u, long long U, int G) { return (int)(((u + 1) * G - 1) / U); }
 
-// The weight operand of the kernel: one tensor map, or one per product for the
-// multi-weight variant.
-template <bool kMulti>
-struct WArg {
-  using type = CUtensorMap;
-};
-template <>
-struct WArg<true> {
-  using type = Fp8WMaps;
-};
-
-// a[g] of a per-product parameter array, read with constant indices only
-template <typename T>
-__device__ __forceinline__ T pick(const T (&a)[kFp8MaxWeights], int g) {
-  T r = a[0];
-#pragma unroll
-  for (int i = 1; i < kFp8MaxWeights; ++i)
-    if (g == i) r = a[i];
-  return r;
-}
-
 // kMulti: G products Y_g = X W_g^T that share the token operand run as one
 // list of tiles, product-major (tile t is tile t mod T of product t / T, T =
 // tiles of one product), so a decode step's projections stream their weights
@@ -693,7 +672,7 @@ static cudaError_t launch_multi(const Fp8Launch& L, cudaStream_t stream) {
 cudaError_t launch_fp8_gemm(const Fp8Launch& L, cudaStream_t stream) {
   if (L.grid <= 0) return cudaErrorInvalidValue;
   if (L.p.G > 1) {
-    if (L.p.G > kFp8MaxWeights || L.p.rowwise) return cudaErrorInvalidValue;
+    if (L.p.G > kMaxProducts || L.p.rowwise) return cudaErrorInvalidValue;
     return L.p.stream_k ? launch_multi<true>(L, stream) : launch_multi<false>(L, stream);
   }
   if (L.p.rowwise) return L.p.stream_k ? launch_sk<true, true>(L, stream) : launch_sk<false, true>(L, stream);

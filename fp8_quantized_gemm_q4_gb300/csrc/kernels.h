@@ -108,6 +108,32 @@ cudaError_t launch_fp4_pair_gemm(const Fp4PairLaunch& L, cudaStream_t stream);
 int fp4_pair_stages(bool lora, int bk);
 
 // FP4 decode shapes (M <= 32): swap-AB, stream-K over all SMs.
+// Multi-weight launches: G <= kMaxProducts products Y_g = X W_g^T that share
+// the token operand X, one weight tensor map per product.
+constexpr int kMaxProducts = 8;
+struct WeightMaps {
+  CUtensorMap m[kMaxProducts];
+};
+// The weight-map kernel parameter: one map, or one per product.
+template <bool kMulti>
+struct WArg {
+  using type = CUtensorMap;
+};
+template <>
+struct WArg<true> {
+  using type = WeightMaps;
+};
+// a[g] of a per-product parameter array, read with constant indices only (no
+// local-memory copy of the parameter)
+template <typename T>
+__device__ __forceinline__ T pick(const T (&a)[kMaxProducts], int g) {
+  T r = a[0];
+#pragma unroll
+  for (int i = 1; i < kMaxProducts; ++i)
+    if (g == i) r = a[i];
+  return r;
+}
+
 struct Fp4DecodeParams {
   const uint8_t* sfw;     // weight scales, MMA layout for [N, K]
   const uint8_t* sfx;     // token scales, MMA layout for [M, K] (block 0 holds every row)
@@ -126,22 +152,19 @@ struct Fp4DecodeParams {
   int pre_b;              // weight stages loaded before waiting on the preceding kernel
   int* status;
   unsigned long long wait_ns;
+  int G;                  // products sharing the tokens: 1 = one GEMM (sfw, out); > 1 = sfw_g, out_g
+  const uint8_t* sfw_g[kMaxProducts];
+  void* out_g[kMaxProducts];
 };
 struct Fp4DecodeLaunch {
   CUtensorMap tmW, tmX;
+  WeightMaps tmW_g;       // G > 1: the weight map of every product (tmW unused)
   Fp4DecodeParams p;
   int tile_n;             // 16 or 32 token columns
   int grid;
 };
 cudaError_t launch_fp4_decode(const Fp4DecodeLaunch& L, cudaStream_t stream);
 int fp4_decode_stages(int tile_n);
-
-// Products one multi-weight FP8 launch computes (G weight sets that share the
-// activation operand).
-constexpr int kFp8MaxWeights = 8;
-struct Fp8WMaps {
-  CUtensorMap m[kFp8MaxWeights];
-};
 
 struct Fp8Params {
   const float* sfa;       // [K/128, M]
@@ -160,13 +183,13 @@ struct Fp8Params {
   unsigned long long wait_ns;  // bound of every pipeline wait (%globaltimer ns)
   int G;                  // products sharing the activation: 1 = one GEMM (sfb, out); > 1 = the
                           // multi-weight kernel (sfb_g, out_g; block scaling, M <= 32)
-  const float* sfb_g[kFp8MaxWeights];
-  void* out_g[kFp8MaxWeights];
+  const float* sfb_g[kMaxProducts];
+  void* out_g[kMaxProducts];
 };
 
 struct Fp8Launch {
   CUtensorMap tmA, tmB;
-  Fp8WMaps tmA_g;         // G > 1: the weight map of every product (tmA unused)
+  WeightMaps tmA_g;       // G > 1: the weight map of every product (tmA unused)
   Fp8Params p;
   int tile_n;             // MMA N (token columns per tile): 16, 32, 64 or 128
   int grid;

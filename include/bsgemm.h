@@ -303,34 +303,41 @@ size_t bs_gemm_workspace_bytes(const bs_gemm_args *args);
 bs_status bs_gemm(const bs_gemm_args *args, bs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * bs_gemm_multi -- G FP8 GEMMs that read one activation, in one launch:
+ * bs_gemm_multi -- G GEMMs that read one activation, in one launch:
  *     Y_g = A B_g^T,  g = 0 .. G-1,
- * each exactly as bs_gemm computes it with fmt = BS_FMT_FP8 and block scaling
- * (promotion per 128-wide K block; "DeepGEMM teardown (FP8 GEMM)", sections
- * 2.2-2.3).  The output tiles of all G products form one tile list on one
- * grid, so a decode step's projections of the same tokens pay the launch,
- * first-load and stream-K fix-up latencies that dominate a GEMM with M <= 32
- * once instead of G times ("DeepGEMM teardown", section 1.2: small M leaves
- * most of the GPU idle; section 3.2: wave scheduling; "Tencent AI Infra
- * interview notes", decode: the GEMM streams its weights, 2KN FLOPs per KN
- * weight bytes).
+ * each exactly as bs_gemm computes it for a decode shape (M <= 32): FP8 with
+ * block scaling (promotion per 128-wide K block; "DeepGEMM teardown (FP8
+ * GEMM)", sections 2.2-2.3), or FP4 through the decode kernel
+ * ("Warp-specialised W4A4 kernel", section 1).  The output tiles of all G
+ * products form one tile list on one grid, so a decode step's projections of
+ * the same tokens pay the launch, first-load and stream-K fix-up latencies
+ * that dominate a GEMM with M <= 32 once instead of G times ("DeepGEMM
+ * teardown", section 1.2: small M leaves most of the GPU idle; section 3.2:
+ * wave scheduling; "Tencent AI Infra interview notes", decode: the GEMM
+ * streams its weights, 2KN FLOPs per KN weight bytes).
  *
- *   args      as for bs_gemm, with fmt = BS_FMT_FP8, fp8_scaling 0 or 1 and
- *             M <= 32; args->a / sfa are the shared tokens; args->b, sfb and
- *             out are ignored; N, K, out_dtype, ldo, num_sms, fp8_stream_k,
- *             weights_ready, wait_timeout_us apply to every product; the
- *             workspace is sized by bs_gemm_multi_workspace_bytes
+ *   args      as for bs_gemm with M <= 32; args->a / sfa are the shared
+ *             tokens; args->b, sfb and out are ignored; N, K, out_dtype, ldo,
+ *             num_sms, fp8_stream_k, weights_ready, wait_timeout_us apply to
+ *             every product; the workspace is sized by
+ *             bs_gemm_multi_workspace_bytes.
+ *             FP8: fp8_scaling 0 or 1 (not W8A8).
+ *             FP4: K % 256 == 0; alpha and a_tensor_scale apply to every
+ *             product; no low-rank branch, col_scale, bias or b_tensor_scale;
+ *             fp4_decode must not be 2.
  *   G         number of products, 1 .. 8
  *   b, sfb, out
- *             HOST arrays of G DEVICE pointers: B_g e4m3 [N, K], its fp32
- *             [N/128, K/128] block scales (q8_quantize BLOCK mode), Y_g
+ *             HOST arrays of G DEVICE pointers: B_g codes (e4m3 [N, K] or FP4
+ *             [N, K/2]), its scales (FP8: fp32 [N/128, K/128] from q8_quantize
+ *             BLOCK mode; FP4: bs_sf_bytes(N, K) bytes in the MMA layout), Y_g
  *             [M, ldo]; every pointer 16-byte aligned; the outputs must not
  *             overlap one another or any input
- * Returns BS_ERR_UNSUPPORTED for FP4, W8A8 or M > 32, BS_ERR_INVALID for
- * G outside [1, 8] or a null array or pointer; otherwise as bs_gemm.
+ * Returns BS_ERR_UNSUPPORTED for W8A8, M > 32 or an FP4 option above,
+ * BS_ERR_INVALID for G outside [1, 8] or a null array or pointer; otherwise
+ * as bs_gemm.
  * ------------------------------------------------------------------------- */
 size_t bs_gemm_multi_workspace_bytes(const bs_gemm_args *args, int G);
-bs_status bs_gemm_multi(const bs_gemm_args *args, int G, const uint8_t *const *b, const float *const *sfb,
+bs_status bs_gemm_multi(const bs_gemm_args *args, int G, const uint8_t *const *b, const void *const *sfb,
                         void *const *out, bs_stream_t stream);
 
 /* ---------------------------------------------------------------------------

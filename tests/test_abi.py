@@ -154,8 +154,15 @@ def test_host_validation_rejects_before_launch(lib):
     g.fp8_scaling = 2
     assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_ERR_UNSUPPORTED
     g.fp8_scaling = 0
-    g.fmt = 0
+    g.fmt = 5
+    assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_ERR_INVALID
+    g.fmt, g.K = 0, 320                                                              # FP4: K % 256
+    assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_ERR_ALIGN
+    g.K, g.col_scale = 256, 1 << 20                                                  # FP4: per-column scale
     assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_ERR_UNSUPPORTED
+    g.col_scale, g.fp4_decode = None, 2                                              # FP4: decode kernel only
+    assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_ERR_UNSUPPORTED
+    g.fp4_decode = 0
     g.fmt, g.M = 1, 0
     assert multi(ctypes.byref(g), 3, arr3, arr3, arr3, None) == bs.BS_OK           # M == 0: nothing to do
     assert lib.bs_gemm_multi_workspace_bytes(ctypes.byref(g), 3) == 0

@@ -1,9 +1,11 @@
-"""bs_gemm_multi: G block-scaled FP8 GEMMs that share one activation, in one
-launch, on the GPU.  Every product must equal the oracle's FP64 GEMM of the
-same codes within the FP8 GEMM tolerance (|y - y_ref| <= 1e-3 S + 2^-8
-|y_ref|, plus the tighter 1e-4 S diagnostic), and -- where both run whole
-tiles, so that each output tile is accumulated by one CTA in K order -- be bit
-for bit the single-weight bs_gemm result for that weight set."""
+"""bs_gemm_multi: G GEMMs that share one activation (M <= 32), in one launch,
+on the GPU -- block-scaled FP8 and FP4 through the decode kernel.  Every
+product must equal the oracle's FP64 GEMM of the same codes within the GEMM
+tolerance (|y - y_ref| <= 1e-3 S + 2^-8 |y_ref|, plus the tighter 1e-4 S
+diagnostic).  FP8 products also equal, bit for bit, the single-weight bs_gemm
+result wherever both run whole tiles (each output tile accumulated by one CTA
+in K order); FP4 products run stream-K over all products' K stages, so their
+pieces differ from a single call's and only G = 1 is compared bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -134,3 +136,75 @@ def test_multi_rejects(cuda_lib):
     with pytest.raises(bs.BSError) as e:
         bs.gemm_fp8_multi(xq[:16], xs, [(wq, wsc)] * 9)         # G = 9
     assert e.value.status == bs.BS_ERR_INVALID
+
+
+# ----------------------------------------------------------------------------- FP4
+
+
+def fp4_inputs(bs, M, N, K, G, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    ws = weight_sets(G, N, K, seed + 1)
+    xq, xs, _ = bs.q4_quantize(x.cuda())
+    wqs = [bs.q4_quantize(w.cuda())[:2] for w in ws]
+    return x, ws, xq, xs, wqs
+
+
+def check_fp4_vs_oracle(x, w, y, K, alpha=1.0):
+    oa, osa = oracle.q4_quantize(x)
+    ob, osb = oracle.q4_quantize(w)
+    yr, s = oracle.gemm_fp4(oa, osa, ob, osb, K, alpha=alpha)
+    bf = y.dtype == torch.bfloat16
+    yg = y.float().cpu().numpy()
+    ok, ratio, rel = gemm_errors(yg, yr, s, bf)
+    tok, tratio = tight_errors(yg, yr, s, bf)
+    return ok and tok, (ratio, rel, tratio)
+
+
+@pytest.mark.parametrize("M,N,K,G", [(1, 1024, 1024, 3), (16, 384, 2048, 8), (32, 640, 256, 5), (5, 128, 768, 2)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_fp4_multi_vs_oracle(cuda_lib, M, N, K, G, out_dtype):
+    """Every product within tolerance of the oracle (alpha 0.75 on all of
+    them); the call repeatable bit for bit and equal as the weights-ready
+    dependent of the activation quantizer (stream-K counters back at zero)."""
+    bs = cuda_lib
+    x, ws, xq, xs, wqs = fp4_inputs(bs, M, N, K, G, seed=M * 31 + N + K + G)
+    y1 = [y.clone() for y in bs.gemm_fp4_multi(xq, xs, wqs, K, out_dtype=out_dtype, alpha=0.75)]
+    xq2, xs2, _ = bs.q4_quantize(x.cuda())
+    y2 = bs.gemm_fp4_multi(xq2, xs2, wqs, K, out_dtype=out_dtype, alpha=0.75, weights_ready=True)
+    torch.cuda.synchronize()
+    assert bs.device_status()[0] == 0
+    for a, b in zip(y1, y2):
+        assert torch.equal(a, b)
+    for i in range(G):
+        ok, info = check_fp4_vs_oracle(x, ws[i], y1[i], K, alpha=0.75)
+        assert ok, (i, info)
+
+
+def test_fp4_multi_single_product_is_bs_gemm(cuda_lib):
+    bs = cuda_lib
+    x, ws, xq, xs, wqs = fp4_inputs(bs, 16, 1024, 1024, 1, seed=5)
+    y = bs.gemm_fp4_multi(xq, xs, wqs, 1024)[0]
+    y1 = bs.gemm_fp4(xq, xs, *wqs[0], 1024)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y1)
+
+
+def test_fp4_multi_decode_full_size(cuda_lib):
+    """8 FP4 weight sets of [7168, 4096] against M = 16 tokens in one launch:
+    the first and last products against the oracle on every row; every
+    product within a tight bound of its own single-weight call (the same
+    arithmetic up to the stream-K split of the fp32 sum)."""
+    bs = cuda_lib
+    G, M, N, K = 8, 16, 7168, 4096
+    x, ws, xq, xs, wqs = fp4_inputs(bs, M, N, K, G, seed=77)
+    ys = bs.gemm_fp4_multi(xq, xs, wqs, K, out_dtype=torch.float32)
+    singles = [bs.gemm_fp4(xq, xs, wq, wsc, K, out_dtype=torch.float32) for wq, wsc in wqs]
+    torch.cuda.synchronize()
+    assert bs.device_status()[0] == 0
+    for i, (y, y1) in enumerate(zip(ys, singles)):
+        scale = y1.abs().max().item()
+        assert torch.allclose(y, y1, rtol=1e-5, atol=1e-5 * scale), i
+    for i in (0, G - 1):
+        ok, info = check_fp4_vs_oracle(x, ws[i], ys[i], K)
+        assert ok, (i, info)

@@ -168,3 +168,20 @@ def test_wait_runs_out_fp8_multi(cuda_lib, pdl_hold):
             return torch.stack(bs.gemm_fp8_multi(xq, xs, wqs))
 
     _timeout_then_same_result(bs, pdl_hold, run, SITES_FP8)
+
+
+def test_wait_runs_out_fp4_multi(cuda_lib, pdl_hold):
+    """The FP4 decode kernel's multi-weight variant (three products)."""
+    bs = cuda_lib
+    g = torch.Generator().manual_seed(7)
+    K, N = 4096, 1024
+    x = torch.randn(16, K, generator=g).to(torch.bfloat16).cuda()
+    xq, xs, _ = bs.q4_quantize(x)
+    wqs = [bs.q4_quantize((torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda())[:2] for _ in range(3)]
+
+    def run(opts, before):
+        with bs.kernel_options(**opts):
+            before()
+            return torch.stack(bs.gemm_fp4_multi(xq, xs, wqs, K))
+
+    _timeout_then_same_result(bs, pdl_hold, run, SITES_DECODE)
