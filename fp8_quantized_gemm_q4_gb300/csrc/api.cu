@@ -580,10 +580,9 @@ static bs_status launch_fp4_decode(const bs_gemm_args* a, int G, const uint8_t* 
     p.counters = static_cast<int*>(a->workspace);
     p.work = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + kStreamKCounterBytes);
   } else {
-    // no workspace: whole tiles only, on the largest grid that divides them
-    int g = (int)(tiles < sms ? tiles : sms);
-    while (tiles % g) --g;
-    L.grid = g;
+    // no workspace (or more tiles than counters): whole tiles only, at least
+    // one per CTA, balanced to within one tile
+    L.grid = (int)(tiles < sms ? tiles : sms);
   }
   cudaError_t e = bsk::launch_fp4_decode(L, s);
   if (e != cudaSuccess) return cuda_fail(e, G == 1 ? "FP4 decode GEMM launch" : "FP4 multi-weight decode launch");

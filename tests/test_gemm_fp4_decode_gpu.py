@@ -62,7 +62,7 @@ def test_fp4_decode_epilogue_fp32(cuda_lib, M):
 @pytest.mark.parametrize("num_sms", [3, 57, 100, 151])
 def test_fp4_decode_grid_sizes(cuda_lib, num_sms):
     """56 tiles x 16 K stages cut unevenly over the grid (3 SMs: fewer CTAs
-    than tiles, several whole tiles per CTA plus cut ones)."""
+    than tiles, so each CTA takes a contiguous run of whole tiles)."""
     x, w, _, _ = _case(16, 7168, 4096, 5)
     _check(cuda_lib, x, w, None, None, torch.bfloat16, 1.0, True, num_sms=num_sms)
 
@@ -80,3 +80,28 @@ def test_fp4_decode_two_level_weights(cuda_lib):
     yr, s = oracle.gemm_fp4(oa, osa, ob, osb, 1024, alpha=tb)
     ok, ratio, rel = gemm_errors(y.float().cpu().numpy(), yr, s, True)
     assert ok, (ratio, rel)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 1024, 1024), (16, 7168, 512), (32, 3968, 256)])
+def test_fp4_decode_without_workspace(cuda_lib, M, N, K):
+    """No caller workspace: whole tiles only, min(tiles, SMs) CTAs each taking a
+    contiguous run balanced to within one tile (3968 = 31 tiles, a prime
+    count); the result within tolerance of the oracle."""
+    import ctypes
+    bs = cuda_lib
+    x, w, _, _ = _case(M, N, K, 3 * M + N + K)
+    xq, xs, _ = bs.q4_quantize(x.cuda())
+    wq, ws, _ = bs.q4_quantize(w.cuda())
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g = bs._args(bs.FMT_FP4, xq, xs, wq, ws, M, N, K, y)
+    assert g.workspace is None
+    bs._check(bs.load().bs_gemm(ctypes.byref(g), bs._stream()))
+    torch.cuda.synchronize()
+    assert bs.device_status()[0] == 0
+    oa, osa = oracle.q4_quantize(x)
+    ob, osb = oracle.q4_quantize(w)
+    yr, s = oracle.gemm_fp4(oa, osa, ob, osb, K)
+    yg = y.float().cpu().numpy()
+    ok, ratio, rel = gemm_errors(yg, yr, s, True)
+    tok, tratio = tight_errors(yg, yr, s, True)
+    assert ok and tok, (ratio, rel, tratio)
