@@ -645,7 +645,11 @@ static bs_status launch_fp8(const bs_gemm_args* a, int G, const uint8_t* const* 
     L.p.counters = static_cast<int*>(a->workspace);
     L.p.work = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + kStreamKCounterBytes);
   } else {
-    L.grid = (int)(P.tiles < sms ? P.tiles : sms);  // one CTA per tile
+    // whole tiles; the 16-token kernel fits two CTAs on an SM, so with at
+    // least a tile per SM and the default grid it runs two per SM (twice the
+    // weight bytes in flight)
+    const int ctas = (P.tile_n == 16 && a->num_sms == 0 && P.tiles >= sms) ? 2 * sms : sms;
+    L.grid = (int)(P.tiles < ctas ? P.tiles : ctas);
   }
   cudaError_t e = bsk::launch_fp8_gemm(L, s);
   if (e != cudaSuccess) return cuda_fail(e, G == 1 ? "FP8 GEMM launch" : "FP8 multi-weight GEMM launch");
