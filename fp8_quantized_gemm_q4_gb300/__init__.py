@@ -360,6 +360,10 @@ def gemm_fp8(a, sa, b, sb, out_dtype=torch.bfloat16, out=None, num_sms: int = 0,
 def _gemm_multi(fmt, a, sa, weights, M, N, K, out_dtype, outs, num_sms, weights_ready, alpha=1.0,
                 a_tensor_scale=None, stream=None):
     G = len(weights)
+    if G == 0:
+        raise ValueError("bs_gemm_multi needs at least one weight set")
+    if outs is not None and len(outs) != G:
+        raise ValueError(f"{len(outs)} outputs for {G} weight sets")
     if outs is None:
         outs = [torch.empty((M, N), dtype=out_dtype, device=a.device) for _ in range(G)]
     b0, sb0 = weights[0]
@@ -387,8 +391,8 @@ def gemm_fp8_multi(a, sa, weights, out_dtype=torch.bfloat16, outs=None, num_sms:
     [N, K], BLOCK-mode scales) pairs, one per product; returns the G outputs
     [M, N] (or fills ``outs``)."""
     M, K = a.shape
-    return _gemm_multi(FMT_FP8, a, sa, weights, M, weights[0][0].shape[0], K, out_dtype, outs, num_sms,
-                       weights_ready, stream=stream)
+    N = weights[0][0].shape[0] if weights else 0
+    return _gemm_multi(FMT_FP8, a, sa, weights, M, N, K, out_dtype, outs, num_sms, weights_ready, stream=stream)
 
 
 def gemm_fp4_multi(a, sfa, weights, K: int, out_dtype=torch.bfloat16, outs=None, alpha: float = 1.0,
@@ -397,8 +401,9 @@ def gemm_fp4_multi(a, sfa, weights, K: int, out_dtype=torch.bfloat16, outs=None,
     scales ``sfa``) in one launch: ``weights`` is a list of (codes [N, K/2],
     scales) pairs from q4_quantize; returns the G outputs [M, N]."""
     M = a.shape[0]
-    return _gemm_multi(FMT_FP4, a, sfa, weights, M, weights[0][0].shape[0], K, out_dtype, outs, num_sms,
-                       weights_ready, alpha=alpha, a_tensor_scale=a_tensor_scale, stream=stream)
+    N = weights[0][0].shape[0] if weights else 0
+    return _gemm_multi(FMT_FP4, a, sfa, weights, M, N, K, out_dtype, outs, num_sms, weights_ready, alpha=alpha,
+                       a_tensor_scale=a_tensor_scale, stream=stream)
 
 
 def grouped_gemm_fp4(a, sfa, b, sfb, K: int, N: int, E: int, offsets, counts, epilogue: int, out=None,

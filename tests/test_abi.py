@@ -181,3 +181,17 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "liboracle" not in src, f
+
+
+def test_multi_binding_checks_its_lists():
+    """The binding's list checks for bs_gemm_multi (before any library call)."""
+    import torch
+    import fp8_quantized_gemm_q4_gb300 as bs
+    a = torch.zeros(16, 256, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        bs.gemm_fp8_multi(a, torch.zeros(2, 16), [])
+    with pytest.raises(ValueError):
+        bs.gemm_fp4_multi(a[:, :128], torch.zeros(512, dtype=torch.uint8), [], 256)
+    w = (torch.zeros(128, 256, dtype=torch.uint8), torch.zeros(1, 2))
+    with pytest.raises(ValueError):
+        bs.gemm_fp8_multi(a, torch.zeros(2, 16), [w, w], outs=[torch.zeros(16, 128)])
