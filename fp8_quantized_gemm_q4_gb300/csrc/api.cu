@@ -478,6 +478,13 @@ static bool fp4_decode_applies(const bs_gemm_args* a) {
 static bool fp4_decode_stream_k(long long tiles) {
   return tiles <= (long long)(kStreamKCounterBytes / sizeof(int));
 }
+// CTAs of an FP4 decode launch over `tiles` weight tiles: with at least one
+// tile per SM the kernel walks whole tiles, and the 16-token variant, which
+// fits two CTAs on an SM, then runs two per SM on the default grid (twice the
+// weight bytes in flight); otherwise one per SM.
+static int fp4_decode_ctas(const bs_gemm_args* a, long long tiles, int sms) {
+  return (a->M <= 16 && a->num_sms == 0 && tiles >= sms) ? 2 * sms : sms;
+}
 
 struct Fp8Plan {
   int tile_n;
@@ -522,7 +529,9 @@ size_t bs_gemm_workspace_bytes(const bs_gemm_args* a) {
   if (a->num_sms > 0 && a->num_sms < sms) sms = a->num_sms;
   if (fp4_decode_applies(a)) {
     const long long tiles = (a->N + 127) / 128;
-    return fp4_decode_stream_k(tiles) ? sk_split(tiles, a->K / 256, a->M <= 16 ? 16 : 32, sms).ws_bytes : 0;
+    return fp4_decode_stream_k(tiles)
+               ? sk_split(tiles, a->K / 256, a->M <= 16 ? 16 : 32, fp4_decode_ctas(a, tiles, sms)).ws_bytes
+               : 0;
   }
   if (a->fmt != BS_FMT_FP8) return 0;
   const Fp8Plan P = fp8_plan(a, sms);
@@ -570,8 +579,9 @@ static bs_status launch_fp4_decode(const bs_gemm_args* a, int G, const uint8_t* 
     p.out_g[g] = out[g];
   }
   const long long tiles = (long long)G * ((a->N + 127) / 128), units = a->K / 256;
+  const int ctas = fp4_decode_ctas(a, tiles, sms);
   if (a->workspace && fp4_decode_stream_k(tiles)) {
-    const SkSplit k = sk_split(tiles, units, L.tile_n, sms);
+    const SkSplit k = sk_split(tiles, units, L.tile_n, ctas);
     if (!aligned16(a->workspace)) return fail(BS_ERR_ALIGN, "workspace must be 16-byte aligned");
     if (a->workspace_bytes < k.ws_bytes)
       return fail(BS_ERR_INVALID, "workspace too small (%zu < %zu bytes)", a->workspace_bytes, k.ws_bytes);
@@ -581,8 +591,8 @@ static bs_status launch_fp4_decode(const bs_gemm_args* a, int G, const uint8_t* 
     p.work = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + kStreamKCounterBytes);
   } else {
     // no workspace (or more tiles than counters): whole tiles only, at least
-    // one per CTA, balanced to within one tile
-    L.grid = (int)(tiles < sms ? tiles : sms);
+    // one per CTA
+    L.grid = (int)(tiles < ctas ? tiles : ctas);
   }
   cudaError_t e = bsk::launch_fp4_decode(L, s);
   if (e != cudaSuccess) return cuda_fail(e, G == 1 ? "FP4 decode GEMM launch" : "FP4 multi-weight decode launch");
@@ -729,7 +739,9 @@ size_t bs_gemm_multi_workspace_bytes(const bs_gemm_args* a, int G) {
   if (a->fmt == BS_FMT_FP4) {
     if (a->K % 256) return 0;
     const long long tiles = (long long)G * ((a->N + 127) / 128);
-    return fp4_decode_stream_k(tiles) ? sk_split(tiles, a->K / 256, a->M <= 16 ? 16 : 32, sms).ws_bytes : 0;
+    return fp4_decode_stream_k(tiles)
+               ? sk_split(tiles, a->K / 256, a->M <= 16 ? 16 : 32, fp4_decode_ctas(a, tiles, sms)).ws_bytes
+               : 0;
   }
   const Fp8Plan P = fp8_plan(a, sms, G);
   return P.stream_k ? P.ws_bytes : 0;

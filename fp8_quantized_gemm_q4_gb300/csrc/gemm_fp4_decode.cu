@@ -14,7 +14,7 @@
 // Work units are (weight tile of 128 rows, K stage of 256) pairs; with fewer
 // tiles than CTAs they form one sequence shared out evenly over the grid
 // (stream-K, "DeepGEMM teardown" sections 1.2 and 3.2: small M leaves SMs
-// idle), otherwise each CTA takes a contiguous run of whole tiles.  A CTA accumulates its K
+// idle), otherwise the CTAs take whole tiles in turn.  A CTA accumulates its K
 // range of a tile in one tensor-memory slot; a tile cut between CTAs is
 // finished by the last of them (acquire-release counter in the caller's
 // workspace, pieces summed in K order, counter reset), as in the FP8 kernel.
@@ -79,23 +79,34 @@ struct Seg {
   int t, kb0, kb1;  // weight tile t, K stages [kb0, kb1)
 };
 
-// A CTA's range of the (tile, K stage) sequence.  With at least as many tiles
-// as CTAs the ranges are whole tiles (contiguous, balanced to within one
-// tile), so no tile is cut and no fix-up runs; with fewer, stream-K.
+// A CTA's share of the (tile, K stage) sequence.  With at least as many tiles
+// as CTAs, whole tiles t = c, c + G, ... (no tile is cut, no fix-up runs; two
+// CTAs of an SM, c and c + G / 2, then hold at most one tile more than the
+// average between them); with fewer, one contiguous stream-K range.
 struct Walk {
   long long cur, end;
+  int step;  // > 0: whole tiles, cur / end count tiles; 0: stream-K, they count units
   __device__ __forceinline__ Walk(int total, int nks) {
     if (total >= (int)gridDim.x) {
-      cur = (long long)blockIdx.x * total / gridDim.x * nks;
-      end = (long long)(blockIdx.x + 1) * total / gridDim.x * nks;
+      cur = blockIdx.x;
+      end = total;
+      step = (int)gridDim.x;
     } else {
       const long long U = (long long)total * nks;
       cur = (long long)blockIdx.x * U / gridDim.x;
       end = (long long)(blockIdx.x + 1) * U / gridDim.x;
+      step = 0;
     }
   }
   __device__ __forceinline__ bool next(int nks, Seg& s) {
     if (cur >= end) return false;
+    if (step) {
+      s.t = (int)cur;
+      s.kb0 = 0;
+      s.kb1 = nks;
+      cur += step;
+      return true;
+    }
     s.t = (int)(cur / nks);
     s.kb0 = (int)(cur % nks);
     s.kb1 = (int)min((long long)nks, s.kb0 + (end - cur));
