@@ -287,8 +287,9 @@ typedef struct {
     const float *b_tensor_scale;
     int fp4_decode;          /* FP4 with M <= 32 and K % 256 == 0, no low-rank branch: 1 = the
                                 decode kernel (swap-AB: weight rows fill the MMA's 128 rows, the
-                                tokens its N = 16 or 32; stream-K over every SM through
-                                `workspace`; default); 2 = the regular tile kernels */
+                                tokens its N = 16 or 32; with fewer weight tiles than SMs,
+                                stream-K over every SM through `workspace`, else whole
+                                tiles; default); 2 = the regular tile kernels */
 } bs_gemm_args;
 
 /* Bytes of `workspace` bs_gemm would use for these arguments (sizes, format,
